@@ -1,0 +1,87 @@
+"""Dynamic decomposer + attention task reorder, restated for the oracle (test infrastructure only).
+
+[XY] §2.2 component 1 / §4.4 ``decompose_attention``: the (q_len x kv_len) work of a
+sequence is cut into fixed-size (query block x KV block) tasks that record their ranges,
+their actual shape and a compute load equal to the tile area (times the heads).
+[XY] §2.2 component 2 ``AttentionTaskReorder.reorder``: tasks are sorted by load,
+largest first, and dealt round-robin, task i going to core i mod num_cores; the ratio
+min/max of the per-core load sums measures the balance.
+
+Readings taken here (the pages are written for 16 x 16 Ascend blocks):
+
+* The unit of work is one (sequence, KV head, query tile, KV chunk).  A query tile holds
+  ``q_tile`` tokens and all G = Hq / Hkv query heads that share the KV head, so a tile
+  has q_rows * G score rows.  The KV range of a tile is cut into chunks of ``kv_chunk``
+  keys ("split-KV"); with causal attention the range ends at the last visible key of the
+  tile's last row (L - q + row_end), otherwise at L.
+* load = q_rows * G * (kv_end - kv_start): the tile area times the heads it carries.
+* The sort is stable (Python ``sorted`` keeps equal keys in enumeration order, which is
+  sequence -> KV head -> query tile -> chunk); the deal is plain ``i % num_ctas``.
+* A tile split into n > 1 chunks writes n partial results to a workspace and needs one
+  merge; partial rows are numbered in enumeration order: the tile's group starts at
+  ws_row and chunk c owns rows ws_row + c * q_rows * G + t * G + h_local.
+"""
+
+import numpy as np
+
+TASK_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "kv_start", "kv_end", "num_splits", "ws_row")
+MERGE_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "num_splits", "ws_row", "zero0", "zero1")
+
+
+def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
+                     num_ctas, q_tile, kv_chunk):
+    """Return dict(tasks=int32 [n, 8] in dealt order, merges=int32 [m, 8], loads=int64 [n],
+    cta_loads=int64 [num_ctas], balance=min/max, workspace_bytes=int).
+
+    CTA c runs tasks c, c + num_ctas, c + 2*num_ctas, ... of ``tasks``.
+    """
+    if num_heads_q % num_heads_kv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    if q_tile < 1 or kv_chunk < 1 or num_ctas < 1:
+        raise ValueError("q_tile, kv_chunk and num_ctas must be positive")
+    G = num_heads_q // num_heads_kv
+    cu = [int(x) for x in cu_seqlens_q]
+    S = len(cu) - 1
+
+    records, loads, merges = [], [], []
+    ws_rows = 0
+    for i in range(S):
+        qn = cu[i + 1] - cu[i]
+        L = int(context_lens[i])
+        if qn < 1 or qn > L:
+            raise ValueError(f"sequence {i}: need 1 <= q_len <= context_len")
+        for g in range(num_heads_kv):
+            for t0 in range(0, qn, q_tile):
+                rows = min(q_tile, qn - t0)
+                kv_hi = (L - qn + t0 + rows) if causal else L
+                nsplit = -(-kv_hi // kv_chunk)
+                base = -1
+                if nsplit > 1:
+                    base = ws_rows
+                    merges.append((i, g, t0, rows, nsplit, base, 0, 0))
+                    ws_rows += nsplit * rows * G
+                for c in range(nsplit):
+                    k0 = c * kv_chunk
+                    k1 = min(kv_hi, k0 + kv_chunk)
+                    row = -1 if nsplit == 1 else base + c * rows * G
+                    records.append((i, g, t0, rows, k0, k1, nsplit, row))
+                    loads.append(rows * G * (k1 - k0))
+
+    order = sorted(range(len(records)), key=lambda k: loads[k], reverse=True)
+    tasks = np.array([records[k] for k in order], dtype=np.int32).reshape(-1, 8)
+    sorted_loads = np.array([loads[k] for k in order], dtype=np.int64)
+
+    cta_loads = np.zeros(num_ctas, dtype=np.int64)
+    for pos, ld in enumerate(sorted_loads):
+        cta_loads[pos % num_ctas] += ld
+    mx = int(cta_loads.max()) if num_ctas else 0
+    balance = (int(cta_loads.min()) / mx) if mx > 0 else 1.0
+
+    return dict(
+        tasks=tasks,
+        merges=np.array(merges, dtype=np.int32).reshape(-1, 8),
+        loads=sorted_loads,
+        cta_loads=cta_loads,
+        balance=balance,
+        workspace_bytes=ws_rows * (head_dim + 1) * 4,
+    )

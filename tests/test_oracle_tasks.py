@@ -1,0 +1,137 @@
+"""Pins for the oracle's decomposer + reorder (task table): the pages' 16 x 16 decomposition,
+brute-force coverage of every visible (row, key) pair, an independent stable sort and deal,
+and the workspace layout of split tiles."""
+
+import numpy as np
+import pytest
+
+from oracle import build_task_table, pack_cu_seqlens
+
+
+def _pages_decompose(q_len, kv_len, blk, heads):
+    """The decomposer as the pages describe it: every (q block, kv block) pair of a
+    q_len x kv_len problem becomes a task whose load is its actual area times the heads."""
+    out = []
+    for q0 in range(0, q_len, blk):
+        for k0 in range(0, kv_len, blk):
+            aq, ak = min(blk, q_len - q0), min(blk, kv_len - k0)
+            out.append((q0, aq, k0, k0 + ak, aq * ak * heads))
+    return out
+
+
+def test_matches_pages_16x16_decomposition():
+    q_lens, ctx = [7, 40, 1, 16], [7, 40, 33, 100]
+    cu = pack_cu_seqlens(q_lens)
+    r = build_task_table(cu, ctx, 3, 3, 64, False, 5, 16, 16)
+    tasks = r["tasks"]
+    for i in range(4):
+        for g in range(3):
+            mine = sorted((int(t[2]), int(t[3]), int(t[4]), int(t[5])) for t in tasks
+                          if t[0] == i and t[1] == g)
+            ref = sorted((q0, aq, k0, k1) for (q0, aq, k0, k1, _) in _pages_decompose(q_lens[i], ctx[i], 16, 1))
+            assert mine == ref
+    expect_loads = sorted((ld for i in range(4) for g in range(3)
+                           for *_, ld in _pages_decompose(q_lens[i], ctx[i], 16, 1)), reverse=True)
+    assert r["loads"].tolist() == expect_loads
+    assert len(tasks) == 3 * sum(-(-q // 16) * -(-L // 16) for q, L in zip(q_lens, ctx))
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("q_tile,kv_chunk,Hq,Hkv", [(3, 5, 4, 2), (1, 7, 2, 2), (4, 4, 6, 3), (128, 4096, 8, 8)])
+def test_every_visible_pair_covered_exactly_once(causal, q_tile, kv_chunk, Hq, Hkv):
+    q_lens, ctx = [7, 1, 9, 2, 13], [7, 19, 12, 2, 30]
+    cu = pack_cu_seqlens(q_lens)
+    r = build_task_table(cu, ctx, Hq, Hkv, 16, causal, 3, q_tile, kv_chunk)
+    G = Hq // Hkv
+    cover = {}
+    for t in r["tasks"]:
+        i, g, q0, qr, k0, k1, ns, ws = (int(x) for x in t)
+        assert 1 <= qr <= q_tile and k0 < k1 and k1 - k0 <= kv_chunk
+        assert k0 % kv_chunk == 0
+        for j in range(q0, q0 + qr):
+            for h in range(g * G, (g + 1) * G):
+                for k in range(k0, k1):
+                    cover[(i, h, j, k)] = cover.get((i, h, j, k), 0) + 1
+    for i, (qn, L) in enumerate(zip(q_lens, ctx)):
+        for h in range(Hq):
+            for j in range(qn):
+                last = (L - qn + j) if causal else L - 1
+                for k in range(L):
+                    c = cover.get((i, h, j, k), 0)
+                    if k <= last:
+                        assert c == 1, (i, h, j, k)
+                    else:
+                        assert c <= 1
+    # keys beyond what the tile's last row can see are never scheduled
+    for (i, h, j, k) in cover:
+        assert k < ctx[i]
+
+
+def test_sort_is_stable_descending_and_dealt_round_robin():
+    rng = np.random.default_rng(0)
+    q_lens = rng.integers(1, 40, size=12)
+    ctx = q_lens + rng.integers(0, 90, size=12)
+    cu = pack_cu_seqlens(q_lens)
+    num_ctas = 7
+    r = build_task_table(cu, ctx, 4, 2, 32, True, num_ctas, 8, 32)
+    # rebuild the enumeration independently and sort with numpy's stable sort
+    recs = []
+    for i in range(12):
+        for g in range(2):
+            for q0 in range(0, int(q_lens[i]), 8):
+                qr = min(8, int(q_lens[i]) - q0)
+                hi = int(ctx[i]) - int(q_lens[i]) + q0 + qr
+                for k0 in range(0, hi, 32):
+                    recs.append((i, g, q0, qr, k0, min(hi, k0 + 32), qr * 2 * (min(hi, k0 + 32) - k0)))
+    loads = np.array([x[-1] for x in recs])
+    order = np.argsort(-loads, kind="stable")
+    assert [tuple(int(v) for v in r["tasks"][p][:6]) for p in range(len(order))] == [recs[k][:6] for k in order]
+    assert r["loads"].tolist() == loads[order].tolist()
+    cta = np.zeros(num_ctas, np.int64)
+    for p, k in enumerate(order):
+        cta[p % num_ctas] += loads[k]
+    assert r["cta_loads"].tolist() == cta.tolist()
+    assert r["balance"] == cta.min() / cta.max()
+    assert np.all(np.diff(r["loads"]) <= 0)
+
+
+def test_workspace_layout_of_split_tiles():
+    q_lens, ctx = [1, 20, 3], [100, 20, 50]
+    cu = pack_cu_seqlens(q_lens)
+    d, G = 32, 4
+    r = build_task_table(cu, ctx, 8, 2, d, True, 4, 8, 16)
+    merges = r["merges"]
+    used = np.zeros(r["workspace_bytes"] // ((d + 1) * 4), dtype=np.int32)
+    for m in merges:
+        i, g, q0, qr, ns, base, z0, z1 = (int(x) for x in m)
+        assert ns > 1 and z0 == 0 and z1 == 0
+        used[base: base + ns * qr * G] += 1
+        # the tile's splits point at consecutive slices of its region
+        mine = sorted(int(t[7]) for t in r["tasks"] if t[0] == i and t[1] == g and t[2] == q0)
+        assert mine == [base + c * qr * G for c in range(ns)]
+    assert np.all(used == 1)
+    for t in r["tasks"]:
+        assert (int(t[6]) == 1) == (int(t[7]) == -1)
+    # merges are listed in enumeration order and regions are allocated in that order
+    bases = [int(m[5]) for m in merges]
+    assert bases == sorted(bases)
+    total_rows = sum(int(m[3]) * G * int(m[4]) for m in merges)
+    assert r["workspace_bytes"] == total_rows * (d + 1) * 4
+
+
+def test_decode_tile_and_split_counts():
+    # decode: one tile of one token, kv range [0, L) cut into ceil(L / chunk) splits
+    r = build_task_table([0, 1, 2], [4096, 4097], 64, 8, 128, True, 152, 16, 4096)
+    t = r["tasks"]
+    assert len(t) == 8 * (1 + 2)
+    assert sorted(set(int(x) for x in t[:, 6])) == [1, 2]
+    assert sum(int(x[5]) - int(x[4]) for x in t if x[0] == 1) == 8 * 4097
+
+
+def test_empty_batch_and_errors():
+    r = build_task_table([0], [], 4, 2, 64, True, 3, 8, 64)
+    assert r["tasks"].shape == (0, 8) and r["workspace_bytes"] == 0 and r["balance"] == 1.0
+    with pytest.raises(ValueError):
+        build_task_table([0, 5], [4], 4, 2, 64, True, 3, 8, 64)   # q_len > context
+    with pytest.raises(ValueError):
+        build_task_table([0, 1], [4], 6, 4, 64, True, 3, 8, 64)   # Hq not a multiple of Hkv
