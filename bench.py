@@ -1,0 +1,351 @@
+"""Benchmark of one step of the paged-KV varlen attention path on GB300.
+
+A step is one pass of the whole hot path over one batch: slot mapping, KV append, paged
+attention (+ split-KV merge), with the block table and task table (host-built per batch)
+already on the device.  The default workload is the decode batch (64 sequences, q = 1, context
+U[128, 4096], 32/32 heads, d = 128, 16-token pages); `--config` picks another.
+
+Prints one JSON line (rank 0).  `value` is device-timed throughput of the step with inputs
+resident in HBM; `e2e` is the same metric through the public Python API with pinned host
+inputs copied in and the output copied out every step; `roofline` reports the attention
+kernel's achieved bandwidth (or TFLOP/s) against the measured peak; `cpu_baseline` times the
+oracle on a bounded sample on the host cores.  `--impl reference` times the oracle alone.
+Multi-GPU (torchrun): independent replicas, one per rank (weak scaling, no data-path collective).
+"""
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the oracle baseline runs single-threaded BLAS so its core count is exact
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s vs roofline, tokens/s, 1×GB300"
+DESC = {
+    "tiny": "tiny mixed: 4 seqs (q 7,16,1,1; L 7,16,33,50), Hq 4 / Hkv 2, d 64, bs 16",
+    "decode": "decode: 64 seqs, q=1, L~U[128,4096], Hq=Hkv=32, d=128, bs=16, + kv_append of 64 tokens",
+    "prefill": "packed prefill: 16 seqs lognormal(512,1) in [32,8192], causal, Hq 32 / Hkv 8, d 128, bs 16",
+    "mixed": "mixed: 8 chunks x 512 (prior U[0,16384]) + 120 decodes L~U[256,32768], Hq 32 / Hkv 8, d 128, bs 16",
+    "skew": "long-context skew: 256 decodes (4 x 131072, 252 x 512), Hq 64 / Hkv 8, d 128, bs 256",
+}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], tc=d["bf16_tflops"], tc_sustained=d.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sustained=1700.0, source="fallback")
+
+
+def work(wl):
+    """Algorithmic work of one step: attention bytes (K/V read once + Q in + O out), append bytes
+    (new K/V read + written), and flops (4 d per visible (row, key) pair per query head)."""
+    d, Hq, Hkv = wl.head_dim, wl.num_heads_q, wl.num_heads_kv
+    L = wl.context_lens.astype(np.int64)
+    q = wl.q_lens.astype(np.int64)
+    kv_bytes = int(np.sum(L) * 2 * Hkv * d * 2)
+    qo_bytes = int(wl.num_tokens * Hq * d * 2 * 2)
+    append_bytes = int(wl.num_tokens * Hkv * d * 2 * 2 * 2)
+    if wl.causal:
+        pairs = int(np.sum(q * (L - q) + q * (q + 1) // 2))
+    else:
+        pairs = int(np.sum(q * L))
+    flops = 4 * d * Hq * pairs
+    return dict(attn_bytes=kv_bytes + qo_bytes, append_bytes=append_bytes, flops=flops, kv_bytes=kv_bytes)
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None):
+    """Time the oracle (as it stands) on a bounded sample of the workload's sequences, all their
+    rows.  Returns (seconds, sampled work dict, description)."""
+    import oracle
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    bt = oracle.allocate_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
+    rng = np.random.default_rng(0)
+    order = rng.permutation(wl.num_seqs)
+    cu = wl.cu_seqlens_q
+    spent, done = 0.0, []
+    q_all, kn_all, vn_all = bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"])
+    for i in order:
+        if spent >= budget_s or (max_seqs and len(done) >= max_seqs):
+            break
+        i = int(i)
+        pages = bt[i][bt[i] >= 0]
+        idx = torch.from_numpy(pages).long().to(vals["k_pool"].device)
+        kp, vp = bits(vals["k_pool"].index_select(0, idx)), bits(vals["v_pool"].index_select(0, idx))
+        t0, t1 = int(cu[i]), int(cu[i + 1])
+        sub_cu = np.array([0, t1 - t0], np.int32)
+        t = time.perf_counter()
+        oracle.step.run_step(sub_cu, wl.context_lens[i:i + 1], pages, wl.block_size, wl.max_blocks,
+                             q_all[t0:t1], kn_all[t0:t1], vn_all[t0:t1], kp, vp, wl.scale, wl.causal,
+                             pool_pages=pages)
+        spent += time.perf_counter() - t
+        done.append(i)
+    sub = workloads.custom(wl.q_lens[done], wl.context_lens[done], wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
+                           wl.block_size, wl.causal)
+    desc = f"{len(done)} of {wl.num_seqs} sequences (seeded random order), every row, full oracle step"
+    return spent, work(sub), desc
+
+
+def unit_of(config):
+    return ("TFLOP/s", "tensor") if config == "prefill" else ("GB/s", "hbm")
+
+
+def throughput(config, w, seconds):
+    if config == "prefill":
+        return w["flops"] / seconds / 1e12
+    return (w["attn_bytes"] + w["append_bytes"]) / seconds / 1e9
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = workloads.make(args.config)
+    vals = wl.tensors("cuda" if torch.cuda.is_available() else "cpu")
+    unit, _ = unit_of(args.config)
+    times = []
+    for k in range(args.warmup + args.steps):
+        secs, w, desc = oracle_sample(wl, vals, budget_s=args.ref_budget)
+        if k >= args.warmup:
+            times.append((secs, w))
+    secs = sum(t for t, _ in times)
+    value = sum(throughput(args.config, w, t) * t for t, w in times) / secs if secs else 0.0
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": DESC[args.config]},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode", choices=list(workloads.CONFIGS))
+    ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "xy" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import paged_kv_varlen_xy_gb300 as xy
+    from paged_kv_varlen_xy_gb300 import build as xybuild
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    xybuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+
+    wl = workloads.make(args.config)
+    vals = wl.tensors(dev)
+    w = work(wl)
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
+    pl = batch.plan
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty_like(vals["q"])
+    P = wl.num_pages
+
+    def step(ev=None):
+        xy.xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, wl.block_size, P, batch.slots, batch.err)
+        xy.xy_kv_append(vals["k_new"], vals["v_new"], batch.slots, vals["k_pool"], vals["v_pool"], batch.err)
+        if ev:
+            ev[0].record(stream)
+        xy.xy_paged_attention(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"], vals["v_pool"],
+                              wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
+        if ev:
+            ev[1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    xystep.check(batch)
+
+    # ---- device-timed region: K steps, inputs resident in HBM ----
+    n_launch_per_step = 3 + (1 if pl.merges.shape[0] else 0)
+    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        time.sleep(0.25)
+        t_start.record(stream)
+        for k in range(args.steps):
+            step(attn_ev[k])
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+        time.sleep(0.05)
+    xystep.check(batch)
+    total_ms = t_start.elapsed_time(t_stop)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    value = throughput(args.config, w, ms_per_step / 1e3) * world
+    unit, bound = unit_of(args.config)
+    if bound == "hbm":
+        achieved = w["attn_bytes"] / (attn_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
+                "traffic": None, "kernel": "paged_attention_kernel", "algorithmic_bytes": w["attn_bytes"],
+                "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
+    else:
+        achieved = w["flops"] / (attn_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["tc"], "unit": "TFLOP/s",
+                "frac": achieved / pk["tc"], "traffic": None, "kernel": "paged_attention_kernel",
+                "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
+
+    # ---- end to end through the public API: pinned host inputs in, output out, every step ----
+    host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    meta = dict(cu=wl.cu_seqlens_q, ctx=wl.context_lens, free=wl.free_list)
+    e2e_times = []
+    h2d = d2h = 0
+    for k in range(args.warmup + args.steps):
+        if world > 1 and k == args.warmup:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        b2 = xystep.PagedBatch(meta["cu"], meta["ctx"], meta["free"], wl.block_size, wl.max_blocks, wl.num_heads_q,
+                               wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, num_ctas=pl.num_ctas)
+        qd = host["q"].to(dev, non_blocking=True)
+        kd = host["k_new"].to(dev, non_blocking=True)
+        vd = host["v_new"].to(dev, non_blocking=True)
+        o = xystep.run_step(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
+        out_host.copy_(o, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_times.append(time.perf_counter() - t0)
+        if k == 0:
+            h2d = sum(host[x].numel() * 2 for x in host) + sum(t.numel() * t.element_size() for t in
+                                                                (b2.cu, b2.ctx, b2.block_table, b2.plan.tasks,
+                                                                 b2.plan.merges))
+            d2h = out_host.numel() * 2
+    e2e_s = sum(e2e_times[args.warmup:]) / args.steps
+    e2e_val = throughput(args.config, w, e2e_s) * world
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        secs, sw, desc = oracle_sample(wl, vals, budget_s=12.0)
+        cpu = {"value": throughput(args.config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
+               "sample": desc}
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": DESC[args.config], "parallelism": f"replicas x{world}",
+                       "l2": "KV working set larger than the 129 MB L2; no flush between steps"
+                             if w["kv_bytes"] > 4 * 129e6 else "L2 not flushed (small working set)",
+                       "step": "slot_mapping + kv_append + paged_attention" +
+                               (" + combine" if pl.merges.shape[0] else ""),
+                       "tokens_per_s": wl.num_tokens * world / (ms_per_step / 1e3),
+                       "tflops": w["flops"] / (ms_per_step / 1e3) / 1e12,
+                       "num_tasks": int(pl.tasks.shape[0]), "num_merges": int(pl.merges.shape[0]),
+                       "num_ctas": pl.num_ctas, "balance": pl.stats["balance"]},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_s * 1e3},
+            "gpu_launches": n_launch_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

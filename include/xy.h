@@ -1,0 +1,199 @@
+/*
+ * xy.h — C ABI of libxy: unified attention over a block-paged KV cache for a continuous
+ * batch of packed variable-length queries, on one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages on the subject, cited by title and section):
+ *   [XY]    "XY-Serve 深度实战：当昇腾 NPU 终于学会「驯服动态负载」" (chenxutan.com/d/5031)
+ *   [MindIE] MindIE serving notes (hwcomputing.csdn.net/6a130621662f9a54cb76c319)
+ *   [CANN]  cann-recipes-infer Paged KV Cache / Packed Sequence notes (dpshk.com/news/5336026)
+ *   [ATB]   ATB dynamic batching / speculative decoding / KV reuse notes (ai6s.net/6a38a2a6662f9a54cb828d66)
+ *
+ * One step of the path, in call order:
+ *   xy_build_block_table  (host)   logical -> physical page table from a FIFO free list
+ *   xy_slot_mapping       (device) physical slot of every new packed token
+ *   xy_kv_append          (device) write the new tokens' K/V into their slots
+ *   xy_build_task_table   (host)   decompose the batch into load-sorted, round-robin dealt tasks
+ *   xy_paged_attention    (device) fused QK^T -> masked online softmax -> PV over the pages,
+ *                                  plus the split-KV merge
+ *
+ * Conventions shared by every call:
+ *   - Notation: S sequences, T = cu_seqlens_q[S] packed new tokens, Hq query heads, Hkv KV heads
+ *     (Hq % Hkv == 0, query head h reads KV head h / (Hq/Hkv)), d = head_dim, bs = block_size,
+ *     P = num_pages, MB = max_blocks (columns of the block table).
+ *   - context_lens[i] = L_i counts the keys of sequence i INCLUDING its q_i new tokens;
+ *     new token j of sequence i sits at absolute position L_i - q_i + j.  1 <= q_i <= L_i.
+ *   - Causal attention is aligned bottom-right: new token j sees keys 0 .. L_i - q_i + j.
+ *   - Layouts (all row-major, contiguous): q/out [T, Hq, d] bf16; k_new/v_new [T, Hkv, d] bf16;
+ *     k_pages/v_pages [P, Hkv, bs, d] bf16 (one page of one head is a contiguous bs*d block);
+ *     block_table [S, MB] int32, -1 = unallocated; cu_seqlens_q [S+1] int32; context_lens [S]
+ *     int32; slot_mapping [T] int64, slot = page * bs + offset, negative = skip.
+ *   - Ownership: the caller allocates and frees every buffer; the library never allocates
+ *     device memory, never frees, never synchronises.  Device calls are asynchronous on the
+ *     given stream (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Errors: every call returns an xy_status; no exception crosses the ABI.  Host-visible
+ *     argument errors are reported before anything is launched.  Errors that only the device
+ *     can see (a page index outside [0, P), a slot outside the pool, a malformed task, a
+ *     bounded wait that expired) are OR-ed into *err_word (a device int32 the caller zeroes and
+ *     reads back after the stream has completed, see XY_DEV_*); the contents of the outputs are
+ *     then unspecified.  No kernel traps, asserts or waits without a bound.
+ */
+#ifndef XY_H
+#define XY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    XY_OK = 0,
+    XY_ERR_INVALID_ARG = -1,      /* null pointer, bad size, misaligned pointer */
+    XY_ERR_CU_SEQLENS = -2,       /* cu_seqlens_q[0] != 0 or not strictly increasing ([CANN] §4.4) */
+    XY_ERR_PAGE_OOB = -3,         /* a block-table entry outside [0, P) ([CANN] §4.4) */
+    XY_ERR_CONTEXT_LT_QLEN = -4,  /* some context_lens[i] < q_i */
+    XY_ERR_UNSUPPORTED = -5,      /* shape the kernels do not handle (head_dim, block_size, tiles) */
+    XY_ERR_WORKSPACE = -6,        /* workspace missing or smaller than xy_build_task_table asked for */
+    XY_ERR_CUDA = -7,             /* a CUDA runtime/driver call failed */
+    XY_ERR_TIMEOUT = -8,          /* reserved for a host-side wait; device waits use XY_DEV_TIMEOUT */
+    XY_ERR_OUT_OF_PAGES = -9,     /* free list exhausted ([XY] §4.2 allocator raises) */
+    XY_ERR_CAPACITY = -10         /* an output array given to a host call is too small */
+} xy_status;
+
+/* Bits OR-ed into *err_word by device code. */
+#define XY_DEV_PAGE_OOB   0x1     /* block-table entry needed by a key < L is outside [0, P) */
+#define XY_DEV_SLOT_OOB   0x2     /* slot outside [0, P*bs) in xy_kv_append */
+#define XY_DEV_BAD_TASK   0x4     /* task record violates the kernel's tile constraints */
+#define XY_DEV_TIMEOUT    0x8     /* a bounded mbarrier wait expired; the kernel returned early */
+
+/* One unit of attention work: rows [q_start, q_start + q_rows) of sequence `seq` (token index
+ * relative to the sequence) for all G = Hq/Hkv query heads of KV head `kv_head`, against keys
+ * [kv_start, kv_end).  num_splits > 1 means the tile's KV range is cut into that many chunks;
+ * this chunk then writes its normalised partial output and log-sum-exp to workspace rows
+ * ws_row + t*G + h_local (t < q_rows, h_local < G) instead of `out`; ws_row = -1 otherwise. */
+typedef struct {
+    int32_t seq, kv_head, q_start, q_rows, kv_start, kv_end, num_splits, ws_row;
+} xy_task;
+
+/* One split tile to merge: chunk c of the tile owns workspace rows
+ * ws_row + c*q_rows*G + t*G + h_local.  zero0/zero1 are 0. */
+typedef struct {
+    int32_t seq, kv_head, q_start, q_rows, num_splits, ws_row, zero0, zero1;
+} xy_merge;
+
+/* Balance of the static deal ([XY] §2.2 component 2: balance ratio = min/max core load). */
+typedef struct {
+    int64_t total_load;
+    int64_t max_cta_load;
+    int64_t min_cta_load;
+    double balance;           /* min/max of per-CTA load sums, 1.0 for an empty batch */
+} xy_task_stats;
+
+/* Static description of a status code ("ok", "invalid argument", ...). Never NULL. */
+const char *xy_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int xy_version(void);
+
+/* Number of CTAs the persistent attention kernel runs per GPU (SM count x CTAs per SM) for
+ * `device`, or a negative xy_status.  Host call; needs a CUDA device. */
+int xy_default_num_ctas(int device);
+
+/*
+ * a1 — block table ([CANN] §2.2 page table, §3.2 allocate_pages; [XY] §4.2 KVCacheAllocator).
+ * Host call, pure.  For sequences in batch order, takes ceil(L_i / bs) pages from the front of
+ * free_list (FIFO) and writes them to block_table[i][0..n_i); the rest of row i is -1.
+ *   context_lens [num_seqs] host; free_list [num_free] host, physical page ids;
+ *   block_table [num_seqs, max_blocks] host, written in full; *pages_used = pages taken.
+ * Errors: XY_ERR_INVALID_ARG (null pointers, num_seqs < 0, block_size not a power of two >= 16,
+ *   L_i < 1), XY_ERR_CAPACITY (ceil(L_i/bs) > max_blocks), XY_ERR_OUT_OF_PAGES (list exhausted).
+ */
+xy_status xy_build_block_table(const int32_t *context_lens, int num_seqs, int block_size,
+                               const int32_t *free_list, int num_free, int max_blocks,
+                               int32_t *block_table, int *pages_used);
+
+/*
+ * a2 — slot mapping (pages silent; reading: new token j of sequence i at absolute position
+ * p = L_i - q_i + j goes to slot block_table[i][p / bs] * bs + p % bs).  Device call.
+ *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs], block_table [num_seqs, max_blocks]:
+ *   device int32; slot_mapping [num_tokens] device int64, written in full.
+ * A block-table entry outside [0, num_pages) sets XY_DEV_PAGE_OOB and that token's slot to -1.
+ * Errors: XY_ERR_INVALID_ARG, XY_ERR_CUDA (launch failure).
+ */
+xy_status xy_slot_mapping(const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                          const int32_t *block_table, int num_seqs, int max_blocks, int num_tokens,
+                          int block_size, int num_pages, int64_t *slot_mapping, int32_t *err_word,
+                          void *stream);
+
+/*
+ * a3 — KV append ([CANN] §2.2 pages filled on demand, §3.1 page layout; [ATB] KV缓存复用:
+ * chunked prefill appends to the existing cache).  Device call: for every token t with
+ * slot_mapping[t] >= 0 and every KV head h, copies k_new[t][h][:] to
+ * k_pages[slot / bs][h][slot % bs][:] and the same for V.  Bit copy; tokens are written in no
+ * particular order, so two tokens with the same slot leave either one's data.
+ *   k_new, v_new [num_tokens, Hkv, d] bf16 device; slot_mapping [num_tokens] int64 device;
+ *   k_pages, v_pages [num_pages, Hkv, bs, d] bf16 device, updated in place.
+ * All pointers 16-byte aligned; head_dim a multiple of 8.  A slot >= num_pages*bs sets
+ * XY_DEV_SLOT_OOB and is skipped.
+ * Errors: XY_ERR_INVALID_ARG, XY_ERR_CUDA.
+ */
+xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                       int num_tokens, void *k_pages, void *v_pages, int num_pages,
+                       int num_heads_kv, int block_size, int head_dim, int32_t *err_word,
+                       void *stream);
+
+/*
+ * a4 — task table: dynamic decomposer + attention task reorder ([XY] §2.2 components 1 and 2,
+ * §4.4 decompose_attention / analyze_load_balance).  Host call, pure.
+ * Enumerates, for sequence i -> KV head g -> query tile (q_tile tokens) -> KV chunk (kv_chunk
+ * keys), one xy_task with load = q_rows * G * (kv_end - kv_start), where the tile's KV range is
+ * [0, L_i) or, if causal, [0, L_i - q_i + q_start + q_rows); stable-sorts by load, largest first;
+ * CTA c of the persistent launch runs tasks[c], tasks[c + num_ctas], ...  Split tiles
+ * (num_splits > 1) get workspace rows in enumeration order and one xy_merge each.
+ *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs]: host int32.
+ *   tasks [max_tasks], merges [max_merges]: host outputs; pass NULL (with max 0) to query counts.
+ *   *num_tasks, *num_merges: counts; *workspace_bytes = rows * (head_dim + 1) * 4 (fp32 partial
+ *   outputs followed by fp32 log-sum-exps); stats may be NULL.
+ * Errors: XY_ERR_INVALID_ARG (sizes <= 0, Hq % Hkv), XY_ERR_CU_SEQLENS,
+ *   XY_ERR_CONTEXT_LT_QLEN, XY_ERR_CAPACITY (non-NULL arrays too small).
+ */
+xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                              int num_seqs, int num_heads_q, int num_heads_kv, int head_dim,
+                              int causal, int num_ctas, int q_tile, int kv_chunk,
+                              xy_task *tasks, int max_tasks, int *num_tasks,
+                              xy_merge *merges, int max_merges, int *num_merges,
+                              size_t *workspace_bytes, xy_task_stats *stats);
+
+/*
+ * a5..a10 — paged attention ([XY] §2.2 component 3 Meta-Attention: one GEMM-softmax-GEMM
+ * kernel driven by the task table, with no prefill/decode distinction; [CANN] §3.3 packed
+ * paged_attention(q_packed, kv_pages, cu_seqlens, page_table, is_causal); [XY] §2.3 virtual
+ * padding: only valid rows/keys are used and stored).  Device call.
+ * out[t][h][:] = sum_k softmax_k(scale * q[t][h] . K_k) V_k over the keys k the token sees,
+ * K/V gathered through block_table; fp32 accumulation, output rounded to bf16 (nearest even).
+ *   q [num_tokens, Hq, d], k_pages/v_pages [num_pages, Hkv, bs, d], out [num_tokens, Hq, d]:
+ *   bf16 device, 16-byte aligned.  cu_seqlens_q, context_lens, block_table: device int32.
+ *   tasks [num_tasks], merges [num_merges]: device copies of xy_build_task_table's output for
+ *   the same batch and the same num_ctas.
+ *   workspace: device, >= the workspace_bytes the builder returned (may be NULL when 0).
+ *   err_word: device int32 (see XY_DEV_*).
+ * Supported: head_dim 64 or 128; block_size a power of two in [16, 256]; kv chunks that are
+ * multiples of 64 keys; q_rows * (Hq/Hkv) <= 64 rows per task.
+ * Errors: XY_ERR_INVALID_ARG, XY_ERR_UNSUPPORTED, XY_ERR_WORKSPACE, XY_ERR_CUDA.
+ */
+xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q,
+                             const int32_t *context_lens, const int32_t *block_table,
+                             int max_blocks, const void *k_pages, const void *v_pages,
+                             int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                             int num_heads_kv, int head_dim, int block_size, float scale,
+                             int causal, const xy_task *tasks, int num_tasks,
+                             const xy_merge *merges, int num_merges, int num_ctas,
+                             void *workspace, size_t workspace_bytes, int32_t *err_word,
+                             void *out, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XY_H */

@@ -53,6 +53,7 @@ from .attention import (
     virtual_mask,
 )
 from .tasks import build_task_table, TASK_FIELDS, MERGE_FIELDS
+from . import step
 
 __all__ = [
     "bf16_bits_to_f64",
@@ -71,4 +72,5 @@ __all__ = [
     "build_task_table",
     "TASK_FIELDS",
     "MERGE_FIELDS",
+    "step",
 ]

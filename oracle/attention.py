@@ -89,12 +89,16 @@ def attention_rows(rows, q, cu_seqlens_q, context_lens, block_table, k_pages, v_
     G = Hq // Hkv
     cu = np.asarray(cu_seqlens_q)
     res = []
+    gathered = {}           # (sequence, kv head) -> (K, V), gathered once per call
     for (t, h) in rows:
         i = int(np.searchsorted(cu, t, side="right") - 1)
         qn, L = int(cu[i + 1] - cu[i]), int(context_lens[i])
         j = t - int(cu[i])
-        K = gather_kv(k_pages, block_table[i], L, h // G)
-        V = gather_kv(v_pages, block_table[i], L, h // G)
+        key = (i, h // G)
+        if key not in gathered:
+            gathered[key] = (gather_kv(k_pages, block_table[i], L, h // G),
+                             gather_kv(v_pages, block_table[i], L, h // G))
+        K, V = gathered[key]
         res.append(attention_row(q[t, h], K, V, _visible_keys(L, qn, j, causal), scale))
     return np.array(res, dtype=np.float64).reshape(len(rows), q.shape[2])
 

@@ -1,0 +1,258 @@
+"""Python binding of libxy (unified paged-KV varlen attention on GB300).
+
+Argument marshalling only: every step of the path runs in libxy's C++ host code or CUDA
+kernels.  The functions carry the C-ABI's names (``xy_*``, declared in ``include/xy.h``);
+torch tensors supply device memory and the current CUDA stream, numpy arrays the host inputs
+of the host-side builders.  If libxy.so has not been built the import still succeeds, but
+every call raises; there is no fallback path.
+"""
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libxy.so")
+
+XY_DEV_PAGE_OOB = 0x1
+XY_DEV_SLOT_OOB = 0x2
+XY_DEV_BAD_TASK = 0x4
+XY_DEV_TIMEOUT = 0x8
+
+C_ABI = ("xy_status_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
+         "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention")
+
+
+class XYError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class XYDeviceError(RuntimeError):
+    def __init__(self, bits):
+        self.bits = bits
+        names = [n for b, n in ((XY_DEV_PAGE_OOB, "page index out of range"), (XY_DEV_SLOT_OOB, "slot out of range"),
+                                (XY_DEV_BAD_TASK, "malformed task"), (XY_DEV_TIMEOUT, "bounded wait expired"))
+                 if bits & b]
+        super().__init__("libxy device error: " + ", ".join(names or [hex(bits)]))
+
+
+class TaskStats(ctypes.Structure):
+    _fields_ = [("total_load", ctypes.c_int64), ("max_cta_load", ctypes.c_int64),
+                ("min_cta_load", ctypes.c_int64), ("balance", ctypes.c_double)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libxy (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libxy.so is not built ({LIB_PATH}); run paged_kv_varlen_xy_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, I64, F, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
+    SZ = ctypes.c_size_t
+    L.xy_status_string.argtypes = [I]
+    L.xy_status_string.restype = ctypes.c_char_p
+    L.xy_version.argtypes = []
+    L.xy_version.restype = I
+    L.xy_default_num_ctas.argtypes = [I]
+    L.xy_default_num_ctas.restype = I
+    L.xy_build_block_table.argtypes = [P, I, I, P, I, I, P, P]
+    L.xy_build_block_table.restype = I
+    L.xy_slot_mapping.argtypes = [P, P, P, I, I, I, I, I, P, P, P]
+    L.xy_slot_mapping.restype = I
+    L.xy_kv_append.argtypes = [P, P, P, I, P, P, I, I, I, I, P, P]
+    L.xy_kv_append.restype = I
+    L.xy_build_task_table.argtypes = [P, P, I, I, I, I, I, I, I, I, P, I, P, P, I, P, P, P]
+    L.xy_build_task_table.restype = I
+    L.xy_paged_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P, P, P]
+    L.xy_paged_attention.restype = I
+    _lib = L
+    return L
+
+
+def status_string(status):
+    return lib().xy_status_string(int(status)).decode()
+
+
+def _check(status, where):
+    if status != 0:
+        raise XYError(status, where)
+
+
+def _host_i32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _dev(t, dtype, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def xy_version():
+    return lib().xy_version()
+
+
+def xy_default_num_ctas(device=0):
+    n = lib().xy_default_num_ctas(int(device))
+    if n < 0:
+        raise XYError(n, "xy_default_num_ctas")
+    return n
+
+
+def xy_build_block_table(context_lens, block_size, free_list, max_blocks):
+    """a1 (host): block table [S, max_blocks] int32 from the FIFO free list; returns (table, pages_used)."""
+    ctx, pctx = _host_i32(context_lens)
+    free, pfree = _host_i32(free_list)
+    S = len(ctx)
+    table = np.empty((S, int(max_blocks)), dtype=np.int32)
+    used = ctypes.c_int(0)
+    _check(lib().xy_build_block_table(pctx, S, int(block_size), pfree, len(free), int(max_blocks),
+                                      table.ctypes.data_as(ctypes.c_void_p), ctypes.byref(used)),
+           "xy_build_block_table")
+    return table, used.value
+
+
+def xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, num_ctas,
+                        q_tile, kv_chunk):
+    """a4 (host): returns dict(tasks [n,8] int32, merges [m,8] int32, workspace_bytes, stats)."""
+    cu, pcu = _host_i32(cu_seqlens_q)
+    ctx, pctx = _host_i32(context_lens)
+    S = len(cu) - 1
+    args = (pcu, pctx, S, int(num_heads_q), int(num_heads_kv), int(head_dim), int(bool(causal)), int(num_ctas),
+            int(q_tile), int(kv_chunk))
+    n, m, ws = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
+    L = lib()
+    _check(L.xy_build_task_table(*args, None, 0, ctypes.byref(n), None, 0, ctypes.byref(m), ctypes.byref(ws), None),
+           "xy_build_task_table")
+    tasks = np.zeros((n.value, 8), dtype=np.int32)
+    merges = np.zeros((m.value, 8), dtype=np.int32)
+    st = TaskStats()
+    _check(L.xy_build_task_table(*args, tasks.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n),
+                                 merges.ctypes.data_as(ctypes.c_void_p), m.value, ctypes.byref(m),
+                                 ctypes.byref(ws), ctypes.byref(st)), "xy_build_task_table")
+    return dict(tasks=tasks, merges=merges, workspace_bytes=ws.value,
+                stats=dict(total_load=st.total_load, max_cta_load=st.max_cta_load,
+                           min_cta_load=st.min_cta_load, balance=st.balance))
+
+
+def xy_slot_mapping(cu_seqlens_q, context_lens, block_table, block_size, num_pages, slot_mapping, err_word,
+                    stream=None):
+    """a2 (device): fills slot_mapping [T] int64 on the stream."""
+    import torch
+    S = cu_seqlens_q.numel() - 1
+    _check(lib().xy_slot_mapping(_dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"),
+                                 _dev(context_lens, torch.int32, "context_lens"),
+                                 _dev(block_table, torch.int32, "block_table"), S, block_table.shape[1],
+                                 slot_mapping.numel(), int(block_size), int(num_pages),
+                                 _dev(slot_mapping, torch.int64, "slot_mapping"),
+                                 _dev(err_word, torch.int32, "err_word"), _stream(stream)), "xy_slot_mapping")
+
+
+def xy_kv_append(k_new, v_new, slot_mapping, k_pages, v_pages, err_word, stream=None):
+    """a3 (device): writes k_new/v_new [T, Hkv, d] into k_pages/v_pages [P, Hkv, bs, d] at the slots."""
+    import torch
+    P, Hkv, bs, d = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or tuple(k_new.shape) != tuple(v_new.shape):
+        raise ValueError("K and V shapes differ")
+    if k_new.shape[1:] != (Hkv, d) or k_new.shape[0] != slot_mapping.numel():
+        raise ValueError("k_new must be [T, Hkv, d] with T = len(slot_mapping)")
+    bf = torch.bfloat16
+    _check(lib().xy_kv_append(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"),
+                              _dev(slot_mapping, torch.int64, "slot_mapping"), k_new.shape[0],
+                              _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P, Hkv, bs, d,
+                              _dev(err_word, torch.int32, "err_word"), _stream(stream)), "xy_kv_append")
+
+
+def xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, tasks, merges,
+                       num_ctas, workspace, err_word, out, stream=None):
+    """a5..a10 (device): out [T, Hq, d] bf16.  tasks/merges: device int32 [n, 8] / [m, 8] from
+    xy_build_task_table with the same num_ctas; workspace: device uint8 tensor (or None when no merges)."""
+    import torch
+    T, Hq, d = q.shape
+    P, Hkv, bs, d2 = k_pages.shape
+    if d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch between q, out and the page pools")
+    bf = torch.bfloat16
+    nm = merges.shape[0] if merges is not None else 0
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None and workspace.numel() else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().xy_paged_attention(
+        _dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(context_lens, torch.int32, "context_lens"),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _dev(k_pages, bf, "k_pages"),
+        _dev(v_pages, bf, "v_pages"), P, cu_seqlens_q.numel() - 1, T, Hq, Hkv, d, bs, float(scale), int(bool(causal)),
+        _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
+        _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
+        _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention")
+
+
+def check_err_word(err_word):
+    """Synchronise on err_word's value and raise XYDeviceError if any device check fired."""
+    bits = int(err_word.item())
+    if bits:
+        raise XYDeviceError(bits)
+
+
+def default_tiles(num_heads_q, num_heads_kv):
+    """Tile policy of the kernels: a query tile holds up to 64 (token, head) rows, so
+    q_tile = max(1, 64 // G) tokens; KV chunks of 4096 keys (a multiple of every page size)."""
+    G = num_heads_q // num_heads_kv
+    return max(1, 64 // G), 4096
+
+
+class Plan:
+    """Per-batch state for xy_paged_attention: the task table (built on the host from host copies of
+    cu_seqlens_q and context_lens) uploaded to the device, and the workspace it needs."""
+
+    def __init__(self, cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, device="cuda",
+                 num_ctas=None, q_tile=None, kv_chunk=None):
+        import torch
+        dev = torch.device(device)
+        self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)
+        dq, dk = default_tiles(num_heads_q, num_heads_kv)
+        self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
+        r = xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
+                                self.num_ctas, self.q_tile, self.kv_chunk)
+        self.host = r
+        self.stats = r["stats"]
+        self.tasks = torch.from_numpy(r["tasks"]).to(dev)
+        self.merges = torch.from_numpy(r["merges"]).to(dev)
+        self.workspace = torch.empty(max(r["workspace_bytes"], 16), dtype=torch.uint8, device=dev)
+        self.causal = causal
+
+
+def paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, plan=None,
+                    out=None, err_word=None, check=True):
+    """out = attention of the packed queries over the paged cache (signature of the pages' packed
+    paged_attention call).  Builds a Plan from host copies of cu_seqlens_q/context_lens when none is given."""
+    import torch
+    if plan is None:
+        plan = Plan(cu_seqlens_q.cpu().numpy(), context_lens.cpu().numpy(), q.shape[1], k_pages.shape[1], q.shape[2],
+                    causal, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    own_err = err_word is None
+    err_word = torch.zeros(1, dtype=torch.int32, device=q.device) if own_err else err_word
+    xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, plan.tasks,
+                       plan.merges, plan.num_ctas, plan.workspace, err_word, out)
+    if check and own_err:
+        check_err_word(err_word)
+    return out

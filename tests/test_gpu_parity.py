@@ -1,0 +1,156 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle on the same seeded inputs.
+
+Block table, slot mapping and appended pages are compared bit for bit; attention outputs (bf16,
+fp32 accumulation) against the fp64 oracle within max-abs 2e-2 and mean-abs 2e-3.  Small batches
+are compared on every row; the full-size workloads on sampled sequences and rows, in the launch
+configuration bench.py times."""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_cases import assert_parity, run, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_varlen_xy_gb300 import build
+    build.build()
+
+
+def test_tiny_mixed_batch_every_row():
+    r = run(workloads.tiny())
+    assert_parity(r)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("bs", [16, 256])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ragged_batch_every_row(d, bs, causal):
+    # several 64-row tiles with ragged tails, GQA 4, prior context, decode rows
+    wl = workloads.custom([1, 17, 130, 77, 40, 1], [1, 40, 130, 500, 333, 700], 8, 2, d, bs, causal=causal,
+                          seed=100 + d + bs + int(causal))
+    assert_parity(run(wl))
+
+
+@pytest.mark.parametrize("kv_chunk", [64, 128, 192])
+def test_split_kv_and_combine_every_row(kv_chunk):
+    wl = workloads.custom([3, 1, 50, 1], [300, 257, 190, 64], 8, 2, 128, 16, seed=kv_chunk)
+    r = run(wl, kv_chunk=kv_chunk)
+    assert len(r["batch"].plan.host["merges"]) > 0
+    assert_parity(r)
+
+
+@pytest.mark.parametrize("G", [1, 2, 8, 16])
+def test_gqa_groups(G):
+    wl = workloads.custom([1, 5, 33, 2], [90, 5, 70, 130], 2 * G, 2, 128, 16, seed=G)
+    assert_parity(run(wl))
+
+
+def test_nan_in_unused_slots_never_reaches_outputs():
+    # the whole pool starts as NaN; the step appends every context token (q = L), so only
+    # slots past each context end and untouched pages stay NaN
+    wl = workloads.custom([5, 37, 64, 70], [5, 37, 64, 70], 4, 2, 128, 16, seed=3)
+    r = run(wl, pool_fill=float("nan"))
+    assert_parity(r, check_pages=False)
+    wl = workloads.custom([5, 37, 64, 70], [5, 37, 64, 70], 4, 2, 128, 16, seed=3)
+    r = run(wl, pool_fill=float("nan"), kv_chunk=64)
+    assert_parity(r, check_pages=False)
+
+
+def test_num_ctas_variants():
+    wl = workloads.custom([1, 9, 1, 100], [300, 9, 20, 130], 8, 4, 64, 16, seed=5)
+    for n in (1, 3, 300):
+        assert_parity(run(wl, num_ctas=n))
+
+
+def test_full_size_decode_sampled():
+    wl = workloads.decode()
+    rng = np.random.default_rng(0)
+    seqs = sorted(rng.choice(wl.num_seqs, size=6, replace=False).tolist())
+    seqs.append(int(np.argmax(wl.context_lens)))
+    r = run(wl, rows=sample_rows(wl, seqs, rng), sample_seqs=seqs)
+    assert_parity(r)
+
+
+def test_full_size_prefill_sampled():
+    wl = workloads.prefill()
+    rng = np.random.default_rng(1)
+    seqs = sorted({int(np.argmax(wl.q_lens)), int(np.argmin(wl.q_lens)), int(rng.integers(wl.num_seqs))})
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=64 // wl.group), sample_seqs=seqs)
+    assert_parity(r)
+
+
+def test_full_size_mixed_sampled():
+    wl = workloads.mixed()
+    rng = np.random.default_rng(2)
+    seqs = [0, 5, 8, 60, 127, int(np.argmax(wl.context_lens))]
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=64 // wl.group), sample_seqs=seqs)
+    assert_parity(r)
+
+
+def test_full_size_skew_sampled():
+    wl = workloads.skew()
+    long_seq = int(np.argmax(wl.context_lens))
+    seqs = [long_seq, int(np.argmin(wl.context_lens))]
+    rng = np.random.default_rng(3)
+    r = run(wl, rows=sample_rows(wl, seqs, rng), sample_seqs=seqs)
+    assert_parity(r)
+
+
+def test_page_index_out_of_range_sets_error_bit():
+    import paged_kv_varlen_xy_gb300 as xy
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    wl = workloads.custom([1, 1], [40, 20], 4, 2, 64, 16, seed=9)
+    vals = wl.tensors("cuda")
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal)
+    batch.block_table[0, 1] = wl.num_pages + 5          # a page outside the pool, inside the context
+    xystep.run_step(batch, vals["q"], vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"], wl.scale)
+    torch.cuda.synchronize()
+    with pytest.raises(xy.XYDeviceError) as e:
+        xystep.check(batch)
+    assert e.value.bits & xy.XY_DEV_PAGE_OOB
+    # the context is still usable
+    r = run(workloads.tiny())
+    assert_parity(r)
+
+
+def test_host_validation_rejects_bad_arguments():
+    import paged_kv_varlen_xy_gb300 as xy
+    wl = workloads.tiny()
+    vals = wl.tensors("cuda")
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal)
+    pl = batch.plan
+    out = torch.empty_like(vals["q"])
+    with pytest.raises(xy.XYError) as e:    # head_dim 48 is not supported
+        q48 = torch.zeros(vals["q"].shape[0], 4, 48, dtype=torch.bfloat16, device="cuda")
+        kp48 = torch.zeros(64, 2, 16, 48, dtype=torch.bfloat16, device="cuda")
+        xy.xy_paged_attention(q48, batch.cu, batch.ctx, batch.block_table, kp48, kp48, 0.1, True, pl.tasks,
+                              pl.merges, pl.num_ctas, pl.workspace, batch.err, torch.empty_like(q48))
+    assert e.value.status == -5
+    with pytest.raises(xy.XYError) as e:    # misaligned pointer
+        T = vals["q"].shape[0]
+        qv = vals["q"].view(-1)[1: 1 + (T - 1) * 256].view(T - 1, 4, 64)
+        xy.xy_paged_attention(qv, batch.cu, batch.ctx, batch.block_table, vals["k_pool"], vals["v_pool"], 0.1,
+                              True, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, torch.empty_like(qv))
+    assert e.value.status == -1
+    torch.cuda.synchronize()
+    assert int(batch.err.item()) == 0
+
+
+def test_empty_batch_launches_nothing():
+    import paged_kv_varlen_xy_gb300 as xy
+    dev = "cuda"
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kp = torch.zeros(4, 1, 16, 64, dtype=torch.bfloat16, device=dev)
+    empty = torch.zeros(0, 1, 64, dtype=torch.bfloat16, device=dev)
+    slots = torch.zeros(0, dtype=torch.int64, device=dev)
+    xy.xy_kv_append(empty, empty, slots, kp, kp, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0

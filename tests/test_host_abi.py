@@ -1,0 +1,137 @@
+"""CPU checks of the C ABI: libxy loads without a GPU, exports every declared symbol, and its host
+calls (block table, task table) agree bit-exactly with the oracle and reject bad input."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from paged_kv_varlen_xy_gb300 import build as xybuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def xy():
+    xybuild.build()
+    import paged_kv_varlen_xy_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "xy.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(xy_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(xy):
+    names = _declared()
+    assert len(names) >= 8
+    L = ctypes.CDLL(xy.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert sorted(xy.C_ABI) == names
+
+
+def test_status_strings(xy):
+    assert xy.status_string(0) == "ok"
+    for code in range(-10, 0):
+        assert xy.status_string(code) != "unknown status"
+    assert xy.status_string(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_block_table_matches_oracle_on_configs(xy, name):
+    wl = workloads.make(name)
+    mine, used = xy.xy_build_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
+    ref = oracle.allocate_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
+    assert np.array_equal(mine, ref)
+    assert used == int(np.sum(-(-wl.context_lens.astype(np.int64) // wl.block_size)))
+
+
+def test_block_table_fuzz(xy):
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        S = int(rng.integers(1, 20))
+        bs = int(2 ** rng.integers(4, 9))
+        ctx = rng.integers(1, 2000, size=S)
+        need = int(np.sum(-(-ctx // bs)))
+        P = need + int(rng.integers(0, 10))
+        free = rng.permutation(P).astype(np.int32)
+        MB = int(np.max(-(-ctx // bs))) + int(rng.integers(0, 3))
+        mine, _ = xy.xy_build_block_table(ctx, bs, free, MB)
+        assert np.array_equal(mine, oracle.allocate_block_table(ctx, bs, free, MB))
+
+
+def test_block_table_errors(xy):
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_block_table([16, 17], 16, np.arange(2), 2)
+    assert e.value.status == -9            # pool exhausted
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_block_table([33], 16, np.arange(8), 2)
+    assert e.value.status == -10           # more blocks than the table has columns
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_block_table([3], 12, np.arange(8), 2)
+    assert e.value.status == -1            # page size must be a power of two >= 16
+
+
+def _tiles(G):
+    return max(1, 64 // G), 4096
+
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_task_table_matches_oracle_on_configs(xy, name):
+    wl = workloads.make(name)
+    qt, ch = _tiles(wl.group)
+    args = (wl.cu_seqlens_q, wl.context_lens, wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, 152, qt, ch)
+    mine = xy.xy_build_task_table(*args)
+    ref = oracle.build_task_table(*args)
+    assert np.array_equal(mine["tasks"], ref["tasks"])
+    assert np.array_equal(mine["merges"], ref["merges"])
+    assert mine["workspace_bytes"] == ref["workspace_bytes"]
+    assert mine["stats"]["max_cta_load"] == int(ref["cta_loads"].max())
+    assert mine["stats"]["min_cta_load"] == int(ref["cta_loads"].min())
+    assert mine["stats"]["total_load"] == int(ref["loads"].sum())
+    assert mine["stats"]["balance"] == pytest.approx(ref["balance"], rel=1e-15)
+
+
+def test_task_table_fuzz(xy):
+    rng = np.random.default_rng(1)
+    for _ in range(60):
+        S = int(rng.integers(1, 12))
+        q = rng.integers(1, 300, size=S)
+        ctx = q + rng.integers(0, 3000, size=S)
+        Hkv = int(rng.integers(1, 5))
+        Hq = Hkv * int(rng.integers(1, 9))
+        args = (oracle.pack_cu_seqlens(q), ctx, Hq, Hkv, int(rng.choice([64, 128])), bool(rng.integers(0, 2)),
+                int(rng.integers(1, 200)), int(rng.integers(1, 70)), int(rng.choice([16, 64, 100, 256, 4096])))
+        mine = xy.xy_build_task_table(*args)
+        ref = oracle.build_task_table(*args)
+        assert np.array_equal(mine["tasks"], ref["tasks"])
+        assert np.array_equal(mine["merges"], ref["merges"])
+        assert mine["workspace_bytes"] == ref["workspace_bytes"]
+
+
+def test_task_table_errors(xy):
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_task_table([1, 3], [5], 4, 2, 64, True, 8, 8, 64)
+    assert e.value.status == -2            # cu_seqlens[0] != 0
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_task_table([0, 3, 3], [5, 5], 4, 2, 64, True, 8, 8, 64)
+    assert e.value.status == -2            # not strictly increasing
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_task_table([0, 6], [5], 4, 2, 64, True, 8, 8, 64)
+    assert e.value.status == -4            # context shorter than the query
+    with pytest.raises(xy.XYError) as e:
+        xy.xy_build_task_table([0, 6], [9], 6, 4, 64, True, 8, 8, 64)
+    assert e.value.status == -1            # Hq not a multiple of Hkv
+
+
+def test_task_table_empty_batch(xy):
+    r = xy.xy_build_task_table([0], [], 4, 2, 64, True, 8, 8, 64)
+    assert r["tasks"].shape == (0, 8) and r["workspace_bytes"] == 0 and r["stats"]["balance"] == 1.0
