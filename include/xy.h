@@ -192,6 +192,38 @@ xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q,
                              void *workspace, size_t workspace_bytes, int32_t *err_word,
                              void *out, void *stream);
 
+/*
+ * Paged attention that allocates nothing (no counterpart in the pages: it is a convenience for
+ * callers of this library).
+ *
+ * Some callers cannot allocate device memory where they run a step: a serving process that
+ * hands all free HBM to the KV page pool at start-up, so a per-step cudaMalloc of the split-KV
+ * workspace would fail, or an engine whose device memory belongs to an allocator that this
+ * library cannot call.  This entry point does what xy_paged_attention does, but takes its
+ * split-KV scratch from a fixed array inside libxy (XY_NOALLOC_SCRATCH_BYTES bytes of device
+ * memory, which every GPU that loads the library holds until the process exits) instead of a
+ * caller buffer.  It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   workspace_bytes: the bytes xy_build_task_table reported for this batch; a value above
+ *   XY_NOALLOC_SCRATCH_BYTES returns XY_ERR_WORKSPACE before anything is launched.
+ *   All other arguments, layouts and errors are those of xy_paged_attention.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  Every call on a device
+ * shares the one array and it keeps the last call's contents (nothing in it has to start at
+ * zero), so calls that overlap on the GPU -- on different streams, or from different host
+ * threads -- race on it and must be serialised by the caller.
+ */
+#define XY_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
+                                     const int32_t *context_lens, const int32_t *block_table,
+                                     int max_blocks, const void *k_pages, const void *v_pages,
+                                     int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                     int num_heads_kv, int head_dim, int block_size, float scale,
+                                     int causal, const xy_task *tasks, int num_tasks,
+                                     const xy_merge *merges, int num_merges, int num_ctas,
+                                     size_t workspace_bytes, int32_t *err_word, void *out,
+                                     void *stream);
+
 #ifdef __cplusplus
 }
 #endif

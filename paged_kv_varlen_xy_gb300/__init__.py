@@ -21,7 +21,11 @@ XY_DEV_BAD_TASK = 0x4
 XY_DEV_TIMEOUT = 0x8
 
 C_ABI = ("xy_status_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
-         "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention")
+         "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
+         "xy_paged_attention_noalloc")
+
+# size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
+XY_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class XYError(RuntimeError):
@@ -73,6 +77,9 @@ def lib():
     L.xy_build_task_table.restype = I
     L.xy_paged_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P, P, P]
     L.xy_paged_attention.restype = I
+    L.xy_paged_attention_noalloc.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, SZ, P, P,
+                                             P]
+    L.xy_paged_attention_noalloc.restype = I
     _lib = L
     return L
 
@@ -203,6 +210,29 @@ def xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pa
         _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
         _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
         _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention")
+
+
+def xy_paged_attention_noalloc(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, tasks,
+                               merges, num_ctas, workspace_bytes, err_word, out, stream=None):
+    """xy_paged_attention for callers that cannot allocate device memory: the split-KV scratch
+    comes from a fixed array inside libxy (XY_NOALLOC_SCRATCH_BYTES).  workspace_bytes is the
+    size xy_build_task_table reported; larger batches raise XYError (XY_ERR_WORKSPACE).  Calls
+    on one device share that array, so they must not overlap on the GPU."""
+    import torch
+    T, Hq, d = q.shape
+    P, Hkv, bs, d2 = k_pages.shape
+    if d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch between q, out and the page pools")
+    bf = torch.bfloat16
+    nm = merges.shape[0] if merges is not None else 0
+    _check(lib().xy_paged_attention_noalloc(
+        _dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(context_lens, torch.int32, "context_lens"),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _dev(k_pages, bf, "k_pages"),
+        _dev(v_pages, bf, "v_pages"), P, cu_seqlens_q.numel() - 1, T, Hq, Hkv, d, bs, float(scale), int(bool(causal)),
+        _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
+        _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), int(workspace_bytes),
+        _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)),
+        "xy_paged_attention_noalloc")
 
 
 def check_err_word(err_word):

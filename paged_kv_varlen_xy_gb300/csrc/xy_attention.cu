@@ -23,6 +23,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <vector>
 
 #include "xy.h"
 #include "xy_device.cuh"
@@ -609,4 +610,51 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return head_dim == 128 ? launch<128>(p, km, vm, num_ctas, merges, num_merges, st)
                            : launch<64>(p, km, vm, num_ctas, merges, num_merges, st);
+}
+
+// ---------------------------------------------------------------------------------------------
+// No-allocation variant: the split-KV scratch is a fixed array in this library instead of a caller
+// buffer.  Host code only ever sees a stand-in symbol for the array, never its device address, so
+// the address is looked up once per device (with that device current) and cached.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[XY_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+xy_status noalloc_scratch(void **ptr) {
+    static std::mutex mu;
+    static std::vector<void *> by_device;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return XY_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if ((int)by_device.size() <= dev) by_device.resize(dev + 1, nullptr);
+    if (!by_device[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return XY_ERR_CUDA;
+        by_device[dev] = p;
+    }
+    *ptr = by_device[dev];
+    return XY_OK;
+}
+
+}  // namespace
+
+extern "C" xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
+                                                const int32_t *context_lens, const int32_t *block_table,
+                                                int max_blocks, const void *k_pages, const void *v_pages,
+                                                int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                                int num_heads_kv, int head_dim, int block_size, float scale,
+                                                int causal, const xy_task *tasks, int num_tasks,
+                                                const xy_merge *merges, int num_merges, int num_ctas,
+                                                size_t workspace_bytes, int32_t *err_word, void *out,
+                                                void *stream) {
+    if (workspace_bytes > (size_t)XY_NOALLOC_SCRATCH_BYTES) return XY_ERR_WORKSPACE;
+    if (num_tasks == 0 && num_merges == 0) return XY_OK;
+    void *scratch = nullptr;
+    const xy_status st = noalloc_scratch(&scratch);
+    if (st != XY_OK) return st;
+    return xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages, num_pages,
+                              num_seqs, num_tokens, num_heads_q, num_heads_kv, head_dim, block_size, scale, causal,
+                              tasks, num_tasks, merges, num_merges, num_ctas, scratch, workspace_bytes, err_word,
+                              out, stream);
 }
