@@ -39,8 +39,9 @@ struct Cfg {
     static constexpr int kHalves = HD / 64;                     // 128-byte swizzle atoms per row
     static constexpr int kHalfBytes = kStageKeys * 128;         // one half of K or V in a stage
     static constexpr int kTensorBytes = kHalves * kHalfBytes;   // K or V of one stage
-    static constexpr int kStageBytes = 2 * kTensorBytes;
-    static constexpr int kStages = HD == 128 ? 5 : 8;
+    static constexpr int kQBytes = kMaxRows * HD * 2;           // the task's Q rows (first stage only)
+    static constexpr int kStageBytes = 2 * kTensorBytes + kQBytes;
+    static constexpr int kStages = HD == 128 ? 4 : 6;
     static constexpr int kThreads = (kMathWarps + 1) * 32;
     static constexpr int kSlotFloats = 16 * HD + 32;            // merge slot: O[16][HD], m[16], l[16]
     static constexpr int kStagesOff = 0;
@@ -48,6 +49,7 @@ struct Cfg {
     static constexpr int kBarOff = kSlotsOff + kMathWarps * kSlotFloats * 4;
     static constexpr int kFlagOff = kBarOff + 2 * kStages * 8;  // abort flag + 2 x 4 vote words
     static constexpr int kSmemBytes = kFlagOff + 64 + 1024;     // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
 struct AttnParams {
@@ -71,25 +73,46 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-template <int HD>
-__device__ __forceinline__ bool task_ok(const xy_task &t, const AttnParams &p) {
+// A task record plus the per-sequence numbers it needs; fetched one task ahead so that the
+// global-load latency overlaps the current task's stages.
+struct TaskInfo {
+    xy_task t;
+    int seq_start, qn, L;
+};
+
+__device__ __forceinline__ TaskInfo fetch_info(const xy_task &t, const AttnParams &p) {
+    TaskInfo f;
+    f.t = t;
+    f.seq_start = f.qn = f.L = 0;
+    if (t.seq >= 0 && t.seq < p.S) {
+        f.seq_start = __ldg(p.cu + t.seq);
+        f.qn = __ldg(p.cu + t.seq + 1) - f.seq_start;
+        f.L = __ldg(p.ctx + t.seq);
+    }
+    return f;
+}
+
+__device__ __forceinline__ bool info_ok(const TaskInfo &f, const AttnParams &p) {
+    const xy_task &t = f.t;
     if (t.seq < 0 || t.seq >= p.S || t.kv_head < 0 || t.kv_head >= p.Hkv) return false;
     if (t.q_rows < 1 || t.q_rows * p.G > kMaxRows || t.q_start < 0) return false;
     if (t.kv_start < 0 || t.kv_start >= t.kv_end || (t.kv_start % kStageKeys) != 0) return false;
-    const int qn = __ldg(p.cu + t.seq + 1) - __ldg(p.cu + t.seq);
-    const int L = __ldg(p.ctx + t.seq);
-    if (qn < 1 || qn > L || t.q_start + t.q_rows > qn || t.kv_end > L) return false;
+    if (f.qn < 1 || f.qn > f.L || t.q_start + t.q_rows > f.qn || t.kv_end > f.L) return false;
     if (t.num_splits > 1 && (t.ws_row < 0 || (int64_t)t.ws_row + (int64_t)t.q_rows * p.G > p.ws_rows))
         return false;
     return true;
 }
 
-// Byte offset of element (row, col) of a 64-row stage tensor laid out by TMA with 128-byte
-// swizzle: rows are 128 B per half, the 16-byte chunk index is XOR-ed with (row & 7).
+// Byte offset of element (key, col) of a stage tensor.  The stage holds 64 keys in boxes of BR =
+// 2^sh keys (one box per page, or per 64 keys of a larger page); a box is [half][BR][128 B] with
+// the TMA 128-byte swizzle, i.e. the 16-byte chunk index is XOR-ed with (key & 7), so eight
+// consecutive keys of one half hit eight different bank groups.
 template <int HD>
-__device__ __forceinline__ uint32_t swz(int row, int col) {
+__device__ __forceinline__ uint32_t swz(int key, int col, int sh) {
     const int half = col >> 6, chunk = (col & 63) >> 3;
-    return (uint32_t)(half * Cfg<HD>::kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 7) * 2);
+    const int r = key & ((1 << sh) - 1);
+    return (uint32_t)((key - r) * Cfg<HD>::kHalves * 128 + ((half * 128) << sh) + r * 128 +
+                      ((chunk ^ (key & 7)) << 4) + (col & 7) * 2);
 }
 
 template <int HD>
@@ -119,7 +142,8 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
     }
     __syncthreads();
 
-    const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;  // rows per TMA box
+    const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;  // keys per TMA box
+    const int br_sh = 31 - __clz(BR);
 
     if (warp == kMathWarps) {
         // ------------------------------ producer warp ------------------------------
@@ -127,51 +151,98 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
             xy::prefetch_tensormap(&kmap);
             xy::prefetch_tensormap(&vmap);
         }
+        // Block-table entries are read 32 logical pages at a time (one per lane) and the next
+        // window is loaded before it is needed, so no stage waits on a dependent global load.
+        auto load_win = [&](const int32_t *row, int base) -> int {
+            const int idx = base + lane;
+            return (idx >= 0 && idx < p.MB) ? __ldg(row + idx) : -1;
+        };
         int ctr = 0;
         bool ok = true;
-        for (int ti = blockIdx.x; ti < p.num_tasks && ok; ti += gridDim.x) {
-            const xy_task t = p.tasks[ti];
-            if (!task_ok<HD>(t, p)) {
+        int ti = blockIdx.x;
+        bool have = ti < p.num_tasks;
+        TaskInfo cur;
+        if (have) cur = fetch_info(p.tasks[ti], p);
+        int pref_win = -1;
+        bool pref_valid = false;
+        while (have && ok) {
+            const int tn = ti + gridDim.x;
+            const bool have_next = tn < p.num_tasks;
+            xy_task rec_next;
+            if (have_next) rec_next = p.tasks[tn];
+            TaskInfo nxt;
+            bool nxt_fetched = false;
+            if (!info_ok(cur, p)) {
                 if (lane == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
-                continue;
-            }
-            const int32_t *bt_row = p.bt + (int64_t)t.seq * p.MB;
-            for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
-                const int s = ctr % C::kStages;
-                if (ctr >= C::kStages &&
-                    !xy::mbar_wait(empty_bar + 8 * s, ((ctr / C::kStages) - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int nkeys = min(kStageKeys, t.kv_end - kv0);
-                const int nbox = (nkeys + BR - 1) / BR;
-                // lane b < nbox looks up the page of box b
-                int pg = 0;
-                if (lane < nbox) {
-                    const int key = kv0 + lane * BR;
-                    const int lb = key / p.bs;
-                    pg = lb < p.MB ? __ldg(bt_row + lb) : -1;
-                    if (pg < 0 || pg >= p.P) {
-                        xy::set_err(p.err, XY_DEV_PAGE_OOB);
-                        pg = 0;
+            } else {
+                const xy_task &t = cur.t;
+                const int32_t *bt_row = p.bt + (int64_t)t.seq * p.MB;
+                int win0 = t.kv_start / p.bs;
+                int pg_win = pref_valid ? pref_win : load_win(bt_row, win0);
+                int pg_nxt = load_win(bt_row, win0 + 32);
+                bool first_stage = true;
+                for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
+                    const int s = ctr % C::kStages;
+                    if (ctr >= C::kStages &&
+                        !xy::mbar_wait(empty_bar + 8 * s, ((ctr / C::kStages) - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    const int nkeys = min(kStageKeys, t.kv_end - kv0);
+                    const int nbox = (nkeys + BR - 1) / BR;
+                    if ((kv0 + nkeys - 1) / p.bs - win0 >= 32) {  // stage reaches into the next window
+                        win0 += 32;
+                        pg_win = pg_nxt;
+                        pg_nxt = load_win(bt_row, win0 + 32);
+                    }
+                    const int n_copies = nbox * 2;  // one box per (page, tensor), both column halves
+                    const int b = lane % nbox;
+                    int my_pg = __shfl_sync(0xffffffffu, pg_win, (kv0 + b * BR) / p.bs - win0);
+                    if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
+                        xy::set_err(p.err, XY_DEV_PAGE_OOB);
+                        my_pg = 0;
+                    }
+                    const uint32_t row_bytes = (uint32_t)p.G * HD * 2;  // one token's G query rows
+                    const uint32_t q_bytes = first_stage ? (uint32_t)t.q_rows * row_bytes : 0u;
+                    const uint32_t stage = stages + s * C::kStageBytes;
+                    if (lane == 0)
+                        xy::mbar_arrive_expect_tx(full_bar + 8 * s,
+                                                  (uint32_t)(n_copies * C::kHalves * BR * 128) + q_bytes);
+                    __syncwarp();
+                    if (lane < n_copies) {
+                        const int tensor = lane / nbox;
+                        const int key = kv0 + b * BR;
+                        const int y = (my_pg * p.Hkv + t.kv_head) * p.bs + (key % p.bs);
+                        const uint32_t dst = stage + tensor * C::kTensorBytes + b * C::kHalves * BR * 128;
+                        xy::tma_load_3d(dst, tensor ? &vmap : &kmap, 0, y, 0, full_bar + 8 * s);
+                    }
+                    if (first_stage) {
+                        // the task's query rows: token j's G heads are one contiguous run of q
+                        for (int j = lane; j < t.q_rows; j += 32) {
+                            const int64_t tok = (int64_t)cur.seq_start + t.q_start + j;
+                            const __nv_bfloat16 *src = p.q + (tok * p.Hq + (int64_t)t.kv_head * p.G) * HD;
+                            xy::bulk_load(stage + 2 * C::kTensorBytes + j * row_bytes, src, row_bytes,
+                                          full_bar + 8 * s);
+                        }
+                        first_stage = false;
+                        if (have_next) {  // the next record has arrived by now: prefetch its numbers
+                            nxt = fetch_info(rec_next, p);
+                            nxt_fetched = true;
+                            pref_valid = rec_next.seq >= 0 && rec_next.seq < p.S && rec_next.kv_start >= 0;
+                            if (pref_valid)
+                                pref_win = load_win(p.bt + (int64_t)rec_next.seq * p.MB, rec_next.kv_start / p.bs);
+                        }
+                    }
+                    __syncwarp();
                 }
-                const int n_copies = nbox * C::kHalves * 2;
-                const int b = lane % nbox;
-                const int my_pg = __shfl_sync(0xffffffffu, pg, b);
-                if (lane == 0) xy::mbar_arrive_expect_tx(full_bar + 8 * s, (uint32_t)(n_copies * BR * 128));
-                __syncwarp();
-                if (lane < n_copies) {
-                    const int rest = lane / nbox;
-                    const int half = rest % C::kHalves, tensor = rest / C::kHalves;
-                    const int key = kv0 + b * BR;
-                    const int y = (my_pg * p.Hkv + t.kv_head) * p.bs + (key % p.bs);
-                    const uint32_t dst = stages + s * C::kStageBytes + tensor * C::kTensorBytes +
-                                         half * C::kHalfBytes + b * BR * 128;
-                    xy::tma_load_2d(dst, tensor ? &vmap : &kmap, half * 64, y, full_bar + 8 * s);
-                }
-                __syncwarp();
             }
+            if (!nxt_fetched) {
+                pref_valid = false;
+                if (have_next) nxt = fetch_info(rec_next, p);
+            }
+            cur = nxt;
+            ti = tn;
+            have = have_next;
         }
         if (!ok) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
@@ -186,18 +257,34 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
     // ------------------------------ math warps ------------------------------
     const int g4 = lane >> 2, c4 = lane & 3;
     int ctr = 0, iter = 0;
-    for (int ti = blockIdx.x; ti < p.num_tasks; ti += gridDim.x) {
-        const xy_task t = p.tasks[ti];
-        if (!task_ok<HD>(t, p)) continue;
+    int ti = blockIdx.x;
+    bool have = ti < p.num_tasks;
+    TaskInfo cur;
+    if (have) cur = fetch_info(p.tasks[ti], p);
+    while (have) {
+        const int tn = ti + gridDim.x;
+        const bool have_next = tn < p.num_tasks;
+        xy_task rec_next;
+        if (have_next) rec_next = p.tasks[tn];
+        TaskInfo nxt;
+        bool nxt_fetched = false;
+        if (!info_ok(cur, p)) {
+            if (have_next) nxt = fetch_info(rec_next, p);
+            cur = nxt;
+            ti = tn;
+            have = have_next;
+            continue;
+        }
+        const xy_task t = cur.t;
         const int R = t.q_rows * p.G;
         int nrg = (R + 15) >> 4;
         if (nrg == 3) nrg = 4;
         const int wpg = kMathWarps / nrg;      // warps sharing one 16-row slice
         const int rg = warp % nrg, ks = warp / nrg;
         const int row_a = rg * 16 + g4, row_b = row_a + 8;
-        const int seq_start = __ldg(p.cu + t.seq);
-        const int qn = __ldg(p.cu + t.seq + 1) - seq_start;
-        const int L = __ldg(p.ctx + t.seq);
+        const int seq_start = cur.seq_start;
+        const int qn = cur.qn;
+        const int L = cur.L;
 
         auto row_limit = [&](int r) -> int {
             if (r >= R) return t.kv_end;    // padding rows: never stored, kept finite
@@ -209,25 +296,9 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, o));
 
-        // Q fragments (A operand, row-major 16 x HD), rows past R are zero.
+        // Q fragments (A operand, row-major 16 x HD) come from the first stage of the task, where
+        // the producer placed the task's rows in (token, head) order; rows past R are zero.
         uint32_t qa[HD / 16][4];
-        {
-            auto qrow = [&](int r) -> const uint32_t * {
-                if (r >= R) return nullptr;
-                const int64_t tok = seq_start + t.q_start + r / p.G;
-                const int h = t.kv_head * p.G + r % p.G;
-                return reinterpret_cast<const uint32_t *>(p.q + (tok * p.Hq + h) * HD);
-            };
-            const uint32_t *qa_ptr = qrow(row_a), *qb_ptr = qrow(row_b);
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) {
-                const int w0 = kk * 8 + c4, w1 = w0 + 4;  // 32-bit words: cols 16kk+2c and +8
-                qa[kk][0] = qa_ptr ? __ldg(qa_ptr + w0) : 0u;
-                qa[kk][1] = qb_ptr ? __ldg(qb_ptr + w0) : 0u;
-                qa[kk][2] = qa_ptr ? __ldg(qa_ptr + w1) : 0u;
-                qa[kk][3] = qb_ptr ? __ldg(qb_ptr + w1) : 0u;
-            }
-        }
 
         float o_acc[HD / 8][4];
 #pragma unroll
@@ -244,6 +315,24 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
             }
             const uint32_t kst = stages + s * C::kStageBytes;
             const uint32_t vst = kst + C::kTensorBytes;
+            if (kv0 == t.kv_start) {
+                const uint8_t *qs = gbase + C::kStagesOff + s * C::kStageBytes + 2 * C::kTensorBytes;
+                const uint32_t *qa_ptr = row_a < R ? reinterpret_cast<const uint32_t *>(qs + row_a * HD * 2) : nullptr;
+                const uint32_t *qb_ptr = row_b < R ? reinterpret_cast<const uint32_t *>(qs + row_b * HD * 2) : nullptr;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const int w0 = kk * 8 + c4, w1 = w0 + 4;  // 32-bit words: cols 16kk+2c and +8
+                    qa[kk][0] = qa_ptr ? qa_ptr[w0] : 0u;
+                    qa[kk][1] = qb_ptr ? qb_ptr[w0] : 0u;
+                    qa[kk][2] = qa_ptr ? qa_ptr[w1] : 0u;
+                    qa[kk][3] = qb_ptr ? qb_ptr[w1] : 0u;
+                }
+                if (have_next) {  // prefetch the next task's numbers while this one runs
+                    nxt = fetch_info(rec_next, p);
+                    nxt_fetched = true;
+                }
+            }
+
             const int k_lo = kv0 + ks * sub;
             const int k_hi = min(min(k_lo + sub, t.kv_end), lim_max);
             for (int kc = k_lo; kc < k_hi; kc += 16) {
@@ -255,7 +344,7 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < HD / 16; ++kk) {
                         uint32_t b0, b1, b2, b3;
-                        xy::ldsm_x4(kst + swz<HD>(krow, kk * 16 + ((mi & 1) << 3)), b0, b1, b2, b3);
+                        xy::ldsm_x4(kst + swz<HD>(krow, kk * 16 + ((mi & 1) << 3), br_sh), b0, b1, b2, b3);
                         xy::mma_bf16_16816(sc[0], qa[kk], b0, b1);
                         xy::mma_bf16_16816(sc[1], qa[kk], b2, b3);
                     }
@@ -319,7 +408,7 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
 #pragma unroll
                     for (int jd = 0; jd < HD / 16; ++jd) {
                         uint32_t b0, b1, b2, b3;
-                        xy::ldsm_x4_t(vst + swz<HD>(vrow, 8 * (2 * jd + (mi >> 1))), b0, b1, b2, b3);
+                        xy::ldsm_x4_t(vst + swz<HD>(vrow, 8 * (2 * jd + (mi >> 1)), br_sh), b0, b1, b2, b3);
                         if (tail) {
                             b0 &= keep0;
                             b1 &= keep1;
@@ -409,6 +498,10 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
             }
             xy::named_bar_sync(1, kMathWarps * 32);
         }
+        if (!nxt_fetched && have_next) nxt = fetch_info(rec_next, p);
+        cur = nxt;
+        ti = tn;
+        have = have_next;
         if (ks != 0) continue;
 
         // store: the final bf16 rows, or this chunk's normalised partial + log2-sum-exp
@@ -511,16 +604,19 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D map over a page pool viewed as [P * Hkv * bs rows, head_dim] bf16; box = 64 columns x
-// min(bs, 64) rows with 128-byte swizzle.
+// 3-D map over a page pool viewed as [P * Hkv * bs rows, head_dim] bf16, with the two 64-column
+// halves of a row as the outer dimension: dims (64 columns, rows, head_dim / 64 halves), strides
+// (head_dim * 2 bytes per row, 128 bytes per half).  A box of (64, box_rows, halves) lands in
+// shared memory as [half][box_rows][128 B] with the 128-byte swizzle.
 bool make_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_dim, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
-    cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1u, 1u};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides, box, estr,
+    const int halves = head_dim / 64;
+    cuuint64_t dims[3] = {64u, (cuuint64_t)rows, (cuuint64_t)halves};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, 128u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)halves};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
