@@ -242,10 +242,13 @@ def check_err_word(err_word):
         raise XYDeviceError(bits)
 
 
-def default_tiles(num_heads_q, num_heads_kv):
-    """Tile policy of the kernels: a query tile holds up to 64 (token, head) rows, so
-    q_tile = max(1, 64 // G) tokens; KV chunks of 4096 keys (a multiple of every page size)."""
+def default_tiles(num_heads_q, num_heads_kv, head_dim=128):
+    """Tile policy of the kernels.  With head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
+    128/G tokens (128 rows: the tcgen05 tile); otherwise up to 64 rows (q_tile = 64 // G).  KV
+    chunks are 4096 keys, a multiple of every page size and of both kernels' KV tiles."""
     G = num_heads_q // num_heads_kv
+    if head_dim == 128 and 128 % G == 0:
+        return 128 // G, 4096
     return max(1, 64 // G), 4096
 
 
@@ -258,7 +261,7 @@ class Plan:
         import torch
         dev = torch.device(device)
         self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)
-        dq, dk = default_tiles(num_heads_q, num_heads_kv)
+        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim)
         self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
         r = xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
                                 self.num_ctas, self.q_tile, self.kv_chunk)

@@ -17,8 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libxy.so")
 
-SOURCES = ["xy_host.cpp", "xy_append.cu", "xy_attention.cu"]
-HEADERS = ["xy_device.cuh"]
+SOURCES = ["xy_host.cpp", "xy_append.cu", "xy_attention.cu", "xy_tile.cu"]
+HEADERS = ["xy_device.cuh", "xy_attn_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -27,8 +27,14 @@
 
 #include "xy.h"
 #include "xy_device.cuh"
+#include "xy_attn_common.cuh"
 
 namespace {
+
+using xy::AttnParams;
+using xy::TaskInfo;
+using xy::ex2;
+using xy::fetch_info;
 
 constexpr int kStageKeys = 64;
 constexpr int kMathWarps = 4;
@@ -52,54 +58,16 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
-struct AttnParams {
-    const __nv_bfloat16 *q;
-    const int32_t *cu;
-    const int32_t *ctx;
-    const int32_t *bt;
-    const xy_task *tasks;
-    float *ws_o;
-    float *ws_lse;
-    int32_t *err;
-    __nv_bfloat16 *out;
-    int64_t ws_rows;
-    int MB, P, S, Hq, Hkv, G, bs, causal, num_tasks;
-    float scale_log2;
-};
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// A task record plus the per-sequence numbers it needs; fetched one task ahead so that the
-// global-load latency overlaps the current task's stages.
-struct TaskInfo {
-    xy_task t;
-    int seq_start, qn, L;
-};
-
-__device__ __forceinline__ TaskInfo fetch_info(const xy_task &t, const AttnParams &p) {
-    TaskInfo f;
-    f.t = t;
-    f.seq_start = f.qn = f.L = 0;
-    if (t.seq >= 0 && t.seq < p.S) {
-        f.seq_start = __ldg(p.cu + t.seq);
-        f.qn = __ldg(p.cu + t.seq + 1) - f.seq_start;
-        f.L = __ldg(p.ctx + t.seq);
-    }
-    return f;
+// Tasks of the CUDA-core/mma.sync path: the ones the tcgen05 tile kernel does not own.
+template <int HD>
+__device__ __forceinline__ bool mine(const TaskInfo &f, const AttnParams &p) {
+    return !xy::is_tile_task(f.t, p.G, HD);
 }
 
 __device__ __forceinline__ bool info_ok(const TaskInfo &f, const AttnParams &p) {
     const xy_task &t = f.t;
-    if (t.seq < 0 || t.seq >= p.S || t.kv_head < 0 || t.kv_head >= p.Hkv) return false;
-    if (t.q_rows < 1 || t.q_rows * p.G > kMaxRows || t.q_start < 0) return false;
-    if (t.kv_start < 0 || t.kv_start >= t.kv_end || (t.kv_start % kStageKeys) != 0) return false;
-    if (f.qn < 1 || f.qn > f.L || t.q_start + t.q_rows > f.qn || t.kv_end > f.L) return false;
-    if (t.num_splits > 1 && (t.ws_row < 0 || (int64_t)t.ws_row + (int64_t)t.q_rows * p.G > p.ws_rows))
-        return false;
+    if (!xy::task_common_ok(f, p)) return false;
+    if (t.q_rows * p.G > kMaxRows || (t.kv_start % kStageKeys) != 0) return false;
     return true;
 }
 
@@ -172,7 +140,9 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
             if (have_next) rec_next = p.tasks[tn];
             TaskInfo nxt;
             bool nxt_fetched = false;
-            if (!info_ok(cur, p)) {
+            if (!mine<HD>(cur, p)) {
+                // a tcgen05 tile task: the tile kernel runs it
+            } else if (!info_ok(cur, p)) {
                 if (lane == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
             } else {
                 const xy_task &t = cur.t;
@@ -268,7 +238,7 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
         if (have_next) rec_next = p.tasks[tn];
         TaskInfo nxt;
         bool nxt_fetched = false;
-        if (!info_ok(cur, p)) {
+        if (!mine<HD>(cur, p) || !info_ok(cur, p)) {
             if (have_next) nxt = fetch_info(rec_next, p);
             cur = nxt;
             ti = tn;
@@ -696,6 +666,7 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     p.MB = max_blocks;
     p.P = num_pages;
     p.S = num_seqs;
+    p.T = num_tokens;
     p.Hq = num_heads_q;
     p.Hkv = num_heads_kv;
     p.G = num_heads_q / num_heads_kv;
@@ -704,6 +675,12 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     p.num_tasks = num_tasks;
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Prefill/chunk tiles (more than 16 rows) run on the tcgen05 kernel first; a batch with one
+    // query token per sequence and G <= 16 has none.
+    if (num_tasks > 0 && head_dim == 128 && (128 % p.G) == 0 && (num_tokens > num_seqs || p.G > 16)) {
+        const xy_status ts = xy::launch_tile_attention(p, k_pages, v_pages, num_pages, block_size, num_ctas, st);
+        if (ts != XY_OK) return ts;
+    }
     return head_dim == 128 ? launch<128>(p, km, vm, num_ctas, merges, num_merges, st)
                            : launch<64>(p, km, vm, num_ctas, merges, num_merges, st);
 }

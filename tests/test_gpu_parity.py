@@ -36,9 +36,9 @@ def test_ragged_batch_every_row(d, bs, causal):
     assert_parity(run(wl))
 
 
-@pytest.mark.parametrize("kv_chunk", [64, 128, 192])
+@pytest.mark.parametrize("kv_chunk", [128, 256, 384])
 def test_split_kv_and_combine_every_row(kv_chunk):
-    wl = workloads.custom([3, 1, 50, 1], [300, 257, 190, 64], 8, 2, 128, 16, seed=kv_chunk)
+    wl = workloads.custom([3, 1, 50, 1], [700, 520, 190, 64], 8, 2, 128, 16, seed=kv_chunk)
     r = run(wl, kv_chunk=kv_chunk)
     assert len(r["batch"].plan.host["merges"]) > 0
     assert_parity(r)
@@ -57,7 +57,7 @@ def test_nan_in_unused_slots_never_reaches_outputs():
     r = run(wl, pool_fill=float("nan"))
     assert_parity(r, check_pages=False)
     wl = workloads.custom([5, 37, 64, 70], [5, 37, 64, 70], 4, 2, 128, 16, seed=3)
-    r = run(wl, pool_fill=float("nan"), kv_chunk=64)
+    r = run(wl, pool_fill=float("nan"), kv_chunk=128)
     assert_parity(r, check_pages=False)
 
 
@@ -80,7 +80,7 @@ def test_full_size_prefill_sampled():
     wl = workloads.prefill()
     rng = np.random.default_rng(1)
     seqs = sorted({int(np.argmax(wl.q_lens)), int(np.argmin(wl.q_lens)), int(rng.integers(wl.num_seqs))})
-    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=64 // wl.group), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=128 // wl.group), sample_seqs=seqs)
     assert_parity(r)
 
 
@@ -88,7 +88,7 @@ def test_full_size_mixed_sampled():
     wl = workloads.mixed()
     rng = np.random.default_rng(2)
     seqs = [0, 5, 8, 60, 127, int(np.argmax(wl.context_lens))]
-    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=64 // wl.group), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=128 // wl.group), sample_seqs=seqs)
     assert_parity(r)
 
 

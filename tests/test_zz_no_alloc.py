@@ -39,7 +39,7 @@ def _prepared(xy, kv_chunk):
 
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls(xy):
-    wl, vals, batch = _prepared(xy, kv_chunk=64)
+    wl, vals, batch = _prepared(xy, kv_chunk=128)
     pl = batch.plan
     assert pl.merges.shape[0] > 0 and 0 < pl.host["workspace_bytes"] <= xy.XY_NOALLOC_SCRATCH_BYTES
     ref = torch.empty_like(vals["q"])
@@ -62,7 +62,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(xy):
 
 
 def test_noalloc_rejects_batches_beyond_its_scratch(xy):
-    wl, vals, batch = _prepared(xy, kv_chunk=64)
+    wl, vals, batch = _prepared(xy, kv_chunk=128)
     pl = batch.plan
     out = torch.empty_like(vals["q"])
     with pytest.raises(xy.XYError) as e:
