@@ -358,21 +358,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 xy::tc_fence_after();
                 if (j == 0) tc.prefetch_next(p);
                 const int kt0 = t.kv_start + j * kTileKeys;
-                float sv[128];
+                uint32_t sr[128];
+                xy::tmem_ld128(tbase + lane_off + b * 128, sr);
+                // masked row max (keys at or past this row's limit are -inf), eight independent chains
+                float mx8[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    xy::tmem_ld32(tbase + lane_off + b * 128 + c * 32, r);
+                for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+                if (kt0 + kTileKeys <= lim) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) sv[c * 32 + i] = __uint_as_float(r[i]);
+                    for (int i = 0; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) {
+                        if (kt0 + i >= lim) sr[i] = __float_as_uint(-INFINITY);
+                        mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+                    }
                 }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 128; ++i) {
-                    sv[i] = (kt0 + i < lim) ? sv[i] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[i]);
-                }
-                const float m_new = fmaxf(m, mx);
+                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
                 if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
                     const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
                     m = m_new;
@@ -383,29 +387,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         xy::tc_fence_after();
+#pragma unroll 1
+                        for (int h = 0; h < 4; ++h) {
+                            uint32_t orow[32];
+                            xy::tmem_ld32(tbase + lane_off + kTmemO + h * 32, orow);
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            uint32_t r[32];
-                            xy::tmem_ld32(tbase + lane_off + kTmemO + c * 32, r);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                            xy::tmem_st32(tbase + lane_off + kTmemO + c * 32, r);
+                            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                            xy::tmem_st32(tbase + lane_off + kTmemO + h * 32, orow);
                         }
                     }
                 }
-                const float mu = m == -INFINITY ? 0.f : m;
-                float ls = 0.f;
+                // p = 2^(s * scale_log2 - m), packed to bf16 pairs, written over the S columns
+                const float neg_mu = m == -INFINITY ? 0.f : -m;
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int h = 0; h < 2; ++h) {
                     uint32_t pk[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2(sv[c * 64 + 2 * i] - mu), p1 = ex2(sv[c * 64 + 2 * i + 1] - mu);
-                        ls += p0 + p1;
+                        const float p0 = ex2(fmaf(__uint_as_float(sr[64 * h + 2 * i]), p.scale_log2, neg_mu));
+                        const float p1 = ex2(fmaf(__uint_as_float(sr[64 * h + 2 * i + 1]), p.scale_log2, neg_mu));
+                        ls4[i & 3] += p0 + p1;
                         pk[i] = xy::pack_bf16x2(p0, p1);
                     }
-                    xy::tmem_st32(tbase + lane_off + b * 128 + c * 32, pk);
+                    xy::tmem_st32(tbase + lane_off + b * 128 + 32 * h, pk);
                 }
+                const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                 l += ls;
                 if (kt0 + kTileKeys > t.kv_end) {
                     // keys at or past kv_end: unused page slots or stale stage data; their P is 0 and
