@@ -93,6 +93,10 @@ typedef struct {
 /* Static description of a status code ("ok", "invalid argument", ...). Never NULL. */
 const char *xy_status_string(int status);
 
+/* Text of the CUDA error behind the last XY_ERR_CUDA returned on the calling host thread (or ""
+ * if none).  The pointer stays valid until the next libxy call on that thread. */
+const char *xy_last_error_string(void);
+
 /* Library ABI version (major * 100 + minor). */
 int xy_version(void);
 

@@ -20,7 +20,7 @@ XY_DEV_SLOT_OOB = 0x2
 XY_DEV_BAD_TASK = 0x4
 XY_DEV_TIMEOUT = 0x8
 
-C_ABI = ("xy_status_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
+C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
          "xy_paged_attention_noalloc")
 
@@ -31,7 +31,10 @@ XY_NOALLOC_SCRATCH_BYTES = 32 << 20
 class XYError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} (status {status})")
+        detail = ""
+        if status == -7:  # XY_ERR_CUDA: add the CUDA error text the library recorded
+            detail = " [" + lib().xy_last_error_string().decode(errors="replace") + "]"
+        super().__init__(f"{where}: {status_string(status)} (status {status}){detail}")
 
 
 class XYDeviceError(RuntimeError):
@@ -63,6 +66,8 @@ def lib():
     SZ = ctypes.c_size_t
     L.xy_status_string.argtypes = [I]
     L.xy_status_string.restype = ctypes.c_char_p
+    L.xy_last_error_string.argtypes = []
+    L.xy_last_error_string.restype = ctypes.c_char_p
     L.xy_version.argtypes = []
     L.xy_version.restype = I
     L.xy_default_num_ctas.argtypes = [I]

@@ -608,7 +608,8 @@ xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &
     }
     if (p.num_tasks > 0) {
         paged_attention_kernel<HD><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
-        if (cudaGetLastError() != cudaSuccess) return XY_ERR_CUDA;
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel launch");
     }
     if (num_merges > 0) {
         combine_kernel<HD><<<num_merges, 128, 0, st>>>(merges, p.ws_o, p.ws_lse, p.cu, p.Hq, p.G, p.ws_rows, p.err,
@@ -619,6 +620,14 @@ xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &
 }
 
 }  // namespace
+
+namespace xy {
+void set_last_error(const char *what, const char *msg);
+xy_status cuda_fail(cudaError_t e, const char *what) {
+    set_last_error(what, cudaGetErrorString(e));
+    return XY_ERR_CUDA;
+}
+}  // namespace xy
 
 extern "C" int xy_default_num_ctas(int device) {
     int sms = 0;

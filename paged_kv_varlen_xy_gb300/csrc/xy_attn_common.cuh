@@ -69,6 +69,9 @@ __host__ __device__ __forceinline__ bool is_tile_task(const xy_task &t, int G, i
     return head_dim == 128 && (128 % G) == 0 && t.q_rows * G > 16;
 }
 
+// Records a CUDA error for xy_last_error_string() and returns XY_ERR_CUDA.
+xy_status cuda_fail(cudaError_t e, const char *what);
+
 // Launches the tcgen05 tile kernel over the tasks it owns (defined in xy_tile.cu).
 xy_status launch_tile_attention(const AttnParams &p, const void *k_pages, const void *v_pages, int num_pages,
                                 int block_size, int num_ctas, cudaStream_t st);

@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <limits>
 #include <vector>
@@ -30,6 +31,16 @@ extern "C" const char *xy_status_string(int status) {
 }
 
 extern "C" int xy_version(void) { return 100; }
+
+// Last CUDA failure seen on this host thread (written by the device-call entry points).
+namespace xy {
+thread_local char g_last_error[256] = "";
+void set_last_error(const char *what, const char *msg) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, msg);
+}
+}  // namespace xy
+
+extern "C" const char *xy_last_error_string(void) { return xy::g_last_error; }
 
 static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 

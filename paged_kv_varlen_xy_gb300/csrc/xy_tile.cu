@@ -5,18 +5,22 @@
 // GEMM-softmax-GEMM over a task's (query block x KV block) tiles; §2.3 technique 1: ragged tiles
 // are masked on chip and only valid rows are stored.
 //
-// One persistent CTA per SM, six warps:
-//   warp 4      producer: TMA loads of the task's 128 query rows (G heads x 128/G tokens, one 3-D
-//               box per 64-column half) and of 128-key K/V tiles gathered page by page through
-//               the block table (2-D boxes, 128-byte swizzle) into a 3-stage ring;
-//   warp 5      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM buffers, then
-//               O += P_{j-1} V_{j-1} with P read from TMEM (it overwrites the first 64 columns of
-//               its S buffer as packed bf16);
-//   warps 0..3  softmax, one query row per thread (TMEM lane = row): masked row max, exp2,
-//               row sum, P back to TMEM; O is rescaled in TMEM only when a row's running max grows
-//               by more than 2^8 (the stale max is otherwise kept, which is exact because O and
-//               the row sum share it); epilogue O / l straight from TMEM to global memory.
-// TMEM: S0 = columns [0,128), S1 = [128,256), O = [256,384) of a 512-column allocation.
+// One persistent CTA per SM, eighteen warps:
+//   warp 16     producer: TMA loads of the task's 128 query rows (G heads x 128/G tokens, one 3-D
+//               box per 64-column half) into one of two Q buffers, and of 128-key K and V tiles,
+//               gathered page by page through the block table (2-D boxes, 128-byte swizzle), into
+//               a 4-slot ring (K_j and V_j take separate slots, so K runs ahead of V);
+//   warp 17     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM buffers, then
+//               O += P_{j-1} V_{j-1} with P read from TMEM (packed bf16, two buffers of its own,
+//               so the next S never waits for a PV);
+//   warps 0..15 softmax, four threads per query row (TMEM lane = row; warps 4q..4q+3 take key
+//               columns 32q..32q+31), the row max exchanged through shared memory:
+//               masked max, exp2, row sum, P back to TMEM.  O is rescaled in TMEM only when a row's
+//               running max grows by more than 2^8 (otherwise the stale max is kept, which is exact
+//               because O and the row sum share it).  Epilogue: O / l from TMEM to global memory.
+// TMEM: S0 = columns [0,128), S1 = [128,256), P0 = [256,320), P1 = [320,384), O = [384,512).
+// The softmax warps release an S buffer as soon as they have loaded it, so S_{j+2} overlaps the
+// softmax and PV of tile j.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,34 +42,44 @@ using xy::TaskInfo;
 
 constexpr int HD = 128;
 constexpr int kTileKeys = 128;
-constexpr int kStages = 3;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kSlots = 4;                       // K/V ring slots (one K or V tile each)
+constexpr int kSoftmaxWarps = 16;               // kQ threads per query row
+constexpr int kQ = kSoftmaxWarps / 4;
+constexpr int kCols = 128 / kQ;                 // S / O columns per softmax thread
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
+constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
+static_assert(kCols == 32, "the softmax code moves 32 TMEM columns per thread");
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 columns
 constexpr int kTileBytes = 2 * kHalfBytes;      // Q, K or V tile: [half][128 rows][128 B]
-constexpr int kQOff = 0;
-constexpr int kStageOff = kTileBytes;
-constexpr int kStageBytes = 2 * kTileBytes;     // K then V
+constexpr int kQOff = 0;                        // Q0, Q1
+constexpr int kSlotOff = 2 * kTileBytes;
 enum {
-    B_QFULL = 0,
-    B_QEMPTY,
-    B_KVFULL0,
-    B_KVEMPTY0 = B_KVFULL0 + kStages,
-    B_SFULL0 = B_KVEMPTY0 + kStages,
+    B_QFULL0 = 0,
+    B_QEMPTY0 = B_QFULL0 + 2,
+    B_FULL0 = B_QEMPTY0 + 2,
+    B_EMPTY0 = B_FULL0 + kSlots,
+    B_SFULL0 = B_EMPTY0 + kSlots,
     B_SFREE0 = B_SFULL0 + 2,
     B_PFULL0 = B_SFREE0 + 2,
-    B_OBAR = B_PFULL0 + 2,
+    B_PFREE0 = B_PFULL0 + 2,
+    B_OFREE = B_PFREE0 + 2,
+    B_OBAR,
     B_DONE,
     B_COUNT
 };
-constexpr int kBarOff = kStageOff + kStages * kStageBytes;
-constexpr int kMiscOff = kBarOff + B_COUNT * 8;  // TMEM base address, abort flag
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
+constexpr int kMiscOff = kBarOff + B_COUNT * 8;     // TMEM base address, abort flag
+constexpr int kVoteOff = kMiscOff + 16;              // one vote per softmax warp
+constexpr int kRedOff = kVoteOff + 4 * kSoftmaxWarps; // row-max exchange [2 parity][kQ][128]
+constexpr int kSumOff = kRedOff + 2 * kQ * 128 * 4;  // row-sum exchange [kQ][128]
+constexpr int kSmemBytes = kSumOff + kQ * 128 * 4 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 256;
+constexpr uint32_t kTmemO = 384;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kSoftmaxBar = 1;        // named barrier id of the softmax warps
 
 __device__ __forceinline__ bool mine(const TaskInfo &f, const AttnParams &p) {
     return xy::is_tile_task(f.t, p.G, HD);
@@ -120,19 +134,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return base + kBarOff + 8 * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff + 4);
+    volatile int *vote = reinterpret_cast<volatile int *>(gbase + kVoteOff);
+    float *red = reinterpret_cast<float *>(gbase + kRedOff);
+    float *sums = reinterpret_cast<float *>(gbase + kSumOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        xy::mbar_init(bar(B_QFULL), 1);
-        xy::mbar_init(bar(B_QEMPTY), 1);
-        for (int s = 0; s < kStages; ++s) {
-            xy::mbar_init(bar(B_KVFULL0 + s), 1);
-            xy::mbar_init(bar(B_KVEMPTY0 + s), 1);
+        for (int i = 0; i < 2; ++i) {
+            xy::mbar_init(bar(B_QFULL0 + i), 1);
+            xy::mbar_init(bar(B_QEMPTY0 + i), 1);
+            xy::mbar_init(bar(B_SFULL0 + i), 1);
+            xy::mbar_init(bar(B_SFREE0 + i), kSoftmaxWarps);
+            xy::mbar_init(bar(B_PFULL0 + i), kSoftmaxWarps);
+            xy::mbar_init(bar(B_PFREE0 + i), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            xy::mbar_init(bar(B_SFULL0 + b), 1);
-            xy::mbar_init(bar(B_SFREE0 + b), 1);
-            xy::mbar_init(bar(B_PFULL0 + b), 4);  // one arrival per softmax warp
+        xy::mbar_init(bar(B_OFREE), kSoftmaxWarps);
+        for (int s = 0; s < kSlots; ++s) {
+            xy::mbar_init(bar(B_FULL0 + s), 1);
+            xy::mbar_init(bar(B_EMPTY0 + s), 1);
         }
         xy::mbar_init(bar(B_OBAR), 1);
         xy::mbar_init(bar(B_DONE), 1);
@@ -160,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int idx = b0 + lane;
             return (idx >= 0 && idx < p.MB) ? __ldg(row + idx) : -1;
         };
-        int ctr = 0, qk = 0;
+        int c = 0, qk = 0;
         bool ok = true;
         int pref_win = -1;
         bool pref_valid = false;
@@ -180,15 +199,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const TaskInfo f = tc.cur;
             const xy_task &t = f.t;
-            if (qk > 0 && !warp_all(xy::mbar_wait(bar(B_QEMPTY), (qk - 1) & 1, abort_flag))) {
+            const int qb = qk & 1;
+            if (qk >= 2 && !warp_all(xy::mbar_wait(bar(B_QEMPTY0 + qb), ((qk >> 1) - 1) & 1, abort_flag))) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                xy::mbar_arrive_expect_tx(bar(B_QFULL), kTileBytes);
+                xy::mbar_arrive_expect_tx(bar(B_QFULL0 + qb), kTileBytes);
                 const int y = t.kv_head * p.G, z = f.seq_start + t.q_start;
-                xy::tma_load_3d(base + kQOff, &qmap, 0, y, z, bar(B_QFULL));
-                xy::tma_load_3d(base + kQOff + kHalfBytes, &qmap, 64, y, z, bar(B_QFULL));
+                const uint32_t qdst = base + kQOff + qb * kTileBytes;
+                xy::tma_load_3d(qdst, &qmap, 0, y, z, bar(B_QFULL0 + qb));
+                xy::tma_load_3d(qdst + kHalfBytes, &qmap, 64, y, z, bar(B_QFULL0 + qb));
             }
             ++qk;
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.MB;
@@ -197,13 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pg_nxt = load_win(bt_row, win0 + 32);
             pref_valid = false;
             bool first = true;
-            for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kTileKeys, ++ctr) {
-                const int s = ctr % kStages;
-                if (ctr >= kStages &&
-                    !warp_all(xy::mbar_wait(bar(B_KVEMPTY0 + s), ((ctr / kStages) - 1) & 1, abort_flag))) {
-                    ok = false;
-                    break;
-                }
+            for (int kv0 = t.kv_start; kv0 < t.kv_end && ok; kv0 += kTileKeys) {
                 const int nkeys = min(kTileKeys, t.kv_end - kv0);
                 const int nbox = (nkeys + BRt - 1) / BRt;
                 if ((kv0 + nkeys - 1) / p.bs - win0 >= 32) {
@@ -211,25 +226,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pg_win = pg_nxt;
                     pg_nxt = load_win(bt_row, win0 + 32);
                 }
-                const int n_copies = nbox * 4;  // (page box) x (2 halves) x (K, V)
                 const int b = lane % nbox;
                 int my_pg = __shfl_sync(0xffffffffu, pg_win, (kv0 + b * BRt) / p.bs - win0);
+                const int n_copies = nbox * 2;  // (page box) x (2 halves), per tensor
                 if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
                     xy::set_err(p.err, XY_DEV_PAGE_OOB);
                     my_pg = 0;
                 }
-                if (lane == 0) xy::mbar_arrive_expect_tx(bar(B_KVFULL0 + s), (uint32_t)(n_copies * BRt * 128));
-                __syncwarp();
-                if (lane < n_copies) {
-                    const int rest = lane / nbox;
-                    const int half = rest & 1, tensor = rest >> 1;
-                    const int key = kv0 + b * BRt;
-                    const int y = (my_pg * p.Hkv + t.kv_head) * p.bs + (key % p.bs);
-                    const uint32_t dst =
-                        base + kStageOff + s * kStageBytes + tensor * kTileBytes + half * kHalfBytes + b * BRt * 128;
-                    xy::tma_load_2d(dst, tensor ? &vmap : &kmap, half * 64, y, bar(B_KVFULL0 + s));
+                const int y = (my_pg * p.Hkv + t.kv_head) * p.bs + ((kv0 + b * BRt) % p.bs);
+                const int half = lane / nbox;
+#pragma unroll
+                for (int tensor = 0; tensor < 2; ++tensor, ++c) {
+                    const int s = c % kSlots;
+                    if (c >= kSlots &&
+                        !warp_all(xy::mbar_wait(bar(B_EMPTY0 + s), ((c / kSlots) - 1) & 1, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) xy::mbar_arrive_expect_tx(bar(B_FULL0 + s), (uint32_t)(n_copies * BRt * 128));
+                    __syncwarp();
+                    if (lane < n_copies) {
+                        const uint32_t dst = base + kSlotOff + s * kTileBytes + half * kHalfBytes + b * BRt * 128;
+                        xy::tma_load_2d(dst, tensor ? &vmap : &kmap, half * 64, y, bar(B_FULL0 + s));
+                    }
+                    __syncwarp();
                 }
-                __syncwarp();
                 if (first) {
                     first = false;
                     tc.prefetch_next(p);
@@ -247,28 +268,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
         }
         // every issued copy must land before the CTA may exit
-        for (int k = ctr - 1; k >= 0 && k >= ctr - kStages; --k)
-            xy::mbar_wait(bar(B_KVFULL0 + k % kStages), (k / kStages) & 1);
-        if (qk > 0) xy::mbar_wait(bar(B_QFULL), (qk - 1) & 1);
+        for (int k = c - 1; k >= 0 && k >= c - kSlots; --k)
+            xy::mbar_wait(bar(B_FULL0 + k % kSlots), (k / kSlots) & 1);
+        for (int k = qk - 1; k >= 0 && k >= qk - 2; --k) xy::mbar_wait(bar(B_QFULL0 + (k & 1)), (k >> 1) & 1);
     } else if (warp == kMmaWarp) {
         // ---------------------------------- MMA issuer ----------------------------------
         if (lane == 0) {
             const uint32_t id_s = xy::idesc_bf16(128, 128, 0, 0);   // Q (K-major) x K tile (K-major)
             const uint32_t id_o = xy::idesc_bf16(128, 128, 0, 1);   // P (TMEM) x V tile (MN-major)
-            int ctr = 0, g = 0, qk = 0;
+            int c = 0, g = 0, qk = 0;
             bool ok = true, issued = false;
-            auto issue_pv = [&](int jj) -> bool {
+            // Descriptors are built once; a k-step or a buffer only adds a constant to the 14-bit
+            // address field (addresses stay below 256 KB), so the issue loop is a few adds per MMA
+            // and the single issuing thread keeps up with the tensor core.
+            const uint64_t q_desc0 = xy::smem_desc_sw128(base + kQOff, 16, 1024);
+            const uint64_t k_desc0 = xy::smem_desc_sw128(base + kSlotOff, 16, 1024);
+            const uint64_t v_desc0 = xy::smem_desc_sw128(base + kSlotOff, kHalfBytes, 1024);
+            constexpr uint32_t kTileDesc = kTileBytes >> 4;  // one Q buffer or ring slot
+            auto issue_pv = [&](int jj, uint32_t o_addr) -> bool {
                 const int gb = g + jj, b = gb & 1;
+                if (jj == 0 && qk >= 1 && !xy::mbar_wait(bar(B_OFREE), (qk - 1) & 1, abort_flag))
+                    return false;  // the previous task's epilogue has read O
                 if (!xy::mbar_wait(bar(B_PFULL0 + b), (gb >> 1) & 1, abort_flag)) return false;
+                const int cv = c + 2 * jj + 1, s = cv % kSlots;
+                if (!xy::mbar_wait(bar(B_FULL0 + s), (cv / kSlots) & 1, abort_flag)) return false;
                 xy::tc_fence_after();
-                const int s = (ctr + jj) % kStages;
-                const uint32_t vst = base + kStageOff + s * kStageBytes + kTileBytes;
+                const uint64_t vd = v_desc0 + (uint64_t)(s * kTileDesc);
+                const uint32_t pa = tbase + kTmemP + b * 64;
+                xy::umma_ts(o_addr, pa, vd, id_o, jj > 0 ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    xy::umma_ts(tbase + kTmemO, tbase + b * 128 + k * 8, xy::smem_desc_sw128(vst + k * 2048, kHalfBytes, 1024),
-                                id_o, (jj > 0 || k > 0) ? 1u : 0u);
-                xy::umma_commit(bar(B_KVEMPTY0 + s));
-                xy::umma_commit(bar(B_SFREE0 + b));
+                for (int k = 1; k < 8; ++k) xy::umma_ts(o_addr, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), id_o, 1u);
+                xy::umma_commit(bar(B_EMPTY0 + s));
+                xy::umma_commit(bar(B_PFREE0 + b));
                 xy::umma_commit(bar(B_OBAR));
                 return true;
             };
@@ -282,15 +313,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const xy_task t = tc.cur.t;
                 const int n = (t.kv_end - t.kv_start + kTileKeys - 1) / kTileKeys;
-                if (!xy::mbar_wait(bar(B_QFULL), qk & 1, abort_flag)) {
+                const int qb = qk & 1;
+                const uint32_t o_addr = tbase + kTmemO;
+                if (!xy::mbar_wait(bar(B_QFULL0 + qb), (qk >> 1) & 1, abort_flag)) {
                     ok = false;
                     break;
                 }
                 xy::tc_fence_after();
                 tc.prefetch_next(p);
                 for (int j = 0; j < n && ok; ++j) {
-                    const int s = (ctr + j) % kStages;
-                    if (!xy::mbar_wait(bar(B_KVFULL0 + s), ((ctr + j) / kStages) & 1, abort_flag)) {
+                    const int ck = c + 2 * j, s = ck % kSlots;
+                    if (!xy::mbar_wait(bar(B_FULL0 + s), (ck / kSlots) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
@@ -301,20 +334,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     xy::tc_fence_after();
                     issued = true;
-                    const uint32_t kst = base + kStageOff + s * kStageBytes;
+                    const uint64_t qd = q_desc0 + (uint64_t)(qb * kTileDesc);
+                    const uint64_t kd = k_desc0 + (uint64_t)(s * kTileDesc);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const uint32_t koff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                        xy::umma_ss(tbase + b * 128, xy::smem_desc_sw128(base + kQOff + koff, 16, 1024),
-                                    xy::smem_desc_sw128(kst + koff, 16, 1024), id_s, k > 0 ? 1u : 0u);
+                        const uint64_t koff = (uint64_t)(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+                        xy::umma_ss(tbase + b * 128, qd + koff, kd + koff, id_s, k > 0 ? 1u : 0u);
                     }
+                    xy::umma_commit(bar(B_EMPTY0 + s));
                     xy::umma_commit(bar(B_SFULL0 + b));
-                    if (j >= 1) ok = issue_pv(j - 1);
+                    if (j == n - 1) xy::umma_commit(bar(B_QEMPTY0 + qb));
+                    if (j >= 1) ok = issue_pv(j - 1, o_addr);
                 }
-                if (ok) ok = issue_pv(n - 1);
-                xy::umma_commit(bar(B_QEMPTY));
+                if (ok) ok = issue_pv(n - 1, o_addr);
                 g += n;
-                ctr += n;
+                c += 2 * n;
                 ++qk;
                 tc.advance(p);
             }
@@ -328,15 +362,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
+    } else {
         // ---------------------------------- softmax ----------------------------------
-        const int row = warp * 32 + lane;
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-        int ctr = 0, g = 0;
+        const int q4 = warp >> 2;                   // key columns [kCols*q4, kCols*q4 + kCols)
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const int col0 = kCols * q4;
+        int c = 0, g = 0, qk = 0;
         bool ok = true;
         TaskCursor tc;
         tc.begin(p);
-        while (tc.have && ok) {
+        while (tc.have) {
             tc.load_next_record(p);
             if (!mine(tc.cur, p) || !tile_ok(tc.cur, p)) {
                 tc.advance(p);
@@ -348,84 +384,84 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = (t.kv_end - t.kv_start + kTileKeys - 1) / kTileKeys;
             const bool valid = row < R;
             const int lim = valid ? min(t.kv_end, p.causal ? f.L - f.qn + t.q_start + row / p.G + 1 : f.L) : t.kv_end;
+            const uint32_t o_addr = tbase + lane_off + kTmemO + col0;
             float m = -INFINITY, l = 0.f;
             for (int j = 0; j < n; ++j) {
                 const int gb = g + j, b = gb & 1;
-                if (!warp_all(xy::mbar_wait(bar(B_SFULL0 + b), (gb >> 1) & 1, abort_flag))) {
-                    ok = false;
-                    break;
-                }
+                // a failed wait (timeout or abort) is recorded, not acted on: every softmax warp
+                // keeps executing the same named barriers and the decision to stop is voted below
+                ok = warp_all(xy::mbar_wait(bar(B_SFULL0 + b), (gb >> 1) & 1, abort_flag)) && ok;
                 xy::tc_fence_after();
                 if (j == 0) tc.prefetch_next(p);
-                const int kt0 = t.kv_start + j * kTileKeys;
-                uint32_t sr[128];
-                xy::tmem_ld128(tbase + lane_off + b * 128, sr);
-                // masked row max (keys at or past this row's limit are -inf), eight independent chains
-                float mx8[8];
+                const int kt0 = t.kv_start + j * kTileKeys + col0;
+                uint32_t sr[kCols];
+                xy::tmem_ld32(tbase + lane_off + b * 128 + col0, sr);
+                xy::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) xy::mbar_arrive(bar(B_SFREE0 + b));  // S_b may be overwritten now
+                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (kt0 + kCols <= lim) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
-                if (kt0 + kTileKeys <= lim) {
-#pragma unroll
-                    for (int i = 0; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+                    for (int i = 0; i < kCols; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 128; ++i) {
+                    for (int i = 0; i < kCols; ++i) {
                         if (kt0 + i >= lim) sr[i] = __float_as_uint(-INFINITY);
-                        mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+                        mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
                     }
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                       fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                // exchange the partial row maxima of the kQ threads of a row
+                float *rd = red + (gb & 1) * (kQ * 128);
+                rd[q4 * 128 + row] = mx;
+                xy::named_bar_sync(kSoftmaxBar, kSoftmaxWarps * 32);
+#pragma unroll
+                for (int o = 1; o < kQ; ++o) mx = fmaxf(mx, rd[((q4 + o) % kQ) * 128 + row]);
                 const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
                 if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
                     const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
                     m = m_new;
                     l *= alpha;
-                    if (j > 0) {  // O has PV_0..PV_{j-1}; rescale it once the last of them is done
-                        if (!warp_all(xy::mbar_wait(bar(B_OBAR), (g + j - 1) & 1, abort_flag))) {
-                            ok = false;
-                            break;
-                        }
+                    if (j > 0) {  // O has PV_0..PV_{j-1}; rescale these columns once the last one is done
+                        ok = warp_all(xy::mbar_wait(bar(B_OBAR), (gb - 1) & 1, abort_flag)) && ok;
                         xy::tc_fence_after();
-#pragma unroll 1
-                        for (int h = 0; h < 4; ++h) {
-                            uint32_t orow[32];
-                            xy::tmem_ld32(tbase + lane_off + kTmemO + h * 32, orow);
+                        uint32_t orow[kCols];
+                        xy::tmem_ld32(o_addr, orow);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                            xy::tmem_st32(tbase + lane_off + kTmemO + h * 32, orow);
-                        }
+                        for (int i = 0; i < kCols; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                        xy::tmem_st32(o_addr, orow);
                     }
                 }
-                // p = 2^(s * scale_log2 - m), packed to bf16 pairs, written over the S columns
+                // p = 2^(s * scale_log2 - m), packed to bf16 pairs, into this thread's P columns
                 const float neg_mu = m == -INFINITY ? 0.f : -m;
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[kCols / 2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sr[64 * h + 2 * i]), p.scale_log2, neg_mu));
-                        const float p1 = ex2(fmaf(__uint_as_float(sr[64 * h + 2 * i + 1]), p.scale_log2, neg_mu));
-                        ls4[i & 3] += p0 + p1;
-                        pk[i] = xy::pack_bf16x2(p0, p1);
-                    }
-                    xy::tmem_st32(tbase + lane_off + b * 128 + 32 * h, pk);
+                for (int i = 0; i < kCols / 2; ++i) {
+                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, neg_mu));
+                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, neg_mu));
+                    ls4[i & 3] += p0 + p1;
+                    pk[i] = xy::pack_bf16x2(p0, p1);
                 }
-                const float ls = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-                l += ls;
-                if (kt0 + kTileKeys > t.kv_end) {
-                    // keys at or past kv_end: unused page slots or stale stage data; their P is 0 and
-                    // their V rows are zeroed so that 0 * NaN cannot reach O
-                    if (kt0 + row >= t.kv_end) {
-                        const int s = (ctr + j) % kStages;
-                        uint8_t *vrow = gbase + kStageOff + s * kStageBytes + kTileBytes + row * 128;
+                if (gb >= 2) {  // P_b is free once PV of tile gb-2 has read it
+                    ok = warp_all(xy::mbar_wait(bar(B_PFREE0 + b), ((gb >> 1) - 1) & 1, abort_flag)) && ok;
+                    xy::tc_fence_after();
+                }
+                xy::tmem_st16(tbase + lane_off + kTmemP + b * 64 + (kCols / 2) * q4, pk);
+                l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+                if (t.kv_start + (j + 1) * kTileKeys > t.kv_end) {
+                    // keys at or past kv_end: unused page slots or stale data; their P is 0 and their V
+                    // rows are zeroed so that 0 * NaN cannot occur.  The V tile has its own slot: wait
+                    // for its copy to land first.  This thread zeroes its row's kCols columns, which in
+                    // the 128-byte swizzle are 16-byte chunks (q4 % 2) * 4 .. +3 XOR (row & 7).
+                    const int cv = c + 2 * j + 1, s = cv % kSlots;
+                    ok = warp_all(xy::mbar_wait(bar(B_FULL0 + s), (cv / kSlots) & 1, abort_flag)) && ok;
+                    if (t.kv_start + j * kTileKeys + row >= t.kv_end) {
+                        uint4 *vrow = reinterpret_cast<uint4 *>(gbase + kSlotOff + s * kTileBytes +
+                                                                (col0 >> 6) * kHalfBytes + row * 128);
                         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            reinterpret_cast<uint4 *>(vrow)[i] = z;
-                            reinterpret_cast<uint4 *>(vrow + kHalfBytes)[i] = z;
-                        }
+                        for (int i = 0; i < kCols / 8; ++i) vrow[(((col0 & 63) >> 3) + i) ^ (row & 7)] = z;
                     }
                     xy::fence_async_smem();
                 }
@@ -433,56 +469,57 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) xy::mbar_arrive(bar(B_PFULL0 + b));
             }
-            if (!ok) break;
-            if (!warp_all(xy::mbar_wait(bar(B_OBAR), (g + n - 1) & 1, abort_flag))) {
-                ok = false;
+            ok = warp_all(xy::mbar_wait(bar(B_OBAR), (g + n - 1) & 1, abort_flag)) && ok;
+            xy::tc_fence_after();
+            // row sums of the kQ threads of a row, and the vote on whether to go on
+            sums[q4 * 128 + row] = l;
+            if (lane == 0) vote[warp] = ok ? 0 : 1;
+            xy::named_bar_sync(kSoftmaxBar, kSoftmaxWarps * 32);
+            float L = l;
+#pragma unroll
+            for (int o = 1; o < kQ; ++o) L += sums[((q4 + o) % kQ) * 128 + row];
+            int bad = 0;
+#pragma unroll
+            for (int w = 0; w < kSoftmaxWarps; ++w) bad |= vote[w];
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            uint32_t r[kCols];
+            xy::tmem_ld32(o_addr, r);
+            if (valid && !bad) {
+                if (t.num_splits == 1) {
+                    const int64_t tok = f.seq_start + t.q_start + row / p.G;
+                    const int h = t.kv_head * p.G + row % p.G;
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.Hq + h) * HD + col0);
+#pragma unroll
+                    for (int v = 0; v < kCols / 8; ++v) {
+                        uint4 w;
+                        w.x = xy::pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                        w.y = xy::pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                        w.z = xy::pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                        w.w = xy::pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                        dst[v] = w;
+                    }
+                } else {
+                    const int64_t wr = (int64_t)t.ws_row + row;
+                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wr * HD + col0);
+#pragma unroll
+                    for (int v = 0; v < kCols / 4; ++v)
+                        dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                             __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                    if (q4 == 0) p.ws_lse[wr] = L > 0.f ? m + __log2f(L) : -INFINITY;
+                }
+            }
+            xy::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) xy::mbar_arrive(bar(B_OFREE));
+            g += n;
+            c += 2 * n;
+            ++qk;
+            if (bad) {
+                *abort_flag = 1;
+                if (warp == 0 && lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
                 break;
             }
-            xy::tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            if (t.num_splits == 1) {
-                const int64_t tok = f.seq_start + t.q_start + row / p.G;
-                const int h = t.kv_head * p.G + row % p.G;
-                uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.Hq + h) * HD);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    xy::tmem_ld32(tbase + lane_off + kTmemO + c * 32, r);
-                    if (valid) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            uint4 w;
-                            w.x = xy::pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                            w.y = xy::pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                            w.z = xy::pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                            w.w = xy::pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-                            dst[c * 4 + v] = w;
-                        }
-                    }
-                }
-            } else {
-                const int64_t wr = (int64_t)t.ws_row + row;
-                float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wr * HD);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    xy::tmem_ld32(tbase + lane_off + kTmemO + c * 32, r);
-                    if (valid) {
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            dst[c * 8 + v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                                         __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-                    }
-                }
-                if (valid) p.ws_lse[wr] = l > 0.f ? m + __log2f(l) : -INFINITY;
-            }
-            g += n;
-            ctr += n;
             tc.advance(p);
-        }
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
         }
     }
 
@@ -516,6 +553,8 @@ EncodeTiledFn encode_fn() {
 
 namespace xy {
 
+void set_last_error(const char *what, const char *msg);
+
 xy_status launch_tile_attention(const AttnParams &p, const void *k_pages, const void *v_pages, int num_pages,
                                 int block_size, int num_ctas, cudaStream_t st) {
     EncodeTiledFn fn = encode_fn();
@@ -548,15 +587,16 @@ xy_status launch_tile_attention(const AttnParams &p, const void *k_pages, const 
         return XY_ERR_CUDA;
     static int configured_device = -1;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return XY_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(tile_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-            cudaSuccess)
-            return XY_ERR_CUDA;
+        const cudaError_t e =
+            cudaFuncSetAttribute(tile_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "tile_attention_kernel smem attribute");
         configured_device = dev;
     }
     tile_attention_kernel<<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, p);
-    return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? XY_OK : cuda_fail(e, "tile_attention_kernel launch");
 }
 
 }  // namespace xy
