@@ -183,9 +183,9 @@ xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *contex
  *   workspace: device, >= the workspace_bytes the builder returned (may be NULL when 0).
  *   err_word: device int32 (see XY_DEV_*).
  * Supported: head_dim 64 or 128; block_size a power of two in [16, 256]; kv_chunk (of
- * xy_build_task_table) a multiple of 128 keys.  Rows per task (q_rows * G, G = Hq/Hkv): up to 128
+ * xy_build_task_table) a multiple of 128 keys.  Rows per task (q_rows * G, G = Hq/Hkv): up to 256
  * when head_dim is 128 and G divides 128 (tasks with more than 16 rows then run on tcgen05 tensor
- * cores), otherwise up to 64.  Tasks outside these limits set XY_DEV_BAD_TASK.
+ * cores as two 128-row tiles), otherwise up to 64.  Tasks outside these limits set XY_DEV_BAD_TASK.
  * Errors: XY_ERR_INVALID_ARG, XY_ERR_UNSUPPORTED, XY_ERR_WORKSPACE, XY_ERR_CUDA.
  */
 xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q,

@@ -1,26 +1,28 @@
 // Tensor-core (tcgen05 / TMEM) tiles of the paged attention: the prefill and chunk tasks, whose
-// (token, head) rows fill a 128-row MMA tile.  The decode-sized tasks run in xy_attention.cu.
+// (token, head) rows fill 128-row MMA tiles.  The decode-sized tasks run in xy_attention.cu.
 //
 // "XY-Serve 深度实战" (chenxutan.com/d/5031) §2.2 component 3: Meta-Attention is one fused
 // GEMM-softmax-GEMM over a task's (query block x KV block) tiles; §2.3 technique 1: ragged tiles
 // are masked on chip and only valid rows are stored.
 //
-// One persistent CTA per SM, eighteen warps:
-//   warp 16     producer: TMA loads of the task's 128 query rows (G heads x 128/G tokens, one 3-D
-//               box per 64-column half) into one of two Q buffers, and of 128-key K and V tiles,
-//               gathered page by page through the block table (2-D boxes, 128-byte swizzle), into
-//               a 4-slot ring (K_j and V_j take separate slots, so K runs ahead of V);
-//   warp 17     MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM buffers, then
-//               O += P_{j-1} V_{j-1} with P read from TMEM (packed bf16, two buffers of its own,
-//               so the next S never waits for a PV);
-//   warps 0..15 softmax, four threads per query row (TMEM lane = row; warps 4q..4q+3 take key
-//               columns 32q..32q+31), the row max exchanged through shared memory:
-//               masked max, exp2, row sum, P back to TMEM.  O is rescaled in TMEM only when a row's
-//               running max grows by more than 2^8 (otherwise the stale max is kept, which is exact
-//               because O and the row sum share it).  Epilogue: O / l from TMEM to global memory.
-// TMEM: S0 = columns [0,128), S1 = [128,256), P0 = [256,320), P1 = [320,384), O = [384,512).
-// The softmax warps release an S buffer as soon as they have loaded it, so S_{j+2} overlaps the
-// softmax and PV of tile j.
+// A task holds up to 256 (token, head) rows: query tile A (rows 0..127) and tile B (rows
+// 128..255), both against the same 128-key K/V tiles, so each K/V tile loaded serves two MMA
+// tiles.  One persistent CTA per SM, ten warps:
+//   warp 8      producer: TMA loads of the task's query rows (G heads x 128/G tokens per tile,
+//               one 3-D box per 64-column half) and of 128-key K and V tiles gathered page by
+//               page through the block table (2-D boxes, 128-byte swizzle) into a 5-slot ring
+//               (K_j and V_j take separate slots, so K runs ahead of V);
+//   warp 9      MMA issuer (one thread), per K/V tile j:
+//                 PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)
+//               with S_X = Q_X K^T into TMEM and O_X += P_X V, P_X read from TMEM where the
+//               softmax wrote it over the first 64 columns of S_X (the MMAs of one thread run in
+//               issue order, so PV_X(j-1) has read P_X before S_X(j) overwrites it);
+//   warps 0..3  softmax of tile A, warps 4..7 softmax of tile B: one query row per thread (TMEM
+//               lane = row), masked row max, exp2, row sum, P back to TMEM.  While one group
+//               works, the tensor core runs the other tile's MMAs.  O_X is rescaled in TMEM only
+//               when a row's running max grows by more than 2^8 (otherwise the stale max is kept,
+//               which is exact because O and the row sum share it).  Epilogue: O / l from TMEM.
+// TMEM: S_A = columns [0,128), S_B = [128,256), O_A = [256,384), O_B = [384,512).
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -42,51 +44,41 @@ using xy::TaskInfo;
 
 constexpr int HD = 128;
 constexpr int kTileKeys = 128;
-constexpr int kSlots = 4;                       // K/V ring slots (one K or V tile each)
-constexpr int kSoftmaxWarps = 16;               // kQ threads per query row
-constexpr int kQ = kSoftmaxWarps / 4;
-constexpr int kCols = 128 / kQ;                 // S / O columns per softmax thread
-constexpr int kProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;
-constexpr int kThreads = (kSoftmaxWarps + 2) * 32;
-static_assert(kCols == 32, "the softmax code moves 32 TMEM columns per thread");
+constexpr int kSlots = 5;                       // K/V ring slots (one K or V tile each)
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 columns
-constexpr int kTileBytes = 2 * kHalfBytes;      // Q, K or V tile: [half][128 rows][128 B]
-constexpr int kQOff = 0;                        // Q0, Q1
+constexpr int kTileBytes = 2 * kHalfBytes;      // one Q, K or V tile: [half][128 rows][128 B]
+constexpr int kQOff = 0;                        // Q_A, Q_B
 constexpr int kSlotOff = 2 * kTileBytes;
 enum {
-    B_QFULL0 = 0,
-    B_QEMPTY0 = B_QFULL0 + 2,
-    B_FULL0 = B_QEMPTY0 + 2,
+    B_QFULL = 0,
+    B_QEMPTY,
+    B_FULL0,
     B_EMPTY0 = B_FULL0 + kSlots,
-    B_SFULL0 = B_EMPTY0 + kSlots,
-    B_SFREE0 = B_SFULL0 + 2,
-    B_PFULL0 = B_SFREE0 + 2,
-    B_PFREE0 = B_PFULL0 + 2,
-    B_OFREE = B_PFREE0 + 2,
-    B_OBAR,
-    B_DONE,
+    B_SFULL0 = B_EMPTY0 + kSlots,   // per query tile X
+    B_PFULL0 = B_SFULL0 + 2,
+    B_OBAR0 = B_PFULL0 + 2,
+    B_OFREE0 = B_OBAR0 + 2,
+    B_DONE = B_OFREE0 + 2,
     B_COUNT
 };
 constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
 constexpr int kMiscOff = kBarOff + B_COUNT * 8;     // TMEM base address, abort flag
-constexpr int kVoteOff = kMiscOff + 16;              // one vote per softmax warp
-constexpr int kRedOff = kVoteOff + 4 * kSoftmaxWarps; // row-max exchange [2 parity][kQ][128]
-constexpr int kSumOff = kRedOff + 2 * kQ * 128 * 4;  // row-sum exchange [kQ][128]
-constexpr int kSmemBytes = kSumOff + kQ * 128 * 4 + 1024;
+constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp
+constexpr int kSmemBytes = kVoteOff + 64 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemP = 256;
-constexpr uint32_t kTmemO = 384;
+constexpr uint32_t kTmemO = 256;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr uint32_t kSoftmaxBar = 1;        // named barrier id of the softmax warps
 
 __device__ __forceinline__ bool mine(const TaskInfo &f, const AttnParams &p) {
     return xy::is_tile_task(f.t, p.G, HD);
 }
 
 __device__ __forceinline__ bool tile_ok(const TaskInfo &f, const AttnParams &p) {
-    return xy::task_common_ok(f, p) && f.t.q_rows * p.G <= 128 && (f.t.kv_start % kTileKeys) == 0;
+    return xy::task_common_ok(f, p) && f.t.q_rows * p.G <= 256 && (f.t.kv_start % kTileKeys) == 0;
 }
 
 // Walks this CTA's tasks (blockIdx.x, +gridDim.x, ...), fetching the next task's record and
@@ -135,25 +127,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff + 4);
     volatile int *vote = reinterpret_cast<volatile int *>(gbase + kVoteOff);
-    float *red = reinterpret_cast<float *>(gbase + kRedOff);
-    float *sums = reinterpret_cast<float *>(gbase + kSumOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
-            xy::mbar_init(bar(B_QFULL0 + i), 1);
-            xy::mbar_init(bar(B_QEMPTY0 + i), 1);
-            xy::mbar_init(bar(B_SFULL0 + i), 1);
-            xy::mbar_init(bar(B_SFREE0 + i), kSoftmaxWarps);
-            xy::mbar_init(bar(B_PFULL0 + i), kSoftmaxWarps);
-            xy::mbar_init(bar(B_PFREE0 + i), 1);
-        }
-        xy::mbar_init(bar(B_OFREE), kSoftmaxWarps);
+        xy::mbar_init(bar(B_QFULL), 1);
+        xy::mbar_init(bar(B_QEMPTY), 1);
         for (int s = 0; s < kSlots; ++s) {
             xy::mbar_init(bar(B_FULL0 + s), 1);
             xy::mbar_init(bar(B_EMPTY0 + s), 1);
         }
-        xy::mbar_init(bar(B_OBAR), 1);
+        for (int x = 0; x < 2; ++x) {
+            xy::mbar_init(bar(B_SFULL0 + x), 1);
+            xy::mbar_init(bar(B_PFULL0 + x), 4);   // the four warps of softmax group x
+            xy::mbar_init(bar(B_OBAR0 + x), 1);
+            xy::mbar_init(bar(B_OFREE0 + x), 4);
+        }
         xy::mbar_init(bar(B_DONE), 1);
         *abort_flag = 0;
         xy::fence_mbarrier_init();
@@ -167,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     xy::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
     const int BRt = p.bs < kTileKeys ? p.bs : kTileKeys;  // keys per K/V box
+    const int qt_tokens = 128 / p.G;                      // tokens per query tile
 
     if (warp == kProducerWarp) {
         // ---------------------------------- producer ----------------------------------
@@ -199,17 +188,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const TaskInfo f = tc.cur;
             const xy_task &t = f.t;
-            const int qb = qk & 1;
-            if (qk >= 2 && !warp_all(xy::mbar_wait(bar(B_QEMPTY0 + qb), ((qk >> 1) - 1) & 1, abort_flag))) {
+            const bool has_b = t.q_rows * p.G > 128;
+            if (qk >= 1 && !warp_all(xy::mbar_wait(bar(B_QEMPTY), (qk - 1) & 1, abort_flag))) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                xy::mbar_arrive_expect_tx(bar(B_QFULL0 + qb), kTileBytes);
+                xy::mbar_arrive_expect_tx(bar(B_QFULL), (has_b ? 2 : 1) * kTileBytes);
                 const int y = t.kv_head * p.G, z = f.seq_start + t.q_start;
-                const uint32_t qdst = base + kQOff + qb * kTileBytes;
-                xy::tma_load_3d(qdst, &qmap, 0, y, z, bar(B_QFULL0 + qb));
-                xy::tma_load_3d(qdst + kHalfBytes, &qmap, 64, y, z, bar(B_QFULL0 + qb));
+                for (int x = 0; x < (has_b ? 2 : 1); ++x) {
+                    const uint32_t qdst = base + kQOff + x * kTileBytes;
+                    xy::tma_load_3d(qdst, &qmap, 0, y, z + x * qt_tokens, bar(B_QFULL));
+                    xy::tma_load_3d(qdst + kHalfBytes, &qmap, 64, y, z + x * qt_tokens, bar(B_QFULL));
+                }
             }
             ++qk;
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.MB;
@@ -270,38 +261,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         // every issued copy must land before the CTA may exit
         for (int k = c - 1; k >= 0 && k >= c - kSlots; --k)
             xy::mbar_wait(bar(B_FULL0 + k % kSlots), (k / kSlots) & 1);
-        for (int k = qk - 1; k >= 0 && k >= qk - 2; --k) xy::mbar_wait(bar(B_QFULL0 + (k & 1)), (k >> 1) & 1);
+        if (qk > 0) xy::mbar_wait(bar(B_QFULL), (qk - 1) & 1);
     } else if (warp == kMmaWarp) {
         // ---------------------------------- MMA issuer ----------------------------------
         if (lane == 0) {
             const uint32_t id_s = xy::idesc_bf16(128, 128, 0, 0);   // Q (K-major) x K tile (K-major)
             const uint32_t id_o = xy::idesc_bf16(128, 128, 0, 1);   // P (TMEM) x V tile (MN-major)
-            int c = 0, g = 0, qk = 0;
-            bool ok = true, issued = false;
-            // Descriptors are built once; a k-step or a buffer only adds a constant to the 14-bit
-            // address field (addresses stay below 256 KB), so the issue loop is a few adds per MMA
-            // and the single issuing thread keeps up with the tensor core.
+            // Descriptors are built once; a k-step or buffer only adds a constant to the 14-bit
+            // address field (addresses stay below 256 KB), keeping the single issuing thread cheap.
             const uint64_t q_desc0 = xy::smem_desc_sw128(base + kQOff, 16, 1024);
             const uint64_t k_desc0 = xy::smem_desc_sw128(base + kSlotOff, 16, 1024);
             const uint64_t v_desc0 = xy::smem_desc_sw128(base + kSlotOff, kHalfBytes, 1024);
-            constexpr uint32_t kTileDesc = kTileBytes >> 4;  // one Q buffer or ring slot
-            auto issue_pv = [&](int jj, uint32_t o_addr) -> bool {
-                const int gb = g + jj, b = gb & 1;
-                if (jj == 0 && qk >= 1 && !xy::mbar_wait(bar(B_OFREE), (qk - 1) & 1, abort_flag))
-                    return false;  // the previous task's epilogue has read O
-                if (!xy::mbar_wait(bar(B_PFULL0 + b), (gb >> 1) & 1, abort_flag)) return false;
-                const int cv = c + 2 * jj + 1, s = cv % kSlots;
-                if (!xy::mbar_wait(bar(B_FULL0 + s), (cv / kSlots) & 1, abort_flag)) return false;
-                xy::tc_fence_after();
-                const uint64_t vd = v_desc0 + (uint64_t)(s * kTileDesc);
-                const uint32_t pa = tbase + kTmemP + b * 64;
-                xy::umma_ts(o_addr, pa, vd, id_o, jj > 0 ? 1u : 0u);
-#pragma unroll
-                for (int k = 1; k < 8; ++k) xy::umma_ts(o_addr, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), id_o, 1u);
-                xy::umma_commit(bar(B_EMPTY0 + s));
-                xy::umma_commit(bar(B_PFREE0 + b));
-                xy::umma_commit(bar(B_OBAR));
+            constexpr uint32_t kTileDesc = kTileBytes >> 4;
+            int c = 0, qk = 0;
+            int ns[2] = {0, 0};   // S_X issued so far (= PV_X issued, = tiles of group X)
+            int nt[2] = {0, 0};   // tasks in which query tile X was active (= its O_X epilogues)
+            bool ok = true, issued = false;
+            auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+                if (!xy::mbar_wait(b, parity, abort_flag)) {
+                    ok = false;
+                    return false;
+                }
                 return true;
+            };
+            auto issue_s = [&](int x, int j) {
+                const int s = (c + 2 * j) % kSlots;
+                const uint64_t qd = q_desc0 + (uint64_t)(x * kTileDesc);
+                const uint64_t kd = k_desc0 + (uint64_t)(s * kTileDesc);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t koff = (uint64_t)(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+                    xy::umma_ss(tbase + x * 128, qd + koff, kd + koff, id_s, k > 0 ? 1u : 0u);
+                }
+                xy::umma_commit(bar(B_SFULL0 + x));
+                ++ns[x];
+            };
+            auto issue_pv = [&](int x, int j) {
+                const int s = (c + 2 * j + 1) % kSlots;
+                const uint64_t vd = v_desc0 + (uint64_t)(s * kTileDesc);
+                const uint32_t pa = tbase + x * 128, od = tbase + kTmemO + x * 128;
+                xy::umma_ts(od, pa, vd, id_o, j > 0 ? 1u : 0u);
+#pragma unroll
+                for (int k = 1; k < 8; ++k) xy::umma_ts(od, pa + k * 8, vd + (uint64_t)(k * (2048 >> 4)), id_o, 1u);
+                xy::umma_commit(bar(B_OBAR0 + x));
             };
             TaskCursor tc;
             tc.begin(p);
@@ -313,43 +315,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const xy_task t = tc.cur.t;
                 const int n = (t.kv_end - t.kv_start + kTileKeys - 1) / kTileKeys;
-                const int qb = qk & 1;
-                const uint32_t o_addr = tbase + kTmemO;
-                if (!xy::mbar_wait(bar(B_QFULL0 + qb), (qk >> 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+                const int nx = t.q_rows * p.G > 128 ? 2 : 1;
+                if (!wait(bar(B_QFULL), qk & 1)) break;
                 xy::tc_fence_after();
                 tc.prefetch_next(p);
-                for (int j = 0; j < n && ok; ++j) {
-                    const int ck = c + 2 * j, s = ck % kSlots;
-                    if (!xy::mbar_wait(bar(B_FULL0 + s), (ck / kSlots) & 1, abort_flag)) {
-                        ok = false;
-                        break;
+                issued = true;
+                for (int j = 0; j <= n && ok; ++j) {
+                    if (j < n) {  // K_j has landed
+                        const int ck = c + 2 * j;
+                        if (!wait(bar(B_FULL0 + ck % kSlots), (ck / kSlots) & 1)) break;
                     }
-                    const int gb = g + j, b = gb & 1;
-                    if (gb >= 2 && !xy::mbar_wait(bar(B_SFREE0 + b), ((gb >> 1) - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
+                    if (j >= 1) {  // V_{j-1} has landed
+                        const int cv = c + 2 * (j - 1) + 1;
+                        if (!wait(bar(B_FULL0 + cv % kSlots), (cv / kSlots) & 1)) break;
                     }
-                    xy::tc_fence_after();
-                    issued = true;
-                    const uint64_t qd = q_desc0 + (uint64_t)(qb * kTileDesc);
-                    const uint64_t kd = k_desc0 + (uint64_t)(s * kTileDesc);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint64_t koff = (uint64_t)(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
-                        xy::umma_ss(tbase + b * 128, qd + koff, kd + koff, id_s, k > 0 ? 1u : 0u);
+                    for (int x = 0; x < nx && ok; ++x) {
+                        if (j >= 1) {
+                            // P_X(j-1) written (and O_X corrected) by its softmax group; for the
+                            // first PV of the task the previous task's epilogue must have read O_X
+                            if (!wait(bar(B_PFULL0 + x), (ns[x] - 1) & 1)) break;
+                            if (j == 1 && nt[x] >= 1 && !wait(bar(B_OFREE0 + x), (nt[x] - 1) & 1)) break;
+                            xy::tc_fence_after();
+                            issue_pv(x, j - 1);
+                        }
+                        if (j < n) issue_s(x, j);
                     }
-                    xy::umma_commit(bar(B_EMPTY0 + s));
-                    xy::umma_commit(bar(B_SFULL0 + b));
-                    if (j == n - 1) xy::umma_commit(bar(B_QEMPTY0 + qb));
-                    if (j >= 1) ok = issue_pv(j - 1, o_addr);
+                    if (!ok) break;
+                    if (j >= 1) xy::umma_commit(bar(B_EMPTY0 + (c + 2 * (j - 1) + 1) % kSlots));  // V_{j-1}
+                    if (j < n) xy::umma_commit(bar(B_EMPTY0 + (c + 2 * j) % kSlots));             // K_j
+                    if (j == n - 1) xy::umma_commit(bar(B_QEMPTY));  // the last S of the task
                 }
-                if (ok) ok = issue_pv(n - 1, o_addr);
-                g += n;
                 c += 2 * n;
                 ++qk;
+                for (int x = 0; x < nx; ++x) ++nt[x];
                 tc.advance(p);
             }
             if (!ok) {
@@ -362,13 +360,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else {
+    } else if (warp < 8) {
         // ---------------------------------- softmax ----------------------------------
-        const int q4 = warp >> 2;                   // key columns [kCols*q4, kCols*q4 + kCols)
-        const int row = (warp & 3) * 32 + lane;
+        const int x = warp >> 2;                            // query tile of this group
+        const int trow = (warp & 3) * 32 + lane;            // row within the tile = TMEM lane
+        const int row = x * 128 + trow;                     // row within the task
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        const int col0 = kCols * q4;
-        int c = 0, g = 0, qk = 0;
+        const uint32_t s_addr = tbase + lane_off + x * 128;
+        const uint32_t o_addr = tbase + lane_off + kTmemO + x * 128;
+        int c = 0, qk = 0, ns = 0;   // ns: tiles this group has processed (= its S and PV count)
         bool ok = true;
         TaskCursor tc;
         tc.begin(p);
@@ -382,136 +382,176 @@ __global__ void __launch_bounds__(kThreads, 1)
             const xy_task t = f.t;
             const int R = t.q_rows * p.G;
             const int n = (t.kv_end - t.kv_start + kTileKeys - 1) / kTileKeys;
+            const bool active = x == 0 || R > 128;  // tile B exists only for tasks with > 128 rows
             const bool valid = row < R;
             const int lim = valid ? min(t.kv_end, p.causal ? f.L - f.qn + t.q_start + row / p.G + 1 : f.L) : t.kv_end;
-            const uint32_t o_addr = tbase + lane_off + kTmemO + col0;
             float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < n; ++j) {
-                const int gb = g + j, b = gb & 1;
-                // a failed wait (timeout or abort) is recorded, not acted on: every softmax warp
-                // keeps executing the same named barriers and the decision to stop is voted below
-                ok = warp_all(xy::mbar_wait(bar(B_SFULL0 + b), (gb >> 1) & 1, abort_flag)) && ok;
-                xy::tc_fence_after();
-                if (j == 0) tc.prefetch_next(p);
-                const int kt0 = t.kv_start + j * kTileKeys + col0;
-                uint32_t sr[kCols];
-                xy::tmem_ld32(tbase + lane_off + b * 128 + col0, sr);
-                xy::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) xy::mbar_arrive(bar(B_SFREE0 + b));  // S_b may be overwritten now
-                float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                if (kt0 + kCols <= lim) {
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) {
-                        if (kt0 + i >= lim) sr[i] = __float_as_uint(-INFINITY);
-                        mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
-                    }
-                }
-                float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-                // exchange the partial row maxima of the kQ threads of a row
-                float *rd = red + (gb & 1) * (kQ * 128);
-                rd[q4 * 128 + row] = mx;
-                xy::named_bar_sync(kSoftmaxBar, kSoftmaxWarps * 32);
-#pragma unroll
-                for (int o = 1; o < kQ; ++o) mx = fmaxf(mx, rd[((q4 + o) % kQ) * 128 + row]);
-                const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
-                if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-                    const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
-                    m = m_new;
-                    l *= alpha;
-                    if (j > 0) {  // O has PV_0..PV_{j-1}; rescale these columns once the last one is done
-                        ok = warp_all(xy::mbar_wait(bar(B_OBAR), (gb - 1) & 1, abort_flag)) && ok;
-                        xy::tc_fence_after();
-                        uint32_t orow[kCols];
-                        xy::tmem_ld32(o_addr, orow);
-#pragma unroll
-                        for (int i = 0; i < kCols; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                        xy::tmem_st32(o_addr, orow);
-                    }
-                }
-                // p = 2^(s * scale_log2 - m), packed to bf16 pairs, into this thread's P columns
-                const float neg_mu = m == -INFINITY ? 0.f : -m;
-                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[kCols / 2];
-#pragma unroll
-                for (int i = 0; i < kCols / 2; ++i) {
-                    const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), p.scale_log2, neg_mu));
-                    const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), p.scale_log2, neg_mu));
-                    ls4[i & 3] += p0 + p1;
-                    pk[i] = xy::pack_bf16x2(p0, p1);
-                }
-                if (gb >= 2) {  // P_b is free once PV of tile gb-2 has read it
-                    ok = warp_all(xy::mbar_wait(bar(B_PFREE0 + b), ((gb >> 1) - 1) & 1, abort_flag)) && ok;
+            if (active) {
+                for (int j = 0; j < n; ++j) {
+                    // a failed wait (timeout or abort) is recorded, not acted on: the group keeps
+                    // executing the same steps and the decision to stop is voted below
+                    ok = warp_all(xy::mbar_wait(bar(B_SFULL0 + x), ns & 1, abort_flag)) && ok;
                     xy::tc_fence_after();
-                }
-                xy::tmem_st16(tbase + lane_off + kTmemP + b * 64 + (kCols / 2) * q4, pk);
-                l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-                if (t.kv_start + (j + 1) * kTileKeys > t.kv_end) {
-                    // keys at or past kv_end: unused page slots or stale data; their P is 0 and their V
-                    // rows are zeroed so that 0 * NaN cannot occur.  The V tile has its own slot: wait
-                    // for its copy to land first.  This thread zeroes its row's kCols columns, which in
-                    // the 128-byte swizzle are 16-byte chunks (q4 % 2) * 4 .. +3 XOR (row & 7).
-                    const int cv = c + 2 * j + 1, s = cv % kSlots;
-                    ok = warp_all(xy::mbar_wait(bar(B_FULL0 + s), (cv / kSlots) & 1, abort_flag)) && ok;
-                    if (t.kv_start + j * kTileKeys + row >= t.kv_end) {
-                        uint4 *vrow = reinterpret_cast<uint4 *>(gbase + kSlotOff + s * kTileBytes +
-                                                                (col0 >> 6) * kHalfBytes + row * 128);
-                        const uint4 z = make_uint4(0, 0, 0, 0);
+                    if (j == 0) tc.prefetch_next(p);
+                    const int kt0 = t.kv_start + j * kTileKeys;
+                    // a warp whose rows all see the whole tile skips the per-key mask
+                    const bool full = __all_sync(0xffffffffu, kt0 + kTileKeys <= lim);
+                    // pass 1: masked row max; 32-column TMEM loads, the next one in flight while
+                    // the current one is reduced
+                    uint32_t ca[32], cb[32];
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    auto max_chunk = [&](const uint32_t (&r)[32], int c0) {
+                        if (full) {
 #pragma unroll
-                        for (int i = 0; i < kCols / 8; ++i) vrow[(((col0 & 63) >> 3) + i) ^ (row & 7)] = z;
+                            for (int i = 0; i < 32; i += 8) {
+                                m4[0] = xy::max3(m4[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                                m4[1] = xy::max3(m4[1], __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                                m4[2] = xy::max3(m4[2], __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                                m4[3] = xy::max3(m4[3], __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
+                        }
+                    };
+                    xy::tmem_ld32_nowait(s_addr, ca);
+                    xy::tmem_wait_ld(ca);
+                    xy::tmem_ld32_nowait(s_addr + 32, cb);
+                    max_chunk(ca, 0);
+                    xy::tmem_wait_ld(cb);
+                    xy::tmem_ld32_nowait(s_addr + 64, ca);
+                    max_chunk(cb, 32);
+                    xy::tmem_wait_ld(ca);
+                    xy::tmem_ld32_nowait(s_addr + 96, cb);
+                    max_chunk(ca, 64);
+                    xy::tmem_wait_ld(cb);
+                    xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
+                    max_chunk(cb, 96);
+                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
+                    const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
+                    xy::tmem_wait_ld(ca);
+                    if (rescale) {
+                        const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
+                        m = m_new;
+                        l *= alpha;
+                        if (j > 0) {  // O_X has PV_X(0..j-1); rescale once the last of them is done
+                            ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
+                            xy::tc_fence_after();
+#pragma unroll 1
+                            for (int h = 0; h < 4; ++h) {
+                                uint32_t orow[32];
+                                xy::tmem_ld32(o_addr + h * 32, orow);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                                xy::tmem_st32(o_addr + h * 32, orow);
+                            }
+                        }
                     }
-                    xy::fence_async_smem();
-                }
-                xy::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) xy::mbar_arrive(bar(B_PFULL0 + b));
-            }
-            ok = warp_all(xy::mbar_wait(bar(B_OBAR), (g + n - 1) & 1, abort_flag)) && ok;
-            xy::tc_fence_after();
-            // row sums of the kQ threads of a row, and the vote on whether to go on
-            sums[q4 * 128 + row] = l;
-            if (lane == 0) vote[warp] = ok ? 0 : 1;
-            xy::named_bar_sync(kSoftmaxBar, kSoftmaxWarps * 32);
-            float L = l;
+                    // pass 2: p = 2^(s * scale_log2 - m) for 32 columns at a time, packed to bf16
+                    // pairs and written over S columns that pass 2 has already read
+                    const float neg_mu = m == -INFINITY ? 0.f : -m;
+                    const uint64_t sc2 = xy::f2_pack(p.scale_log2, p.scale_log2), nm2 = xy::f2_pack(neg_mu, neg_mu);
+                    uint64_t acc2[2] = {0ull, 0ull};
+                    auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
+                        uint32_t pk[16];
 #pragma unroll
-            for (int o = 1; o < kQ; ++o) L += sums[((q4 + o) % kQ) * 128 + row];
+                        for (int i = 0; i < 16; ++i) {
+                            float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+                            if (!full) {
+                                s0 = kt0 + c0 + 2 * i < lim ? s0 : -INFINITY;
+                                s1 = kt0 + c0 + 2 * i + 1 < lim ? s1 : -INFINITY;
+                            }
+                            float e0, e1;
+                            xy::f2_unpack(xy::f2_fma(xy::f2_pack(s0, s1), sc2, nm2), e0, e1);
+                            const float p0 = ex2(e0), p1 = ex2(e1);
+                            acc2[i & 1] = xy::f2_add(acc2[i & 1], xy::f2_pack(p0, p1));
+                            pk[i] = xy::pack_bf16x2(p0, p1);
+                        }
+                        xy::tmem_st16(s_addr + 16 * chunk, pk);
+                    };
+                    xy::tmem_ld32_nowait(s_addr + 32, cb);
+                    exp_chunk(ca, 0, 0);
+                    xy::tmem_wait_ld(cb);
+                    xy::tmem_ld32_nowait(s_addr + 64, ca);
+                    exp_chunk(cb, 32, 1);
+                    xy::tmem_wait_ld(ca);
+                    xy::tmem_ld32_nowait(s_addr + 96, cb);
+                    exp_chunk(ca, 64, 2);
+                    xy::tmem_wait_ld(cb);
+                    exp_chunk(cb, 96, 3);
+                    float ls4[4];
+                    xy::f2_unpack(acc2[0], ls4[0], ls4[1]);
+                    xy::f2_unpack(acc2[1], ls4[2], ls4[3]);
+                    l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+                    if (x == 0 && kt0 + kTileKeys > t.kv_end) {
+                        // keys at or past kv_end: unused page slots or stale data; their P is 0 and
+                        // their V rows are zeroed (group A, before both tiles' PV of this K/V tile)
+                        // so that 0 * NaN cannot occur.  Wait for the V copy to land first.
+                        const int cv = c + 2 * j + 1, s = cv % kSlots;
+                        ok = warp_all(xy::mbar_wait(bar(B_FULL0 + s), (cv / kSlots) & 1, abort_flag)) && ok;
+                        if (kt0 + trow >= t.kv_end) {
+                            uint4 *v0 = reinterpret_cast<uint4 *>(gbase + kSlotOff + s * kTileBytes + trow * 128);
+                            uint4 *v1 = reinterpret_cast<uint4 *>(gbase + kSlotOff + s * kTileBytes + kHalfBytes + trow * 128);
+                            const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                v0[i] = z;
+                                v1[i] = z;
+                            }
+                        }
+                        xy::fence_async_smem();
+                    }
+                    xy::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) xy::mbar_arrive(bar(B_PFULL0 + x));
+                    ++ns;
+                }
+                ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
+                xy::tc_fence_after();
+            }
+            // the group's vote on whether to go on
+            if (lane == 0) vote[warp] = ok ? 0 : 1;
+            xy::named_bar_sync(1 + x, 128);
             int bad = 0;
 #pragma unroll
-            for (int w = 0; w < kSoftmaxWarps; ++w) bad |= vote[w];
-            const float inv = L > 0.f ? 1.f / L : 0.f;
-            uint32_t r[kCols];
-            xy::tmem_ld32(o_addr, r);
-            if (valid && !bad) {
-                if (t.num_splits == 1) {
-                    const int64_t tok = f.seq_start + t.q_start + row / p.G;
-                    const int h = t.kv_head * p.G + row % p.G;
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.Hq + h) * HD + col0);
+            for (int w = 0; w < 4; ++w) bad |= vote[x * 4 + w];
+            if (active) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t r[32];
+                    xy::tmem_ld32(o_addr + cc * 32, r);
+                    if (valid && !bad) {
+                        if (t.num_splits == 1) {
+                            const int64_t tok = f.seq_start + t.q_start + row / p.G;
+                            const int h = t.kv_head * p.G + row % p.G;
+                            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.Hq + h) * HD + cc * 32);
 #pragma unroll
-                    for (int v = 0; v < kCols / 8; ++v) {
-                        uint4 w;
-                        w.x = xy::pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                        w.y = xy::pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                        w.z = xy::pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                        w.w = xy::pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-                        dst[v] = w;
+                            for (int v = 0; v < 4; ++v) {
+                                uint4 w;
+                                w.x = xy::pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+                                w.y = xy::pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+                                w.z = xy::pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+                                w.w = xy::pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+                                dst[v] = w;
+                            }
+                        } else {
+                            const int64_t wr = (int64_t)t.ws_row + row;
+                            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wr * HD + cc * 32);
+#pragma unroll
+                            for (int v = 0; v < 8; ++v)
+                                dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                                     __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                        }
                     }
-                } else {
-                    const int64_t wr = (int64_t)t.ws_row + row;
-                    float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wr * HD + col0);
-#pragma unroll
-                    for (int v = 0; v < kCols / 4; ++v)
-                        dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                             __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-                    if (q4 == 0) p.ws_lse[wr] = L > 0.f ? m + __log2f(L) : -INFINITY;
                 }
+                if (valid && !bad && t.num_splits > 1) p.ws_lse[(int64_t)t.ws_row + row] = l > 0.f ? m + __log2f(l) : -INFINITY;
+                xy::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) xy::mbar_arrive(bar(B_OFREE0 + x));
             }
-            xy::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) xy::mbar_arrive(bar(B_OFREE));
-            g += n;
             c += 2 * n;
             ++qk;
             if (bad) {

@@ -80,7 +80,7 @@ def test_full_size_prefill_sampled():
     wl = workloads.prefill()
     rng = np.random.default_rng(1)
     seqs = sorted({int(np.argmax(wl.q_lens)), int(np.argmin(wl.q_lens)), int(rng.integers(wl.num_seqs))})
-    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=128 // wl.group), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=256 // wl.group), sample_seqs=seqs)
     assert_parity(r)
 
 
@@ -88,7 +88,7 @@ def test_full_size_mixed_sampled():
     wl = workloads.mixed()
     rng = np.random.default_rng(2)
     seqs = [0, 5, 8, 60, 127, int(np.argmax(wl.context_lens))]
-    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=128 // wl.group), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=256 // wl.group), sample_seqs=seqs)
     assert_parity(r)
 
 
