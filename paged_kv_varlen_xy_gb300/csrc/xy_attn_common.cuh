@@ -51,6 +51,46 @@ __device__ __forceinline__ TaskInfo fetch_info(const xy_task &t, const AttnParam
     return f;
 }
 
+// Walks this CTA's tasks (blockIdx.x, +gridDim.x, ...), fetching the next task's record and
+// per-sequence numbers while the current one runs.
+struct TaskCursor {
+    int ti;
+    bool have, have_next, nxt_ready;
+    TaskInfo cur, nxt;
+    xy_task rec_next;
+
+    __device__ void begin(const AttnParams &p) {
+        ti = blockIdx.x;
+        have = ti < p.num_tasks;
+        if (have) cur = fetch_info(p.tasks[ti], p);
+    }
+    __device__ void load_next_record(const AttnParams &p) {
+        const int tn = ti + gridDim.x;
+        have_next = tn < p.num_tasks;
+        if (have_next) rec_next = p.tasks[tn];
+        nxt_ready = false;
+    }
+    __device__ void prefetch_next(const AttnParams &p) {
+        if (have_next && !nxt_ready) {
+            nxt = fetch_info(rec_next, p);
+            nxt_ready = true;
+        }
+    }
+    __device__ void advance(const AttnParams &p) {
+        prefetch_next(p);
+        cur = nxt;
+        ti += gridDim.x;
+        have = have_next;
+    }
+};
+
+// Block-table window of a producer warp: lane i holds the physical page of logical page b0 + i of
+// sequence `seq` (-1 past the table).
+__device__ __forceinline__ int load_window(const AttnParams &p, int seq, int b0, int lane) {
+    const int idx = b0 + lane;
+    return (idx >= 0 && idx < p.MB) ? __ldg(p.bt + (int64_t)seq * p.MB + idx) : -1;
+}
+
 // Checks every kernel applies to a task before touching memory through it.
 __device__ __forceinline__ bool task_common_ok(const TaskInfo &f, const AttnParams &p) {
     const xy_task &t = f.t;
@@ -63,17 +103,28 @@ __device__ __forceinline__ bool task_common_ok(const TaskInfo &f, const AttnPara
     return true;
 }
 
-// A task belongs to the tcgen05 tile kernel when its rows fill a good part of a 128-row MMA
-// tile: head_dim 128, G divides 128 (the query box is G heads x 128/G tokens), more than 16 rows.
+// Tasks with more than this many (token, head) rows run on the tcgen05 tile kernel.
+#ifndef XY_TILE_MIN_ROWS
+#define XY_TILE_MIN_ROWS 16
+#endif
+
+// The tcgen05 tile kernel handles head_dim 128 when G divides 128 (a query box is G heads x
+// 128/G tokens); it takes the tasks with more than XY_TILE_MIN_ROWS rows.
+__host__ __device__ __forceinline__ bool tile_shape_ok(int G, int head_dim) {
+    return head_dim == 128 && (128 % G) == 0;
+}
 __host__ __device__ __forceinline__ bool is_tile_task(const xy_task &t, int G, int head_dim) {
-    return head_dim == 128 && (128 % G) == 0 && t.q_rows * G > 16;
+    return tile_shape_ok(G, head_dim) && t.q_rows * G > XY_TILE_MIN_ROWS;
 }
 
 // Records a CUDA error for xy_last_error_string() and returns XY_ERR_CUDA.
 xy_status cuda_fail(cudaError_t e, const char *what);
 
-// Launches the tcgen05 tile kernel over the tasks it owns (defined in xy_tile.cu).
-xy_status launch_tile_attention(const AttnParams &p, const void *k_pages, const void *v_pages, int num_pages,
-                                int block_size, int num_ctas, cudaStream_t st);
+// Launches the unified kernel (xy_tile.cu): tcgen05 tiles for tasks of more than
+// XY_TILE_MIN_ROWS rows, the decode path for the others, one persistent launch over the task
+// table.  kmap_d / vmap_d are the decode path's 3-D page-pool maps.
+xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const void *v_pages, int num_pages,
+                                int block_size, int num_ctas, const CUtensorMap &kmap_d, const CUtensorMap &vmap_d,
+                                cudaStream_t st);
 
 }  // namespace xy

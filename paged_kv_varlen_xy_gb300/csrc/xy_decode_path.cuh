@@ -1,0 +1,395 @@
+// The decode path of the paged attention: tasks with few (token, head) rows, which are
+// HBM-bound.  Used by the stand-alone kernel in xy_attention.cu and by the unified kernel in
+// xy_tile.cu, which host it with their own warp layout and shared-memory map.
+//
+// "XY-Serve 深度实战" (chenxutan.com/d/5031) §2.2 component 3 (one GEMM-softmax-GEMM per task of
+// the task table) and §2.3 technique 1 (virtual padding: masked on chip, valid rows stored).
+//
+// A producer warp gathers each 64-key stage of K and V with 3-D TMA boxes -- one box per page
+// (both 64-column halves), rows addressed as (physical_page * Hkv + kv_head) * bs + offset --
+// into a ring of shared-memory stages with 128-byte swizzle; the task's query rows travel with
+// its first stage as bulk copies.  Four math warps own 16-row slices of the task's rows; QK^T and
+// PV run on m16n8k16 tensor-core fragments, the online softmax on the accumulator registers with
+// quad shuffles.  When a task has fewer rows than warps x 16 the warps split each stage's keys
+// and merge their (max, sum, O) triples through shared memory at the end of the task.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "xy.h"
+#include "xy_attn_common.cuh"
+#include "xy_device.cuh"
+
+namespace xy {
+namespace dec {
+
+constexpr int kStageKeys = 64;
+constexpr int kMathWarps = 4;
+
+// Geometry of a decode stage ring: NS stages of K, V (64 keys x HD) and room for QR query rows.
+template <int HD, int NS, int QR>
+struct Ring {
+    static constexpr int kHalves = HD / 64;                        // 128-byte swizzle atoms per row
+    static constexpr int kTensorBytes = kHalves * kStageKeys * 128;  // K or V of one stage
+    static constexpr int kQBytes = QR * HD * 2;                    // the task's rows (first stage only)
+    static constexpr int kStageBytes = 2 * kTensorBytes + kQBytes;
+    static constexpr int kStages = NS;
+    static constexpr int kMaxRows = QR;
+    static constexpr int kBytes = NS * kStageBytes;
+    static constexpr int kSlotFloats = 16 * HD + 32;               // merge slot: O[16][HD], m[16], l[16]
+    static constexpr int kSlotBytes = kMathWarps * kSlotFloats * 4;
+    static_assert(QR % 16 == 0 && QR <= 16 * kMathWarps, "rows per decode task");
+};
+
+// Shared-memory handles of the decode path, set up by the hosting kernel.
+struct Smem {
+    uint32_t stages;             // shared address of the stage ring (1024-aligned)
+    uint8_t *stages_gen;         // generic pointer to the same ring
+    float *slots;                // merge slots
+    uint32_t full_bar;           // kStages mbarriers, count 1 (+ transaction bytes)
+    uint32_t empty_bar;          // kStages mbarriers, count kMathWarps
+    volatile int *abort_flag;    // CTA-wide
+    volatile int *vote;          // [2][kMathWarps]
+    uint32_t bar_id;             // named barrier shared by the four math warps
+};
+
+// Byte offset of element (key, col) of a stage tensor.  The stage holds 64 keys in boxes of BR =
+// 2^sh keys (one box per page, or per 64 keys of a larger page); a box is [half][BR][128 B] with
+// the TMA 128-byte swizzle, i.e. the 16-byte chunk index is XOR-ed with (key & 7), so eight
+// consecutive keys of one half hit eight different bank groups.
+template <int HD>
+__device__ __forceinline__ uint32_t swz(int key, int col, int sh) {
+    const int half = col >> 6, chunk = (col & 63) >> 3;
+    const int r = key & ((1 << sh) - 1);
+    return (uint32_t)((key - r) * (HD / 64) * 128 + ((half * 128) << sh) + r * 128 + ((chunk ^ (key & 7)) << 4) +
+                      (col & 7) * 2);
+}
+
+// Checks of a decode-path task beyond task_common_ok.
+template <class RG>
+__device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) {
+    return task_common_ok(f, p) && f.t.q_rows * p.G <= RG::kMaxRows && (f.t.kv_start % kStageKeys) == 0;
+}
+
+// Producer warp: issue every stage of decode task `f`.  `ctr` counts stages issued on the ring.
+// `pg_first` is the task's first block-table window if it was prefetched (else -1 with
+// have_first false).  `first_stage_done()` runs once, right after the first stage is issued
+// (the caller prefetches the next task there).  Returns false if a wait gave up.
+template <int HD, class RG, class F>
+__device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUtensorMap *kmap, const CUtensorMap *vmap,
+                             const Smem &sm, int &ctr, int lane, int pg_first, bool have_first, F first_stage_done) {
+    const xy_task &t = f.t;
+    const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;  // keys per TMA box
+    // block-table entries are read 32 logical pages at a time (one per lane), the next window
+    // loaded before it is needed, so no stage waits on a dependent global load
+    int win0 = t.kv_start / p.bs;
+    int pg_win = have_first ? pg_first : load_window(p, t.seq, win0, lane);
+    int pg_nxt = load_window(p, t.seq, win0 + 32, lane);
+    bool first_stage = true;
+    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
+        const int s = ctr % RG::kStages;
+        if (ctr >= RG::kStages &&
+            !__all_sync(0xffffffffu, mbar_wait(sm.empty_bar + 8 * s, ((ctr / RG::kStages) - 1) & 1, sm.abort_flag)))
+            return false;
+        const int nkeys = min(kStageKeys, t.kv_end - kv0);
+        const int nbox = (nkeys + BR - 1) / BR;
+        if ((kv0 + nkeys - 1) / p.bs - win0 >= 32) {  // the stage reaches into the next window
+            win0 += 32;
+            pg_win = pg_nxt;
+            pg_nxt = load_window(p, t.seq, win0 + 32, lane);
+        }
+        const int n_copies = nbox * 2;  // one box per (page, tensor), both column halves
+        const int b = lane % nbox;
+        int my_pg = __shfl_sync(0xffffffffu, pg_win, (kv0 + b * BR) / p.bs - win0);
+        if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
+            set_err(p.err, XY_DEV_PAGE_OOB);
+            my_pg = 0;
+        }
+        const uint32_t row_bytes = (uint32_t)p.G * HD * 2;  // one token's G query rows
+        const uint32_t q_bytes = first_stage ? (uint32_t)t.q_rows * row_bytes : 0u;
+        const uint32_t stage = sm.stages + s * RG::kStageBytes;
+        if (lane == 0)
+            mbar_arrive_expect_tx(sm.full_bar + 8 * s, (uint32_t)(n_copies * RG::kHalves * BR * 128) + q_bytes);
+        __syncwarp();
+        if (lane < n_copies) {
+            const int tensor = lane / nbox;
+            const int key = kv0 + b * BR;
+            const int y = (my_pg * p.Hkv + t.kv_head) * p.bs + (key % p.bs);
+            const uint32_t dst = stage + tensor * RG::kTensorBytes + b * RG::kHalves * BR * 128;
+            tma_load_3d(dst, tensor ? vmap : kmap, 0, y, 0, sm.full_bar + 8 * s);
+        }
+        if (first_stage) {
+            // the task's query rows: token j's G heads are one contiguous run of q
+            for (int j = lane; j < t.q_rows; j += 32) {
+                const int64_t tok = (int64_t)f.seq_start + t.q_start + j;
+                const __nv_bfloat16 *src = p.q + (tok * p.Hq + (int64_t)t.kv_head * p.G) * HD;
+                bulk_load(stage + 2 * RG::kTensorBytes + j * row_bytes, src, row_bytes, sm.full_bar + 8 * s);
+            }
+            first_stage = false;
+            first_stage_done();
+        }
+        __syncwarp();
+    }
+    return true;
+}
+
+// Math warp w (0..3) runs decode task `f`.  `ctr` counts stages consumed on the ring, `iter` the
+// tasks run (vote parity).  `first_stage_seen()` runs once, after the first stage has landed.
+// Returns false when the math warps voted to stop (a wait gave up); every math warp returns the
+// same value, and all of them pass the same named barriers.
+template <int HD, class RG, class F>
+__device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
+                             int lane, F first_stage_seen) {
+    const int g4 = lane >> 2, c4 = lane & 3;
+    const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;
+    const int br_sh = 31 - __clz(BR);
+    const xy_task t = f.t;
+    const int R = t.q_rows * p.G;
+    int nrg = (R + 15) >> 4;
+    if (nrg == 3) nrg = 4;
+    const int wpg = kMathWarps / nrg;  // warps sharing one 16-row slice
+    const int rg = w % nrg, ks = w / nrg;
+    const int row_a = rg * 16 + g4, row_b = row_a + 8;
+    const int qn = f.qn, L = f.L;
+
+    auto row_limit = [&](int r) -> int {
+        if (r >= R) return t.kv_end;  // padding rows: never stored, kept finite
+        const int lim = p.causal ? (L - qn + t.q_start + r / p.G + 1) : L;
+        return min(lim, t.kv_end);
+    };
+    const int lim_a = row_limit(row_a), lim_b = row_limit(row_b);
+    int lim_max = max(lim_a, lim_b);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, o));
+
+    // Q fragments (A operand, row-major 16 x HD) come from the first stage of the task, where the
+    // producer placed the task's rows in (token, head) order; rows past R are zero.
+    uint32_t qa[HD / 16][4];
+    float o_acc[HD / 8][4];
+#pragma unroll
+    for (int n = 0; n < HD / 8; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+    const int sub = kStageKeys / wpg;
+    bool ok = true;
+    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
+        const int s = ctr % RG::kStages;
+        if (!mbar_wait(sm.full_bar + 8 * s, (ctr / RG::kStages) & 1, sm.abort_flag)) {
+            ok = false;
+            break;
+        }
+        const uint32_t kst = sm.stages + s * RG::kStageBytes;
+        const uint32_t vst = kst + RG::kTensorBytes;
+        if (kv0 == t.kv_start) {
+            const uint8_t *qs = sm.stages_gen + s * RG::kStageBytes + 2 * RG::kTensorBytes;
+            const uint32_t *qa_ptr = row_a < R ? reinterpret_cast<const uint32_t *>(qs + row_a * HD * 2) : nullptr;
+            const uint32_t *qb_ptr = row_b < R ? reinterpret_cast<const uint32_t *>(qs + row_b * HD * 2) : nullptr;
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const int w0 = kk * 8 + c4, w1 = w0 + 4;  // 32-bit words: cols 16kk+2c and +8
+                qa[kk][0] = qa_ptr ? qa_ptr[w0] : 0u;
+                qa[kk][1] = qb_ptr ? qb_ptr[w0] : 0u;
+                qa[kk][2] = qa_ptr ? qa_ptr[w1] : 0u;
+                qa[kk][3] = qb_ptr ? qb_ptr[w1] : 0u;
+            }
+            first_stage_seen();
+        }
+
+        const int k_lo = kv0 + ks * sub;
+        const int k_hi = min(min(k_lo + sub, t.kv_end), lim_max);
+        for (int kc = k_lo; kc < k_hi; kc += 16) {
+            const int kr = kc - kv0;
+            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            {
+                const int mi = lane >> 3;
+                const int krow = kr + ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kst + swz<HD>(krow, kk * 16 + ((mi & 1) << 3), br_sh), b0, b1, b2, b3);
+                    mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                    mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                }
+            }
+            // virtual + causal mask, then online softmax in the log2 domain
+            float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = kc + 8 * j + 2 * c4 + e;
+                    sc[j][e] = key < lim_a ? sc[j][e] * p.scale_log2 : -INFINITY;
+                    sc[j][2 + e] = key < lim_b ? sc[j][2 + e] * p.scale_log2 : -INFINITY;
+                    mx_a = fmaxf(mx_a, sc[j][e]);
+                    mx_b = fmaxf(mx_b, sc[j][2 + e]);
+                }
+            }
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+            const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
+            const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
+            const float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
+            m_a = mn_a;
+            m_b = mn_b;
+            float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                sc[j][0] = ex2(sc[j][0] - mu_a);
+                sc[j][1] = ex2(sc[j][1] - mu_a);
+                sc[j][2] = ex2(sc[j][2] - mu_b);
+                sc[j][3] = ex2(sc[j][3] - mu_b);
+                ps_a += sc[j][0] + sc[j][1];
+                ps_b += sc[j][2] + sc[j][3];
+            }
+            l_a = l_a * al_a + ps_a;
+            l_b = l_b * al_b + ps_b;
+#pragma unroll
+            for (int n = 0; n < HD / 8; ++n) {
+                o_acc[n][0] *= al_a;
+                o_acc[n][1] *= al_a;
+                o_acc[n][2] *= al_b;
+                o_acc[n][3] *= al_b;
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+            pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+            pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+            pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+            // keys at or past kv_end may hold anything (unused slots, stale stage data): their
+            // weights are 0, and their V entries are zeroed so 0 * NaN cannot occur
+            const bool tail = kc + 16 > t.kv_end;
+            const int key_lo = kc + 2 * c4;
+            const uint32_t keep0 =
+                (key_lo < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 1 < t.kv_end ? 0xffff0000u : 0u);
+            const uint32_t keep1 =
+                (key_lo + 8 < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 9 < t.kv_end ? 0xffff0000u : 0u);
+            {
+                const int mi = lane >> 3;
+                const int vrow = kr + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int jd = 0; jd < HD / 16; ++jd) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vst + swz<HD>(vrow, 8 * (2 * jd + (mi >> 1)), br_sh), b0, b1, b2, b3);
+                    if (tail) {
+                        b0 &= keep0;
+                        b1 &= keep1;
+                        b2 &= keep0;
+                        b3 &= keep1;
+                    }
+                    mma_bf16_16816(o_acc[2 * jd], pa, b0, b1);
+                    mma_bf16_16816(o_acc[2 * jd + 1], pa, b2, b3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty_bar + 8 * s);
+    }
+
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+
+    if (wpg > 1) {
+        float *my = sm.slots + w * RG::kSlotFloats;
+#pragma unroll
+        for (int n = 0; n < HD / 8; ++n) {
+            const int col = 8 * n + 2 * c4;
+            *reinterpret_cast<float2 *>(my + g4 * HD + col) = make_float2(o_acc[n][0], o_acc[n][1]);
+            *reinterpret_cast<float2 *>(my + (g4 + 8) * HD + col) = make_float2(o_acc[n][2], o_acc[n][3]);
+        }
+        if (c4 == 0) {
+            my[16 * HD + g4] = m_a;
+            my[16 * HD + g4 + 8] = m_b;
+            my[16 * HD + 16 + g4] = l_a;
+            my[16 * HD + 16 + g4 + 8] = l_b;
+        }
+    }
+    // Every math warp reaches this barrier (all waits above are bounded), so the vote makes the
+    // decision to stop uniform and no warp is left waiting at a named barrier.
+    if (lane == 0) sm.vote[(iter & 1) * kMathWarps + w] = (!ok || *sm.abort_flag) ? 1 : 0;
+    named_bar_sync(sm.bar_id, kMathWarps * 32);
+    {
+        int bad = 0;
+        for (int v = 0; v < kMathWarps; ++v) bad |= sm.vote[(iter & 1) * kMathWarps + v];
+        ++iter;
+        if (bad) return false;
+    }
+    if (wpg > 1) {
+        if (ks == 0) {
+            float M_a = m_a, M_b = m_b;
+            for (int k = 1; k < wpg; ++k) {
+                const float *ot = sm.slots + (rg + k * nrg) * RG::kSlotFloats;
+                M_a = fmaxf(M_a, ot[16 * HD + g4]);
+                M_b = fmaxf(M_b, ot[16 * HD + g4 + 8]);
+            }
+            const float U_a = M_a == -INFINITY ? 0.f : M_a, U_b = M_b == -INFINITY ? 0.f : M_b;
+            const float f_a = ex2(m_a - U_a), f_b = ex2(m_b - U_b);
+            l_a *= f_a;
+            l_b *= f_b;
+#pragma unroll
+            for (int n = 0; n < HD / 8; ++n) {
+                o_acc[n][0] *= f_a;
+                o_acc[n][1] *= f_a;
+                o_acc[n][2] *= f_b;
+                o_acc[n][3] *= f_b;
+            }
+            for (int k = 1; k < wpg; ++k) {
+                const float *ot = sm.slots + (rg + k * nrg) * RG::kSlotFloats;
+                const float ga = ex2(ot[16 * HD + g4] - U_a), gb = ex2(ot[16 * HD + g4 + 8] - U_b);
+                l_a += ga * ot[16 * HD + 16 + g4];
+                l_b += gb * ot[16 * HD + 16 + g4 + 8];
+#pragma unroll
+                for (int n = 0; n < HD / 8; ++n) {
+                    const int col = 8 * n + 2 * c4;
+                    const float2 xa = *reinterpret_cast<const float2 *>(ot + g4 * HD + col);
+                    const float2 xb = *reinterpret_cast<const float2 *>(ot + (g4 + 8) * HD + col);
+                    o_acc[n][0] += ga * xa.x;
+                    o_acc[n][1] += ga * xa.y;
+                    o_acc[n][2] += gb * xb.x;
+                    o_acc[n][3] += gb * xb.y;
+                }
+            }
+            m_a = M_a;
+            m_b = M_b;
+        }
+        named_bar_sync(sm.bar_id, kMathWarps * 32);
+    }
+    if (ks != 0) return true;
+
+    // store: the final bf16 rows, or this chunk's normalised partial + log2-sum-exp
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int r = half ? row_b : row_a;
+        if (r >= R) continue;
+        const float l = half ? l_b : l_a, m = half ? m_b : m_a;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (t.num_splits == 1) {
+            const int64_t tok = f.seq_start + t.q_start + r / p.G;
+            const int h = t.kv_head * p.G + r % p.G;
+            __nv_bfloat16 *dst = p.out + (tok * p.Hq + h) * HD;
+#pragma unroll
+            for (int n = 0; n < HD / 8; ++n) {
+                const float x0 = o_acc[n][2 * half] * inv, x1 = o_acc[n][2 * half + 1] * inv;
+                *reinterpret_cast<uint32_t *>(dst + 8 * n + 2 * c4) = pack_bf16x2(x0, x1);
+            }
+        } else {
+            const int64_t wr = (int64_t)t.ws_row + r;
+            float *dst = p.ws_o + wr * HD;
+#pragma unroll
+            for (int n = 0; n < HD / 8; ++n)
+                *reinterpret_cast<float2 *>(dst + 8 * n + 2 * c4) =
+                    make_float2(o_acc[n][2 * half] * inv, o_acc[n][2 * half + 1] * inv);
+            if (c4 == 0) p.ws_lse[wr] = l > 0.f ? m + __log2f(l) : -INFINITY;
+        }
+    }
+    return true;
+}
+
+}  // namespace dec
+}  // namespace xy

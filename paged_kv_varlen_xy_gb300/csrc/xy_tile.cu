@@ -33,6 +33,7 @@
 
 #include "xy.h"
 #include "xy_attn_common.cuh"
+#include "xy_decode_path.cuh"
 #include "xy_device.cuh"
 
 namespace {
@@ -40,6 +41,7 @@ namespace {
 using xy::AttnParams;
 using xy::ex2;
 using xy::fetch_info;
+using xy::TaskCursor;
 using xy::TaskInfo;
 
 constexpr int HD = 128;
@@ -64,10 +66,19 @@ enum {
     B_DONE = B_OFREE0 + 2,
     B_COUNT
 };
+// The decode path (tasks of at most XY_TILE_MIN_ROWS rows, xy_decode_path.cuh) uses the same
+// bytes: its stage ring from offset 0 and its merge slots after it.  A switch of task kind waits
+// until the other kind's consumers are done with shared memory.
+using DecRing = xy::dec::Ring<HD, 4, 16>;
+static_assert(XY_TILE_MIN_ROWS <= 16, "decode-path tasks of the unified kernel have at most 16 rows");
+constexpr int kDecStagesOff = 0;
+constexpr int kDecSlotsOff = DecRing::kBytes;
 constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
-constexpr int kMiscOff = kBarOff + B_COUNT * 8;     // TMEM base address, abort flag
-constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp
-constexpr int kSmemBytes = kVoteOff + 64 + 1024;
+static_assert(kDecSlotsOff + DecRing::kSlotBytes <= kBarOff, "decode path fits in the tile path's bytes");
+constexpr int kDecBarOff = kBarOff + B_COUNT * 8;    // decode ring full[4], empty[4], task-done
+constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 1) * 8;  // TMEM base address, abort flag
+constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp, then 2 x 4 decode votes
+constexpr int kSmemBytes = kVoteOff + 64 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
@@ -81,44 +92,12 @@ __device__ __forceinline__ bool tile_ok(const TaskInfo &f, const AttnParams &p) 
     return xy::task_common_ok(f, p) && f.t.q_rows * p.G <= 256 && (f.t.kv_start % kTileKeys) == 0;
 }
 
-// Walks this CTA's tasks (blockIdx.x, +gridDim.x, ...), fetching the next task's record and
-// per-sequence numbers while the current one runs.
-struct TaskCursor {
-    int ti;
-    bool have, have_next, nxt_ready;
-    TaskInfo cur, nxt;
-    xy_task rec_next;
-
-    __device__ void begin(const AttnParams &p) {
-        ti = blockIdx.x;
-        have = ti < p.num_tasks;
-        if (have) cur = fetch_info(p.tasks[ti], p);
-    }
-    __device__ void load_next_record(const AttnParams &p) {
-        const int tn = ti + gridDim.x;
-        have_next = tn < p.num_tasks;
-        if (have_next) rec_next = p.tasks[tn];
-        nxt_ready = false;
-    }
-    __device__ void prefetch_next(const AttnParams &p) {
-        if (have_next && !nxt_ready) {
-            nxt = fetch_info(rec_next, p);
-            nxt_ready = true;
-        }
-    }
-    __device__ void advance(const AttnParams &p) {
-        prefetch_next(p);
-        cur = nxt;
-        ti += gridDim.x;
-        have = have_next;
-    }
-};
-
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    tile_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                          const __grid_constant__ CUtensorMap qmap, const AttnParams p) {
+    meta_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                          const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_d,
+                          const __grid_constant__ CUtensorMap vmap_d, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = xy::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -128,6 +107,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff + 4);
     volatile int *vote = reinterpret_cast<volatile int *>(gbase + kVoteOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    xy::dec::Smem dsm;
+    dsm.stages = base + kDecStagesOff;
+    dsm.stages_gen = gbase + kDecStagesOff;
+    dsm.slots = reinterpret_cast<float *>(gbase + kDecSlotsOff);
+    dsm.full_bar = base + kDecBarOff;
+    dsm.empty_bar = dsm.full_bar + DecRing::kStages * 8;
+    dsm.abort_flag = abort_flag;
+    dsm.vote = vote + 16;
+    dsm.bar_id = 3;
+    const uint32_t dec_done = base + kDecBarOff + 8 * (2 * DecRing::kStages);  // one per decode task
 
     if (threadIdx.x == 0) {
         xy::mbar_init(bar(B_QFULL), 1);
@@ -143,6 +132,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             xy::mbar_init(bar(B_OFREE0 + x), 4);
         }
         xy::mbar_init(bar(B_DONE), 1);
+        for (int st = 0; st < DecRing::kStages; ++st) {
+            xy::mbar_init(base + kDecBarOff + 8 * st, 1);
+            xy::mbar_init(base + kDecBarOff + 8 * (DecRing::kStages + st), xy::dec::kMathWarps);
+        }
+        xy::mbar_init(base + kDecBarOff + 8 * (2 * DecRing::kStages), xy::dec::kMathWarps);
         *abort_flag = 0;
         xy::fence_mbarrier_init();
     }
@@ -163,12 +157,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             xy::prefetch_tensormap(&kmap);
             xy::prefetch_tensormap(&vmap);
             xy::prefetch_tensormap(&qmap);
+            xy::prefetch_tensormap(&kmap_d);
+            xy::prefetch_tensormap(&vmap_d);
         }
         auto load_win = [&](const int32_t *row, int b0) -> int {
             const int idx = b0 + lane;
             return (idx >= 0 && idx < p.MB) ? __ldg(row + idx) : -1;
         };
-        int c = 0, qk = 0;
+        int c = 0, qk = 0;          // tile path: ring slot uses, tasks
+        int dctr = 0, nd = 0;       // decode path: stages issued, tasks
+        int last_kind = 0;          // 1 tile, 2 decode
         bool ok = true;
         int pref_win = -1;
         bool pref_valid = false;
@@ -176,13 +174,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
-            bool run = mine(tc.cur, p);
-            if (run && !tile_ok(tc.cur, p)) {
+            const bool tile = mine(tc.cur, p);
+            if (!(tile ? tile_ok(tc.cur, p) : xy::dec::task_ok<DecRing>(tc.cur, p))) {
                 if (lane == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
-                run = false;
-            }
-            if (!run) {
                 pref_valid = false;
+                tc.advance(p);
+                continue;
+            }
+            const int kind = tile ? 1 : 2;
+            if (last_kind != 0 && kind != last_kind) {
+                // The two paths share shared memory: before writing it for the other kind, wait
+                // until the consumers of the previous kind are done with it.
+                bool w = true;
+                if (last_kind == 1) {  // the last tile task's MMAs have read Q and every slot
+                    w = xy::mbar_wait(bar(B_QEMPTY), (qk - 1) & 1, abort_flag);
+                    for (int k = c - 1; w && k >= 0 && k >= c - kSlots; --k)
+                        w = xy::mbar_wait(bar(B_EMPTY0 + k % kSlots), (k / kSlots) & 1, abort_flag);
+                } else {  // the math warps have finished the last decode task (merge slots included)
+                    w = xy::mbar_wait(dec_done, (nd - 1) & 1, abort_flag);
+                }
+                if (!warp_all(w)) {
+                    ok = false;
+                    break;
+                }
+            }
+            last_kind = kind;
+            if (!tile) {
+                const TaskInfo f = tc.cur;
+                const bool have_first = pref_valid;
+                pref_valid = false;
+                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, dsm, dctr, lane, pref_win, have_first,
+                                                        [&]() {
+                                                            tc.prefetch_next(p);
+                                                            if (tc.have_next) {
+                                                                const xy_task &tn = tc.nxt.t;
+                                                                pref_valid = tn.seq >= 0 && tn.seq < p.S && tn.kv_start >= 0;
+                                                                if (pref_valid)
+                                                                    pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
+                                                            }
+                                                        });
+                ++nd;
                 tc.advance(p);
                 continue;
             }
@@ -262,6 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = c - 1; k >= 0 && k >= c - kSlots; --k)
             xy::mbar_wait(bar(B_FULL0 + k % kSlots), (k / kSlots) & 1);
         if (qk > 0) xy::mbar_wait(bar(B_QFULL), (qk - 1) & 1);
+        for (int k = dctr - 1; k >= 0 && k >= dctr - DecRing::kStages; --k)
+            xy::mbar_wait(dsm.full_bar + 8 * (k % DecRing::kStages), (k / DecRing::kStages) & 1);
     } else if (warp == kMmaWarp) {
         // ---------------------------------- MMA issuer ----------------------------------
         if (lane == 0) {
@@ -369,12 +402,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_addr = tbase + lane_off + x * 128;
         const uint32_t o_addr = tbase + lane_off + kTmemO + x * 128;
         int c = 0, qk = 0, ns = 0;   // ns: tiles this group has processed (= its S and PV count)
+        int dctr = 0, diter = 0;     // decode path (warps 0..3): stages consumed, tasks run
         bool ok = true;
         TaskCursor tc;
         tc.begin(p);
         while (tc.have) {
             tc.load_next_record(p);
-            if (!mine(tc.cur, p) || !tile_ok(tc.cur, p)) {
+            if (!mine(tc.cur, p)) {
+                // a decode-path task: warps 0..3 are its math warps, warps 4..7 sit it out
+                if (warp < 4 && xy::dec::task_ok<DecRing>(tc.cur, p)) {
+                    const TaskInfo f = tc.cur;
+                    if (!xy::dec::consume_task<HD, DecRing>(p, f, dsm, dctr, diter, warp, lane,
+                                                            [&]() { tc.prefetch_next(p); })) {
+                        *abort_flag = 1;
+                        if (warp == 0 && lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
+                        break;
+                    }
+                    __syncwarp();
+                    if (lane == 0) xy::mbar_arrive(dec_done);
+                }
+                tc.advance(p);
+                continue;
+            }
+            if (!tile_ok(tc.cur, p)) {
                 tc.advance(p);
                 continue;
             }
@@ -382,7 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const xy_task t = f.t;
             const int R = t.q_rows * p.G;
             const int n = (t.kv_end - t.kv_start + kTileKeys - 1) / kTileKeys;
-            const bool active = x == 0 || R > 128;  // tile B exists only for tasks with > 128 rows
+            // tile B exists only for tasks with more than 128 rows; a warp whose 32 rows are all
+            // padding does no softmax work (its P and O rows are never stored; rows of an MMA are
+            // independent, so whatever its TMEM lanes hold cannot reach a real row)
+            const bool active = x == 0 || R > 128;
+            const bool rows_on = active && (row - lane) < R;
             const bool valid = row < R;
             const int lim = valid ? min(t.kv_end, p.causal ? f.L - f.qn + t.q_start + row / p.G + 1 : f.L) : t.kv_end;
             float m = -INFINITY, l = 0.f;
@@ -394,97 +448,99 @@ __global__ void __launch_bounds__(kThreads, 1)
                     xy::tc_fence_after();
                     if (j == 0) tc.prefetch_next(p);
                     const int kt0 = t.kv_start + j * kTileKeys;
+                    if (rows_on) {
                     // a warp whose rows all see the whole tile skips the per-key mask
-                    const bool full = __all_sync(0xffffffffu, kt0 + kTileKeys <= lim);
-                    // pass 1: masked row max; 32-column TMEM loads, the next one in flight while
-                    // the current one is reduced
-                    uint32_t ca[32], cb[32];
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    auto max_chunk = [&](const uint32_t (&r)[32], int c0) {
-                        if (full) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 8) {
-                                m4[0] = xy::max3(m4[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                                m4[1] = xy::max3(m4[1], __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                                m4[2] = xy::max3(m4[2], __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-                                m4[3] = xy::max3(m4[3], __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                        const bool full = __all_sync(0xffffffffu, kt0 + kTileKeys <= lim);
+                        // pass 1: masked row max; 32-column TMEM loads, the next one in flight while
+                        // the current one is reduced
+                        uint32_t ca[32], cb[32];
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                        auto max_chunk = [&](const uint32_t (&r)[32], int c0) {
+                            if (full) {
+    #pragma unroll
+                                for (int i = 0; i < 32; i += 8) {
+                                    m4[0] = xy::max3(m4[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                                    m4[1] = xy::max3(m4[1], __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                                    m4[2] = xy::max3(m4[2], __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                                    m4[3] = xy::max3(m4[3], __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                                }
+                            } else {
+    #pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
                             }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
-                        }
-                    };
-                    xy::tmem_ld32_nowait(s_addr, ca);
-                    xy::tmem_wait_ld(ca);
-                    xy::tmem_ld32_nowait(s_addr + 32, cb);
-                    max_chunk(ca, 0);
-                    xy::tmem_wait_ld(cb);
-                    xy::tmem_ld32_nowait(s_addr + 64, ca);
-                    max_chunk(cb, 32);
-                    xy::tmem_wait_ld(ca);
-                    xy::tmem_ld32_nowait(s_addr + 96, cb);
-                    max_chunk(ca, 64);
-                    xy::tmem_wait_ld(cb);
-                    xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
-                    max_chunk(cb, 96);
-                    const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                    const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
-                    const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
-                    xy::tmem_wait_ld(ca);
-                    if (rescale) {
-                        const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
-                        m = m_new;
-                        l *= alpha;
-                        if (j > 0) {  // O_X has PV_X(0..j-1); rescale once the last of them is done
-                            ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
-                            xy::tc_fence_after();
-#pragma unroll 1
-                            for (int h = 0; h < 4; ++h) {
-                                uint32_t orow[32];
-                                xy::tmem_ld32(o_addr + h * 32, orow);
-#pragma unroll
-                                for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                                xy::tmem_st32(o_addr + h * 32, orow);
+                        };
+                        xy::tmem_ld32_nowait(s_addr, ca);
+                        xy::tmem_wait_ld(ca);
+                        xy::tmem_ld32_nowait(s_addr + 32, cb);
+                        max_chunk(ca, 0);
+                        xy::tmem_wait_ld(cb);
+                        xy::tmem_ld32_nowait(s_addr + 64, ca);
+                        max_chunk(cb, 32);
+                        xy::tmem_wait_ld(ca);
+                        xy::tmem_ld32_nowait(s_addr + 96, cb);
+                        max_chunk(ca, 64);
+                        xy::tmem_wait_ld(cb);
+                        xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
+                        max_chunk(cb, 96);
+                        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                        const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
+                        const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
+                        xy::tmem_wait_ld(ca);
+                        if (rescale) {
+                            const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
+                            m = m_new;
+                            l *= alpha;
+                            if (j > 0) {  // O_X has PV_X(0..j-1); rescale once the last of them is done
+                                ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
+                                xy::tc_fence_after();
+    #pragma unroll 1
+                                for (int h = 0; h < 4; ++h) {
+                                    uint32_t orow[32];
+                                    xy::tmem_ld32(o_addr + h * 32, orow);
+    #pragma unroll
+                                    for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                                    xy::tmem_st32(o_addr + h * 32, orow);
+                                }
                             }
                         }
+                        // pass 2: p = 2^(s * scale_log2 - m) for 32 columns at a time, packed to bf16
+                        // pairs and written over S columns that pass 2 has already read
+                        const float neg_mu = m == -INFINITY ? 0.f : -m;
+                        const uint64_t sc2 = xy::f2_pack(p.scale_log2, p.scale_log2), nm2 = xy::f2_pack(neg_mu, neg_mu);
+                        uint64_t acc2[2] = {0ull, 0ull};
+                        auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
+                            uint32_t pk[16];
+    #pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+                                if (!full) {
+                                    s0 = kt0 + c0 + 2 * i < lim ? s0 : -INFINITY;
+                                    s1 = kt0 + c0 + 2 * i + 1 < lim ? s1 : -INFINITY;
+                                }
+                                float e0, e1;
+                                xy::f2_unpack(xy::f2_fma(xy::f2_pack(s0, s1), sc2, nm2), e0, e1);
+                                const float p0 = ex2(e0), p1 = ex2(e1);
+                                acc2[i & 1] = xy::f2_add(acc2[i & 1], xy::f2_pack(p0, p1));
+                                pk[i] = xy::pack_bf16x2(p0, p1);
+                            }
+                            xy::tmem_st16(s_addr + 16 * chunk, pk);
+                        };
+                        xy::tmem_ld32_nowait(s_addr + 32, cb);
+                        exp_chunk(ca, 0, 0);
+                        xy::tmem_wait_ld(cb);
+                        xy::tmem_ld32_nowait(s_addr + 64, ca);
+                        exp_chunk(cb, 32, 1);
+                        xy::tmem_wait_ld(ca);
+                        xy::tmem_ld32_nowait(s_addr + 96, cb);
+                        exp_chunk(ca, 64, 2);
+                        xy::tmem_wait_ld(cb);
+                        exp_chunk(cb, 96, 3);
+                        float ls4[4];
+                        xy::f2_unpack(acc2[0], ls4[0], ls4[1]);
+                        xy::f2_unpack(acc2[1], ls4[2], ls4[3]);
+                        l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                     }
-                    // pass 2: p = 2^(s * scale_log2 - m) for 32 columns at a time, packed to bf16
-                    // pairs and written over S columns that pass 2 has already read
-                    const float neg_mu = m == -INFINITY ? 0.f : -m;
-                    const uint64_t sc2 = xy::f2_pack(p.scale_log2, p.scale_log2), nm2 = xy::f2_pack(neg_mu, neg_mu);
-                    uint64_t acc2[2] = {0ull, 0ull};
-                    auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-                            if (!full) {
-                                s0 = kt0 + c0 + 2 * i < lim ? s0 : -INFINITY;
-                                s1 = kt0 + c0 + 2 * i + 1 < lim ? s1 : -INFINITY;
-                            }
-                            float e0, e1;
-                            xy::f2_unpack(xy::f2_fma(xy::f2_pack(s0, s1), sc2, nm2), e0, e1);
-                            const float p0 = ex2(e0), p1 = ex2(e1);
-                            acc2[i & 1] = xy::f2_add(acc2[i & 1], xy::f2_pack(p0, p1));
-                            pk[i] = xy::pack_bf16x2(p0, p1);
-                        }
-                        xy::tmem_st16(s_addr + 16 * chunk, pk);
-                    };
-                    xy::tmem_ld32_nowait(s_addr + 32, cb);
-                    exp_chunk(ca, 0, 0);
-                    xy::tmem_wait_ld(cb);
-                    xy::tmem_ld32_nowait(s_addr + 64, ca);
-                    exp_chunk(cb, 32, 1);
-                    xy::tmem_wait_ld(ca);
-                    xy::tmem_ld32_nowait(s_addr + 96, cb);
-                    exp_chunk(ca, 64, 2);
-                    xy::tmem_wait_ld(cb);
-                    exp_chunk(cb, 96, 3);
-                    float ls4[4];
-                    xy::f2_unpack(acc2[0], ls4[0], ls4[1]);
-                    xy::f2_unpack(acc2[1], ls4[2], ls4[3]);
-                    l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                     if (x == 0 && kt0 + kTileKeys > t.kv_end) {
                         // keys at or past kv_end: unused page slots or stale data; their P is 0 and
                         // their V rows are zeroed (group A, before both tiles' PV of this K/V tile)
@@ -508,8 +564,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) xy::mbar_arrive(bar(B_PFULL0 + x));
                     ++ns;
                 }
-                ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
-                xy::tc_fence_after();
+                if (rows_on) {
+                    ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
+                    xy::tc_fence_after();
+                }
             }
             // the group's vote on whether to go on
             if (lane == 0) vote[warp] = ok ? 0 : 1;
@@ -517,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int bad = 0;
 #pragma unroll
             for (int w = 0; w < 4; ++w) bad |= vote[x * 4 + w];
-            if (active) {
+            if (rows_on) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
                 for (int cc = 0; cc < 4; ++cc) {
@@ -548,6 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (valid && !bad && t.num_splits > 1) p.ws_lse[(int64_t)t.ws_row + row] = l > 0.f ? m + __log2f(l) : -INFINITY;
+            }
+            if (active) {
                 xy::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) xy::mbar_arrive(bar(B_OFREE0 + x));
@@ -595,8 +655,9 @@ namespace xy {
 
 void set_last_error(const char *what, const char *msg);
 
-xy_status launch_tile_attention(const AttnParams &p, const void *k_pages, const void *v_pages, int num_pages,
-                                int block_size, int num_ctas, cudaStream_t st) {
+xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const void *v_pages, int num_pages,
+                                int block_size, int num_ctas, const CUtensorMap &kmap_d, const CUtensorMap &vmap_d,
+                                cudaStream_t st) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return XY_ERR_CUDA;
     const int64_t rows = (int64_t)num_pages * p.Hkv * block_size;
@@ -630,13 +691,13 @@ xy_status launch_tile_attention(const AttnParams &p, const void *k_pages, const 
     if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
     if (configured_device != dev) {
         const cudaError_t e =
-            cudaFuncSetAttribute(tile_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return cuda_fail(e, "tile_attention_kernel smem attribute");
+            cudaFuncSetAttribute(meta_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e, "meta_attention_kernel smem attribute");
         configured_device = dev;
     }
-    tile_attention_kernel<<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, p);
+    meta_attention_kernel<<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
     const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? XY_OK : cuda_fail(e, "tile_attention_kernel launch");
+    return e == cudaSuccess ? XY_OK : cuda_fail(e, "meta_attention_kernel launch");
 }
 
 }  // namespace xy
