@@ -155,6 +155,15 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  * [0, L_i) or, if causal, [0, L_i - q_i + q_start + q_rows); stable-sorts by load, largest first;
  * CTA c of the persistent launch runs tasks[c], tasks[c + num_ctas], ...  Split tiles
  * (num_splits > 1) get workspace rows in enumeration order and one xy_merge each.
+ * schedule: XY_SCHEDULE_AREA follows the pages exactly.  XY_SCHEDULE_MIXED is a variant for
+ * batches that mix HBM-bound decode tasks with tensor-core tiles: a task is charged
+ * 128 * max(1, ceil(rows / 128)) * keys (a tile costs its padded 128-row MMA area; a task of at most
+ * XY_SCHEDULE_SMALL_ROWS rows streams its KV in about the time of one such tile), sorted and dealt
+ * the same way; then each CTA interleaves its small and large tasks in proportion to their charged
+ * loads, CTA c starting at phase c / num_ctas, so that at any time about the small tasks' share of
+ * the CTAs streams KV from HBM while the others keep the tensor cores busy.  The per-CTA load sums
+ * (stats) are those of the deal.  Returns XY_ERR_UNSUPPORTED when the total charged load
+ * reaches 2^55 or num_ctas exceeds 65536.
  *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs]: host int32.
  *   tasks [max_tasks], merges [max_merges]: host outputs; pass NULL (with max 0) to query counts.
  *   *num_tasks, *num_merges: counts; *workspace_bytes = rows * (head_dim + 1) * 4 (fp32 partial
@@ -162,9 +171,14 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  * Errors: XY_ERR_INVALID_ARG (sizes <= 0, Hq % Hkv), XY_ERR_CU_SEQLENS,
  *   XY_ERR_CONTEXT_LT_QLEN, XY_ERR_CAPACITY (non-NULL arrays too small).
  */
+#define XY_SCHEDULE_AREA 0        /* the pages' reorder: load = area, sort, round-robin deal */
+#define XY_SCHEDULE_MIXED 1       /* padded-tile load, sort, deal, per-CTA proportional interleave */
+#define XY_SCHEDULE_TILE_ROWS 128 /* MMA tile height: the unit of XY_SCHEDULE_MIXED's load */
+#define XY_SCHEDULE_SMALL_ROWS 16 /* tasks of at most this many rows count as small */
+
 xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
                               int num_seqs, int num_heads_q, int num_heads_kv, int head_dim,
-                              int causal, int num_ctas, int q_tile, int kv_chunk,
+                              int causal, int num_ctas, int q_tile, int kv_chunk, int schedule,
                               xy_task *tasks, int max_tasks, int *num_tasks,
                               xy_merge *merges, int max_merges, int *num_merges,
                               size_t *workspace_bytes, xy_task_stats *stats);

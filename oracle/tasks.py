@@ -22,19 +22,62 @@ Readings taken here (the pages are written for 16 x 16 Ascend blocks):
   ws_row and chunk c owns rows ws_row + c * q_rows * G + t * G + h_local.
 """
 
+from fractions import Fraction
+
 import numpy as np
 
 TASK_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "kv_start", "kv_end", "num_splits", "ws_row")
 MERGE_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "num_splits", "ws_row", "zero0", "zero1")
 
 
+# schedule 1 (a variant of the pages' reorder for batches that mix HBM-bound decode tasks with
+# tensor-core tiles; the pages' load is the plain area):
+# * charged load = TILE_ROWS * max(1, ceil(rows / TILE_ROWS)) * keys: a tile costs its padded
+#   128-row MMA area, and a small task (rows <= SMALL_ROWS) streams its keys' KV in about the
+#   time of one 128-row tile over the same keys;
+# * the same stable sort and round-robin deal;
+# * each CTA then interleaves its small and large tasks in proportion to their charged loads,
+#   starting at phase c / num_ctas of its timeline, so that at any moment about the small tasks'
+#   share of the CTAs streams KV while the others keep the tensor cores busy.
+SMALL_ROWS = 16
+TILE_ROWS = 128
+MAX_TOTAL_LOAD = 1 << 55
+MAX_CTAS = 1 << 16
+
+
+def _charged_rows(rows):
+    return TILE_ROWS * max(1, -(-rows // TILE_ROWS))
+
+
+def _interleave(big, small, c, num_ctas):
+    """Order one CTA's tasks.  big / small: lists of (task, load) in dealt order.  Each task gets
+    the key (start of the task within its own list + phase) mod 1, where start = loads before it /
+    the list's total and phase = c / num_ctas; tasks run by increasing key, a large task first
+    on a tie.  Exact rational arithmetic (Python integers)."""
+    if not big or not small:
+        return [t for t, _ in big] + [t for t, _ in small]
+    keyed = []
+    for kind, lst in ((0, big), (1, small)):
+        tot = sum(ld for _, ld in lst)
+        done = 0
+        for t, ld in lst:
+            keyed.append(((Fraction(done, tot) + Fraction(c, num_ctas)) % 1, kind, t))
+            done += ld
+    keyed.sort(key=lambda x: (x[0], x[1]))
+    return [t for _, _, t in keyed]
+
+
 def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
-                     num_ctas, q_tile, kv_chunk):
+                     num_ctas, q_tile, kv_chunk, schedule=0):
     """Return dict(tasks=int32 [n, 8] in dealt order, merges=int32 [m, 8], loads=int64 [n],
     cta_loads=int64 [num_ctas], balance=min/max, workspace_bytes=int).
 
     CTA c runs tasks c, c + num_ctas, c + 2*num_ctas, ... of ``tasks``.
+    schedule 0: the pages' reorder (load = area, stable sort descending, round-robin deal).
+    schedule 1: the charged load and per-CTA proportional interleave described above.
     """
+    if schedule not in (0, 1):
+        raise ValueError("schedule must be 0 or 1")
     if num_heads_q % num_heads_kv:
         raise ValueError("Hq must be a multiple of Hkv")
     if q_tile < 1 or kv_chunk < 1 or num_ctas < 1:
@@ -65,9 +108,22 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
                     k1 = min(kv_hi, k0 + kv_chunk)
                     row = -1 if nsplit == 1 else base + c * rows * G
                     records.append((i, g, t0, rows, k0, k1, nsplit, row))
-                    loads.append(rows * G * (k1 - k0))
+                    r = rows * G
+                    if schedule == 1:
+                        r = _charged_rows(r)
+                    loads.append(r * (k1 - k0))
 
     order = sorted(range(len(records)), key=lambda k: loads[k], reverse=True)
+    if schedule == 1:
+        if sum(loads) >= MAX_TOTAL_LOAD or num_ctas > MAX_CTAS:
+            raise ValueError("total load or num_ctas too large for schedule 1")
+        # positions c, c + num_ctas, ... belong to CTA c; reorder each CTA's tasks among them
+        for c in range(min(num_ctas, len(order))):
+            pos = list(range(c, len(order), num_ctas))
+            big = [(k, loads[k]) for k in (order[q] for q in pos) if records[k][3] * G > SMALL_ROWS]
+            small = [(k, loads[k]) for k in (order[q] for q in pos) if records[k][3] * G <= SMALL_ROWS]
+            for q, k in zip(pos, _interleave(big, small, c, num_ctas)):
+                order[q] = k
     tasks = np.array([records[k] for k in order], dtype=np.int32).reshape(-1, 8)
     sorted_loads = np.array([loads[k] for k in order], dtype=np.int64)
 

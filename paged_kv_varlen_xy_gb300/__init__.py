@@ -78,7 +78,7 @@ def lib():
     L.xy_slot_mapping.restype = I
     L.xy_kv_append.argtypes = [P, P, P, I, P, P, I, I, I, I, P, P]
     L.xy_kv_append.restype = I
-    L.xy_build_task_table.argtypes = [P, P, I, I, I, I, I, I, I, I, P, I, P, P, I, P, P, P]
+    L.xy_build_task_table.argtypes = [P, P, I, I, I, I, I, I, I, I, I, P, I, P, P, I, P, P, P]
     L.xy_build_task_table.restype = I
     L.xy_paged_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P, P, P]
     L.xy_paged_attention.restype = I
@@ -144,14 +144,18 @@ def xy_build_block_table(context_lens, block_size, free_list, max_blocks):
     return table, used.value
 
 
+XY_SCHEDULE_AREA = 0
+XY_SCHEDULE_MIXED = 1
+
+
 def xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, num_ctas,
-                        q_tile, kv_chunk):
+                        q_tile, kv_chunk, schedule=XY_SCHEDULE_AREA):
     """a4 (host): returns dict(tasks [n,8] int32, merges [m,8] int32, workspace_bytes, stats)."""
     cu, pcu = _host_i32(cu_seqlens_q)
     ctx, pctx = _host_i32(context_lens)
     S = len(cu) - 1
     args = (pcu, pctx, S, int(num_heads_q), int(num_heads_kv), int(head_dim), int(bool(causal)), int(num_ctas),
-            int(q_tile), int(kv_chunk))
+            int(q_tile), int(kv_chunk), int(schedule))
     n, m, ws = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
     L = lib()
     _check(L.xy_build_task_table(*args, None, 0, ctypes.byref(n), None, 0, ctypes.byref(m), ctypes.byref(ws), None),
@@ -263,14 +267,15 @@ class Plan:
     cu_seqlens_q and context_lens) uploaded to the device, and the workspace it needs."""
 
     def __init__(self, cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, device="cuda",
-                 num_ctas=None, q_tile=None, kv_chunk=None):
+                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=XY_SCHEDULE_MIXED):
         import torch
         dev = torch.device(device)
         self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)
         dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim)
         self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
+        self.schedule = schedule
         r = xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
-                                self.num_ctas, self.q_tile, self.kv_chunk)
+                                self.num_ctas, self.q_tile, self.kv_chunk, schedule)
         self.host = r
         self.stats = r["stats"]
         self.tasks = torch.from_numpy(r["tasks"]).to(dev)

@@ -75,12 +75,51 @@ struct Rec {
 };
 }  // namespace
 
+// XY_SCHEDULE_MIXED, per CTA: the tasks at positions c, c + num_ctas, ... split into large
+// (rows > XY_SCHEDULE_SMALL_ROWS) and small ones, each list in dealt order.  A task's key is
+// (its start within its own list + phase) mod 1, with start = charged loads before it / the list's
+// total and phase = c / num_ctas; tasks run by increasing key, a large task first on a tie.  The
+// keys are compared exactly as fractions over the common denominator big_total * small_total *
+// num_ctas (128-bit products; total load < 2^55 and num_ctas <= 2^16 keep them below 2^126).
+static void interleave_cta(const std::vector<Rec> &recs, size_t c, size_t num_ctas, int G,
+                           std::vector<Rec> &out) {
+    using u128 = unsigned __int128;
+    struct Item {
+        u128 key;
+        int kind;
+        size_t pos;
+    };
+    const size_t n = recs.size();
+    uint64_t tot[2] = {0, 0};
+    for (size_t q = c; q < n; q += num_ctas)
+        tot[(int64_t)recs[q].t.q_rows * G > XY_SCHEDULE_SMALL_ROWS ? 0 : 1] += (uint64_t)recs[q].load;
+    out.clear();
+    if (tot[0] == 0 || tot[1] == 0) {
+        for (size_t q = c; q < n; q += num_ctas) out.push_back(recs[q]);
+        return;
+    }
+    std::vector<Item> items;
+    uint64_t done[2] = {0, 0};
+    for (size_t q = c; q < n; q += num_ctas) {
+        const int kind = (int64_t)recs[q].t.q_rows * G > XY_SCHEDULE_SMALL_ROWS ? 0 : 1;
+        // numerator over tot[kind] * num_ctas, then scaled by the other list's total
+        const u128 span = (u128)tot[kind] * num_ctas;
+        const u128 num = ((u128)done[kind] * num_ctas + (u128)c * tot[kind]) % span;
+        items.push_back({num * tot[1 - kind], kind, q});
+        done[kind] += (uint64_t)recs[q].load;
+    }
+    std::stable_sort(items.begin(), items.end(), [](const Item &a, const Item &b) {
+        return a.key != b.key ? a.key < b.key : a.kind < b.kind;
+    });
+    for (const Item &it : items) out.push_back(recs[it.pos]);
+}
+
 // a4: decomposer + reorder.  Enumeration order sequence -> KV head -> query tile -> KV chunk;
 // stable sort by load, largest first; task at sorted position p belongs to CTA p % num_ctas.
 extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
                                          int num_seqs, int num_heads_q, int num_heads_kv,
                                          int head_dim, int causal, int num_ctas, int q_tile,
-                                         int kv_chunk, xy_task *tasks, int max_tasks,
+                                         int kv_chunk, int schedule, xy_task *tasks, int max_tasks,
                                          int *num_tasks, xy_merge *merges, int max_merges,
                                          int *num_merges, size_t *workspace_bytes,
                                          xy_task_stats *stats) {
@@ -89,6 +128,7 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
         return XY_ERR_INVALID_ARG;
     if (num_seqs > 0 && !context_lens) return XY_ERR_INVALID_ARG;
     if (num_heads_q % num_heads_kv) return XY_ERR_INVALID_ARG;
+    if (schedule != XY_SCHEDULE_AREA && schedule != XY_SCHEDULE_MIXED) return XY_ERR_INVALID_ARG;
     if (cu_seqlens_q[0] != 0) return XY_ERR_CU_SEQLENS;
     const int G = num_heads_q / num_heads_kv;
 
@@ -133,7 +173,11 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
                     r.t.kv_end = (int32_t)k1;
                     r.t.num_splits = (int32_t)nsplit;
                     r.t.ws_row = nsplit == 1 ? -1 : (int32_t)(base + c * rows * G);
-                    r.load = rows * G * (k1 - k0);
+                    int64_t charged = rows * G;
+                    if (schedule == XY_SCHEDULE_MIXED)
+                        charged = XY_SCHEDULE_TILE_ROWS *
+                                  std::max<int64_t>(1, (charged + XY_SCHEDULE_TILE_ROWS - 1) / XY_SCHEDULE_TILE_ROWS);
+                    r.load = charged * (k1 - k0);
                     recs.push_back(r);
                 }
             }
@@ -141,7 +185,18 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
     }
     std::stable_sort(recs.begin(), recs.end(),
                      [](const Rec &a, const Rec &b) { return a.load > b.load; });
-
+    if (schedule == XY_SCHEDULE_MIXED) {
+        int64_t total = 0;
+        for (const Rec &r : recs) total += r.load;
+        if (total >= (int64_t(1) << 55) || num_ctas > (1 << 16)) return XY_ERR_UNSUPPORTED;
+        const size_t n = recs.size();
+        std::vector<Rec> out;
+        for (size_t c = 0; c < (size_t)num_ctas && c < n; ++c) {
+            interleave_cta(recs, c, (size_t)num_ctas, G, out);
+            size_t k = 0;
+            for (size_t q = c; q < n; q += num_ctas) recs[q] = out[k++];
+        }
+    }
     *num_tasks = (int)recs.size();
     *num_merges = (int)mrg.size();
     *workspace_bytes = (size_t)ws_rows * (size_t)(head_dim + 1) * 4u;

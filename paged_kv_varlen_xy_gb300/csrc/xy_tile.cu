@@ -75,8 +75,8 @@ constexpr int kDecStagesOff = 0;
 constexpr int kDecSlotsOff = DecRing::kBytes;
 constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
 static_assert(kDecSlotsOff + DecRing::kSlotBytes <= kBarOff, "decode path fits in the tile path's bytes");
-constexpr int kDecBarOff = kBarOff + B_COUNT * 8;    // decode ring full[4], empty[4], task-done
-constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 1) * 8;  // TMEM base address, abort flag
+constexpr int kDecBarOff = kBarOff + B_COUNT * 8;    // decode ring full[4], empty[4], task-done[2]
+constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 2) * 8;  // TMEM base address, abort flag
 constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp, then 2 x 4 decode votes
 constexpr int kSmemBytes = kVoteOff + 64 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -116,7 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     dsm.abort_flag = abort_flag;
     dsm.vote = vote + 16;
     dsm.bar_id = 3;
-    const uint32_t dec_done = base + kDecBarOff + 8 * (2 * DecRing::kStages);  // one per decode task
+    // decode task j done (math warps past its last shared-memory access): dec_done + 8 * (j & 1),
+    // phase j >> 1.  Two barriers, and the producer confirms task j - 2 before issuing task j, so
+    // every wait below is on the latest phase issued on its barrier and parity cannot alias.
+    const uint32_t dec_done = base + kDecBarOff + 8 * (2 * DecRing::kStages);
 
     if (threadIdx.x == 0) {
         xy::mbar_init(bar(B_QFULL), 1);
@@ -136,7 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             xy::mbar_init(base + kDecBarOff + 8 * st, 1);
             xy::mbar_init(base + kDecBarOff + 8 * (DecRing::kStages + st), xy::dec::kMathWarps);
         }
-        xy::mbar_init(base + kDecBarOff + 8 * (2 * DecRing::kStages), xy::dec::kMathWarps);
+        xy::mbar_init(dec_done, xy::dec::kMathWarps);
+        xy::mbar_init(dec_done + 8, xy::dec::kMathWarps);
         *abort_flag = 0;
         xy::fence_mbarrier_init();
     }
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = c - 1; w && k >= 0 && k >= c - kSlots; --k)
                         w = xy::mbar_wait(bar(B_EMPTY0 + k % kSlots), (k / kSlots) & 1, abort_flag);
                 } else {  // the math warps have finished the last decode task (merge slots included)
-                    w = xy::mbar_wait(dec_done, (nd - 1) & 1, abort_flag);
+                    w = xy::mbar_wait(dec_done + 8 * ((nd - 1) & 1), ((nd - 1) >> 1) & 1, abort_flag);
                 }
                 if (!warp_all(w)) {
                     ok = false;
@@ -200,6 +204,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             last_kind = kind;
             if (!tile) {
+                if (nd >= 2 &&
+                    !warp_all(xy::mbar_wait(dec_done + 8 * (nd & 1), ((nd - 2) >> 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
                 const TaskInfo f = tc.cur;
                 const bool have_first = pref_valid;
                 pref_valid = false;
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     __syncwarp();
-                    if (lane == 0) xy::mbar_arrive(dec_done);
+                    if (lane == 0) xy::mbar_arrive(dec_done + 8 * ((diter - 1) & 1));
                 }
                 tc.advance(p);
                 continue;

@@ -12,13 +12,13 @@ class PagedBatch:
     buffer and the attention plan.  Built from host arrays (the scheduler's view of the batch)."""
 
     def __init__(self, cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
-                 head_dim, causal, device="cuda", num_ctas=None, q_tile=None, kv_chunk=None):
+                 head_dim, causal, device="cuda", num_ctas=None, q_tile=None, kv_chunk=None, schedule=1):
         dev = torch.device(device)
         self.cu_host = np.asarray(cu_seqlens_q, dtype=np.int32)
         self.ctx_host = np.asarray(context_lens, dtype=np.int32)
         self.block_table_host, self.pages_used = xy_build_block_table(self.ctx_host, block_size, free_list, max_blocks)
         self.plan = Plan(self.cu_host, self.ctx_host, num_heads_q, num_heads_kv, head_dim, causal, device=dev,
-                         num_ctas=num_ctas, q_tile=q_tile, kv_chunk=kv_chunk)
+                         num_ctas=num_ctas, q_tile=q_tile, kv_chunk=kv_chunk, schedule=schedule)
         self.cu = torch.from_numpy(self.cu_host).to(dev)
         self.ctx = torch.from_numpy(self.ctx_host).to(dev)
         self.block_table = torch.from_numpy(self.block_table_host).to(dev)

@@ -135,3 +135,94 @@ def test_empty_batch_and_errors():
         build_task_table([0, 5], [4], 4, 2, 64, True, 3, 8, 64)   # q_len > context
     with pytest.raises(ValueError):
         build_task_table([0, 1], [4], 6, 4, 64, True, 3, 8, 64)   # Hq not a multiple of Hkv
+
+
+def _area_order(r0):
+    return [tuple(int(v) for v in t) for t in r0["tasks"]]
+
+
+def test_mixed_schedule_equals_area_schedule_without_small_tasks():
+    # every task carries >= 128 rows (q_tile 32 x G 4, q_len a multiple of 32): charging
+    # max(rows, 128) changes no load and there is nothing to alternate with, so the tables coincide
+    cu = pack_cu_seqlens([192, 256, 128])
+    ctx = [900, 256, 4000]
+    a = build_task_table(cu, ctx, 8, 2, 128, True, 5, 32, 256, schedule=0)
+    b = build_task_table(cu, ctx, 8, 2, 128, True, 5, 32, 256, schedule=1)
+    assert all(int(t[3]) * 4 >= 128 for t in a["tasks"])
+    assert np.array_equal(a["tasks"], b["tasks"]) and a["balance"] == b["balance"]
+
+
+def test_mixed_schedule_equals_area_schedule_for_pure_decode():
+    # all tasks are 1-row decode tasks (G = 1): every load is scaled by the same 128
+    rng = np.random.default_rng(3)
+    ctx = rng.integers(1, 5000, size=40)
+    cu = pack_cu_seqlens(np.ones(40, dtype=np.int64))
+    a = build_task_table(cu, ctx, 4, 4, 128, True, 9, 1, 512, schedule=0)
+    b = build_task_table(cu, ctx, 4, 4, 128, True, 9, 1, 512, schedule=1)
+    assert np.array_equal(a["tasks"], b["tasks"])
+    assert b["loads"].tolist() == (a["loads"] * 128).tolist()
+
+
+def test_mixed_schedule_interleaves_in_proportion_within_each_cta():
+    rng = np.random.default_rng(4)
+    q_lens = np.concatenate([np.full(6, 300), np.ones(50, dtype=np.int64)])
+    ctx = q_lens + rng.integers(0, 3000, size=len(q_lens))
+    cu = pack_cu_seqlens(q_lens)
+    G, num_ctas, q_tile, chunk = 4, 11, 32, 512
+    b = build_task_table(cu, ctx, 8, 2, 128, True, num_ctas, q_tile, chunk, schedule=1)
+    # rebuild the charged loads (padded 128-row tiles; small tasks as one tile), sort and deal
+    recs = []
+    for i in range(len(q_lens)):
+        qn, L = int(q_lens[i]), int(ctx[i])
+        for g in range(2):
+            for q0 in range(0, qn, q_tile):
+                qr = min(q_tile, qn - q0)
+                hi = L - qn + q0 + qr
+                for k0 in range(0, hi, chunk):
+                    k1 = min(hi, k0 + chunk)
+                    recs.append(((i, g, q0, qr, k0, k1), 128 * (k1 - k0)))
+    order = np.argsort(-np.array([x[1] for x in recs]), kind="stable")
+    assert len(order) == len(b["tasks"])
+    got = [tuple(int(v) for v in t[:6]) for t in b["tasks"]]
+    load_of = {x[0]: x[1] for x in recs}
+    both = 0
+    for c in range(num_ctas):
+        dealt = [recs[k][0] for k in order[c::num_ctas]]
+        mine = got[c::num_ctas]
+        assert sorted(mine) == sorted(dealt)
+        assert int(b["cta_loads"][c]) == sum(load_of[x] for x in dealt)
+        lists = {}
+        for kind in (True, False):
+            want = [x for x in dealt if (x[3] * G > 16) == kind]
+            seen = [x for x in mine if (x[3] * G > 16) == kind]
+            # each kind runs its dealt order, rotated to start at the CTA's phase c / num_ctas
+            assert len(seen) == len(want)
+            if want:
+                r = want.index(seen[0])
+                assert seen == want[r:] + want[:r]
+                tot = sum(load_of[x] for x in want)
+                starts = np.cumsum([0] + [load_of[x] for x in want[:-1]])
+                # a task starting at fraction s of its list runs at time (s + c / num_ctas) mod 1:
+                # the CTA begins with the first task at s >= 1 - c / num_ctas (else the first one)
+                late = [q for q in range(len(want)) if starts[q] * num_ctas >= (num_ctas - c) * tot]
+                assert r == (late[0] if late else 0)
+            lists[kind] = (want, seen)
+        if not lists[True][0] or not lists[False][0]:
+            continue
+        both += 1
+        # proportionality: whenever a task starts, the fraction of each list already run (from
+        # the phase on) differs by less than one task's share of that list
+        frac = {k: 0.0 for k in (True, False)}
+        tot = {k: sum(load_of[x] for x in lists[k][0]) for k in (True, False)}
+        biggest = {k: max(load_of[x] for x in lists[k][0]) / tot[k] for k in (True, False)}
+        for x in mine:
+            k = x[3] * G > 16
+            other = not k
+            assert frac[k] <= frac[other] + biggest[other] + 1e-12
+            frac[k] += load_of[x] / tot[k]
+    assert both > 0
+
+
+def test_unknown_schedule_rejected():
+    with pytest.raises(ValueError):
+        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=2)
