@@ -90,7 +90,8 @@ def work(wl):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons; `summary(t0, t1)` keeps
+    the samples whose host arrival time lies inside the timed region [t0, t1] (perf_counter)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -104,7 +105,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -114,7 +115,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -124,10 +125,12 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -142,7 +145,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "timed region" if t0 is not None else "whole run"}
 
 
 def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None):
@@ -182,6 +185,17 @@ def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None):
 
 def unit_of(config):
     return ("TFLOP/s", "tensor") if config == "prefill" else ("GB/s", "hbm")
+
+
+def attention_kernel(wl):
+    """The attention kernel the library dispatches to: the tcgen05 tile kernel when head_dim is
+    128, G divides 128 and the batch is not pure decode (one token per sequence, G <= 16);
+    otherwise the decode-path kernel."""
+    G = wl.num_heads_q // wl.num_heads_kv
+    pure_decode = wl.num_tokens == wl.num_seqs and G <= 16
+    if wl.head_dim == 128 and 128 % G == 0 and not pure_decode:
+        return "meta_attention_kernel"
+    return "paged_attention_kernel"
 
 
 def throughput(config, w, seconds):
@@ -276,11 +290,13 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         time.sleep(0.25)
+        w0 = time.perf_counter()
         t_start.record(stream)
         for k in range(args.steps):
             step(attn_ev[k])
         t_stop.record(stream)
         torch.cuda.synchronize()
+        w1 = time.perf_counter()
         time.sleep(0.05)
     xystep.check(batch)
     total_ms = t_start.elapsed_time(t_stop)
@@ -292,16 +308,26 @@ def main():
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
     value = throughput(args.config, w, ms_per_step / 1e3) * world
     unit, bound = unit_of(args.config)
+    kname = attention_kernel(wl)
+    attn_s = attn_ms / 1e3
     if bound == "hbm":
-        achieved = w["attn_bytes"] / (attn_ms / 1e3) / 1e9
+        achieved = w["attn_bytes"] / attn_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
-                "traffic": measured_traffic(args.config), "kernel": "paged_attention_kernel", "algorithmic_bytes": w["attn_bytes"],
+                "traffic": measured_traffic(args.config), "kernel": kname, "algorithmic_bytes": w["attn_bytes"],
                 "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
+        if args.config == "mixed":
+            # both bounds matter: time at the roofline = bytes / HBM + flops / tensor (the sum, as the
+            # two phases need not overlap) and max(.) (perfect overlap)
+            t_sum = w["attn_bytes"] / (pk["hbm"] * 1e9) + w["flops"] / (pk["tc"] * 1e12)
+            t_max = max(w["attn_bytes"] / (pk["hbm"] * 1e9), w["flops"] / (pk["tc"] * 1e12))
+            roof.update({"tensor_achieved_tflops": w["flops"] / attn_s / 1e12, "algorithmic_flops": w["flops"],
+                         "combined_frac_sum": t_sum / attn_s, "combined_frac_max": t_max / attn_s})
     else:
-        achieved = w["flops"] / (attn_ms / 1e3) / 1e12
+        achieved = w["flops"] / attn_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["tc"], "unit": "TFLOP/s",
-                "frac": achieved / pk["tc"], "traffic": measured_traffic(args.config), "kernel": "paged_attention_kernel",
+                "frac": achieved / pk["tc"], "traffic": measured_traffic(args.config), "kernel": kname,
                 "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
+    roof["timed"] = "attention call (kernel" + (" + combine" if pl.merges.shape[0] else "") + "), CUDA events"
 
     # ---- end to end through the public API: pinned host inputs in, output out, every step ----
     host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
@@ -337,7 +363,10 @@ def main():
         cpu = {"value": throughput(args.config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
                "sample": desc}
 
-    clocks = clk.summary()
+    clocks = clk.summary(w0, w1)
+    if clocks["samples"] == 0:  # the timed region was shorter than one sampling period
+        clocks = clk.summary()
+        clocks["window"] = "whole run (timed region shorter than the 20 ms sampling period)"
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
