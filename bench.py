@@ -187,6 +187,23 @@ def unit_of(config):
     return ("TFLOP/s", "tensor") if config == "prefill" else ("GB/s", "hbm")
 
 
+def max_over_ranks(x, world, device="cpu"):
+    """The largest of one float per rank (the slowest replica sets the job's time); `device` is
+    where the reduction tensor lives ("cuda:i" under NCCL, "cpu" under gloo)."""
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(config, w, seconds, world):
+    """Whole-job throughput of `world` replicas that each process work `w` in `seconds` (the max
+    over ranks): the units all ranks processed / that time."""
+    return throughput(config, w, seconds) * world
+
+
 def attention_kernel(wl):
     """The attention kernel the library dispatches to: the tcgen05 tile kernel when head_dim is
     128, G divides 128 and the batch is not pure decode (one token per sequence, G <= 16);
@@ -229,7 +246,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode", choices=list(workloads.CONFIGS))
     ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
@@ -299,14 +316,10 @@ def main():
         w1 = time.perf_counter()
         time.sleep(0.05)
     xystep.check(batch)
-    total_ms = t_start.elapsed_time(t_stop)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world, device=dev)
     ms_per_step = total_ms / args.steps
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
-    value = throughput(args.config, w, ms_per_step / 1e3) * world
+    value = job_throughput(args.config, w, ms_per_step / 1e3, world)
     unit, bound = unit_of(args.config)
     kname = attention_kernel(wl)
     attn_s = attn_ms / 1e3
@@ -354,8 +367,8 @@ def main():
                                                                 (b2.cu, b2.ctx, b2.block_table, b2.plan.tasks,
                                                                  b2.plan.merges))
             d2h = out_host.numel() * 2
-    e2e_s = sum(e2e_times[args.warmup:]) / args.steps
-    e2e_val = throughput(args.config, w, e2e_s) * world
+    e2e_s = max_over_ranks(sum(e2e_times[args.warmup:]) / args.steps, world, device=dev)
+    e2e_val = job_throughput(args.config, w, e2e_s, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

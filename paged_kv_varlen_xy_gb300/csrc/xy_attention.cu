@@ -148,45 +148,61 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
 }
 
 // Split-KV merge: for each split tile, out = sum_c 2^(lse_c - M) O_c / sum_c 2^(lse_c - M).
-// One CTA per merge record, one warp per (token, head) row, lanes across head_dim.
+// Grid (merge records, kCombineY): one warp per (token, head) row, kCombineY x 8 rows of a merge
+// in flight, lanes across head_dim.  Lane c of a warp turns split c's lse into its weight, so the
+// O rows of all splits load independently (no dependent chain per split).
+constexpr int kCombineY = 8;
+
 template <int HD>
-__global__ void __launch_bounds__(128) combine_kernel(const xy_merge *__restrict__ merges, const float *__restrict__ ws_o,
+__global__ void __launch_bounds__(256) combine_kernel(const xy_merge *__restrict__ merges, const float *__restrict__ ws_o,
                                                       const float *__restrict__ ws_lse, const int32_t *__restrict__ cu,
                                                       int Hq, int G, int64_t ws_rows, int32_t *err,
                                                       __nv_bfloat16 *__restrict__ out) {
     const xy_merge m = merges[blockIdx.x];
     const int R = m.q_rows * G;
-    if (m.num_splits < 2 || m.ws_row < 0 || (int64_t)m.ws_row + (int64_t)m.num_splits * R > ws_rows) {
-        if (threadIdx.x == 0) xy::set_err(err, XY_DEV_BAD_TASK);
+    const int ns = m.num_splits;
+    if (ns < 2 || m.ws_row < 0 || (int64_t)m.ws_row + (int64_t)ns * R > ws_rows) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) xy::set_err(err, XY_DEV_BAD_TASK);
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int V = HD / 32;  // floats per lane
     const int seq_start = __ldg(cu + m.seq);
-    for (int r = warp; r < R; r += blockDim.x >> 5) {
+    const int64_t base = m.ws_row;
+    for (int r = blockIdx.y * 8 + warp; r < R; r += kCombineY * 8) {
         float M = -INFINITY;
-        for (int c = 0; c < m.num_splits; ++c) M = fmaxf(M, __ldg(ws_lse + m.ws_row + (int64_t)c * R + r));
+        for (int c = lane; c < ns; c += 32) M = fmaxf(M, __ldg(ws_lse + base + (int64_t)c * R + r));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
         const float U = M == -INFINITY ? 0.f : M;
         float acc[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] = 0.f;
         float W = 0.f;
-        for (int c = 0; c < m.num_splits; ++c) {
-            const int64_t row = m.ws_row + (int64_t)c * R + r;
-            const float w = ex2(__ldg(ws_lse + row) - U);
-            W += w;
-            const float *src = ws_o + row * HD + lane * V;
-            if (V == 4) {
-                const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
-                acc[0] += w * x.x;
-                acc[1] += w * x.y;
-                acc[2] += w * x.z;
-                acc[3] += w * x.w;
-            } else {
-#pragma unroll
-                for (int v = 0; v < V; ++v) acc[v] += w * __ldg(src + v);
+        for (int c0 = 0; c0 < ns; c0 += 32) {
+            const int c = c0 + lane;
+            const float wl = c < ns ? ex2(__ldg(ws_lse + base + (int64_t)c * R + r) - U) : 0.f;
+            W += wl;
+            const int nc = min(32, ns - c0);
+#pragma unroll 4
+            for (int k = 0; k < nc; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wl, k);
+                const float *src = ws_o + (base + (int64_t)(c0 + k) * R + r) * HD + lane * V;
+                if (V == 4) {
+                    const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
+                    acc[0] += w * x.x;
+                    acc[1] += w * x.y;
+                    acc[2] += w * x.z;
+                    acc[3] += w * x.w;
+                } else {
+                    const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
+                    acc[0] += w * x.x;
+                    acc[1] += w * x.y;
+                }
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
         const float inv = W > 0.f ? 1.f / W : 0.f;
         const int64_t tok = seq_start + m.q_start + r / G;
         const int h = m.kv_head * G + r % G;
@@ -256,8 +272,8 @@ xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &
         if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel launch");
     }
     if (num_merges > 0) {
-        combine_kernel<HD><<<num_merges, 128, 0, st>>>(merges, p.ws_o, p.ws_lse, p.cu, p.Hq, p.G, p.ws_rows, p.err,
-                                                       p.out);
+        combine_kernel<HD><<<dim3(num_merges, kCombineY), 256, 0, st>>>(merges, p.ws_o, p.ws_lse, p.cu, p.Hq, p.G,
+                                                                        p.ws_rows, p.err, p.out);
         if (cudaGetLastError() != cudaSuccess) return XY_ERR_CUDA;
     }
     return XY_OK;

@@ -17,7 +17,7 @@ def bits(t):
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None):
+def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None, schedule=1):
     """Run the CUDA step and the oracle step on workload `wl`.
 
     rows: list of (token, head) to compare, or None for every row.  sample_seqs: sequences whose
@@ -32,7 +32,7 @@ def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=No
         vals["v_pool"].fill_(pool_fill)
     batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
                               wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
-                              num_ctas=num_ctas, q_tile=q_tile, kv_chunk=kv_chunk)
+                              num_ctas=num_ctas, q_tile=q_tile, kv_chunk=kv_chunk, schedule=schedule)
     bt = batch.block_table_host
     if sample_seqs is None:
         pages = None

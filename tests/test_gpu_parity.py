@@ -67,6 +67,32 @@ def test_num_ctas_variants():
         assert_parity(run(wl, num_ctas=n))
 
 
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_verify_shaped_queries(G):
+    # speculative-verify batches ([ATB] 投机解码技术): 2..8 new tokens per sequence over long
+    # contexts; with G = 1 every task is decode-shaped, with G = 4 and 8 some become tiles
+    rng = np.random.default_rng(40 + G)
+    q = rng.integers(2, 9, size=24)
+    ctx = q + rng.integers(500, 6000, size=24)
+    wl = workloads.custom(q, ctx, 4 * G, 4, 128, 16, True, seed=60 + G, name="verify")
+    assert_parity(run(wl))
+
+
+@pytest.mark.parametrize("schedule", [0, 1])
+def test_kind_switches_in_one_launch(schedule):
+    # short decode tasks (one or two 64-key stages) interleaved with chunk tiles on few CTAs, so
+    # every CTA switches between the decode path and the tile path many times in one launch
+    rng = np.random.default_rng(7)
+    dq = np.ones(48, dtype=np.int64)
+    dctx = rng.integers(20, 130, size=48)
+    cq = np.full(6, 256)
+    cctx = cq + rng.integers(0, 1500, size=6)
+    q = np.concatenate([dq[:24], cq[:3], dq[24:], cq[3:]])
+    ctx = np.concatenate([dctx[:24], cctx[:3], dctx[24:], cctx[3:]])
+    wl = workloads.custom(q, ctx, 16, 4, 128, 16, True, seed=71, name="switches")
+    assert_parity(run(wl, num_ctas=5, kv_chunk=512, schedule=schedule))
+
+
 def test_full_size_decode_sampled():
     wl = workloads.decode()
     rng = np.random.default_rng(0)
