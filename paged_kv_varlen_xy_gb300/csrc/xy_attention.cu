@@ -38,13 +38,19 @@ using xy::TaskCursor;
 using xy::TaskInfo;
 using xy::dec::kMathWarps;
 
-// Stand-alone decode-path kernel: one persistent CTA per SM, a producer warp and four math warps
-// (xy_decode_path.cuh).  It runs every task when the tcgen05 tile kernel cannot (head_dim 64, or
-// G not dividing 128); tasks then have at most 64 rows.
+// Stand-alone decode-path kernel: one persistent CTA per SM, four math warps and two producer
+// warps that issue alternate stages (xy_decode_path.cuh).  Issuing a stage -- block-table window
+// lookup, eight page boxes, barrier bookkeeping -- costs a producer warp about as long as the math
+// warps need to consume one, so two producers keep the ring ahead of the math.  It runs every
+// task when the tcgen05 tile kernel cannot (head_dim 64, or G not dividing 128), and pure decode
+// batches; tasks then have at most 64 rows.
+constexpr int kProducers = 2;
+
 template <int HD>
 struct Cfg {
     using RG = xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>;
-    static constexpr int kThreads = (kMathWarps + 1) * 32;
+    static_assert(RG::kStages % kProducers == 0, "a stage always has the same producer");
+    static constexpr int kThreads = (kMathWarps + kProducers) * 32;
     static constexpr int kStagesOff = 0;
     static constexpr int kSlotsOff = RG::kBytes;
     static constexpr int kBarOff = kSlotsOff + RG::kSlotBytes;
@@ -85,8 +91,9 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
     }
     __syncthreads();
 
-    if (warp == kMathWarps) {
-        // ------------------------------ producer warp ------------------------------
+    if (warp >= kMathWarps) {
+        // ------------------------------ producer warps ------------------------------
+        const int pw = warp - kMathWarps;
         if (lane == 0) {
             xy::prefetch_tensormap(&kmap);
             xy::prefetch_tensormap(&vmap);
@@ -106,24 +113,26 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
             const TaskInfo f = tc.cur;
             const bool have_first = pref_valid;
             pref_valid = false;
-            ok = xy::dec::produce_task<HD, RG>(p, f, &kmap, &vmap, sm, ctr, lane, pref_win, have_first, [&]() {
-                // the next record has arrived by now: prefetch its numbers and first window
-                tc.prefetch_next(p);
-                if (tc.have_next) {
-                    const xy_task &tn = tc.nxt.t;
-                    pref_valid = tn.seq >= 0 && tn.seq < p.S && tn.kv_start >= 0;
-                    if (pref_valid) pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
-                }
-            });
+            ok = xy::dec::produce_task<HD, RG>(
+                p, f, &kmap, &vmap, sm, ctr, lane, pref_win, have_first,
+                [&]() {
+                    // the next record has arrived by now: prefetch its numbers and first window
+                    tc.prefetch_next(p);
+                    if (tc.have_next) {
+                        const xy_task &tn = tc.nxt.t;
+                        pref_valid = tn.seq >= 0 && tn.seq < p.S && tn.kv_start >= 0;
+                        if (pref_valid) pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
+                    }
+                },
+                pw, kProducers);
             tc.advance(p);
         }
         if (!ok) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             *abort_flag = 1;
         }
-        // every issued stage must have landed before the CTA may exit
-        for (int k = ctr - 1; k >= 0 && k >= ctr - RG::kStages; --k)
-            xy::mbar_wait(sm.full_bar + 8 * (k % RG::kStages), (k / RG::kStages) & 1);
+        // every stage this warp issued must have landed before the CTA may exit
+        xy::dec::drain<RG>(sm, ctr, pw, kProducers);
         return;
     }
 

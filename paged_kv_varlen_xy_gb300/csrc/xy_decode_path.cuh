@@ -73,66 +73,84 @@ __device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) 
     return task_common_ok(f, p) && f.t.q_rows * p.G <= RG::kMaxRows && (f.t.kv_start % kStageKeys) == 0;
 }
 
-// Producer warp: issue every stage of decode task `f`.  `ctr` counts stages issued on the ring.
+// Producer warp `pw` of `npw`: issue the stages of decode task `f` whose ring counter is pw
+// modulo npw (with npw dividing the ring depth, a stage always has the same producer, so each
+// producer waits only on its own stages' empty barriers).  `ctr` counts all of the task's stages.
 // `pg_first` is the task's first block-table window if it was prefetched (else -1 with
-// have_first false).  `first_stage_done()` runs once, right after the first stage is issued
-// (the caller prefetches the next task there).  Returns false if a wait gave up.
+// have_first false).  `first_stage_done()` runs once, right after this warp's first stage of the
+// task is issued (the caller prefetches the next task there).  Returns false if a wait gave up.
 template <int HD, class RG, class F>
 __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUtensorMap *kmap, const CUtensorMap *vmap,
-                             const Smem &sm, int &ctr, int lane, int pg_first, bool have_first, F first_stage_done) {
+                             const Smem &sm, int &ctr, int lane, int pg_first, bool have_first, F first_stage_done,
+                             int pw = 0, int npw = 1) {
     const xy_task &t = f.t;
+    const int bs_sh = 31 - __clz(p.bs);                   // page size is a power of two
     const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;  // keys per TMA box
+    const int br_sh = 31 - __clz(BR);
+    const uint32_t row_bytes = (uint32_t)p.G * HD * 2;     // one token's G query rows
     // block-table entries are read 32 logical pages at a time (one per lane), the next window
     // loaded before it is needed, so no stage waits on a dependent global load
-    int win0 = t.kv_start / p.bs;
+    int win0 = t.kv_start >> bs_sh;
     int pg_win = have_first ? pg_first : load_window(p, t.seq, win0, lane);
     int pg_nxt = load_window(p, t.seq, win0 + 32, lane);
-    bool first_stage = true;
+    bool first_mine = true;
     for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
+        if (ctr % npw != pw) continue;  // another producer's stage
         const int s = ctr % RG::kStages;
         if (ctr >= RG::kStages &&
             !__all_sync(0xffffffffu, mbar_wait(sm.empty_bar + 8 * s, ((ctr / RG::kStages) - 1) & 1, sm.abort_flag)))
             return false;
         const int nkeys = min(kStageKeys, t.kv_end - kv0);
-        const int nbox = (nkeys + BR - 1) / BR;
-        if ((kv0 + nkeys - 1) / p.bs - win0 >= 32) {  // the stage reaches into the next window
+        const int nbox = (nkeys + BR - 1) >> br_sh;
+        while (((kv0 + nkeys - 1) >> bs_sh) - win0 >= 32) {  // the stage reaches into the next window
             win0 += 32;
             pg_win = pg_nxt;
             pg_nxt = load_window(p, t.seq, win0 + 32, lane);
         }
         const int n_copies = nbox * 2;  // one box per (page, tensor), both column halves
         const int b = lane % nbox;
-        int my_pg = __shfl_sync(0xffffffffu, pg_win, (kv0 + b * BR) / p.bs - win0);
+        int my_pg = __shfl_sync(0xffffffffu, pg_win, ((kv0 + (b << br_sh)) >> bs_sh) - win0);
         if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
             set_err(p.err, XY_DEV_PAGE_OOB);
             my_pg = 0;
         }
-        const uint32_t row_bytes = (uint32_t)p.G * HD * 2;  // one token's G query rows
-        const uint32_t q_bytes = first_stage ? (uint32_t)t.q_rows * row_bytes : 0u;
+        // the task's first stage also carries its query rows
+        const bool q_here = kv0 == t.kv_start;
+        const uint32_t q_bytes = q_here ? (uint32_t)t.q_rows * row_bytes : 0u;
         const uint32_t stage = sm.stages + s * RG::kStageBytes;
         if (lane == 0)
             mbar_arrive_expect_tx(sm.full_bar + 8 * s, (uint32_t)(n_copies * RG::kHalves * BR * 128) + q_bytes);
         __syncwarp();
         if (lane < n_copies) {
             const int tensor = lane / nbox;
-            const int key = kv0 + b * BR;
-            const int y = (my_pg * p.Hkv + t.kv_head) * p.bs + (key % p.bs);
+            const int key = kv0 + (b << br_sh);
+            const int y = ((my_pg * p.Hkv + t.kv_head) << bs_sh) + (key & (p.bs - 1));
             const uint32_t dst = stage + tensor * RG::kTensorBytes + b * RG::kHalves * BR * 128;
             tma_load_3d(dst, tensor ? vmap : kmap, 0, y, 0, sm.full_bar + 8 * s);
         }
-        if (first_stage) {
-            // the task's query rows: token j's G heads are one contiguous run of q
+        if (q_here) {
+            // token j's G heads are one contiguous run of q
             for (int j = lane; j < t.q_rows; j += 32) {
                 const int64_t tok = (int64_t)f.seq_start + t.q_start + j;
                 const __nv_bfloat16 *src = p.q + (tok * p.Hq + (int64_t)t.kv_head * p.G) * HD;
                 bulk_load(stage + 2 * RG::kTensorBytes + j * row_bytes, src, row_bytes, sm.full_bar + 8 * s);
             }
-            first_stage = false;
+        }
+        if (first_mine) {
+            first_mine = false;
             first_stage_done();
         }
         __syncwarp();
     }
     return true;
+}
+
+// Producer `pw` of `npw`, before exiting: every stage it issued (`ctr` stages issued in all) has
+// landed.
+template <class RG>
+__device__ __forceinline__ void drain(const Smem &sm, int ctr, int pw = 0, int npw = 1) {
+    for (int k = ctr - 1; k >= 0 && k >= ctr - RG::kStages; --k)
+        if (k % npw == pw) mbar_wait(sm.full_bar + 8 * (k % RG::kStages), (k / RG::kStages) & 1);
 }
 
 // Math warp w (0..3) runs decode task `f`.  `ctr` counts stages consumed on the ring, `iter` the

@@ -49,7 +49,8 @@ constexpr int kTileKeys = 128;
 constexpr int kSlots = 5;                       // K/V ring slots (one K or V tile each)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kThreads = 10 * 32;
+constexpr int kDecProducerWarp = 10;   // second producer of the decode ring (odd stages)
+constexpr int kThreads = 11 * 32;
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 columns
 constexpr int kTileBytes = 2 * kHalfBytes;      // one Q, K or V tile: [half][128 rows][128 B]
 constexpr int kQOff = 0;                        // Q_A, Q_B
@@ -76,7 +77,7 @@ constexpr int kDecSlotsOff = DecRing::kBytes;
 constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
 static_assert(kDecSlotsOff + DecRing::kSlotBytes <= kBarOff, "decode path fits in the tile path's bytes");
 constexpr int kDecBarOff = kBarOff + B_COUNT * 8;    // decode ring full[4], empty[4], task-done[2]
-constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 2) * 8;  // TMEM base address, abort flag
+constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 2) * 8;  // TMEM base, abort flag, decode go
 constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp, then 2 x 4 decode votes
 constexpr int kSmemBytes = kVoteOff + 64 + 32 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -105,6 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bar = [&](int i) -> uint32_t { return base + kBarOff + 8 * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + kMiscOff);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kMiscOff + 4);
+    // decode tasks 0 .. *dec_go - 1 may write the decode ring: the producer warp raises it once the
+    // tile work before a decode task no longer reads shared memory (a count, so no phase aliasing)
+    volatile int *dec_go = reinterpret_cast<volatile int *>(gbase + kMiscOff + 8);
     volatile int *vote = reinterpret_cast<volatile int *>(gbase + kVoteOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     xy::dec::Smem dsm;
@@ -142,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         xy::mbar_init(dec_done, xy::dec::kMathWarps);
         xy::mbar_init(dec_done + 8, xy::dec::kMathWarps);
         *abort_flag = 0;
+        *dec_go = 0;
         xy::fence_mbarrier_init();
     }
     if (warp == kMmaWarp) {
@@ -209,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                __threadfence_block();
+                if (lane == 0) *dec_go = nd + 1;  // the second decode producer may write task nd
                 const TaskInfo f = tc.cur;
                 const bool have_first = pref_valid;
                 pref_valid = false;
@@ -221,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                 if (pref_valid)
                                                                     pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
                                                             }
-                                                        });
+                                                        },
+                                                        0, 2);
                 ++nd;
                 tc.advance(p);
                 continue;
@@ -302,8 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = c - 1; k >= 0 && k >= c - kSlots; --k)
             xy::mbar_wait(bar(B_FULL0 + k % kSlots), (k / kSlots) & 1);
         if (qk > 0) xy::mbar_wait(bar(B_QFULL), (qk - 1) & 1);
-        for (int k = dctr - 1; k >= 0 && k >= dctr - DecRing::kStages; --k)
-            xy::mbar_wait(dsm.full_bar + 8 * (k % DecRing::kStages), (k / DecRing::kStages) & 1);
+        xy::dec::drain<DecRing>(dsm, dctr, 0, 2);
     } else if (warp == kMmaWarp) {
         // ---------------------------------- MMA issuer ----------------------------------
         if (lane == 0) {
@@ -402,6 +409,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp == kDecProducerWarp) {
+        // ------------------------- second decode-ring producer -------------------------
+        // Issuing a decode stage (block-table window, page boxes, barrier bookkeeping) takes a
+        // warp about as long as the math warps need to consume one; with the producer warp on the
+        // even stages and this warp on the odd ones the ring stays ahead of the math.
+        int dctr = 0, nd = 0, pref_win = -1;
+        bool ok = true, pref_valid = false, after_tile = false;
+        TaskCursor tc;
+        tc.begin(p);
+        while (tc.have && ok) {
+            tc.load_next_record(p);
+            if (mine(tc.cur, p)) {
+                after_tile = after_tile || tile_ok(tc.cur, p);
+                pref_valid = false;
+                tc.advance(p);
+                continue;
+            }
+            if (!xy::dec::task_ok<DecRing>(tc.cur, p)) {
+                pref_valid = false;
+                tc.advance(p);
+                continue;
+            }
+            if (after_tile) {
+                // the decode ring overlays the tile buffers: wait until the producer warp has seen
+                // the tile work before this task stop reading shared memory
+                bool w = true;
+                if (lane == 0) {
+                    const uint64_t t0 = xy::global_timer_ns();
+                    while (*dec_go < nd + 1) {
+                        if (*abort_flag || xy::global_timer_ns() - t0 > xy::kWaitTimeoutNs) {
+                            w = false;
+                            break;
+                        }
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+                __threadfence_block();
+                after_tile = false;
+            }
+            ++nd;
+            const TaskInfo f = tc.cur;
+            const bool have_first = pref_valid;
+            pref_valid = false;
+            ok = xy::dec::produce_task<HD, DecRing>(
+                p, f, &kmap_d, &vmap_d, dsm, dctr, lane, pref_win, have_first,
+                [&]() {
+                    tc.prefetch_next(p);
+                    if (tc.have_next) {
+                        const xy_task &tn = tc.nxt.t;
+                        pref_valid = tn.seq >= 0 && tn.seq < p.S && tn.kv_start >= 0;
+                        if (pref_valid) pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
+                    }
+                },
+                1, 2);
+            tc.advance(p);
+        }
+        if (!ok) {
+            if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+        // every stage this warp issued must land before the CTA may exit
+        xy::dec::drain<DecRing>(dsm, dctr, 1, 2);
     } else if (warp < 8) {
         // ---------------------------------- softmax ----------------------------------
         const int x = warp >> 2;                            // query tile of this group
