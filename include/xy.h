@@ -155,15 +155,19 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  * [0, L_i) or, if causal, [0, L_i - q_i + q_start + q_rows); stable-sorts by load, largest first;
  * CTA c of the persistent launch runs tasks[c], tasks[c + num_ctas], ...  Split tiles
  * (num_splits > 1) get workspace rows in enumeration order and one xy_merge each.
- * schedule: XY_SCHEDULE_AREA follows the pages exactly.  XY_SCHEDULE_MIXED is a variant for
- * batches that mix HBM-bound decode tasks with tensor-core tiles: a task is charged
- * 128 * max(1, ceil(rows / 128)) * keys (a tile costs its padded 128-row MMA area; a task of at most
- * XY_SCHEDULE_SMALL_ROWS rows streams its KV in about the time of one such tile), sorted and dealt
- * the same way; then each CTA interleaves its small and large tasks in proportion to their charged
- * loads, CTA c starting at phase c / num_ctas, so that at any time about the small tasks' share of
- * the CTAs streams KV from HBM while the others keep the tensor cores busy.  The per-CTA load sums
- * (stats) are those of the deal.  Returns XY_ERR_UNSUPPORTED when the total charged load
- * reaches 2^55 or num_ctas exceeds 65536.
+ * schedule: XY_SCHEDULE_AREA follows the pages' code exactly (task i to CTA i mod num_ctas).
+ * XY_SCHEDULE_SERPENTINE reads the pages' "symmetric round-robin" as a serpentine deal: the same
+ * sort, then every complete odd round of num_ctas positions goes to the CTAs in reverse order, so
+ * a CTA that took one of a round's largest tasks takes one of the next round's smallest (the
+ * final partial round keeps the plain order, so the table stays dense).  XY_SCHEDULE_MIXED is a
+ * variant for batches that mix HBM-bound decode tasks with tensor-core tiles: a task is charged
+ * 128 * max(1, ceil(rows / 128)) * keys (a tile costs its padded 128-row MMA area; a task of at
+ * most XY_SCHEDULE_SMALL_ROWS rows streams its KV in about the time of one such tile), sorted and
+ * dealt serpentine; then each CTA interleaves its small and large tasks in proportion to their
+ * charged loads, CTA c starting at phase c / num_ctas, so that at any time about the small tasks'
+ * share of the CTAs streams KV from HBM while the others keep the tensor cores busy.  The per-CTA
+ * load sums (stats) are those of the deal.  XY_SCHEDULE_MIXED returns XY_ERR_UNSUPPORTED when the
+ * total charged load reaches 2^55 or num_ctas exceeds 65536.
  *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs]: host int32.
  *   tasks [max_tasks], merges [max_merges]: host outputs; pass NULL (with max 0) to query counts.
  *   *num_tasks, *num_merges: counts; *workspace_bytes = rows * (head_dim + 1) * 4 (fp32 partial
@@ -172,7 +176,8 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  *   XY_ERR_CONTEXT_LT_QLEN, XY_ERR_CAPACITY (non-NULL arrays too small).
  */
 #define XY_SCHEDULE_AREA 0        /* the pages' reorder: load = area, sort, round-robin deal */
-#define XY_SCHEDULE_MIXED 1       /* padded-tile load, sort, deal, per-CTA proportional interleave */
+#define XY_SCHEDULE_SERPENTINE 1  /* the same sort, serpentine ("symmetric round-robin") deal */
+#define XY_SCHEDULE_MIXED 2       /* padded-tile load, sort, serpentine deal, per-CTA interleave */
 #define XY_SCHEDULE_TILE_ROWS 128 /* MMA tile height: the unit of XY_SCHEDULE_MIXED's load */
 #define XY_SCHEDULE_SMALL_ROWS 16 /* tasks of at most this many rows count as small */
 

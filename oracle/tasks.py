@@ -30,19 +30,31 @@ TASK_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "kv_start", "kv_end", "num
 MERGE_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "num_splits", "ws_row", "zero0", "zero1")
 
 
-# schedule 1 (a variant of the pages' reorder for batches that mix HBM-bound decode tasks with
-# tensor-core tiles; the pages' load is the plain area):
-# * charged load = TILE_ROWS * max(1, ceil(rows / TILE_ROWS)) * keys: a tile costs its padded
-#   128-row MMA area, and a small task (rows <= SMALL_ROWS) streams its keys' KV in about the
-#   time of one 128-row tile over the same keys;
-# * the same stable sort and round-robin deal;
-# * each CTA then interleaves its small and large tasks in proportion to their charged loads,
-#   starting at phase c / num_ctas of its timeline, so that at any moment about the small tasks'
-#   share of the CTAs streams KV while the others keep the tensor cores busy.
+# Schedules (the pages' reorder is schedule 0):
+# * 1 reads "symmetric round-robin" as a serpentine deal: the same stable sort by area, then every
+#   complete odd round of num_ctas positions goes to the CTAs in reverse order (CTA num_ctas-1
+#   first), so a CTA that took one of the largest tasks of a round takes one of the smallest of the
+#   next; the final partial round keeps the plain order, so the table stays dense.
+# * 2 is a variant for batches that mix HBM-bound decode tasks with tensor-core tiles:
+#   charged load = TILE_ROWS * max(1, ceil(rows / TILE_ROWS)) * keys (a tile costs its padded
+#   128-row MMA area; a small task, rows <= SMALL_ROWS, streams its keys' KV in about the time of
+#   one 128-row tile over the same keys), the serpentine deal of schedule 1, then each CTA
+#   interleaves its small and large tasks in proportion to their charged loads, starting at phase
+#   c / num_ctas of its timeline, so that at any moment about the small tasks' share of the CTAs
+#   streams KV while the others keep the tensor cores busy.
 SMALL_ROWS = 16
 TILE_ROWS = 128
 MAX_TOTAL_LOAD = 1 << 55
 MAX_CTAS = 1 << 16
+SCHEDULES = (0, 1, 2)
+
+
+def _serpentine(order, num_ctas):
+    """Reverse every complete odd round of the dealt order (see schedule 1)."""
+    out = list(order)
+    for r in range(1, len(order) // num_ctas, 2):
+        out[r * num_ctas:(r + 1) * num_ctas] = order[r * num_ctas:(r + 1) * num_ctas][::-1]
+    return out
 
 
 def _charged_rows(rows):
@@ -74,10 +86,11 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
 
     CTA c runs tasks c, c + num_ctas, c + 2*num_ctas, ... of ``tasks``.
     schedule 0: the pages' reorder (load = area, stable sort descending, round-robin deal).
-    schedule 1: the charged load and per-CTA proportional interleave described above.
+    schedule 1: the same sort, serpentine deal.  schedule 2: charged load, serpentine deal and
+    per-CTA proportional interleave (see above).
     """
-    if schedule not in (0, 1):
-        raise ValueError("schedule must be 0 or 1")
+    if schedule not in SCHEDULES:
+        raise ValueError("schedule must be 0, 1 or 2")
     if num_heads_q % num_heads_kv:
         raise ValueError("Hq must be a multiple of Hkv")
     if q_tile < 1 or kv_chunk < 1 or num_ctas < 1:
@@ -109,12 +122,14 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
                     row = -1 if nsplit == 1 else base + c * rows * G
                     records.append((i, g, t0, rows, k0, k1, nsplit, row))
                     r = rows * G
-                    if schedule == 1:
+                    if schedule == 2:
                         r = _charged_rows(r)
                     loads.append(r * (k1 - k0))
 
     order = sorted(range(len(records)), key=lambda k: loads[k], reverse=True)
-    if schedule == 1:
+    if schedule in (1, 2):
+        order = _serpentine(order, num_ctas)
+    if schedule == 2:
         if sum(loads) >= MAX_TOTAL_LOAD or num_ctas > MAX_CTAS:
             raise ValueError("total load or num_ctas too large for schedule 1")
         # positions c, c + num_ctas, ... belong to CTA c; reorder each CTA's tasks among them

@@ -145,7 +145,8 @@ def xy_build_block_table(context_lens, block_size, free_list, max_blocks):
 
 
 XY_SCHEDULE_AREA = 0
-XY_SCHEDULE_MIXED = 1
+XY_SCHEDULE_SERPENTINE = 1
+XY_SCHEDULE_MIXED = 2
 
 
 def xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, num_ctas,

@@ -128,7 +128,8 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
         return XY_ERR_INVALID_ARG;
     if (num_seqs > 0 && !context_lens) return XY_ERR_INVALID_ARG;
     if (num_heads_q % num_heads_kv) return XY_ERR_INVALID_ARG;
-    if (schedule != XY_SCHEDULE_AREA && schedule != XY_SCHEDULE_MIXED) return XY_ERR_INVALID_ARG;
+    if (schedule != XY_SCHEDULE_AREA && schedule != XY_SCHEDULE_SERPENTINE && schedule != XY_SCHEDULE_MIXED)
+        return XY_ERR_INVALID_ARG;
     if (cu_seqlens_q[0] != 0) return XY_ERR_CU_SEQLENS;
     const int G = num_heads_q / num_heads_kv;
 
@@ -185,6 +186,12 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
     }
     std::stable_sort(recs.begin(), recs.end(),
                      [](const Rec &a, const Rec &b) { return a.load > b.load; });
+    if (schedule == XY_SCHEDULE_SERPENTINE || schedule == XY_SCHEDULE_MIXED) {
+        // serpentine deal: every complete odd round of num_ctas positions is reversed
+        const size_t n = (size_t)num_ctas;
+        for (size_t r = 1; (r + 1) * n <= recs.size(); r += 2)
+            std::reverse(recs.begin() + r * n, recs.begin() + (r + 1) * n);
+    }
     if (schedule == XY_SCHEDULE_MIXED) {
         int64_t total = 0;
         for (const Rec &r : recs) total += r.load;

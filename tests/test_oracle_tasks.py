@@ -141,24 +141,24 @@ def _area_order(r0):
     return [tuple(int(v) for v in t) for t in r0["tasks"]]
 
 
-def test_mixed_schedule_equals_area_schedule_without_small_tasks():
+def test_mixed_schedule_equals_serpentine_schedule_without_small_tasks():
     # every task carries >= 128 rows (q_tile 32 x G 4, q_len a multiple of 32): charging
     # max(rows, 128) changes no load and there is nothing to alternate with, so the tables coincide
     cu = pack_cu_seqlens([192, 256, 128])
     ctx = [900, 256, 4000]
-    a = build_task_table(cu, ctx, 8, 2, 128, True, 5, 32, 256, schedule=0)
-    b = build_task_table(cu, ctx, 8, 2, 128, True, 5, 32, 256, schedule=1)
+    a = build_task_table(cu, ctx, 8, 2, 128, True, 5, 32, 256, schedule=1)
+    b = build_task_table(cu, ctx, 8, 2, 128, True, 5, 32, 256, schedule=2)
     assert all(int(t[3]) * 4 >= 128 for t in a["tasks"])
     assert np.array_equal(a["tasks"], b["tasks"]) and a["balance"] == b["balance"]
 
 
-def test_mixed_schedule_equals_area_schedule_for_pure_decode():
+def test_mixed_schedule_equals_serpentine_schedule_for_pure_decode():
     # all tasks are 1-row decode tasks (G = 1): every load is scaled by the same 128
     rng = np.random.default_rng(3)
     ctx = rng.integers(1, 5000, size=40)
     cu = pack_cu_seqlens(np.ones(40, dtype=np.int64))
-    a = build_task_table(cu, ctx, 4, 4, 128, True, 9, 1, 512, schedule=0)
-    b = build_task_table(cu, ctx, 4, 4, 128, True, 9, 1, 512, schedule=1)
+    a = build_task_table(cu, ctx, 4, 4, 128, True, 9, 1, 512, schedule=1)
+    b = build_task_table(cu, ctx, 4, 4, 128, True, 9, 1, 512, schedule=2)
     assert np.array_equal(a["tasks"], b["tasks"])
     assert b["loads"].tolist() == (a["loads"] * 128).tolist()
 
@@ -169,7 +169,7 @@ def test_mixed_schedule_interleaves_in_proportion_within_each_cta():
     ctx = q_lens + rng.integers(0, 3000, size=len(q_lens))
     cu = pack_cu_seqlens(q_lens)
     G, num_ctas, q_tile, chunk = 4, 11, 32, 512
-    b = build_task_table(cu, ctx, 8, 2, 128, True, num_ctas, q_tile, chunk, schedule=1)
+    b = build_task_table(cu, ctx, 8, 2, 128, True, num_ctas, q_tile, chunk, schedule=2)
     # rebuild the charged loads (padded 128-row tiles; small tasks as one tile), sort and deal
     recs = []
     for i in range(len(q_lens)):
@@ -185,9 +185,10 @@ def test_mixed_schedule_interleaves_in_proportion_within_each_cta():
     assert len(order) == len(b["tasks"])
     got = [tuple(int(v) for v in t[:6]) for t in b["tasks"]]
     load_of = {x[0]: x[1] for x in recs}
+    dealt_to = _serpentine_assignment(len(order), num_ctas)
     both = 0
     for c in range(num_ctas):
-        dealt = [recs[k][0] for k in order[c::num_ctas]]
+        dealt = [recs[order[p]][0] for p in range(len(order)) if dealt_to[p] == c]
         mine = got[c::num_ctas]
         assert sorted(mine) == sorted(dealt)
         assert int(b["cta_loads"][c]) == sum(load_of[x] for x in dealt)
@@ -223,6 +224,39 @@ def test_mixed_schedule_interleaves_in_proportion_within_each_cta():
     assert both > 0
 
 
+def _serpentine_assignment(N, n):
+    """CTA of each sorted position under the serpentine reading of "symmetric round-robin":
+    complete rounds alternate direction (round 0 forwards), the final partial round forwards."""
+    out = []
+    for p in range(N):
+        r, i = divmod(p, n)
+        backwards = r % 2 == 1 and (r + 1) * n <= N
+        out.append(n - 1 - i if backwards else i)
+    return out
+
+
+def test_serpentine_schedule_deals_alternate_rounds_backwards():
+    rng = np.random.default_rng(9)
+    q_lens = rng.integers(1, 60, size=15)
+    ctx = q_lens + rng.integers(0, 200, size=15)
+    cu = pack_cu_seqlens(q_lens)
+    num_ctas = 5
+    a = build_task_table(cu, ctx, 4, 2, 32, True, num_ctas, 8, 32, schedule=0)
+    s = build_task_table(cu, ctx, 4, 2, 32, True, num_ctas, 8, 32, schedule=1)
+    N = len(a["tasks"])
+    assert N % num_ctas != 0 and (N // num_ctas) % 2 == 1   # a partial final round after an odd one
+    sorted_tasks = [tuple(int(v) for v in t) for t in a["tasks"]]   # schedule 0 = the plain sorted list
+    cta = _serpentine_assignment(N, num_ctas)
+    for c in range(num_ctas):
+        mine = [sorted_tasks[p] for p in range(N) if cta[p] == c]
+        assert [tuple(int(v) for v in t) for t in s["tasks"][c::num_ctas]] == mine
+    # every CTA of a complete round gets one task of it; the sum of loads is unchanged
+    assert int(s["loads"].sum()) == int(a["loads"].sum())
+    assert sorted(s["loads"].tolist()) == sorted(a["loads"].tolist())
+    # on a sorted list the serpentine deal is never less balanced than the plain one here
+    assert s["balance"] >= a["balance"]
+
+
 def test_unknown_schedule_rejected():
     with pytest.raises(ValueError):
-        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=2)
+        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=3)
