@@ -17,12 +17,15 @@ def bits(t):
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None, schedule=2):
+def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None, schedule=2,
+        transform=None):
     """Run the CUDA step and the oracle step on workload `wl`.
 
     rows: list of (token, head) to compare, or None for every row.  sample_seqs: sequences whose
     pages the oracle receives (default: all).  pool_fill: value written to the whole pool before
     the step instead of random data (e.g. NaN, to check unused slots never leak into outputs).
+    transform: callable applied in place to the device tensors before the step (both sides see
+    its result).
     Returns dict with both sides' results and error statistics.
     """
     dev = torch.device("cuda")
@@ -30,6 +33,8 @@ def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=No
     if pool_fill is not None:
         vals["k_pool"].fill_(pool_fill)
         vals["v_pool"].fill_(pool_fill)
+    if transform is not None:
+        transform(vals)
     batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
                               wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
                               num_ctas=num_ctas, q_tile=q_tile, kv_chunk=kv_chunk, schedule=schedule)

@@ -93,6 +93,20 @@ def test_kind_switches_in_one_launch(schedule):
     assert_parity(run(wl, num_ctas=5, kv_chunk=512, schedule=schedule))
 
 
+def test_sharp_score_growth_across_tiles():
+    # K pages scaled by powers of two in random page order (and the new tokens' K by the largest),
+    # so a row's max jumps by far more than 2^24 between KV tiles: the tile softmax must raise its
+    # reference and rescale P, l and O on the fly; outputs are nearly one-hot and must still match
+    def spiky(vals):
+        g = torch.Generator().manual_seed(5)
+        f = torch.tensor([1.0, 4.0, 16.0, 64.0])[torch.randint(0, 4, (vals["k_pool"].shape[0],), generator=g)]
+        vals["k_pool"].mul_(f.to(vals["k_pool"].device, torch.bfloat16).view(-1, 1, 1, 1))
+        vals["k_new"].mul_(64.0)
+
+    wl = workloads.custom([300, 1, 129, 64], [1500, 2000, 700, 64], 16, 4, 128, 16, True, seed=81, name="spiky")
+    assert_parity(run(wl, transform=spiky))
+
+
 def test_full_size_decode_sampled():
     wl = workloads.decode()
     rng = np.random.default_rng(0)
