@@ -30,6 +30,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "xy.h"
 #include "xy_attn_common.cuh"
@@ -532,95 +533,105 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (rows_on) {
                     // a warp whose rows all see the whole tile skips the per-key mask
                         const bool full = __all_sync(0xffffffffu, kt0 + kTileKeys <= lim);
-                        // pass 1: masked row max; 32-column TMEM loads, the next one in flight while
-                        // the current one is reduced
-                        uint32_t ca[32], cb[32];
-                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                        auto max_chunk = [&](const uint32_t (&r)[32], int c0) {
-                            if (full) {
-    #pragma unroll
-                                for (int i = 0; i < 32; i += 8) {
-                                    m4[0] = xy::max3(m4[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                                    m4[1] = xy::max3(m4[1], __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                                    m4[2] = xy::max3(m4[2], __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
-                                    m4[3] = xy::max3(m4[3], __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                        // The tile's softmax is compiled twice -- without any masking code for
+                        // tiles every row of the warp sees whole, and with the per-key mask -- so
+                        // the common case carries no selects (the warp picks one per tile).
+                        auto tile_softmax = [&](auto full_c) {
+                            constexpr bool kFull = decltype(full_c)::value;
+                            // pass 1: masked row max; 32-column TMEM loads, the next one in flight while
+                            // the current one is reduced
+                            uint32_t ca[32], cb[32];
+                            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                            auto max_chunk = [&](const uint32_t (&r)[32], int c0) {
+                                if constexpr (kFull) {
+        #pragma unroll
+                                    for (int i = 0; i < 32; i += 8) {
+                                        m4[0] = xy::max3(m4[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                                        m4[1] = xy::max3(m4[1], __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                                        m4[2] = xy::max3(m4[2], __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+                                        m4[3] = xy::max3(m4[3], __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+                                    }
+                                } else {
+        #pragma unroll
+                                    for (int i = 0; i < 32; ++i)
+                                        m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
                                 }
-                            } else {
-    #pragma unroll
-                                for (int i = 0; i < 32; ++i)
-                                    m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
+                            };
+                            xy::tmem_ld32_nowait(s_addr, ca);
+                            xy::tmem_wait_ld(ca);
+                            xy::tmem_ld32_nowait(s_addr + 32, cb);
+                            max_chunk(ca, 0);
+                            xy::tmem_wait_ld(cb);
+                            xy::tmem_ld32_nowait(s_addr + 64, ca);
+                            max_chunk(cb, 32);
+                            xy::tmem_wait_ld(ca);
+                            xy::tmem_ld32_nowait(s_addr + 96, cb);
+                            max_chunk(ca, 64);
+                            xy::tmem_wait_ld(cb);
+                            xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
+                            max_chunk(cb, 96);
+                            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                            const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
+                            const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
+                            xy::tmem_wait_ld(ca);
+                            if (rescale) {
+                                const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
+                                m = m_new;
+                                l *= alpha;
+                                if (j > 0) {  // O_X has PV_X(0..j-1); rescale once the last of them is done
+                                    ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
+                                    xy::tc_fence_after();
+        #pragma unroll 1
+                                    for (int h = 0; h < 4; ++h) {
+                                        uint32_t orow[32];
+                                        xy::tmem_ld32(o_addr + h * 32, orow);
+        #pragma unroll
+                                        for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                                        xy::tmem_st32(o_addr + h * 32, orow);
+                                    }
+                                }
                             }
+                            // pass 2: p = 2^(s * scale_log2 - m) for 32 columns at a time, packed to bf16
+                            // pairs and written over S columns that pass 2 has already read
+                            const float neg_mu = m == -INFINITY ? 0.f : -m;
+                            const uint64_t sc2 = xy::f2_pack(p.scale_log2, p.scale_log2), nm2 = xy::f2_pack(neg_mu, neg_mu);
+                            uint64_t acc2[2] = {0ull, 0ull};
+                            auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
+                                uint32_t pk[16];
+        #pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
+                                    if constexpr (!kFull) {
+                                        s0 = kt0 + c0 + 2 * i < lim ? s0 : -INFINITY;
+                                        s1 = kt0 + c0 + 2 * i + 1 < lim ? s1 : -INFINITY;
+                                    }
+                                    float e0, e1;
+                                    xy::f2_unpack(xy::f2_fma(xy::f2_pack(s0, s1), sc2, nm2), e0, e1);
+                                    const float p0 = ex2(e0), p1 = ex2(e1);
+                                    acc2[i & 1] = xy::f2_add(acc2[i & 1], xy::f2_pack(p0, p1));
+                                    pk[i] = xy::pack_bf16x2(p0, p1);
+                                }
+                                xy::tmem_st16(s_addr + 16 * chunk, pk);
+                            };
+                            xy::tmem_ld32_nowait(s_addr + 32, cb);
+                            exp_chunk(ca, 0, 0);
+                            xy::tmem_wait_ld(cb);
+                            xy::tmem_ld32_nowait(s_addr + 64, ca);
+                            exp_chunk(cb, 32, 1);
+                            xy::tmem_wait_ld(ca);
+                            xy::tmem_ld32_nowait(s_addr + 96, cb);
+                            exp_chunk(ca, 64, 2);
+                            xy::tmem_wait_ld(cb);
+                            exp_chunk(cb, 96, 3);
+                            float ls4[4];
+                            xy::f2_unpack(acc2[0], ls4[0], ls4[1]);
+                            xy::f2_unpack(acc2[1], ls4[2], ls4[3]);
+                            l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                         };
-                        xy::tmem_ld32_nowait(s_addr, ca);
-                        xy::tmem_wait_ld(ca);
-                        xy::tmem_ld32_nowait(s_addr + 32, cb);
-                        max_chunk(ca, 0);
-                        xy::tmem_wait_ld(cb);
-                        xy::tmem_ld32_nowait(s_addr + 64, ca);
-                        max_chunk(cb, 32);
-                        xy::tmem_wait_ld(ca);
-                        xy::tmem_ld32_nowait(s_addr + 96, cb);
-                        max_chunk(ca, 64);
-                        xy::tmem_wait_ld(cb);
-                        xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
-                        max_chunk(cb, 96);
-                        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                        const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
-                        const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
-                        xy::tmem_wait_ld(ca);
-                        if (rescale) {
-                            const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
-                            m = m_new;
-                            l *= alpha;
-                            if (j > 0) {  // O_X has PV_X(0..j-1); rescale once the last of them is done
-                                ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
-                                xy::tc_fence_after();
-    #pragma unroll 1
-                                for (int h = 0; h < 4; ++h) {
-                                    uint32_t orow[32];
-                                    xy::tmem_ld32(o_addr + h * 32, orow);
-    #pragma unroll
-                                    for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
-                                    xy::tmem_st32(o_addr + h * 32, orow);
-                                }
-                            }
-                        }
-                        // pass 2: p = 2^(s * scale_log2 - m) for 32 columns at a time, packed to bf16
-                        // pairs and written over S columns that pass 2 has already read
-                        const float neg_mu = m == -INFINITY ? 0.f : -m;
-                        const uint64_t sc2 = xy::f2_pack(p.scale_log2, p.scale_log2), nm2 = xy::f2_pack(neg_mu, neg_mu);
-                        uint64_t acc2[2] = {0ull, 0ull};
-                        auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
-                            uint32_t pk[16];
-    #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-                                if (!full) {
-                                    s0 = kt0 + c0 + 2 * i < lim ? s0 : -INFINITY;
-                                    s1 = kt0 + c0 + 2 * i + 1 < lim ? s1 : -INFINITY;
-                                }
-                                float e0, e1;
-                                xy::f2_unpack(xy::f2_fma(xy::f2_pack(s0, s1), sc2, nm2), e0, e1);
-                                const float p0 = ex2(e0), p1 = ex2(e1);
-                                acc2[i & 1] = xy::f2_add(acc2[i & 1], xy::f2_pack(p0, p1));
-                                pk[i] = xy::pack_bf16x2(p0, p1);
-                            }
-                            xy::tmem_st16(s_addr + 16 * chunk, pk);
-                        };
-                        xy::tmem_ld32_nowait(s_addr + 32, cb);
-                        exp_chunk(ca, 0, 0);
-                        xy::tmem_wait_ld(cb);
-                        xy::tmem_ld32_nowait(s_addr + 64, ca);
-                        exp_chunk(cb, 32, 1);
-                        xy::tmem_wait_ld(ca);
-                        xy::tmem_ld32_nowait(s_addr + 96, cb);
-                        exp_chunk(ca, 64, 2);
-                        xy::tmem_wait_ld(cb);
-                        exp_chunk(cb, 96, 3);
-                        float ls4[4];
-                        xy::f2_unpack(acc2[0], ls4[0], ls4[1]);
-                        xy::f2_unpack(acc2[1], ls4[2], ls4[3]);
-                        l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+                        if (full)
+                            tile_softmax(std::true_type{});
+                        else
+                            tile_softmax(std::false_type{});
                     }
                     if (x == 0 && kt0 + kTileKeys > t.kv_end) {
                         // keys at or past kv_end: unused page slots or stale data; their P is 0 and
