@@ -669,34 +669,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int w = 0; w < 4; ++w) bad |= vote[x * 4 + w];
             if (rows_on) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t r[32];
-                    xy::tmem_ld32(o_addr + cc * 32, r);
-                    if (valid && !bad) {
-                        if (t.num_splits == 1) {
-                            const int64_t tok = f.seq_start + t.q_start + row / p.G;
-                            const int h = t.kv_head * p.G + row % p.G;
-                            uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.Hq + h) * HD + cc * 32);
+                // each thread writes its own row: 32-byte stores (one full sector each) when the
+                // buffers allow, the next 32 O columns loading from TMEM meanwhile
+                const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | reinterpret_cast<uintptr_t>(p.ws_o)) & 31) == 0;
+                auto store_chunk = [&](const uint32_t (&r)[32], int cc) {
+                    if (!valid || bad) return;
+                    if (t.num_splits == 1) {
+                        const int64_t tok = f.seq_start + t.q_start + row / p.G;
+                        const int h = t.kv_head * p.G + row % p.G;
+                        __nv_bfloat16 *dst = p.out + (tok * p.Hq + h) * HD + cc * 32;
+                        uint32_t w[16];
 #pragma unroll
-                            for (int v = 0; v < 4; ++v) {
-                                uint4 w;
-                                w.x = xy::pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-                                w.y = xy::pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-                                w.z = xy::pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-                                w.w = xy::pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-                                dst[v] = w;
-                            }
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = xy::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                        if (v8) {
+                            xy::st_global_v8(dst, reinterpret_cast<const uint32_t(&)[8]>(w[0]));
+                            xy::st_global_v8(dst + 16, reinterpret_cast<const uint32_t(&)[8]>(w[8]));
                         } else {
-                            const int64_t wr = (int64_t)t.ws_row + row;
-                            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + wr * HD + cc * 32);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                        }
+                    } else {
+                        float *dst = p.ws_o + ((int64_t)t.ws_row + row) * HD + cc * 32;
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(r[i]) * inv);
+                        if (v8) {
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                xy::st_global_v8(dst + 8 * v, reinterpret_cast<const uint32_t(&)[8]>(w[8 * v]));
+                        } else {
 #pragma unroll
                             for (int v = 0; v < 8; ++v)
-                                dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                                     __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+                                reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                         }
                     }
-                }
+                };
+                uint32_t ra[32], rb[32];
+                xy::tmem_ld32_nowait(o_addr, ra);
+                xy::tmem_wait_ld(ra);
+                xy::tmem_ld32_nowait(o_addr + 32, rb);
+                store_chunk(ra, 0);
+                xy::tmem_wait_ld(rb);
+                xy::tmem_ld32_nowait(o_addr + 64, ra);
+                store_chunk(rb, 1);
+                xy::tmem_wait_ld(ra);
+                xy::tmem_ld32_nowait(o_addr + 96, rb);
+                store_chunk(ra, 2);
+                xy::tmem_wait_ld(rb);
+                store_chunk(rb, 3);
                 if (valid && !bad && t.num_splits > 1) p.ws_lse[(int64_t)t.ws_row + row] = l > 0.f ? m + __log2f(l) : -INFINITY;
             }
             if (active) {
