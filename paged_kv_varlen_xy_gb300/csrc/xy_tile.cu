@@ -542,8 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // the current one is reduced
                             uint32_t ca[32], cb[32];
                             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                            // in a masked tile a 32-key chunk is still whole or empty for all rows of
+                            // the warp unless it holds one of their limits (warp-uniform tests)
+                            auto chunk_whole = [&](int c0) { return kFull || __all_sync(0xffffffffu, kt0 + c0 + 32 <= lim); };
+                            auto chunk_empty = [&](int c0) { return !kFull && __all_sync(0xffffffffu, kt0 + c0 >= lim); };
                             auto max_chunk = [&](const uint32_t (&r)[32], int c0) {
-                                if constexpr (kFull) {
+                                if (chunk_whole(c0)) {
         #pragma unroll
                                     for (int i = 0; i < 32; i += 8) {
                                         m4[0] = xy::max3(m4[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         m4[2] = xy::max3(m4[2], __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
                                         m4[3] = xy::max3(m4[3], __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
                                     }
-                                } else {
+                                } else if (!chunk_empty(c0)) {
         #pragma unroll
                                     for (int i = 0; i < 32; ++i)
                                         m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
@@ -596,12 +600,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float neg_mu = m == -INFINITY ? 0.f : -m;
                             const uint64_t sc2 = xy::f2_pack(p.scale_log2, p.scale_log2), nm2 = xy::f2_pack(neg_mu, neg_mu);
                             uint64_t acc2[2] = {0ull, 0ull};
-                            auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
-                                uint32_t pk[16];
+                            auto exp_loop = [&](const uint32_t (&r)[32], int c0, uint32_t (&pk)[16], auto masked_c) {
+                                constexpr bool kMasked = decltype(masked_c)::value;
         #pragma unroll
                                 for (int i = 0; i < 16; ++i) {
                                     float s0 = __uint_as_float(r[2 * i]), s1 = __uint_as_float(r[2 * i + 1]);
-                                    if constexpr (!kFull) {
+                                    if constexpr (kMasked) {
                                         s0 = kt0 + c0 + 2 * i < lim ? s0 : -INFINITY;
                                         s1 = kt0 + c0 + 2 * i + 1 < lim ? s1 : -INFINITY;
                                     }
@@ -610,6 +614,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const float p0 = ex2(e0), p1 = ex2(e1);
                                     acc2[i & 1] = xy::f2_add(acc2[i & 1], xy::f2_pack(p0, p1));
                                     pk[i] = xy::pack_bf16x2(p0, p1);
+                                }
+                            };
+                            auto exp_chunk = [&](const uint32_t (&r)[32], int c0, int chunk) {
+                                uint32_t pk[16];
+                                if (chunk_whole(c0)) {
+                                    exp_loop(r, c0, pk, std::false_type{});
+                                } else if (chunk_empty(c0)) {
+        #pragma unroll
+                                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                                } else {
+                                    exp_loop(r, c0, pk, std::true_type{});
                                 }
                                 xy::tmem_st16(s_addr + 16 * chunk, pk);
                             };
