@@ -249,6 +249,17 @@ xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
                                      size_t workspace_bytes, int32_t *err_word, void *out,
                                      void *stream);
 
+/* Self-test of the bounded waits (no counterpart in the pages; not a step of the path).
+ * Every mbarrier wait in the attention kernels gives up after a time limit, or when its CTA's
+ * abort flag is raised, sets XY_DEV_TIMEOUT in *err_word and lets the kernel return instead of
+ * hanging the GPU.  This launches one CTA whose first warp waits on a barrier nobody arrives at
+ * with a limit of limit_us microseconds (1 .. 10^7), then raises the abort flag that releases the
+ * second warp's wait (which has the kernels' own 2 s limit).  result (device, 3 int32, caller
+ * owned): [0] 1 if the first wait succeeded (it must not), [1] microseconds it waited, [2] 1 if
+ * the second wait succeeded (it must not).  *err_word (device) gets XY_DEV_TIMEOUT.  Asynchronous
+ * on `stream`; XY_ERR_INVALID_ARG for null pointers or a limit out of range. */
+xy_status xy_selftest_bounded_wait(uint32_t limit_us, int32_t *err_word, int32_t *result, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ XY_DEV_TIMEOUT = 0x8
 
 C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
-         "xy_paged_attention_noalloc")
+         "xy_paged_attention_noalloc", "xy_selftest_bounded_wait")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -85,6 +85,8 @@ def lib():
     L.xy_paged_attention_noalloc.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, SZ, P, P,
                                              P]
     L.xy_paged_attention_noalloc.restype = I
+    L.xy_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P, P]
+    L.xy_selftest_bounded_wait.restype = I
     _lib = L
     return L
 
@@ -243,6 +245,17 @@ def xy_paged_attention_noalloc(q, cu_seqlens_q, context_lens, block_table, k_pag
         _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), int(workspace_bytes),
         _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)),
         "xy_paged_attention_noalloc")
+
+
+def xy_selftest_bounded_wait(limit_us, err_word, result, stream=None):
+    """Self-test of the kernels' bounded waits (see include/xy.h): err_word int32 [1] and
+    result int32 [3] on the device."""
+    import torch
+    if result.numel() < 3:
+        raise ValueError("result must hold 3 int32")
+    _check(lib().xy_selftest_bounded_wait(int(limit_us), _dev(err_word, torch.int32, "err_word"),
+                                          _dev(result, torch.int32, "result"), _stream(stream)),
+           "xy_selftest_bounded_wait")
 
 
 def check_err_word(err_word):

@@ -58,14 +58,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete.  Returns false after kWaitTimeoutNs, or
 // as soon as *abort (a CTA-wide flag in shared memory, may be null) becomes non-zero.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort = nullptr) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, const volatile int *abort,
+                                              uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
         if (abort && *abort) return false;
-        if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int *abort = nullptr) {
+    return mbar_wait_for(bar, parity, abort, kWaitTimeoutNs);
 }
 
 // 2-D tiled TMA load global -> shared, completion counted on `bar` in bytes.
