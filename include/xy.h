@@ -167,7 +167,13 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  * charged loads, CTA c starting at phase c / num_ctas, so that at any time about the small tasks'
  * share of the CTAs streams KV from HBM while the others keep the tensor cores busy.  The per-CTA
  * load sums (stats) are those of the deal.  XY_SCHEDULE_MIXED returns XY_ERR_UNSUPPORTED when the
- * total charged load reaches 2^55 or num_ctas exceeds 65536.
+ * total charged load reaches 2^55 or num_ctas exceeds 65536.  XY_SCHEDULE_GREEDY charges a task
+ * 128 * max(1, ceil(rows / 128)) * (keys + XY_SCHEDULE_TASK_KEYS) (its padded MMA area plus a
+ * fixed per-task cost: query load, pipeline fill, output epilogue), sorts the same way and hands
+ * each task to the CTA with the smallest load so far (the lowest index on ties), longest first.
+ * CTAs then hold different numbers of tasks: the table keeps the layout above and the positions
+ * a CTA does not use hold hole records {-1, 0, 0, 0, 0, 0, 0, -1}, which the kernels skip, so
+ * *num_tasks counts the holes too (num_ctas times the longest list).
  *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs]: host int32.
  *   tasks [max_tasks], merges [max_merges]: host outputs; pass NULL (with max 0) to query counts.
  *   *num_tasks, *num_merges: counts; *workspace_bytes = rows * (head_dim + 1) * 4 (fp32 partial
@@ -178,6 +184,8 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
 #define XY_SCHEDULE_AREA 0        /* the pages' reorder: load = area, sort, round-robin deal */
 #define XY_SCHEDULE_SERPENTINE 1  /* the same sort, serpentine ("symmetric round-robin") deal */
 #define XY_SCHEDULE_MIXED 2       /* padded-tile load, sort, serpentine deal, per-CTA interleave */
+#define XY_SCHEDULE_GREEDY 3      /* padded-tile load + per-task cost, greedy deal, hole records */
+#define XY_SCHEDULE_TASK_KEYS 512 /* per-task cost of XY_SCHEDULE_GREEDY, in keys */
 #define XY_SCHEDULE_TILE_ROWS 128 /* MMA tile height: the unit of XY_SCHEDULE_MIXED's load */
 #define XY_SCHEDULE_SMALL_ROWS 16 /* tasks of at most this many rows count as small */
 

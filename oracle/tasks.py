@@ -23,6 +23,7 @@ Readings taken here (the pages are written for 16 x 16 Ascend blocks):
 """
 
 from fractions import Fraction
+import heapq
 
 import numpy as np
 
@@ -42,11 +43,18 @@ MERGE_FIELDS = ("seq", "kv_head", "q_start", "q_rows", "num_splits", "ws_row", "
 #   interleaves its small and large tasks in proportion to their charged loads, starting at phase
 #   c / num_ctas of its timeline, so that at any moment about the small tasks' share of the CTAs
 #   streams KV while the others keep the tensor cores busy.
+# * 3 deals greedily (longest processing time first): tasks sorted by a load that also charges
+#   a fixed per-task cost, TILE_ROWS * max(1, ceil(rows / TILE_ROWS)) * (keys + TASK_KEYS), each to
+#   the CTA with the smallest load so far (the lowest index on ties).  CTAs then hold different
+#   numbers of tasks; the table keeps the layout "CTA c runs positions c, c + num_ctas, ..." and
+#   fills the positions a CTA does not use with HOLE records, which the kernels skip.
 SMALL_ROWS = 16
 TILE_ROWS = 128
+TASK_KEYS = 512
 MAX_TOTAL_LOAD = 1 << 55
 MAX_CTAS = 1 << 16
-SCHEDULES = (0, 1, 2)
+SCHEDULES = (0, 1, 2, 3)
+HOLE = (-1, 0, 0, 0, 0, 0, 0, -1)
 
 
 def _serpentine(order, num_ctas):
@@ -87,10 +95,10 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
     CTA c runs tasks c, c + num_ctas, c + 2*num_ctas, ... of ``tasks``.
     schedule 0: the pages' reorder (load = area, stable sort descending, round-robin deal).
     schedule 1: the same sort, serpentine deal.  schedule 2: charged load, serpentine deal and
-    per-CTA proportional interleave (see above).
+    per-CTA proportional interleave.  schedule 3: greedy deal with HOLE records (see above).
     """
     if schedule not in SCHEDULES:
-        raise ValueError("schedule must be 0, 1 or 2")
+        raise ValueError("schedule must be 0, 1, 2 or 3")
     if num_heads_q % num_heads_kv:
         raise ValueError("Hq must be a multiple of Hkv")
     if q_tile < 1 or kv_chunk < 1 or num_ctas < 1:
@@ -124,7 +132,10 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
                     r = rows * G
                     if schedule == 2:
                         r = _charged_rows(r)
-                    loads.append(r * (k1 - k0))
+                    if schedule == 3:
+                        loads.append(_charged_rows(r) * (k1 - k0 + TASK_KEYS))
+                    else:
+                        loads.append(r * (k1 - k0))
 
     order = sorted(range(len(records)), key=lambda k: loads[k], reverse=True)
     if schedule in (1, 2):
@@ -139,8 +150,22 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
             small = [(k, loads[k]) for k in (order[q] for q in pos) if records[k][3] * G <= SMALL_ROWS]
             for q, k in zip(pos, _interleave(big, small, c, num_ctas)):
                 order[q] = k
-    tasks = np.array([records[k] for k in order], dtype=np.int32).reshape(-1, 8)
-    sorted_loads = np.array([loads[k] for k in order], dtype=np.int64)
+    if schedule == 3:
+        if sum(loads) >= MAX_TOTAL_LOAD:
+            raise ValueError("total load too large for schedule 3")
+        heap = [(0, c) for c in range(num_ctas)]
+        lists = [[] for _ in range(num_ctas)]
+        for k in order:
+            ld, c = heapq.heappop(heap)
+            lists[c].append(k)
+            heapq.heappush(heap, (ld + loads[k], c))
+        depth = max((len(x) for x in lists), default=0)
+        order = [None] * (depth * num_ctas)
+        for c, lst in enumerate(lists):
+            for pos, k in enumerate(lst):
+                order[pos * num_ctas + c] = k
+    tasks = np.array([records[k] if k is not None else HOLE for k in order], dtype=np.int32).reshape(-1, 8)
+    sorted_loads = np.array([loads[k] if k is not None else 0 for k in order], dtype=np.int64)
 
     cta_loads = np.zeros(num_ctas, dtype=np.int64)
     for pos, ld in enumerate(sorted_loads):

@@ -149,6 +149,7 @@ def xy_build_block_table(context_lens, block_size, free_list, max_blocks):
 XY_SCHEDULE_AREA = 0
 XY_SCHEDULE_SERPENTINE = 1
 XY_SCHEDULE_MIXED = 2
+XY_SCHEDULE_GREEDY = 3
 
 
 def xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, num_ctas,
@@ -281,7 +282,7 @@ class Plan:
     cu_seqlens_q and context_lens) uploaded to the device, and the workspace it needs."""
 
     def __init__(self, cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, device="cuda",
-                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=XY_SCHEDULE_MIXED):
+                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=XY_SCHEDULE_GREEDY):
         import torch
         dev = torch.device(device)
         self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)

@@ -104,6 +104,11 @@ __global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
+            if (xy::is_hole(tc.cur.t)) {
+                pref_valid = false;
+                tc.advance(p);
+                continue;
+            }
             if (!xy::dec::task_ok<RG>(tc.cur, p)) {
                 if (lane == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
                 pref_valid = false;

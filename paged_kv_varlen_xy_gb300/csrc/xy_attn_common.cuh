@@ -91,6 +91,9 @@ __device__ __forceinline__ int load_window(const AttnParams &p, int seq, int b0,
     return (idx >= 0 && idx < p.MB) ? __ldg(p.bt + (int64_t)seq * p.MB + idx) : -1;
 }
 
+// A hole record of a greedy deal (a position its CTA does not use): every role skips it.
+__device__ __forceinline__ bool is_hole(const xy_task &t) { return t.seq == -1 && t.q_rows == 0; }
+
 // Checks every kernel applies to a task before touching memory through it.
 __device__ __forceinline__ bool task_common_ok(const TaskInfo &f, const AttnParams &p) {
     const xy_task &t = f.t;

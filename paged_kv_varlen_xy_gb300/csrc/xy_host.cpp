@@ -9,6 +9,8 @@
 #include <cstdio>
 #include <cstring>
 #include <limits>
+#include <queue>
+#include <utility>
 #include <vector>
 
 #include "xy.h"
@@ -128,7 +130,8 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
         return XY_ERR_INVALID_ARG;
     if (num_seqs > 0 && !context_lens) return XY_ERR_INVALID_ARG;
     if (num_heads_q % num_heads_kv) return XY_ERR_INVALID_ARG;
-    if (schedule != XY_SCHEDULE_AREA && schedule != XY_SCHEDULE_SERPENTINE && schedule != XY_SCHEDULE_MIXED)
+    if (schedule != XY_SCHEDULE_AREA && schedule != XY_SCHEDULE_SERPENTINE && schedule != XY_SCHEDULE_MIXED &&
+        schedule != XY_SCHEDULE_GREEDY)
         return XY_ERR_INVALID_ARG;
     if (cu_seqlens_q[0] != 0) return XY_ERR_CU_SEQLENS;
     const int G = num_heads_q / num_heads_kv;
@@ -174,11 +177,12 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
                     r.t.kv_end = (int32_t)k1;
                     r.t.num_splits = (int32_t)nsplit;
                     r.t.ws_row = nsplit == 1 ? -1 : (int32_t)(base + c * rows * G);
-                    int64_t charged = rows * G;
-                    if (schedule == XY_SCHEDULE_MIXED)
+                    int64_t charged = rows * G, keys = k1 - k0;
+                    if (schedule == XY_SCHEDULE_MIXED || schedule == XY_SCHEDULE_GREEDY)
                         charged = XY_SCHEDULE_TILE_ROWS *
                                   std::max<int64_t>(1, (charged + XY_SCHEDULE_TILE_ROWS - 1) / XY_SCHEDULE_TILE_ROWS);
-                    r.load = charged * (k1 - k0);
+                    if (schedule == XY_SCHEDULE_GREEDY) keys += XY_SCHEDULE_TASK_KEYS;
+                    r.load = charged * keys;
                     recs.push_back(r);
                 }
             }
@@ -204,6 +208,34 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
             for (size_t q = c; q < n; q += num_ctas) recs[q] = out[k++];
         }
     }
+    if (schedule == XY_SCHEDULE_GREEDY) {
+        int64_t total = 0;
+        for (const Rec &r : recs) total += r.load;
+        if (total >= (int64_t(1) << 55)) return XY_ERR_UNSUPPORTED;
+        // longest processing time first: each task (in sorted order) to the least loaded CTA,
+        // the lowest index on ties; unused positions become holes
+        using Slot = std::pair<int64_t, int>;
+        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+        for (int c = 0; c < num_ctas; ++c) heap.push({0, c});
+        std::vector<std::vector<size_t>> lists(num_ctas);
+        for (size_t k = 0; k < recs.size(); ++k) {
+            Slot s = heap.top();
+            heap.pop();
+            lists[s.second].push_back(k);
+            heap.push({s.first + recs[k].load, s.second});
+        }
+        size_t depth = 0;
+        for (const auto &l : lists) depth = std::max(depth, l.size());
+        if (depth * (size_t)num_ctas > (size_t)std::numeric_limits<int32_t>::max()) return XY_ERR_UNSUPPORTED;
+        Rec hole;
+        hole.t = xy_task{-1, 0, 0, 0, 0, 0, 0, -1};
+        hole.load = 0;
+        std::vector<Rec> dealt(depth * (size_t)num_ctas, hole);
+        for (int c = 0; c < num_ctas; ++c)
+            for (size_t pos = 0; pos < lists[c].size(); ++pos) dealt[pos * num_ctas + c] = recs[lists[c][pos]];
+        recs.swap(dealt);
+    }
+
     *num_tasks = (int)recs.size();
     *num_merges = (int)mrg.size();
     *workspace_bytes = (size_t)ws_rows * (size_t)(head_dim + 1) * 4u;

@@ -184,6 +184,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
+            if (xy::is_hole(tc.cur.t)) {
+                pref_valid = false;
+                tc.advance(p);
+                continue;
+            }
             const bool tile = mine(tc.cur, p);
             if (!(tile ? tile_ok(tc.cur, p) : xy::dec::task_ok<DecRing>(tc.cur, p))) {
                 if (lane == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);

@@ -12,7 +12,7 @@ class PagedBatch:
     buffer and the attention plan.  Built from host arrays (the scheduler's view of the batch)."""
 
     def __init__(self, cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
-                 head_dim, causal, device="cuda", num_ctas=None, q_tile=None, kv_chunk=None, schedule=2):
+                 head_dim, causal, device="cuda", num_ctas=None, q_tile=None, kv_chunk=None, schedule=3):
         dev = torch.device(device)
         self.cu_host = np.asarray(cu_seqlens_q, dtype=np.int32)
         self.ctx_host = np.asarray(context_lens, dtype=np.int32)

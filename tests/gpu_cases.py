@@ -17,7 +17,7 @@ def bits(t):
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None, schedule=2,
+def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None, schedule=3,
         transform=None):
     """Run the CUDA step and the oracle step on workload `wl`.
 

@@ -259,4 +259,41 @@ def test_serpentine_schedule_deals_alternate_rounds_backwards():
 
 def test_unknown_schedule_rejected():
     with pytest.raises(ValueError):
-        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=3)
+        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=4)
+
+
+def test_greedy_schedule_is_longest_processing_time_first():
+    rng = np.random.default_rng(12)
+    q_lens = np.concatenate([rng.integers(30, 400, size=6), np.ones(30, dtype=np.int64)])
+    ctx = q_lens + rng.integers(0, 3000, size=len(q_lens))
+    cu = pack_cu_seqlens(q_lens)
+    n, G = 7, 4
+    g = build_task_table(cu, ctx, 8, 2, 128, True, n, 32, 512, schedule=3)
+    a = build_task_table(cu, ctx, 8, 2, 128, True, n, 32, 512, schedule=0)
+    real = [tuple(int(v) for v in t) for t in a["tasks"]]
+    # the same tasks, plus hole records; the table is num_ctas times the longest list
+    got = [tuple(int(v) for v in t) for t in g["tasks"]]
+    holes = [t for t in got if t == (-1, 0, 0, 0, 0, 0, 0, -1)]
+    assert sorted(t for t in got if t[0] >= 0) == sorted(real)
+    assert len(got) % n == 0 and len(got) == len(real) + len(holes)
+    # independent restatement: charged load, stable sort, each task to the least loaded CTA
+    def charged(t):
+        rows = t[3] * G
+        return 128 * max(1, -(-rows // 128)) * (t[5] - t[4] + 512)
+    real.sort(key=lambda t: (t[0], t[1], t[2], t[4]))       # enumeration order
+    order = sorted(range(len(real)), key=lambda k: charged(real[k]), reverse=True)
+    load = [0] * n
+    lists = [[] for _ in range(n)]
+    for k in order:
+        c = min(range(n), key=lambda c: (load[c], c))
+        lists[c].append(real[k])
+        load[c] += charged(real[k])
+    for c in range(n):
+        mine = [t for t in got[c::n] if t[0] >= 0]
+        assert mine == lists[c]
+        # a CTA's holes come after its tasks
+        seq = [t[0] >= 0 for t in got[c::n]]
+        assert seq == sorted(seq, reverse=True)
+    assert g["cta_loads"].tolist() == load
+    # greedy never balances worse than the plain deal of the same charged loads
+    assert g["balance"] >= min(load) / max(load) - 1e-12
