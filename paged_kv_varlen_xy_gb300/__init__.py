@@ -269,12 +269,13 @@ def check_err_word(err_word):
 def default_tiles(num_heads_q, num_heads_kv, head_dim=128):
     """Tile policy of the kernels.  With head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
     256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise up to 64 rows
-    (q_tile = 64 // G).  KV chunks are 4096 keys, a multiple of every page size and of both
-    kernels' KV tiles."""
+    (q_tile = 64 // G).  KV chunks are 8192 keys, a multiple of every page size and of both
+    kernels' KV tiles: long enough that split partials and merges stay few, short enough that a
+    few long contexts still spread over the SMs (measured on the mixed and long-context batches)."""
     G = num_heads_q // num_heads_kv
     if head_dim == 128 and 128 % G == 0:
-        return 256 // G, 4096
-    return max(1, 64 // G), 4096
+        return 256 // G, 8192
+    return max(1, 64 // G), 8192
 
 
 class Plan:
