@@ -257,6 +257,21 @@ xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
                                      size_t workspace_bytes, int32_t *err_word, void *out,
                                      void *stream);
 
+/* 8-bit KV pages (a variant of the pool; [CANN] §5.2 keeps scale metadata beside the pages).
+ * k_pages/v_pages: uint8 [P, Hkv, bs, d] of OCP E4M3 codes ("E4M3FN": bias 7, max 448, no
+ * infinities); k_scales/v_scales: fp32 [P, Hkv, bs], one scale per stored (token, KV head) row;
+ * the row's values are code * scale.  Appending a row quantizes it with s = max|x| / 448 (1 for an
+ * all-zero row) and codes = E4M3(x / s) rounded to nearest even and saturated to +-448, both
+ * IEEE fp32 operations, so rows already in a page are never rescaled.
+ *
+ * xy_kv_append_fp8: the append of xy_kv_append for 8-bit pages.  k_new/v_new [T, Hkv, d] bf16
+ * (16-byte aligned), slot_mapping [T] int64 (negative = skip), d in {64, 128}, bs a power of two
+ * >= 16.  A slot outside [0, P*bs) sets XY_DEV_SLOT_OOB and is skipped.  Device pointers,
+ * asynchronous on `stream`; XY_ERR_UNSUPPORTED for other head dims. */
+xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping, int num_tokens,
+                           void *k_pages, void *v_pages, float *k_scales, float *v_scales, int num_pages,
+                           int num_heads_kv, int block_size, int head_dim, int32_t *err_word, void *stream);
+
 /* Self-test of the bounded waits (no counterpart in the pages; not a step of the path).
  * Every mbarrier wait in the attention kernels gives up after a time limit, or when its CTA's
  * abort flag is raised, sets XY_DEV_TIMEOUT in *err_word and lets the kernel return instead of

@@ -23,7 +23,8 @@ Sources (web pages on the subject; cited by title and section):
 * [CANN]  cann-recipes-infer Paged KV Cache / Packed Sequence notes (dpshk.com/news/5336026):
           §2.2 (paged KV cache, page table), §2.3 (packed sequence, cu_seqlens),
           §3.1 (page pool layout), §3.2 (page allocation), §3.3 (packed paged_attention
-          call), §4.4 (fault checks), §5.3 (page-size rule).
+          call), §4.4 (fault checks), §5.2 (scale metadata beside the pages), §5.3
+          (page-size rule).
 * [ATB]   ATB dynamic batching / speculative decoding / KV reuse notes
           (ai6s.net/6a38a2a6662f9a54cb828d66): "KV缓存复用", "端到端推理调优".
 
@@ -53,6 +54,7 @@ from .attention import (
     virtual_mask,
 )
 from .tasks import build_task_table, TASK_FIELDS, MERGE_FIELDS
+from .fp8 import e4m3_to_f64, f64_to_e4m3, quantize_rows, dequantize, kv_append_fp8
 from . import step
 
 __all__ = [
@@ -69,6 +71,11 @@ __all__ = [
     "split_row_partials",
     "combine_partials",
     "virtual_mask",
+    "e4m3_to_f64",
+    "f64_to_e4m3",
+    "quantize_rows",
+    "dequantize",
+    "kv_append_fp8",
     "build_task_table",
     "TASK_FIELDS",
     "MERGE_FIELDS",

@@ -22,7 +22,7 @@ XY_DEV_TIMEOUT = 0x8
 
 C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
-         "xy_paged_attention_noalloc", "xy_selftest_bounded_wait")
+         "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -87,6 +87,8 @@ def lib():
     L.xy_paged_attention_noalloc.restype = I
     L.xy_selftest_bounded_wait.argtypes = [ctypes.c_uint32, P, P, P]
     L.xy_selftest_bounded_wait.restype = I
+    L.xy_kv_append_fp8.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, P, P]
+    L.xy_kv_append_fp8.restype = I
     _lib = L
     return L
 
@@ -246,6 +248,25 @@ def xy_paged_attention_noalloc(q, cu_seqlens_q, context_lens, block_table, k_pag
         _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), int(workspace_bytes),
         _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)),
         "xy_paged_attention_noalloc")
+
+
+def xy_kv_append_fp8(k_new, v_new, slot_mapping, k_pages, v_pages, k_scales, v_scales, err_word, stream=None):
+    """a3 for 8-bit pages: quantizes k_new/v_new [T, Hkv, d] bf16 into k_pages/v_pages [P, Hkv, bs, d]
+    uint8 (E4M3 codes) with one fp32 scale per row in k_scales/v_scales [P, Hkv, bs]."""
+    import torch
+    P, Hkv, bs, d = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or tuple(k_new.shape) != tuple(v_new.shape):
+        raise ValueError("K and V shapes differ")
+    if tuple(k_scales.shape) != (P, Hkv, bs) or tuple(v_scales.shape) != (P, Hkv, bs):
+        raise ValueError("scales must be [P, Hkv, bs]")
+    if k_new.shape[1:] != (Hkv, d) or k_new.shape[0] != slot_mapping.numel():
+        raise ValueError("k_new must be [T, Hkv, d] with T = len(slot_mapping)")
+    bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+    _check(lib().xy_kv_append_fp8(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"),
+                                  _dev(slot_mapping, torch.int64, "slot_mapping"), k_new.shape[0],
+                                  _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
+                                  _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv, bs, d,
+                                  _dev(err_word, torch.int32, "err_word"), _stream(stream)), "xy_kv_append_fp8")
 
 
 def xy_selftest_bounded_wait(limit_us, err_word, result, stream=None):

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libxy.so")
 
-SOURCES = ["xy_host.cpp", "xy_append.cu", "xy_attention.cu", "xy_tile.cu", "xy_selftest.cu"]
+SOURCES = ["xy_host.cpp", "xy_append.cu", "xy_attention.cu", "xy_tile.cu", "xy_selftest.cu", "xy_fp8.cu"]
 HEADERS = ["xy_device.cuh", "xy_attn_common.cuh", "xy_decode_path.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,0 +1,105 @@
+// 8-bit KV pages: the append that quantizes new K/V rows into E4M3 pages with one fp32 scale per
+// (token, KV head) row.
+//
+// cann-recipes-infer Paged KV Cache notes (dpshk.com/news/5336026) §5.2: scale metadata kept
+// beside the pages so values can be stored narrower than they are computed in.  Here every stored
+// row has its own scale s = max|x| / 448 (1 for an all-zero row) and its elements are the E4M3
+// codes of x / s (round to nearest even, saturating at +-448), so appending a token never rescales
+// rows already in a page.  The scale and the division are IEEE fp32 operations.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "xy.h"
+#include "xy_device.cuh"
+
+namespace {
+
+// Two fp32 values -> two E4M3 codes in memory order (lo first).
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// One warp per (token, KV head) row of K and of V; D = head_dim (64 or 128).
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __nv_bfloat16 *__restrict__ k_new,
+                                                             const __nv_bfloat16 *__restrict__ v_new,
+                                                             const int64_t *__restrict__ slots, int T, int H, int bs,
+                                                             int64_t pool_slots, uint8_t *__restrict__ k_pages,
+                                                             uint8_t *__restrict__ v_pages, float *__restrict__ k_scales,
+                                                             float *__restrict__ v_scales, int32_t *err) {
+    constexpr int E = D / 32;  // elements per lane
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < 2 * (int64_t)T * H;
+         row += warps) {
+        const int tensor = (int)(row / ((int64_t)T * H));  // 0: K, 1: V
+        const int64_t th = row - tensor * (int64_t)T * H;
+        const int64_t t = th / H;
+        const int h = (int)(th - t * H);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= pool_slots) {
+            if (lane == 0 && tensor == 0 && h == 0) xy::set_err(err, XY_DEV_SLOT_OOB);
+            continue;
+        }
+        const __nv_bfloat16 *src = (tensor ? v_new : k_new) + th * D + lane * E;
+        float x[E];
+#pragma unroll
+        for (int i = 0; i < E; i += 2) {
+            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(src + i);
+            x[i] = __low2float(pr);
+            x[i + 1] = __high2float(pr);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        uint16_t code[E / 2];
+#pragma unroll
+        for (int i = 0; i < E; i += 2) code[i / 2] = e4m3x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
+        const int64_t page = slot / bs, off = slot - page * bs;
+        const int64_t drow = (page * H + h) * bs + off;
+        uint8_t *dst = (tensor ? v_pages : k_pages) + drow * D + lane * E;
+        if (E == 4)
+            *reinterpret_cast<uint32_t *>(dst) = (uint32_t)code[0] | ((uint32_t)code[E / 2 - 1] << 16);
+        else
+            *reinterpret_cast<uint16_t *>(dst) = code[0];
+        if (lane == 0) (tensor ? v_scales : k_scales)[drow] = s;
+    }
+}
+
+}  // namespace
+
+extern "C" xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                                      int num_tokens, void *k_pages, void *v_pages, float *k_scales,
+                                      float *v_scales, int num_pages, int num_heads_kv, int block_size,
+                                      int head_dim, int32_t *err_word, void *stream) {
+    if (num_tokens < 0 || num_pages < 1 || num_heads_kv < 1 || block_size < 16 || (block_size & (block_size - 1)))
+        return XY_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return XY_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return XY_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_pages || !v_pages || !k_scales || !v_scales || !err_word)
+        return XY_ERR_INVALID_ARG;
+    if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15) return XY_ERR_INVALID_ARG;
+    const int64_t rows = 2 * (int64_t)num_tokens * num_heads_kv;
+    const int threads = 256, blocks = (int)((rows + 7) / 8 < 4096 ? (rows + 7) / 8 : 4096);
+    const int64_t pool_slots = (int64_t)num_pages * block_size;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_dim == 128)
+        kv_append_fp8_kernel<128><<<blocks, threads, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new), slot_mapping,
+            num_tokens, num_heads_kv, block_size, pool_slots, static_cast<uint8_t *>(k_pages),
+            static_cast<uint8_t *>(v_pages), k_scales, v_scales, err_word);
+    else
+        kv_append_fp8_kernel<64><<<blocks, threads, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new), slot_mapping,
+            num_tokens, num_heads_kv, block_size, pool_slots, static_cast<uint8_t *>(k_pages),
+            static_cast<uint8_t *>(v_pages), k_scales, v_scales, err_word);
+    return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
+}
