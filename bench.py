@@ -72,15 +72,17 @@ def measured_traffic(config):
     return e["bytes_per_launch"] if h.hexdigest()[:16] == e["kernel_hash"] else None
 
 
-def work(wl):
+def work(wl, kv="bf16"):
     """Algorithmic work of one step: attention bytes (K/V read once + Q in + O out), append bytes
-    (new K/V read + written), and flops (4 d per visible (row, key) pair per query head)."""
+    (new K/V read + written), and flops (4 d per visible (row, key) pair per query head).  A stored
+    K or V row is d bf16 values, or over 8-bit pages d codes and one fp32 scale."""
     d, Hq, Hkv = wl.head_dim, wl.num_heads_q, wl.num_heads_kv
     L = wl.context_lens.astype(np.int64)
     q = wl.q_lens.astype(np.int64)
-    kv_bytes = int(np.sum(L) * 2 * Hkv * d * 2)
+    row_bytes = d + 4 if kv == "fp8" else 2 * d
+    kv_bytes = int(np.sum(L) * 2 * Hkv * row_bytes)
     qo_bytes = int(wl.num_tokens * Hq * d * 2 * 2)
-    append_bytes = int(wl.num_tokens * Hkv * d * 2 * 2 * 2)
+    append_bytes = int(wl.num_tokens * Hkv * 2 * (2 * d + row_bytes))
     if wl.causal:
         pairs = int(np.sum(q * (L - q) + q * (q + 1) // 2))
     else:
@@ -148,9 +150,10 @@ class ClockSampler:
                 "samples": len(sm), "window": "timed region" if t0 is not None else "whole run"}
 
 
-def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None):
+def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None, kv="bf16"):
     """Time the oracle (as it stands) on a bounded sample of the workload's sequences, all their
-    rows.  Returns (seconds, sampled work dict, description)."""
+    rows (over 8-bit pages: its 8-bit step, quantizing the sampled pages first).  Returns
+    (seconds, sampled work dict, description)."""
     import oracle
 
     def bits(t):
@@ -172,15 +175,15 @@ def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None):
         t0, t1 = int(cu[i]), int(cu[i + 1])
         sub_cu = np.array([0, t1 - t0], np.int32)
         t = time.perf_counter()
-        oracle.step.run_step(sub_cu, wl.context_lens[i:i + 1], pages, wl.block_size, wl.max_blocks,
-                             q_all[t0:t1], kn_all[t0:t1], vn_all[t0:t1], kp, vp, wl.scale, wl.causal,
-                             pool_pages=pages)
+        run = oracle.step.run_step_fp8 if kv == "fp8" else oracle.step.run_step
+        run(sub_cu, wl.context_lens[i:i + 1], pages, wl.block_size, wl.max_blocks, q_all[t0:t1], kn_all[t0:t1],
+            vn_all[t0:t1], kp, vp, wl.scale, wl.causal, pool_pages=pages)
         spent += time.perf_counter() - t
         done.append(i)
     sub = workloads.custom(wl.q_lens[done], wl.context_lens[done], wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
                            wl.block_size, wl.causal)
     desc = f"{len(done)} of {wl.num_seqs} sequences (seeded random order), every row, full oracle step"
-    return spent, work(sub), desc
+    return spent, work(sub, kv), desc
 
 
 def unit_of(config):
@@ -204,10 +207,12 @@ def job_throughput(config, w, seconds, world):
     return throughput(config, w, seconds) * world
 
 
-def attention_kernel(wl):
+def attention_kernel(wl, kv="bf16"):
     """The attention kernel the library dispatches to: the tcgen05 tile kernel when head_dim is
     128, G divides 128 and the batch is not pure decode (one token per sequence, G <= 16);
-    otherwise the decode-path kernel."""
+    otherwise, and always over 8-bit pages, the decode-path kernel."""
+    if kv == "fp8":
+        return "paged_attention_kernel"
     G = wl.num_heads_q // wl.num_heads_kv
     pure_decode = wl.num_tokens == wl.num_seqs and G <= 16
     if wl.head_dim == 128 and 128 % G == 0 and not pure_decode:
@@ -221,6 +226,10 @@ def throughput(config, w, seconds):
     return (w["attn_bytes"] + w["append_bytes"]) / seconds / 1e9
 
 
+def describe(args):
+    return DESC[args.config] + (", 8-bit E4M3 KV pages + per-row fp32 scales" if args.kv == "fp8" else "")
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -229,7 +238,7 @@ def run_reference(args, rank, world):
     unit, _ = unit_of(args.config)
     times = []
     for k in range(args.warmup + args.steps):
-        secs, w, desc = oracle_sample(wl, vals, budget_s=args.ref_budget)
+        secs, w, desc = oracle_sample(wl, vals, budget_s=args.ref_budget, kv=args.kv)
         if k >= args.warmup:
             times.append((secs, w))
     secs = sum(t for t, _ in times)
@@ -237,7 +246,7 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": DESC[args.config]},
+            "config": {"workload": describe(args)},
             "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -250,6 +259,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="decode", choices=list(workloads.CONFIGS))
     ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="page format of the KV cache")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference step")
     args = ap.parse_args()
@@ -275,21 +285,42 @@ def main():
 
     wl = workloads.make(args.config)
     vals = wl.tensors(dev)
-    w = work(wl)
+    fp8 = args.kv == "fp8"
+    w = work(wl, args.kv)
     batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
-                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, kv_fp8=fp8)
     pl = batch.plan
     stream = torch.cuda.current_stream(dev)
     out = torch.empty_like(vals["q"])
     P = wl.num_pages
+    if fp8:
+        # the 8-bit pool: every bf16 pool row appended (quantized) once, before any timing
+        Pp, Hkv, bs, d = vals["k_pool"].shape
+        for name in ("k", "v"):
+            vals[name + "_codes"] = torch.empty(Pp, Hkv, bs, d, dtype=torch.uint8, device=dev)
+            vals[name + "_scales"] = torch.empty(Pp, Hkv, bs, dtype=torch.float32, device=dev)
+        rows = {n: vals[n + "_pool"].permute(0, 2, 1, 3).reshape(Pp * bs, Hkv, d).contiguous() for n in ("k", "v")}
+        xy.xy_kv_append_fp8(rows["k"], rows["v"], torch.arange(Pp * bs, dtype=torch.int64, device=dev),
+                            vals["k_codes"], vals["v_codes"], vals["k_scales"], vals["v_scales"], batch.err)
+        del rows
+        torch.cuda.synchronize()
 
     def step(ev=None):
         xy.xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, wl.block_size, P, batch.slots, batch.err)
-        xy.xy_kv_append(vals["k_new"], vals["v_new"], batch.slots, vals["k_pool"], vals["v_pool"], batch.err)
+        if fp8:
+            xy.xy_kv_append_fp8(vals["k_new"], vals["v_new"], batch.slots, vals["k_codes"], vals["v_codes"],
+                                vals["k_scales"], vals["v_scales"], batch.err)
+        else:
+            xy.xy_kv_append(vals["k_new"], vals["v_new"], batch.slots, vals["k_pool"], vals["v_pool"], batch.err)
         if ev:
             ev[0].record(stream)
-        xy.xy_paged_attention(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"], vals["v_pool"],
-                              wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
+        if fp8:
+            xy.xy_paged_attention_fp8(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_codes"],
+                                      vals["v_codes"], vals["k_scales"], vals["v_scales"], wl.scale, wl.causal,
+                                      pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
+        else:
+            xy.xy_paged_attention(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"], vals["v_pool"],
+                                  wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
         if ev:
             ev[1].record(stream)
 
@@ -321,12 +352,13 @@ def main():
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
     value = job_throughput(args.config, w, ms_per_step / 1e3, world)
     unit, bound = unit_of(args.config)
-    kname = attention_kernel(wl)
+    traffic_key = args.config + ("_fp8" if fp8 else "")
+    kname = attention_kernel(wl, args.kv)
     attn_s = attn_ms / 1e3
     if bound == "hbm":
         achieved = w["attn_bytes"] / attn_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
-                "traffic": measured_traffic(args.config), "kernel": kname, "algorithmic_bytes": w["attn_bytes"],
+                "traffic": measured_traffic(traffic_key), "kernel": kname, "algorithmic_bytes": w["attn_bytes"],
                 "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
         if args.config == "mixed":
             # both bounds matter: time at the roofline = bytes / HBM + flops / tensor (the sum, as the
@@ -338,7 +370,7 @@ def main():
     else:
         achieved = w["flops"] / attn_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["tc"], "unit": "TFLOP/s",
-                "frac": achieved / pk["tc"], "traffic": measured_traffic(args.config), "kernel": kname,
+                "frac": achieved / pk["tc"], "traffic": measured_traffic(traffic_key), "kernel": kname,
                 "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
     roof["timed"] = "attention call (kernel" + (" + combine" if pl.merges.shape[0] else "") + "), CUDA events"
 
@@ -354,11 +386,15 @@ def main():
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         b2 = xystep.PagedBatch(meta["cu"], meta["ctx"], meta["free"], wl.block_size, wl.max_blocks, wl.num_heads_q,
-                               wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, num_ctas=pl.num_ctas)
+                               wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8)
         qd = host["q"].to(dev, non_blocking=True)
         kd = host["k_new"].to(dev, non_blocking=True)
         vd = host["v_new"].to(dev, non_blocking=True)
-        o = xystep.run_step(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
+        if fp8:
+            o = xystep.run_step_fp8(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], vals["k_scales"],
+                                    vals["v_scales"], wl.scale)
+        else:
+            o = xystep.run_step(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
         out_host.copy_(o, non_blocking=True)
         torch.cuda.synchronize()
         e2e_times.append(time.perf_counter() - t0)
@@ -372,7 +408,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, sw, desc = oracle_sample(wl, vals, budget_s=12.0)
+        secs, sw, desc = oracle_sample(wl, vals, budget_s=12.0, kv=args.kv)
         cpu = {"value": throughput(args.config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
                "sample": desc}
 
@@ -384,8 +420,8 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": DESC[args.config], "parallelism": f"replicas x{world}",
+            "vs_baseline": None, "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16", "data": "synthetic",
+            "config": {"workload": describe(args), "parallelism": f"replicas x{world}",
                        "l2": "KV working set larger than the 129 MB L2; no flush between steps"
                              if w["kv_bytes"] > 4 * 129e6 else "L2 not flushed (small working set)",
                        "step": "slot_mapping + kv_append + paged_attention" +

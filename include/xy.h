@@ -272,6 +272,24 @@ xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *
                            void *k_pages, void *v_pages, float *k_scales, float *v_scales, int num_pages,
                            int num_heads_kv, int block_size, int head_dim, int32_t *err_word, void *stream);
 
+/* xy_paged_attention_fp8: xy_paged_attention over 8-bit pages.  The result is the attention of
+ * xy_paged_attention over the dequantized pages (code * scale per row): K scales multiply the fp32
+ * scores, V scales the softmax weights, the codes become f16 exactly on chip.  q, out, tasks,
+ * merges, workspace, err_word and every other argument as for xy_paged_attention; k_pages/v_pages
+ * uint8 [num_pages, Hkv, bs, 128] and k_scales/v_scales fp32 [num_pages, Hkv, bs] (device,
+ * 16-byte aligned), written by xy_kv_append_fp8.  The query rows are rounded to f16 on chip
+ * (exact for bf16 values of magnitude 2^-14 .. 65504).  Every task runs on the decode path, so
+ * rows per task (q_rows * G) are at most 64: build the task table with q_tile <= 64 / G.
+ * Errors: as xy_paged_attention; XY_ERR_UNSUPPORTED for head_dim other than 128 or G > 64. */
+xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                 const int32_t *block_table, int max_blocks, const void *k_pages,
+                                 const void *v_pages, const float *k_scales, const float *v_scales,
+                                 int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                 int num_heads_kv, int head_dim, int block_size, float scale, int causal,
+                                 const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                 int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                                 int32_t *err_word, void *out, void *stream);
+
 /* Self-test of the bounded waits (no counterpart in the pages; not a step of the path).
  * Every mbarrier wait in the attention kernels gives up after a time limit, or when its CTA's
  * abort flag is raised, sets XY_DEV_TIMEOUT in *err_word and lets the kernel return instead of

@@ -22,7 +22,8 @@ XY_DEV_TIMEOUT = 0x8
 
 C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
-         "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8")
+         "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
+         "xy_paged_attention_fp8")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -89,6 +90,9 @@ def lib():
     L.xy_selftest_bounded_wait.restype = I
     L.xy_kv_append_fp8.argtypes = [P, P, P, I, P, P, P, P, I, I, I, I, P, P]
     L.xy_kv_append_fp8.restype = I
+    L.xy_paged_attention_fp8.argtypes = [P, P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ,
+                                         P, P, P]
+    L.xy_paged_attention_fp8.restype = I
     _lib = L
     return L
 
@@ -269,6 +273,32 @@ def xy_kv_append_fp8(k_new, v_new, slot_mapping, k_pages, v_pages, k_scales, v_s
                                   _dev(err_word, torch.int32, "err_word"), _stream(stream)), "xy_kv_append_fp8")
 
 
+def xy_paged_attention_fp8(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_scales, v_scales, scale,
+                           causal, tasks, merges, num_ctas, workspace, err_word, out, stream=None):
+    """xy_paged_attention over 8-bit pages: k_pages/v_pages [P, Hkv, bs, 128] uint8 E4M3 codes,
+    k_scales/v_scales [P, Hkv, bs] fp32 (as written by xy_kv_append_fp8).  tasks from a task table
+    built with q_tile <= 64 // G (Plan(..., kv_fp8=True))."""
+    import torch
+    T, Hq, d = q.shape
+    P, Hkv, bs, d2 = k_pages.shape
+    if d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch between q, out and the page pools")
+    if tuple(k_scales.shape) != (P, Hkv, bs) or tuple(v_scales.shape) != (P, Hkv, bs):
+        raise ValueError("scales must be [P, Hkv, bs]")
+    bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+    nm = merges.shape[0] if merges is not None else 0
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None and workspace.numel() else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().xy_paged_attention_fp8(
+        _dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(context_lens, torch.int32, "context_lens"),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _dev(k_pages, u8, "k_pages"),
+        _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P,
+        cu_seqlens_q.numel() - 1, T, Hq, Hkv, d, bs, float(scale), int(bool(causal)),
+        _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
+        _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
+        _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention_fp8")
+
+
 def xy_selftest_bounded_wait(limit_us, err_word, result, stream=None):
     """Self-test of the kernels' bounded waits (see include/xy.h): err_word int32 [1] and
     result int32 [3] on the device."""
@@ -287,14 +317,15 @@ def check_err_word(err_word):
         raise XYDeviceError(bits)
 
 
-def default_tiles(num_heads_q, num_heads_kv, head_dim=128):
+def default_tiles(num_heads_q, num_heads_kv, head_dim=128, kv_fp8=False):
     """Tile policy of the kernels.  With head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
-    256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise up to 64 rows
-    (q_tile = 64 // G).  KV chunks are 8192 keys, a multiple of every page size and of both
-    kernels' KV tiles: long enough that split partials and merges stay few, short enough that a
-    few long contexts still spread over the SMs (measured on the mixed and long-context batches)."""
+    256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise, and always over
+    8-bit pages, up to 64 rows (q_tile = 64 // G).  KV chunks are 8192 keys, a multiple of every
+    page size and of both kernels' KV tiles: long enough that split partials and merges stay few,
+    short enough that a few long contexts still spread over the SMs (measured on the mixed and
+    long-context batches)."""
     G = num_heads_q // num_heads_kv
-    if head_dim == 128 and 128 % G == 0:
+    if head_dim == 128 and 128 % G == 0 and not kv_fp8:
         return 256 // G, 8192
     return max(1, 64 // G), 8192
 
@@ -304,11 +335,11 @@ class Plan:
     cu_seqlens_q and context_lens) uploaded to the device, and the workspace it needs."""
 
     def __init__(self, cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, device="cuda",
-                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=XY_SCHEDULE_GREEDY):
+                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=XY_SCHEDULE_GREEDY, kv_fp8=False):
         import torch
         dev = torch.device(device)
         self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)
-        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim)
+        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
         self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
         self.schedule = schedule
         r = xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,

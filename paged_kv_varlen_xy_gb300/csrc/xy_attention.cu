@@ -23,6 +23,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <type_traits>
 #include <vector>
 
 #include "xy.h"
@@ -42,13 +43,14 @@ using xy::dec::kMathWarps;
 // warps that issue alternate stages (xy_decode_path.cuh).  Issuing a stage -- block-table window
 // lookup, eight page boxes, barrier bookkeeping -- costs a producer warp about as long as the math
 // warps need to consume one, so two producers keep the ring ahead of the math.  It runs every
-// task when the tcgen05 tile kernel cannot (head_dim 64, or G not dividing 128), and pure decode
-// batches; tasks then have at most 64 rows.
+// task when the tcgen05 tile kernel cannot (head_dim 64, or G not dividing 128), pure decode
+// batches, and every batch over 8-bit pages; tasks then have at most 64 rows.
 constexpr int kProducers = 2;
 
-template <int HD>
+template <int HD, bool FP8>
 struct Cfg {
-    using RG = xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>;
+    using RG = typename std::conditional<FP8, xy::dec::RingF8<4, 16 * kMathWarps>,
+                                         xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type;
     static_assert(RG::kStages % kProducers == 0, "a stage always has the same producer");
     static constexpr int kThreads = (kMathWarps + kProducers) * 32;
     static constexpr int kStagesOff = 0;
@@ -59,11 +61,11 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
-template <int HD>
-__global__ void __launch_bounds__(Cfg<HD>::kThreads, 1)
+template <int HD, bool FP8>
+__global__ void __launch_bounds__(Cfg<HD, FP8>::kThreads, 1)
     paged_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p) {
-    using C = Cfg<HD>;
+    using C = Cfg<HD, FP8>;
     using RG = typename C::RG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = xy::smem_u32(smem_raw);
@@ -265,23 +267,37 @@ bool make_pool_map(CUtensorMap *map, const void *pool, int64_t rows, int head_di
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over an 8-bit page pool viewed as [P * Hkv * bs rows, 128 bytes] (head_dim 128): a box of
+// (128, box_rows) lands in shared memory as [box_rows][128 B] with the 128-byte swizzle.
+bool make_pool_map_u8(CUtensorMap *map, const void *pool, int64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {128u, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {128u};
+    cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int HD>
+template <int HD, bool FP8>
 xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
                  const xy_merge *merges, int num_merges, cudaStream_t st) {
-    using C = Cfg<HD>;
+    using C = Cfg<HD, FP8>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return XY_ERR_CUDA;
     if (configured_device != dev) {  // the attribute is per device
-        if (cudaFuncSetAttribute(paged_attention_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_attention_kernel<HD, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return XY_ERR_CUDA;
         configured_device = dev;
     }
     if (p.num_tasks > 0) {
-        paged_attention_kernel<HD><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
+        paged_attention_kernel<HD, FP8><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel launch");
     }
@@ -309,15 +325,15 @@ extern "C" int xy_default_num_ctas(int device) {
     return sms;  // one persistent CTA per SM
 }
 
-extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
-                                        const int32_t *block_table, int max_blocks, const void *k_pages,
-                                        const void *v_pages, int num_pages, int num_seqs, int num_tokens,
-                                        int num_heads_q, int num_heads_kv, int head_dim, int block_size, float scale,
-                                        int causal, const xy_task *tasks, int num_tasks, const xy_merge *merges,
-                                        int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
-                                        int32_t *err_word, void *out, void *stream) {
-    if (num_tasks < 0 || num_merges < 0 || num_seqs < 0 || num_tokens < 0) return XY_ERR_INVALID_ARG;
-    if (num_tasks == 0 && num_merges == 0) return XY_OK;
+namespace {
+
+// Argument checks shared by both page formats, and the kernel parameters they give.
+xy_status make_params(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                      const int32_t *block_table, int max_blocks, const void *k_pages, const void *v_pages,
+                      int num_pages, int num_seqs, int num_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                      int block_size, float scale, int causal, const xy_task *tasks, int num_tasks,
+                      const xy_merge *merges, int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                      int32_t *err_word, void *out, AttnParams *pp) {
     if (!q || !cu_seqlens_q || !context_lens || !block_table || !k_pages || !v_pages || !tasks || !out ||
         !err_word || num_ctas < 1 || max_blocks < 1 || num_pages < 1 || num_seqs < 1 || num_heads_kv < 1 ||
         num_heads_q < num_heads_kv || num_heads_q % num_heads_kv)
@@ -326,16 +342,9 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     if (head_dim != 64 && head_dim != 128) return XY_ERR_UNSUPPORTED;
     if (block_size < 16 || block_size > 256 || (block_size & (block_size - 1))) return XY_ERR_UNSUPPORTED;
     if (num_merges > 0 && (!merges || !workspace || !aligned16(workspace))) return XY_ERR_WORKSPACE;
+    if ((int64_t)num_pages * num_heads_kv * block_size > INT32_MAX) return XY_ERR_UNSUPPORTED;
 
-    const int64_t rows = (int64_t)num_pages * num_heads_kv * block_size;
-    if (rows > INT32_MAX) return XY_ERR_UNSUPPORTED;
-    const int box_rows = block_size < xy::dec::kStageKeys ? block_size : xy::dec::kStageKeys;
-    CUtensorMap km, vm;
-    if (!make_pool_map(&km, k_pages, rows, head_dim, box_rows) ||
-        !make_pool_map(&vm, v_pages, rows, head_dim, box_rows))
-        return XY_ERR_CUDA;
-
-    AttnParams p;
+    AttnParams &p = *pp;
     p.q = static_cast<const __nv_bfloat16 *>(q);
     p.cu = cu_seqlens_q;
     p.ctx = context_lens;
@@ -346,6 +355,8 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     p.ws_lse = workspace ? static_cast<float *>(workspace) + p.ws_rows * head_dim : nullptr;
     p.err = err_word;
     p.out = static_cast<__nv_bfloat16 *>(out);
+    p.ksc = nullptr;
+    p.vsc = nullptr;
     p.MB = max_blocks;
     p.P = num_pages;
     p.S = num_seqs;
@@ -357,6 +368,33 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     p.causal = causal ? 1 : 0;
     p.num_tasks = num_tasks;
     p.scale_log2 = scale * 1.4426950408889634f;
+    return XY_OK;
+}
+
+}  // namespace
+
+extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                        const int32_t *block_table, int max_blocks, const void *k_pages,
+                                        const void *v_pages, int num_pages, int num_seqs, int num_tokens,
+                                        int num_heads_q, int num_heads_kv, int head_dim, int block_size, float scale,
+                                        int causal, const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                        int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                                        int32_t *err_word, void *out, void *stream) {
+    if (num_tasks < 0 || num_merges < 0 || num_seqs < 0 || num_tokens < 0) return XY_ERR_INVALID_ARG;
+    if (num_tasks == 0 && num_merges == 0) return XY_OK;
+    AttnParams p;
+    const xy_status ps = make_params(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages,
+                                     num_pages, num_seqs, num_tokens, num_heads_q, num_heads_kv, head_dim,
+                                     block_size, scale, causal, tasks, num_tasks, merges, num_merges, num_ctas,
+                                     workspace, workspace_bytes, err_word, out, &p);
+    if (ps != XY_OK) return ps;
+
+    const int64_t rows = (int64_t)num_pages * num_heads_kv * block_size;
+    const int box_rows = block_size < xy::dec::kStageKeys ? block_size : xy::dec::kStageKeys;
+    CUtensorMap km, vm;
+    if (!make_pool_map(&km, k_pages, rows, head_dim, box_rows) ||
+        !make_pool_map(&vm, v_pages, rows, head_dim, box_rows))
+        return XY_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // A batch of one new token per sequence with G <= XY_TILE_MIN_ROWS has only decode-path tasks:
     // the stand-alone decode kernel (more registers, deeper stages) runs it.  Any other batch the
@@ -371,8 +409,38 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
         }
         p.num_tasks = 0;  // ... so only the split-KV merge remains
     }
-    return head_dim == 128 ? launch<128>(p, km, vm, num_ctas, merges, num_merges, st)
-                           : launch<64>(p, km, vm, num_ctas, merges, num_merges, st);
+    return head_dim == 128 ? launch<128, false>(p, km, vm, num_ctas, merges, num_merges, st)
+                           : launch<64, false>(p, km, vm, num_ctas, merges, num_merges, st);
+}
+
+extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                            const int32_t *block_table, int max_blocks, const void *k_pages,
+                                            const void *v_pages, const float *k_scales, const float *v_scales,
+                                            int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                            int num_heads_kv, int head_dim, int block_size, float scale, int causal,
+                                            const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                            int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                                            int32_t *err_word, void *out, void *stream) {
+    if (num_tasks < 0 || num_merges < 0 || num_seqs < 0 || num_tokens < 0) return XY_ERR_INVALID_ARG;
+    if (num_tasks == 0 && num_merges == 0) return XY_OK;
+    if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)) return XY_ERR_INVALID_ARG;
+    AttnParams p;
+    const xy_status ps = make_params(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages,
+                                     num_pages, num_seqs, num_tokens, num_heads_q, num_heads_kv, head_dim,
+                                     block_size, scale, causal, tasks, num_tasks, merges, num_merges, num_ctas,
+                                     workspace, workspace_bytes, err_word, out, &p);
+    if (ps != XY_OK) return ps;
+    if (head_dim != 128 || p.G > 16 * kMathWarps) return XY_ERR_UNSUPPORTED;
+    p.ksc = k_scales;
+    p.vsc = v_scales;
+
+    const int64_t rows = (int64_t)num_pages * num_heads_kv * block_size;
+    const int box_rows = block_size < xy::dec::kStageKeys ? block_size : xy::dec::kStageKeys;
+    CUtensorMap km, vm;
+    if (!make_pool_map_u8(&km, k_pages, rows, box_rows) || !make_pool_map_u8(&vm, v_pages, rows, box_rows))
+        return XY_ERR_CUDA;
+    // every task runs on the decode path (f16 MMAs on converted codes)
+    return launch<128, true>(p, km, vm, num_ctas, merges, num_merges, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------------------------

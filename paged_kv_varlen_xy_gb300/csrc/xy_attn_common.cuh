@@ -21,6 +21,8 @@ struct AttnParams {
     float *ws_lse;
     int32_t *err;
     __nv_bfloat16 *out;
+    const float *ksc;  // 8-bit pages: per-row K and V scales [P, Hkv, bs] (null for bf16 pages)
+    const float *vsc;
     int64_t ws_rows;
     int MB, P, S, T, Hq, Hkv, G, bs, causal, num_tasks;
     float scale_log2;

@@ -12,6 +12,14 @@
 // PV run on m16n8k16 tensor-core fragments, the online softmax on the accumulator registers with
 // quad shuffles.  When a task has fewer rows than warps x 16 the warps split each stage's keys
 // and merge their (max, sum, O) triples through shared memory at the end of the task.
+//
+// 8-bit pages (E4M3 codes with one fp32 scale per stored (token, KV head) row, head_dim 128):
+// the stage holds the codes (a 128-byte row per key) and the stage keys' K and V scales.  The
+// math warps turn codes into f16 in registers (exact) right after the fragment loads and run f16
+// MMAs; the query rows are converted bf16 -> f16 once per task.  K scales multiply the fp32
+// scores; V scales multiply the softmax weights before they are rounded to f16, relative to the
+// largest V scale seen so far (so the packed weights stay in [0, 1]), and that largest scale
+// multiplies O once at the end of the task.
 #pragma once
 
 #include <cuda.h>
@@ -31,8 +39,11 @@ constexpr int kMathWarps = 4;
 // Geometry of a decode stage ring: NS stages of K, V (64 keys x HD) and room for QR query rows.
 template <int HD, int NS, int QR>
 struct Ring {
+    static constexpr bool kFp8 = false;
     static constexpr int kHalves = HD / 64;                        // 128-byte swizzle atoms per row
     static constexpr int kTensorBytes = kHalves * kStageKeys * 128;  // K or V of one stage
+    static constexpr int kQOff = 2 * kTensorBytes;                 // query rows
+    static constexpr int kScaleOff = 0;                            // (no scales)
     static constexpr int kQBytes = QR * HD * 2;                    // the task's rows (first stage only)
     static constexpr int kStageBytes = 2 * kTensorBytes + kQBytes;
     static constexpr int kStages = NS;
@@ -42,6 +53,32 @@ struct Ring {
     static constexpr int kSlotBytes = kMathWarps * kSlotFloats * 4;
     static_assert(QR % 16 == 0 && QR <= 16 * kMathWarps, "rows per decode task");
 };
+
+// Geometry of an 8-bit decode stage ring (head_dim 128): NS stages, each holding the K and V codes
+// of 64 keys (one 128-byte row per key, 128-byte swizzle), the 64 keys' K scales then V scales
+// (fp32), and room for QR bf16 query rows.
+template <int NS, int QR>
+struct RingF8 {
+    static constexpr bool kFp8 = true;
+    static constexpr int kHalves = 1;
+    static constexpr int kTensorBytes = kStageKeys * 128;
+    static constexpr int kScaleOff = 2 * kTensorBytes;
+    static constexpr int kQOff = kScaleOff + 2 * kStageKeys * 4;
+    static constexpr int kQBytes = QR * 128 * 2;
+    static constexpr int kStageBytes = (kQOff + kQBytes + 1023) / 1024 * 1024;  // stages stay 1024-aligned
+    static constexpr int kStages = NS;
+    static constexpr int kMaxRows = QR;
+    static constexpr int kBytes = NS * kStageBytes;
+    static constexpr int kSlotFloats = 16 * 128 + 32;
+    static constexpr int kSlotBytes = kMathWarps * kSlotFloats * 4;
+    static_assert(QR % 16 == 0 && QR <= 16 * kMathWarps, "rows per decode task");
+};
+
+// Byte offset of 16-byte chunk `chunk` of key `key` in an 8-bit stage tensor: boxes of BR keys
+// are contiguous [BR][128 B] (so key k's row starts at k * 128) with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz8(int key, int chunk) {
+    return (uint32_t)(key * 128 + ((chunk ^ (key & 7)) << 4));
+}
 
 // Shared-memory handles of the decode path, set up by the hosting kernel.
 struct Smem {
@@ -107,7 +144,8 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
             pg_win = pg_nxt;
             pg_nxt = load_window(p, t.seq, win0 + 32, lane);
         }
-        const int n_copies = nbox * 2;  // one box per (page, tensor), both column halves
+        // one box per (page, tensor), both column halves; 8-bit pages add each box's K and V scales
+        const int n_copies = nbox * (RG::kFp8 ? 4 : 2);
         const int b = lane % nbox;
         int my_pg = __shfl_sync(0xffffffffu, pg_win, ((kv0 + (b << br_sh)) >> bs_sh) - win0);
         if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
@@ -118,22 +156,34 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
         const bool q_here = kv0 == t.kv_start;
         const uint32_t q_bytes = q_here ? (uint32_t)t.q_rows * row_bytes : 0u;
         const uint32_t stage = sm.stages + s * RG::kStageBytes;
-        if (lane == 0)
-            mbar_arrive_expect_tx(sm.full_bar + 8 * s, (uint32_t)(n_copies * RG::kHalves * BR * 128) + q_bytes);
+        const uint32_t kv_bytes =
+            RG::kFp8 ? (uint32_t)(nbox * BR * (2 * 128 + 2 * 4)) : (uint32_t)(n_copies * RG::kHalves * BR * 128);
+        if (lane == 0) mbar_arrive_expect_tx(sm.full_bar + 8 * s, kv_bytes + q_bytes);
         __syncwarp();
         if (lane < n_copies) {
             const int tensor = lane / nbox;
             const int key = kv0 + (b << br_sh);
             const int y = ((my_pg * p.Hkv + t.kv_head) << bs_sh) + (key & (p.bs - 1));
-            const uint32_t dst = stage + tensor * RG::kTensorBytes + b * RG::kHalves * BR * 128;
-            tma_load_3d(dst, tensor ? vmap : kmap, 0, y, 0, sm.full_bar + 8 * s);
+            if constexpr (RG::kFp8) {
+                if (tensor < 2) {
+                    tma_load_2d(stage + tensor * RG::kTensorBytes + b * BR * 128, tensor ? vmap : kmap, 0, y,
+                                sm.full_bar + 8 * s);
+                } else {
+                    const float *src = (tensor == 2 ? p.ksc : p.vsc) + y;  // the box's BR scales
+                    bulk_load(stage + RG::kScaleOff + (tensor - 2) * kStageKeys * 4 + b * BR * 4, src,
+                              (uint32_t)BR * 4, sm.full_bar + 8 * s);
+                }
+            } else {
+                const uint32_t dst = stage + tensor * RG::kTensorBytes + b * RG::kHalves * BR * 128;
+                tma_load_3d(dst, tensor ? vmap : kmap, 0, y, 0, sm.full_bar + 8 * s);
+            }
         }
         if (q_here) {
             // token j's G heads are one contiguous run of q
             for (int j = lane; j < t.q_rows; j += 32) {
                 const int64_t tok = (int64_t)f.seq_start + t.q_start + j;
                 const __nv_bfloat16 *src = p.q + (tok * p.Hq + (int64_t)t.kv_head * p.G) * HD;
-                bulk_load(stage + 2 * RG::kTensorBytes + j * row_bytes, src, row_bytes, sm.full_bar + 8 * s);
+                bulk_load(stage + RG::kQOff + j * row_bytes, src, row_bytes, sm.full_bar + 8 * s);
             }
         }
         if (first_mine) {
@@ -178,6 +228,10 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         return min(lim, t.kv_end);
     };
     const int lim_a = row_limit(row_a), lim_b = row_limit(row_b);
+    static_assert(!RG::kFp8 || HD == 128, "8-bit pages: head_dim 128");
+    // 8-bit pages: output column of accumulator pair n (see the V fragments below)
+    auto ocol = [&](int n) -> int { return RG::kFp8 ? 16 * (n >> 1) + 4 * c4 + 2 * (n & 1) : 8 * n + 2 * c4; };
+    float s_max = 0.f, s_inv = 0.f;  // 8-bit pages: largest V scale seen, and its reciprocal
     int lim_max = max(lim_a, lim_b);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, o));
@@ -201,16 +255,26 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         const uint32_t kst = sm.stages + s * RG::kStageBytes;
         const uint32_t vst = kst + RG::kTensorBytes;
         if (kv0 == t.kv_start) {
-            const uint8_t *qs = sm.stages_gen + s * RG::kStageBytes + 2 * RG::kTensorBytes;
+            const uint8_t *qs = sm.stages_gen + s * RG::kStageBytes + RG::kQOff;
             const uint32_t *qa_ptr = row_a < R ? reinterpret_cast<const uint32_t *>(qs + row_a * HD * 2) : nullptr;
             const uint32_t *qb_ptr = row_b < R ? reinterpret_cast<const uint32_t *>(qs + row_b * HD * 2) : nullptr;
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
-                const int w0 = kk * 8 + c4, w1 = w0 + 4;  // 32-bit words: cols 16kk+2c and +8
-                qa[kk][0] = qa_ptr ? qa_ptr[w0] : 0u;
-                qa[kk][1] = qb_ptr ? qb_ptr[w0] : 0u;
-                qa[kk][2] = qa_ptr ? qa_ptr[w1] : 0u;
-                qa[kk][3] = qb_ptr ? qb_ptr[w1] : 0u;
+                if constexpr (RG::kFp8) {
+                    // k-order of the 8-bit K fragments: k 2c, 2c+1 hold cols 16kk+4c, +1 and
+                    // k 2c+8, 2c+9 hold cols 16kk+4c+2, +3 (a dot product may sum in any order)
+                    const int w0 = kk * 8 + 2 * c4, w1 = w0 + 1;
+                    qa[kk][0] = qa_ptr ? bf16x2_to_f16x2(qa_ptr[w0]) : 0u;
+                    qa[kk][1] = qb_ptr ? bf16x2_to_f16x2(qb_ptr[w0]) : 0u;
+                    qa[kk][2] = qa_ptr ? bf16x2_to_f16x2(qa_ptr[w1]) : 0u;
+                    qa[kk][3] = qb_ptr ? bf16x2_to_f16x2(qb_ptr[w1]) : 0u;
+                } else {
+                    const int w0 = kk * 8 + c4, w1 = w0 + 4;  // 32-bit words: cols 16kk+2c and +8
+                    qa[kk][0] = qa_ptr ? qa_ptr[w0] : 0u;
+                    qa[kk][1] = qb_ptr ? qb_ptr[w0] : 0u;
+                    qa[kk][2] = qa_ptr ? qa_ptr[w1] : 0u;
+                    qa[kk][3] = qb_ptr ? qb_ptr[w1] : 0u;
+                }
             }
             first_stage_seen();
         }
@@ -220,7 +284,36 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         for (int kc = k_lo; kc < k_hi; kc += 16) {
             const int kr = kc - kv0;
             float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            {
+            // 8-bit pages: the scales of this thread's keys kc + 8j + 2c + e (V scales of keys at or
+            // past kv_end, which may hold anything, read as 0)
+            float ksc[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            if constexpr (RG::kFp8) {
+                const float *scl = reinterpret_cast<const float *>(sm.stages_gen + s * RG::kStageBytes + RG::kScaleOff);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 kx = *reinterpret_cast<const float2 *>(scl + kr + 8 * j + 2 * c4);
+                    const float2 vx = *reinterpret_cast<const float2 *>(scl + kStageKeys + kr + 8 * j + 2 * c4);
+                    const int key = kc + 8 * j + 2 * c4;
+                    ksc[j][0] = kx.x;
+                    ksc[j][1] = kx.y;
+                    vsc[j][0] = key < t.kv_end ? vx.x : 0.f;
+                    vsc[j][1] = key + 1 < t.kv_end ? vx.y : 0.f;
+                }
+                // ldmatrix over the code rows: matrix i holds keys 8(i&1).. of 16-byte chunk 2cc+(i>>1);
+                // lane (g, c) gets codes of cols 4c..4c+3 of key g, i.e. the B fragment of a k-step
+                // in the k-order the query fragments use
+                const int mi = lane >> 3;
+                const int krow = kr + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int cc = 0; cc < HD / 32; ++cc) {
+                    uint32_t r[4];
+                    ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        mma_f16_16816(sc[i & 1], qa[2 * cc + (i >> 1)], e4m3x2_to_f16x2((uint16_t)(r[i] & 0xffffu)),
+                                      e4m3x2_to_f16x2((uint16_t)(r[i] >> 16)));
+                }
+            } else {
                 const int mi = lane >> 3;
                 const int krow = kr + ((mi >> 1) << 3) + (lane & 7);
 #pragma unroll
@@ -238,8 +331,9 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int key = kc + 8 * j + 2 * c4 + e;
-                    sc[j][e] = key < lim_a ? sc[j][e] * p.scale_log2 : -INFINITY;
-                    sc[j][2 + e] = key < lim_b ? sc[j][2 + e] * p.scale_log2 : -INFINITY;
+                    const float f = RG::kFp8 ? p.scale_log2 * ksc[j][e] : p.scale_log2;
+                    sc[j][e] = key < lim_a ? sc[j][e] * f : -INFINITY;
+                    sc[j][2 + e] = key < lim_b ? sc[j][2 + e] * f : -INFINITY;
                     mx_a = fmaxf(mx_a, sc[j][e]);
                     mx_b = fmaxf(mx_b, sc[j][2 + e]);
                 }
@@ -251,7 +345,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
             const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
             const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
             const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
-            const float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
+            float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
             m_a = mn_a;
             m_b = mn_b;
             float ps_a = 0.f, ps_b = 0.f;
@@ -266,6 +360,28 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
             }
             l_a = l_a * al_a + ps_a;
             l_b = l_b * al_b + ps_b;
+            if constexpr (RG::kFp8) {
+                // weights times V scale / s_max: s_max is the largest V scale so far, so the packed
+                // weights stay in [0, 1]; O (kept in units of s_max) is rescaled when it grows
+                float sm_new = fmaxf(fmaxf(vsc[0][0], vsc[0][1]), fmaxf(vsc[1][0], vsc[1][1]));
+                sm_new = fmaxf(sm_new, __shfl_xor_sync(0xffffffffu, sm_new, 1));
+                sm_new = fmaxf(sm_new, __shfl_xor_sync(0xffffffffu, sm_new, 2));
+                if (sm_new > s_max) {  // the same in every quad: warp-uniform
+                    const float g = s_max / sm_new;
+                    al_a *= g;
+                    al_b *= g;
+                    s_max = sm_new;
+                    s_inv = 1.f / sm_new;
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float w0 = vsc[j][0] * s_inv, w1 = vsc[j][1] * s_inv;
+                    sc[j][0] *= w0;
+                    sc[j][1] *= w1;
+                    sc[j][2] *= w0;
+                    sc[j][3] *= w1;
+                }
+            }
 #pragma unroll
             for (int n = 0; n < HD / 8; ++n) {
                 o_acc[n][0] *= al_a;
@@ -274,10 +390,17 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 o_acc[n][3] *= al_b;
             }
             uint32_t pa[4];
-            pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
-            pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
-            pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
-            pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+            if constexpr (RG::kFp8) {
+                pa[0] = pack_f16x2(sc[0][0], sc[0][1]);
+                pa[1] = pack_f16x2(sc[0][2], sc[0][3]);
+                pa[2] = pack_f16x2(sc[1][0], sc[1][1]);
+                pa[3] = pack_f16x2(sc[1][2], sc[1][3]);
+            } else {
+                pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
+                pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
+                pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
+                pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
+            }
             // keys at or past kv_end may hold anything (unused slots, stale stage data): their
             // weights are 0, and their V entries are zeroed so 0 * NaN cannot occur
             const bool tail = kc + 16 > t.kv_end;
@@ -286,7 +409,38 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 (key_lo < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 1 < t.kv_end ? 0xffff0000u : 0u);
             const uint32_t keep1 =
                 (key_lo + 8 < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 9 < t.kv_end ? 0xffff0000u : 0u);
-            {
+            if constexpr (RG::kFp8) {
+                // ldmatrix.trans over the code rows: matrix i holds keys 8(i&1).. of chunk 2cc+(i>>1);
+                // lane (g, c) gets the code pairs (cols 2g, 2g+1) of keys 2c and 2c+1 (+8).  Byte
+                // pairs regrouped by column give the B fragments of two n-tiles: even columns 2g
+                // and odd columns 2g+1 of the chunk, so accumulator pair n of this lane covers
+                // columns 16(n/2) + 4c + 2(n%2) + {0, 1} once the tiles are interleaved below.
+                const int mi = lane >> 3;
+                const int vrow = kr + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+                for (int cc = 0; cc < HD / 32; ++cc) {
+                    uint32_t r[4];
+                    ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t x0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu));
+                        const uint32_t x1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16));
+                        const uint32_t y0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu));
+                        const uint32_t y1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16));
+                        uint32_t ea0 = __byte_perm(x0, x1, 0x5410), eb0 = __byte_perm(x0, x1, 0x7632);
+                        uint32_t ea1 = __byte_perm(y0, y1, 0x5410), eb1 = __byte_perm(y0, y1, 0x7632);
+                        if (tail) {
+                            ea0 &= keep0;
+                            eb0 &= keep0;
+                            ea1 &= keep1;
+                            eb1 &= keep1;
+                        }
+                        const int ch = 2 * cc + h;
+                        mma_f16_16816(o_acc[2 * ch], pa, ea0, ea1);
+                        mma_f16_16816(o_acc[2 * ch + 1], pa, eb0, eb1);
+                    }
+                }
+            } else {
                 const int mi = lane >> 3;
                 const int vrow = kr + ((mi & 1) << 3) + (lane & 7);
 #pragma unroll
@@ -308,6 +462,22 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         if (lane == 0) mbar_arrive(sm.empty_bar + 8 * s);
     }
 
+    if constexpr (RG::kFp8) {
+        // back from units of s_max; interleave the even- and odd-column tiles so that pair n holds
+        // columns ocol(n), ocol(n) + 1 (register renaming only)
+#pragma unroll
+        for (int ch = 0; ch < HD / 16; ++ch) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float a0 = o_acc[2 * ch][2 * h] * s_max, a1 = o_acc[2 * ch][2 * h + 1] * s_max;
+                const float b0 = o_acc[2 * ch + 1][2 * h] * s_max, b1 = o_acc[2 * ch + 1][2 * h + 1] * s_max;
+                o_acc[2 * ch][2 * h] = a0;
+                o_acc[2 * ch][2 * h + 1] = b0;
+                o_acc[2 * ch + 1][2 * h] = a1;
+                o_acc[2 * ch + 1][2 * h + 1] = b1;
+            }
+        }
+    }
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
     l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
@@ -317,7 +487,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         float *my = sm.slots + w * RG::kSlotFloats;
 #pragma unroll
         for (int n = 0; n < HD / 8; ++n) {
-            const int col = 8 * n + 2 * c4;
+            const int col = ocol(n);
             *reinterpret_cast<float2 *>(my + g4 * HD + col) = make_float2(o_acc[n][0], o_acc[n][1]);
             *reinterpret_cast<float2 *>(my + (g4 + 8) * HD + col) = make_float2(o_acc[n][2], o_acc[n][3]);
         }
@@ -364,7 +534,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 l_b += gb * ot[16 * HD + 16 + g4 + 8];
 #pragma unroll
                 for (int n = 0; n < HD / 8; ++n) {
-                    const int col = 8 * n + 2 * c4;
+                    const int col = ocol(n);
                     const float2 xa = *reinterpret_cast<const float2 *>(ot + g4 * HD + col);
                     const float2 xb = *reinterpret_cast<const float2 *>(ot + (g4 + 8) * HD + col);
                     o_acc[n][0] += ga * xa.x;
@@ -394,14 +564,14 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
 #pragma unroll
             for (int n = 0; n < HD / 8; ++n) {
                 const float x0 = o_acc[n][2 * half] * inv, x1 = o_acc[n][2 * half + 1] * inv;
-                *reinterpret_cast<uint32_t *>(dst + 8 * n + 2 * c4) = pack_bf16x2(x0, x1);
+                *reinterpret_cast<uint32_t *>(dst + ocol(n)) = pack_bf16x2(x0, x1);
             }
         } else {
             const int64_t wr = (int64_t)t.ws_row + r;
             float *dst = p.ws_o + wr * HD;
 #pragma unroll
             for (int n = 0; n < HD / 8; ++n)
-                *reinterpret_cast<float2 *>(dst + 8 * n + 2 * c4) =
+                *reinterpret_cast<float2 *>(dst + ocol(n)) =
                     make_float2(o_acc[n][2 * half] * inv, o_acc[n][2 * half + 1] * inv);
             if (c4 == 0) p.ws_lse[wr] = l > 0.f ? m + __log2f(l) : -INFINITY;
         }

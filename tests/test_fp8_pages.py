@@ -1,4 +1,5 @@
-"""8-bit (E4M3) KV pages on the GPU against the oracle: the quantizing append bit for bit."""
+"""8-bit (E4M3) KV pages on the GPU against the oracle: the quantizing append bit for bit, and
+attention over the 8-bit pages against the oracle's attention over the dequantized pages."""
 
 import numpy as np
 import pytest
@@ -41,3 +42,84 @@ def test_append_fp8_bit_exact(d):
     assert np.array_equal(dev[2].cpu().numpy(), ref[0]) and np.array_equal(dev[3].cpu().numpy(), ref[1])
     assert np.array_equal(dev[4].cpu().numpy().view(np.uint32), ref[2].view(np.uint32))
     assert np.array_equal(dev[5].cpu().numpy().view(np.uint32), ref[3].view(np.uint32))
+
+
+# ---------------------------------------------------------------------------------------------
+# attention over 8-bit pages
+
+def _run_fp8(wl, kv_chunk=None, row_scale=None):
+    """One step over 8-bit pages on the GPU and in the oracle, on workload wl's bf16 values
+    (optionally with each pool / new row multiplied by a power of two from row_scale)."""
+    import paged_kv_varlen_xy_gb300 as xy
+    from paged_kv_varlen_xy_gb300 import build
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    build.build()
+    dev = torch.device("cuda")
+    vals = wl.tensors("cpu")
+    if row_scale is not None:
+        g = torch.Generator().manual_seed(wl.seed)
+        for name in ("k_pool", "v_pool", "k_new", "v_new"):
+            shp = vals[name].shape[:-1] + (1,)
+            f = torch.tensor(row_scale, dtype=torch.float32)[torch.randint(0, len(row_scale), shp, generator=g)]
+            vals[name] = (vals[name].float() * f).to(torch.bfloat16)
+    P, Hkv, bs, d = vals["k_pool"].shape
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    codes = {n: torch.zeros(P, Hkv, bs, d, dtype=torch.uint8, device=dev) for n in ("k", "v")}
+    scl = {n: torch.zeros(P, Hkv, bs, dtype=torch.float32, device=dev) for n in ("k", "v")}
+    slots_all = torch.arange(P * bs, dtype=torch.int64, device=dev)
+    krows = vals["k_pool"].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous().to(dev)
+    vrows = vals["v_pool"].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous().to(dev)
+    xy.xy_kv_append_fp8(krows, vrows, slots_all, codes["k"], codes["v"], scl["k"], scl["v"], err)
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
+                              kv_chunk=kv_chunk, kv_fp8=True)
+    q, kn, vn = (vals[n].to(dev) for n in ("q", "k_new", "v_new"))
+    out = xystep.run_step_fp8(batch, q, kn, vn, codes["k"], codes["v"], scl["k"], scl["v"], wl.scale)
+    torch.cuda.synchronize()
+    ref = oracle.step.run_step_fp8(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                   _bits(vals["q"]), _bits(vals["k_new"]), _bits(vals["v_new"]),
+                                   _bits(vals["k_pool"]), _bits(vals["v_pool"]), wl.scale, wl.causal)
+    return dict(err=int(err.item()) | int(batch.err.item()), batch=batch, out=oracle.bf16_bits_to_f64(_bits(out)),
+                ref=ref, codes={n: c.cpu().numpy() for n, c in codes.items()},
+                scales={n: s.cpu().numpy() for n, s in scl.items()})
+
+
+def _assert_fp8_parity(r, per_row_scale=False):
+    """Bit-exact slots, codes and scales; outputs within the bf16 tolerance (with per_row_scale,
+    relative to each output row's largest magnitude when that exceeds 1: bf16 rounds relatively)."""
+    from gpu_cases import MAX_ABS, MEAN_ABS
+    assert r["err"] == 0, f"device error word {r['err']:#x}"
+    assert np.array_equal(r["batch"].slots.cpu().numpy(), r["ref"]["slots"])
+    assert np.array_equal(r["codes"]["k"], r["ref"]["k_codes"]) and np.array_equal(r["codes"]["v"], r["ref"]["v_codes"])
+    assert np.array_equal(r["scales"]["k"].view(np.uint32), r["ref"]["k_scales"].view(np.uint32))
+    assert np.array_equal(r["scales"]["v"].view(np.uint32), r["ref"]["v_scales"].view(np.uint32))
+    assert np.isfinite(r["out"]).all()
+    diff = np.abs(r["out"] - r["ref"]["out"])
+    if per_row_scale:
+        diff = diff / np.maximum(1.0, np.abs(r["ref"]["out"]).max(axis=-1, keepdims=True))
+    assert diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS, (diff.max(), diff.mean())
+
+
+@pytest.mark.parametrize("G,bs", [(1, 16), (4, 16), (8, 64), (16, 256)])
+def test_fp8_decode_matches_oracle(G, bs):
+    # decode rows over ragged contexts (1 key, partial pages, partial 64-key stages, several chunks)
+    ctx = [1, 15, 16, 17, 63, 64, 65, 200, 1000, 2500, 777, 4096]
+    wl = workloads.custom(np.ones(len(ctx)), ctx, 4 * G, 4, 128, bs, seed=40 + G, name="fp8_decode")
+    _assert_fp8_parity(_run_fp8(wl))
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_fp8_mixed_batch_matches_oracle(G):
+    # prefill, chunked-prefill and verify-shaped queries (causal), several row groups per task
+    q_lens = [37, 1, 5, 100, 1, 16, 3]
+    ctx = [37, 900, 64, 612, 129, 16, 2050]
+    wl = workloads.custom(q_lens, ctx, 2 * G, 2, 128, 16, seed=50 + G, name="fp8_mixed")
+    _assert_fp8_parity(_run_fp8(wl))
+
+
+def test_fp8_split_kv_and_row_magnitudes():
+    # KV chunks of 256 keys (split partials and the combine) and rows of very different magnitude
+    # (the largest V scale grows along a task: O is rescaled as it does)
+    ctx = [3000, 1, 700, 5000, 257]
+    wl = workloads.custom(np.ones(len(ctx)), ctx, 32, 8, 128, 16, seed=61, name="fp8_split")
+    _assert_fp8_parity(_run_fp8(wl, kv_chunk=256, row_scale=[2.0 ** -12, 1.0, 2.0 ** 4]), per_row_scale=True)

@@ -111,3 +111,31 @@ def test_kv_append_fp8_writes_rows_and_scales():
     changed = (kp2 != kp).any(axis=-1)
     assert changed.sum() <= 2 * Hkv                          # only the two written slots
     assert np.array_equal(vp2[1, :, 1], quantize_rows(v_new)[0][0])
+
+
+def test_step_fp8_equals_bf16_step_when_quantization_is_exact():
+    # Rows whose every value k/64 (|k| <= 16) plus one 7 give s = 7/448 = 1/64 exactly and codes
+    # k and 448 that hold x/s without rounding: the 8-bit step then sees the same K and V as the
+    # bf16 step, so the two oracle steps agree to the last bit.
+    import oracle
+    rng = np.random.default_rng(3)
+    q_lens, ctx = [5, 1, 1, 20], [5, 40, 17, 70]
+    Hq, Hkv, d, bs, P = 4, 2, 64, 16, 24
+    cu = oracle.pack_cu_seqlens(q_lens)
+    T = int(cu[-1])
+
+    def rows(shape):
+        x = rng.integers(-16, 17, size=shape) / 64.0
+        x[..., rng.integers(0, d)] = 7.0
+        return f64_to_bf16_bits(x)
+
+    q = f64_to_bf16_bits(rng.standard_normal((T, Hq, d)))
+    kn, vn = rows((T, Hkv, d)), rows((T, Hkv, d))
+    kp, vp = rows((P, Hkv, bs, d)), rows((P, Hkv, bs, d))
+    free = rng.permutation(P).astype(np.int32)
+    args = (cu, np.asarray(ctx, dtype=np.int32), free, bs, 8, q, kn, vn, kp, vp, 0.125, True)
+    a = oracle.step.run_step(*args)
+    b = oracle.step.run_step_fp8(*args)
+    assert np.array_equal(a["slots"], b["slots"])
+    assert np.all(b["k_scales"] == np.float32(1.0 / 64)) and np.all(b["v_scales"] == np.float32(1.0 / 64))
+    assert np.array_equal(a["out"], b["out"])
