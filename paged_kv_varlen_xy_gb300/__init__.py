@@ -27,6 +27,8 @@ C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_n
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
+# 8-bit pages: rows per task when G <= this (include/xy.h)
+XY_FP8_NARROW_ROWS = 16
 
 
 class XYError(RuntimeError):
@@ -319,13 +321,16 @@ def check_err_word(err_word):
 
 def default_tiles(num_heads_q, num_heads_kv, head_dim=128, kv_fp8=False):
     """Tile policy of the kernels.  With head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
-    256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise, and always over
-    8-bit pages, up to 64 rows (q_tile = 64 // G).  KV chunks are 8192 keys, a multiple of every
+    256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise up to 64 rows
+    (q_tile = 64 // G).  Over 8-bit pages every task runs on the decode path with at most 16 rows
+    when G <= 16 (q_tile = 16 // G, so the kernel can keep 8 stages in flight), else 64.  KV chunks are 8192 keys, a multiple of every
     page size and of both kernels' KV tiles: long enough that split partials and merges stay few,
     short enough that a few long contexts still spread over the SMs (measured on the mixed and
     long-context batches)."""
     G = num_heads_q // num_heads_kv
-    if head_dim == 128 and 128 % G == 0 and not kv_fp8:
+    if kv_fp8:
+        return (max(1, XY_FP8_NARROW_ROWS // G) if G <= XY_FP8_NARROW_ROWS else max(1, 64 // G)), 8192
+    if head_dim == 128 and 128 % G == 0:
         return 256 // G, 8192
     return max(1, 64 // G), 8192
 

@@ -45,12 +45,20 @@ using xy::dec::kMathWarps;
 // warps need to consume one, so two producers keep the ring ahead of the math.  It runs every
 // task when the tcgen05 tile kernel cannot (head_dim 64, or G not dividing 128), pure decode
 // batches, and every batch over 8-bit pages; tasks then have at most 64 rows.
-constexpr int kProducers = 2;
+//
+// Page formats (KIND): kBf16; kFp8Narrow, 8-bit pages with tasks of at most 16 rows (G <= 16);
+// kFp8Wide, 8-bit pages with up to 64 rows per task (G > 16).  8-bit stages hold 128 keys (about
+// the bytes of a 64-key bf16 stage); with 16-token pages that is 32 copies per stage (codes and
+// scales of 8 pages), so four producer warps, one per ring stage, keep the ring ahead.
+enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2 };
 
-template <int HD, bool FP8>
+template <int HD, int KIND>
 struct Cfg {
-    using RG = typename std::conditional<FP8, xy::dec::RingF8<4, 16 * kMathWarps>,
-                                         xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type;
+    using RG = typename std::conditional<
+        KIND == kFp8Narrow, xy::dec::RingF8<4, 16>,
+        typename std::conditional<KIND == kFp8Wide, xy::dec::RingF8<4, 16 * kMathWarps>,
+                                  xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type;
+    static constexpr int kProducers = KIND == kBf16 ? 2 : 4;
     static_assert(RG::kStages % kProducers == 0, "a stage always has the same producer");
     static constexpr int kThreads = (kMathWarps + kProducers) * 32;
     static constexpr int kStagesOff = 0;
@@ -61,11 +69,11 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
-template <int HD, bool FP8>
-__global__ void __launch_bounds__(Cfg<HD, FP8>::kThreads, 1)
+template <int HD, int KIND>
+__global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
     paged_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p) {
-    using C = Cfg<HD, FP8>;
+    using C = Cfg<HD, KIND>;
     using RG = typename C::RG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = xy::smem_u32(smem_raw);
@@ -131,7 +139,7 @@ __global__ void __launch_bounds__(Cfg<HD, FP8>::kThreads, 1)
                         if (pref_valid) pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
                     }
                 },
-                pw, kProducers);
+                pw, C::kProducers);
             tc.advance(p);
         }
         if (!ok) {
@@ -139,7 +147,7 @@ __global__ void __launch_bounds__(Cfg<HD, FP8>::kThreads, 1)
             *abort_flag = 1;
         }
         // every stage this warp issued must have landed before the CTA may exit
-        xy::dec::drain<RG>(sm, ctr, pw, kProducers);
+        xy::dec::drain<RG>(sm, ctr, pw, C::kProducers);
         return;
     }
 
@@ -283,21 +291,21 @@ bool make_pool_map_u8(CUtensorMap *map, const void *pool, int64_t rows, int box_
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int HD, bool FP8>
+template <int HD, int KIND>
 xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
                  const xy_merge *merges, int num_merges, cudaStream_t st) {
-    using C = Cfg<HD, FP8>;
+    using C = Cfg<HD, KIND>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return XY_ERR_CUDA;
     if (configured_device != dev) {  // the attribute is per device
-        if (cudaFuncSetAttribute(paged_attention_kernel<HD, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_attention_kernel<HD, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return XY_ERR_CUDA;
         configured_device = dev;
     }
     if (p.num_tasks > 0) {
-        paged_attention_kernel<HD, FP8><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
+        paged_attention_kernel<HD, KIND><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel launch");
     }
@@ -409,8 +417,8 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
         }
         p.num_tasks = 0;  // ... so only the split-KV merge remains
     }
-    return head_dim == 128 ? launch<128, false>(p, km, vm, num_ctas, merges, num_merges, st)
-                           : launch<64, false>(p, km, vm, num_ctas, merges, num_merges, st);
+    return head_dim == 128 ? launch<128, kBf16>(p, km, vm, num_ctas, merges, num_merges, st)
+                           : launch<64, kBf16>(p, km, vm, num_ctas, merges, num_merges, st);
 }
 
 extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
@@ -435,12 +443,16 @@ extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seq
     p.vsc = v_scales;
 
     const int64_t rows = (int64_t)num_pages * num_heads_kv * block_size;
-    const int box_rows = block_size < xy::dec::kStageKeys ? block_size : xy::dec::kStageKeys;
+    const int keys = Cfg<128, kFp8Narrow>::RG::kKeys;  // both 8-bit rings stage 128 keys
+    static_assert(Cfg<128, kFp8Wide>::RG::kKeys == Cfg<128, kFp8Narrow>::RG::kKeys, "one box height");
+    const int box_rows = block_size < keys ? block_size : keys;
     CUtensorMap km, vm;
     if (!make_pool_map_u8(&km, k_pages, rows, box_rows) || !make_pool_map_u8(&vm, v_pages, rows, box_rows))
         return XY_ERR_CUDA;
     // every task runs on the decode path (f16 MMAs on converted codes)
-    return launch<128, true>(p, km, vm, num_ctas, merges, num_merges, static_cast<cudaStream_t>(stream));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return p.G <= XY_FP8_NARROW_ROWS ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
+                                     : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
 }
 
 // ---------------------------------------------------------------------------------------------

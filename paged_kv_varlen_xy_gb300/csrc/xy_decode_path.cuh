@@ -40,6 +40,7 @@ constexpr int kMathWarps = 4;
 template <int HD, int NS, int QR>
 struct Ring {
     static constexpr bool kFp8 = false;
+    static constexpr int kKeys = kStageKeys;                       // keys per stage
     static constexpr int kHalves = HD / 64;                        // 128-byte swizzle atoms per row
     static constexpr int kTensorBytes = kHalves * kStageKeys * 128;  // K or V of one stage
     static constexpr int kQOff = 2 * kTensorBytes;                 // query rows
@@ -50,28 +51,31 @@ struct Ring {
     static constexpr int kMaxRows = QR;
     static constexpr int kBytes = NS * kStageBytes;
     static constexpr int kSlotFloats = 16 * HD + 32;               // merge slot: O[16][HD], m[16], l[16]
-    static constexpr int kSlotBytes = kMathWarps * kSlotFloats * 4;
+    static constexpr int kSlotBytes = (kMathWarps - 1) * kSlotFloats * 4;  // warps ks >= 1
     static_assert(QR % 16 == 0 && QR <= 16 * kMathWarps, "rows per decode task");
 };
 
 // Geometry of an 8-bit decode stage ring (head_dim 128): NS stages, each holding the K and V codes
-// of 64 keys (one 128-byte row per key, 128-byte swizzle), the 64 keys' K scales then V scales
-// (fp32), and room for QR bf16 query rows.
-template <int NS, int QR>
+// of KEYS keys (one 128-byte row per key, 128-byte swizzle), their K scales then V scales (fp32),
+// and room for QR bf16 query rows.  A stage of 128 keys carries about as many bytes as a 64-key
+// bf16 stage, and gives each of four key-splitting math warps 32 keys.
+template <int NS, int QR, int KEYS = 128>
 struct RingF8 {
     static constexpr bool kFp8 = true;
+    static constexpr int kKeys = KEYS;
     static constexpr int kHalves = 1;
-    static constexpr int kTensorBytes = kStageKeys * 128;
+    static constexpr int kTensorBytes = KEYS * 128;
     static constexpr int kScaleOff = 2 * kTensorBytes;
-    static constexpr int kQOff = kScaleOff + 2 * kStageKeys * 4;
+    static constexpr int kQOff = kScaleOff + 2 * KEYS * 4;
     static constexpr int kQBytes = QR * 128 * 2;
     static constexpr int kStageBytes = (kQOff + kQBytes + 1023) / 1024 * 1024;  // stages stay 1024-aligned
     static constexpr int kStages = NS;
     static constexpr int kMaxRows = QR;
     static constexpr int kBytes = NS * kStageBytes;
     static constexpr int kSlotFloats = 16 * 128 + 32;
-    static constexpr int kSlotBytes = kMathWarps * kSlotFloats * 4;
+    static constexpr int kSlotBytes = (kMathWarps - 1) * kSlotFloats * 4;
     static_assert(QR % 16 == 0 && QR <= 16 * kMathWarps, "rows per decode task");
+    static_assert(KEYS % (32 * kMathWarps) == 0, "32 keys per math warp and step");
 };
 
 // Byte offset of 16-byte chunk `chunk` of key `key` in an 8-bit stage tensor: boxes of BR keys
@@ -107,7 +111,7 @@ __device__ __forceinline__ uint32_t swz(int key, int col, int sh) {
 // Checks of a decode-path task beyond task_common_ok.
 template <class RG>
 __device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) {
-    return task_common_ok(f, p) && f.t.q_rows * p.G <= RG::kMaxRows && (f.t.kv_start % kStageKeys) == 0;
+    return task_common_ok(f, p) && f.t.q_rows * p.G <= RG::kMaxRows && (f.t.kv_start % RG::kKeys) == 0;
 }
 
 // Producer warp `pw` of `npw`: issue the stages of decode task `f` whose ring counter is pw
@@ -122,7 +126,7 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
                              int pw = 0, int npw = 1) {
     const xy_task &t = f.t;
     const int bs_sh = 31 - __clz(p.bs);                   // page size is a power of two
-    const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;  // keys per TMA box
+    const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;  // keys per TMA box
     const int br_sh = 31 - __clz(BR);
     const uint32_t row_bytes = (uint32_t)p.G * HD * 2;     // one token's G query rows
     // block-table entries are read 32 logical pages at a time (one per lane), the next window
@@ -131,13 +135,13 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
     int pg_win = have_first ? pg_first : load_window(p, t.seq, win0, lane);
     int pg_nxt = load_window(p, t.seq, win0 + 32, lane);
     bool first_mine = true;
-    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
+    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += RG::kKeys, ++ctr) {
         if (ctr % npw != pw) continue;  // another producer's stage
         const int s = ctr % RG::kStages;
         if (ctr >= RG::kStages &&
             !__all_sync(0xffffffffu, mbar_wait(sm.empty_bar + 8 * s, ((ctr / RG::kStages) - 1) & 1, sm.abort_flag)))
             return false;
-        const int nkeys = min(kStageKeys, t.kv_end - kv0);
+        const int nkeys = min(RG::kKeys, t.kv_end - kv0);
         const int nbox = (nkeys + BR - 1) >> br_sh;
         while (((kv0 + nkeys - 1) >> bs_sh) - win0 >= 32) {  // the stage reaches into the next window
             win0 += 32;
@@ -170,7 +174,7 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
                                 sm.full_bar + 8 * s);
                 } else {
                     const float *src = (tensor == 2 ? p.ksc : p.vsc) + y;  // the box's BR scales
-                    bulk_load(stage + RG::kScaleOff + (tensor - 2) * kStageKeys * 4 + b * BR * 4, src,
+                    bulk_load(stage + RG::kScaleOff + (tensor - 2) * RG::kKeys * 4 + b * BR * 4, src,
                               (uint32_t)BR * 4, sm.full_bar + 8 * s);
                 }
             } else {
@@ -211,7 +215,7 @@ template <int HD, class RG, class F>
 __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
                              int lane, F first_stage_seen) {
     const int g4 = lane >> 2, c4 = lane & 3;
-    const int BR = p.bs < kStageKeys ? p.bs : kStageKeys;
+    const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;
     const int br_sh = 31 - __clz(BR);
     const xy_task t = f.t;
     const int R = t.q_rows * p.G;
@@ -229,7 +233,8 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
     };
     const int lim_a = row_limit(row_a), lim_b = row_limit(row_b);
     static_assert(!RG::kFp8 || HD == 128, "8-bit pages: head_dim 128");
-    // 8-bit pages: output column of accumulator pair n (see the V fragments below)
+    // output columns of accumulator pair n: 8n + 2c, +1; over 8-bit pages 16(n/2) + 4c + 2(n%2), +1
+    // (see the V fragments of fp8_keys32)
     auto ocol = [&](int n) -> int { return RG::kFp8 ? 16 * (n >> 1) + 4 * c4 + 2 * (n & 1) : 8 * n + 2 * c4; };
     float s_max = 0.f, s_inv = 0.f;  // 8-bit pages: largest V scale seen, and its reciprocal
     int lim_max = max(lim_a, lim_b);
@@ -244,9 +249,151 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
     for (int n = 0; n < HD / 8; ++n) o_acc[n][0] = o_acc[n][1] = o_acc[n][2] = o_acc[n][3] = 0.f;
     float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
 
-    const int sub = kStageKeys / wpg;
+    // 8-bit pages: 32 keys of one stage, as two 16-key blocks b = 0, 1 whose QK^T chains are
+    // independent and which share one max / rescale step.  K scales multiply the fp32 scores;
+    // V scales the weights, relative to s_max (the largest V scale so far, so the packed f16
+    // weights stay in [0, 1]); O is kept in units of s_max and rescaled when s_max grows.
+    auto fp8_keys32 = [&](uint32_t kst, uint32_t vst, const float *scl, int kc, int kr) {
+        const int mi = lane >> 3;
+        float sc[2][2][4];  // [block][n-tile: keys 8j..8j+7 of the block][C fragment]
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) sc[b][j][0] = sc[b][j][1] = sc[b][j][2] = sc[b][j][3] = 0.f;
+        // ldmatrix over the code rows: matrix i holds keys 8(i&1).. of 16-byte chunk 2cc+(i>>1);
+        // lane (g, c) gets the codes of cols 4c..4c+3 of key g, i.e. the B fragment of one k-step
+        // in the k-order of the query fragments
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int krow = kr + 16 * b + ((mi & 1) << 3) + (lane & 7);
+                uint32_t r[4];
+                ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    mma_f16_16816(sc[b][i & 1], qa[2 * cc + (i >> 1)], e4m3x2_to_f16x2((uint16_t)(r[i] & 0xffffu)),
+                                  e4m3x2_to_f16x2((uint16_t)(r[i] >> 16)));
+            }
+        }
+        // scales of this lane's keys kc + 16b + 8j + 2c + e (V scales of keys at or past kv_end,
+        // which may hold anything, read as 0); virtual + causal mask; online softmax (log2 domain)
+        float vsc[2][2][2];
+        float mx_a = -INFINITY, mx_b = -INFINITY, vmax = 0.f;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int o = kr + 16 * b + 8 * j + 2 * c4;
+                const float2 kx = *reinterpret_cast<const float2 *>(scl + o);
+                const float2 vx = *reinterpret_cast<const float2 *>(scl + RG::kKeys + o);
+                const int key = kc + 16 * b + 8 * j + 2 * c4;
+                vsc[b][j][0] = key < t.kv_end ? vx.x : 0.f;
+                vsc[b][j][1] = key + 1 < t.kv_end ? vx.y : 0.f;
+                vmax = fmaxf(vmax, fmaxf(vsc[b][j][0], vsc[b][j][1]));
+                const float f0 = p.scale_log2 * kx.x, f1 = p.scale_log2 * kx.y;
+                sc[b][j][0] = key < lim_a ? sc[b][j][0] * f0 : -INFINITY;
+                sc[b][j][1] = key + 1 < lim_a ? sc[b][j][1] * f1 : -INFINITY;
+                sc[b][j][2] = key < lim_b ? sc[b][j][2] * f0 : -INFINITY;
+                sc[b][j][3] = key + 1 < lim_b ? sc[b][j][3] * f1 : -INFINITY;
+                mx_a = fmaxf(mx_a, fmaxf(sc[b][j][0], sc[b][j][1]));
+                mx_b = fmaxf(mx_b, fmaxf(sc[b][j][2], sc[b][j][3]));
+            }
+        }
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
+        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+        const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
+        const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
+        float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
+        m_a = mn_a;
+        m_b = mn_b;
+        float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                sc[b][j][0] = ex2(sc[b][j][0] - mu_a);
+                sc[b][j][1] = ex2(sc[b][j][1] - mu_a);
+                sc[b][j][2] = ex2(sc[b][j][2] - mu_b);
+                sc[b][j][3] = ex2(sc[b][j][3] - mu_b);
+                ps_a += sc[b][j][0] + sc[b][j][1];
+                ps_b += sc[b][j][2] + sc[b][j][3];
+            }
+        }
+        l_a = l_a * al_a + ps_a;
+        l_b = l_b * al_b + ps_b;
+        if (vmax > s_max) {  // the same in every quad: warp-uniform
+            const float g = s_max / vmax;
+            al_a *= g;
+            al_b *= g;
+            s_max = vmax;
+            s_inv = 1.f / vmax;
+        }
+#pragma unroll
+        for (int n = 0; n < HD / 8; ++n) {
+            o_acc[n][0] *= al_a;
+            o_acc[n][1] *= al_a;
+            o_acc[n][2] *= al_b;
+            o_acc[n][3] *= al_b;
+        }
+        uint32_t pa[2][4];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float w0 = vsc[b][j][0] * s_inv, w1 = vsc[b][j][1] * s_inv;
+                pa[b][2 * j] = pack_f16x2(sc[b][j][0] * w0, sc[b][j][1] * w1);
+                pa[b][2 * j + 1] = pack_f16x2(sc[b][j][2] * w0, sc[b][j][3] * w1);
+            }
+        }
+        // ldmatrix.trans over the code rows: matrix i holds keys 8(i&1).. of chunk 2cc+(i>>1);
+        // lane (g, c) gets the code pairs (cols 2g, 2g+1) of keys 2c and 2c+1 (+8).  Regrouped by
+        // column they are the B fragments of two n-tiles: even columns 2g and odd columns 2g+1 of
+        // the chunk, so the C fragments of pair 2ch + {0, 1} hold columns 16ch + 4c + {0, 2} and
+        // {1, 3}.  Keys at or past kv_end get zero V entries, so 0 * NaN cannot occur.
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int key_lo = kc + 16 * b + 2 * c4;
+            const bool tail = kc + 16 * b + 16 > t.kv_end;
+            const uint32_t keep0 =
+                (key_lo < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 1 < t.kv_end ? 0xffff0000u : 0u);
+            const uint32_t keep1 =
+                (key_lo + 8 < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 9 < t.kv_end ? 0xffff0000u : 0u);
+            const int vrow = kr + 16 * b + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc) {
+                uint32_t r[4];
+                ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t x0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu));
+                    const uint32_t x1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16));
+                    const uint32_t y0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu));
+                    const uint32_t y1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16));
+                    uint32_t ea0 = __byte_perm(x0, x1, 0x5410), eb0 = __byte_perm(x0, x1, 0x7632);
+                    uint32_t ea1 = __byte_perm(y0, y1, 0x5410), eb1 = __byte_perm(y0, y1, 0x7632);
+                    if (tail) {
+                        ea0 &= keep0;
+                        eb0 &= keep0;
+                        ea1 &= keep1;
+                        eb1 &= keep1;
+                    }
+                    const int ch = 2 * cc + h;
+                    mma_f16_16816(o_acc[2 * ch], pa[b], ea0, ea1);
+                    mma_f16_16816(o_acc[2 * ch + 1], pa[b], eb0, eb1);
+                }
+            }
+        }
+    };
+
+    const int sub = RG::kKeys / wpg;
     bool ok = true;
-    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += kStageKeys, ++ctr) {
+    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += RG::kKeys, ++ctr) {
         const int s = ctr % RG::kStages;
         if (!mbar_wait(sm.full_bar + 8 * s, (ctr / RG::kStages) & 1, sm.abort_flag)) {
             ok = false;
@@ -261,8 +408,8 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 if constexpr (RG::kFp8) {
-                    // k-order of the 8-bit K fragments: k 2c, 2c+1 hold cols 16kk+4c, +1 and
-                    // k 2c+8, 2c+9 hold cols 16kk+4c+2, +3 (a dot product may sum in any order)
+                    // f16, in the k-order of the 8-bit K fragments: k 2c, 2c+1 hold cols 16kk+4c,
+                    // +1 and k 2c+8, 2c+9 cols 16kk+4c+2, +3 (a dot product may sum in any order)
                     const int w0 = kk * 8 + 2 * c4, w1 = w0 + 1;
                     qa[kk][0] = qa_ptr ? bf16x2_to_f16x2(qa_ptr[w0]) : 0u;
                     qa[kk][1] = qb_ptr ? bf16x2_to_f16x2(qb_ptr[w0]) : 0u;
@@ -281,180 +428,95 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
 
         const int k_lo = kv0 + ks * sub;
         const int k_hi = min(min(k_lo + sub, t.kv_end), lim_max);
-        for (int kc = k_lo; kc < k_hi; kc += 16) {
-            const int kr = kc - kv0;
-            float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            // 8-bit pages: the scales of this thread's keys kc + 8j + 2c + e (V scales of keys at or
-            // past kv_end, which may hold anything, read as 0)
-            float ksc[2][2] = {{1.f, 1.f}, {1.f, 1.f}}, vsc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-            if constexpr (RG::kFp8) {
-                const float *scl = reinterpret_cast<const float *>(sm.stages_gen + s * RG::kStageBytes + RG::kScaleOff);
-#pragma unroll
+        if constexpr (RG::kFp8) {
+            const float *scl = reinterpret_cast<const float *>(sm.stages_gen + s * RG::kStageBytes + RG::kScaleOff);
+            for (int kc = k_lo; kc < k_hi; kc += 32) fp8_keys32(kst, vst, scl, kc, kc - kv0);
+        } else {
+            for (int kc = k_lo; kc < k_hi; kc += 16) {
+                const int kr = kc - kv0;
+                float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                {
+                    const int mi = lane >> 3;
+                    const int krow = kr + ((mi >> 1) << 3) + (lane & 7);
+    #pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(kst + swz<HD>(krow, kk * 16 + ((mi & 1) << 3), br_sh), b0, b1, b2, b3);
+                        mma_bf16_16816(sc[0], qa[kk], b0, b1);
+                        mma_bf16_16816(sc[1], qa[kk], b2, b3);
+                    }
+                }
+                // virtual + causal mask, then online softmax in the log2 domain
+                float mx_a = -INFINITY, mx_b = -INFINITY;
+    #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const float2 kx = *reinterpret_cast<const float2 *>(scl + kr + 8 * j + 2 * c4);
-                    const float2 vx = *reinterpret_cast<const float2 *>(scl + kStageKeys + kr + 8 * j + 2 * c4);
-                    const int key = kc + 8 * j + 2 * c4;
-                    ksc[j][0] = kx.x;
-                    ksc[j][1] = kx.y;
-                    vsc[j][0] = key < t.kv_end ? vx.x : 0.f;
-                    vsc[j][1] = key + 1 < t.kv_end ? vx.y : 0.f;
+    #pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int key = kc + 8 * j + 2 * c4 + e;
+                        sc[j][e] = key < lim_a ? sc[j][e] * p.scale_log2 : -INFINITY;
+                        sc[j][2 + e] = key < lim_b ? sc[j][2 + e] * p.scale_log2 : -INFINITY;
+                        mx_a = fmaxf(mx_a, sc[j][e]);
+                        mx_b = fmaxf(mx_b, sc[j][2 + e]);
+                    }
                 }
-                // ldmatrix over the code rows: matrix i holds keys 8(i&1).. of 16-byte chunk 2cc+(i>>1);
-                // lane (g, c) gets codes of cols 4c..4c+3 of key g, i.e. the B fragment of a k-step
-                // in the k-order the query fragments use
-                const int mi = lane >> 3;
-                const int krow = kr + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    uint32_t r[4];
-                    ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        mma_f16_16816(sc[i & 1], qa[2 * cc + (i >> 1)], e4m3x2_to_f16x2((uint16_t)(r[i] & 0xffffu)),
-                                      e4m3x2_to_f16x2((uint16_t)(r[i] >> 16)));
-                }
-            } else {
-                const int mi = lane >> 3;
-                const int krow = kr + ((mi >> 1) << 3) + (lane & 7);
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kst + swz<HD>(krow, kk * 16 + ((mi & 1) << 3), br_sh), b0, b1, b2, b3);
-                    mma_bf16_16816(sc[0], qa[kk], b0, b1);
-                    mma_bf16_16816(sc[1], qa[kk], b2, b3);
-                }
-            }
-            // virtual + causal mask, then online softmax in the log2 domain
-            float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = kc + 8 * j + 2 * c4 + e;
-                    const float f = RG::kFp8 ? p.scale_log2 * ksc[j][e] : p.scale_log2;
-                    sc[j][e] = key < lim_a ? sc[j][e] * f : -INFINITY;
-                    sc[j][2 + e] = key < lim_b ? sc[j][2 + e] * f : -INFINITY;
-                    mx_a = fmaxf(mx_a, sc[j][e]);
-                    mx_b = fmaxf(mx_b, sc[j][2 + e]);
-                }
-            }
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-            const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
-            const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
-            float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
-            m_a = mn_a;
-            m_b = mn_b;
-            float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                sc[j][0] = ex2(sc[j][0] - mu_a);
-                sc[j][1] = ex2(sc[j][1] - mu_a);
-                sc[j][2] = ex2(sc[j][2] - mu_b);
-                sc[j][3] = ex2(sc[j][3] - mu_b);
-                ps_a += sc[j][0] + sc[j][1];
-                ps_b += sc[j][2] + sc[j][3];
-            }
-            l_a = l_a * al_a + ps_a;
-            l_b = l_b * al_b + ps_b;
-            if constexpr (RG::kFp8) {
-                // weights times V scale / s_max: s_max is the largest V scale so far, so the packed
-                // weights stay in [0, 1]; O (kept in units of s_max) is rescaled when it grows
-                float sm_new = fmaxf(fmaxf(vsc[0][0], vsc[0][1]), fmaxf(vsc[1][0], vsc[1][1]));
-                sm_new = fmaxf(sm_new, __shfl_xor_sync(0xffffffffu, sm_new, 1));
-                sm_new = fmaxf(sm_new, __shfl_xor_sync(0xffffffffu, sm_new, 2));
-                if (sm_new > s_max) {  // the same in every quad: warp-uniform
-                    const float g = s_max / sm_new;
-                    al_a *= g;
-                    al_b *= g;
-                    s_max = sm_new;
-                    s_inv = 1.f / sm_new;
-                }
-#pragma unroll
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+                const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+                const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
+                const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
+                const float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
+                m_a = mn_a;
+                m_b = mn_b;
+                float ps_a = 0.f, ps_b = 0.f;
+    #pragma unroll
                 for (int j = 0; j < 2; ++j) {
-                    const float w0 = vsc[j][0] * s_inv, w1 = vsc[j][1] * s_inv;
-                    sc[j][0] *= w0;
-                    sc[j][1] *= w1;
-                    sc[j][2] *= w0;
-                    sc[j][3] *= w1;
+                    sc[j][0] = ex2(sc[j][0] - mu_a);
+                    sc[j][1] = ex2(sc[j][1] - mu_a);
+                    sc[j][2] = ex2(sc[j][2] - mu_b);
+                    sc[j][3] = ex2(sc[j][3] - mu_b);
+                    ps_a += sc[j][0] + sc[j][1];
+                    ps_b += sc[j][2] + sc[j][3];
                 }
-            }
-#pragma unroll
-            for (int n = 0; n < HD / 8; ++n) {
-                o_acc[n][0] *= al_a;
-                o_acc[n][1] *= al_a;
-                o_acc[n][2] *= al_b;
-                o_acc[n][3] *= al_b;
-            }
-            uint32_t pa[4];
-            if constexpr (RG::kFp8) {
-                pa[0] = pack_f16x2(sc[0][0], sc[0][1]);
-                pa[1] = pack_f16x2(sc[0][2], sc[0][3]);
-                pa[2] = pack_f16x2(sc[1][0], sc[1][1]);
-                pa[3] = pack_f16x2(sc[1][2], sc[1][3]);
-            } else {
+                l_a = l_a * al_a + ps_a;
+                l_b = l_b * al_b + ps_b;
+    #pragma unroll
+                for (int n = 0; n < HD / 8; ++n) {
+                    o_acc[n][0] *= al_a;
+                    o_acc[n][1] *= al_a;
+                    o_acc[n][2] *= al_b;
+                    o_acc[n][3] *= al_b;
+                }
+                uint32_t pa[4];
                 pa[0] = pack_bf16x2(sc[0][0], sc[0][1]);
                 pa[1] = pack_bf16x2(sc[0][2], sc[0][3]);
                 pa[2] = pack_bf16x2(sc[1][0], sc[1][1]);
                 pa[3] = pack_bf16x2(sc[1][2], sc[1][3]);
-            }
-            // keys at or past kv_end may hold anything (unused slots, stale stage data): their
-            // weights are 0, and their V entries are zeroed so 0 * NaN cannot occur
-            const bool tail = kc + 16 > t.kv_end;
-            const int key_lo = kc + 2 * c4;
-            const uint32_t keep0 =
-                (key_lo < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 1 < t.kv_end ? 0xffff0000u : 0u);
-            const uint32_t keep1 =
-                (key_lo + 8 < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 9 < t.kv_end ? 0xffff0000u : 0u);
-            if constexpr (RG::kFp8) {
-                // ldmatrix.trans over the code rows: matrix i holds keys 8(i&1).. of chunk 2cc+(i>>1);
-                // lane (g, c) gets the code pairs (cols 2g, 2g+1) of keys 2c and 2c+1 (+8).  Byte
-                // pairs regrouped by column give the B fragments of two n-tiles: even columns 2g
-                // and odd columns 2g+1 of the chunk, so accumulator pair n of this lane covers
-                // columns 16(n/2) + 4c + 2(n%2) + {0, 1} once the tiles are interleaved below.
-                const int mi = lane >> 3;
-                const int vrow = kr + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    uint32_t r[4];
-                    ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t x0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu));
-                        const uint32_t x1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16));
-                        const uint32_t y0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu));
-                        const uint32_t y1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16));
-                        uint32_t ea0 = __byte_perm(x0, x1, 0x5410), eb0 = __byte_perm(x0, x1, 0x7632);
-                        uint32_t ea1 = __byte_perm(y0, y1, 0x5410), eb1 = __byte_perm(y0, y1, 0x7632);
+                // keys at or past kv_end may hold anything (unused slots, stale stage data): their
+                // weights are 0, and their V entries are zeroed so 0 * NaN cannot occur
+                const bool tail = kc + 16 > t.kv_end;
+                const int key_lo = kc + 2 * c4;
+                const uint32_t keep0 =
+                    (key_lo < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 1 < t.kv_end ? 0xffff0000u : 0u);
+                const uint32_t keep1 =
+                    (key_lo + 8 < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 9 < t.kv_end ? 0xffff0000u : 0u);
+                {
+                    const int mi = lane >> 3;
+                    const int vrow = kr + ((mi & 1) << 3) + (lane & 7);
+    #pragma unroll
+                    for (int jd = 0; jd < HD / 16; ++jd) {
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4_t(vst + swz<HD>(vrow, 8 * (2 * jd + (mi >> 1)), br_sh), b0, b1, b2, b3);
                         if (tail) {
-                            ea0 &= keep0;
-                            eb0 &= keep0;
-                            ea1 &= keep1;
-                            eb1 &= keep1;
+                            b0 &= keep0;
+                            b1 &= keep1;
+                            b2 &= keep0;
+                            b3 &= keep1;
                         }
-                        const int ch = 2 * cc + h;
-                        mma_f16_16816(o_acc[2 * ch], pa, ea0, ea1);
-                        mma_f16_16816(o_acc[2 * ch + 1], pa, eb0, eb1);
+                        mma_bf16_16816(o_acc[2 * jd], pa, b0, b1);
+                        mma_bf16_16816(o_acc[2 * jd + 1], pa, b2, b3);
                     }
-                }
-            } else {
-                const int mi = lane >> 3;
-                const int vrow = kr + ((mi & 1) << 3) + (lane & 7);
-#pragma unroll
-                for (int jd = 0; jd < HD / 16; ++jd) {
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vst + swz<HD>(vrow, 8 * (2 * jd + (mi >> 1)), br_sh), b0, b1, b2, b3);
-                    if (tail) {
-                        b0 &= keep0;
-                        b1 &= keep1;
-                        b2 &= keep0;
-                        b3 &= keep1;
-                    }
-                    mma_bf16_16816(o_acc[2 * jd], pa, b0, b1);
-                    mma_bf16_16816(o_acc[2 * jd + 1], pa, b2, b3);
                 }
             }
         }
@@ -483,8 +545,8 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
     l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
 
-    if (wpg > 1) {
-        float *my = sm.slots + w * RG::kSlotFloats;
+    if (wpg > 1 && ks > 0) {  // warps ks >= 1 hand their triples to warp ks = 0 of their slice
+        float *my = sm.slots + (w - nrg) * RG::kSlotFloats;
 #pragma unroll
         for (int n = 0; n < HD / 8; ++n) {
             const int col = ocol(n);
@@ -512,7 +574,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         if (ks == 0) {
             float M_a = m_a, M_b = m_b;
             for (int k = 1; k < wpg; ++k) {
-                const float *ot = sm.slots + (rg + k * nrg) * RG::kSlotFloats;
+                const float *ot = sm.slots + (rg + (k - 1) * nrg) * RG::kSlotFloats;
                 M_a = fmaxf(M_a, ot[16 * HD + g4]);
                 M_b = fmaxf(M_b, ot[16 * HD + g4 + 8]);
             }
@@ -528,7 +590,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 o_acc[n][3] *= f_b;
             }
             for (int k = 1; k < wpg; ++k) {
-                const float *ot = sm.slots + (rg + k * nrg) * RG::kSlotFloats;
+                const float *ot = sm.slots + (rg + (k - 1) * nrg) * RG::kSlotFloats;
                 const float ga = ex2(ot[16 * HD + g4] - U_a), gb = ex2(ot[16 * HD + g4 + 8] - U_b);
                 l_a += ga * ot[16 * HD + 16 + g4];
                 l_b += gb * ot[16 * HD + 16 + g4 + 8];
