@@ -49,7 +49,7 @@ using xy::dec::kMathWarps;
 // Page formats (KIND): kBf16; kFp8Narrow, 8-bit pages with tasks of at most 16 rows (G <= 16);
 // kFp8Wide, 8-bit pages with up to 64 rows per task (G > 16).  8-bit stages hold 128 keys (about
 // the bytes of a 64-key bf16 stage); with 16-token pages that is 32 copies per stage (codes and
-// scales of 8 pages), so four producer warps, one per ring stage, keep the ring ahead.
+// scales of 8 pages), so four producer warps, one per ring slot, keep the ring ahead.
 enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2 };
 
 template <int HD, int KIND>
@@ -59,7 +59,7 @@ struct Cfg {
         typename std::conditional<KIND == kFp8Wide, xy::dec::RingF8<4, 16 * kMathWarps>,
                                   xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type;
     static constexpr int kProducers = KIND == kBf16 ? 2 : 4;
-    static_assert(RG::kStages % kProducers == 0, "a stage always has the same producer");
+    static_assert(RG::kStages >= kProducers, "every producer owns a ring slot");
     static constexpr int kThreads = (kMathWarps + kProducers) * 32;
     static constexpr int kStagesOff = 0;
     static constexpr int kSlotsOff = RG::kBytes;

@@ -114,9 +114,9 @@ __device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) 
     return task_common_ok(f, p) && f.t.q_rows * p.G <= RG::kMaxRows && (f.t.kv_start % RG::kKeys) == 0;
 }
 
-// Producer warp `pw` of `npw`: issue the stages of decode task `f` whose ring counter is pw
-// modulo npw (with npw dividing the ring depth, a stage always has the same producer, so each
-// producer waits only on its own stages' empty barriers).  `ctr` counts all of the task's stages.
+// Producer warp `pw` of `npw`: issue the stages of decode task `f` that land in ring slots
+// s = pw, pw + npw, ... (a slot always has the same producer, which issues its uses in order, so
+// each producer waits only on its own slots' empty barriers).  `ctr` counts all of the stages.
 // `pg_first` is the task's first block-table window if it was prefetched (else -1 with
 // have_first false).  `first_stage_done()` runs once, right after this warp's first stage of the
 // task is issued (the caller prefetches the next task there).  Returns false if a wait gave up.
@@ -136,7 +136,7 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
     int pg_nxt = load_window(p, t.seq, win0 + 32, lane);
     bool first_mine = true;
     for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += RG::kKeys, ++ctr) {
-        if (ctr % npw != pw) continue;  // another producer's stage
+        if ((ctr % RG::kStages) % npw != pw) continue;  // another producer's slot
         const int s = ctr % RG::kStages;
         if (ctr >= RG::kStages &&
             !__all_sync(0xffffffffu, mbar_wait(sm.empty_bar + 8 * s, ((ctr / RG::kStages) - 1) & 1, sm.abort_flag)))
@@ -204,7 +204,7 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
 template <class RG>
 __device__ __forceinline__ void drain(const Smem &sm, int ctr, int pw = 0, int npw = 1) {
     for (int k = ctr - 1; k >= 0 && k >= ctr - RG::kStages; --k)
-        if (k % npw == pw) mbar_wait(sm.full_bar + 8 * (k % RG::kStages), (k / RG::kStages) & 1);
+        if ((k % RG::kStages) % npw == pw) mbar_wait(sm.full_bar + 8 * (k % RG::kStages), (k / RG::kStages) & 1);
 }
 
 // Math warp w (0..3) runs decode task `f`.  `ctr` counts stages consumed on the ring, `iter` the
@@ -271,9 +271,11 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 uint32_t r[4];
                 ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    mma_f16_16816(sc[b][i & 1], qa[2 * cc + (i >> 1)], e4m3x2_to_f16x2((uint16_t)(r[i] & 0xffffu)),
-                                  e4m3x2_to_f16x2((uint16_t)(r[i] >> 16)));
+                for (int i = 0; i < 4; ++i) {
+                    uint32_t b0, b1;
+                    e4m3x4_to_f16x2x2(r[i], b0, b1);
+                    mma_f16_16816(sc[b][i & 1], qa[2 * cc + (i >> 1)], b0, b1);
+                }
             }
         }
         // scales of this lane's keys kc + 16b + 8j + 2c + e (V scales of keys at or past kv_end,
@@ -306,12 +308,19 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
         vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
-        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-        const float mu_a = mn_a == -INFINITY ? 0.f : mn_a;
-        const float mu_b = mn_b == -INFINITY ? 0.f : mn_b;
-        float al_a = ex2(m_a - mu_a), al_b = ex2(m_b - mu_b);
-        m_a = mn_a;
-        m_b = mn_b;
+        // The reference max m is raised only when a row's max exceeds it by more than 8 (weights
+        // then stay <= 2^8, fine in f16 and fp32); the stale reference cancels in O / l.
+        float al_a = 1.f, al_b = 1.f;
+        const bool grow_a = mx_a > m_a + 8.f, grow_b = mx_b > m_b + 8.f;
+        if (__any_sync(0xffffffffu, grow_a || grow_b)) {
+            const float mn_a = grow_a ? mx_a : m_a, mn_b = grow_b ? mx_b : m_b;
+            al_a = ex2(m_a - (mn_a == -INFINITY ? 0.f : mn_a));
+            al_b = ex2(m_b - (mn_b == -INFINITY ? 0.f : mn_b));
+            m_a = mn_a;
+            m_b = mn_b;
+        }
+        const float mu_a = m_a == -INFINITY ? 0.f : m_a;
+        const float mu_b = m_b == -INFINITY ? 0.f : m_b;
         float ps_a = 0.f, ps_b = 0.f;
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
@@ -327,19 +336,23 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         }
         l_a = l_a * al_a + ps_a;
         l_b = l_b * al_b + ps_b;
+        bool rescale = al_a != 1.f || al_b != 1.f;
         if (vmax > s_max) {  // the same in every quad: warp-uniform
             const float g = s_max / vmax;
             al_a *= g;
             al_b *= g;
             s_max = vmax;
             s_inv = 1.f / vmax;
+            rescale = true;
         }
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-        for (int n = 0; n < HD / 8; ++n) {
-            o_acc[n][0] *= al_a;
-            o_acc[n][1] *= al_a;
-            o_acc[n][2] *= al_b;
-            o_acc[n][3] *= al_b;
+            for (int n = 0; n < HD / 8; ++n) {
+                o_acc[n][0] *= al_a;
+                o_acc[n][1] *= al_a;
+                o_acc[n][2] *= al_b;
+                o_acc[n][3] *= al_b;
+            }
         }
         uint32_t pa[2][4];
 #pragma unroll
@@ -371,12 +384,10 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const uint32_t x0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] & 0xffffu));
-                    const uint32_t x1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h] >> 16));
-                    const uint32_t y0 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] & 0xffffu));
-                    const uint32_t y1 = e4m3x2_to_f16x2((uint16_t)(r[2 * h + 1] >> 16));
-                    uint32_t ea0 = __byte_perm(x0, x1, 0x5410), eb0 = __byte_perm(x0, x1, 0x7632);
-                    uint32_t ea1 = __byte_perm(y0, y1, 0x5410), eb1 = __byte_perm(y0, y1, 0x7632);
+                    // bytes (k0 c0, k0 c1, k1 c0, k1 c1) regrouped as (k0 c0, k1 c0, k0 c1, k1 c1)
+                    uint32_t ea0, eb0, ea1, eb1;
+                    e4m3x4_to_f16x2x2(__byte_perm(r[2 * h], 0u, 0x3120), ea0, eb0);
+                    e4m3x4_to_f16x2x2(__byte_perm(r[2 * h + 1], 0u, 0x3120), ea1, eb1);
                     if (tail) {
                         ea0 &= keep0;
                         eb0 &= keep0;

@@ -136,11 +136,12 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two E4M3 codes (lo in bits 0-7) -> two f16 values (exact; lo in bits 0-15).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
-    return r;
+// Four E4M3 codes (bytes 0-3 of w) -> two f16x2 (exact): lo from bytes 0, 1 and hi from bytes 2, 3,
+// the lower byte of each pair in the lower half.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 // Two fp32 values -> f16x2 (lo in bits 0-15), round to nearest even.
