@@ -378,6 +378,10 @@ def main():
     host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     meta = dict(cu=wl.cu_seqlens_q, ctx=wl.context_lens, free=wl.free_list)
+    # a serving loop re-plans every step: block table, task table and their upload (packed into
+    # one copy by the Planner, created once like an engine's state) are inside the timed region
+    planner = xystep.Planner(wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.block_size, wl.max_blocks, wl.causal,
+                             device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8)
     e2e_times = []
     h2d = d2h = 0
     for k in range(args.warmup + args.steps):
@@ -385,23 +389,20 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        b2 = xystep.PagedBatch(meta["cu"], meta["ctx"], meta["free"], wl.block_size, wl.max_blocks, wl.num_heads_q,
-                               wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8)
+        b2 = planner.plan(meta["cu"], meta["ctx"], meta["free"])
         qd = host["q"].to(dev, non_blocking=True)
         kd = host["k_new"].to(dev, non_blocking=True)
         vd = host["v_new"].to(dev, non_blocking=True)
         if fp8:
-            o = xystep.run_step_fp8(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], vals["k_scales"],
-                                    vals["v_scales"], wl.scale)
+            o = planner.run(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], wl.scale, k_scales=vals["k_scales"],
+                            v_scales=vals["v_scales"])
         else:
-            o = xystep.run_step(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
+            o = planner.run(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
         out_host.copy_(o, non_blocking=True)
         torch.cuda.synchronize()
         e2e_times.append(time.perf_counter() - t0)
         if k == 0:
-            h2d = sum(host[x].numel() * 2 for x in host) + sum(t.numel() * t.element_size() for t in
-                                                                (b2.cu, b2.ctx, b2.block_table, b2.plan.tasks,
-                                                                 b2.plan.merges))
+            h2d = sum(host[x].numel() * 2 for x in host) + planner.last_upload_bytes
             d2h = out_host.numel() * 2
     e2e_s = max_over_ranks(sum(e2e_times[args.warmup:]) / args.steps, world, device=dev)
     e2e_val = job_throughput(args.config, w, e2e_s, world)

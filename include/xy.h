@@ -197,6 +197,34 @@ xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *contex
                               size_t *workspace_bytes, xy_task_stats *stats);
 
 /*
+ * One step's host-built metadata in one buffer (no counterpart in the pages: a runtime helper
+ * for callers that re-plan every step).  Builds the block table (as xy_build_block_table) and the
+ * task table (as xy_build_task_table) and packs, into the caller's host buffer `staging`
+ * (ideally pinned), at offsets that are multiples of XY_STEP_TABLES_ALIGN bytes: a zero int32
+ * error word, cu_seqlens_q [S+1], context_lens [S], the block table [S, max_blocks], the task
+ * records and the merge records, so one host->device copy of the first `bytes` bytes gives the
+ * device every table of the step (the caller passes device addresses base + offset to the device
+ * calls).  *out receives the offsets, sizes, counts, workspace bytes and stats; if
+ * staging_bytes < out->bytes it returns XY_ERR_CAPACITY with *out filled and nothing written.
+ * Errors: those of the two builders; XY_ERR_INVALID_ARG for a null out.
+ */
+#define XY_STEP_TABLES_ALIGN 256
+
+typedef struct {
+    size_t err_off, cu_off, ctx_off, bt_off, tasks_off, merges_off; /* byte offsets in staging */
+    size_t bytes;                                                   /* end of the merge records */
+    size_t workspace_bytes;                                         /* split-KV workspace needed */
+    int num_tasks, num_merges, pages_used;
+    xy_task_stats stats;
+} xy_step_tables;
+
+xy_status xy_build_step_tables(const int32_t *cu_seqlens_q, const int32_t *context_lens, int num_seqs,
+                               const int32_t *free_list, int num_free, int block_size, int max_blocks,
+                               int num_heads_q, int num_heads_kv, int head_dim, int causal, int num_ctas,
+                               int q_tile, int kv_chunk, int schedule, void *staging, size_t staging_bytes,
+                               xy_step_tables *out);
+
+/*
  * a5..a10 — paged attention ([XY] §2.2 component 3 Meta-Attention: one GEMM-softmax-GEMM
  * kernel driven by the task table, with no prefill/decode distinction; [CANN] §3.3 packed
  * paged_attention(q_packed, kv_pages, cu_seqlens, page_table, is_causal); [XY] §2.3 virtual

@@ -23,7 +23,7 @@ XY_DEV_TIMEOUT = 0x8
 C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
          "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
-         "xy_paged_attention_fp8")
+         "xy_paged_attention_fp8", "xy_build_step_tables")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -52,6 +52,14 @@ class XYDeviceError(RuntimeError):
 class TaskStats(ctypes.Structure):
     _fields_ = [("total_load", ctypes.c_int64), ("max_cta_load", ctypes.c_int64),
                 ("min_cta_load", ctypes.c_int64), ("balance", ctypes.c_double)]
+
+
+class StepTables(ctypes.Structure):
+    """xy_step_tables: where xy_build_step_tables put each table in the staging buffer."""
+    _fields_ = [("err_off", ctypes.c_size_t), ("cu_off", ctypes.c_size_t), ("ctx_off", ctypes.c_size_t),
+                ("bt_off", ctypes.c_size_t), ("tasks_off", ctypes.c_size_t), ("merges_off", ctypes.c_size_t),
+                ("bytes", ctypes.c_size_t), ("workspace_bytes", ctypes.c_size_t), ("num_tasks", ctypes.c_int),
+                ("num_merges", ctypes.c_int), ("pages_used", ctypes.c_int), ("stats", TaskStats)]
 
 
 _lib = None
@@ -95,6 +103,8 @@ def lib():
     L.xy_paged_attention_fp8.argtypes = [P, P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ,
                                          P, P, P]
     L.xy_paged_attention_fp8.restype = I
+    L.xy_build_step_tables.argtypes = [P, P, I, P, I, I, I, I, I, I, I, I, I, I, I, P, SZ, P]
+    L.xy_build_step_tables.restype = I
     _lib = L
     return L
 
@@ -141,12 +151,18 @@ def xy_default_num_ctas(device=0):
     return n
 
 
-def xy_build_block_table(context_lens, block_size, free_list, max_blocks):
-    """a1 (host): block table [S, max_blocks] int32 from the FIFO free list; returns (table, pages_used)."""
+def xy_build_block_table(context_lens, block_size, free_list, max_blocks, out=None):
+    """a1 (host): block table [S, max_blocks] int32 from the FIFO free list; returns (table, pages_used).
+    out: optional C-contiguous int32 array [S, max_blocks] to write the table into."""
     ctx, pctx = _host_i32(context_lens)
     free, pfree = _host_i32(free_list)
     S = len(ctx)
-    table = np.empty((S, int(max_blocks)), dtype=np.int32)
+    if out is None:
+        table = np.empty((S, int(max_blocks)), dtype=np.int32)
+    else:
+        table = out
+        if table.dtype != np.int32 or table.shape != (S, int(max_blocks)) or not table.flags.c_contiguous:
+            raise ValueError("out must be a C-contiguous int32 array [S, max_blocks]")
     used = ctypes.c_int(0)
     _check(lib().xy_build_block_table(pctx, S, int(block_size), pfree, len(free), int(max_blocks),
                                       table.ctypes.data_as(ctypes.c_void_p), ctypes.byref(used)),
@@ -160,9 +176,27 @@ XY_SCHEDULE_MIXED = 2
 XY_SCHEDULE_GREEDY = 3
 
 
+_XY_ERR_CAPACITY = -10
+
+
+def task_table_bound(cu_seqlens_q, context_lens, num_heads_kv, q_tile, kv_chunk):
+    """Upper bounds on the tasks (before hole records) and merge records of a batch: every query
+    tile counted with the chunks of its sequence's whole context."""
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    L = np.asarray(context_lens, dtype=np.int64)
+    q = cu[1:] - cu[:-1]
+    tiles = (q + q_tile - 1) // q_tile
+    chunks = np.maximum(1, (L + kv_chunk - 1) // kv_chunk)
+    return int(num_heads_kv * np.sum(tiles * chunks)), int(num_heads_kv * np.sum(tiles * (chunks > 1)))
+
+
 def xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, num_ctas,
-                        q_tile, kv_chunk, schedule=XY_SCHEDULE_AREA):
-    """a4 (host): returns dict(tasks [n,8] int32, merges [m,8] int32, workspace_bytes, stats)."""
+                        q_tile, kv_chunk, schedule=XY_SCHEDULE_AREA, tasks_out=None, merges_out=None):
+    """a4 (host): returns dict(tasks [n,8] int32, merges [m,8] int32, workspace_bytes, stats).
+
+    tasks_out / merges_out: optional C-contiguous int32 arrays [capacity, 8] to write into (the
+    returned tasks / merges are then views of their first rows).  The builder runs once when they
+    are large enough, else a second time into arrays of the reported size."""
     cu, pcu = _host_i32(cu_seqlens_q)
     ctx, pctx = _host_i32(context_lens)
     S = len(cu) - 1
@@ -170,17 +204,48 @@ def xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, h
             int(q_tile), int(kv_chunk), int(schedule))
     n, m, ws = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_size_t(0)
     L = lib()
-    _check(L.xy_build_task_table(*args, None, 0, ctypes.byref(n), None, 0, ctypes.byref(m), ctypes.byref(ws), None),
-           "xy_build_task_table")
-    tasks = np.zeros((n.value, 8), dtype=np.int32)
-    merges = np.zeros((m.value, 8), dtype=np.int32)
     st = TaskStats()
-    _check(L.xy_build_task_table(*args, tasks.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n),
-                                 merges.ctypes.data_as(ctypes.c_void_p), m.value, ctypes.byref(m),
-                                 ctypes.byref(ws), ctypes.byref(st)), "xy_build_task_table")
-    return dict(tasks=tasks, merges=merges, workspace_bytes=ws.value,
+    for arr in (tasks_out, merges_out):
+        if arr is not None and (arr.dtype != np.int32 or arr.ndim != 2 or arr.shape[1] != 8
+                                or not arr.flags.c_contiguous):
+            raise ValueError("tasks_out / merges_out must be C-contiguous int32 arrays [capacity, 8]")
+    if tasks_out is None or merges_out is None:
+        n_est, m_est = task_table_bound(cu, ctx, num_heads_kv, q_tile, kv_chunk)
+        n_est += 4 * int(num_ctas)  # room for hole records
+    tasks = tasks_out if tasks_out is not None else np.zeros((max(1, n_est), 8), np.int32)
+    merges = merges_out if merges_out is not None else np.zeros((max(1, m_est), 8), np.int32)
+    status = L.xy_build_task_table(*args, tasks.ctypes.data_as(ctypes.c_void_p), tasks.shape[0], ctypes.byref(n),
+                                   merges.ctypes.data_as(ctypes.c_void_p), merges.shape[0], ctypes.byref(m),
+                                   ctypes.byref(ws), ctypes.byref(st))
+    if status == _XY_ERR_CAPACITY:
+        # n and m hold the sizes needed
+        tasks = np.zeros((n.value, 8), dtype=np.int32)
+        merges = np.zeros((max(1, m.value), 8), dtype=np.int32)
+        status = L.xy_build_task_table(*args, tasks.ctypes.data_as(ctypes.c_void_p), n.value, ctypes.byref(n),
+                                       merges.ctypes.data_as(ctypes.c_void_p), merges.shape[0], ctypes.byref(m),
+                                       ctypes.byref(ws), ctypes.byref(st))
+    _check(status, "xy_build_task_table")
+    return dict(tasks=tasks[:n.value], merges=merges[:m.value], workspace_bytes=ws.value,
                 stats=dict(total_load=st.total_load, max_cta_load=st.max_cta_load,
                            min_cta_load=st.min_cta_load, balance=st.balance))
+
+
+def xy_build_step_tables(cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
+                         head_dim, causal, num_ctas, q_tile, kv_chunk, schedule, staging_ptr, staging_bytes):
+    """One step's block table, task table and merge records packed into the host buffer at
+    staging_ptr (see include/xy.h).  Returns (status, StepTables): status 0, or XY_ERR_CAPACITY
+    with StepTables.bytes the size needed; other errors raise."""
+    cu, pcu = _host_i32(cu_seqlens_q)
+    ctx, pctx = _host_i32(context_lens)
+    free, pfree = _host_i32(free_list)
+    out = StepTables()
+    st = lib().xy_build_step_tables(pcu, pctx, len(ctx), pfree, len(free), int(block_size), int(max_blocks),
+                                    int(num_heads_q), int(num_heads_kv), int(head_dim), int(bool(causal)),
+                                    int(num_ctas), int(q_tile), int(kv_chunk), int(schedule),
+                                    ctypes.c_void_p(staging_ptr), int(staging_bytes), ctypes.byref(out))
+    if st != _XY_ERR_CAPACITY:
+        _check(st, "xy_build_step_tables")
+    return st, out
 
 
 def xy_slot_mapping(cu_seqlens_q, context_lens, block_table, block_size, num_pages, slot_mapping, err_word,

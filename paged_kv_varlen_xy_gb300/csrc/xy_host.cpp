@@ -9,7 +9,6 @@
 #include <cstdio>
 #include <cstring>
 #include <limits>
-#include <queue>
 #include <utility>
 #include <vector>
 
@@ -75,6 +74,50 @@ struct Rec {
     xy_task t;
     int64_t load;
 };
+// Scratch of the task-table builder, kept per host thread (a batch's tables are rebuilt every
+// step; this keeps the builder free of allocations once warm).
+struct BuildScratch {
+    std::vector<Rec> recs, sorted;
+    std::vector<xy_merge> mrg;
+    std::vector<uint32_t> order, order2;
+    std::vector<uint32_t> hist;
+    std::vector<int64_t> tload;
+    std::vector<int> tree, cta_of, pos_of, count;
+};
+thread_local BuildScratch g_scratch;
+
+// order = 0 .. n-1 sorted stably by recs[i].load, largest first: LSD radix sort of the
+// complemented loads (loads are below 2^55), 11-bit digits, digits that are equal for every
+// key skipped.
+void sort_by_load_desc(const std::vector<Rec> &recs, BuildScratch &sc) {
+    const size_t n = recs.size();
+    std::vector<uint32_t> &a = sc.order, &b = sc.order2;
+    a.resize(n);
+    b.resize(n);
+    for (size_t i = 0; i < n; ++i) a[i] = (uint32_t)i;
+    const uint64_t kMask = (uint64_t(1) << 55) - 1;
+    auto key = [&](uint32_t i) { return kMask - (uint64_t)recs[i].load; };
+    uint64_t all_or = 0, all_and = ~uint64_t(0);
+    for (size_t i = 0; i < n; ++i) {
+        all_or |= key((uint32_t)i);
+        all_and &= key((uint32_t)i);
+    }
+    const uint64_t varies = all_or ^ all_and;
+    sc.hist.resize(2048);
+    for (int shift = 0; shift < 55; shift += 11) {
+        if (((varies >> shift) & 2047u) == 0) continue;
+        std::fill(sc.hist.begin(), sc.hist.end(), 0u);
+        for (size_t i = 0; i < n; ++i) ++sc.hist[(key(a[i]) >> shift) & 2047u];
+        uint32_t sum = 0;
+        for (uint32_t &h : sc.hist) {
+            const uint32_t c = h;
+            h = sum;
+            sum += c;
+        }
+        for (size_t i = 0; i < n; ++i) b[sc.hist[(key(a[i]) >> shift) & 2047u]++] = a[i];
+        a.swap(b);
+    }
+}
 }  // namespace
 
 // XY_SCHEDULE_MIXED, per CTA: the tasks at positions c, c + num_ctas, ... split into large
@@ -118,15 +161,13 @@ static void interleave_cta(const std::vector<Rec> &recs, size_t c, size_t num_ct
 
 // a4: decomposer + reorder.  Enumeration order sequence -> KV head -> query tile -> KV chunk;
 // stable sort by load, largest first; task at sorted position p belongs to CTA p % num_ctas.
-extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
-                                         int num_seqs, int num_heads_q, int num_heads_kv,
-                                         int head_dim, int causal, int num_ctas, int q_tile,
-                                         int kv_chunk, int schedule, xy_task *tasks, int max_tasks,
-                                         int *num_tasks, xy_merge *merges, int max_merges,
-                                         int *num_merges, size_t *workspace_bytes,
-                                         xy_task_stats *stats) {
+// The decomposer and deal: the dealt records in g_scratch.recs, the merge records in
+// g_scratch.mrg, the split-KV workspace rows in *ws_rows_out.
+static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context_lens, int num_seqs,
+                             int num_heads_q, int num_heads_kv, int head_dim, int causal, int num_ctas,
+                             int q_tile, int kv_chunk, int schedule, int64_t *ws_rows_out) {
     if (!cu_seqlens_q || num_seqs < 0 || num_heads_q < 1 || num_heads_kv < 1 || head_dim < 1 ||
-        num_ctas < 1 || q_tile < 1 || kv_chunk < 1 || !num_tasks || !num_merges || !workspace_bytes)
+        num_ctas < 1 || q_tile < 1 || kv_chunk < 1)
         return XY_ERR_INVALID_ARG;
     if (num_seqs > 0 && !context_lens) return XY_ERR_INVALID_ARG;
     if (num_heads_q % num_heads_kv) return XY_ERR_INVALID_ARG;
@@ -136,60 +177,94 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
     if (cu_seqlens_q[0] != 0) return XY_ERR_CU_SEQLENS;
     const int G = num_heads_q / num_heads_kv;
 
-    std::vector<Rec> recs;
-    std::vector<xy_merge> mrg;
+    BuildScratch &sc = g_scratch;
+    std::vector<Rec> &recs = sc.recs;
+    std::vector<xy_merge> &mrg = sc.mrg;
+    recs.clear();
+    mrg.clear();
+    {
+        // upper bound on the task count (a chunk count from the full context), so that the
+        // enumeration below never reallocates
+        int64_t bound = 0;
+        for (int i = 0; i < num_seqs; ++i) {
+            const int64_t qn = (int64_t)cu_seqlens_q[i + 1] - cu_seqlens_q[i];
+            const int64_t L = context_lens[i];
+            if (qn < 1 || L < qn) break;  // reported by the enumeration
+            bound += num_heads_kv * ((qn + q_tile - 1) / q_tile) * ((L + kv_chunk - 1) / kv_chunk);
+        }
+        recs.reserve((size_t)std::min<int64_t>(bound, int64_t(1) << 26));
+    }
     int64_t ws_rows = 0;
+    // per query tile of the current sequence: rows, keys it sees, chunk count (the same for every
+    // KV head, so computed once per sequence)
+    struct Tile {
+        int64_t t0, rows, kv_hi, nsplit, charged;
+    };
+    std::vector<Tile> tiles;
     for (int i = 0; i < num_seqs; ++i) {
         const int64_t qn = (int64_t)cu_seqlens_q[i + 1] - cu_seqlens_q[i];
         const int64_t L = context_lens[i];
         if (qn < 1) return XY_ERR_CU_SEQLENS;
         if (L < qn) return XY_ERR_CONTEXT_LT_QLEN;
+        tiles.clear();
+        for (int64_t t0 = 0; t0 < qn; t0 += q_tile) {
+            Tile tl;
+            tl.t0 = t0;
+            tl.rows = std::min<int64_t>(q_tile, qn - t0);
+            tl.kv_hi = causal ? (L - qn + t0 + tl.rows) : L;
+            tl.nsplit = (tl.kv_hi + kv_chunk - 1) / kv_chunk;
+            tl.charged = tl.rows * G;
+            if (schedule == XY_SCHEDULE_MIXED || schedule == XY_SCHEDULE_GREEDY)
+                tl.charged = XY_SCHEDULE_TILE_ROWS *
+                             std::max<int64_t>(1, (tl.charged + XY_SCHEDULE_TILE_ROWS - 1) / XY_SCHEDULE_TILE_ROWS);
+            tiles.push_back(tl);
+        }
         for (int g = 0; g < num_heads_kv; ++g) {
-            for (int64_t t0 = 0; t0 < qn; t0 += q_tile) {
-                const int64_t rows = std::min<int64_t>(q_tile, qn - t0);
-                const int64_t kv_hi = causal ? (L - qn + t0 + rows) : L;
-                const int64_t nsplit = (kv_hi + kv_chunk - 1) / kv_chunk;
+            for (const Tile &tl : tiles) {
                 int64_t base = -1;
-                if (nsplit > 1) {
+                if (tl.nsplit > 1) {
                     base = ws_rows;
                     xy_merge m;
                     m.seq = i;
                     m.kv_head = g;
-                    m.q_start = (int32_t)t0;
-                    m.q_rows = (int32_t)rows;
-                    m.num_splits = (int32_t)nsplit;
+                    m.q_start = (int32_t)tl.t0;
+                    m.q_rows = (int32_t)tl.rows;
+                    m.num_splits = (int32_t)tl.nsplit;
                     m.ws_row = (int32_t)base;
                     m.zero0 = 0;
                     m.zero1 = 0;
                     mrg.push_back(m);
-                    ws_rows += nsplit * rows * G;
+                    ws_rows += tl.nsplit * tl.rows * G;
                     if (ws_rows > std::numeric_limits<int32_t>::max()) return XY_ERR_UNSUPPORTED;
                 }
-                for (int64_t c = 0; c < nsplit; ++c) {
-                    const int64_t k0 = c * kv_chunk;
-                    const int64_t k1 = std::min<int64_t>(kv_hi, k0 + kv_chunk);
+                for (int64_t c = 0, k0 = 0; c < tl.nsplit; ++c, k0 += kv_chunk) {
+                    const int64_t k1 = std::min<int64_t>(tl.kv_hi, k0 + kv_chunk);
                     Rec r;
                     r.t.seq = i;
                     r.t.kv_head = g;
-                    r.t.q_start = (int32_t)t0;
-                    r.t.q_rows = (int32_t)rows;
+                    r.t.q_start = (int32_t)tl.t0;
+                    r.t.q_rows = (int32_t)tl.rows;
                     r.t.kv_start = (int32_t)k0;
                     r.t.kv_end = (int32_t)k1;
-                    r.t.num_splits = (int32_t)nsplit;
-                    r.t.ws_row = nsplit == 1 ? -1 : (int32_t)(base + c * rows * G);
-                    int64_t charged = rows * G, keys = k1 - k0;
-                    if (schedule == XY_SCHEDULE_MIXED || schedule == XY_SCHEDULE_GREEDY)
-                        charged = XY_SCHEDULE_TILE_ROWS *
-                                  std::max<int64_t>(1, (charged + XY_SCHEDULE_TILE_ROWS - 1) / XY_SCHEDULE_TILE_ROWS);
-                    if (schedule == XY_SCHEDULE_GREEDY) keys += XY_SCHEDULE_TASK_KEYS;
-                    r.load = charged * keys;
+                    r.t.num_splits = (int32_t)tl.nsplit;
+                    r.t.ws_row = tl.nsplit == 1 ? -1 : (int32_t)(base + c * tl.rows * G);
+                    const int64_t keys = (k1 - k0) + (schedule == XY_SCHEDULE_GREEDY ? XY_SCHEDULE_TASK_KEYS : 0);
+                    r.load = tl.charged * keys;
                     recs.push_back(r);
                 }
             }
         }
     }
-    std::stable_sort(recs.begin(), recs.end(),
-                     [](const Rec &a, const Rec &b) { return a.load > b.load; });
+    for (const Rec &r : recs)
+        if (r.load >= (int64_t(1) << 55)) return XY_ERR_UNSUPPORTED;
+    {
+        // stable sort by load, largest first
+        sort_by_load_desc(recs, sc);
+        std::vector<Rec> &sorted = sc.sorted;
+        sorted.resize(recs.size());
+        for (size_t k = 0; k < recs.size(); ++k) sorted[k] = recs[sc.order[k]];
+        recs.swap(sorted);
+    }
     if (schedule == XY_SCHEDULE_SERPENTINE || schedule == XY_SCHEDULE_MIXED) {
         // serpentine deal: every complete odd round of num_ctas positions is reversed
         const size_t n = (size_t)num_ctas;
@@ -213,29 +288,75 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
         for (const Rec &r : recs) total += r.load;
         if (total >= (int64_t(1) << 55)) return XY_ERR_UNSUPPORTED;
         // longest processing time first: each task (in sorted order) to the least loaded CTA,
-        // the lowest index on ties; unused positions become holes
-        using Slot = std::pair<int64_t, int>;
-        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-        for (int c = 0; c < num_ctas; ++c) heap.push({0, c});
-        std::vector<std::vector<size_t>> lists(num_ctas);
+        // the lowest index on ties; unused positions become holes.  A tournament tree over the
+        // CTAs (leaf c at W + c, W a power of two; padding leaves carry an infinite load) keeps
+        // the winner of (load, index) at the root; a task's load re-runs one leaf-to-root path.
+        const int C = num_ctas;
+        int W = 1;
+        while (W < C) W <<= 1;
+        std::vector<int64_t> &load = sc.tload;
+        std::vector<int> &tree = sc.tree, &cta_of = sc.cta_of, &pos_of = sc.pos_of, &count = sc.count;
+        load.assign(W, std::numeric_limits<int64_t>::max());
+        for (int c = 0; c < C; ++c) load[c] = 0;
+        tree.assign(2 * W, 0);
+        for (int c = 0; c < W; ++c) tree[W + c] = c;
+        auto win = [&](int a, int b) { return load[b] < load[a] ? b : a; };  // a < b: ties keep a
+        for (int i = W - 1; i >= 1; --i) tree[i] = win(tree[2 * i], tree[2 * i + 1]);
+        cta_of.resize(recs.size());
+        pos_of.resize(recs.size());
+        count.assign(C, 0);
         for (size_t k = 0; k < recs.size(); ++k) {
-            Slot s = heap.top();
-            heap.pop();
-            lists[s.second].push_back(k);
-            heap.push({s.first + recs[k].load, s.second});
+            const int c = tree[1];
+            cta_of[k] = c;
+            pos_of[k] = count[c]++;
+            load[c] += recs[k].load;
+            for (int i = (W + c) >> 1; i >= 1; i >>= 1) tree[i] = win(tree[2 * i], tree[2 * i + 1]);
         }
         size_t depth = 0;
-        for (const auto &l : lists) depth = std::max(depth, l.size());
+        for (int c = 0; c < C; ++c) depth = std::max(depth, (size_t)count[c]);
         if (depth * (size_t)num_ctas > (size_t)std::numeric_limits<int32_t>::max()) return XY_ERR_UNSUPPORTED;
         Rec hole;
         hole.t = xy_task{-1, 0, 0, 0, 0, 0, 0, -1};
         hole.load = 0;
-        std::vector<Rec> dealt(depth * (size_t)num_ctas, hole);
-        for (int c = 0; c < num_ctas; ++c)
-            for (size_t pos = 0; pos < lists[c].size(); ++pos) dealt[pos * num_ctas + c] = recs[lists[c][pos]];
+        std::vector<Rec> &dealt = sc.sorted;
+        dealt.assign(depth * (size_t)num_ctas, hole);
+        for (size_t k = 0; k < recs.size(); ++k) dealt[(size_t)pos_of[k] * num_ctas + cta_of[k]] = recs[k];
         recs.swap(dealt);
     }
 
+    *ws_rows_out = ws_rows;
+    return XY_OK;
+}
+
+static void task_stats(const std::vector<Rec> &recs, int num_ctas, xy_task_stats *stats) {
+    std::vector<int64_t> cta(num_ctas, 0);
+    int64_t total = 0;
+    for (size_t k = 0; k < recs.size(); ++k) {
+        cta[k % num_ctas] += recs[k].load;
+        total += recs[k].load;
+    }
+    const int64_t mx = *std::max_element(cta.begin(), cta.end());
+    const int64_t mn = *std::min_element(cta.begin(), cta.end());
+    stats->total_load = total;
+    stats->max_cta_load = mx;
+    stats->min_cta_load = mn;
+    stats->balance = mx > 0 ? (double)mn / (double)mx : 1.0;
+}
+
+extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                         int num_seqs, int num_heads_q, int num_heads_kv,
+                                         int head_dim, int causal, int num_ctas, int q_tile,
+                                         int kv_chunk, int schedule, xy_task *tasks, int max_tasks,
+                                         int *num_tasks, xy_merge *merges, int max_merges,
+                                         int *num_merges, size_t *workspace_bytes,
+                                         xy_task_stats *stats) {
+    if (!num_tasks || !num_merges || !workspace_bytes) return XY_ERR_INVALID_ARG;
+    int64_t ws_rows = 0;
+    const xy_status st = build_tasks(cu_seqlens_q, context_lens, num_seqs, num_heads_q, num_heads_kv, head_dim,
+                                     causal, num_ctas, q_tile, kv_chunk, schedule, &ws_rows);
+    if (st != XY_OK) return st;
+    const std::vector<Rec> &recs = g_scratch.recs;
+    const std::vector<xy_merge> &mrg = g_scratch.mrg;
     *num_tasks = (int)recs.size();
     *num_merges = (int)mrg.size();
     *workspace_bytes = (size_t)ws_rows * (size_t)(head_dim + 1) * 4u;
@@ -247,19 +368,49 @@ extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int3
         if (max_merges < (int)mrg.size()) return XY_ERR_CAPACITY;
         if (!mrg.empty()) std::memcpy(merges, mrg.data(), mrg.size() * sizeof(xy_merge));
     }
-    if (stats) {
-        std::vector<int64_t> cta(num_ctas, 0);
-        int64_t total = 0;
-        for (size_t k = 0; k < recs.size(); ++k) {
-            cta[k % num_ctas] += recs[k].load;
-            total += recs[k].load;
-        }
-        const int64_t mx = *std::max_element(cta.begin(), cta.end());
-        const int64_t mn = *std::min_element(cta.begin(), cta.end());
-        stats->total_load = total;
-        stats->max_cta_load = mx;
-        stats->min_cta_load = mn;
-        stats->balance = mx > 0 ? (double)mn / (double)mx : 1.0;
-    }
+    if (stats) task_stats(recs, num_ctas, stats);
+    return XY_OK;
+}
+
+// One step's host-built metadata packed for a single host->device copy (see xy.h).
+extern "C" xy_status xy_build_step_tables(const int32_t *cu_seqlens_q, const int32_t *context_lens, int num_seqs,
+                                          const int32_t *free_list, int num_free, int block_size, int max_blocks,
+                                          int num_heads_q, int num_heads_kv, int head_dim, int causal, int num_ctas,
+                                          int q_tile, int kv_chunk, int schedule, void *staging,
+                                          size_t staging_bytes, xy_step_tables *out) {
+    if (!out || (staging_bytes > 0 && !staging) || max_blocks < 1) return XY_ERR_INVALID_ARG;
+    int64_t ws_rows = 0;
+    xy_status st = build_tasks(cu_seqlens_q, context_lens, num_seqs, num_heads_q, num_heads_kv, head_dim, causal,
+                               num_ctas, q_tile, kv_chunk, schedule, &ws_rows);
+    if (st != XY_OK) return st;
+    const std::vector<Rec> &recs = g_scratch.recs;
+    const std::vector<xy_merge> &mrg = g_scratch.mrg;
+    const size_t A = XY_STEP_TABLES_ALIGN;
+    auto up = [&](size_t x) { return (x + A - 1) / A * A; };
+    const size_t S = (size_t)num_seqs;
+    out->err_off = 0;
+    out->cu_off = up(4);
+    out->ctx_off = up(out->cu_off + 4 * (S + 1));
+    out->bt_off = up(out->ctx_off + 4 * S);
+    out->tasks_off = up(out->bt_off + 4 * S * (size_t)max_blocks);
+    out->merges_off = up(out->tasks_off + sizeof(xy_task) * recs.size());
+    out->bytes = out->merges_off + sizeof(xy_merge) * mrg.size();
+    out->num_tasks = (int)recs.size();
+    out->num_merges = (int)mrg.size();
+    out->workspace_bytes = (size_t)ws_rows * (size_t)(head_dim + 1) * 4u;
+    task_stats(recs, num_ctas, &out->stats);
+    out->pages_used = 0;
+    if (out->bytes > staging_bytes) return XY_ERR_CAPACITY;
+    uint8_t *base = static_cast<uint8_t *>(staging);
+    st = xy_build_block_table(context_lens, num_seqs, block_size, free_list, num_free, max_blocks,
+                              reinterpret_cast<int32_t *>(base + out->bt_off), &out->pages_used);
+    if (st != XY_OK) return st;
+    const int32_t zero = 0;
+    std::memcpy(base + out->err_off, &zero, 4);
+    std::memcpy(base + out->cu_off, cu_seqlens_q, 4 * (S + 1));
+    if (S) std::memcpy(base + out->ctx_off, context_lens, 4 * S);
+    xy_task *t = reinterpret_cast<xy_task *>(base + out->tasks_off);
+    for (size_t k = 0; k < recs.size(); ++k) t[k] = recs[k].t;
+    if (!mrg.empty()) std::memcpy(base + out->merges_off, mrg.data(), sizeof(xy_merge) * mrg.size());
     return XY_OK;
 }

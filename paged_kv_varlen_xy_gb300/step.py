@@ -4,8 +4,8 @@ KV append and paged attention (device).  Composition of libxy calls only; no ari
 import numpy as np
 import torch
 
-from . import (Plan, check_err_word, xy_build_block_table, xy_kv_append, xy_kv_append_fp8, xy_paged_attention,
-               xy_paged_attention_fp8, xy_slot_mapping)
+from . import (Plan, check_err_word, default_tiles, xy_build_block_table, xy_build_step_tables, xy_default_num_ctas,
+               xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_fp8, xy_slot_mapping)
 
 
 class PagedBatch:
@@ -28,6 +28,196 @@ class PagedBatch:
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
         self.block_size = block_size
         self.causal = causal
+
+
+class _PlanView:
+    """The attention plan of a Planner batch (the fields run_step reads from Plan)."""
+
+    def __init__(self, batch, num_ctas, workspace, tbl, host_np):
+        self._b, self.num_ctas, self.workspace, self._tbl, self._h = batch, num_ctas, workspace, tbl, host_np
+
+    @property
+    def stats(self):
+        st = self._tbl.stats
+        return dict(total_load=st.total_load, max_cta_load=st.max_cta_load, min_cta_load=st.min_cta_load,
+                    balance=st.balance)
+
+    @property
+    def host(self):
+        t, h, n, m = self._tbl, self._h, self._b.num_tasks, self._b.num_merges
+        return dict(tasks=h[t.tasks_off:t.tasks_off + 32 * n].view(np.int32).reshape(n, 8),
+                    merges=h[t.merges_off:t.merges_off + 32 * m].view(np.int32).reshape(m, 8),
+                    workspace_bytes=t.workspace_bytes, stats=self.stats)
+
+    @property
+    def tasks(self):
+        return self._b._view("tasks", (self._b.num_tasks, 8))
+
+    @property
+    def merges(self):
+        return self._b._view("merges", (self._b.num_merges, 8))
+
+
+class _StepBatch:
+    """A Planner batch: the attributes of PagedBatch.  Its device tables live in the planner's
+    device buffer (valid until the planner's next plan()); tensor views of them are made on
+    demand, while Planner.run passes their addresses straight to libxy."""
+
+    def __init__(self, dbuf, off, S, MB, n, m):
+        self._dbuf, self._off, self.S, self.MB, self.num_tasks, self.num_merges = dbuf, off, S, MB, n, m
+        self._base = dbuf.data_ptr()
+
+    def addr(self, name):
+        return self._base + self._off[name]
+
+    def _view(self, name, shape):
+        n_el = int(np.prod(shape))
+        o = self._off[name]
+        return self._dbuf[o:o + 4 * n_el].view(torch.int32).view(*shape)
+
+    cu = property(lambda self: self._view("cu", (self.S + 1,)))
+    ctx = property(lambda self: self._view("ctx", (self.S,)))
+    block_table = property(lambda self: self._view("bt", (self.S, self.MB)))
+    err = property(lambda self: self._view("err", (1,)))
+
+    def _hv(self, name, n):
+        o = self._off[name]
+        return self._host_np[o:o + 4 * n].view(np.int32)
+
+    # host views of the staged tables (valid until the planner's next plan())
+    cu_host = property(lambda self: self._hv("cu", self.S + 1))
+    ctx_host = property(lambda self: self._hv("ctx", self.S))
+    block_table_host = property(lambda self: self._hv("bt", self.S * self.MB).reshape(self.S, self.MB))
+
+
+class Planner:
+    """Reusable builder of per-step metadata for one stream: the host-built block table, task and
+    merge tables, cu_seqlens_q, context_lens and a zeroed error word are packed into one pinned
+    staging buffer and reach the device in one host->device copy; the device buffer, split-KV
+    workspace and slot-mapping buffer are kept between steps and grown when a batch needs more.
+    A serving loop that re-plans every step calls plan() then run() once per step (PagedBatch
+    instead builds and uploads each table separately).  The batch returned by plan() stays valid
+    until the next plan() call; use one Planner per stream."""
+
+    _ALIGN = 256
+
+    def __init__(self, num_heads_q, num_heads_kv, head_dim, block_size, max_blocks, causal, device="cuda",
+                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=3, kv_fp8=False):
+        self.dev = torch.device(device)
+        self.Hq, self.Hkv, self.d = num_heads_q, num_heads_kv, head_dim
+        self.block_size, self.max_blocks, self.causal, self.kv_fp8 = block_size, max_blocks, causal, kv_fp8
+        self.num_ctas = num_ctas or xy_default_num_ctas(self.dev.index or 0)
+        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
+        self.q_tile, self.kv_chunk, self.schedule = q_tile or dq, kv_chunk or dk, schedule
+        self._host = None
+        self._dev_buf = None
+        self._ws = torch.empty(16, dtype=torch.uint8, device=self.dev)
+        self._slots = torch.empty(1, dtype=torch.int64, device=self.dev)
+        self._slot_views = {}
+        self._copied = torch.cuda.Event()   # recorded after each upload
+        self._pending = False
+        self.last_upload_bytes = 0
+
+    def _ensure(self, nbytes):
+        """Staging and device buffers of at least nbytes (the staging buffer's contents are lost
+        when it grows)."""
+        if self._host is None or self._host.numel() < nbytes:
+            size = max(nbytes, 2 * (self._host.numel() if self._host is not None else 0), 1 << 16)
+            self._wait_upload()
+            self._host = torch.empty(size, dtype=torch.uint8).pin_memory()
+            self._host_np = self._host.numpy()
+            self._host_ptr = self._host.data_ptr()
+            self._dev_buf = torch.empty(size, dtype=torch.uint8, device=self.dev)
+
+    def _wait_upload(self):
+        if self._pending:
+            self._copied.synchronize()   # the previous upload has left the staging buffer
+            self._pending = False
+
+    def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
+        """Build and upload the metadata of one batch; returns a batch for run() (or run_step)."""
+        self._ensure(1 << 16)
+        self._wait_upload()   # the staging buffer is written below
+        for _ in range(2):
+            st, tbl = xy_build_step_tables(cu_seqlens_q, context_lens, free_list, self.block_size, self.max_blocks,
+                                           self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, self.q_tile,
+                                           self.kv_chunk, self.schedule, self._host_ptr, self._host.numel())
+            if st == 0:
+                break
+            self._ensure(tbl.bytes)   # too small: grow and build again
+        used_bytes = tbl.bytes
+        stm = torch.cuda.current_stream(self.dev) if stream is None else stream
+        if stream is None:
+            self._dev_buf[:used_bytes].copy_(self._host[:used_bytes], non_blocking=True)
+        else:
+            with torch.cuda.stream(stm):
+                self._dev_buf[:used_bytes].copy_(self._host[:used_bytes], non_blocking=True)
+        self._copied.record(stm)
+        self._pending = True
+        self.last_upload_bytes = used_bytes
+        ws = tbl.workspace_bytes
+        if self._ws.numel() < ws:
+            self._ws = torch.empty(max(ws, 2 * self._ws.numel()), dtype=torch.uint8, device=self.dev)
+        S = len(context_lens)
+        T = int(cu_seqlens_q[-1])
+        if self._slots.numel() < T:
+            self._slots = torch.empty(max(T, 2 * self._slots.numel()), dtype=torch.int64, device=self.dev)
+            self._slot_views = {}
+        slots = self._slot_views.get(T)
+        if slots is None:
+            slots = self._slot_views[T] = self._slots[:T]
+        off = {"err": tbl.err_off, "cu": tbl.cu_off, "ctx": tbl.ctx_off, "bt": tbl.bt_off, "tasks": tbl.tasks_off,
+               "merges": tbl.merges_off}
+        b = _StepBatch(self._dev_buf, off, S, self.max_blocks, tbl.num_tasks, tbl.num_merges)
+        b._host_np = self._host_np
+        b.T = T
+        b.pages_used = tbl.pages_used
+        b.slots = slots
+        b.block_size, b.causal = self.block_size, self.causal
+        b.ws_bytes = ws
+        b.plan = _PlanView(b, self.num_ctas, self._ws, tbl, self._host_np)
+        return b
+
+    def run(self, batch, q, k_new, v_new, k_pages, v_pages, scale, out=None, stream=None, k_scales=None,
+            v_scales=None):
+        """One step on a batch from plan(): slot mapping -> KV append -> paged attention (-> split-KV
+        combine), the same libxy calls as run_step / run_step_fp8 with the batch's tables passed by
+        address.  8-bit pages (kv_fp8 planners) take k_scales / v_scales.  Returns out."""
+        import ctypes
+        from . import _check, _dev, _stream, lib
+        L = lib()
+        out = torch.empty_like(q) if out is None else out
+        T, Hq, d = q.shape
+        P, Hkv, bs, _ = k_pages.shape
+        if T != batch.T or Hq != self.Hq or Hkv != self.Hkv or d != self.d or bs != self.block_size:
+            raise ValueError("tensor shapes differ from the planner's batch")
+        st = _stream(stream)
+        cu, ctx, bt, err = (ctypes.c_void_p(batch.addr(k)) for k in ("cu", "ctx", "bt", "err"))
+        slots = _dev(batch.slots, torch.int64, "slots")
+        _check(L.xy_slot_mapping(cu, ctx, bt, batch.S, batch.MB, T, bs, P, slots, err, st), "xy_slot_mapping")
+        tasks, merges = ctypes.c_void_p(batch.addr("tasks")), ctypes.c_void_p(batch.addr("merges"))
+        ws = ctypes.c_void_p(self._ws.data_ptr())
+        common = (batch.S, T, Hq, Hkv, d, bs, float(scale), int(bool(self.causal)), tasks, batch.num_tasks,
+                  merges if batch.num_merges else None, batch.num_merges, self.num_ctas, ws, self._ws.numel(), err)
+        bf = torch.bfloat16
+        if self.kv_fp8:
+            u8, f32 = torch.uint8, torch.float32
+            _check(L.xy_kv_append_fp8(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), slots, T,
+                                      _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
+                                      _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv, bs,
+                                      d, err, st), "xy_kv_append_fp8")
+            _check(L.xy_paged_attention_fp8(_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, u8, "k_pages"),
+                                            _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"),
+                                            _dev(v_scales, f32, "v_scales"), P, *common, _dev(out, bf, "out"), st),
+                   "xy_paged_attention_fp8")
+        else:
+            _check(L.xy_kv_append(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), slots, T,
+                                  _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P, Hkv, bs, d, err, st),
+                   "xy_kv_append")
+            _check(L.xy_paged_attention(_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, bf, "k_pages"),
+                                        _dev(v_pages, bf, "v_pages"), P, *common, _dev(out, bf, "out"), st),
+                   "xy_paged_attention")
+        return out
 
 
 def run_step(batch, q, k_new, v_new, k_pages, v_pages, scale, out=None, stream=None):

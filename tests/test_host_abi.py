@@ -143,3 +143,47 @@ def test_task_table_errors(xy):
 def test_task_table_empty_batch(xy):
     r = xy.xy_build_task_table([0], [], 4, 2, 64, True, 8, 8, 64)
     assert r["tasks"].shape == (0, 8) and r["workspace_bytes"] == 0 and r["stats"]["balance"] == 1.0
+
+
+def test_task_table_capacity_retry_and_out_arrays():
+    # outputs written into caller arrays (one builder call), or retried when they are too small
+    import paged_kv_varlen_xy_gb300 as xy
+    cu = np.array([0, 1, 2, 40, 41], dtype=np.int32)
+    ctx = np.array([900, 50, 7000, 33], dtype=np.int32)
+    ref = xy.xy_build_task_table(cu, ctx, 16, 4, 128, 1, 9, 16, 256, 3)
+    big_t, big_m = np.zeros((4096, 8), np.int32), np.zeros((512, 8), np.int32)
+    r = xy.xy_build_task_table(cu, ctx, 16, 4, 128, 1, 9, 16, 256, 3, tasks_out=big_t, merges_out=big_m)
+    assert np.shares_memory(r["tasks"], big_t) and np.shares_memory(r["merges"], big_m)
+    small_t, small_m = np.zeros((3, 8), np.int32), np.zeros((1, 8), np.int32)
+    r2 = xy.xy_build_task_table(cu, ctx, 16, 4, 128, 1, 9, 16, 256, 3, tasks_out=small_t, merges_out=small_m)
+    for a in (r, r2):
+        assert np.array_equal(a["tasks"], ref["tasks"]) and np.array_equal(a["merges"], ref["merges"])
+        assert a["workspace_bytes"] == ref["workspace_bytes"]
+    n, m = xy.task_table_bound(cu, ctx, 4, 16, 256)
+    assert n >= int(np.sum(ref["tasks"][:, 0] >= 0)) and m >= len(ref["merges"])
+
+
+def test_step_tables_pack_both_builders_outputs():
+    import paged_kv_varlen_xy_gb300 as xy
+    cu = np.array([0, 1, 2, 40, 41], dtype=np.int32)
+    ctx = np.array([900, 50, 7000, 33], dtype=np.int32)
+    free = np.random.default_rng(0).permutation(1000).astype(np.int32)
+    args = (cu, ctx, free, 16, 448, 16, 4, 128, True, 9, 16, 256, 3)
+    small = np.zeros(64, dtype=np.uint8)
+    st, tbl = xy.xy_build_step_tables(*args, small.ctypes.data, small.nbytes)
+    assert st == -10 and tbl.bytes > small.nbytes          # XY_ERR_CAPACITY, size reported
+    buf = np.full(tbl.bytes + 100, 0xAB, dtype=np.uint8)
+    st, tbl = xy.xy_build_step_tables(*args, buf.ctypes.data, buf.nbytes)
+    assert st == 0
+    for o in (tbl.err_off, tbl.cu_off, tbl.ctx_off, tbl.bt_off, tbl.tasks_off, tbl.merges_off):
+        assert o % 256 == 0
+    i32 = lambda off, n: buf[off:off + 4 * n].view(np.int32)
+    bt, used = xy.xy_build_block_table(ctx, 16, free, 448)
+    ref = xy.xy_build_task_table(cu, ctx, 16, 4, 128, True, 9, 16, 256, 3)
+    assert i32(tbl.err_off, 1)[0] == 0
+    assert np.array_equal(i32(tbl.cu_off, 5), cu) and np.array_equal(i32(tbl.ctx_off, 4), ctx)
+    assert np.array_equal(i32(tbl.bt_off, bt.size).reshape(bt.shape), bt) and tbl.pages_used == used
+    assert np.array_equal(i32(tbl.tasks_off, 8 * tbl.num_tasks).reshape(-1, 8), ref["tasks"])
+    assert np.array_equal(i32(tbl.merges_off, 8 * tbl.num_merges).reshape(-1, 8), ref["merges"])
+    assert tbl.workspace_bytes == ref["workspace_bytes"] and tbl.stats.balance == ref["stats"]["balance"]
+    assert tbl.bytes == tbl.merges_off + 32 * tbl.num_merges
