@@ -51,12 +51,13 @@ def run_step(cu_seqlens_q, context_lens, free_list, block_size, max_blocks, q_bi
 
 
 def run_step_fp8(cu_seqlens_q, context_lens, free_list, block_size, max_blocks, q_bits, k_new_bits, v_new_bits,
-                 k_pool_bits, v_pool_bits, scale, causal, pool_pages=None):
+                 k_pool_bits, v_pool_bits, scale, causal, pool_pages=None, rows=None):
     """The step over 8-bit pages.  The pool before the step holds the bf16 rows k_pool_bits /
     v_pool_bits [n, Hkv, bs, d] (all P pages, or the pages listed in pool_pages, as in run_step)
     quantized row by row (as if each had been appended); the new tokens are appended quantized,
-    and attention runs on the dequantized pages.  Returns dict(block_table, slots, k_codes,
-    v_codes, k_scales, v_scales (the pool after the append), out)."""
+    and attention runs on the dequantized pages (all rows, or the (token, query head) pairs in
+    rows).  Returns dict(block_table, slots, k_codes, v_codes, k_scales, v_scales (the pool after
+    the append), out)."""
     bt = allocate_block_table(context_lens, block_size, free_list, max_blocks)
     slots = slot_mapping(cu_seqlens_q, context_lens, bt, block_size)
     local_bt, local_slots = _localize(bt, slots, block_size, pool_pages)
@@ -64,6 +65,9 @@ def run_step_fp8(cu_seqlens_q, context_lens, free_list, block_size, max_blocks, 
     vc, vs = quantize_rows(v_pool_bits)
     kc, vc, ks, vs = kv_append_fp8(kc, vc, ks, vs, k_new_bits, v_new_bits, local_slots)
     q = bf16_bits_to_f64(q_bits)
-    out = paged_attention(q, cu_seqlens_q, context_lens, local_bt, dequantize(kc, ks), dequantize(vc, vs), scale,
-                          causal)
+    kf, vf = dequantize(kc, ks), dequantize(vc, vs)
+    if rows is None:
+        out = paged_attention(q, cu_seqlens_q, context_lens, local_bt, kf, vf, scale, causal)
+    else:
+        out = attention_rows(rows, q, cu_seqlens_q, context_lens, local_bt, kf, vf, scale, causal)
     return dict(block_table=bt, slots=slots, k_codes=kc, v_codes=vc, k_scales=ks, v_scales=vs, out=out)

@@ -124,3 +124,49 @@ def test_fp8_split_kv_and_row_magnitudes():
     ctx = [3000, 1, 700, 5000, 257]
     wl = workloads.custom(np.ones(len(ctx)), ctx, 32, 8, 128, 16, seed=61, name="fp8_split")
     _assert_fp8_parity(_run_fp8(wl, kv_chunk=256, row_scale=[2.0 ** -12, 1.0, 2.0 ** 4]), per_row_scale=True)
+
+
+@pytest.mark.parametrize("name", ["decode", "skew"])
+def test_fp8_full_size_sampled_rows(name):
+    # the full decode / skew batches over 8-bit pages in the bench's launch configuration; the oracle
+    # checks sampled sequences (all their rows), pages and codes of those sequences bit for bit
+    import paged_kv_varlen_xy_gb300 as xy
+    from paged_kv_varlen_xy_gb300 import build
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    from gpu_cases import MAX_ABS, MEAN_ABS
+    build.build()
+    wl = workloads.make(name)
+    vals = wl.tensors("cuda")
+    P, Hkv, bs, d = vals["k_pool"].shape
+    codes = [torch.empty(P, Hkv, bs, d, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    scl = [torch.empty(P, Hkv, bs, dtype=torch.float32, device="cuda") for _ in range(2)]
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, kv_fp8=True)
+    rows = [vals[n].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous() for n in ("k_pool", "v_pool")]
+    xy.xy_kv_append_fp8(rows[0], rows[1], torch.arange(P * bs, dtype=torch.int64, device="cuda"), codes[0], codes[1],
+                        scl[0], scl[1], batch.err)
+    del rows
+    out = xystep.run_step_fp8(batch, vals["q"], vals["k_new"], vals["v_new"], codes[0], codes[1], scl[0], scl[1],
+                              wl.scale)
+    torch.cuda.synchronize()
+    xystep.check(batch)
+    # sampled sequences: short ones only for skew (a 131072-key sequence is too large for the oracle)
+    rng = np.random.default_rng(7)
+    ok_seqs = [i for i in range(wl.num_seqs) if wl.context_lens[i] <= 8192]
+    sample = sorted(rng.choice(ok_seqs, size=min(6, len(ok_seqs)), replace=False).tolist())
+    bt = batch.block_table_host
+    pages = np.unique(np.concatenate([bt[i][bt[i] >= 0] for i in sample]))
+    idx = torch.from_numpy(pages).long().cuda()
+    cu = wl.cu_seqlens_q
+    rows = [(t, h) for i in sample for t in range(int(cu[i]), int(cu[i + 1])) for h in range(wl.num_heads_q)]
+    ref = oracle.step.run_step_fp8(cu, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                   _bits(vals["q"]), _bits(vals["k_new"]), _bits(vals["v_new"]),
+                                   _bits(vals["k_pool"].index_select(0, idx)), _bits(vals["v_pool"].index_select(0, idx)),
+                                   wl.scale, wl.causal, pool_pages=pages, rows=rows)
+    assert np.array_equal(codes[0].index_select(0, idx).cpu().numpy(), ref["k_codes"])
+    assert np.array_equal(codes[1].index_select(0, idx).cpu().numpy(), ref["v_codes"])
+    assert np.array_equal(scl[1].index_select(0, idx).cpu().numpy().view(np.uint32), ref["v_scales"].view(np.uint32))
+    got = oracle.bf16_bits_to_f64(_bits(out))
+    got = np.stack([got[t, h] for (t, h) in rows])
+    diff = np.abs(got - ref["out"])
+    assert np.isfinite(got).all() and diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS, (diff.max(), diff.mean())
