@@ -302,17 +302,17 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
                 mx_b = fmaxf(mx_b, fmaxf(sc[b][j][2], sc[b][j][3]));
             }
         }
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
-        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
-        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
-        vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
         // The reference max m is raised only when a row's max exceeds it by more than 8 (weights
-        // then stay <= 2^8, fine in f16 and fp32); the stale reference cancels in O / l.
+        // then stay <= 2^8, fine in f16 and fp32); the stale reference cancels in O / l.  Each
+        // lane tests its own scores, so the row maxima (quad shuffles) are formed only when some
+        // reference has to grow -- in a task's first step and rarely after it.
         float al_a = 1.f, al_b = 1.f;
-        const bool grow_a = mx_a > m_a + 8.f, grow_b = mx_b > m_b + 8.f;
-        if (__any_sync(0xffffffffu, grow_a || grow_b)) {
+        if (__any_sync(0xffffffffu, mx_a > m_a + 8.f || mx_b > m_b + 8.f)) {
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+            mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+            mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+            const bool grow_a = mx_a > m_a + 8.f, grow_b = mx_b > m_b + 8.f;  // the same in a row's quad
             const float mn_a = grow_a ? mx_a : m_a, mn_b = grow_b ? mx_b : m_b;
             al_a = ex2(m_a - (mn_a == -INFINITY ? 0.f : mn_a));
             al_b = ex2(m_b - (mn_b == -INFINITY ? 0.f : mn_b));
@@ -337,7 +337,11 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
         l_a = l_a * al_a + ps_a;
         l_b = l_b * al_b + ps_b;
         bool rescale = al_a != 1.f || al_b != 1.f;
-        if (vmax > s_max) {  // the same in every quad: warp-uniform
+        if (__any_sync(0xffffffffu, vmax > s_max)) {
+            // a larger V scale: the step's largest (every quad holds the same keys, so the quad
+            // maximum is the same in every quad and the branch below is warp-uniform)
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 1));
+            vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, 2));
             const float g = s_max / vmax;
             al_a *= g;
             al_b *= g;
