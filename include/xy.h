@@ -306,10 +306,10 @@ xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *
  * merges, workspace, err_word and every other argument as for xy_paged_attention; k_pages/v_pages
  * uint8 [num_pages, Hkv, bs, 128] and k_scales/v_scales fp32 [num_pages, Hkv, bs] (device,
  * 16-byte aligned), written by xy_kv_append_fp8.  The query rows are rounded to f16 on chip
- * (exact for bf16 values of magnitude 2^-14 .. 65504).  Every task runs on the decode path: rows
- * per task (q_rows * G) are at most XY_FP8_NARROW_ROWS when G <= XY_FP8_NARROW_ROWS (build the
- * task table with q_tile <= 16 / G; the kernel then keeps 8 stages of K/V in flight), else at
- * most 64 (q_tile <= 64 / G).  Tasks outside these limits set XY_DEV_BAD_TASK.
+ * (exact for bf16 values of magnitude 2^-14 .. 65504).  Every task runs on the decode path: in a
+ * pure decode batch (num_tokens == num_seqs) with G <= XY_FP8_NARROW_ROWS a task has at most
+ * XY_FP8_NARROW_ROWS rows (q_rows = 1), otherwise at most 64 rows (q_tile <= 64 / G).  Tasks
+ * outside these limits set XY_DEV_BAD_TASK.
  * Errors: as xy_paged_attention; XY_ERR_UNSUPPORTED for head_dim other than 128 or G > 64. */
 #define XY_FP8_NARROW_ROWS 16
 xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,

@@ -384,17 +384,18 @@ def check_err_word(err_word):
         raise XYDeviceError(bits)
 
 
-def default_tiles(num_heads_q, num_heads_kv, head_dim=128, kv_fp8=False):
+def default_tiles(num_heads_q, num_heads_kv, head_dim=128, kv_fp8=False, pure_decode=False):
     """Tile policy of the kernels.  With head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
     256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise up to 64 rows
-    (q_tile = 64 // G).  Over 8-bit pages every task runs on the decode path with at most 16 rows
-    when G <= 16 (q_tile = 16 // G, so the kernel can keep 8 stages in flight), else 64.  KV chunks are 8192 keys, a multiple of every
+    (q_tile = 64 // G).  Over 8-bit pages every task runs on the decode path: one token per task in
+    pure decode batches (pure_decode: one new token per sequence) with G <= 16, else up to 64 rows.
+    KV chunks are 8192 keys, a multiple of every
     page size and of both kernels' KV tiles: long enough that split partials and merges stay few,
     short enough that a few long contexts still spread over the SMs (measured on the mixed and
     long-context batches)."""
     G = num_heads_q // num_heads_kv
     if kv_fp8:
-        return (max(1, XY_FP8_NARROW_ROWS // G) if G <= XY_FP8_NARROW_ROWS else max(1, 64 // G)), 8192
+        return (1 if pure_decode and G <= XY_FP8_NARROW_ROWS else max(1, 64 // G)), 8192
     if head_dim == 128 and 128 % G == 0:
         return 256 // G, 8192
     return max(1, 64 // G), 8192
@@ -409,7 +410,9 @@ class Plan:
         import torch
         dev = torch.device(device)
         self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)
-        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
+        cu = np.asarray(cu_seqlens_q)
+        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8,
+                               pure_decode=len(cu) > 1 and int(cu[-1]) == len(cu) - 1)
         self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
         self.schedule = schedule
         r = xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,

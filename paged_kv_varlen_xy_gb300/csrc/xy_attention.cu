@@ -46,8 +46,9 @@ using xy::dec::kMathWarps;
 // task when the tcgen05 tile kernel cannot (head_dim 64, or G not dividing 128), pure decode
 // batches, and every batch over 8-bit pages; tasks then have at most 64 rows.
 //
-// Page formats (KIND): kBf16; kFp8Narrow, 8-bit pages with tasks of at most 16 rows (G <= 16);
-// kFp8Wide, 8-bit pages with up to 64 rows per task (G > 16).  8-bit stages hold 128 keys (about
+// Page formats (KIND): kBf16; kFp8Narrow, 8-bit pages in pure decode batches with G <= 16 (tasks
+// of at most 16 rows); kFp8Wide, 8-bit pages otherwise (up to 64 rows per task, so that a
+// prefill or chunk task shares each K/V stage among 64 rows).  8-bit stages hold 128 keys (about
 // the bytes of a 64-key bf16 stage); with 16-token pages that is 32 copies per stage (codes and
 // scales of 8 pages), so four producer warps, one per ring slot, keep the ring ahead.
 enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2 };
@@ -451,8 +452,9 @@ extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seq
         return XY_ERR_CUDA;
     // every task runs on the decode path (f16 MMAs on converted codes)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return p.G <= XY_FP8_NARROW_ROWS ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
-                                     : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
+    const bool narrow = num_tokens == num_seqs && p.G <= XY_FP8_NARROW_ROWS;
+    return narrow ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
+                  : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -107,8 +107,10 @@ class Planner:
         self.Hq, self.Hkv, self.d = num_heads_q, num_heads_kv, head_dim
         self.block_size, self.max_blocks, self.causal, self.kv_fp8 = block_size, max_blocks, causal, kv_fp8
         self.num_ctas = num_ctas or xy_default_num_ctas(self.dev.index or 0)
-        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
-        self.q_tile, self.kv_chunk, self.schedule = q_tile or dq, kv_chunk or dk, schedule
+        # q_tile per batch over 8-bit pages (it depends on whether the batch is pure decode)
+        self._q_tile_arg = q_tile
+        self.kv_chunk = kv_chunk or default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)[1]
+        self.q_tile, self.schedule = q_tile or default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)[0], schedule
         self._host = None
         self._dev_buf = None
         self._ws = torch.empty(16, dtype=torch.uint8, device=self.dev)
@@ -138,6 +140,9 @@ class Planner:
         """Build and upload the metadata of one batch; returns a batch for run() (or run_step)."""
         self._ensure(1 << 16)
         self._wait_upload()   # the staging buffer is written below
+        if self.kv_fp8 and self._q_tile_arg is None:
+            T = int(cu_seqlens_q[-1])
+            self.q_tile = default_tiles(self.Hq, self.Hkv, self.d, True, pure_decode=T == len(context_lens))[0]
         for _ in range(2):
             st, tbl = xy_build_step_tables(cu_seqlens_q, context_lens, free_list, self.block_size, self.max_blocks,
                                            self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, self.q_tile,

@@ -110,8 +110,8 @@ def test_fp8_decode_matches_oracle(G, bs):
 
 @pytest.mark.parametrize("G", [1, 4, 8, 32])
 def test_fp8_mixed_batch_matches_oracle(G):
-    # prefill, chunked-prefill and verify-shaped queries (causal); G <= 16 runs tasks of up to 16
-    # rows on the 8-stage ring, G = 32 tasks of 64 rows (four row groups) on the 4-stage ring
+    # prefill, chunked-prefill and verify-shaped queries (causal): tasks of up to 64 rows (up to
+    # four 16-row groups) on the ring for batches that are not pure decode
     q_lens = [37, 1, 5, 100, 1, 16, 3]
     ctx = [37, 900, 64, 612, 129, 16, 2050]
     wl = workloads.custom(q_lens, ctx, 2 * G, 2, 128, 16, seed=50 + G, name="fp8_mixed")
