@@ -287,9 +287,23 @@ def main():
     vals = wl.tensors(dev)
     fp8 = args.kv == "fp8"
     w = work(wl, args.kv)
-    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
-                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, kv_fp8=fp8)
-    pl = batch.plan
+    # over 8-bit pages a batch with prefill / chunk sequences runs them on the tile path over bf16
+    # copies of their pages and its decode sequences on the 8-bit decode path (when the two kinds
+    # form contiguous sequence ranges and the tile shape allows)
+    G = wl.num_heads_q // wl.num_heads_kv
+    split = (fp8 and wl.num_tokens != wl.num_seqs and wl.head_dim == 128 and 128 % G == 0
+             and xystep.split_ranges(wl.q_lens) is not None)
+    if split:
+        batch = xystep.Fp8SplitBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                     wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
+        parts = [x["plan"] for x in (batch.tile, batch.decode) if x is not None]
+    else:
+        batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                  wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, kv_fp8=fp8)
+        parts = [batch.plan]
+    pl = parts[0]
+    n_tasks = sum(int(x.tasks.shape[0]) for x in parts)
+    n_merges = sum(int(x.merges.shape[0]) for x in parts)
     stream = torch.cuda.current_stream(dev)
     out = torch.empty_like(vals["q"])
     P = wl.num_pages
@@ -314,7 +328,10 @@ def main():
             xy.xy_kv_append(vals["k_new"], vals["v_new"], batch.slots, vals["k_pool"], vals["v_pool"], batch.err)
         if ev:
             ev[0].record(stream)
-        if fp8:
+        if split:
+            xystep.attention_fp8_split(batch, vals["q"], vals["k_codes"], vals["v_codes"], vals["k_scales"],
+                                       vals["v_scales"], wl.scale, out)
+        elif fp8:
             xy.xy_paged_attention_fp8(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_codes"],
                                       vals["v_codes"], vals["k_scales"], vals["v_scales"], wl.scale, wl.causal,
                                       pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
@@ -330,7 +347,7 @@ def main():
     xystep.check(batch)
 
     # ---- device-timed region: K steps, inputs resident in HBM ----
-    n_launch_per_step = 3 + (1 if pl.merges.shape[0] else 0)
+    n_launch_per_step = 2 + sum(1 + (1 if x.merges.shape[0] else 0) for x in parts) + (1 if split and batch.tile else 0)
     attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -353,7 +370,7 @@ def main():
     value = job_throughput(args.config, w, ms_per_step / 1e3, world)
     unit, bound = unit_of(args.config)
     traffic_key = args.config + ("_fp8" if fp8 else "")
-    kname = attention_kernel(wl, args.kv)
+    kname = attention_kernel(wl, args.kv) if not split else "dequant_pages_kernel + meta_attention_kernel + paged_attention_kernel<fp8>"
     attn_s = attn_ms / 1e3
     if bound == "hbm":
         achieved = w["attn_bytes"] / attn_s / 1e9
@@ -372,7 +389,8 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["tc"], "unit": "TFLOP/s",
                 "frac": achieved / pk["tc"], "traffic": measured_traffic(traffic_key), "kernel": kname,
                 "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
-    roof["timed"] = "attention call (kernel" + (" + combine" if pl.merges.shape[0] else "") + "), CUDA events"
+    roof["timed"] = ("attention call (kernel" + (" + combine" if n_merges else "") + "), CUDA events" if not split else
+                     "page dequantization + tile attention + 8-bit decode attention (+ combines), CUDA events")
 
     # ---- end to end through the public API: pinned host inputs in, output out, every step ----
     host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
@@ -389,11 +407,18 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        b2 = planner.plan(meta["cu"], meta["ctx"], meta["free"])
+        if split:
+            b2 = xystep.Fp8SplitBatch(meta["cu"], meta["ctx"], meta["free"], wl.block_size, wl.max_blocks,
+                                      wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
+        else:
+            b2 = planner.plan(meta["cu"], meta["ctx"], meta["free"])
         qd = host["q"].to(dev, non_blocking=True)
         kd = host["k_new"].to(dev, non_blocking=True)
         vd = host["v_new"].to(dev, non_blocking=True)
-        if fp8:
+        if split:
+            o = xystep.run_step_fp8_split(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], vals["k_scales"],
+                                          vals["v_scales"], wl.scale)
+        elif fp8:
             o = planner.run(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], wl.scale, k_scales=vals["k_scales"],
                             v_scales=vals["v_scales"])
         else:
@@ -402,7 +427,8 @@ def main():
         torch.cuda.synchronize()
         e2e_times.append(time.perf_counter() - t0)
         if k == 0:
-            h2d = sum(host[x].numel() * 2 for x in host) + planner.last_upload_bytes
+            h2d = sum(host[x].numel() * 2 for x in host) + (planner.last_upload_bytes if not split else sum(
+                t.numel() * t.element_size() for t in (b2.cu, b2.ctx, b2.block_table)))
             d2h = out_host.numel() * 2
     e2e_s = max_over_ranks(sum(e2e_times[args.warmup:]) / args.steps, world, device=dev)
     e2e_val = job_throughput(args.config, w, e2e_s, world)
@@ -425,11 +451,11 @@ def main():
             "config": {"workload": describe(args), "parallelism": f"replicas x{world}",
                        "l2": "KV working set larger than the 129 MB L2; no flush between steps"
                              if w["kv_bytes"] > 4 * 129e6 else "L2 not flushed (small working set)",
-                       "step": "slot_mapping + kv_append + paged_attention" +
-                               (" + combine" if pl.merges.shape[0] else ""),
+                       "step": "slot_mapping + kv_append + paged_attention" + (" + combine" if n_merges else "") +
+                               (" (8-bit pages: tile part on bf16 page copies, decode part on codes)" if split else ""),
                        "tokens_per_s": wl.num_tokens * world / (ms_per_step / 1e3),
                        "tflops": w["flops"] / (ms_per_step / 1e3) / 1e12,
-                       "num_tasks": int(pl.tasks.shape[0]), "num_merges": int(pl.merges.shape[0]),
+                       "num_tasks": n_tasks, "num_merges": n_merges,
                        "num_ctas": pl.num_ctas, "balance": pl.stats["balance"]},
             "roofline": roof,
             "cpu_baseline": cpu,

@@ -300,6 +300,17 @@ xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *
                            void *k_pages, void *v_pages, float *k_scales, float *v_scales, int num_pages,
                            int num_heads_kv, int block_size, int head_dim, int32_t *err_word, void *stream);
 
+/* xy_dequant_pages_fp8: bf16 copies of listed 8-bit pages (a helper of the tensor-core path for
+ * prefill and chunk tasks over 8-bit pages, which runs on dequantized copies of the pages those
+ * sequences read).  Output page i of k_out / v_out (bf16 [num_out, Hkv, bs, d], device, 16-byte
+ * aligned) holds source page pages[i] (device int32 [num_out]): element = bf16(fp32(E4M3 value *
+ * row scale)), the product an IEEE fp32 multiply, both roundings to nearest even.  A source page
+ * outside [0, num_pages) sets XY_DEV_PAGE_OOB and its output page is left unwritten.  Asynchronous
+ * on `stream`; XY_ERR_UNSUPPORTED for d other than 64 and 128. */
+xy_status xy_dequant_pages_fp8(const void *k_codes, const void *v_codes, const float *k_scales, const float *v_scales,
+                               int num_pages, int num_heads_kv, int block_size, int head_dim, const int32_t *pages,
+                               int num_out, void *k_out, void *v_out, int32_t *err_word, void *stream);
+
 /* xy_paged_attention_fp8: xy_paged_attention over 8-bit pages.  The result is the attention of
  * xy_paged_attention over the dequantized pages (code * scale per row): K scales multiply the fp32
  * scores, V scales the softmax weights, the codes become f16 exactly on chip.  q, out, tasks,

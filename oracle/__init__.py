@@ -54,7 +54,7 @@ from .attention import (
     virtual_mask,
 )
 from .tasks import build_task_table, TASK_FIELDS, MERGE_FIELDS
-from .fp8 import e4m3_to_f64, f64_to_e4m3, quantize_rows, dequantize, kv_append_fp8
+from .fp8 import e4m3_to_f64, f64_to_e4m3, quantize_rows, dequantize, dequantize_to_bf16_bits, kv_append_fp8
 from . import step
 
 __all__ = [
@@ -75,6 +75,7 @@ __all__ = [
     "f64_to_e4m3",
     "quantize_rows",
     "dequantize",
+    "dequantize_to_bf16_bits",
     "kv_append_fp8",
     "build_task_table",
     "TASK_FIELDS",

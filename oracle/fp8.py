@@ -15,7 +15,7 @@ itself are fp32 operations, as in the CUDA path.
 
 import numpy as np
 
-from .bf16 import bf16_bits_to_f64
+from .bf16 import bf16_bits_to_f64, f64_to_bf16_bits
 
 E4M3_MAX = 448.0
 
@@ -92,3 +92,11 @@ def kv_append_fp8(k_pages, v_pages, k_scales, v_scales, k_new_bits, v_new_bits, 
         ks[page, :, off] = kscale[t]
         vs[page, :, off] = vscale[t]
     return kp, vp, ks, vs
+
+
+def dequantize_to_bf16_bits(codes, scales):
+    """bf16 bit patterns of dequantized rows as a bf16 copy holds them: the E4M3 value (exact in
+    fp32) times the row's fp32 scale as an IEEE fp32 product, rounded to bf16 (nearest even)."""
+    v = e4m3_to_f64(codes).astype(np.float32)
+    prod = v * np.asarray(scales, dtype=np.float32)[..., None]      # fp32 multiply, round to nearest
+    return f64_to_bf16_bits(prod.astype(np.float64))

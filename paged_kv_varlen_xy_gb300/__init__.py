@@ -23,7 +23,7 @@ XY_DEV_TIMEOUT = 0x8
 C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
          "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
-         "xy_paged_attention_fp8", "xy_build_step_tables")
+         "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -105,6 +105,8 @@ def lib():
     L.xy_paged_attention_fp8.restype = I
     L.xy_build_step_tables.argtypes = [P, P, I, P, I, I, I, I, I, I, I, I, I, I, I, P, SZ, P]
     L.xy_build_step_tables.restype = I
+    L.xy_dequant_pages_fp8.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P, P, P]
+    L.xy_dequant_pages_fp8.restype = I
     _lib = L
     return L
 
@@ -364,6 +366,22 @@ def xy_paged_attention_fp8(q, cu_seqlens_q, context_lens, block_table, k_pages, 
         _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
         _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
         _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention_fp8")
+
+
+def xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, pages, k_out, v_out, err_word, stream=None):
+    """bf16 copies of the listed 8-bit pages: k_out/v_out [n, Hkv, bs, d] bf16 <- pages[i] of
+    k_pages/v_pages [P, Hkv, bs, d] uint8 with k_scales/v_scales [P, Hkv, bs] fp32; pages int32 [n]."""
+    import torch
+    P, Hkv, bs, d = k_pages.shape
+    n = pages.numel()
+    if tuple(k_out.shape) != (n, Hkv, bs, d) or tuple(v_out.shape) != (n, Hkv, bs, d):
+        raise ValueError("k_out / v_out must be [len(pages), Hkv, bs, d]")
+    u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+    _check(lib().xy_dequant_pages_fp8(_dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
+                                      _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv, bs, d,
+                                      _dev(pages, torch.int32, "pages"), n, _dev(k_out, bf, "k_out"),
+                                      _dev(v_out, bf, "v_out"), _dev(err_word, torch.int32, "err_word"),
+                                      _stream(stream)), "xy_dequant_pages_fp8")
 
 
 def xy_selftest_bounded_wait(limit_us, err_word, result, stream=None):

@@ -8,6 +8,7 @@
 // rows already in a page.  The scale and the division are IEEE fp32 operations.
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -74,7 +75,77 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __nv_bfloat16 
     }
 }
 
+// Dequantized copies of listed pages: out page i = bf16(fp32(code value * scale)) of source page
+// pages[i], both tensors; one thread per 8 codes of a row (D = 64 or 128).
+template <int D>
+__global__ void __launch_bounds__(256) dequant_pages_kernel(const uint8_t *__restrict__ k_codes,
+                                                             const uint8_t *__restrict__ v_codes,
+                                                             const float *__restrict__ k_scales,
+                                                             const float *__restrict__ v_scales,
+                                                             const int32_t *__restrict__ pages, int num_out, int H,
+                                                             int bs, int num_pages, __nv_bfloat16 *__restrict__ k_out,
+                                                             __nv_bfloat16 *__restrict__ v_out, int32_t *err) {
+    constexpr int C = D / 8;  // 8-code groups per row
+    const int64_t rows_per_tensor = (int64_t)num_out * H * bs;
+    const int64_t total = 2 * rows_per_tensor * C;
+    for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+        const int tensor = (int)(g / (rows_per_tensor * C));
+        const int64_t rem = g - tensor * rows_per_tensor * C;
+        const int64_t orow = rem / C;          // (out page, head, offset) row
+        const int c = (int)(rem - orow * C);
+        const int64_t opage = orow / ((int64_t)H * bs);
+        const int64_t in_page = orow - opage * H * bs;
+        const int src = __ldg(pages + opage);
+        if (src < 0 || src >= num_pages) {
+            if (c == 0 && in_page == 0 && tensor == 0) xy::set_err(err, XY_DEV_PAGE_OOB);
+            continue;
+        }
+        const int64_t srow = (int64_t)src * H * bs + in_page;
+        const float s = __ldg((tensor ? v_scales : k_scales) + srow);
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>((tensor ? v_codes : k_codes) + srow * D) + c);
+        uint32_t h[4];
+        xy::e4m3x4_to_f16x2x2(w.x, h[0], h[1]);
+        xy::e4m3x4_to_f16x2x2(w.y, h[2], h[3]);
+        uint4 o;
+        uint32_t *ov = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 hv = *reinterpret_cast<const __half2 *>(&h[i]);
+            const float lo = __low2float(hv) * s, hi = __high2float(hv) * s;  // IEEE fp32 products
+            ov[i] = xy::pack_bf16x2(lo, hi);
+        }
+        *(reinterpret_cast<uint4 *>((tensor ? v_out : k_out) + orow * D) + c) = o;
+    }
+}
+
 }  // namespace
+
+extern "C" xy_status xy_dequant_pages_fp8(const void *k_codes, const void *v_codes, const float *k_scales,
+                                          const float *v_scales, int num_pages, int num_heads_kv, int block_size,
+                                          int head_dim, const int32_t *pages, int num_out, void *k_out, void *v_out,
+                                          int32_t *err_word, void *stream) {
+    if (num_out < 0 || num_pages < 1 || num_heads_kv < 1 || block_size < 1) return XY_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return XY_ERR_UNSUPPORTED;
+    if (num_out == 0) return XY_OK;
+    if (!k_codes || !v_codes || !k_scales || !v_scales || !pages || !k_out || !v_out || !err_word)
+        return XY_ERR_INVALID_ARG;
+    if (((uintptr_t)k_codes | (uintptr_t)v_codes | (uintptr_t)k_out | (uintptr_t)v_out) & 15) return XY_ERR_INVALID_ARG;
+    const int64_t groups = 2 * (int64_t)num_out * num_heads_kv * block_size * (head_dim / 8);
+    const int threads = 256;
+    const int blocks = (int)((groups + threads - 1) / threads < 152 * 16 ? (groups + threads - 1) / threads : 152 * 16);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (head_dim == 128)
+        dequant_pages_kernel<128><<<blocks, threads, 0, st>>>(
+            static_cast<const uint8_t *>(k_codes), static_cast<const uint8_t *>(v_codes), k_scales, v_scales, pages,
+            num_out, num_heads_kv, block_size, num_pages, static_cast<__nv_bfloat16 *>(k_out),
+            static_cast<__nv_bfloat16 *>(v_out), err_word);
+    else
+        dequant_pages_kernel<64><<<blocks, threads, 0, st>>>(
+            static_cast<const uint8_t *>(k_codes), static_cast<const uint8_t *>(v_codes), k_scales, v_scales, pages,
+            num_out, num_heads_kv, block_size, num_pages, static_cast<__nv_bfloat16 *>(k_out),
+            static_cast<__nv_bfloat16 *>(v_out), err_word);
+    return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
+}
 
 extern "C" xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping,
                                       int num_tokens, void *k_pages, void *v_pages, float *k_scales,

@@ -5,7 +5,8 @@ import numpy as np
 import torch
 
 from . import (Plan, check_err_word, default_tiles, xy_build_block_table, xy_build_step_tables, xy_default_num_ctas,
-               xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_fp8, xy_slot_mapping)
+               xy_dequant_pages_fp8, xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_fp8,
+               xy_slot_mapping)
 
 
 class PagedBatch:
@@ -247,6 +248,108 @@ def run_step_fp8(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, s
     pl = batch.plan
     xy_paged_attention_fp8(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales, v_scales, scale,
                            batch.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out, stream)
+    return out
+
+
+def split_ranges(q_lens):
+    """(multi, single): the sequence ranges [a, b) of sequences with several new tokens and of
+    one-token sequences, when each kind is one contiguous range (either may be empty); None when
+    the kinds interleave."""
+    multi = np.asarray(q_lens) > 1
+    S = len(multi)
+    changes = int(np.count_nonzero(multi[1:] != multi[:-1])) if S > 1 else 0
+    if changes > 1:
+        return None
+    k = int(np.argmax(multi[1:] != multi[:-1])) + 1 if changes else S
+    first = (0, k) if S else (0, 0)
+    second = (k, S)
+    if S and multi[0]:
+        return first, second
+    return second, first
+
+
+class Fp8SplitBatch:
+    """A batch over 8-bit pages run in two parts: its one-token (decode) sequences on the 8-bit
+    decode path, its sequences with several new tokens (prefill, chunks, verify) on the tcgen05
+    tile path over bf16 copies of the pages those sequences read (xy_dequant_pages_fp8).  The two
+    kinds must form contiguous sequence ranges (see split_ranges); the tile part needs head_dim 128
+    and G dividing 128.  The tile part computes with K and V rounded to bf16 after dequantization."""
+
+    def __init__(self, cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
+                 head_dim, causal, device="cuda", num_ctas=None):
+        dev = torch.device(device)
+        cu = np.asarray(cu_seqlens_q, dtype=np.int32)
+        ctx = np.asarray(context_lens, dtype=np.int32)
+        q_lens = cu[1:] - cu[:-1]
+        rng = split_ranges(q_lens)
+        G = num_heads_q // num_heads_kv
+        if rng is None or head_dim != 128 or 128 % G:
+            raise ValueError("batch cannot be split into a decode range and a tile range")
+        (ta, tb), (da, db) = rng
+        self.cu_host, self.ctx_host = cu, ctx
+        self.block_table_host, self.pages_used = xy_build_block_table(ctx, block_size, free_list, max_blocks)
+        self.cu = torch.from_numpy(cu).to(dev)
+        self.ctx = torch.from_numpy(ctx).to(dev)
+        self.block_table = torch.from_numpy(self.block_table_host).to(dev)
+        self.slots = torch.empty(int(cu[-1]), dtype=torch.int64, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.block_size, self.causal = block_size, causal
+        self.Hkv, self.d = num_heads_kv, head_dim
+
+        def sub(a, b, fp8):
+            cu_s = (cu[a:b + 1] - cu[a]).astype(np.int32)
+            plan = Plan(cu_s, ctx[a:b], num_heads_q, num_heads_kv, head_dim, causal, device=dev, num_ctas=num_ctas,
+                        kv_fp8=fp8)
+            return dict(seq=(a, b), tok=(int(cu[a]), int(cu[b])), cu=torch.from_numpy(cu_s).to(dev), ctx=self.ctx[a:b],
+                        plan=plan)
+
+        self.decode = sub(da, db, True) if db > da else None
+        self.tile = None
+        if tb > ta:
+            t = sub(ta, tb, False)
+            # pages of the tile sequences, in order, and their block table over the copies
+            n = (ctx[ta:tb].astype(np.int64) + block_size - 1) // block_size
+            pages = np.concatenate([self.block_table_host[i][:k] for i, k in zip(range(ta, tb), n)]).astype(np.int32)
+            bt = -np.ones((tb - ta, max_blocks), dtype=np.int32)
+            base = np.concatenate([[0], np.cumsum(n)[:-1]])
+            for r, (b0, k) in enumerate(zip(base, n)):
+                bt[r, :k] = np.arange(b0, b0 + k, dtype=np.int32)
+            t["pages"] = torch.from_numpy(pages).to(dev)
+            t["bt"] = torch.from_numpy(bt).to(dev)
+            t["k"] = torch.empty(len(pages), num_heads_kv, block_size, head_dim, dtype=torch.bfloat16, device=dev)
+            t["v"] = torch.empty_like(t["k"])
+            self.tile = t
+
+
+def run_step_fp8_split(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, scale, out=None, stream=None):
+    """One step of an Fp8SplitBatch: slot mapping and the quantizing append for the whole batch,
+    then attention_fp8_split."""
+    out = torch.empty_like(q) if out is None else out
+    P = k_pages.shape[0]
+    xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, batch.block_size, P, batch.slots, batch.err, stream)
+    xy_kv_append_fp8(k_new, v_new, batch.slots, k_pages, v_pages, k_scales, v_scales, batch.err, stream)
+    return attention_fp8_split(batch, q, k_pages, v_pages, k_scales, v_scales, scale, out, stream)
+
+
+def attention_fp8_split(batch, q, k_pages, v_pages, k_scales, v_scales, scale, out, stream=None):
+    """The attention of an Fp8SplitBatch: the tile part (bf16 copies of its pages, tcgen05
+    attention) and the decode part (8-bit decode path), each writing its own rows of out."""
+    t = batch.tile
+    if t is not None:
+        a, b = t["tok"]
+        xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, t["pages"], t["k"], t["v"], batch.err, stream)
+        pl = t["plan"]
+        xy_paged_attention(q[a:b], t["cu"], t["ctx"], t["bt"], t["k"], t["v"], scale, batch.causal, pl.tasks,
+                           pl.merges, pl.num_ctas, pl.workspace, batch.err, out[a:b], stream)
+    dd = batch.decode
+    if dd is not None:  # (pages appended above are visible: same stream)
+        a, b = dd["tok"]
+        pl = dd["plan"]
+        sa, sb = dd["seq"]
+        xy_paged_attention_fp8(q[a:b], dd["cu"], dd["ctx"], batch.block_table[sa:sb], k_pages, v_pages, k_scales,
+                               v_scales, scale,
+                               batch.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out[a:b],
+                               stream)
     return out
 
 

@@ -47,7 +47,7 @@ def test_append_fp8_bit_exact(d):
 # ---------------------------------------------------------------------------------------------
 # attention over 8-bit pages
 
-def _run_fp8(wl, kv_chunk=None, row_scale=None):
+def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False):
     """One step over 8-bit pages on the GPU and in the oracle, on workload wl's bf16 values
     (optionally with each pool / new row multiplied by a power of two from row_scale)."""
     import paged_kv_varlen_xy_gb300 as xy
@@ -70,11 +70,16 @@ def _run_fp8(wl, kv_chunk=None, row_scale=None):
     krows = vals["k_pool"].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous().to(dev)
     vrows = vals["v_pool"].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous().to(dev)
     xy.xy_kv_append_fp8(krows, vrows, slots_all, codes["k"], codes["v"], scl["k"], scl["v"], err)
-    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
-                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
-                              kv_chunk=kv_chunk, kv_fp8=True)
     q, kn, vn = (vals[n].to(dev) for n in ("q", "k_new", "v_new"))
-    out = xystep.run_step_fp8(batch, q, kn, vn, codes["k"], codes["v"], scl["k"], scl["v"], wl.scale)
+    if split:
+        batch = xystep.Fp8SplitBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                     wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
+        out = xystep.run_step_fp8_split(batch, q, kn, vn, codes["k"], codes["v"], scl["k"], scl["v"], wl.scale)
+    else:
+        batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                  wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
+                                  kv_chunk=kv_chunk, kv_fp8=True)
+        out = xystep.run_step_fp8(batch, q, kn, vn, codes["k"], codes["v"], scl["k"], scl["v"], wl.scale)
     torch.cuda.synchronize()
     ref = oracle.step.run_step_fp8(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
                                    _bits(vals["q"]), _bits(vals["k_new"]), _bits(vals["v_new"]),
@@ -170,3 +175,39 @@ def test_fp8_full_size_sampled_rows(name):
     got = np.stack([got[t, h] for (t, h) in rows])
     diff = np.abs(got - ref["out"])
     assert np.isfinite(got).all() and diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS, (diff.max(), diff.mean())
+
+
+def test_dequant_pages_bit_exact():
+    import paged_kv_varlen_xy_gb300 as xy
+    from paged_kv_varlen_xy_gb300 import build
+    build.build()
+    g = torch.Generator().manual_seed(3)
+    P, Hkv, bs, d = 40, 4, 16, 128
+    codes = [torch.randint(0, 256, (P, Hkv, bs, d), generator=g, dtype=torch.uint8) for _ in range(2)]
+    for c in codes:
+        c[(c & 0x7F) == 0x7F] = 0                                   # no NaN codes
+    scl = [torch.rand(P, Hkv, bs, generator=g) * 4 for _ in range(2)]
+    pages = torch.tensor([7, 0, 39, 7, 12], dtype=torch.int32)
+    outs = [torch.empty(5, Hkv, bs, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dev = [t.cuda() for t in codes + scl]
+    xy.xy_dequant_pages_fp8(dev[0], dev[1], dev[2], dev[3], pages.cuda(), outs[0], outs[1], err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    for n in range(2):
+        ref = oracle.dequantize_to_bf16_bits(codes[n].numpy()[pages.numpy()], scl[n].numpy()[pages.numpy()])
+        assert np.array_equal(_bits(outs[n]), ref)
+
+
+@pytest.mark.parametrize("q_lens,ctx", [([37, 100, 5, 1, 1, 1], [37, 612, 2050, 900, 129, 16]),
+                                         ([1, 1, 1, 64, 3], [700, 33, 4000, 300, 1500]),
+                                         ([200, 17], [200, 5000])])
+def test_fp8_split_tile_and_decode_parts(q_lens, ctx):
+    # prefill / chunk sequences on the tile path over bf16 copies, decode sequences on the 8-bit
+    # path, in one step; against the oracle's attention over the exactly dequantized pages
+    from paged_kv_varlen_xy_gb300 import build
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    build.build()
+    wl = workloads.custom(q_lens, ctx, 16, 4, 128, 16, True, seed=71)
+    r = _run_fp8(wl, split=True)
+    _assert_fp8_parity(r)

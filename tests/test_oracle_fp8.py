@@ -139,3 +139,23 @@ def test_step_fp8_equals_bf16_step_when_quantization_is_exact():
     assert np.array_equal(a["slots"], b["slots"])
     assert np.all(b["k_scales"] == np.float32(1.0 / 64)) and np.all(b["v_scales"] == np.float32(1.0 / 64))
     assert np.array_equal(a["out"], b["out"])
+
+
+def test_bf16_copy_of_dequantized_rows():
+    # the bf16 copy of a dequantized row is within half a bf16 step (plus the fp32 product's
+    # rounding) of the exact value, exact where bf16 holds the value, and rounds as a worked case does
+    from oracle import dequantize_to_bf16_bits
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F].reshape(1, -1)           # the finite codes
+    for scale in (1.0, 0.25, 3.0, 1.0 / 448, 7.5e-3):
+        s = np.array([scale], dtype=np.float32)
+        got = bf16_bits_to_f64(dequantize_to_bf16_bits(codes, s))
+        exact = e4m3_to_f64(codes) * float(s[0])
+        rel = np.abs(got - exact) / np.maximum(np.abs(exact), 1e-300)
+        assert np.all(rel[exact != 0] <= 2.0 ** -8 + 2.0 ** -23)  # half a bf16 step (8 significant bits)
+        if scale in (1.0, 0.25):                                     # 4-bit values times a power of 2
+            assert np.array_equal(got, exact)
+    # 1.0 (code 0x38) times fp32(1/3) = 0.3333333432674408 rounds to bf16 0x3EAB = 0.333984375;
+    # -448 (code 0xFE) times 1.5 = -672 is exact in bf16 (0xC428)
+    bits = dequantize_to_bf16_bits(np.array([[0x38], [0xFE]], dtype=np.uint8), np.array([1 / 3, 1.5], np.float32))
+    assert bits[0, 0] == 0x3EAB and bits[1, 0] == 0xC428
