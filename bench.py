@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 import workloads  # noqa: E402
 
 METRIC = "paged-attn decode KV GB/s & prefill TFLOP/s vs roofline, tokens/s, 1×GB300"
+NOMINAL = {"hbm": 8000.0, "tc": 2250.0}   # the nominal GB300 figures (GB/s, dense BF16 TFLOP/s)
 DESC = {
     "tiny": "tiny mixed: 4 seqs (q 7,16,1,1; L 7,16,33,50), Hq 4 / Hkv 2, d 64, bs 16",
     "decode": "decode: 64 seqs, q=1, L~U[128,4096], Hq=Hkv=32, d=128, bs=16, + kv_append of 64 tokens",
@@ -320,6 +321,8 @@ def main():
         torch.cuda.synchronize()
 
     def step(ev=None):
+        if ev:
+            ev[2].record(stream)
         xy.xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, wl.block_size, P, batch.slots, batch.err)
         if fp8:
             xy.xy_kv_append_fp8(vals["k_new"], vals["v_new"], batch.slots, vals["k_codes"], vals["v_codes"],
@@ -348,7 +351,7 @@ def main():
 
     # ---- device-timed region: K steps, inputs resident in HBM ----
     n_launch_per_step = 2 + sum(1 + (1 if x.merges.shape[0] else 0) for x in parts) + (1 if split and batch.tile else 0)
-    attn_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -366,9 +369,13 @@ def main():
     xystep.check(batch)
     total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world, device=dev)
     ms_per_step = total_ms / args.steps
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_ev)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in attn_ev)
+    append_ms = statistics.mean(c.elapsed_time(a) for a, b, c in attn_ev)   # slot mapping + append
     value = job_throughput(args.config, w, ms_per_step / 1e3, world)
     unit, bound = unit_of(args.config)
+    input_bytes = sum(t.numel() * t.element_size() for k, t in vals.items()
+                      if k in ("q", "k_new", "v_new") or (k in ("k_codes", "v_codes", "k_scales", "v_scales") if fp8
+                                                         else k in ("k_pool", "v_pool")))
     traffic_key = args.config + ("_fp8" if fp8 else "")
     kname = attention_kernel(wl, args.kv) if not split else "dequant_pages_kernel + meta_attention_kernel + paged_attention_kernel<fp8>"
     attn_s = attn_ms / 1e3
@@ -389,6 +396,13 @@ def main():
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["tc"], "unit": "TFLOP/s",
                 "frac": achieved / pk["tc"], "traffic": measured_traffic(traffic_key), "kernel": kname,
                 "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
+    roof["frac_nominal"] = (roof["achieved"] / (NOMINAL["hbm"] if roof["bound"] == "hbm" else NOMINAL["tc"]))
+    roof["peak_nominal"] = NOMINAL["hbm"] if roof["bound"] == "hbm" else NOMINAL["tc"]
+    append_gbs = w["append_bytes"] / (append_ms / 1e3) / 1e9
+    append_roof = {"achieved": append_gbs, "unit": "GB/s", "peak": pk["hbm"], "frac": append_gbs / pk["hbm"],
+                   "algorithmic_bytes": w["append_bytes"], "avg_ms": append_ms,
+                   "timed": "slot mapping + KV append, CUDA events", "kernel": "kv_append_fp8_kernel" if fp8 else
+                   "kv_append_kernel"}
     roof["timed"] = ("attention call (kernel" + (" + combine" if n_merges else "") + "), CUDA events" if not split else
                      "page dequantization + tile attention + 8-bit decode attention (+ combines), CUDA events")
 
@@ -410,7 +424,7 @@ def main():
                                         wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
         return planner.plan(meta["cu"], meta["ctx"], meta["free"])
 
-    e2e_times = []
+    e2e_times, plan_times = [], []
     h2d = d2h = 0
     b_next = make_batch()
     for k in range(args.warmup + args.steps):
@@ -430,7 +444,9 @@ def main():
                             v_scales=vals["v_scales"])
         else:
             o = planner.run(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
+        tp = time.perf_counter()
         b_next = make_batch()   # the next step's plan, on the host while this step runs
+        plan_times.append(time.perf_counter() - tp)
         out_host.copy_(o, non_blocking=True)
         torch.cuda.synchronize()
         e2e_times.append(time.perf_counter() - t0)
@@ -457,8 +473,9 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16", "data": "synthetic",
             "config": {"workload": describe(args), "parallelism": f"replicas x{world}",
-                       "l2": "KV working set larger than the 129 MB L2; no flush between steps"
-                             if w["kv_bytes"] > 4 * 129e6 else "L2 not flushed (small working set)",
+                       "l2": (f"inputs (q, new K/V, page pool) {input_bytes / 1e6:.0f} MB, larger than the 129 MB L2; "
+                              "no flush between steps") if input_bytes > 129e6 else
+                             f"inputs {input_bytes / 1e6:.1f} MB fit in the 129 MB L2 (parity-size batch)",
                        "step": "slot_mapping + kv_append + paged_attention" + (" + combine" if n_merges else "") +
                                (" (8-bit pages: tile part on bf16 page copies, decode part on codes)" if split else ""),
                        "tokens_per_s": wl.num_tokens * world / (ms_per_step / 1e3),
@@ -466,11 +483,13 @@ def main():
                        "num_tasks": n_tasks, "num_merges": n_merges,
                        "num_ctas": pl.num_ctas, "balance": pl.stats["balance"]},
             "roofline": roof,
+            "append": append_roof,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_s * 1e3,
                     "loop": "per step: inputs H2D, step, output D2H, sync; tables re-planned every step, the next "
-                            "step's on the host while this one runs"},
+                            "step's on the host while this one runs",
+                    "plan_us": 1e6 * statistics.median(plan_times[args.warmup:])},
             "gpu_launches": n_launch_per_step * args.steps,
             "clocks": clocks,
         }

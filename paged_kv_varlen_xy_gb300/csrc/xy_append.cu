@@ -66,6 +66,34 @@ __global__ void kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *_
     }
 }
 
+// The same copy when the page size and the 16-byte vectors per row are powers of two and there
+// are fewer than 2^31 (token, head) rows: shifts instead of 64-bit divisions (which bound the
+// general kernel), one 32-bit division per vector for the token.
+template <int VSH>
+__global__ void kv_append_pow2_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                                      const int64_t *__restrict__ slots, int T, int H, int bs_sh,
+                                      int64_t pool_slots, uint4 *__restrict__ k_pages, uint4 *__restrict__ v_pages,
+                                      int32_t *err) {
+    const int64_t total = ((int64_t)T * H) << VSH;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t row = (uint32_t)(v >> VSH);  // (t, h)
+        const int c = (int)(v & ((1 << VSH) - 1));
+        const uint32_t t = row / (uint32_t)H;
+        const int h = (int)(row - t * (uint32_t)H);
+        const int64_t slot = __ldg(slots + t);
+        if (slot < 0) continue;
+        if (slot >= pool_slots) {
+            if (h == 0 && c == 0) xy::set_err(err, XY_DEV_SLOT_OOB);
+            continue;
+        }
+        const int64_t page = slot >> bs_sh, off = slot & ((int64_t(1) << bs_sh) - 1);
+        const int64_t dst = ((((page * H + h) << bs_sh) + off) << VSH) + c;
+        k_pages[dst] = __ldg(k_new + v);
+        v_pages[dst] = __ldg(v_new + v);
+    }
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int device_sm_count() {
@@ -112,6 +140,25 @@ extern "C" xy_status xy_kv_append(const void *k_new, const void *v_new, const in
     if (sms <= 0) return XY_ERR_CUDA;
     const int64_t want = (total + threads - 1) / threads;
     const int blocks = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    const bool pow2 = (block_size & (block_size - 1)) == 0 && (vec_per_row == 8 || vec_per_row == 16) &&
+                      (int64_t)num_tokens * num_heads_kv < (int64_t(1) << 31);
+    if (pow2) {
+        int bs_sh = 0;
+        while ((1 << bs_sh) < block_size) ++bs_sh;
+        const int64_t pool_slots = (int64_t)num_pages * block_size;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        auto *kn = static_cast<const uint4 *>(k_new);
+        auto *vn = static_cast<const uint4 *>(v_new);
+        auto *kp = static_cast<uint4 *>(k_pages);
+        auto *vp = static_cast<uint4 *>(v_pages);
+        if (vec_per_row == 16)
+            kv_append_pow2_kernel<4><<<blocks, threads, 0, st>>>(kn, vn, slot_mapping, num_tokens, num_heads_kv,
+                                                                 bs_sh, pool_slots, kp, vp, err_word);
+        else
+            kv_append_pow2_kernel<3><<<blocks, threads, 0, st>>>(kn, vn, slot_mapping, num_tokens, num_heads_kv,
+                                                                 bs_sh, pool_slots, kp, vp, err_word);
+        return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
+    }
     kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
         num_heads_kv, block_size, vec_per_row, (int64_t)num_pages * block_size, static_cast<uint4 *>(k_pages),
