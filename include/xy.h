@@ -173,7 +173,10 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  * each task to the CTA with the smallest load so far (the lowest index on ties), longest first.
  * CTAs then hold different numbers of tasks: the table keeps the layout above and the positions
  * a CTA does not use hold hole records {-1, 0, 0, 0, 0, 0, 0, -1}, which the kernels skip, so
- * *num_tasks counts the holes too (num_ctas times the longest list).
+ * *num_tasks counts the holes too (num_ctas times the longest list).  XY_SCHEDULE_DYNAMIC charges
+ * tasks as XY_SCHEDULE_GREEDY does and only sorts them: the table is meant for
+ * xy_paged_attention_dynamic, whose CTAs claim tasks in table order at run time (stats are the
+ * sums of positions modulo num_ctas).
  *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs]: host int32.
  *   tasks [max_tasks], merges [max_merges]: host outputs; pass NULL (with max 0) to query counts.
  *   *num_tasks, *num_merges: counts; *workspace_bytes = rows * (head_dim + 1) * 4 (fp32 partial
@@ -185,6 +188,7 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
 #define XY_SCHEDULE_SERPENTINE 1  /* the same sort, serpentine ("symmetric round-robin") deal */
 #define XY_SCHEDULE_MIXED 2       /* padded-tile load, sort, serpentine deal, per-CTA interleave */
 #define XY_SCHEDULE_GREEDY 3      /* padded-tile load + per-task cost, greedy deal, hole records */
+#define XY_SCHEDULE_DYNAMIC 4     /* the same loads, sorted; claimed by CTAs at run time */
 #define XY_SCHEDULE_TASK_KEYS 512 /* per-task cost of XY_SCHEDULE_GREEDY, in keys */
 #define XY_SCHEDULE_TILE_ROWS 128 /* MMA tile height: the unit of XY_SCHEDULE_MIXED's load */
 #define XY_SCHEDULE_SMALL_ROWS 16 /* tasks of at most this many rows count as small */

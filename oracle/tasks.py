@@ -53,7 +53,7 @@ TILE_ROWS = 128
 TASK_KEYS = 512
 MAX_TOTAL_LOAD = 1 << 55
 MAX_CTAS = 1 << 16
-SCHEDULES = (0, 1, 2, 3)
+SCHEDULES = (0, 1, 2, 3, 4)
 HOLE = (-1, 0, 0, 0, 0, 0, 0, -1)
 
 
@@ -96,9 +96,11 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
     schedule 0: the pages' reorder (load = area, stable sort descending, round-robin deal).
     schedule 1: the same sort, serpentine deal.  schedule 2: charged load, serpentine deal and
     per-CTA proportional interleave.  schedule 3: greedy deal with HOLE records (see above).
+    schedule 4: schedule 3's loads, sorted, not dealt: the CTAs claim tasks in this order at run
+    time (the cta_loads reported are those of positions mod num_ctas).
     """
     if schedule not in SCHEDULES:
-        raise ValueError("schedule must be 0, 1, 2 or 3")
+        raise ValueError("schedule must be 0, 1, 2, 3 or 4")
     if num_heads_q % num_heads_kv:
         raise ValueError("Hq must be a multiple of Hkv")
     if q_tile < 1 or kv_chunk < 1 or num_ctas < 1:
@@ -132,7 +134,7 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
                     r = rows * G
                     if schedule == 2:
                         r = _charged_rows(r)
-                    if schedule == 3:
+                    if schedule in (3, 4):
                         loads.append(_charged_rows(r) * (k1 - k0 + TASK_KEYS))
                     else:
                         loads.append(r * (k1 - k0))

@@ -176,6 +176,7 @@ XY_SCHEDULE_AREA = 0
 XY_SCHEDULE_SERPENTINE = 1
 XY_SCHEDULE_MIXED = 2
 XY_SCHEDULE_GREEDY = 3
+XY_SCHEDULE_DYNAMIC = 4
 
 
 _XY_ERR_CAPACITY = -10

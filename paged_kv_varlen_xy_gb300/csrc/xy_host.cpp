@@ -172,7 +172,7 @@ static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context
     if (num_seqs > 0 && !context_lens) return XY_ERR_INVALID_ARG;
     if (num_heads_q % num_heads_kv) return XY_ERR_INVALID_ARG;
     if (schedule != XY_SCHEDULE_AREA && schedule != XY_SCHEDULE_SERPENTINE && schedule != XY_SCHEDULE_MIXED &&
-        schedule != XY_SCHEDULE_GREEDY)
+        schedule != XY_SCHEDULE_GREEDY && schedule != XY_SCHEDULE_DYNAMIC)
         return XY_ERR_INVALID_ARG;
     if (cu_seqlens_q[0] != 0) return XY_ERR_CU_SEQLENS;
     const int G = num_heads_q / num_heads_kv;
@@ -214,7 +214,7 @@ static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context
             tl.kv_hi = causal ? (L - qn + t0 + tl.rows) : L;
             tl.nsplit = (tl.kv_hi + kv_chunk - 1) / kv_chunk;
             tl.charged = tl.rows * G;
-            if (schedule == XY_SCHEDULE_MIXED || schedule == XY_SCHEDULE_GREEDY)
+            if (schedule == XY_SCHEDULE_MIXED || schedule == XY_SCHEDULE_GREEDY || schedule == XY_SCHEDULE_DYNAMIC)
                 tl.charged = XY_SCHEDULE_TILE_ROWS *
                              std::max<int64_t>(1, (tl.charged + XY_SCHEDULE_TILE_ROWS - 1) / XY_SCHEDULE_TILE_ROWS);
             tiles.push_back(tl);
@@ -248,7 +248,8 @@ static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context
                     r.t.kv_end = (int32_t)k1;
                     r.t.num_splits = (int32_t)tl.nsplit;
                     r.t.ws_row = tl.nsplit == 1 ? -1 : (int32_t)(base + c * tl.rows * G);
-                    const int64_t keys = (k1 - k0) + (schedule == XY_SCHEDULE_GREEDY ? XY_SCHEDULE_TASK_KEYS : 0);
+                    const bool per_task = schedule == XY_SCHEDULE_GREEDY || schedule == XY_SCHEDULE_DYNAMIC;
+                    const int64_t keys = (k1 - k0) + (per_task ? XY_SCHEDULE_TASK_KEYS : 0);
                     r.load = tl.charged * keys;
                     recs.push_back(r);
                 }

@@ -84,7 +84,7 @@ def _tiles(G):
     return max(1, 64 // G), 4096
 
 
-@pytest.mark.parametrize("schedule", [0, 1, 2, 3])
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4])
 @pytest.mark.parametrize("name", list(workloads.CONFIGS))
 def test_task_table_matches_oracle_on_configs(xy, name, schedule):
     wl = workloads.make(name)
@@ -114,7 +114,7 @@ def test_task_table_fuzz(xy):
         Hq = Hkv * int(rng.integers(1, 9))
         args = (oracle.pack_cu_seqlens(q), ctx, Hq, Hkv, int(rng.choice([64, 128])), bool(rng.integers(0, 2)),
                 int(rng.integers(1, 200)), int(rng.integers(1, 70)), int(rng.choice([16, 64, 100, 256, 4096])),
-                int(rng.integers(0, 4)))
+                int(rng.integers(0, 5)))
         mine = xy.xy_build_task_table(*args)
         ref = oracle.build_task_table(*args)
         assert np.array_equal(mine["tasks"], ref["tasks"])
@@ -136,7 +136,7 @@ def test_task_table_errors(xy):
         xy.xy_build_task_table([0, 6], [9], 6, 4, 64, True, 8, 8, 64)
     assert e.value.status == -1            # Hq not a multiple of Hkv
     with pytest.raises(xy.XYError) as e:
-        xy.xy_build_task_table([0, 3], [5], 4, 2, 64, True, 8, 8, 64, schedule=4)
+        xy.xy_build_task_table([0, 3], [5], 4, 2, 64, True, 8, 8, 64, schedule=5)
     assert e.value.status == -1            # unknown schedule
 
 

@@ -259,7 +259,28 @@ def test_serpentine_schedule_deals_alternate_rounds_backwards():
 
 def test_unknown_schedule_rejected():
     with pytest.raises(ValueError):
-        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=4)
+        build_task_table([0, 1], [4], 4, 2, 64, True, 3, 8, 64, schedule=5)
+
+
+def test_dynamic_schedule_is_the_greedy_loads_sorted_and_undealt():
+    # schedule 4 holds exactly the greedy schedule's tasks (no holes), in stable descending order
+    # of the same loads: the order in which CTAs claim them at run time
+    rng = np.random.default_rng(8)
+    q = rng.integers(1, 40, size=9)
+    L = q + rng.integers(0, 900, size=9)
+    cu = np.concatenate([[0], np.cumsum(q)])
+    dyn = build_task_table(cu, L, 8, 2, 128, True, 5, 16, 256, schedule=4)
+    gre = build_task_table(cu, L, 8, 2, 128, True, 5, 16, 256, schedule=3)
+    real = gre["tasks"][gre["tasks"][:, 0] >= 0]
+    assert len(dyn["tasks"]) == len(real) and not np.any(dyn["tasks"][:, 0] < 0)
+    key = lambda t: tuple(t)
+    assert sorted(map(key, dyn["tasks"])) == sorted(map(key, real))
+    assert np.all(np.diff(dyn["loads"]) <= 0)
+    # ties keep enumeration order (sequence, kv head, query tile, chunk)
+    for a in range(len(dyn["tasks"]) - 1):
+        if dyn["loads"][a] == dyn["loads"][a + 1]:
+            ta, tb = dyn["tasks"][a], dyn["tasks"][a + 1]
+            assert (ta[0], ta[1], ta[2], ta[4]) < (tb[0], tb[1], tb[2], tb[4])
 
 
 def test_greedy_schedule_is_longest_processing_time_first():
