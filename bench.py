@@ -208,10 +208,12 @@ def job_throughput(config, w, seconds, world):
     return throughput(config, w, seconds) * world
 
 
-def attention_kernel(wl, kv="bf16"):
+def attention_kernel(wl, kv="bf16", schedule=3):
     """The attention kernel the library dispatches to: the tcgen05 tile kernel when head_dim is
     128, G divides 128 and the batch is not pure decode (one token per sequence, G <= 16);
     otherwise, and always over 8-bit pages, the decode-path kernel."""
+    if schedule == 4:
+        return attention_kernel(wl, kv) + " (dynamic deal)"
     if kv == "fp8":
         return "paged_attention_kernel"
     G = wl.num_heads_q // wl.num_heads_kv
@@ -228,7 +230,9 @@ def throughput(config, w, seconds):
 
 
 def describe(args):
-    return DESC[args.config] + (", 8-bit E4M3 KV pages + per-row fp32 scales" if args.kv == "fp8" else "")
+    return (DESC[args.config] + (", 8-bit E4M3 KV pages + per-row fp32 scales" if args.kv == "fp8" else "") +
+            (", dynamic deal (CTAs claim tasks at run time)" if args.schedule == 4 else
+             f", static deal (task-table schedule {args.schedule})"))
 
 
 def run_reference(args, rank, world):
@@ -261,10 +265,18 @@ def main():
     ap.add_argument("--config", default="decode", choices=list(workloads.CONFIGS))
     ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="page format of the KV cache")
+    ap.add_argument("--schedule", type=int, default=None, choices=[0, 1, 2, 3, 4],
+                    help="task-table schedule (default: 4, the dynamic deal, over bf16 pages; 3, the greedy static "
+                         "deal, over 8-bit pages)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    args.default_schedule = 3 if args.kv == "fp8" else 4
+    if args.schedule is None:
+        args.schedule = args.default_schedule
+    if args.schedule == 4 and args.kv == "fp8":
+        ap.error("--schedule 4 (the dynamic deal) runs over bf16 pages only")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -300,7 +312,8 @@ def main():
         parts = [x["plan"] for x in (batch.tile, batch.decode) if x is not None]
     else:
         batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
-                                  wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, kv_fp8=fp8)
+                                  wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, kv_fp8=fp8,
+                                  schedule=args.schedule)
         parts = [batch.plan]
     pl = parts[0]
     n_tasks = sum(int(x.tasks.shape[0]) for x in parts)
@@ -338,6 +351,10 @@ def main():
             xy.xy_paged_attention_fp8(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_codes"],
                                       vals["v_codes"], vals["k_scales"], vals["v_scales"], wl.scale, wl.causal,
                                       pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
+        elif pl.dynamic:
+            xy.xy_paged_attention_dynamic(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"],
+                                          vals["v_pool"], wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas,
+                                          pl.workspace, pl.task_counter, batch.err, out)
         else:
             xy.xy_paged_attention(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"], vals["v_pool"],
                                   wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
@@ -367,6 +384,16 @@ def main():
         w1 = time.perf_counter()
         time.sleep(0.05)
     xystep.check(batch)
+    # how evenly the deal spread the work: one traced launch after the timed region
+    deal_trace = None
+    if not fp8 and not split:
+        trace = torch.zeros(pl.num_ctas, 4, dtype=torch.int64, device=dev)
+        xy.xy_paged_attention_traced(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"],
+                                     vals["v_pool"], wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas,
+                                     pl.workspace, pl.task_counter if pl.dynamic else None, trace, batch.err, out)
+        torch.cuda.synchronize()
+        xystep.check(batch)
+        deal_trace = xy.trace_summary(trace.cpu().numpy())
     total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world, device=dev)
     ms_per_step = total_ms / args.steps
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in attn_ev)
@@ -376,8 +403,9 @@ def main():
     input_bytes = sum(t.numel() * t.element_size() for k, t in vals.items()
                       if k in ("q", "k_new", "v_new") or (k in ("k_codes", "v_codes", "k_scales", "v_scales") if fp8
                                                          else k in ("k_pool", "v_pool")))
-    traffic_key = args.config + ("_fp8" if fp8 else "")
-    kname = attention_kernel(wl, args.kv) if not split else "dequant_pages_kernel + meta_attention_kernel + paged_attention_kernel<fp8>"
+    traffic_key = (args.config + ("_fp8" if fp8 else "") +
+                   (f"_s{args.schedule}" if args.schedule != args.default_schedule else ""))
+    kname = attention_kernel(wl, args.kv, args.schedule) if not split else "dequant_pages_kernel + meta_attention_kernel + paged_attention_kernel<fp8>"
     attn_s = attn_ms / 1e3
     if bound == "hbm":
         achieved = w["attn_bytes"] / attn_s / 1e9
@@ -416,7 +444,7 @@ def main():
     # engine's scheduler overlaps the next batch with the current one); every step's timed region
     # holds one plan, its inputs' upload, the step and its output's download.
     planner = xystep.Planner(wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.block_size, wl.max_blocks, wl.causal,
-                             device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8)
+                             device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8, schedule=args.schedule)
 
     def make_batch():
         if split:
@@ -481,7 +509,9 @@ def main():
                        "tokens_per_s": wl.num_tokens * world / (ms_per_step / 1e3),
                        "tflops": w["flops"] / (ms_per_step / 1e3) / 1e12,
                        "num_tasks": n_tasks, "num_merges": n_merges,
-                       "num_ctas": pl.num_ctas, "balance": pl.stats["balance"]},
+                       "num_ctas": pl.num_ctas, "schedule": args.schedule,
+                       "balance" if args.schedule != 4 else "balance_if_dealt": pl.stats["balance"],
+                       "deal_trace": deal_trace},
             "roofline": roof,
             "append": append_roof,
             "cpu_baseline": cpu,

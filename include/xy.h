@@ -289,6 +289,67 @@ xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
                                      size_t workspace_bytes, int32_t *err_word, void *out,
                                      void *stream);
 
+/*
+ * Paged attention with a dynamic deal (a variant of the reorder's static deal, [XY] §2.2
+ * component 2: the pages deal sorted tasks to cores before the launch; here the cores take them
+ * while the kernel runs).
+ *
+ * The kernels xy_paged_attention launches for the batch (the unified tcgen05 kernel, or the
+ * decode-path kernel for pure decode batches and shapes the tile kernel does not take) run every
+ * task, but instead of walking a fixed share of the table, each persistent CTA claims the next
+ * unclaimed task with an atomic add on task_counter[0]: a scheduler warp claims task k + 1 when
+ * the CTA starts task k.  CTAs thus take tasks in table order (largest first for XY_SCHEDULE_DYNAMIC
+ * tables), and a CTA that drew short tasks takes more of them.  A task's result does not depend
+ * on which CTA runs it: outputs are bit-identical to xy_paged_attention's on the same tasks.
+ *   task_counter: device int32[2], 8-byte aligned, owned by the caller, zero before the first
+ *   call (e.g. zeroed at allocation).  Word 0 counts claims, word 1 the CTAs done claiming; the
+ *   last CTA to finish claiming returns both to zero, so every launch leaves the counter ready for
+ *   the next one, with no reset on the host or the stream.  Calls that overlap on the GPU need
+ *   different counters.
+ *   tasks: any table of xy_build_task_table for this batch (XY_SCHEDULE_DYNAMIC: sorted, no
+ *   holes; hole records of other schedules are skipped).
+ *   All other arguments, layouts, limits and errors are those of xy_paged_attention;
+ *   XY_ERR_INVALID_ARG also for a null or misaligned task_counter.  A launch whose waits gave up
+ *   (XY_DEV_TIMEOUT) still returns the counter to zero.
+ */
+xy_status xy_paged_attention_dynamic(const void *q, const int32_t *cu_seqlens_q,
+                                     const int32_t *context_lens, const int32_t *block_table,
+                                     int max_blocks, const void *k_pages, const void *v_pages,
+                                     int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                     int num_heads_kv, int head_dim, int block_size, float scale,
+                                     int causal, const xy_task *tasks, int num_tasks,
+                                     const xy_merge *merges, int num_merges, int num_ctas,
+                                     void *workspace, size_t workspace_bytes,
+                                     int32_t *task_counter, int32_t *err_word, void *out,
+                                     void *stream);
+
+/*
+ * Paged attention with a per-CTA trace, to measure how evenly a deal spreads the work ([XY] §2.2
+ * component 2 reports the balance ratio = min/max core load; the trace gives the time each CTA
+ * was busy, so the ratio and the tail -- the time the last CTA runs after the others are done --
+ * can be measured for the static and the dynamic deal alike).  No counterpart in the pages beyond
+ * that ratio.
+ *   task_counter: NULL runs what xy_paged_attention runs (the static deal: CTA c takes positions
+ *   c, c + num_ctas, ... of the table, on the unified tcgen05 kernel or the decode-path kernel);
+ *   a counter runs what xy_paged_attention_dynamic runs (the dynamic deal).
+ *   cta_trace: device uint64 [num_ctas][4], 8-byte aligned: {start ns, end ns, tasks run, sum of
+ *   q_rows * G * (kv_end - kv_start) over them}; times from the GPU's global timer (ns), start
+ *   when the CTA begins, end when its last task is stored.  A CTA whose waits gave up
+ *   (XY_DEV_TIMEOUT) leaves its end, tasks and work unwritten: zero the buffer first.
+ *   All other arguments, limits and errors are those of the call it stands for.  The split-KV
+ *   merge that follows is not traced.
+ */
+xy_status xy_paged_attention_traced(const void *q, const int32_t *cu_seqlens_q,
+                                    const int32_t *context_lens, const int32_t *block_table,
+                                    int max_blocks, const void *k_pages, const void *v_pages,
+                                    int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                    int num_heads_kv, int head_dim, int block_size, float scale,
+                                    int causal, const xy_task *tasks, int num_tasks,
+                                    const xy_merge *merges, int num_merges, int num_ctas,
+                                    void *workspace, size_t workspace_bytes,
+                                    int32_t *task_counter, uint64_t *cta_trace, int32_t *err_word,
+                                    void *out, void *stream);
+
 /* 8-bit KV pages (a variant of the pool; [CANN] §5.2 keeps scale metadata beside the pages).
  * k_pages/v_pages: uint8 [P, Hkv, bs, d] of OCP E4M3 codes ("E4M3FN": bias 7, max 448, no
  * infinities); k_scales/v_scales: fp32 [P, Hkv, bs], one scale per stored (token, KV head) row;

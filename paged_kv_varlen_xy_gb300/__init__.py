@@ -23,7 +23,8 @@ XY_DEV_TIMEOUT = 0x8
 C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_num_ctas", "xy_build_block_table",
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
          "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
-         "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8")
+         "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8", "xy_paged_attention_dynamic",
+         "xy_paged_attention_traced")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -107,6 +108,12 @@ def lib():
     L.xy_build_step_tables.restype = I
     L.xy_dequant_pages_fp8.argtypes = [P, P, P, P, I, I, I, I, P, I, P, P, P, P]
     L.xy_dequant_pages_fp8.restype = I
+    L.xy_paged_attention_dynamic.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P,
+                                             P, P, P]
+    L.xy_paged_attention_dynamic.restype = I
+    L.xy_paged_attention_traced.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P,
+                                            P, P, P, P]
+    L.xy_paged_attention_traced.restype = I
     _lib = L
     return L
 
@@ -177,6 +184,13 @@ XY_SCHEDULE_SERPENTINE = 1
 XY_SCHEDULE_MIXED = 2
 XY_SCHEDULE_GREEDY = 3
 XY_SCHEDULE_DYNAMIC = 4
+
+
+def default_schedule(kv_fp8=False):
+    """The task-table schedule a step uses unless told otherwise: the dynamic deal over bf16 pages
+    (CTAs claim tasks while the kernel runs; measured faster than the static deals on the prefill,
+    mixed and skewed batches and level on decode), the greedy static deal over 8-bit pages."""
+    return XY_SCHEDULE_GREEDY if kv_fp8 else XY_SCHEDULE_DYNAMIC
 
 
 _XY_ERR_CAPACITY = -10
@@ -299,6 +313,75 @@ def xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pa
         _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
         _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
         _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention")
+
+
+def xy_paged_attention_dynamic(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, tasks,
+                               merges, num_ctas, workspace, task_counter, err_word, out, stream=None):
+    """xy_paged_attention with a dynamic deal: the persistent CTAs claim tasks in table order from
+    task_counter (device int32 [2], zero before the first call; every launch returns it to zero)
+    while they run."""
+    import torch
+    T, Hq, d = q.shape
+    P, Hkv, bs, d2 = k_pages.shape
+    if d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch between q, out and the page pools")
+    bf = torch.bfloat16
+    nm = merges.shape[0] if merges is not None else 0
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None and workspace.numel() else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().xy_paged_attention_dynamic(
+        _dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(context_lens, torch.int32, "context_lens"),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _dev(k_pages, bf, "k_pages"),
+        _dev(v_pages, bf, "v_pages"), P, cu_seqlens_q.numel() - 1, T, Hq, Hkv, d, bs, float(scale), int(bool(causal)),
+        _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
+        _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
+        _dev(task_counter, torch.int32, "task_counter"), _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"),
+        _stream(stream)), "xy_paged_attention_dynamic")
+
+
+def xy_paged_attention_traced(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, tasks,
+                              merges, num_ctas, workspace, task_counter, cta_trace, err_word, out, stream=None):
+    """Paged attention with a per-CTA trace: cta_trace device int64 [num_ctas, 4] = {start ns, end ns,
+    tasks run, rows x keys}.  task_counter: device int32 [2] for the dynamic deal (as
+    xy_paged_attention_dynamic), or None for the static deal (as xy_paged_attention)."""
+    import torch
+    T, Hq, d = q.shape
+    P, Hkv, bs, d2 = k_pages.shape
+    if d2 != d or tuple(out.shape) != tuple(q.shape) or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("shape mismatch between q, out and the page pools")
+    if tuple(cta_trace.shape) != (int(num_ctas), 4):
+        raise ValueError("cta_trace must be [num_ctas, 4]")
+    bf = torch.bfloat16
+    nm = merges.shape[0] if merges is not None else 0
+    ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None and workspace.numel() else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().xy_paged_attention_traced(
+        _dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(context_lens, torch.int32, "context_lens"),
+        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _dev(k_pages, bf, "k_pages"),
+        _dev(v_pages, bf, "v_pages"), P, cu_seqlens_q.numel() - 1, T, Hq, Hkv, d, bs, float(scale), int(bool(causal)),
+        _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
+        _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
+        _dev(task_counter, torch.int32, "task_counter") if task_counter is not None else None,
+        _dev(cta_trace, torch.int64, "cta_trace"), _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"),
+        _stream(stream)), "xy_paged_attention_traced")
+
+
+def trace_summary(cta_trace):
+    """Balance and tail of one traced launch (cta_trace [num_ctas, 4] host int64 array): CTA busy
+    times (end - start), their min/max ratio, the span from the first start to the last end, and
+    the tail: the last end minus the median end (how long the slowest CTAs run after most are done)."""
+    tr = np.asarray(cta_trace, dtype=np.int64)
+    used = tr[tr[:, 2] > 0]
+    if len(used) == 0:
+        return {"ctas_used": 0}
+    busy = (used[:, 1] - used[:, 0]) / 1e3
+    t0 = int(tr[:, 0].min())
+    ends = (used[:, 1] - t0) / 1e3
+    return {"ctas_used": int(len(used)), "busy_us_min": float(busy.min()), "busy_us_max": float(busy.max()),
+            "busy_balance": float(busy.min() / busy.max()) if busy.max() > 0 else 1.0,
+            "span_us": float(ends.max()), "tail_us": float(ends.max() - np.median(ends)),
+            "work_balance": float(used[:, 3].min() / used[:, 3].max()),
+            "tasks_min": int(used[:, 2].min()), "tasks_max": int(used[:, 2].max())}
 
 
 def xy_paged_attention_noalloc(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, tasks,
@@ -425,15 +508,21 @@ class Plan:
     cu_seqlens_q and context_lens) uploaded to the device, and the workspace it needs."""
 
     def __init__(self, cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal, device="cuda",
-                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=XY_SCHEDULE_GREEDY, kv_fp8=False):
+                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=None, kv_fp8=False):
         import torch
         dev = torch.device(device)
         self.num_ctas = num_ctas or xy_default_num_ctas(dev.index or 0)
         cu = np.asarray(cu_seqlens_q)
+        schedule = default_schedule(kv_fp8) if schedule is None else schedule
+        self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
+        if self.dynamic and kv_fp8:
+            raise ValueError("the dynamic deal runs over bf16 pages only")
         dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8,
                                pure_decode=len(cu) > 1 and int(cu[-1]) == len(cu) - 1)
         self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
         self.schedule = schedule
+        # the dynamic deal's claim counter (every launch returns it to zero)
+        self.task_counter = torch.zeros(2, dtype=torch.int32, device=dev) if self.dynamic else None
         r = xy_build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
                                 self.num_ctas, self.q_tile, self.kv_chunk, schedule)
         self.host = r
@@ -455,8 +544,13 @@ def paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages
     out = torch.empty_like(q) if out is None else out
     own_err = err_word is None
     err_word = torch.zeros(1, dtype=torch.int32, device=q.device) if own_err else err_word
-    xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, plan.tasks,
-                       plan.merges, plan.num_ctas, plan.workspace, err_word, out)
+    if plan.dynamic:
+        xy_paged_attention_dynamic(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal,
+                                   plan.tasks, plan.merges, plan.num_ctas, plan.workspace, plan.task_counter,
+                                   err_word, out)
+    else:
+        xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, plan.tasks,
+                           plan.merges, plan.num_ctas, plan.workspace, err_word, out)
     if check and own_err:
         check_err_word(err_word)
     return out

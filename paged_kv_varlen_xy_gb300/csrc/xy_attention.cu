@@ -53,7 +53,7 @@ using xy::dec::kMathWarps;
 // scales of 8 pages), so four producer warps, one per ring slot, keep the ring ahead.
 enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2 };
 
-template <int HD, int KIND>
+template <int HD, int KIND, bool DYN = false>
 struct Cfg {
     using RG = typename std::conditional<
         KIND == kFp8Narrow, xy::dec::RingF8<4, 16>,
@@ -61,20 +61,26 @@ struct Cfg {
                                   xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type;
     static constexpr int kProducers = KIND == kBf16 ? 2 : 4;
     static_assert(RG::kStages >= kProducers, "every producer owns a ring slot");
-    static constexpr int kThreads = (kMathWarps + kProducers) * 32;
+    // math warps, producer warps, then (dynamic deal) the scheduler warp; bf16 pages only: a ninth
+    // warp would put three warps on one SM sub-partition and cap the registers at 168
+    static_assert(!DYN || KIND == kBf16, "the dynamic deal runs over bf16 pages");
+    static constexpr int kSchedWarp = kMathWarps + kProducers;
+    static constexpr int kThreads = (kSchedWarp + (DYN ? 1 : 0)) * 32;
     static constexpr int kStagesOff = 0;
     static constexpr int kSlotsOff = RG::kBytes;
     static constexpr int kBarOff = kSlotsOff + RG::kSlotBytes;
     static constexpr int kFlagOff = kBarOff + 2 * RG::kStages * 8;  // abort flag + 2 x 4 vote words
-    static constexpr int kSmemBytes = kFlagOff + 64 + 1024;         // + alignment slack
+    static constexpr int kQueueVoteOff = kFlagOff + 64;             // 2 x 4 queue-read votes
+    static constexpr int kQueueOff = kQueueVoteOff + 32;
+    static constexpr int kSmemBytes = kQueueOff + xy::TaskQueue::kBytes + 1024;  // + alignment slack
     static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 };
 
-template <int HD, int KIND>
-__global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
+template <int HD, int KIND, bool DYN>
+__global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, 1)
     paged_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p) {
-    using C = Cfg<HD, KIND>;
+    using C = Cfg<HD, KIND, DYN>;
     using RG = typename C::RG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = xy::smem_u32(smem_raw);
@@ -90,6 +96,10 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
     sm.abort_flag = abort_flag;
     sm.vote = abort_flag + 4;  // [2][kMathWarps], indexed by task parity
     sm.bar_id = 1;
+    // dynamic deal: every math and producer warp reads every entry of the claim queue
+    xy::TaskQueue dq;
+    dq.bind(gbase + C::kQueueOff, base + C::kQueueOff, abort_flag);
+    const xy::TaskQueue *q = DYN ? &dq : nullptr;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -97,11 +107,26 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
             xy::mbar_init(sm.full_bar + 8 * s, 1);
             xy::mbar_init(sm.empty_bar + 8 * s, kMathWarps);
         }
+        if (DYN) dq.init(kMathWarps + C::kProducers);
         *abort_flag = 0;
         xy::fence_mbarrier_init();
+        if (p.trace) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
     }
     __syncthreads();
 
+    if constexpr (DYN) {
+        if (warp == C::kSchedWarp) {
+            // ---------------------------- scheduler (dynamic deal) ----------------------------
+            int r = 1;
+            for (int e = 0; r == 1; ++e) r = dq.publish(e, p, p.dyn, lane);
+            dq.finish(p.dyn, lane);
+            if (r < 0) {
+                if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+            return;
+        }
+    }
     if (warp >= kMathWarps) {
         // ------------------------------ producer warps ------------------------------
         const int pw = warp - kMathWarps;
@@ -112,6 +137,7 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
         int ctr = 0, pref_win = -1;
         bool ok = true, pref_valid = false;
         TaskCursor tc;
+        tc.attach(q, false, pw == 0);
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
@@ -121,16 +147,18 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
                 continue;
             }
             if (!xy::dec::task_ok<RG>(tc.cur, p)) {
-                if (lane == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
+                if (lane == 0 && pw == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
                 pref_valid = false;
                 tc.advance(p);
                 continue;
             }
             const TaskInfo f = tc.cur;
-            const bool have_first = pref_valid;
+            // the first block-table window: prefetched with the task (static deal) or in its entry
+            const bool have_first = DYN || pref_valid;
+            const int first_win = DYN ? tc.win : pref_win;
             pref_valid = false;
             ok = xy::dec::produce_task<HD, RG>(
-                p, f, &kmap, &vmap, sm, ctr, lane, pref_win, have_first,
+                p, f, &kmap, &vmap, sm, ctr, lane, first_win, have_first,
                 [&]() {
                     // the next record has arrived by now: prefetch its numbers and first window
                     tc.prefetch_next(p);
@@ -143,7 +171,7 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
                 pw, C::kProducers);
             tc.advance(p);
         }
-        if (!ok) {
+        if (!ok || tc.failed) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             *abort_flag = 1;
         }
@@ -154,11 +182,15 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
 
     // ------------------------------ math warps ------------------------------
     int ctr = 0, iter = 0;
+    unsigned long long n_run = 0, work = 0;  // trace: tasks run and their rows x keys
     TaskCursor tc;
+    // the math warps pass named barriers together (consume_task), so they vote on each queue read
+    tc.attach(q, false, false, reinterpret_cast<volatile int *>(gbase + C::kQueueVoteOff), sm.bar_id, kMathWarps,
+              warp);
     tc.begin(p);
     while (tc.have) {
         tc.load_next_record(p);
-        if (!xy::dec::task_ok<RG>(tc.cur, p)) {
+        if (xy::is_hole(tc.cur.t) || !xy::dec::task_ok<RG>(tc.cur, p)) {
             tc.advance(p);
             continue;
         }
@@ -168,7 +200,21 @@ __global__ void __launch_bounds__(Cfg<HD, KIND>::kThreads, 1)
             if (warp == 0 && lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             return;
         }
+        ++n_run;
+        work += (unsigned long long)(f.t.q_rows * p.G) * (unsigned long long)(f.t.kv_end - f.t.kv_start);
         tc.advance(p);
+    }
+    if (tc.failed) {
+        *abort_flag = 1;
+        if (warp == 0 && lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
+        return;
+    }
+    // the math warps finish last: math warp 0 closes the CTA's trace record
+    if (p.trace && warp == 0 && lane == 0) {
+        unsigned long long *r = p.trace + 4 * blockIdx.x;
+        r[1] = xy::global_timer_ns();
+        r[2] = n_run;
+        r[3] = work;
     }
 }
 
@@ -292,23 +338,35 @@ bool make_pool_map_u8(CUtensorMap *map, const void *pool, int64_t rows, int box_
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int HD, int KIND>
-xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
-                 const xy_merge *merges, int num_merges, cudaStream_t st) {
-    using C = Cfg<HD, KIND>;
+template <int HD, int KIND, bool DYN>
+xy_status launch_attention_kernel(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
+                                  cudaStream_t st) {
+    using C = Cfg<HD, KIND, DYN>;
     static int configured_device = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return XY_ERR_CUDA;
     if (configured_device != dev) {  // the attribute is per device
-        if (cudaFuncSetAttribute(paged_attention_kernel<HD, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_attention_kernel<HD, KIND, DYN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmemBytes) != cudaSuccess)
             return XY_ERR_CUDA;
         configured_device = dev;
     }
+    paged_attention_kernel<HD, KIND, DYN><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? XY_OK : xy::cuda_fail(e, "paged_attention_kernel launch");
+}
+
+template <int HD, int KIND>
+xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
+                 const xy_merge *merges, int num_merges, cudaStream_t st) {
     if (p.num_tasks > 0) {
-        paged_attention_kernel<HD, KIND><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel launch");
+        xy_status ks;
+        if constexpr (KIND == kBf16)
+            ks = p.dyn ? launch_attention_kernel<HD, KIND, true>(p, km, vm, num_ctas, st)
+                       : launch_attention_kernel<HD, KIND, false>(p, km, vm, num_ctas, st);
+        else
+            ks = launch_attention_kernel<HD, KIND, false>(p, km, vm, num_ctas, st);
+        if (ks != XY_OK) return ks;
     }
     if (num_merges > 0) {
         combine_kernel<HD><<<dim3(num_merges, kCombineY), 256, 0, st>>>(merges, p.ws_o, p.ws_lse, p.cu, p.Hq, p.G,
@@ -366,6 +424,8 @@ xy_status make_params(const void *q, const int32_t *cu_seqlens_q, const int32_t 
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.ksc = nullptr;
     p.vsc = nullptr;
+    p.dyn = nullptr;
+    p.trace = nullptr;
     p.MB = max_blocks;
     p.P = num_pages;
     p.S = num_seqs;
@@ -382,21 +442,28 @@ xy_status make_params(const void *q, const int32_t *cu_seqlens_q, const int32_t 
 
 }  // namespace
 
-extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
-                                        const int32_t *block_table, int max_blocks, const void *k_pages,
-                                        const void *v_pages, int num_pages, int num_seqs, int num_tokens,
-                                        int num_heads_q, int num_heads_kv, int head_dim, int block_size, float scale,
-                                        int causal, const xy_task *tasks, int num_tasks, const xy_merge *merges,
-                                        int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
-                                        int32_t *err_word, void *out, void *stream) {
+namespace {
+
+// xy_paged_attention; the dynamic deal when task_counter is given; the per-CTA trace of
+// xy_paged_attention_traced when cta_trace is given.
+xy_status attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                    const int32_t *block_table, int max_blocks, const void *k_pages, const void *v_pages,
+                    int num_pages, int num_seqs, int num_tokens, int num_heads_q, int num_heads_kv, int head_dim,
+                    int block_size, float scale, int causal, const xy_task *tasks, int num_tasks,
+                    const xy_merge *merges, int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                    int32_t *task_counter, uint64_t *cta_trace, int32_t *err_word, void *out, void *stream) {
     if (num_tasks < 0 || num_merges < 0 || num_seqs < 0 || num_tokens < 0) return XY_ERR_INVALID_ARG;
     if (num_tasks == 0 && num_merges == 0) return XY_OK;
+    if (task_counter && (reinterpret_cast<uintptr_t>(task_counter) & 7)) return XY_ERR_INVALID_ARG;
+    if (cta_trace && (reinterpret_cast<uintptr_t>(cta_trace) & 7)) return XY_ERR_INVALID_ARG;
     AttnParams p;
     const xy_status ps = make_params(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages,
                                      num_pages, num_seqs, num_tokens, num_heads_q, num_heads_kv, head_dim,
                                      block_size, scale, causal, tasks, num_tasks, merges, num_merges, num_ctas,
                                      workspace, workspace_bytes, err_word, out, &p);
     if (ps != XY_OK) return ps;
+    p.dyn = reinterpret_cast<int *>(task_counter);
+    p.trace = reinterpret_cast<unsigned long long *>(cta_trace);
 
     const int64_t rows = (int64_t)num_pages * num_heads_kv * block_size;
     const int box_rows = block_size < xy::dec::kStageKeys ? block_size : xy::dec::kStageKeys;
@@ -420,6 +487,20 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
     }
     return head_dim == 128 ? launch<128, kBf16>(p, km, vm, num_ctas, merges, num_merges, st)
                            : launch<64, kBf16>(p, km, vm, num_ctas, merges, num_merges, st);
+}
+
+}  // namespace
+
+extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                        const int32_t *block_table, int max_blocks, const void *k_pages,
+                                        const void *v_pages, int num_pages, int num_seqs, int num_tokens,
+                                        int num_heads_q, int num_heads_kv, int head_dim, int block_size, float scale,
+                                        int causal, const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                        int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                                        int32_t *err_word, void *out, void *stream) {
+    return attention(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages, num_pages, num_seqs,
+                     num_tokens, num_heads_q, num_heads_kv, head_dim, block_size, scale, causal, tasks, num_tasks, merges,
+                     num_merges, num_ctas, workspace, workspace_bytes, nullptr, nullptr, err_word, out, stream);
 }
 
 extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
@@ -455,6 +536,39 @@ extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seq
     const bool narrow = num_tokens == num_seqs && p.G <= XY_FP8_NARROW_ROWS;
     return narrow ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
                   : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
+}
+
+// Dynamic deal: the kernels xy_paged_attention would launch, each CTA claiming the next task of
+// the table (in table order) from a counter as it starts its current one, instead of walking a
+// fixed share.
+extern "C" xy_status xy_paged_attention_dynamic(const void *q, const int32_t *cu_seqlens_q,
+                                                const int32_t *context_lens, const int32_t *block_table,
+                                                int max_blocks, const void *k_pages, const void *v_pages,
+                                                int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                                int num_heads_kv, int head_dim, int block_size, float scale,
+                                                int causal, const xy_task *tasks, int num_tasks,
+                                                const xy_merge *merges, int num_merges, int num_ctas,
+                                                void *workspace, size_t workspace_bytes, int32_t *task_counter,
+                                                int32_t *err_word, void *out, void *stream) {
+    if (!task_counter) return XY_ERR_INVALID_ARG;
+    return attention(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages, num_pages, num_seqs,
+                     num_tokens, num_heads_q, num_heads_kv, head_dim, block_size, scale, causal, tasks, num_tasks, merges,
+                     num_merges, num_ctas, workspace, workspace_bytes, task_counter, nullptr, err_word, out, stream);
+}
+
+extern "C" xy_status xy_paged_attention_traced(const void *q, const int32_t *cu_seqlens_q,
+                                               const int32_t *context_lens, const int32_t *block_table,
+                                               int max_blocks, const void *k_pages, const void *v_pages,
+                                               int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                               int num_heads_kv, int head_dim, int block_size, float scale,
+                                               int causal, const xy_task *tasks, int num_tasks,
+                                               const xy_merge *merges, int num_merges, int num_ctas,
+                                               void *workspace, size_t workspace_bytes, int32_t *task_counter,
+                                               uint64_t *cta_trace, int32_t *err_word, void *out, void *stream) {
+    if (!cta_trace) return XY_ERR_INVALID_ARG;
+    return attention(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages, num_pages, num_seqs,
+                     num_tokens, num_heads_q, num_heads_kv, head_dim, block_size, scale, causal, tasks, num_tasks, merges,
+                     num_merges, num_ctas, workspace, workspace_bytes, task_counter, cta_trace, err_word, out, stream);
 }
 
 // ---------------------------------------------------------------------------------------------

@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include "xy.h"
+#include "xy_device.cuh"
 
 namespace xy {
 
@@ -23,6 +24,8 @@ struct AttnParams {
     __nv_bfloat16 *out;
     const float *ksc;  // 8-bit pages: per-row K and V scales [P, Hkv, bs] (null for bf16 pages)
     const float *vsc;
+    int *dyn;          // dynamic deal: counter of claimed tasks (null: the static deal)
+    unsigned long long *trace;  // per-CTA record {start ns, end ns, tasks run, rows x keys} (null: off)
     int64_t ws_rows;
     int MB, P, S, T, Hq, Hkv, G, bs, causal, num_tasks;
     float scale_log2;
@@ -53,20 +56,172 @@ __device__ __forceinline__ TaskInfo fetch_info(const xy_task &t, const AttnParam
     return f;
 }
 
-// Walks this CTA's tasks (blockIdx.x, +gridDim.x, ...), fetching the next task's record and
-// per-sequence numbers while the current one runs.
+// Block-table window of a producer warp: lane i holds the physical page of logical page b0 + i of
+// sequence `seq` (-1 past the table).
+__device__ __forceinline__ int load_window(const AttnParams &p, int seq, int b0, int lane) {
+    const int idx = b0 + lane;
+    return (idx >= 0 && idx < p.MB) ? __ldg(p.bt + (int64_t)seq * p.MB + idx) : -1;
+}
+
+// Dynamic deal: a shared-memory ring of the tasks this CTA has claimed.  A scheduler warp claims
+// the next task index of the table with an atomic add on the launch's counter, fetches the record,
+// its per-sequence numbers and its first block-table window, and publishes them as entry e in slot
+// e % kQueueSlots; every other warp of the CTA reads every entry, in order.  Per slot: full completes when the entry is
+// published, empty when all readers have read it, taken when the lead reader (the warp that
+// issues the task's first copies) has read it.  Entry e + 1 is claimed once entry e is taken, so a
+// CTA holds at most one claimed task beyond the one it is starting.
+constexpr int kQueueSlots = 8;
+constexpr int kQueueEnd = -2;  // sequence id of the entry that ends the table
+
+struct QueueEntry {
+    TaskInfo f;
+    int win[32];  // physical pages of logical pages kv_start / bs + 0..31 (-1 past the table)
+};
+
+struct TaskQueue {
+    QueueEntry *entry;  // [kQueueSlots]
+    uint32_t full, empty, taken;  // shared addresses of [kQueueSlots] mbarriers each
+    const volatile int *abort;
+    static constexpr int kBytes = kQueueSlots * (int)sizeof(QueueEntry) + 3 * kQueueSlots * 8;
+
+    // `at`: kBytes of shared memory, 8-byte aligned (generic pointer and its shared address).
+    __device__ void bind(uint8_t *at, uint32_t at_s, const volatile int *abort_flag) {
+        full = at_s;
+        empty = full + 8 * kQueueSlots;
+        taken = empty + 8 * kQueueSlots;
+        entry = reinterpret_cast<QueueEntry *>(at + 3 * kQueueSlots * 8);
+        abort = abort_flag;
+    }
+    // one thread, before the CTA's first barrier; `readers`: arrivals that free a slot
+    __device__ void init(int readers) const {
+        for (int e = 0; e < kQueueSlots; ++e) {
+            mbar_init(full + 8 * e, 1);
+            mbar_init(empty + 8 * e, readers);
+            mbar_init(taken + 8 * e, 1);
+        }
+    }
+    // Scheduler warp: claim a task and publish it as entry e.  Returns 1 (a task), 0 (the end of
+    // the table was published) or -1 (a wait gave up; nothing published).
+    __device__ int publish(int e, const AttnParams &p, int *counter, int lane) const {
+        bool ok = true;
+        if (e >= 1)  // the lead reader has started entry e - 1
+            ok = mbar_wait(taken + 8 * ((e - 1) % kQueueSlots), ((e - 1) / kQueueSlots) & 1, abort);
+        if (ok && e >= kQueueSlots)  // every reader is done with the slot's previous entry
+            ok = mbar_wait(empty + 8 * (e % kQueueSlots), ((e / kQueueSlots) - 1) & 1, abort);
+        if (!__all_sync(0xffffffffu, ok)) return -1;
+        int idx = 0;
+        if (lane == 0) idx = atomicAdd(counter, 1);
+        idx = __shfl_sync(0xffffffffu, idx, 0);
+        QueueEntry &q = entry[e % kQueueSlots];
+        const int r = idx < p.num_tasks ? 1 : 0;
+        if (r) {
+            // lanes 0..7 load one word of the record each
+            const int w = lane < 8 ? __ldg(reinterpret_cast<const int32_t *>(p.tasks + idx) + lane) : 0;
+            xy_task t;
+            t.seq = __shfl_sync(0xffffffffu, w, 0);
+            t.kv_head = __shfl_sync(0xffffffffu, w, 1);
+            t.q_start = __shfl_sync(0xffffffffu, w, 2);
+            t.q_rows = __shfl_sync(0xffffffffu, w, 3);
+            t.kv_start = __shfl_sync(0xffffffffu, w, 4);
+            t.kv_end = __shfl_sync(0xffffffffu, w, 5);
+            t.num_splits = __shfl_sync(0xffffffffu, w, 6);
+            t.ws_row = __shfl_sync(0xffffffffu, w, 7);
+            const TaskInfo f = fetch_info(t, p);
+            const bool seq_ok = t.seq >= 0 && t.seq < p.S && t.kv_start >= 0;
+            q.win[lane] = seq_ok ? load_window(p, t.seq, t.kv_start / p.bs, lane) : -1;
+            if (lane == 0) q.f = f;
+        } else if (lane == 0) {
+            q.f.t = xy_task{kQueueEnd, 0, 0, 0, 0, 0, 0, -1};
+            q.f.seq_start = q.f.qn = q.f.L = 0;
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full + 8 * (e % kQueueSlots));  // release: readers see the entry
+        return r;
+    }
+    // Scheduler warp, after its last claim (whatever the reason it stopped): counter[1] counts the
+    // CTAs done claiming; the last one returns both words to zero for the next launch.
+    __device__ static void finish(int *counter, int lane) {
+        if (lane == 0) {
+            __threadfence();  // this CTA's claims come before its count
+            if (atomicAdd(counter + 1, 1) == (int)gridDim.x - 1) {
+                atomicExch(counter, 0);
+                atomicExch(counter + 1, 0);
+            }
+        }
+        __syncwarp();
+    }
+};
+
+// Walks this CTA's tasks.  Static deal: positions blockIdx.x, +gridDim.x, ... of the table, the
+// next task's record and per-sequence numbers fetched while the current one runs.  Dynamic deal
+// (attach() with a queue): the entries of the CTA's TaskQueue, in order.
 struct TaskCursor {
     int ti;
     bool have, have_next, nxt_ready;
     TaskInfo cur, nxt;
     xy_task rec_next;
+    // dynamic deal
+    const TaskQueue *dq = nullptr;
+    int read = 0;
+    int win = -1;  // this lane's page of the entry's first block-table window (whole-warp readers)
+    bool single = false, lead = false, failed = false;
+    volatile int *votes = nullptr;  // [2][vote_n]: a group of warps that agree on every read
+    int vote_bar = 0, vote_n = 0, vote_i = 0;
 
+    // q: the queue (null: static deal).  single: only the calling thread reads (else the whole
+    // warp).  lead: this reader signals `taken`.  votes/bar/n/i: the reader is warp i of n that
+    // pass named barrier `bar` together, so they vote on each read (a read that gave up in one
+    // of them stops all of them) and no warp is left waiting at that barrier.
+    __device__ void attach(const TaskQueue *q, bool single_thread, bool lead_reader, volatile int *vote_words = nullptr,
+                           int bar = 0, int n = 0, int i = 0) {
+        dq = q;
+        single = single_thread;
+        lead = lead_reader;
+        votes = vote_words;
+        vote_bar = bar;
+        vote_n = n;
+        vote_i = i;
+    }
+    __device__ void read_entry() {
+        const int s = read % kQueueSlots;
+        bool ok = mbar_wait(dq->full + 8 * s, (read / kQueueSlots) & 1, dq->abort);
+        if (!single) ok = __all_sync(0xffffffffu, ok);
+        int r = -1;
+        if (ok) {
+            cur = dq->entry[s].f;
+            if (!single) {
+                win = dq->entry[s].win[threadIdx.x & 31];
+                __syncwarp();
+            }
+            if (single || (threadIdx.x & 31) == 0) {
+                mbar_arrive(dq->empty + 8 * s);
+                if (lead) mbar_arrive(dq->taken + 8 * s);
+            }
+            r = cur.t.seq == kQueueEnd ? 0 : 1;
+        }
+        ++read;
+        if (votes) {
+            volatile int *v = votes + (read & 1) * vote_n;
+            if ((threadIdx.x & 31) == 0) v[vote_i] = r;
+            named_bar_sync(vote_bar, vote_n * 32);
+            for (int k = 0; k < vote_n; ++k) r = min(r, v[k]);
+        }
+        have = r == 1;
+        failed = r < 0;
+        have_next = nxt_ready = false;
+    }
     __device__ void begin(const AttnParams &p) {
+        if (dq) {
+            read_entry();
+            return;
+        }
         ti = blockIdx.x;
         have = ti < p.num_tasks;
         if (have) cur = fetch_info(p.tasks[ti], p);
     }
     __device__ void load_next_record(const AttnParams &p) {
+        if (dq) return;  // the next entry is not known before it is read
         const int tn = ti + gridDim.x;
         have_next = tn < p.num_tasks;
         if (have_next) rec_next = p.tasks[tn];
@@ -79,19 +234,16 @@ struct TaskCursor {
         }
     }
     __device__ void advance(const AttnParams &p) {
+        if (dq) {
+            read_entry();
+            return;
+        }
         prefetch_next(p);
         cur = nxt;
         ti += gridDim.x;
         have = have_next;
     }
 };
-
-// Block-table window of a producer warp: lane i holds the physical page of logical page b0 + i of
-// sequence `seq` (-1 past the table).
-__device__ __forceinline__ int load_window(const AttnParams &p, int seq, int b0, int lane) {
-    const int idx = b0 + lane;
-    return (idx >= 0 && idx < p.MB) ? __ldg(p.bt + (int64_t)seq * p.MB + idx) : -1;
-}
 
 // A hole record of a greedy deal (a position its CTA does not use): every role skips it.
 __device__ __forceinline__ bool is_hole(const xy_task &t) { return t.seq == -1 && t.q_rows == 0; }

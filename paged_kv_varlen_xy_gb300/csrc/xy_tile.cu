@@ -51,7 +51,9 @@ constexpr int kSlots = 5;                       // K/V ring slots (one K or V ti
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDecProducerWarp = 10;   // second producer of the decode ring (odd stages)
-constexpr int kThreads = 11 * 32;
+constexpr int kSchedWarp = 11;         // dynamic deal only: claims tasks into the CTA's queue
+constexpr int kThreads = 11 * 32;      // + the scheduler warp with the dynamic deal
+constexpr int kQueueReaders = 11;      // every warp but the scheduler reads every queue entry
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 columns
 constexpr int kTileBytes = 2 * kHalfBytes;      // one Q, K or V tile: [half][128 rows][128 B]
 constexpr int kQOff = 0;                        // Q_A, Q_B
@@ -80,7 +82,9 @@ static_assert(kDecSlotsOff + DecRing::kSlotBytes <= kBarOff, "decode path fits i
 constexpr int kDecBarOff = kBarOff + B_COUNT * 8;    // decode ring full[4], empty[4], task-done[2]
 constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 2) * 8;  // TMEM base, abort flag, decode go
 constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp, then 2 x 4 decode votes
-constexpr int kSmemBytes = kVoteOff + 64 + 32 + 1024;
+constexpr int kQueueVoteOff = kVoteOff + 96;        // queue-read votes: [softmax group][2][4]
+constexpr int kQueueOff = kQueueVoteOff + 64;       // the dynamic deal's claim queue
+constexpr int kSmemBytes = kQueueOff + xy::TaskQueue::kBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
@@ -96,7 +100,8 @@ __device__ __forceinline__ bool tile_ok(const TaskInfo &f, const AttnParams &p) 
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool DYN>
+__global__ void __launch_bounds__(kThreads + (DYN ? 32 : 0), 1)
     meta_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_d,
                           const __grid_constant__ CUtensorMap vmap_d, const AttnParams p) {
@@ -125,6 +130,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // phase j >> 1.  Two barriers, and the producer confirms task j - 2 before issuing task j, so
     // every wait below is on the latest phase issued on its barrier and parity cannot alias.
     const uint32_t dec_done = base + kDecBarOff + 8 * (2 * DecRing::kStages);
+    // dynamic deal: the claim queue every warp but the scheduler reads
+    xy::TaskQueue dq;
+    dq.bind(gbase + kQueueOff, base + kQueueOff, abort_flag);
+    const xy::TaskQueue *q = DYN ? &dq : nullptr;
 
     if (threadIdx.x == 0) {
         xy::mbar_init(bar(B_QFULL), 1);
@@ -146,9 +155,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         xy::mbar_init(dec_done, xy::dec::kMathWarps);
         xy::mbar_init(dec_done + 8, xy::dec::kMathWarps);
+        if (DYN) dq.init(kQueueReaders);
         *abort_flag = 0;
         *dec_go = 0;
         xy::fence_mbarrier_init();
+        if (p.trace) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
     }
     if (warp == kMmaWarp) {
         xy::tmem_alloc(base + kMiscOff, kTmemCols);
@@ -180,7 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int pref_win = -1;
         bool pref_valid = false;
+        unsigned long long n_run = 0, work = 0;  // trace: tasks issued and their rows x keys
         TaskCursor tc;
+        tc.attach(q, false, true);  // the lead reader: its reads pace the claims
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
@@ -196,6 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc.advance(p);
                 continue;
             }
+            ++n_run;
+            work += (unsigned long long)(tc.cur.t.q_rows * p.G) *
+                    (unsigned long long)(tc.cur.t.kv_end - tc.cur.t.kv_start);
             const int kind = tile ? 1 : 2;
             if (last_kind != 0 && kind != last_kind) {
                 // The two paths share shared memory: before writing it for the other kind, wait
@@ -223,9 +239,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence_block();
                 if (lane == 0) *dec_go = nd + 1;  // the second decode producer may write task nd
                 const TaskInfo f = tc.cur;
-                const bool have_first = pref_valid;
+                // the first block-table window: prefetched (static deal) or in the entry
+                const bool have_first = DYN || pref_valid;
+                const int first_win = DYN ? tc.win : pref_win;
                 pref_valid = false;
-                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, dsm, dctr, lane, pref_win, have_first,
+                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, dsm, dctr, lane, first_win, have_first,
                                                         [&]() {
                                                             tc.prefetch_next(p);
                                                             if (tc.have_next) {
@@ -259,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++qk;
             const int32_t *bt_row = p.bt + (int64_t)t.seq * p.MB;
             int win0 = t.kv_start / p.bs;
-            int pg_win = pref_valid ? pref_win : load_win(bt_row, win0);
+            int pg_win = DYN ? tc.win : pref_valid ? pref_win : load_win(bt_row, win0);
             int pg_nxt = load_win(bt_row, win0 + 32);
             pref_valid = false;
             bool first = true;
@@ -308,9 +326,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc.advance(p);
         }
-        if (!ok) {
+        if (!ok || tc.failed) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             *abort_flag = 1;
+        } else if (p.trace && lane == 0) {
+            p.trace[4 * blockIdx.x + 2] = n_run;
+            p.trace[4 * blockIdx.x + 3] = work;
         }
         // every issued copy must land before the CTA may exit
         for (int k = c - 1; k >= 0 && k >= c - kSlots; --k)
@@ -361,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 xy::umma_commit(bar(B_OBAR0 + x));
             };
             TaskCursor tc;
+            tc.attach(q, true, false);
             tc.begin(p);
             while (tc.have && ok) {
                 tc.load_next_record(p);
@@ -405,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int x = 0; x < nx; ++x) ++nt[x];
                 tc.advance(p);
             }
-            if (!ok) {
+            if (!ok || tc.failed) {
                 xy::set_err(p.err, XY_DEV_TIMEOUT);
                 *abort_flag = 1;
             }
@@ -423,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int dctr = 0, nd = 0, pref_win = -1;
         bool ok = true, pref_valid = false, after_tile = false;
         TaskCursor tc;
+        tc.attach(q, false, false);
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
@@ -459,10 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++nd;
             const TaskInfo f = tc.cur;
-            const bool have_first = pref_valid;
+            const bool have_first = DYN || pref_valid;
+            const int first_win = DYN ? tc.win : pref_win;
             pref_valid = false;
             ok = xy::dec::produce_task<HD, DecRing>(
-                p, f, &kmap_d, &vmap_d, dsm, dctr, lane, pref_win, have_first,
+                p, f, &kmap_d, &vmap_d, dsm, dctr, lane, first_win, have_first,
                 [&]() {
                     tc.prefetch_next(p);
                     if (tc.have_next) {
@@ -474,12 +498,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 1, 2);
             tc.advance(p);
         }
-        if (!ok) {
+        if (!ok || tc.failed) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             *abort_flag = 1;
         }
         // every stage this warp issued must land before the CTA may exit
         xy::dec::drain<DecRing>(dsm, dctr, 1, 2);
+    } else if (warp == kSchedWarp) {
+        // ---------------------------- scheduler (dynamic deal) ----------------------------
+        if constexpr (DYN) {
+            int r = 1;
+            for (int e = 0; r == 1; ++e) r = dq.publish(e, p, p.dyn, lane);
+            dq.finish(p.dyn, lane);
+            if (r < 0) {
+                if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
     } else if (warp < 8) {
         // ---------------------------------- softmax ----------------------------------
         const int x = warp >> 2;                            // query tile of this group
@@ -492,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         int dctr = 0, diter = 0;     // decode path (warps 0..3): stages consumed, tasks run
         bool ok = true;
         TaskCursor tc;
+        // the group passes named barrier 1 + x together, so its four warps vote on each queue read
+        tc.attach(q, false, false, reinterpret_cast<volatile int *>(gbase + kQueueVoteOff) + 8 * x, 1 + x, 4,
+                  warp & 3);
         tc.begin(p);
         while (tc.have) {
             tc.load_next_record(p);
@@ -755,6 +793,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc.advance(p);
         }
+        if (tc.failed) {
+            *abort_flag = 1;
+            if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
+        }
     }
 
     xy::tc_fence_before();
@@ -763,6 +805,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         xy::tc_fence_after();
         xy::tmem_dealloc(tbase, kTmemCols);
     }
+    if (p.trace && threadIdx.x == 0 && !*abort_flag) p.trace[4 * blockIdx.x + 1] = xy::global_timer_ns();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -820,16 +863,20 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return XY_ERR_CUDA;
-    static int configured_device = -1;
+    static int configured_device[2] = {-1, -1};  // per instantiation
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
-    if (configured_device != dev) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(meta_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const int dyn = p.dyn ? 1 : 0;
+    if (configured_device[dyn] != dev) {
+        const cudaError_t e = cudaFuncSetAttribute(dyn ? meta_attention_kernel<true> : meta_attention_kernel<false>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "meta_attention_kernel smem attribute");
-        configured_device = dev;
+        configured_device[dyn] = dev;
     }
-    meta_attention_kernel<<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
+    if (dyn)
+        meta_attention_kernel<true><<<num_ctas, kThreads + 32, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
+    else
+        meta_attention_kernel<false><<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? XY_OK : cuda_fail(e, "meta_attention_kernel launch");
 }

@@ -4,9 +4,9 @@ KV append and paged attention (device).  Composition of libxy calls only; no ari
 import numpy as np
 import torch
 
-from . import (Plan, check_err_word, default_tiles, xy_build_block_table, xy_build_step_tables, xy_default_num_ctas,
-               xy_dequant_pages_fp8, xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_fp8,
-               xy_slot_mapping)
+from . import (XY_SCHEDULE_DYNAMIC, Plan, check_err_word, default_schedule, default_tiles, xy_build_block_table, xy_build_step_tables, xy_default_num_ctas,
+               xy_dequant_pages_fp8, xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_dynamic,
+               xy_paged_attention_fp8, xy_slot_mapping)
 
 
 class PagedBatch:
@@ -14,7 +14,7 @@ class PagedBatch:
     buffer and the attention plan.  Built from host arrays (the scheduler's view of the batch)."""
 
     def __init__(self, cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
-                 head_dim, causal, device="cuda", num_ctas=None, q_tile=None, kv_chunk=None, schedule=3,
+                 head_dim, causal, device="cuda", num_ctas=None, q_tile=None, kv_chunk=None, schedule=None,
                  kv_fp8=False):
         dev = torch.device(device)
         self.cu_host = np.asarray(cu_seqlens_q, dtype=np.int32)
@@ -103,15 +103,22 @@ class Planner:
     _ALIGN = 256
 
     def __init__(self, num_heads_q, num_heads_kv, head_dim, block_size, max_blocks, causal, device="cuda",
-                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=3, kv_fp8=False):
+                 num_ctas=None, q_tile=None, kv_chunk=None, schedule=None, kv_fp8=False):
         self.dev = torch.device(device)
         self.Hq, self.Hkv, self.d = num_heads_q, num_heads_kv, head_dim
         self.block_size, self.max_blocks, self.causal, self.kv_fp8 = block_size, max_blocks, causal, kv_fp8
         self.num_ctas = num_ctas or xy_default_num_ctas(self.dev.index or 0)
         # q_tile per batch over 8-bit pages (it depends on whether the batch is pure decode)
         self._q_tile_arg = q_tile
-        self.kv_chunk = kv_chunk or default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)[1]
-        self.q_tile, self.schedule = q_tile or default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)[0], schedule
+        schedule = default_schedule(kv_fp8) if schedule is None else schedule
+        self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
+        if self.dynamic and kv_fp8:
+            raise ValueError("the dynamic deal runs over bf16 pages only")
+        tiles = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
+        self.kv_chunk = kv_chunk or tiles[1]
+        self.q_tile, self.schedule = q_tile or tiles[0], schedule
+        # the dynamic deal's claim counter (every launch returns it to zero)
+        self._counter = torch.zeros(2, dtype=torch.int32, device=self.dev) if self.dynamic else None
         self._host = None
         self._dev_buf = None
         self._ws = torch.empty(16, dtype=torch.uint8, device=self.dev)
@@ -220,9 +227,15 @@ class Planner:
             _check(L.xy_kv_append(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), slots, T,
                                   _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P, Hkv, bs, d, err, st),
                    "xy_kv_append")
-            _check(L.xy_paged_attention(_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, bf, "k_pages"),
-                                        _dev(v_pages, bf, "v_pages"), P, *common, _dev(out, bf, "out"), st),
-                   "xy_paged_attention")
+            if self.dynamic:
+                _check(L.xy_paged_attention_dynamic(_dev(q, bf, "q"), cu, ctx, bt, batch.MB,
+                                                    _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P,
+                                                    *common[:-1], ctypes.c_void_p(self._counter.data_ptr()), err,
+                                                    _dev(out, bf, "out"), st), "xy_paged_attention_dynamic")
+            else:
+                _check(L.xy_paged_attention(_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, bf, "k_pages"),
+                                            _dev(v_pages, bf, "v_pages"), P, *common, _dev(out, bf, "out"), st),
+                       "xy_paged_attention")
         return out
 
 
@@ -234,8 +247,13 @@ def run_step(batch, q, k_new, v_new, k_pages, v_pages, scale, out=None, stream=N
     xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, batch.block_size, P, batch.slots, batch.err, stream)
     xy_kv_append(k_new, v_new, batch.slots, k_pages, v_pages, batch.err, stream)
     pl = batch.plan
-    xy_paged_attention(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, scale, batch.causal, pl.tasks,
-                       pl.merges, pl.num_ctas, pl.workspace, batch.err, out, stream)
+    if pl.dynamic:
+        xy_paged_attention_dynamic(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, scale, batch.causal,
+                                   pl.tasks, pl.merges, pl.num_ctas, pl.workspace, pl.task_counter, batch.err, out,
+                                   stream)
+    else:
+        xy_paged_attention(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, scale, batch.causal,
+                           pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out, stream)
     return out
 
 
@@ -339,8 +357,13 @@ def attention_fp8_split(batch, q, k_pages, v_pages, k_scales, v_scales, scale, o
         a, b = t["tok"]
         xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, t["pages"], t["k"], t["v"], batch.err, stream)
         pl = t["plan"]
-        xy_paged_attention(q[a:b], t["cu"], t["ctx"], t["bt"], t["k"], t["v"], scale, batch.causal, pl.tasks,
-                           pl.merges, pl.num_ctas, pl.workspace, batch.err, out[a:b], stream)
+        if pl.dynamic:
+            xy_paged_attention_dynamic(q[a:b], t["cu"], t["ctx"], t["bt"], t["k"], t["v"], scale, batch.causal,
+                                       pl.tasks, pl.merges, pl.num_ctas, pl.workspace, pl.task_counter, batch.err,
+                                       out[a:b], stream)
+        else:
+            xy_paged_attention(q[a:b], t["cu"], t["ctx"], t["bt"], t["k"], t["v"], scale, batch.causal, pl.tasks,
+                               pl.merges, pl.num_ctas, pl.workspace, batch.err, out[a:b], stream)
     dd = batch.decode
     if dd is not None:  # (pages appended above are visible: same stream)
         a, b = dd["tok"]
