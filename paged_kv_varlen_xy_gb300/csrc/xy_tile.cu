@@ -7,7 +7,7 @@
 //
 // A task holds up to 256 (token, head) rows: query tile A (rows 0..127) and tile B (rows
 // 128..255), both against the same 128-key K/V tiles, so each K/V tile loaded serves two MMA
-// tiles.  One persistent CTA per SM, ten warps:
+// tiles.  One persistent CTA per SM, twelve warps in three warpgroups:
 //   warp 8      producer: TMA loads of the task's query rows (G heads x 128/G tokens per tile,
 //               one 3-D box per 64-column half) and of 128-key K and V tiles gathered page by
 //               page through the block table (2-D boxes, 128-byte swizzle) into a 5-slot ring
@@ -22,6 +22,11 @@
 //               works, the tensor core runs the other tile's MMAs.  O_X is rescaled in TMEM only
 //               when a row's running max grows by more than 2^8 (otherwise the stale max is kept,
 //               which is exact because O and the row sum share it).  Epilogue: O / l from TMEM.
+//               Warps 0..3 are also the math warps of decode-path tasks;
+//   warp 10     second producer of the decode ring; warp 11 claims tasks under the dynamic deal.
+// Registers: the CTA is launched with 168 per thread; the softmax warpgroups raise theirs to 200
+// and the producer / MMA / scheduler warpgroup lowers its own to 104 (setmaxnreg), so that the
+// softmax and decode-path code runs without spills.
 // TMEM: S_A = columns [0,128), S_B = [128,256), O_A = [256,384), O_B = [384,512).
 
 #include <cuda.h>
@@ -52,7 +57,13 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDecProducerWarp = 10;   // second producer of the decode ring (odd stages)
 constexpr int kSchedWarp = 11;         // dynamic deal only: claims tasks into the CTA's queue
-constexpr int kThreads = 11 * 32;      // + the scheduler warp with the dynamic deal
+constexpr int kThreads = 12 * 32;      // (the scheduler warp idles under the static deals)
+// Registers per thread: launched with kLaunchRegs each, the softmax warpgroups (warps 0..7) raise
+// theirs to kRegsSoftmax and the producer / MMA / scheduler warpgroup (8..11) lowers its own to
+// kRegsControl; the budgets must fit in what the CTA was launched with.
+constexpr int kLaunchRegs = (65536 / kThreads) & ~7;
+constexpr uint32_t kRegsSoftmax = 200, kRegsControl = 104;
+static_assert(2 * kRegsSoftmax + kRegsControl <= 3 * kLaunchRegs, "register split");
 constexpr int kQueueReaders = 11;      // every warp but the scheduler reads every queue entry
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 columns
 constexpr int kTileBytes = 2 * kHalfBytes;      // one Q, K or V tile: [half][128 rows][128 B]
@@ -101,7 +112,7 @@ __device__ __forceinline__ bool tile_ok(const TaskInfo &f, const AttnParams &p) 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 template <bool DYN>
-__global__ void __launch_bounds__(kThreads + (DYN ? 32 : 0), 1)
+__global__ void __launch_bounds__(kThreads, 1)
     meta_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                           const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_d,
                           const __grid_constant__ CUtensorMap vmap_d, const AttnParams p) {
@@ -172,6 +183,9 @@ __global__ void __launch_bounds__(kThreads + (DYN ? 32 : 0), 1)
     const int BRt = p.bs < kTileKeys ? p.bs : kTileKeys;  // keys per K/V box
     const int qt_tokens = 128 / p.G;                      // tokens per query tile
 
+    // Each warpgroup sets its register budget once, at the head of its roles' code.
+    if (warp >= kProducerWarp) {
+    xy::setmaxnreg_dec<kRegsControl>();
     if (warp == kProducerWarp) {
         // ---------------------------------- producer ----------------------------------
         if (lane == 0) {
@@ -515,7 +529,9 @@ __global__ void __launch_bounds__(kThreads + (DYN ? 32 : 0), 1)
                 *abort_flag = 1;
             }
         }
-    } else if (warp < 8) {
+    }
+    } else {
+        xy::setmaxnreg_inc<kRegsSoftmax>();
         // ---------------------------------- softmax ----------------------------------
         const int x = warp >> 2;                            // query tile of this group
         const int trow = (warp & 3) * 32 + lane;            // row within the tile = TMEM lane
@@ -871,10 +887,19 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
         const cudaError_t e = cudaFuncSetAttribute(dyn ? meta_attention_kernel<true> : meta_attention_kernel<false>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "meta_attention_kernel smem attribute");
+        // the warpgroups' register budgets assume the kernel is launched with kLaunchRegs per thread
+        cudaFuncAttributes fa;
+        const cudaError_t ea =
+            cudaFuncGetAttributes(&fa, dyn ? meta_attention_kernel<true> : meta_attention_kernel<false>);
+        if (ea != cudaSuccess) return cuda_fail(ea, "meta_attention_kernel attributes");
+        if (fa.numRegs != kLaunchRegs) {
+            set_last_error("meta_attention_kernel", "unexpected register count at launch");
+            return XY_ERR_UNSUPPORTED;
+        }
         configured_device[dyn] = dev;
     }
     if (dyn)
-        meta_attention_kernel<true><<<num_ctas, kThreads + 32, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
+        meta_attention_kernel<true><<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
     else
         meta_attention_kernel<false><<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
     const cudaError_t e = cudaGetLastError();
