@@ -187,6 +187,82 @@ def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None, kv="bf16"):
     return spent, work(sub, kv), desc
 
 
+def oracle_sample_cores(wl, vals, rate, key, kv="bf16", per_core_s=6.0, max_bytes=1.5e9):
+    """The oracle on all host cores: one single-threaded process per core (`python -m
+    oracle.timing`), each running its share of a seeded sample of whole sequences.  The sample is
+    sized from the single-core rate (`rate`: units of work[key] per second) to about `per_core_s` seconds
+    per core, and holds at most `max_bytes` of page data.  Returns (throughput, cores, desc) with
+    throughput = sampled work / the slowest process's oracle seconds."""
+    import tempfile
+    cores = len(os.sched_getaffinity(0))
+
+    def bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    import oracle
+    bt = oracle.allocate_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
+    order = np.random.default_rng(1).permutation(wl.num_seqs)
+    unit_work = lambda i: work(workloads.custom(wl.q_lens[[i]], wl.context_lens[[i]], wl.num_heads_q,  # noqa: E731
+                                                wl.num_heads_kv, wl.head_dim, wl.block_size, wl.causal), kv)
+    chosen, t_pred, nbytes = [], 0.0, 0
+    for i in order:
+        i = int(i)
+        w_i = unit_work(i)
+        b_i = int((bt[i] >= 0).sum()) * 2 * wl.num_heads_kv * wl.block_size * wl.head_dim * 2
+        if chosen and (t_pred + w_i[key] / rate > per_core_s * cores or nbytes + b_i > max_bytes):
+            break
+        chosen.append(i)
+        t_pred += w_i[key] / rate
+        nbytes += b_i
+    # longest first to the least-loaded process
+    loads = [0.0] * cores
+    parts = [[] for _ in range(cores)]
+    for i in sorted(chosen, key=lambda i: -unit_work(i)[key]):
+        c = loads.index(min(loads))
+        parts[c].append(i)
+        loads[c] += unit_work(i)[key]
+    q_all, kn_all, vn_all = bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"])
+    cu = wl.cu_seqlens_q
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               PYTHONPATH=ROOT + os.pathsep + os.environ.get("PYTHONPATH", ""))
+    with tempfile.TemporaryDirectory() as tmp:
+        procs = []
+        for c, part in enumerate(parts):
+            if not part:
+                continue
+            arrs = {"n": len(part), "kv": kv, "bs": wl.block_size, "mb": wl.max_blocks, "scale": wl.scale,
+                    "causal": int(wl.causal)}
+            for k, i in enumerate(part):
+                pages = bt[i][bt[i] >= 0]
+                idx = torch.from_numpy(pages).long().to(vals["k_pool"].device)
+                t0, t1 = int(cu[i]), int(cu[i + 1])
+                arrs.update({f"cu_{k}": np.array([0, t1 - t0], np.int32), f"ctx_{k}": wl.context_lens[i:i + 1],
+                             f"pages_{k}": pages, f"q_{k}": q_all[t0:t1], f"kn_{k}": kn_all[t0:t1],
+                             f"vn_{k}": vn_all[t0:t1], f"kp_{k}": bits(vals["k_pool"].index_select(0, idx)),
+                             f"vp_{k}": bits(vals["v_pool"].index_select(0, idx))})
+            path = os.path.join(tmp, f"part{c}.npz")
+            np.savez(path, **arrs)
+            procs.append(subprocess.Popen([sys.executable, "-m", "oracle.timing", path], cwd=ROOT, env=env,
+                                          stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True))
+        secs = []
+        for pr in procs:
+            try:
+                out, err = pr.communicate(timeout=300)
+            except subprocess.TimeoutExpired:
+                pr.kill()
+                pr.communicate()
+                raise RuntimeError("an oracle timing process ran past 300 s")
+            if pr.returncode != 0:
+                raise RuntimeError("oracle timing process failed: " + err[-500:])
+            secs.append(json.loads(out.strip().splitlines()[-1])["seconds"])
+    sub = workloads.custom(wl.q_lens[chosen], wl.context_lens[chosen], wl.num_heads_q, wl.num_heads_kv,
+                           wl.head_dim, wl.block_size, wl.causal)
+    desc = (f"{len(chosen)} of {wl.num_seqs} sequences (seeded random order), every row, full oracle step, "
+            f"spread longest-first over {len([p for p in parts if p])} single-threaded processes; time = the "
+            f"slowest process's oracle seconds")
+    return sub, max(secs), cores, desc
+
+
 def unit_of(config):
     return ("TFLOP/s", "tensor") if config == "prefill" else ("GB/s", "hbm")
 
@@ -490,6 +566,11 @@ def main():
         secs, sw, desc = oracle_sample(wl, vals, budget_s=12.0, kv=args.kv)
         cpu = {"value": throughput(args.config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
                "sample": desc}
+        # the same oracle on every host core (one single-threaded process per core)
+        key = "flops" if args.config == "prefill" else "attn_bytes"
+        sub, secs_all, ncores, desc_all = oracle_sample_cores(wl, vals, sw[key] / secs, key, kv=args.kv)
+        cpu["all_cores"] = {"value": throughput(args.config, work(sub, args.kv), secs_all), "unit": unit,
+                            "cores": ncores, "kind": "oracle", "sample": desc_all}
 
     clocks = clk.summary(w0, w1)
     if clocks["samples"] == 0:  # the timed region was shorter than one sampling period
