@@ -164,7 +164,7 @@ def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None, kv="bf16"):
     rng = np.random.default_rng(0)
     order = rng.permutation(wl.num_seqs)
     cu = wl.cu_seqlens_q
-    spent, done = 0.0, []
+    spent, done, per_seq = 0.0, [], []
     q_all, kn_all, vn_all = bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"])
     for i in order:
         if spent >= budget_s or (max_seqs and len(done) >= max_seqs):
@@ -179,20 +179,20 @@ def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None, kv="bf16"):
         run = oracle.step.run_step_fp8 if kv == "fp8" else oracle.step.run_step
         run(sub_cu, wl.context_lens[i:i + 1], pages, wl.block_size, wl.max_blocks, q_all[t0:t1], kn_all[t0:t1],
             vn_all[t0:t1], kp, vp, wl.scale, wl.causal, pool_pages=pages)
-        spent += time.perf_counter() - t
+        per_seq.append(time.perf_counter() - t)
+        spent += per_seq[-1]
         done.append(i)
     sub = workloads.custom(wl.q_lens[done], wl.context_lens[done], wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
                            wl.block_size, wl.causal)
     desc = f"{len(done)} of {wl.num_seqs} sequences (seeded random order), every row, full oracle step"
-    return spent, work(sub, kv), desc
+    return spent, work(sub, kv), desc, done, per_seq
 
 
-def oracle_sample_cores(wl, vals, rate, key, kv="bf16", per_core_s=6.0, max_bytes=1.5e9):
+def oracle_sample_cores(wl, vals, seqs, seq_secs, kv="bf16"):
     """The oracle on all host cores: one single-threaded process per core (`python -m
-    oracle.timing`), each running its share of a seeded sample of whole sequences.  The sample is
-    sized from the single-core rate (`rate`: units of work[key] per second) to about `per_core_s` seconds
-    per core, and holds at most `max_bytes` of page data.  Returns (throughput, cores, desc) with
-    throughput = sampled work / the slowest process's oracle seconds."""
+    oracle.timing`), the sequences of the single-core sample (`seqs`, whose single-core oracle
+    seconds are `seq_secs`) dealt longest-first to the least-loaded process.  Returns (the sampled
+    workload, the slowest process's oracle seconds, cores, description)."""
     import tempfile
     cores = len(os.sched_getaffinity(0))
 
@@ -201,26 +201,13 @@ def oracle_sample_cores(wl, vals, rate, key, kv="bf16", per_core_s=6.0, max_byte
 
     import oracle
     bt = oracle.allocate_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
-    order = np.random.default_rng(1).permutation(wl.num_seqs)
-    unit_work = lambda i: work(workloads.custom(wl.q_lens[[i]], wl.context_lens[[i]], wl.num_heads_q,  # noqa: E731
-                                                wl.num_heads_kv, wl.head_dim, wl.block_size, wl.causal), kv)
-    chosen, t_pred, nbytes = [], 0.0, 0
-    for i in order:
-        i = int(i)
-        w_i = unit_work(i)
-        b_i = int((bt[i] >= 0).sum()) * 2 * wl.num_heads_kv * wl.block_size * wl.head_dim * 2
-        if chosen and (t_pred + w_i[key] / rate > per_core_s * cores or nbytes + b_i > max_bytes):
-            break
-        chosen.append(i)
-        t_pred += w_i[key] / rate
-        nbytes += b_i
-    # longest first to the least-loaded process
+    chosen = list(seqs)
     loads = [0.0] * cores
     parts = [[] for _ in range(cores)]
-    for i in sorted(chosen, key=lambda i: -unit_work(i)[key]):
+    for i, sec in sorted(zip(seqs, seq_secs), key=lambda x: -x[1]):
         c = loads.index(min(loads))
         parts[c].append(i)
-        loads[c] += unit_work(i)[key]
+        loads[c] += sec
     q_all, kn_all, vn_all = bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"])
     cu = wl.cu_seqlens_q
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
@@ -257,9 +244,9 @@ def oracle_sample_cores(wl, vals, rate, key, kv="bf16", per_core_s=6.0, max_byte
             secs.append(json.loads(out.strip().splitlines()[-1])["seconds"])
     sub = workloads.custom(wl.q_lens[chosen], wl.context_lens[chosen], wl.num_heads_q, wl.num_heads_kv,
                            wl.head_dim, wl.block_size, wl.causal)
-    desc = (f"{len(chosen)} of {wl.num_seqs} sequences (seeded random order), every row, full oracle step, "
-            f"spread longest-first over {len([p for p in parts if p])} single-threaded processes; time = the "
-            f"slowest process's oracle seconds")
+    desc = (f"the single-core sample's {len(chosen)} sequences, dealt longest-first (by their single-core "
+            f"time) over {len([p for p in parts if p])} single-threaded processes; time = the slowest process's "
+            f"oracle seconds")
     return sub, max(secs), cores, desc
 
 
@@ -319,7 +306,7 @@ def run_reference(args, rank, world):
     unit, _ = unit_of(args.config)
     times = []
     for k in range(args.warmup + args.steps):
-        secs, w, desc = oracle_sample(wl, vals, budget_s=args.ref_budget, kv=args.kv)
+        secs, w, desc, _, _ = oracle_sample(wl, vals, budget_s=args.ref_budget, kv=args.kv)
         if k >= args.warmup:
             times.append((secs, w))
     secs = sum(t for t, _ in times)
@@ -561,14 +548,27 @@ def main():
     e2e_s = max_over_ranks(sum(e2e_times[args.warmup:]) / args.steps, world, device=dev)
     e2e_val = job_throughput(args.config, w, e2e_s, world)
 
+    # the task-table build alone (host, into preallocated record arrays), as a step re-plans it
+    tt_us = None
+    if not split:
+        cap_t = np.zeros((int(pl.tasks.shape[0]) + 8, 8), np.int32)
+        cap_m = np.zeros((max(1, int(pl.merges.shape[0])) + 8, 8), np.int32)
+        tt = []
+        for _ in range(25):
+            t0 = time.perf_counter()
+            xy.xy_build_task_table(wl.cu_seqlens_q, wl.context_lens, wl.num_heads_q, wl.num_heads_kv, wl.head_dim,
+                                   wl.causal, pl.num_ctas, pl.q_tile, pl.kv_chunk, pl.schedule, tasks_out=cap_t,
+                                   merges_out=cap_m)
+            tt.append(time.perf_counter() - t0)
+        tt_us = 1e6 * statistics.median(tt[5:])
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, sw, desc = oracle_sample(wl, vals, budget_s=12.0, kv=args.kv)
+        secs, sw, desc, seqs, seq_secs = oracle_sample(wl, vals, budget_s=12.0, kv=args.kv)
         cpu = {"value": throughput(args.config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
                "sample": desc}
-        # the same oracle on every host core (one single-threaded process per core)
-        key = "flops" if args.config == "prefill" else "attn_bytes"
-        sub, secs_all, ncores, desc_all = oracle_sample_cores(wl, vals, sw[key] / secs, key, kv=args.kv)
+        # the same sample on every host core (one single-threaded process per core)
+        sub, secs_all, ncores, desc_all = oracle_sample_cores(wl, vals, seqs, seq_secs, kv=args.kv)
         cpu["all_cores"] = {"value": throughput(args.config, work(sub, args.kv), secs_all), "unit": unit,
                             "cores": ncores, "kind": "oracle", "sample": desc_all}
 
@@ -600,7 +600,8 @@ def main():
                     "ms_per_step": e2e_s * 1e3,
                     "loop": "per step: inputs H2D, step, output D2H, sync; tables re-planned every step, the next "
                             "step's on the host while this one runs",
-                    "plan_us": 1e6 * statistics.median(plan_times[args.warmup:])},
+                    "plan_us": 1e6 * statistics.median(plan_times[args.warmup:]),
+                    "task_table_us": tt_us},
             "gpu_launches": n_launch_per_step * args.steps,
             "clocks": clocks,
         }

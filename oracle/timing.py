@@ -24,12 +24,12 @@ def run_file(path):
     n = int(d["n"])
     run = step.run_step_fp8 if str(d["kv"]) == "fp8" else step.run_step
     spent = 0.0
+    bs, mb, scale, causal = int(d["bs"]), int(d["mb"]), float(d["scale"]), bool(d["causal"])
     for k in range(n):
-        g = lambda name: d[f"{name}_{k}"]  # noqa: E731
-        pages = g("pages")
+        a = {name: np.array(d[f"{name}_{k}"]) for name in ("cu", "ctx", "pages", "q", "kn", "vn", "kp", "vp")}
         t = time.perf_counter()
-        run(g("cu"), g("ctx"), pages, int(d["bs"]), int(d["mb"]), g("q"), g("kn"), g("vn"), g("kp"), g("vp"),
-            float(d["scale"]), bool(d["causal"]), pool_pages=pages)
+        run(a["cu"], a["ctx"], a["pages"], bs, mb, a["q"], a["kn"], a["vn"], a["kp"], a["vp"], scale, causal,
+            pool_pages=a["pages"])
         spent += time.perf_counter() - t
     return {"seconds": spent, "seqs": n}
 

@@ -133,6 +133,22 @@ def test_static_table_with_holes_through_the_dynamic_call():
     assert np.abs(got - r_ref["ref"]["out"]).max() <= 2e-2
 
 
+@pytest.mark.parametrize("G", [1, 4, 8])
+def test_verify_shaped_queries(G):
+    # speculative-verify batches: 2..8 new tokens per sequence over long contexts
+    rng = np.random.default_rng(80 + G)
+    q = rng.integers(2, 9, size=24)
+    ctx = q + rng.integers(500, 6000, size=24)
+    wl = workloads.custom(q, ctx, 4 * G, 4, 128, 16, True, seed=90 + G, name="verify")
+    assert_parity(run(wl, schedule=DYN))
+
+
+def test_nan_in_unused_slots_never_reaches_outputs():
+    wl = workloads.custom([5, 37, 64, 70], [5, 37, 64, 70], 4, 2, 128, 16, seed=33)
+    assert_parity(run(wl, pool_fill=float("nan"), schedule=DYN), check_pages=False)
+    assert_parity(run(wl, pool_fill=float("nan"), kv_chunk=128, schedule=DYN), check_pages=False)
+
+
 def test_full_size_decode_sampled():
     wl = workloads.decode()
     rng = np.random.default_rng(10)

@@ -78,7 +78,7 @@ def test_verify_shaped_queries(G):
     assert_parity(run(wl))
 
 
-@pytest.mark.parametrize("schedule", [0, 1, 2, 3])
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4])
 def test_kind_switches_in_one_launch(schedule):
     # short decode tasks (one or two 64-key stages) interleaved with chunk tiles on few CTAs, so
     # every CTA switches between the decode path and the tile path many times in one launch
