@@ -509,10 +509,13 @@ def main():
     planner = xystep.Planner(wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.block_size, wl.max_blocks, wl.causal,
                              device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8, schedule=args.schedule)
 
+    split_planner = (xystep.Fp8SplitPlanner(wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.block_size,
+                                            wl.max_blocks, wl.causal, device=dev, num_ctas=pl.num_ctas)
+                     if split else None)
+
     def make_batch():
         if split:
-            return xystep.Fp8SplitBatch(meta["cu"], meta["ctx"], meta["free"], wl.block_size, wl.max_blocks,
-                                        wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev)
+            return split_planner.plan(meta["cu"], meta["ctx"], meta["free"])
         return planner.plan(meta["cu"], meta["ctx"], meta["free"])
 
     e2e_times, plan_times = [], []
@@ -542,8 +545,7 @@ def main():
         torch.cuda.synchronize()
         e2e_times.append(time.perf_counter() - t0)
         if k == 0:
-            h2d = sum(host[x].numel() * 2 for x in host) + (planner.last_upload_bytes if not split else sum(
-                t.numel() * t.element_size() for t in (b2.cu, b2.ctx, b2.block_table)))
+            h2d = sum(host[x].numel() * 2 for x in host) + (split_planner if split else planner).last_upload_bytes
             d2h = out_host.numel() * 2
     e2e_s = max_over_ranks(sum(e2e_times[args.warmup:]) / args.steps, world, device=dev)
     e2e_val = job_throughput(args.config, w, e2e_s, world)

@@ -4,7 +4,8 @@ KV append and paged attention (device).  Composition of libxy calls only; no ari
 import numpy as np
 import torch
 
-from . import (XY_SCHEDULE_DYNAMIC, Plan, check_err_word, default_schedule, default_tiles, xy_build_block_table, xy_build_step_tables, xy_default_num_ctas,
+from . import (XY_SCHEDULE_DYNAMIC, XY_SCHEDULE_GREEDY, Plan, check_err_word, default_schedule, default_tiles,
+               xy_build_block_table, xy_build_step_tables, xy_build_task_table, xy_default_num_ctas,
                xy_dequant_pages_fp8, xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_dynamic,
                xy_paged_attention_fp8, xy_slot_mapping)
 
@@ -337,6 +338,150 @@ class Fp8SplitBatch:
             t["k"] = torch.empty(len(pages), num_heads_kv, block_size, head_dim, dtype=torch.bfloat16, device=dev)
             t["v"] = torch.empty_like(t["k"])
             self.tile = t
+
+
+class _Part:
+    """The plan of one part of a split batch (the fields the attention calls read from Plan)."""
+
+    def __init__(self, tasks, merges, num_ctas, workspace, schedule, task_counter):
+        self.tasks, self.merges, self.num_ctas, self.workspace = tasks, merges, num_ctas, workspace
+        self.schedule, self.task_counter = schedule, task_counter
+        self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
+
+
+class Fp8SplitPlanner:
+    """Reusable builder of Fp8SplitBatch-shaped batches for one stream, for a serving loop that
+    re-plans every step over 8-bit pages: the host tables of both parts (block table, the tile
+    part's compact page list and block table over the copies, both task and merge tables, the
+    lengths and a zeroed error word) are packed into one pinned staging buffer and reach the
+    device in one copy; the device buffer, the split-KV workspaces, the slot buffer and the bf16
+    page-copy buffers are kept between steps and grown when a batch needs more.  plan() returns a
+    batch for run_step_fp8_split / attention_fp8_split, valid until the next plan()."""
+
+    _ALIGN = 256
+
+    def __init__(self, num_heads_q, num_heads_kv, head_dim, block_size, max_blocks, causal, device="cuda",
+                 num_ctas=None):
+        G = num_heads_q // num_heads_kv
+        if head_dim != 128 or 128 % G:
+            raise ValueError("the split path needs head_dim 128 and G dividing 128")
+        self.dev = torch.device(device)
+        self.Hq, self.Hkv, self.d, self.bs, self.MB, self.causal = (num_heads_q, num_heads_kv, head_dim, block_size,
+                                                                   max_blocks, causal)
+        self.num_ctas = num_ctas or xy_default_num_ctas(self.dev.index or 0)
+        self._host = None
+        self._dev_buf = None
+        self._ws = [torch.empty(16, dtype=torch.uint8, device=self.dev) for _ in range(2)]
+        self._slots = torch.empty(1, dtype=torch.int64, device=self.dev)
+        self._copies = None
+        self._counter = torch.zeros(2, dtype=torch.int32, device=self.dev)  # tile part: dynamic deal
+        self._copied = torch.cuda.Event() if self.dev.type == "cuda" else None
+        self._pending = False
+
+    def _wait_upload(self):
+        if self._pending:
+            self._copied.synchronize()   # the previous upload has left the staging buffer
+            self._pending = False
+
+    def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
+        cu = np.asarray(cu_seqlens_q, dtype=np.int32)
+        ctx = np.asarray(context_lens, dtype=np.int32)
+        q_lens = cu[1:] - cu[:-1]
+        rng = split_ranges(q_lens)
+        if rng is None:
+            raise ValueError("batch cannot be split into a decode range and a tile range")
+        (ta, tb), (da, db) = rng
+        S, MB, bs = len(ctx), self.MB, self.bs
+        bt, pages_used = xy_build_block_table(ctx, bs, free_list, MB)
+        arrays = {"err": np.zeros(1, np.int32), "cu": cu, "ctx": ctx, "bt": bt}
+        parts = {}
+        if tb > ta:
+            cu_t = (cu[ta:tb + 1] - cu[ta]).astype(np.int32)
+            q_tile, kv_chunk = default_tiles(self.Hq, self.Hkv, self.d)
+            r = xy_build_task_table(cu_t, ctx[ta:tb], self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, q_tile,
+                                    kv_chunk, XY_SCHEDULE_DYNAMIC)
+            n = (ctx[ta:tb].astype(np.int64) + bs - 1) // bs
+            pages = np.concatenate([bt[i][:k] for i, k in zip(range(ta, tb), n)]).astype(np.int32)
+            base = np.concatenate([[0], np.cumsum(n)[:-1]])
+            bt_t = -np.ones((tb - ta, MB), dtype=np.int32)
+            for row, (b0, k) in enumerate(zip(base, n)):
+                bt_t[row, :k] = np.arange(b0, b0 + k, dtype=np.int32)
+            arrays.update(cu_t=cu_t, tasks_t=r["tasks"], merges_t=r["merges"], pages_t=pages, bt_t=bt_t)
+            parts["tile"] = (ta, tb, r)
+        if db > da:
+            cu_d = (cu[da:db + 1] - cu[da]).astype(np.int32)
+            T_d = int(cu[db] - cu[da])
+            q_tile, kv_chunk = default_tiles(self.Hq, self.Hkv, self.d, True, pure_decode=T_d == db - da)
+            r = xy_build_task_table(cu_d, ctx[da:db], self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, q_tile,
+                                    kv_chunk, XY_SCHEDULE_GREEDY)
+            arrays.update(cu_d=cu_d, tasks_d=r["tasks"], merges_d=r["merges"])
+            parts["decode"] = (da, db, r)
+        # pack at 256-byte offsets into the pinned staging buffer, one copy to the device
+        off, total = {}, 0
+        for k, a in arrays.items():
+            off[k] = total
+            total += (a.nbytes + self._ALIGN - 1) // self._ALIGN * self._ALIGN
+        self._wait_upload()
+        if self._host is None or self._host.numel() < total:
+            size = max(total, 2 * (self._host.numel() if self._host is not None else 0), 1 << 16)
+            self._host = torch.empty(size, dtype=torch.uint8).pin_memory()
+            self._host_np = self._host.numpy()
+            self._dev_buf = torch.empty(size, dtype=torch.uint8, device=self.dev)
+        for k, a in arrays.items():
+            self._host_np[off[k]:off[k] + a.nbytes] = a.reshape(-1).view(np.uint8)
+        stm = torch.cuda.current_stream(self.dev) if stream is None else stream
+        with torch.cuda.stream(stm):
+            self._dev_buf[:total].copy_(self._host[:total], non_blocking=True)
+        self._copied.record(stm)
+        self._pending = True
+        self.last_upload_bytes = total
+
+        def dv(k, shape):
+            n_el = int(np.prod(shape))
+            return self._dev_buf[off[k]:off[k] + 4 * n_el].view(torch.int32).view(*shape)
+
+        b = _SplitBatch()
+        b.cu_host, b.ctx_host, b.block_table_host, b.pages_used = cu, ctx, bt, pages_used
+        b.cu, b.ctx, b.block_table, b.err = dv("cu", (S + 1,)), dv("ctx", (S,)), dv("bt", (S, MB)), dv("err", (1,))
+        T = int(cu[-1])
+        if self._slots.numel() < T:
+            self._slots = torch.empty(max(T, 2 * self._slots.numel()), dtype=torch.int64, device=self.dev)
+        b.slots = self._slots[:T]
+        b.block_size, b.causal, b.Hkv, b.d = bs, self.causal, self.Hkv, self.d
+        b.tile = b.decode = None
+
+        def ws(i, nbytes):
+            if self._ws[i].numel() < nbytes:
+                self._ws[i] = torch.empty(max(nbytes, 2 * self._ws[i].numel()), dtype=torch.uint8, device=self.dev)
+            return self._ws[i]
+
+        if "tile" in parts:
+            a, bnd, r = parts["tile"]
+            n_t, m_t = len(r["tasks"]), len(r["merges"])
+            plan = _Part(dv("tasks_t", (n_t, 8)), dv("merges_t", (m_t, 8)), self.num_ctas,
+                         ws(0, r["workspace_bytes"]), XY_SCHEDULE_DYNAMIC, self._counter)
+            n_pages = len(arrays["pages_t"])
+            need = n_pages * self.Hkv * bs * self.d
+            if self._copies is None or self._copies[0].numel() < need:
+                self._copies = [torch.empty(max(need, 2 * (self._copies[0].numel() if self._copies else 0)),
+                                            dtype=torch.bfloat16, device=self.dev) for _ in range(2)]
+            b.tile = dict(seq=(a, bnd), tok=(int(cu[a]), int(cu[bnd])), cu=dv("cu_t", (bnd - a + 1,)),
+                          ctx=b.ctx[a:bnd], plan=plan, pages=dv("pages_t", (n_pages,)),
+                          bt=dv("bt_t", (bnd - a, MB)),
+                          k=self._copies[0][:need].view(n_pages, self.Hkv, bs, self.d),
+                          v=self._copies[1][:need].view(n_pages, self.Hkv, bs, self.d))
+        if "decode" in parts:
+            a, bnd, r = parts["decode"]
+            n_d, m_d = len(r["tasks"]), len(r["merges"])
+            plan = _Part(dv("tasks_d", (n_d, 8)), dv("merges_d", (m_d, 8)), self.num_ctas,
+                         ws(1, r["workspace_bytes"]), XY_SCHEDULE_GREEDY, None)
+            b.decode = dict(seq=(a, bnd), tok=(int(cu[a]), int(cu[bnd])), cu=dv("cu_d", (bnd - a + 1,)),
+                            ctx=b.ctx[a:bnd], plan=plan)
+        return b
+
+
+class _SplitBatch:
+    """A batch of Fp8SplitPlanner.plan(): the attributes of Fp8SplitBatch."""
 
 
 def run_step_fp8_split(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, scale, out=None, stream=None):

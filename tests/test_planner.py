@@ -110,3 +110,55 @@ def test_planner_fp8_run_matches_run_step_fp8():
         res.append((bits(out), codes[0].cpu(), scl[1].cpu()))
     assert np.array_equal(res[0][0], res[1][0])
     assert torch.equal(res[0][1], res[1][1]) and torch.equal(res[0][2], res[1][2])
+
+
+def test_split_planner_matches_fp8_split_batch_across_batches():
+    # over 8-bit pages: the packed-upload split planner gives the tables and the outputs of
+    # Fp8SplitBatch, bit for bit, for batches of different sizes planned by one planner
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    import paged_kv_varlen_xy_gb300 as xy
+    dev = torch.device("cuda")
+    shapes = [([40, 1, 1], [300, 700, 33]), ([300, 17, 1, 1, 1, 1], [900, 3000, 40, 9000, 1, 64]),
+              ([64, 1], [64, 5])]
+    MB = 600  # one block-table width for every batch of the planner (>= 9000 / 16)
+    planner = xystep.Fp8SplitPlanner(8, 2, 128, 16, MB, True, device=dev, num_ctas=37)
+    for k, (ql, cl) in enumerate(shapes):
+        wl = workloads.custom(ql, cl, 8, 2, 128, 16, True, seed=200 + k, name="split")
+        vals = wl.tensors(dev)
+        P, Hkv, bs, d = vals["k_pool"].shape
+        codes = [torch.zeros(P, Hkv, bs, d, dtype=torch.uint8, device=dev) for _ in range(2)]
+        scales = [torch.zeros(P, Hkv, bs, dtype=torch.float32, device=dev) for _ in range(2)]
+        rows = [vals[n].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous() for n in ("k_pool", "v_pool")]
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        xy.xy_kv_append_fp8(rows[0], rows[1], torch.arange(P * bs, dtype=torch.int64, device=dev), codes[0],
+                            codes[1], scales[0], scales[1], err)
+        outs, batches = [], []
+        for use_planner in (False, True):
+            cc = [c.clone() for c in codes]
+            ss = [x.clone() for x in scales]
+            if use_planner:
+                b = planner.plan(wl.cu_seqlens_q, wl.context_lens, wl.free_list)
+            else:
+                b = xystep.Fp8SplitBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, MB,
+                                         wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
+                                         num_ctas=37)
+            out = xystep.run_step_fp8_split(b, vals["q"], vals["k_new"], vals["v_new"], cc[0], cc[1], ss[0], ss[1],
+                                            wl.scale)
+            torch.cuda.synchronize()
+            xystep.check(b)
+            outs.append(bits(out))
+            batches.append(b)
+        b0, b1 = batches
+        assert np.array_equal(b0.block_table.cpu().numpy(), b1.block_table.cpu().numpy())
+        for part in ("tile", "decode"):
+            p0, p1 = getattr(b0, part), getattr(b1, part)
+            assert (p0 is None) == (p1 is None)
+            if p0 is not None:
+                assert np.array_equal(p0["plan"].tasks.cpu().numpy(), p1["plan"].tasks.cpu().numpy())
+                assert np.array_equal(p0["plan"].merges.cpu().numpy(), p1["plan"].merges.cpu().numpy())
+        assert np.array_equal(outs[0], outs[1])
+        ref = oracle.step.run_step_fp8(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, MB,
+                                       bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"]), bits(vals["k_pool"]),
+                                       bits(vals["v_pool"]), wl.scale, wl.causal)
+        diff = np.abs(oracle.bf16_bits_to_f64(outs[1]) - ref["out"])
+        assert diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS
