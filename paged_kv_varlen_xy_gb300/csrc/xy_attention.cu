@@ -342,14 +342,14 @@ template <int HD, int KIND, bool DYN>
 xy_status launch_attention_kernel(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
                                   cudaStream_t st) {
     using C = Cfg<HD, KIND, DYN>;
-    static int configured_device = -1;
+    static xy::PerDeviceOnce configured;  // the attribute is per device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return XY_ERR_CUDA;
-    if (configured_device != dev) {  // the attribute is per device
-        if (cudaFuncSetAttribute(paged_attention_kernel<HD, KIND, DYN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::kSmemBytes) != cudaSuccess)
-            return XY_ERR_CUDA;
-        configured_device = dev;
+    if (!configured.done(dev)) {
+        const cudaError_t e = cudaFuncSetAttribute(paged_attention_kernel<HD, KIND, DYN>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel smem attribute");
+        configured.mark(dev);
     }
     paged_attention_kernel<HD, KIND, DYN><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
     const cudaError_t e = cudaGetLastError();

@@ -274,6 +274,18 @@ __host__ __device__ __forceinline__ bool is_tile_task(const xy_task &t, int G, i
     return tile_shape_ok(G, head_dim) && t.q_rows * G > XY_TILE_MIN_ROWS;
 }
 
+// Per-device "done" marks for once-per-device kernel setup (function attributes are set per
+// device): bit d of the word is device d's (devices past 63 set up on every call).
+struct PerDeviceOnce {
+    unsigned long long bits = 0;
+    __host__ bool done(int dev) const {
+        return dev >= 0 && dev < 64 && (__atomic_load_n(&bits, __ATOMIC_ACQUIRE) >> dev & 1ull);
+    }
+    __host__ void mark(int dev) {
+        if (dev >= 0 && dev < 64) __atomic_fetch_or(&bits, 1ull << dev, __ATOMIC_RELEASE);
+    }
+};
+
 // Records a CUDA error for xy_last_error_string() and returns XY_ERR_CUDA.
 xy_status cuda_fail(cudaError_t e, const char *what);
 

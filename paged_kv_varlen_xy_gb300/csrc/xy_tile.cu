@@ -879,11 +879,11 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return XY_ERR_CUDA;
-    static int configured_device[2] = {-1, -1};  // per instantiation
+    static PerDeviceOnce configured[2];  // per instantiation and device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
     const int dyn = p.dyn ? 1 : 0;
-    if (configured_device[dyn] != dev) {
+    if (!configured[dyn].done(dev)) {
         const cudaError_t e = cudaFuncSetAttribute(dyn ? meta_attention_kernel<true> : meta_attention_kernel<false>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return cuda_fail(e, "meta_attention_kernel smem attribute");
@@ -896,7 +896,7 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
             set_last_error("meta_attention_kernel", "unexpected register count at launch");
             return XY_ERR_UNSUPPORTED;
         }
-        configured_device[dyn] = dev;
+        configured[dyn].mark(dev);
     }
     if (dyn)
         meta_attention_kernel<true><<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
