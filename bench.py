@@ -518,36 +518,75 @@ def main():
             return split_planner.plan(meta["cu"], meta["ctx"], meta["free"])
         return planner.plan(meta["cu"], meta["ctx"], meta["free"])
 
-    e2e_times, plan_times = [], []
-    h2d = d2h = 0
-    b_next = make_batch()
-    for k in range(args.warmup + args.steps):
-        if world > 1 and k == args.warmup:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        b2 = b_next
-        qd = host["q"].to(dev, non_blocking=True)
-        kd = host["k_new"].to(dev, non_blocking=True)
-        vd = host["v_new"].to(dev, non_blocking=True)
+    plan_times = []
+    out_hosts = [out_host, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
+    # inputs go up on one copy stream and outputs come down on another, so that the copy engines
+    # overlap the neighbouring steps' kernels (and each other); two device input buffers and two
+    # pinned output buffers alternate between steps
+    cs_up, cs_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    dev_in = [{x: torch.empty_like(vals[x]) for x in ("q", "k_new", "v_new")} for _ in range(2)]
+    up_ev = [torch.cuda.Event() for _ in range(2)]      # step k's inputs are on the device
+    step_ev = [torch.cuda.Event() for _ in range(2)]    # step k's kernels are done
+    down_ev = [torch.cuda.Event() for _ in range(2)]    # step k's output is in host memory
+    planner_now = split_planner if split else planner
+
+    def upload(k):
+        with torch.cuda.stream(cs_up):
+            if k >= 2:
+                cs_up.wait_event(step_ev[k % 2])   # step k - 2 no longer reads this input buffer
+            for x in ("q", "k_new", "v_new"):
+                dev_in[k % 2][x].copy_(host[x], non_blocking=True)
+            up_ev[k % 2].record(cs_up)
+
+    def launch(k, b):
+        """Step k through the public API on the compute stream, once its inputs are up; its output
+        then comes down on the copy stream."""
+        stream.wait_event(up_ev[k % 2])
+        d = dev_in[k % 2]
         if split:
-            o = xystep.run_step_fp8_split(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], vals["k_scales"],
-                                          vals["v_scales"], wl.scale)
+            o = xystep.run_step_fp8_split(b, d["q"], d["k_new"], d["v_new"], vals["k_codes"], vals["v_codes"],
+                                          vals["k_scales"], vals["v_scales"], wl.scale)
         elif fp8:
-            o = planner.run(b2, qd, kd, vd, vals["k_codes"], vals["v_codes"], wl.scale, k_scales=vals["k_scales"],
-                            v_scales=vals["v_scales"])
+            o = planner.run(b, d["q"], d["k_new"], d["v_new"], vals["k_codes"], vals["v_codes"], wl.scale,
+                            k_scales=vals["k_scales"], v_scales=vals["v_scales"])
         else:
-            o = planner.run(b2, qd, kd, vd, vals["k_pool"], vals["v_pool"], wl.scale)
+            o = planner.run(b, d["q"], d["k_new"], d["v_new"], vals["k_pool"], vals["v_pool"], wl.scale)
+        step_ev[k % 2].record(stream)
+        with torch.cuda.stream(cs_down):
+            cs_down.wait_event(step_ev[k % 2])
+            o.record_stream(cs_down)
+            out_hosts[k % 2].copy_(o, non_blocking=True)
+            down_ev[k % 2].record(cs_down)
+
+    # As a serving loop runs: step k + 1's inputs go up while step k computes, the next step's plan
+    # is built on the host meanwhile, and the host waits for step k - 1's output only after step k
+    # is enqueued (so neither the GPU nor the copy engines wait on the host, and every step's
+    # result reaches the host).
+    total = args.warmup + args.steps
+    b_cur = make_batch()
+    t_start = None
+    for k in range(total):
+        if k == args.warmup:
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            t_start = time.perf_counter()
+        if k == 0 or k == args.warmup:
+            upload(k)   # (the first timed step's inputs go up inside the timed region)
+        launch(k, b_cur)
+        if k + 1 < total and k + 1 != args.warmup:
+            upload(k + 1)
+        planner_now.wait_upload()   # (the planner's own wait, kept out of the planning time)
         tp = time.perf_counter()
-        b_next = make_batch()   # the next step's plan, on the host while this step runs
+        b_cur = make_batch()
         plan_times.append(time.perf_counter() - tp)
-        out_host.copy_(o, non_blocking=True)
-        torch.cuda.synchronize()
-        e2e_times.append(time.perf_counter() - t0)
-        if k == 0:
-            h2d = sum(host[x].numel() * 2 for x in host) + (split_planner if split else planner).last_upload_bytes
-            d2h = out_host.numel() * 2
-    e2e_s = max_over_ranks(sum(e2e_times[args.warmup:]) / args.steps, world, device=dev)
+        if k >= 1:
+            down_ev[(k - 1) % 2].synchronize()   # step k - 1's output is on the host
+    down_ev[(total - 1) % 2].synchronize()
+    e2e_total = time.perf_counter() - t_start
+    h2d = sum(host[x].numel() * 2 for x in host) + planner_now.last_upload_bytes
+    d2h = out_host.numel() * 2
+    e2e_s = max_over_ranks(e2e_total / args.steps, world, device=dev)
     e2e_val = job_throughput(args.config, w, e2e_s, world)
 
     # the task-table build alone (host, into preallocated record arrays), as a step re-plans it
@@ -600,8 +639,10 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_s * 1e3,
-                    "loop": "per step: inputs H2D, step, output D2H, sync; tables re-planned every step, the next "
-                            "step's on the host while this one runs",
+                    "loop": "per step: inputs H2D from pinned memory (upload stream), tables re-planned on the host "
+                            "and uploaded, the step (compute stream), output D2H into pinned memory (download stream); "
+                            "step k+1's inputs go up while step k computes, and the host waits for step k's output "
+                            "after enqueuing step k+1",
                     "plan_us": 1e6 * statistics.median(plan_times[args.warmup:]),
                     "task_table_us": tt_us},
             "gpu_launches": n_launch_per_step * args.steps,

@@ -145,6 +145,11 @@ class Planner:
             self._copied.synchronize()   # the previous upload has left the staging buffer
             self._pending = False
 
+    def wait_upload(self):
+        """Block until the last plan's upload has left the pinned staging buffer (plan() does this
+        first; a caller may do it beforehand to keep the wait out of its own timing)."""
+        self._wait_upload()
+
     def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
         """Build and upload the metadata of one batch; returns a batch for run() (or run_step)."""
         self._ensure(1 << 16)
@@ -382,6 +387,11 @@ class Fp8SplitPlanner:
         if self._pending:
             self._copied.synchronize()   # the previous upload has left the staging buffer
             self._pending = False
+
+    def wait_upload(self):
+        """Block until the last plan's upload has left the pinned staging buffer (plan() does this
+        first; a caller may do it beforehand to keep the wait out of its own timing)."""
+        self._wait_upload()
 
     def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
         cu = np.asarray(cu_seqlens_q, dtype=np.int32)
