@@ -513,10 +513,10 @@ def main():
                                             wl.max_blocks, wl.causal, device=dev, num_ctas=pl.num_ctas)
                      if split else None)
 
-    def make_batch():
+    def make_batch(stream=None):
         if split:
-            return split_planner.plan(meta["cu"], meta["ctx"], meta["free"])
-        return planner.plan(meta["cu"], meta["ctx"], meta["free"])
+            return split_planner.plan(meta["cu"], meta["ctx"], meta["free"], stream=stream)
+        return planner.plan(meta["cu"], meta["ctx"], meta["free"], stream=stream)
 
     plan_times = []
     out_hosts = [out_host, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
@@ -531,16 +531,23 @@ def main():
     planner_now = split_planner if split else planner
 
     def upload(k):
+        """Step k's inputs and its freshly planned tables go up on the upload stream (after step k - 2,
+        which used the same input and table buffers, is done).  Returns step k's batch."""
         with torch.cuda.stream(cs_up):
             if k >= 2:
-                cs_up.wait_event(step_ev[k % 2])   # step k - 2 no longer reads this input buffer
+                cs_up.wait_event(step_ev[k % 2])
             for x in ("q", "k_new", "v_new"):
                 dev_in[k % 2][x].copy_(host[x], non_blocking=True)
-            up_ev[k % 2].record(cs_up)
+        planner_now.wait_upload()   # (the planner's own wait, kept out of the planning time)
+        tp = time.perf_counter()
+        b = make_batch(stream=cs_up)
+        plan_times.append(time.perf_counter() - tp)
+        up_ev[k % 2].record(cs_up)
+        return b
 
     def launch(k, b):
-        """Step k through the public API on the compute stream, once its inputs are up; its output
-        then comes down on the copy stream."""
+        """Step k through the public API on the compute stream, once its inputs and tables are up;
+        its output then comes down on the download stream."""
         stream.wait_event(up_ev[k % 2])
         d = dev_in[k % 2]
         if split:
@@ -558,28 +565,24 @@ def main():
             out_hosts[k % 2].copy_(o, non_blocking=True)
             down_ev[k % 2].record(cs_down)
 
-    # As a serving loop runs: step k + 1's inputs go up while step k computes, the next step's plan
-    # is built on the host meanwhile, and the host waits for step k - 1's output only after step k
-    # is enqueued (so neither the GPU nor the copy engines wait on the host, and every step's
-    # result reaches the host).
+    # As a serving loop runs: step k + 1's inputs and tables (planned on the host meanwhile) go up
+    # while step k computes, step k's output comes down while step k + 1 computes, and the host
+    # waits for step k - 1's output only after step k is enqueued (so the GPU waits neither on the
+    # host nor on a copy, and every step's result reaches the host).
     total = args.warmup + args.steps
-    b_cur = make_batch()
     t_start = None
+    b_next = upload(0)
     for k in range(total):
         if k == args.warmup:
             torch.cuda.synchronize()
             if world > 1:
                 torch.distributed.barrier()
             t_start = time.perf_counter()
-        if k == 0 or k == args.warmup:
-            upload(k)   # (the first timed step's inputs go up inside the timed region)
+            b_next = upload(k)   # the first timed step's inputs and tables go up inside the timed region
+        b_cur = b_next
         launch(k, b_cur)
         if k + 1 < total and k + 1 != args.warmup:
-            upload(k + 1)
-        planner_now.wait_upload()   # (the planner's own wait, kept out of the planning time)
-        tp = time.perf_counter()
-        b_cur = make_batch()
-        plan_times.append(time.perf_counter() - tp)
+            b_next = upload(k + 1)
         if k >= 1:
             down_ev[(k - 1) % 2].synchronize()   # step k - 1's output is on the host
     down_ev[(total - 1) % 2].synchronize()

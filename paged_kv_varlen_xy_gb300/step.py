@@ -98,8 +98,10 @@ class Planner:
     staging buffer and reach the device in one host->device copy; the device buffer, split-KV
     workspace and slot-mapping buffer are kept between steps and grown when a batch needs more.
     A serving loop that re-plans every step calls plan() then run() once per step (PagedBatch
-    instead builds and uploads each table separately).  The batch returned by plan() stays valid
-    until the next plan() call; use one Planner per stream."""
+    instead builds and uploads each table separately).  Two device table buffers alternate: a
+    batch's device tables stay valid until the plan() after next, its host views until the next
+    plan().  plan(stream=s) uploads on s, which must then be ordered after the kernels of the batch
+    planned two plans earlier (on the default stream that order holds by itself)."""
 
     _ALIGN = 256
 
@@ -121,7 +123,8 @@ class Planner:
         # the dynamic deal's claim counter (every launch returns it to zero)
         self._counter = torch.zeros(2, dtype=torch.int32, device=self.dev) if self.dynamic else None
         self._host = None
-        self._dev_buf = None
+        self._dev_bufs = [None, None]   # device tables, alternating between plans
+        self._flip = 0
         self._ws = torch.empty(16, dtype=torch.uint8, device=self.dev)
         self._slots = torch.empty(1, dtype=torch.int64, device=self.dev)
         self._slot_views = {}
@@ -138,7 +141,10 @@ class Planner:
             self._host = torch.empty(size, dtype=torch.uint8).pin_memory()
             self._host_np = self._host.numpy()
             self._host_ptr = self._host.data_ptr()
-            self._dev_buf = torch.empty(size, dtype=torch.uint8, device=self.dev)
+            self._dev_bufs = [None, None]
+        for i in range(2):
+            if self._dev_bufs[i] is None:
+                self._dev_bufs[i] = torch.empty(self._host.numel(), dtype=torch.uint8, device=self.dev)
 
     def _wait_upload(self):
         if self._pending:
@@ -166,11 +172,10 @@ class Planner:
             self._ensure(tbl.bytes)   # too small: grow and build again
         used_bytes = tbl.bytes
         stm = torch.cuda.current_stream(self.dev) if stream is None else stream
-        if stream is None:
-            self._dev_buf[:used_bytes].copy_(self._host[:used_bytes], non_blocking=True)
-        else:
-            with torch.cuda.stream(stm):
-                self._dev_buf[:used_bytes].copy_(self._host[:used_bytes], non_blocking=True)
+        self._flip ^= 1
+        dbuf = self._dev_bufs[self._flip]
+        with torch.cuda.stream(stm):
+            dbuf[:used_bytes].copy_(self._host[:used_bytes], non_blocking=True)
         self._copied.record(stm)
         self._pending = True
         self.last_upload_bytes = used_bytes
@@ -187,7 +192,7 @@ class Planner:
             slots = self._slot_views[T] = self._slots[:T]
         off = {"err": tbl.err_off, "cu": tbl.cu_off, "ctx": tbl.ctx_off, "bt": tbl.bt_off, "tasks": tbl.tasks_off,
                "merges": tbl.merges_off}
-        b = _StepBatch(self._dev_buf, off, S, self.max_blocks, tbl.num_tasks, tbl.num_merges)
+        b = _StepBatch(dbuf, off, S, self.max_blocks, tbl.num_tasks, tbl.num_merges)
         b._host_np = self._host_np
         b.T = T
         b.pages_used = tbl.pages_used
@@ -361,7 +366,9 @@ class Fp8SplitPlanner:
     lengths and a zeroed error word) are packed into one pinned staging buffer and reach the
     device in one copy; the device buffer, the split-KV workspaces, the slot buffer and the bf16
     page-copy buffers are kept between steps and grown when a batch needs more.  plan() returns a
-    batch for run_step_fp8_split / attention_fp8_split, valid until the next plan()."""
+    batch for run_step_fp8_split / attention_fp8_split; its device tables alternate between two
+    buffers as the Planner's do (valid until the plan() after next; plan(stream=s) must be ordered
+    after the kernels of the batch planned two plans earlier)."""
 
     _ALIGN = 256
 
@@ -375,7 +382,8 @@ class Fp8SplitPlanner:
                                                                    max_blocks, causal)
         self.num_ctas = num_ctas or xy_default_num_ctas(self.dev.index or 0)
         self._host = None
-        self._dev_buf = None
+        self._dev_bufs = [None, None]   # device tables, alternating between plans
+        self._flip = 0
         self._ws = [torch.empty(16, dtype=torch.uint8, device=self.dev) for _ in range(2)]
         self._slots = torch.empty(1, dtype=torch.int64, device=self.dev)
         self._copies = None
@@ -436,19 +444,21 @@ class Fp8SplitPlanner:
             size = max(total, 2 * (self._host.numel() if self._host is not None else 0), 1 << 16)
             self._host = torch.empty(size, dtype=torch.uint8).pin_memory()
             self._host_np = self._host.numpy()
-            self._dev_buf = torch.empty(size, dtype=torch.uint8, device=self.dev)
+            self._dev_bufs = [torch.empty(size, dtype=torch.uint8, device=self.dev) for _ in range(2)]
         for k, a in arrays.items():
             self._host_np[off[k]:off[k] + a.nbytes] = a.reshape(-1).view(np.uint8)
         stm = torch.cuda.current_stream(self.dev) if stream is None else stream
+        self._flip ^= 1
+        dbuf = self._dev_bufs[self._flip]
         with torch.cuda.stream(stm):
-            self._dev_buf[:total].copy_(self._host[:total], non_blocking=True)
+            dbuf[:total].copy_(self._host[:total], non_blocking=True)
         self._copied.record(stm)
         self._pending = True
         self.last_upload_bytes = total
 
         def dv(k, shape):
             n_el = int(np.prod(shape))
-            return self._dev_buf[off[k]:off[k] + 4 * n_el].view(torch.int32).view(*shape)
+            return dbuf[off[k]:off[k] + 4 * n_el].view(torch.int32).view(*shape)
 
         b = _SplitBatch()
         b.cu_host, b.ctx_host, b.block_table_host, b.pages_used = cu, ctx, bt, pages_used

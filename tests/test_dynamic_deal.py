@@ -217,3 +217,17 @@ def test_trace_accounts_for_every_task(dynamic, mixed):
             assert tr[c, 2] == len(mine)
     s = xy.trace_summary(tr)
     assert 0 < s["busy_balance"] <= 1 and s["tail_us"] >= 0
+
+
+@pytest.mark.parametrize("mixed", [False, True])
+def test_many_tasks_per_cta_wrap_the_claim_queue(mixed):
+    # two CTAs for ~200 tasks: each CTA's 8-slot claim queue wraps around many times
+    rng = np.random.default_rng(31)
+    S = 60
+    ctx = [int(x) for x in rng.integers(20, 900, size=S)]
+    q = [int(min(c, rng.integers(2, 150))) if (mixed and i % 7 == 0) else 1 for i, c in enumerate(ctx)]
+    wl = workloads.custom(q, ctx, 8, 2, 128, 16, True, seed=33 + int(mixed))
+    r = run(wl, num_ctas=2, kv_chunk=256, schedule=DYN)
+    assert len(r["batch"].plan.host["tasks"]) > 100
+    assert_parity(r)
+    assert r["batch"].plan.task_counter.cpu().tolist() == [0, 0]
