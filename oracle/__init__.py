@@ -28,8 +28,8 @@ Sources (web pages on the subject; cited by title and section):
 * [ATB]   ATB dynamic batching / speculative decoding / KV reuse notes
           (ai6s.net/6a38a2a6662f9a54cb828d66): "KV缓存复用", "端到端推理调优".
 
-Readings where the pages are silent or inconsistent are listed in the design doc and
-restated in the docstring of the function that takes them.
+Readings where the pages are silent or inconsistent are stated in the docstring of the
+function that takes them.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against
 closed forms, worked examples printed on the pages (``tests/golden/``), brute force
