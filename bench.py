@@ -329,17 +329,14 @@ def main():
     ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="page format of the KV cache")
     ap.add_argument("--schedule", type=int, default=None, choices=[0, 1, 2, 3, 4],
-                    help="task-table schedule (default: 4, the dynamic deal, over bf16 pages; 3, the greedy static "
-                         "deal, over 8-bit pages)")
+                    help="task-table schedule (default: 4, the dynamic deal)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    args.default_schedule = 3 if args.kv == "fp8" else 4
+    args.default_schedule = 4
     if args.schedule is None:
         args.schedule = args.default_schedule
-    if args.schedule == 4 and args.kv == "fp8":
-        ap.error("--schedule 4 (the dynamic deal) runs over bf16 pages only")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -410,6 +407,11 @@ def main():
         if split:
             xystep.attention_fp8_split(batch, vals["q"], vals["k_codes"], vals["v_codes"], vals["k_scales"],
                                        vals["v_scales"], wl.scale, out)
+        elif fp8 and pl.dynamic:
+            xy.xy_paged_attention_fp8_dynamic(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_codes"],
+                                              vals["v_codes"], vals["k_scales"], vals["v_scales"], wl.scale,
+                                              wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace,
+                                              pl.task_counter, batch.err, out)
         elif fp8:
             xy.xy_paged_attention_fp8(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_codes"],
                                       vals["v_codes"], vals["k_scales"], vals["v_scales"], wl.scale, wl.causal,

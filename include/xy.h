@@ -397,6 +397,26 @@ xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, con
                                  int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
                                  int32_t *err_word, void *out, void *stream);
 
+/* xy_paged_attention_fp8_dynamic: xy_paged_attention_fp8 with the dynamic deal of
+ * xy_paged_attention_dynamic ([XY] §2.2 component 2, the deal taken at run time).  Each CTA's
+ * first producer warp claims the next task from task_counter[0] once it has issued the first
+ * copy of its current task (no separate scheduler warp over 8-bit pages), so CTAs take tasks in
+ * table order.  Outputs are bit-identical to xy_paged_attention_fp8's on the same tasks.
+ *   task_counter: as for xy_paged_attention_dynamic (device int32[2], 8-byte aligned, zero before
+ *   the first call, returned to zero by every launch; overlapping calls need different counters).
+ *   Every other argument, limit and error as for xy_paged_attention_fp8; XY_ERR_INVALID_ARG also
+ *   for a null or misaligned task_counter. */
+xy_status xy_paged_attention_fp8_dynamic(const void *q, const int32_t *cu_seqlens_q,
+                                         const int32_t *context_lens, const int32_t *block_table,
+                                         int max_blocks, const void *k_pages, const void *v_pages,
+                                         const float *k_scales, const float *v_scales, int num_pages,
+                                         int num_seqs, int num_tokens, int num_heads_q, int num_heads_kv,
+                                         int head_dim, int block_size, float scale, int causal,
+                                         const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                         int num_merges, int num_ctas, void *workspace,
+                                         size_t workspace_bytes, int32_t *task_counter, int32_t *err_word,
+                                         void *out, void *stream);
+
 /* Self-test of the bounded waits (no counterpart in the pages; not a step of the path).
  * Every mbarrier wait in the attention kernels gives up after a time limit, or when its CTA's
  * abort flag is raised, sets XY_DEV_TIMEOUT in *err_word and lets the kernel return instead of

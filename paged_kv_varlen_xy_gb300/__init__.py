@@ -24,7 +24,7 @@ C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_n
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
          "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
          "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8", "xy_paged_attention_dynamic",
-         "xy_paged_attention_traced")
+         "xy_paged_attention_traced", "xy_paged_attention_fp8_dynamic")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -114,6 +114,9 @@ def lib():
     L.xy_paged_attention_traced.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P,
                                             P, P, P, P]
     L.xy_paged_attention_traced.restype = I
+    L.xy_paged_attention_fp8_dynamic.argtypes = [P, P, P, P, I, P, P, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I,
+                                                 P, SZ, P, P, P, P]
+    L.xy_paged_attention_fp8_dynamic.restype = I
     _lib = L
     return L
 
@@ -187,10 +190,12 @@ XY_SCHEDULE_DYNAMIC = 4
 
 
 def default_schedule(kv_fp8=False):
-    """The task-table schedule a step uses unless told otherwise: the dynamic deal over bf16 pages
-    (CTAs claim tasks while the kernel runs; measured faster than the static deals on the prefill,
-    mixed and skewed batches and level on decode), the greedy static deal over 8-bit pages."""
-    return XY_SCHEDULE_GREEDY if kv_fp8 else XY_SCHEDULE_DYNAMIC
+    """The task-table schedule a step uses unless told otherwise: the dynamic deal, over bf16 and
+    8-bit pages alike (CTAs claim tasks while the kernel runs; over bf16 pages measured faster than
+    the static deals on the prefill, mixed and skewed batches and level on decode; over 8-bit pages
+    a little faster than the greedy deal on the device, and faster end to end, since the host only
+    sorts the tasks instead of dealing them)."""
+    return XY_SCHEDULE_DYNAMIC
 
 
 _XY_ERR_CAPACITY = -10
@@ -431,6 +436,32 @@ def xy_paged_attention_fp8(q, cu_seqlens_q, context_lens, block_table, k_pages, 
     """xy_paged_attention over 8-bit pages: k_pages/v_pages [P, Hkv, bs, 128] uint8 E4M3 codes,
     k_scales/v_scales [P, Hkv, bs] fp32 (as written by xy_kv_append_fp8).  tasks from a task table
     built with q_tile <= 64 // G (Plan(..., kv_fp8=True))."""
+    a = _fp8_args(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_scales, v_scales, scale, causal,
+                  tasks, merges, num_ctas, workspace, out)
+    import torch
+    _check(lib().xy_paged_attention_fp8(*a, _dev(err_word, torch.int32, "err_word"),
+                                        _dev(out, torch.bfloat16, "out"), _stream(stream)),
+           "xy_paged_attention_fp8")
+
+
+def xy_paged_attention_fp8_dynamic(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_scales, v_scales,
+                                   scale, causal, tasks, merges, num_ctas, workspace, task_counter, err_word, out,
+                                   stream=None):
+    """xy_paged_attention_fp8 with a dynamic deal: the CTAs claim tasks in table order from
+    task_counter (device int32 [2], zero before the first call; every launch returns it to zero)."""
+    import torch
+    a = _fp8_args(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_scales, v_scales, scale, causal,
+                  tasks, merges, num_ctas, workspace, out)
+    _check(lib().xy_paged_attention_fp8_dynamic(*a, _dev(task_counter, torch.int32, "task_counter"),
+                                                _dev(err_word, torch.int32, "err_word"),
+                                                _dev(out, torch.bfloat16, "out"), _stream(stream)),
+           "xy_paged_attention_fp8_dynamic")
+
+
+def _fp8_args(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_scales, v_scales, scale, causal,
+              tasks, merges, num_ctas, workspace, out):
+    """The arguments the two 8-bit-page entries share, up to the workspace size (`out` is checked
+    against q here and passed by the caller)."""
     import torch
     T, Hq, d = q.shape
     P, Hkv, bs, d2 = k_pages.shape
@@ -442,14 +473,12 @@ def xy_paged_attention_fp8(q, cu_seqlens_q, context_lens, block_table, k_pages, 
     nm = merges.shape[0] if merges is not None else 0
     ws_ptr = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None and workspace.numel() else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().xy_paged_attention_fp8(
-        _dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"), _dev(context_lens, torch.int32, "context_lens"),
-        _dev(block_table, torch.int32, "block_table"), block_table.shape[1], _dev(k_pages, u8, "k_pages"),
-        _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P,
-        cu_seqlens_q.numel() - 1, T, Hq, Hkv, d, bs, float(scale), int(bool(causal)),
-        _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
-        _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes,
-        _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention_fp8")
+    return (_dev(q, bf, "q"), _dev(cu_seqlens_q, torch.int32, "cu_seqlens_q"),
+            _dev(context_lens, torch.int32, "context_lens"), _dev(block_table, torch.int32, "block_table"),
+            block_table.shape[1], _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
+            _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, cu_seqlens_q.numel() - 1, T, Hq, Hkv,
+            d, bs, float(scale), int(bool(causal)), _dev(tasks, torch.int32, "tasks"), tasks.shape[0],
+            _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes)
 
 
 def xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, pages, k_out, v_out, err_word, stream=None):
@@ -515,8 +544,6 @@ class Plan:
         cu = np.asarray(cu_seqlens_q)
         schedule = default_schedule(kv_fp8) if schedule is None else schedule
         self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
-        if self.dynamic and kv_fp8:
-            raise ValueError("the dynamic deal runs over bf16 pages only")
         dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8,
                                pure_decode=len(cu) > 1 and int(cu[-1]) == len(cu) - 1)
         self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk

@@ -61,11 +61,13 @@ struct Cfg {
                                   xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type;
     static constexpr int kProducers = KIND == kBf16 ? 2 : 4;
     static_assert(RG::kStages >= kProducers, "every producer owns a ring slot");
-    // math warps, producer warps, then (dynamic deal) the scheduler warp; bf16 pages only: a ninth
-    // warp would put three warps on one SM sub-partition and cap the registers at 168
-    static_assert(!DYN || KIND == kBf16, "the dynamic deal runs over bf16 pages");
+    // math warps, producer warps, then (dynamic deal over bf16 pages) the scheduler warp.  Over
+    // 8-bit pages a ninth warp would put three warps on one SM sub-partition and cap the registers
+    // at 168, so there the first producer warp claims the tasks itself.
+    static constexpr bool kSchedWarpUsed = DYN && KIND == kBf16;
+    static constexpr bool kInlineClaims = DYN && KIND != kBf16;
     static constexpr int kSchedWarp = kMathWarps + kProducers;
-    static constexpr int kThreads = (kSchedWarp + (DYN ? 1 : 0)) * 32;
+    static constexpr int kThreads = (kSchedWarp + (kSchedWarpUsed ? 1 : 0)) * 32;
     static constexpr int kStagesOff = 0;
     static constexpr int kSlotsOff = RG::kBytes;
     static constexpr int kBarOff = kSlotsOff + RG::kSlotBytes;
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, 1)
     }
     __syncthreads();
 
-    if constexpr (DYN) {
+    if constexpr (C::kSchedWarpUsed) {
         if (warp == C::kSchedWarp) {
             // ---------------------------- scheduler (dynamic deal) ----------------------------
             int r = 1;
@@ -136,18 +138,37 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, 1)
         }
         int ctr = 0, pref_win = -1;
         bool ok = true, pref_valid = false;
+        // inline claims (8-bit pages): producer warp 0 claims task k + 1 once it has issued its
+        // first stage of task k (so the claim overlaps the copies), or as it leaves task k
+        const bool claims = C::kInlineClaims && pw == 0;
+        int published = 0;
+        bool claims_done = !claims, claimed = true;
+        auto claim_next = [&]() {
+            if (claims_done || claimed) return;
+            claimed = true;
+            const int r = dq.publish(published++, p, p.dyn, lane);
+            if (r <= 0) claims_done = true;
+            if (r < 0) ok = false;
+        };
+        if (claims) {
+            claimed = false;
+            claim_next();   // entry 0
+        }
         TaskCursor tc;
         tc.attach(q, false, pw == 0);
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
+            claimed = false;
             if (xy::is_hole(tc.cur.t)) {
+                claim_next();
                 pref_valid = false;
                 tc.advance(p);
                 continue;
             }
             if (!xy::dec::task_ok<RG>(tc.cur, p)) {
                 if (lane == 0 && pw == 0) xy::set_err(p.err, XY_DEV_BAD_TASK);
+                claim_next();
                 pref_valid = false;
                 tc.advance(p);
                 continue;
@@ -167,10 +188,13 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, 1)
                         pref_valid = tn.seq >= 0 && tn.seq < p.S && tn.kv_start >= 0;
                         if (pref_valid) pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
                     }
+                    claim_next();
                 },
-                pw, C::kProducers);
+                pw, C::kProducers) && ok;
+            claim_next();   // (no stage of the task fell to this warp)
             tc.advance(p);
         }
+        if (claims) dq.finish(p.dyn, lane);
         if (!ok || tc.failed) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             *abort_flag = 1;
@@ -360,12 +384,8 @@ template <int HD, int KIND>
 xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
                  const xy_merge *merges, int num_merges, cudaStream_t st) {
     if (p.num_tasks > 0) {
-        xy_status ks;
-        if constexpr (KIND == kBf16)
-            ks = p.dyn ? launch_attention_kernel<HD, KIND, true>(p, km, vm, num_ctas, st)
-                       : launch_attention_kernel<HD, KIND, false>(p, km, vm, num_ctas, st);
-        else
-            ks = launch_attention_kernel<HD, KIND, false>(p, km, vm, num_ctas, st);
+        const xy_status ks = p.dyn ? launch_attention_kernel<HD, KIND, true>(p, km, vm, num_ctas, st)
+                                   : launch_attention_kernel<HD, KIND, false>(p, km, vm, num_ctas, st);
         if (ks != XY_OK) return ks;
     }
     if (num_merges > 0) {
@@ -503,14 +523,15 @@ extern "C" xy_status xy_paged_attention(const void *q, const int32_t *cu_seqlens
                      num_merges, num_ctas, workspace, workspace_bytes, nullptr, nullptr, err_word, out, stream);
 }
 
-extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
-                                            const int32_t *block_table, int max_blocks, const void *k_pages,
-                                            const void *v_pages, const float *k_scales, const float *v_scales,
-                                            int num_pages, int num_seqs, int num_tokens, int num_heads_q,
-                                            int num_heads_kv, int head_dim, int block_size, float scale, int causal,
-                                            const xy_task *tasks, int num_tasks, const xy_merge *merges,
-                                            int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
-                                            int32_t *err_word, void *out, void *stream) {
+namespace {
+// xy_paged_attention_fp8; the dynamic deal when task_counter is given
+xy_status attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                        const int32_t *block_table, int max_blocks, const void *k_pages, const void *v_pages,
+                        const float *k_scales, const float *v_scales, int num_pages, int num_seqs, int num_tokens,
+                        int num_heads_q, int num_heads_kv, int head_dim, int block_size, float scale, int causal,
+                        const xy_task *tasks, int num_tasks, const xy_merge *merges, int num_merges, int num_ctas,
+                        void *workspace, size_t workspace_bytes, int32_t *task_counter, int32_t *err_word, void *out,
+                        void *stream) {
     if (num_tasks < 0 || num_merges < 0 || num_seqs < 0 || num_tokens < 0) return XY_ERR_INVALID_ARG;
     if (num_tasks == 0 && num_merges == 0) return XY_OK;
     if (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)) return XY_ERR_INVALID_ARG;
@@ -523,6 +544,8 @@ extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seq
     if (head_dim != 128 || p.G > 16 * kMathWarps) return XY_ERR_UNSUPPORTED;
     p.ksc = k_scales;
     p.vsc = v_scales;
+    if (task_counter && (reinterpret_cast<uintptr_t>(task_counter) & 7)) return XY_ERR_INVALID_ARG;
+    p.dyn = reinterpret_cast<int *>(task_counter);
 
     const int64_t rows = (int64_t)num_pages * num_heads_kv * block_size;
     const int keys = Cfg<128, kFp8Narrow>::RG::kKeys;  // both 8-bit rings stage 128 keys
@@ -536,6 +559,40 @@ extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seq
     const bool narrow = num_tokens == num_seqs && p.G <= XY_FP8_NARROW_ROWS;
     return narrow ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
                   : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
+}
+}  // namespace
+
+extern "C" xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                            const int32_t *block_table, int max_blocks, const void *k_pages,
+                                            const void *v_pages, const float *k_scales, const float *v_scales,
+                                            int num_pages, int num_seqs, int num_tokens, int num_heads_q,
+                                            int num_heads_kv, int head_dim, int block_size, float scale, int causal,
+                                            const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                            int num_merges, int num_ctas, void *workspace, size_t workspace_bytes,
+                                            int32_t *err_word, void *out, void *stream) {
+    return attention_fp8(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages, k_scales, v_scales,
+                         num_pages, num_seqs, num_tokens, num_heads_q, num_heads_kv, head_dim, block_size, scale,
+                         causal, tasks, num_tasks, merges, num_merges, num_ctas, workspace, workspace_bytes, nullptr,
+                         err_word, out, stream);
+}
+
+// Dynamic deal over 8-bit pages: as xy_paged_attention_fp8, each CTA claiming the next task of the
+// table from task_counter (its first producer warp claims, no scheduler warp).
+extern "C" xy_status xy_paged_attention_fp8_dynamic(const void *q, const int32_t *cu_seqlens_q,
+                                                    const int32_t *context_lens, const int32_t *block_table,
+                                                    int max_blocks, const void *k_pages, const void *v_pages,
+                                                    const float *k_scales, const float *v_scales, int num_pages,
+                                                    int num_seqs, int num_tokens, int num_heads_q, int num_heads_kv,
+                                                    int head_dim, int block_size, float scale, int causal,
+                                                    const xy_task *tasks, int num_tasks, const xy_merge *merges,
+                                                    int num_merges, int num_ctas, void *workspace,
+                                                    size_t workspace_bytes, int32_t *task_counter, int32_t *err_word,
+                                                    void *out, void *stream) {
+    if (!task_counter) return XY_ERR_INVALID_ARG;
+    return attention_fp8(q, cu_seqlens_q, context_lens, block_table, max_blocks, k_pages, v_pages, k_scales, v_scales,
+                         num_pages, num_seqs, num_tokens, num_heads_q, num_heads_kv, head_dim, block_size, scale,
+                         causal, tasks, num_tasks, merges, num_merges, num_ctas, workspace, workspace_bytes,
+                         task_counter, err_word, out, stream);
 }
 
 // Dynamic deal: the kernels xy_paged_attention would launch, each CTA claiming the next task of

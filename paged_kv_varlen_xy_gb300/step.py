@@ -7,7 +7,7 @@ import torch
 from . import (XY_SCHEDULE_DYNAMIC, XY_SCHEDULE_GREEDY, Plan, check_err_word, default_schedule, default_tiles,
                xy_build_block_table, xy_build_step_tables, xy_build_task_table, xy_default_num_ctas,
                xy_dequant_pages_fp8, xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_dynamic,
-               xy_paged_attention_fp8, xy_slot_mapping)
+               xy_paged_attention_fp8, xy_paged_attention_fp8_dynamic, xy_slot_mapping)
 
 
 class PagedBatch:
@@ -115,8 +115,6 @@ class Planner:
         self._q_tile_arg = q_tile
         schedule = default_schedule(kv_fp8) if schedule is None else schedule
         self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
-        if self.dynamic and kv_fp8:
-            raise ValueError("the dynamic deal runs over bf16 pages only")
         tiles = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
         self.kv_chunk = kv_chunk or tiles[1]
         self.q_tile, self.schedule = q_tile or tiles[0], schedule
@@ -230,10 +228,14 @@ class Planner:
                                       _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
                                       _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv, bs,
                                       d, err, st), "xy_kv_append_fp8")
-            _check(L.xy_paged_attention_fp8(_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, u8, "k_pages"),
-                                            _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"),
-                                            _dev(v_scales, f32, "v_scales"), P, *common, _dev(out, bf, "out"), st),
-                   "xy_paged_attention_fp8")
+            pools = (_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, u8, "k_pages"),
+                     _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P)
+            if self.dynamic:
+                _check(L.xy_paged_attention_fp8_dynamic(*pools, *common[:-1], ctypes.c_void_p(self._counter.data_ptr()),
+                                                        err, _dev(out, bf, "out"), st),
+                       "xy_paged_attention_fp8_dynamic")
+            else:
+                _check(L.xy_paged_attention_fp8(*pools, *common, _dev(out, bf, "out"), st), "xy_paged_attention_fp8")
         else:
             _check(L.xy_kv_append(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), slots, T,
                                   _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P, Hkv, bs, d, err, st),
@@ -275,8 +277,14 @@ def run_step_fp8(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, s
     xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, batch.block_size, P, batch.slots, batch.err, stream)
     xy_kv_append_fp8(k_new, v_new, batch.slots, k_pages, v_pages, k_scales, v_scales, batch.err, stream)
     pl = batch.plan
-    xy_paged_attention_fp8(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales, v_scales, scale,
-                           batch.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out, stream)
+    if pl.dynamic:
+        xy_paged_attention_fp8_dynamic(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales,
+                                       v_scales, scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace,
+                                       pl.task_counter, batch.err, out, stream)
+    else:
+        xy_paged_attention_fp8(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales, v_scales,
+                               scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out,
+                               stream)
     return out
 
 
@@ -387,7 +395,9 @@ class Fp8SplitPlanner:
         self._ws = [torch.empty(16, dtype=torch.uint8, device=self.dev) for _ in range(2)]
         self._slots = torch.empty(1, dtype=torch.int64, device=self.dev)
         self._copies = None
-        self._counter = torch.zeros(2, dtype=torch.int32, device=self.dev)  # tile part: dynamic deal
+        # the two parts' claim counters (dynamic deal; each launch returns its counter to zero)
+        self._counter = torch.zeros(2, dtype=torch.int32, device=self.dev)
+        self._counter_d = torch.zeros(2, dtype=torch.int32, device=self.dev)
         self._copied = torch.cuda.Event() if self.dev.type == "cuda" else None
         self._pending = False
 
@@ -431,7 +441,7 @@ class Fp8SplitPlanner:
             T_d = int(cu[db] - cu[da])
             q_tile, kv_chunk = default_tiles(self.Hq, self.Hkv, self.d, True, pure_decode=T_d == db - da)
             r = xy_build_task_table(cu_d, ctx[da:db], self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, q_tile,
-                                    kv_chunk, XY_SCHEDULE_GREEDY)
+                                    kv_chunk, XY_SCHEDULE_DYNAMIC)
             arrays.update(cu_d=cu_d, tasks_d=r["tasks"], merges_d=r["merges"])
             parts["decode"] = (da, db, r)
         # pack at 256-byte offsets into the pinned staging buffer, one copy to the device
@@ -494,7 +504,7 @@ class Fp8SplitPlanner:
             a, bnd, r = parts["decode"]
             n_d, m_d = len(r["tasks"]), len(r["merges"])
             plan = _Part(dv("tasks_d", (n_d, 8)), dv("merges_d", (m_d, 8)), self.num_ctas,
-                         ws(1, r["workspace_bytes"]), XY_SCHEDULE_GREEDY, None)
+                         ws(1, r["workspace_bytes"]), XY_SCHEDULE_DYNAMIC, self._counter_d)
             b.decode = dict(seq=(a, bnd), tok=(int(cu[a]), int(cu[bnd])), cu=dv("cu_d", (bnd - a + 1,)),
                             ctx=b.ctx[a:bnd], plan=plan)
         return b
@@ -534,10 +544,14 @@ def attention_fp8_split(batch, q, k_pages, v_pages, k_scales, v_scales, scale, o
         a, b = dd["tok"]
         pl = dd["plan"]
         sa, sb = dd["seq"]
-        xy_paged_attention_fp8(q[a:b], dd["cu"], dd["ctx"], batch.block_table[sa:sb], k_pages, v_pages, k_scales,
-                               v_scales, scale,
-                               batch.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out[a:b],
-                               stream)
+        if pl.dynamic:
+            xy_paged_attention_fp8_dynamic(q[a:b], dd["cu"], dd["ctx"], batch.block_table[sa:sb], k_pages, v_pages,
+                                           k_scales, v_scales, scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas,
+                                           pl.workspace, pl.task_counter, batch.err, out[a:b], stream)
+        else:
+            xy_paged_attention_fp8(q[a:b], dd["cu"], dd["ctx"], batch.block_table[sa:sb], k_pages, v_pages,
+                                   k_scales, v_scales, scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas,
+                                   pl.workspace, batch.err, out[a:b], stream)
     return out
 
 

@@ -47,7 +47,11 @@ def test_append_fp8_bit_exact(d):
 # ---------------------------------------------------------------------------------------------
 # attention over 8-bit pages
 
-def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False):
+# the task-table deals over 8-bit pages: greedy static and dynamic (the default)
+GREEDY, DYN = 3, 4
+
+
+def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False, schedule=None, num_ctas=None):
     """One step over 8-bit pages on the GPU and in the oracle, on workload wl's bf16 values
     (optionally with each pool / new row multiplied by a power of two from row_scale)."""
     import paged_kv_varlen_xy_gb300 as xy
@@ -78,7 +82,7 @@ def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False):
     else:
         batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
                                   wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev,
-                                  kv_chunk=kv_chunk, kv_fp8=True)
+                                  kv_chunk=kv_chunk, kv_fp8=True, schedule=schedule, num_ctas=num_ctas)
         out = xystep.run_step_fp8(batch, q, kn, vn, codes["k"], codes["v"], scl["k"], scl["v"], wl.scale)
     torch.cuda.synchronize()
     ref = oracle.step.run_step_fp8(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
@@ -105,34 +109,41 @@ def _assert_fp8_parity(r, per_row_scale=False):
     assert diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS, (diff.max(), diff.mean())
 
 
+@pytest.mark.parametrize("schedule", [GREEDY, DYN])
 @pytest.mark.parametrize("G,bs", [(1, 16), (4, 16), (8, 64), (16, 256)])
-def test_fp8_decode_matches_oracle(G, bs):
+def test_fp8_decode_matches_oracle(G, bs, schedule):
     # decode rows over ragged contexts (1 key, partial pages, partial 64-key stages, several chunks)
     ctx = [1, 15, 16, 17, 63, 64, 65, 200, 1000, 2500, 777, 4096]
     wl = workloads.custom(np.ones(len(ctx)), ctx, 4 * G, 4, 128, bs, seed=40 + G, name="fp8_decode")
-    _assert_fp8_parity(_run_fp8(wl))
+    r = _run_fp8(wl, schedule=schedule)
+    assert r["batch"].plan.dynamic == (schedule == DYN)
+    _assert_fp8_parity(r)
 
 
+@pytest.mark.parametrize("schedule", [GREEDY, DYN])
 @pytest.mark.parametrize("G", [1, 4, 8, 32])
-def test_fp8_mixed_batch_matches_oracle(G):
+def test_fp8_mixed_batch_matches_oracle(G, schedule):
     # prefill, chunked-prefill and verify-shaped queries (causal): tasks of up to 64 rows (up to
     # four 16-row groups) on the ring for batches that are not pure decode
     q_lens = [37, 1, 5, 100, 1, 16, 3]
     ctx = [37, 900, 64, 612, 129, 16, 2050]
     wl = workloads.custom(q_lens, ctx, 2 * G, 2, 128, 16, seed=50 + G, name="fp8_mixed")
-    _assert_fp8_parity(_run_fp8(wl))
+    _assert_fp8_parity(_run_fp8(wl, schedule=schedule))
 
 
-def test_fp8_split_kv_and_row_magnitudes():
+@pytest.mark.parametrize("schedule", [GREEDY, DYN])
+def test_fp8_split_kv_and_row_magnitudes(schedule):
     # KV chunks of 256 keys (split partials and the combine) and rows of very different magnitude
     # (the largest V scale grows along a task: O is rescaled as it does)
     ctx = [3000, 1, 700, 5000, 257]
     wl = workloads.custom(np.ones(len(ctx)), ctx, 32, 8, 128, 16, seed=61, name="fp8_split")
-    _assert_fp8_parity(_run_fp8(wl, kv_chunk=256, row_scale=[2.0 ** -12, 1.0, 2.0 ** 4]), per_row_scale=True)
+    _assert_fp8_parity(_run_fp8(wl, kv_chunk=256, row_scale=[2.0 ** -12, 1.0, 2.0 ** 4], schedule=schedule),
+                       per_row_scale=True)
 
 
+@pytest.mark.parametrize("schedule", [GREEDY, DYN])
 @pytest.mark.parametrize("name", ["decode", "skew"])
-def test_fp8_full_size_sampled_rows(name):
+def test_fp8_full_size_sampled_rows(name, schedule):
     # the full decode / skew batches over 8-bit pages in the bench's launch configuration; the oracle
     # checks sampled sequences (all their rows), pages and codes of those sequences bit for bit
     import paged_kv_varlen_xy_gb300 as xy
@@ -146,7 +157,8 @@ def test_fp8_full_size_sampled_rows(name):
     codes = [torch.empty(P, Hkv, bs, d, dtype=torch.uint8, device="cuda") for _ in range(2)]
     scl = [torch.empty(P, Hkv, bs, dtype=torch.float32, device="cuda") for _ in range(2)]
     batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
-                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, kv_fp8=True)
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, kv_fp8=True,
+                              schedule=schedule)
     rows = [vals[n].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous() for n in ("k_pool", "v_pool")]
     xy.xy_kv_append_fp8(rows[0], rows[1], torch.arange(P * bs, dtype=torch.int64, device="cuda"), codes[0], codes[1],
                         scl[0], scl[1], batch.err)
@@ -175,6 +187,67 @@ def test_fp8_full_size_sampled_rows(name):
     got = np.stack([got[t, h] for (t, h) in rows])
     diff = np.abs(got - ref["out"])
     assert np.isfinite(got).all() and diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS, (diff.max(), diff.mean())
+
+
+@pytest.mark.parametrize("decode", [True, False])
+def test_fp8_dynamic_deal_bit_identical_and_counter_reused(decode):
+    # a task's result does not depend on the CTA that runs it: the dynamic deal's outputs equal the
+    # greedy deal's bit for bit (same tasks, same split rows); every launch returns the counter to
+    # zero, so repeated launches need no reset; one CTA and more CTAs than tasks run every task
+    import paged_kv_varlen_xy_gb300 as xy
+    rng = np.random.default_rng(23)
+    ctx = [int(x) for x in rng.integers(1, 3000, size=50)]
+    q_lens = [1] * 50 if decode else [int(x) for x in rng.integers(1, 40, size=50)]
+    wl = workloads.custom(q_lens, ctx, 16, 2, 128, 16, seed=24, name="fp8_dyn")
+    outs = {}
+    for schedule, n in ((GREEDY, None), (DYN, None), (DYN, 1), (DYN, 300)):
+        r = _run_fp8(wl, kv_chunk=512, schedule=schedule, num_ctas=n)
+        _assert_fp8_parity(r)
+        outs[(schedule, n)] = r
+    base = _bits_f64(outs[(GREEDY, None)]["out"])
+    for key, r in outs.items():
+        assert np.array_equal(_bits_f64(r["out"]), base), key
+    r = outs[(DYN, None)]
+    batch, pl = r["batch"], r["batch"].plan
+    assert len(pl.host["merges"]) > 0, "expected split tasks"
+    assert pl.task_counter.cpu().tolist() == [0, 0]
+    q = wl.tensors("cpu")["q"].cuda()  # the values _run_fp8 used
+    k, v = (torch.from_numpy(r["codes"][n]).cuda() for n in ("k", "v"))
+    ks, vs = (torch.from_numpy(r["scales"][n]).cuda() for n in ("k", "v"))
+    for _ in range(3):
+        out = torch.empty_like(q)
+        xy.xy_paged_attention_fp8_dynamic(q, batch.cu, batch.ctx, batch.block_table, k, v, ks, vs, wl.scale,
+                                          wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace,
+                                          pl.task_counter, batch.err, out)
+        torch.cuda.synchronize()
+        assert int(batch.err.item()) == 0
+        assert pl.task_counter.cpu().tolist() == [0, 0]
+        assert np.array_equal(_bits(out), base)
+
+
+def test_fp8_greedy_table_with_holes_through_the_dynamic_call():
+    # hole records of a greedy table are skipped by the claiming CTAs: every task runs once
+    import paged_kv_varlen_xy_gb300 as xy
+    wl = workloads.custom([1] * 6, [5000, 30, 30, 30, 900, 17], 8, 2, 128, 16, seed=19, name="fp8_holes")
+    r = _run_fp8(wl, kv_chunk=1024, schedule=GREEDY, num_ctas=5)
+    _assert_fp8_parity(r)
+    batch, pl = r["batch"], r["batch"].plan
+    assert (pl.host["tasks"][:, 0] == -1).any(), "expected hole records"
+    q = wl.tensors("cpu")["q"].cuda()  # the values _run_fp8 used
+    k, v = (torch.from_numpy(r["codes"][n]).cuda() for n in ("k", "v"))
+    ks, vs = (torch.from_numpy(r["scales"][n]).cuda() for n in ("k", "v"))
+    counter = torch.zeros(2, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q)
+    xy.xy_paged_attention_fp8_dynamic(q, batch.cu, batch.ctx, batch.block_table, k, v, ks, vs, wl.scale, wl.causal,
+                                      pl.tasks, pl.merges, pl.num_ctas, pl.workspace, counter, batch.err, out)
+    torch.cuda.synchronize()
+    assert int(batch.err.item()) == 0 and counter.cpu().tolist() == [0, 0]
+    assert np.array_equal(_bits(out), _bits_f64(r["out"]))
+
+
+def _bits_f64(x):
+    """bf16 values held as float64 (exactly) -> their bf16 bit patterns."""
+    return (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
 
 
 def test_dequant_pages_bit_exact():
