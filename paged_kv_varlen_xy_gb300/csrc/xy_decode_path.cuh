@@ -207,6 +207,336 @@ __device__ __forceinline__ void drain(const Smem &sm, int ctr, int pw = 0, int n
         if ((k % RG::kStages) % npw == pw) mbar_wait(sm.full_bar + 8 * (k % RG::kStages), (k / RG::kStages) & 1);
 }
 
+// 8-bit pages, tasks of at most 8 (token, head) rows: the products transposed, S^T = K Q^T and
+// O^T = V^T P^T, so that keys and head-dim columns fill the 16-row side of the m16n8k16 fragments
+// and the (at most 8) query rows its 8-column side.  Per 32 keys a warp then issues 16 + 16 MMAs
+// instead of 32 + 32 and holds 8 scores instead of 16 (a decode row no longer pads 15 of 16 MMA
+// rows).  The packed weights reach the second product's B fragments through an in-register 8x8
+// transpose.  Accumulator tile (cc, e): its row g holds column 32cc + 2g + e and its row g + 8
+// column 32cc + 16 + 2g + e; its columns are the query rows.  Otherwise as consume_task: each math
+// warp takes 32 keys of every stage, and the four merge their (max, sum, O) at the end.
+template <class RG, class F>
+__device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
+                                 int lane, F first_stage_seen) {
+    constexpr int HD = 128;
+    static_assert(RG::kKeys == 32 * kMathWarps, "32 keys per math warp and stage");
+    const int g4 = lane >> 2, c4 = lane & 3;
+    const xy_task t = f.t;
+    const int R = t.q_rows * p.G;  // at most 8
+    const int qn = f.qn, L = f.L;
+    auto row_limit = [&](int r) -> int {
+        if (r >= R) return t.kv_end;  // padding rows: never stored, kept finite
+        const int lim = p.causal ? (L - qn + t.q_start + r / p.G + 1) : L;
+        return min(lim, t.kv_end);
+    };
+    const int r0 = 2 * c4, r1 = r0 + 1;  // this lane's query rows (accumulator columns)
+    const int lim0 = row_limit(r0), lim1 = row_limit(r1);
+    int lim_max = max(lim0, lim1);
+    lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, 1));
+    lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, 2));
+
+    uint32_t qb[HD / 16][2];  // Q^T B fragments, f16, in the k-order of the K code fragments
+    float o[HD / 32][2][4];
+#pragma unroll
+    for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) o[cc][e][0] = o[cc][e][1] = o[cc][e][2] = o[cc][e][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // l: this lane's keys only
+    float s_max = 0.f, s_inv = 0.f;  // largest V scale seen, and its reciprocal
+
+    auto keys32 = [&](uint32_t kst, uint32_t vst, const float *scl, int kc, int kr) {
+        const int mi = lane >> 3;
+        // S^T of 16-key blocks b = 0, 1: C fragment rows are keys kc + 16b + g (0, 1) and + 8
+        // (2, 3), columns the query rows r0, r1; even and odd 16-column k-steps accumulate apart
+        float sp[2][2][4];
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) sp[b][h][0] = sp[b][h][1] = sp[b][h][2] = sp[b][h][3] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                // matrix i: keys 8(i&1).. of chunk 2cc + (i>>1); lane (g, c) gets cols 4c..4c+3 of
+                // its key, i.e. the A fragment (rows = keys) of one k-step in Q's k-order
+                const int krow = kr + 16 * b + ((mi & 1) << 3) + (lane & 7);
+                uint32_t r[4], lo[4], hi[4];
+                ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(r[i], lo[i], hi[i]);
+                const uint32_t a0[4] = {lo[0], lo[1], hi[0], hi[1]};
+                const uint32_t a1[4] = {lo[2], lo[3], hi[2], hi[3]};
+                mma_f16_16816(sp[b][0], a0, qb[2 * cc][0], qb[2 * cc][1]);
+                mma_f16_16816(sp[b][1], a1, qb[2 * cc + 1][0], qb[2 * cc + 1][1]);
+            }
+        }
+        float sc[2][4];
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc[b][j] = sp[b][0][j] + sp[b][1][j];
+        // scales of keys kc + 16b + 8h + g (V scales of keys at or past kv_end, which may hold
+        // anything, read as 0); virtual + causal mask; online softmax (log2 domain)
+        float vs[2][2];
+        float mx0 = -INFINITY, mx1 = -INFINITY, vmax = 0.f;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int o_ = kr + 16 * b + 8 * h + g4;
+                const int key = kc + 16 * b + 8 * h + g4;
+                const float kx = scl[o_], vx = scl[RG::kKeys + o_];
+                vs[b][h] = key < t.kv_end ? vx : 0.f;
+                vmax = fmaxf(vmax, vs[b][h]);
+                const float fk = p.scale_log2 * kx;
+                sc[b][2 * h] = key < lim0 ? sc[b][2 * h] * fk : -INFINITY;
+                sc[b][2 * h + 1] = key < lim1 ? sc[b][2 * h + 1] * fk : -INFINITY;
+                mx0 = fmaxf(mx0, sc[b][2 * h]);
+                mx1 = fmaxf(mx1, sc[b][2 * h + 1]);
+            }
+        }
+        // lazy reference max, as in consume_task; a row's keys lie across the lanes of one column c
+        float al0 = 1.f, al1 = 1.f;
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+            }
+            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+            al0 = ex2(m0 - (mn0 == -INFINITY ? 0.f : mn0));
+            al1 = ex2(m1 - (mn1 == -INFINITY ? 0.f : mn1));
+            m0 = mn0;
+            m1 = mn1;
+        }
+        const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sc[b][2 * h] = ex2(sc[b][2 * h] - mu0);
+                sc[b][2 * h + 1] = ex2(sc[b][2 * h + 1] - mu1);
+                ps0 += sc[b][2 * h];
+                ps1 += sc[b][2 * h + 1];
+            }
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+        bool rescale = al0 != 1.f || al1 != 1.f;
+        if (__any_sync(0xffffffffu, vmax > s_max)) {
+            // every column c holds the same keys, so the maximum over g is warp-uniform
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, x));
+            const float gs = s_max / vmax;
+            al0 *= gs;
+            al1 *= gs;
+            s_max = vmax;
+            s_inv = 1.f / vmax;
+            rescale = true;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    o[cc][e][0] *= al0;
+                    o[cc][e][1] *= al1;
+                    o[cc][e][2] *= al0;
+                    o[cc][e][3] *= al1;
+                }
+        }
+        // P^T B fragments: (key g | g + 8, rows r0, r1) packed, then transposed to (row g, keys
+        // 2c, 2c+1 | 8 + 2c, 9 + 2c)
+        uint32_t pb[2][2];
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const float w0 = vs[b][0] * s_inv, w1 = vs[b][1] * s_inv;
+            pb[b][0] = movm_t(pack_f16x2(sc[b][0] * w0, sc[b][1] * w0));
+            pb[b][1] = movm_t(pack_f16x2(sc[b][2] * w1, sc[b][3] * w1));
+        }
+        // V^T A fragments from ldmatrix.trans over the code rows (as in consume_task: lane (g, c)
+        // gets cols 2g, 2g+1 of keys 2c, 2c+1 of matrix i = keys 8(i&1).. of chunk 2cc + (i>>1));
+        // even columns feed tile (cc, 0), odd ones tile (cc, 1).  Keys at or past kv_end get zero
+        // V entries, so 0 * NaN cannot occur.
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int key_lo = kc + 16 * b + 2 * c4;
+            const bool tail = kc + 16 * b + 16 > t.kv_end;
+            const uint32_t keep0 =
+                (key_lo < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 1 < t.kv_end ? 0xffff0000u : 0u);
+            const uint32_t keep1 =
+                (key_lo + 8 < t.kv_end ? 0x0000ffffu : 0u) | (key_lo + 9 < t.kv_end ? 0xffff0000u : 0u);
+            const int vrow = kr + 16 * b + ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc) {
+                uint32_t r[4], ev[4], od[4];
+                ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    // bytes (k0 c0, k0 c1, k1 c0, k1 c1) regrouped as (k0 c0, k1 c0, k0 c1, k1 c1)
+                    e4m3x4_to_f16x2x2(__byte_perm(r[i], 0u, 0x3120), ev[i], od[i]);
+                    if (tail) {
+                        const uint32_t keep = (i & 1) ? keep1 : keep0;
+                        ev[i] &= keep;
+                        od[i] &= keep;
+                    }
+                }
+                const uint32_t ae[4] = {ev[0], ev[2], ev[1], ev[3]};
+                const uint32_t ao[4] = {od[0], od[2], od[1], od[3]};
+                mma_f16_16816(o[cc][0], ae, pb[b][0], pb[b][1]);
+                mma_f16_16816(o[cc][1], ao, pb[b][0], pb[b][1]);
+            }
+        }
+    };
+
+    const int sub = RG::kKeys / kMathWarps;  // 32
+    bool ok = true;
+    for (int kv0 = t.kv_start; kv0 < t.kv_end; kv0 += RG::kKeys, ++ctr) {
+        const int s = ctr % RG::kStages;
+        if (!mbar_wait(sm.full_bar + 8 * s, (ctr / RG::kStages) & 1, sm.abort_flag)) {
+            ok = false;
+            break;
+        }
+        const uint32_t kst = sm.stages + s * RG::kStageBytes;
+        const uint32_t vst = kst + RG::kTensorBytes;
+        if (kv0 == t.kv_start) {
+            // f16 query rows in the k-order of the K fragments: k 2c, 2c+1 hold cols 16kk+4c, +1
+            // and k 2c+8, 2c+9 cols 16kk+4c+2, +3; rows past R are zero
+            const uint8_t *qs = sm.stages_gen + s * RG::kStageBytes + RG::kQOff;
+            const uint32_t *qp = g4 < R ? reinterpret_cast<const uint32_t *>(qs + g4 * HD * 2) : nullptr;
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+                const int w0 = kk * 8 + 2 * c4;
+                qb[kk][0] = qp ? bf16x2_to_f16x2(qp[w0]) : 0u;
+                qb[kk][1] = qp ? bf16x2_to_f16x2(qp[w0 + 1]) : 0u;
+            }
+            first_stage_seen();
+        }
+        const int k_lo = kv0 + w * sub;
+        const int k_hi = min(min(k_lo + sub, t.kv_end), lim_max);
+        const float *scl = reinterpret_cast<const float *>(sm.stages_gen + s * RG::kStageBytes + RG::kScaleOff);
+        if (k_lo < k_hi) keys32(kst, vst, scl, k_lo, k_lo - kv0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty_bar + 8 * s);
+    }
+
+    // back from units of s_max; row sums over the lanes of a column
+#pragma unroll
+    for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[cc][e][j] *= s_max;
+#pragma unroll
+    for (int x = 4; x < 32; x <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    }
+    // lane (g, c) holds columns 32cc + 16h + 2g, +1 of rows r0 (j = 0) and r1 (j = 1)
+    auto col_of = [&](int cc, int h) -> int { return 32 * cc + 16 * h + 2 * g4; };
+    if (w > 0) {  // warps 1..3 hand their triples to warp 0
+        float *my = sm.slots + (w - 1) * RG::kSlotFloats;
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                *reinterpret_cast<float2 *>(my + r0 * HD + col_of(cc, h)) = make_float2(o[cc][0][2 * h], o[cc][1][2 * h]);
+                *reinterpret_cast<float2 *>(my + r1 * HD + col_of(cc, h)) =
+                    make_float2(o[cc][0][2 * h + 1], o[cc][1][2 * h + 1]);
+            }
+        if (g4 == 0) {
+            my[16 * HD + r0] = m0;
+            my[16 * HD + r1] = m1;
+            my[16 * HD + 16 + r0] = l0;
+            my[16 * HD + 16 + r1] = l1;
+        }
+    }
+    // Every math warp reaches this barrier (all waits above are bounded), so the vote makes the
+    // decision to stop uniform and no warp is left waiting at a named barrier.
+    if (lane == 0) sm.vote[(iter & 1) * kMathWarps + w] = (!ok || *sm.abort_flag) ? 1 : 0;
+    named_bar_sync(sm.bar_id, kMathWarps * 32);
+    {
+        int bad = 0;
+        for (int v = 0; v < kMathWarps; ++v) bad |= sm.vote[(iter & 1) * kMathWarps + v];
+        ++iter;
+        if (bad) return false;
+    }
+    if (w == 0) {
+        float M0 = m0, M1 = m1;
+        for (int k = 1; k < kMathWarps; ++k) {
+            const float *ot = sm.slots + (k - 1) * RG::kSlotFloats;
+            M0 = fmaxf(M0, ot[16 * HD + r0]);
+            M1 = fmaxf(M1, ot[16 * HD + r1]);
+        }
+        const float U0 = M0 == -INFINITY ? 0.f : M0, U1 = M1 == -INFINITY ? 0.f : M1;
+        const float f0 = ex2(m0 - U0), f1 = ex2(m1 - U1);
+        l0 *= f0;
+        l1 *= f1;
+#pragma unroll
+        for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                o[cc][e][0] *= f0;
+                o[cc][e][1] *= f1;
+                o[cc][e][2] *= f0;
+                o[cc][e][3] *= f1;
+            }
+        for (int k = 1; k < kMathWarps; ++k) {
+            const float *ot = sm.slots + (k - 1) * RG::kSlotFloats;
+            const float ga = ex2(ot[16 * HD + r0] - U0), gb = ex2(ot[16 * HD + r1] - U1);
+            l0 += ga * ot[16 * HD + 16 + r0];
+            l1 += gb * ot[16 * HD + 16 + r1];
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 xa = *reinterpret_cast<const float2 *>(ot + r0 * HD + col_of(cc, h));
+                    const float2 xb = *reinterpret_cast<const float2 *>(ot + r1 * HD + col_of(cc, h));
+                    o[cc][0][2 * h] += ga * xa.x;
+                    o[cc][1][2 * h] += ga * xa.y;
+                    o[cc][0][2 * h + 1] += gb * xb.x;
+                    o[cc][1][2 * h + 1] += gb * xb.y;
+                }
+        }
+        m0 = M0;
+        m1 = M1;
+    }
+    named_bar_sync(sm.bar_id, kMathWarps * 32);
+    if (w != 0) return true;
+
+    // store: the final bf16 rows, or this chunk's normalised partial + log2-sum-exp
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int r = r0 + j;
+        if (r >= R) continue;
+        const float l = j ? l1 : l0, m = j ? m1 : m0;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        if (t.num_splits == 1) {
+            const int64_t tok = f.seq_start + t.q_start + r / p.G;
+            const int hq = t.kv_head * p.G + r % p.G;
+            __nv_bfloat16 *dst = p.out + (tok * p.Hq + hq) * HD;
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<uint32_t *>(dst + col_of(cc, h)) =
+                        pack_bf16x2(o[cc][0][2 * h + j] * inv, o[cc][1][2 * h + j] * inv);
+        } else {
+            const int64_t wr = (int64_t)t.ws_row + r;
+            float *dst = p.ws_o + wr * HD;
+#pragma unroll
+            for (int cc = 0; cc < HD / 32; ++cc)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *reinterpret_cast<float2 *>(dst + col_of(cc, h)) =
+                        make_float2(o[cc][0][2 * h + j] * inv, o[cc][1][2 * h + j] * inv);
+            if (g4 == 0) p.ws_lse[wr] = l > 0.f ? m + __log2f(l) : -INFINITY;
+        }
+    }
+    return true;
+}
+
 // Math warp w (0..3) runs decode task `f`.  `ctr` counts stages consumed on the ring, `iter` the
 // tasks run (vote parity).  `first_stage_seen()` runs once, after the first stage has landed.
 // Returns false when the math warps voted to stop (a wait gave up); every math warp returns the
@@ -214,6 +544,9 @@ __device__ __forceinline__ void drain(const Smem &sm, int ctr, int pw = 0, int n
 template <int HD, class RG, class F>
 __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
                              int lane, F first_stage_seen) {
+    if constexpr (RG::kFp8) {
+        if (f.t.q_rows * p.G <= 8) return consume_task_f8t<RG>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
+    }
     const int g4 = lane >> 2, c4 = lane & 3;
     const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;
     const int br_sh = 31 - __clz(BR);

@@ -151,6 +151,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
+// Transpose of an 8x8 matrix of 16-bit values held as one mma fragment (lane 4g + c holds row g,
+// columns 2c, 2c+1): afterwards the lane holds row g, columns 2c, 2c+1 of the transpose.
+__device__ __forceinline__ uint32_t movm_t(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 // A bf16 pair (lo in bits 0-15) -> the same values as f16x2, round to nearest even.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
