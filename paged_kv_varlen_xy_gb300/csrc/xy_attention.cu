@@ -51,15 +51,18 @@ using xy::dec::kMathWarps;
 // prefill or chunk task shares each K/V stage among 64 rows).  8-bit stages hold 128 keys (about
 // the bytes of a 64-key bf16 stage); with 16-token pages that is 32 copies per stage (codes and
 // scales of 8 pages), so four producer warps, one per ring slot, keep the ring ahead.
-enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2 };
+enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2, kFp8Tiny = 3 };
 
 template <int HD, int KIND, bool DYN = false>
 struct Cfg {
     using RG = typename std::conditional<
-        KIND == kFp8Narrow, xy::dec::RingF8<4, 16>,
+        KIND == kFp8Tiny, xy::dec::RingF8<2, 16, 128, true>,
+        typename std::conditional<KIND == kFp8Narrow, xy::dec::RingF8<4, 16>,
         typename std::conditional<KIND == kFp8Wide, xy::dec::RingF8<4, 16 * kMathWarps>,
-                                  xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type;
-    static constexpr int kProducers = KIND == kBf16 ? 2 : 4;
+                                  xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type>::type;
+    static constexpr int kProducers = KIND == kBf16 || KIND == kFp8Tiny ? 2 : 4;
+    // kFp8Tiny: half-size CTAs (two stages, two producers, transposed products only), two per SM
+    static constexpr int kMinBlocks = KIND == kFp8Tiny ? 2 : 1;
     static_assert(RG::kStages >= kProducers, "every producer owns a ring slot");
     // math warps, producer warps, then (dynamic deal over bf16 pages) the scheduler warp.  Over
     // 8-bit pages a ninth warp would put three warps on one SM sub-partition and cap the registers
@@ -79,7 +82,7 @@ struct Cfg {
 };
 
 template <int HD, int KIND, bool DYN>
-__global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DYN>::kMinBlocks)
     paged_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                            const AttnParams p) {
     using C = Cfg<HD, KIND, DYN>;
@@ -557,6 +560,8 @@ xy_status attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_
     // every task runs on the decode path (f16 MMAs on converted codes)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool narrow = num_tokens == num_seqs && p.G <= XY_FP8_NARROW_ROWS;
+    // pure decode with G <= 8 under the dynamic deal: two half-size CTAs per SM slot
+    if (narrow && p.G <= 8 && p.dyn) return launch<128, kFp8Tiny>(p, km, vm, 2 * num_ctas, merges, num_merges, st);
     return narrow ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
                   : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
 }

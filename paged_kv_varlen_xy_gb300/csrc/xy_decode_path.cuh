@@ -59,9 +59,11 @@ struct Ring {
 // of KEYS keys (one 128-byte row per key, 128-byte swizzle), their K scales then V scales (fp32),
 // and room for QR bf16 query rows.  A stage of 128 keys carries about as many bytes as a 64-key
 // bf16 stage, and gives each of four key-splitting math warps 32 keys.
-template <int NS, int QR, int KEYS = 128>
+template <int NS, int QR, int KEYS = 128, bool ONLY_T = false>
 struct RingF8 {
     static constexpr bool kFp8 = true;
+    // every task runs the transposed products (tasks of at most 8 rows; consume_task_f8t)
+    static constexpr bool kOnlyT = ONLY_T;
     static constexpr int kKeys = KEYS;
     static constexpr int kHalves = 1;
     static constexpr int kTensorBytes = KEYS * 128;
@@ -70,7 +72,7 @@ struct RingF8 {
     static constexpr int kQBytes = QR * 128 * 2;
     static constexpr int kStageBytes = (kQOff + kQBytes + 1023) / 1024 * 1024;  // stages stay 1024-aligned
     static constexpr int kStages = NS;
-    static constexpr int kMaxRows = QR;
+    static constexpr int kMaxRows = ONLY_T ? 8 : QR;
     static constexpr int kBytes = NS * kStageBytes;
     static constexpr int kSlotFloats = 16 * 128 + 32;
     static constexpr int kSlotBytes = (kMathWarps - 1) * kSlotFloats * 4;
@@ -545,7 +547,10 @@ template <int HD, class RG, class F>
 __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
                              int lane, F first_stage_seen) {
     if constexpr (RG::kFp8) {
-        if (f.t.q_rows * p.G <= 8) return consume_task_f8t<RG>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
+        if constexpr (RG::kOnlyT)
+            return consume_task_f8t<RG>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
+        else if (f.t.q_rows * p.G <= 8)
+            return consume_task_f8t<RG>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
     }
     const int g4 = lane >> 2, c4 = lane & 3;
     const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;
