@@ -401,7 +401,10 @@ xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, con
  * xy_paged_attention_dynamic ([XY] §2.2 component 2, the deal taken at run time).  Each CTA's
  * first producer warp claims the next task from task_counter[0] once it has issued the first
  * copy of its current task (no separate scheduler warp over 8-bit pages), so CTAs take tasks in
- * table order.  Outputs are bit-identical to xy_paged_attention_fp8's on the same tasks.
+ * table order.  Outputs are bit-identical to xy_paged_attention_fp8's on the same tasks.  A pure
+ * decode batch (num_tokens == num_seqs) with G <= 8 runs as 2 * num_ctas half-size CTAs (two per
+ * SM: two stages and two producer warps each), since the dynamic deal does not depend on the grid
+ * size; other batches run num_ctas CTAs.
  *   task_counter: as for xy_paged_attention_dynamic (device int32[2], 8-byte aligned, zero before
  *   the first call, returned to zero by every launch; overlapping calls need different counters).
  *   Every other argument, limit and error as for xy_paged_attention_fp8; XY_ERR_INVALID_ARG also
