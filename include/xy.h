@@ -30,6 +30,9 @@
  *   - Ownership: the caller allocates and frees every buffer; the library never allocates
  *     device memory, never frees, never synchronises.  Device calls are asynchronous on the
  *     given stream (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Device: a device call launches on the calling thread's current CUDA device (cudaGetDevice)
+ *     and keeps its per-device state (kernel attributes, the no-alloc scratch) by it; every device
+ *     pointer and the stream must belong to that device.  The Python binding checks this.
  *   - Errors: every call returns an xy_status; no exception crosses the ABI.  Host-visible
  *     argument errors are reported before anything is launched.  Errors that only the device
  *     can see (a page index outside [0, P), a slot outside the pool, a malformed task, a
@@ -404,7 +407,10 @@ xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, con
  * table order.  Outputs are bit-identical to xy_paged_attention_fp8's on the same tasks.  A pure
  * decode batch (num_tokens == num_seqs) with G <= 8 runs as 2 * num_ctas half-size CTAs (two per
  * SM: two stages and two producer warps each), since the dynamic deal does not depend on the grid
- * size; other batches run num_ctas CTAs.
+ * size; other batches run num_ctas CTAs.  Those half-size CTAs take tasks of at most 8 rows
+ * (q_rows * G <= 8), which every table built for such a batch has (each sequence has one new
+ * token, so q_rows = 1); a hand-made table with taller tasks sets XY_DEV_BAD_TASK and leaves their
+ * rows unwritten.
  *   task_counter: as for xy_paged_attention_dynamic (device int32[2], 8-byte aligned, zero before
  *   the first call, returned to zero by every launch; overlapping calls need different counters).
  *   Every other argument, limit and error as for xy_paged_attention_fp8; XY_ERR_INVALID_ARG also

@@ -143,12 +143,18 @@ def _dev(t, dtype, name):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    # the library launches on the current device (and picks per-device state by it)
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device} but the current CUDA device is cuda:{torch.cuda.current_device()}; "
+                         "call inside torch.cuda.device(...) of the tensors' device")
     return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream(stream):
     import torch
     s = torch.cuda.current_stream() if stream is None else stream
+    if s.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {s.device} but the current CUDA device is cuda:{torch.cuda.current_device()}")
     return ctypes.c_void_p(s.cuda_stream)
 
 

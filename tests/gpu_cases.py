@@ -18,14 +18,15 @@ def bits(t):
 
 
 def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=None, pool_fill=None, schedule=3,
-        transform=None):
+        transform=None, per_seq_oracle=False):
     """Run the CUDA step and the oracle step on workload `wl`.
 
     rows: list of (token, head) to compare, or None for every row.  sample_seqs: sequences whose
     pages the oracle receives (default: all).  pool_fill: value written to the whole pool before
     the step instead of random data (e.g. NaN, to check unused slots never leak into outputs).
     transform: callable applied in place to the device tensors before the step (both sides see
-    its result).
+    its result).  per_seq_oracle: run the oracle once per sampled sequence, on that sequence's pages
+    only (bounds the oracle's memory for very long contexts; the result is the same).
     Returns dict with both sides' results and error statistics.
     """
     dev = torch.device("cuda")
@@ -51,9 +52,26 @@ def run(wl, rows=None, sample_seqs=None, q_tile=None, kv_chunk=None, num_ctas=No
     torch.cuda.synchronize()
     err = int(batch.err.item())
 
-    ref = oracle.step.run_step(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
-                               bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"]), k_before, v_before,
-                               wl.scale, wl.causal, pool_pages=pages, rows=rows)
+    q_bits, kn_bits, vn_bits = bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"])
+    if per_seq_oracle:
+        cu = wl.cu_seqlens_q
+        pos = {int(p): i for i, p in enumerate(pages)}
+        k_ref, v_ref, outs = k_before.copy(), v_before.copy(), {}
+        for s in sample_seqs:
+            sp = np.unique(bt[s][bt[s] >= 0])
+            sel = np.array([pos[int(p)] for p in sp])
+            srows = [(t, h) for (t, h) in rows if cu[s] <= t < cu[s + 1]]
+            r = oracle.step.run_step(cu, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks, q_bits,
+                                     kn_bits, vn_bits, k_before[sel], v_before[sel], wl.scale, wl.causal,
+                                     pool_pages=sp, rows=srows)
+            k_ref[sel], v_ref[sel] = r["k_pages"], r["v_pages"]
+            outs.update(zip(srows, r["out"]))
+        ref = dict(block_table=r["block_table"], slots=r["slots"], k_pages=k_ref, v_pages=v_ref,
+                   out=np.stack([outs[x] for x in rows]))
+    else:
+        ref = oracle.step.run_step(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                                   q_bits, kn_bits, vn_bits, k_before, v_before, wl.scale, wl.causal,
+                                   pool_pages=pages, rows=rows)
     gpu_out = oracle.bf16_bits_to_f64(bits(out))
     if rows is not None:
         gpu_out = np.stack([gpu_out[t, h] for (t, h) in rows]) if rows else np.zeros((0, wl.head_dim))

@@ -167,10 +167,15 @@ def test_fp8_full_size_sampled_rows(name, schedule):
                               wl.scale)
     torch.cuda.synchronize()
     xystep.check(batch)
-    # sampled sequences: short ones only for skew (a 131072-key sequence is too large for the oracle)
+    # sampled sequences; under the dynamic deal (the bench's launch) the skew sample also holds one of
+    # the 131072-key sequences: its 16 split chunks per tile, their merge and, on this pure decode
+    # batch with G = 8, the two-CTA-per-SM kernel (the oracle quantizes its 512 pages, about two
+    # minutes of host time, so the greedy-deal run keeps to the short ones)
     rng = np.random.default_rng(7)
     ok_seqs = [i for i in range(wl.num_seqs) if wl.context_lens[i] <= 8192]
     sample = sorted(rng.choice(ok_seqs, size=min(6, len(ok_seqs)), replace=False).tolist())
+    if name == "skew" and schedule == DYN:
+        sample = sorted(sample[:5] + [int(np.argmax(wl.context_lens))])
     bt = batch.block_table_host
     pages = np.unique(np.concatenate([bt[i][bt[i] >= 0] for i in sample]))
     idx = torch.from_numpy(pages).long().cuda()
@@ -182,6 +187,7 @@ def test_fp8_full_size_sampled_rows(name, schedule):
                                    wl.scale, wl.causal, pool_pages=pages, rows=rows)
     assert np.array_equal(codes[0].index_select(0, idx).cpu().numpy(), ref["k_codes"])
     assert np.array_equal(codes[1].index_select(0, idx).cpu().numpy(), ref["v_codes"])
+    assert np.array_equal(scl[0].index_select(0, idx).cpu().numpy().view(np.uint32), ref["k_scales"].view(np.uint32))
     assert np.array_equal(scl[1].index_select(0, idx).cpu().numpy().view(np.uint32), ref["v_scales"].view(np.uint32))
     got = oracle.bf16_bits_to_f64(_bits(out))
     got = np.stack([got[t, h] for (t, h) in rows])

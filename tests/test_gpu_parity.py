@@ -112,7 +112,7 @@ def test_full_size_decode_sampled():
     rng = np.random.default_rng(0)
     seqs = sorted(rng.choice(wl.num_seqs, size=6, replace=False).tolist())
     seqs.append(int(np.argmax(wl.context_lens)))
-    r = run(wl, rows=sample_rows(wl, seqs, rng), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng), sample_seqs=seqs, schedule=4)
     assert_parity(r)
 
 
@@ -120,7 +120,7 @@ def test_full_size_prefill_sampled():
     wl = workloads.prefill()
     rng = np.random.default_rng(1)
     seqs = sorted({int(np.argmax(wl.q_lens)), int(np.argmin(wl.q_lens)), int(rng.integers(wl.num_seqs))})
-    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=256 // wl.group), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=12, q_tile=256 // wl.group), sample_seqs=seqs, schedule=4)
     assert_parity(r)
 
 
@@ -128,16 +128,19 @@ def test_full_size_mixed_sampled():
     wl = workloads.mixed()
     rng = np.random.default_rng(2)
     seqs = [0, 5, 8, 60, 127, int(np.argmax(wl.context_lens))]
-    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=256 // wl.group), sample_seqs=seqs)
+    r = run(wl, rows=sample_rows(wl, seqs, rng, per_seq=8, q_tile=256 // wl.group), sample_seqs=seqs, schedule=4)
     assert_parity(r)
 
 
 def test_full_size_skew_sampled():
+    # every one of the four 131072-key sequences (all 64 heads of each), and two 512-key ones
     wl = workloads.skew()
-    long_seq = int(np.argmax(wl.context_lens))
-    seqs = [long_seq, int(np.argmin(wl.context_lens))]
+    long_seqs = [int(i) for i in np.flatnonzero(wl.context_lens == wl.context_lens.max())]
+    assert len(long_seqs) == 4
     rng = np.random.default_rng(3)
-    r = run(wl, rows=sample_rows(wl, seqs, rng), sample_seqs=seqs)
+    short = [int(i) for i in rng.choice(np.flatnonzero(wl.context_lens < wl.context_lens.max()), 2, replace=False)]
+    seqs = sorted(long_seqs + short)
+    r = run(wl, rows=sample_rows(wl, seqs, rng), sample_seqs=seqs, per_seq_oracle=True, schedule=4)
     assert_parity(r)
 
 
