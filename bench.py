@@ -1,21 +1,27 @@
-"""Benchmark of one step of the paged-KV varlen attention path on GB300.
+"""Benchmark of the paged-KV varlen attention path on GB300.
 
-A step is one pass of the whole hot path over one batch: slot mapping, KV append, paged
-attention (+ split-KV merge), with the block table and task table (host-built per batch)
-already on the device.  The default workload is the decode batch (64 sequences, q = 1, context
-U[128, 4096], 32/32 heads, d = 128, 16-token pages); `--config` picks another.
+A step is one pass of the whole hot path over one batch: the KV append (slot mapping fused into
+the copy kernel), paged attention and the split-KV merge, with the block table and task table
+(host-built per batch) already on the device.  The default run measures the decode batch (64
+sequences, q = 1, context U[128, 4096], 32/32 heads, d = 128, 16-token pages) for the headline
+line, and in the same run the packed prefill, mixed continuous, long-context skew,
+speculative-verify and prefix-shared batches, each under its own key with the same
+measurements.  `--config` picks the headline batch, `--only` measures that one alone.
 
-Prints one JSON line (rank 0).  `value` is device-timed throughput of the step with inputs
-resident in HBM; `e2e` is the same metric through the public Python API with pinned host
-inputs copied in and the output copied out every step; `roofline` reports the attention
-kernel's achieved bandwidth (or TFLOP/s) against the measured peak; `cpu_baseline` times the
-oracle on a bounded sample on the host cores.  `--impl reference` times the oracle alone.
+Prints one JSON line (rank 0).  Per batch: `value` is device-timed throughput of the step with
+inputs resident in HBM (CUDA events around exactly `--steps` steps; L2 flushed before each step
+when the batch's working set would otherwise stay in L2); `roofline` reports the attention
+kernel's algorithmic bytes (or flops) over its average launch time, taken in a separate
+instrumented pass, against the measured peak; `e2e` is the same metric through the public Python
+API with pinned host inputs copied in and the output copied out every step; `cpu_baseline` times
+the oracle on a bounded sample on the host cores; `clocks` holds the SM clock and throttle
+reasons sampled during the timed steps.  `--impl reference` times the oracle alone.
 Multi-GPU (torchrun): independent replicas, one per rank (weak scaling, no data-path collective).
 """
 
 import argparse
+import ctypes
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -44,7 +50,12 @@ DESC = {
     "prefill": "packed prefill: 16 seqs lognormal(512,1) in [32,8192], causal, Hq 32 / Hkv 8, d 128, bs 16",
     "mixed": "mixed: 8 chunks x 512 (prior U[0,16384]) + 120 decodes L~U[256,32768], Hq 32 / Hkv 8, d 128, bs 16",
     "skew": "long-context skew: 256 decodes (4 x 131072, 252 x 512), Hq 64 / Hkv 8, d 128, bs 256",
+    "verify": "speculative verify: 64 seqs, q~U{2..8} over L~U[512,8192], Hq 32 / Hkv 8, d 128, bs 16",
+    "prefix": "prefix-shared decode: 64 seqs x L=4096, first 3584 tokens on shared pages, Hq=Hkv=32, d 128, bs 16",
 }
+# measured in the default run beside the headline batch, under these keys of the JSON line
+SECONDARY = {"prefill": "prefill", "mixed": "mixed", "skew": "skew", "verify": "verify", "prefix": "prefix_shared"}
+SECONDARY_FP8 = {"prefill": "prefill", "mixed": "mixed", "skew": "skew"}
 
 
 def peaks():
@@ -73,10 +84,11 @@ def measured_traffic(config):
     return e["bytes_per_launch"] if h.hexdigest()[:16] == e["kernel_hash"] else None
 
 
-def work(wl, kv="bf16"):
+def work(wl, kv="bf16", block_table=None):
     """Algorithmic work of one step: attention bytes (K/V read once + Q in + O out), append bytes
     (new K/V read + written), and flops (4 d per visible (row, key) pair per query head).  A stored
-    K or V row is d bf16 values, or over 8-bit pages d codes and one fp32 scale."""
+    K or V row is d bf16 values, or over 8-bit pages d codes and one fp32 scale.  With a block table
+    whose rows share pages (prefix sharing), `unique_attn_bytes` counts each physical page once."""
     d, Hq, Hkv = wl.head_dim, wl.num_heads_q, wl.num_heads_kv
     L = wl.context_lens.astype(np.int64)
     q = wl.q_lens.astype(np.int64)
@@ -89,25 +101,96 @@ def work(wl, kv="bf16"):
     else:
         pairs = int(np.sum(q * L))
     flops = 4 * d * Hq * pairs
-    return dict(attn_bytes=kv_bytes + qo_bytes, append_bytes=append_bytes, flops=flops, kv_bytes=kv_bytes)
+    w = dict(attn_bytes=kv_bytes + qo_bytes, append_bytes=append_bytes, flops=flops, kv_bytes=kv_bytes)
+    if block_table is not None:
+        # keys held by each distinct physical page (the last page of a row may be partial)
+        bs = wl.block_size
+        held = {}
+        for i, row in enumerate(np.asarray(block_table)):
+            n = -(-int(L[i]) // bs)
+            for j in range(n):
+                held[int(row[j])] = max(held.get(int(row[j]), 0), min(bs, int(L[i]) - j * bs))
+        w["unique_attn_bytes"] = int(sum(held.values()) * 2 * Hkv * row_bytes) + qo_bytes
+    return w
 
 
-class ClockSampler:
-    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons; `summary(t0, t1)` keeps
-    the samples whose host arrival time lies inside the timed region [t0, t1] (perf_counter)."""
+class NvmlClocks:
+    """SM clock and clock-event (throttle) reasons read through NVML every `period_s` while
+    running (reads only; nothing is set).  The GPU is found by the UUID of the CUDA device, so the
+    samples belong to it whatever CUDA_VISIBLE_DEVICES maps."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev, period_s=0.001):
+        self.period_s, self.samples, self.ok = period_s, [], False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+            self.h = ctypes.c_void_p()
+            if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+                return
+            self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 \
+                else None
+            self.ok = True
+        except (OSError, AttributeError, RuntimeError):
+            self.ok = False
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop:
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0 and \
+                    self.reasons_fn(self.h, ctypes.byref(rs)) == 0:
+                self.samples.append((time.perf_counter(), float(clk.value), int(rs.value)))
+            time.sleep(self.period_s)
+
+    def start(self):
+        self.samples, self._stop = [], False
+        if self.ok:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def stop(self):
+        self._stop = True
+        if self.ok:
+            self.thread.join()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:   # a timed region shorter than one NVML read: the samples nearest to it
+            inside = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+        if not inside:
+            return None
+        reasons = sorted({n for _, _, r in inside for b, n in self.REASONS.items() if r & b})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside),
+                "samples_in_window": sum(1 for s in inside if t0 <= s[0] <= t1),
+                "window_ms": 1e3 * (t1 - t0), "source": "NVML, every 1 ms during the timed steps"}
+
+
+class SmiClocks:
+    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons over the whole run (the
+    query line of the profiling recipe); `summary(t0, t1)` keeps the samples inside [t0, t1]."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index):
-        self.device_index = device_index
+    def __init__(self, dev):
+        uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+        self.gpu = f"GPU-{uuid}" if uuid is not None else str(dev.index)
         self.proc = None
         self.lines = []
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
@@ -148,13 +231,14 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "window": "timed region" if t0 is not None else "whole run"}
+                "samples": len(sm), "source": "nvidia-smi every 20 ms, " +
+                ("timed steps" if t0 is not None else "whole run")}
 
 
 def oracle_sample(wl, vals, budget_s=12.0, max_seqs=None, kv="bf16"):
     """Time the oracle (as it stands) on a bounded sample of the workload's sequences, all their
     rows (over 8-bit pages: its 8-bit step, quantizing the sampled pages first).  Returns
-    (seconds, sampled work dict, description)."""
+    (seconds, sampled work dict, description, sampled sequences, seconds per sequence)."""
     import oracle
 
     def bits(t):
@@ -292,8 +376,8 @@ def throughput(config, w, seconds):
     return (w["attn_bytes"] + w["append_bytes"]) / seconds / 1e9
 
 
-def describe(args):
-    return (DESC[args.config] + (", 8-bit E4M3 KV pages + per-row fp32 scales" if args.kv == "fp8" else "") +
+def describe(config, args):
+    return (DESC[config] + (", 8-bit E4M3 KV pages + per-row fp32 scales" if args.kv == "fp8" else "") +
             (", dynamic deal (CTAs claim tasks at run time)" if args.schedule == 4 else
              f", static deal (task-table schedule {args.schedule})"))
 
@@ -314,52 +398,22 @@ def run_reference(args, rank, world):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(args)},
+            "config": {"workload": describe(args.config, args)},
             "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="decode", choices=list(workloads.CONFIGS))
-    ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="page format of the KV cache")
-    ap.add_argument("--schedule", type=int, default=None, choices=[0, 1, 2, 3, 4],
-                    help="task-table schedule (default: 4, the dynamic deal)")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference step")
-    args = ap.parse_args()
-    args.warmup = max(3, args.warmup)
-    args.default_schedule = 4
-    if args.schedule is None:
-        args.schedule = args.default_schedule
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if args.impl == "xy" else "gloo")
-    if args.impl == "reference":
-        run_reference(args, rank, world)
-        return
-
+def measure(config, args, dev, pk, world, rank, cpu_budget, smi):
+    """Every measurement of one batch: device-timed steps, the instrumented pass (attention and
+    append times), a traced launch (deal balance), the end-to-end serving loop and the oracle
+    baseline.  Returns the batch's JSON object (the headline line's fields for the headline)."""
     import paged_kv_varlen_xy_gb300 as xy
-    from paged_kv_varlen_xy_gb300 import build as xybuild
     from paged_kv_varlen_xy_gb300 import step as xystep
-    xybuild.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    pk = peaks()
 
-    wl = workloads.make(args.config)
+    wl = workloads.make(config)
     vals = wl.tensors(dev)
     fp8 = args.kv == "fp8"
-    w = work(wl, args.kv)
     # over 8-bit pages a batch with prefill / chunk sequences runs them on the tile path over bf16
     # copies of their pages and its decode sequences on the 8-bit decode path (when the two kinds
     # form contiguous sequence ranges and the tile shape allows)
@@ -375,6 +429,14 @@ def main():
                                   wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, kv_fp8=fp8,
                                   schedule=args.schedule)
         parts = [batch.plan]
+    shared_bt = None
+    if wl.shared_prefix_tokens:
+        # prefix sharing: every row's first pages are row 0's (the kernels read pages only through
+        # the block table); the new tokens land after the prefix, in each row's own pages
+        shared_bt = workloads.share_prefix(batch.block_table_host, wl.shared_prefix_tokens, wl.block_size)
+        batch.block_table.copy_(torch.from_numpy(shared_bt))
+        batch.block_table_host = shared_bt
+    w = work(wl, args.kv, block_table=shared_bt)
     pl = parts[0]
     n_tasks = sum(int(x.tasks.shape[0]) for x in parts)
     n_merges = sum(int(x.merges.shape[0]) for x in parts)
@@ -393,17 +455,16 @@ def main():
         del rows
         torch.cuda.synchronize()
 
-    def step(ev=None):
-        if ev:
-            ev[2].record(stream)
-        xy.xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, wl.block_size, P, batch.slots, batch.err)
+    def append():
         if fp8:
-            xy.xy_kv_append_fp8(vals["k_new"], vals["v_new"], batch.slots, vals["k_codes"], vals["v_codes"],
-                                vals["k_scales"], vals["v_scales"], batch.err)
+            xy.xy_kv_append_paged_fp8(vals["k_new"], vals["v_new"], batch.cu, batch.ctx, batch.block_table,
+                                      vals["k_codes"], vals["v_codes"], vals["k_scales"], vals["v_scales"], batch.err,
+                                      slot_mapping=batch.slots)
         else:
-            xy.xy_kv_append(vals["k_new"], vals["v_new"], batch.slots, vals["k_pool"], vals["v_pool"], batch.err)
-        if ev:
-            ev[0].record(stream)
+            xy.xy_kv_append_paged(vals["k_new"], vals["v_new"], batch.cu, batch.ctx, batch.block_table,
+                                  vals["k_pool"], vals["v_pool"], batch.err, slot_mapping=batch.slots)
+
+    def attend():
         if split:
             xystep.attention_fp8_split(batch, vals["q"], vals["k_codes"], vals["v_codes"], vals["k_scales"],
                                        vals["v_scales"], wl.scale, out)
@@ -423,32 +484,74 @@ def main():
         else:
             xy.xy_paged_attention(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"], vals["v_pool"],
                                   wl.scale, wl.causal, pl.tasks, pl.merges, pl.num_ctas, pl.workspace, batch.err, out)
-        if ev:
-            ev[1].record(stream)
+
+    def step():
+        append()
+        attend()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     xystep.check(batch)
 
-    # ---- device-timed region: K steps, inputs resident in HBM ----
-    n_launch_per_step = 2 + sum(1 + (1 if x.merges.shape[0] else 0) for x in parts) + (1 if split and batch.tile else 0)
-    attn_ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
-    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
-        time.sleep(0.25)
-        w0 = time.perf_counter()
-        t_start.record(stream)
-        for k in range(args.steps):
-            step(attn_ev[k])
-        t_stop.record(stream)
+    # Between timed steps: a batch whose data would stay in the 129 MB L2 from one step to the next
+    # gets the L2 flushed (a write of twice its size) before every step, outside the timed events;
+    # larger batches run back to back.
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    touched = w.get("unique_attn_bytes", w["attn_bytes"]) + w["append_bytes"]
+    flush = touched < 4 * l2 or shared_bt is not None   # (shared pages would stay in L2 between steps)
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.int32, device=dev) if flush else None
+
+    def timed(fn, k_steps, events_per_step=0):
+        """k_steps calls of fn on the device; with a flush, each between a flush and its own event
+        pair.  Returns (ms per step, per-step marks for events_per_step > 0)."""
+        marks = [[torch.cuda.Event(enable_timing=True) for _ in range(events_per_step)] for _ in range(k_steps)]
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(k_steps if flush else 1)]
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize()
-        w1 = time.perf_counter()
-        time.sleep(0.05)
+        if not flush:
+            pairs[0][0].record(stream)
+        for k in range(k_steps):
+            if flush:
+                flush_buf.fill_(k)
+                pairs[k][0].record(stream)
+            fn(marks[k])
+            if flush:
+                pairs[k][1].record(stream)
+        if not flush:
+            pairs[0][1].record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in pairs) / k_steps
+        return ms, marks
+
+    # ---- device-timed region: exactly K steps, inputs resident in HBM, two events per step (or per run) ----
+    nv = NvmlClocks(dev).start()
+    time.sleep(0.05)
+    w0 = time.perf_counter()
+    ms_step, _ = timed(lambda m: step(), args.steps)
+    w1 = time.perf_counter()
+    time.sleep(0.02)
+    nv.stop()
     xystep.check(batch)
+    ms_per_step = max_over_ranks(ms_step, world, device=dev)
+    clocks = nv.summary(w0, w1) or smi.summary(w0, w1)
+    if not clocks or not clocks.get("samples"):
+        clocks = smi.summary()
+
+    # ---- instrumented pass (not the timed region): append and attention times per step ----
+    def marked(m):
+        m[0].record(stream)
+        append()
+        m[1].record(stream)
+        attend()
+        m[2].record(stream)
+    _, marks = timed(marked, args.steps, 3)
+    xystep.check(batch)
+    append_ms = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
+    attn_ms = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
+
     # how evenly the deal spread the work: one traced launch after the timed region
     deal_trace = None
     if not fp8 and not split:
@@ -459,25 +562,25 @@ def main():
         torch.cuda.synchronize()
         xystep.check(batch)
         deal_trace = xy.trace_summary(trace.cpu().numpy())
-    total_ms = max_over_ranks(t_start.elapsed_time(t_stop), world, device=dev)
-    ms_per_step = total_ms / args.steps
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b, _ in attn_ev)
-    append_ms = statistics.mean(c.elapsed_time(a) for a, b, c in attn_ev)   # slot mapping + append
-    value = job_throughput(args.config, w, ms_per_step / 1e3, world)
-    unit, bound = unit_of(args.config)
-    input_bytes = sum(t.numel() * t.element_size() for k, t in vals.items()
-                      if k in ("q", "k_new", "v_new") or (k in ("k_codes", "v_codes", "k_scales", "v_scales") if fp8
-                                                         else k in ("k_pool", "v_pool")))
-    traffic_key = (args.config + ("_fp8" if fp8 else "") +
+
+    value = job_throughput(config, w, ms_per_step / 1e3, world)
+    unit, bound = unit_of(config)
+    traffic_key = (config + ("_fp8" if fp8 else "") +
                    (f"_s{args.schedule}" if args.schedule != args.default_schedule else ""))
-    kname = attention_kernel(wl, args.kv, args.schedule) if not split else "dequant_pages_kernel + meta_attention_kernel + paged_attention_kernel<fp8>"
+    kname = (attention_kernel(wl, args.kv, args.schedule) if not split else
+             "dequant_pages_kernel + meta_attention_kernel + paged_attention_kernel<fp8>")
     attn_s = attn_ms / 1e3
     if bound == "hbm":
-        achieved = w["attn_bytes"] / attn_s / 1e9
+        # prefix sharing: the bytes DRAM must deliver are the distinct pages' (the logical bytes,
+        # as if every row had its own copy, are reported beside them)
+        alg = w.get("unique_attn_bytes", w["attn_bytes"])
+        achieved = alg / attn_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
-                "traffic": measured_traffic(traffic_key), "kernel": kname, "algorithmic_bytes": w["attn_bytes"],
+                "traffic": measured_traffic(traffic_key), "kernel": kname, "algorithmic_bytes": alg,
                 "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
-        if args.config == "mixed":
+        if "unique_attn_bytes" in w:
+            roof.update({"logical_bytes": w["attn_bytes"], "logical_gbs": w["attn_bytes"] / attn_s / 1e9})
+        if config in ("mixed", "verify"):
             # both bounds matter: time at the roofline = bytes / HBM + flops / tensor (the sum, as the
             # two phases need not overlap) and max(.) (perfect overlap)
             t_sum = w["attn_bytes"] / (pk["hbm"] * 1e9) + w["flops"] / (pk["tc"] * 1e12)
@@ -488,16 +591,18 @@ def main():
         achieved = w["flops"] / attn_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["tc"], "unit": "TFLOP/s",
                 "frac": achieved / pk["tc"], "traffic": measured_traffic(traffic_key), "kernel": kname,
-                "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"]}
+                "algorithmic_flops": w["flops"], "avg_launch_ms": attn_ms, "peak_source": pk["source"],
+                "frac_of_sustained": achieved / pk["tc_sustained"] if pk.get("tc_sustained") else None}
     roof["frac_nominal"] = (roof["achieved"] / (NOMINAL["hbm"] if roof["bound"] == "hbm" else NOMINAL["tc"]))
     roof["peak_nominal"] = NOMINAL["hbm"] if roof["bound"] == "hbm" else NOMINAL["tc"]
+    roof["timed"] = ("attention call (kernel" + (" + combine" if n_merges else "") + "), CUDA events, instrumented "
+                     "pass after the timed steps" if not split else
+                     "page dequantization + tile attention + 8-bit decode attention (+ combines), CUDA events")
     append_gbs = w["append_bytes"] / (append_ms / 1e3) / 1e9
     append_roof = {"achieved": append_gbs, "unit": "GB/s", "peak": pk["hbm"], "frac": append_gbs / pk["hbm"],
                    "algorithmic_bytes": w["append_bytes"], "avg_ms": append_ms,
-                   "timed": "slot mapping + KV append, CUDA events", "kernel": "kv_append_fp8_kernel" if fp8 else
-                   "kv_append_kernel"}
-    roof["timed"] = ("attention call (kernel" + (" + combine" if n_merges else "") + "), CUDA events" if not split else
-                     "page dequantization + tile attention + 8-bit decode attention (+ combines), CUDA events")
+                   "timed": "slot mapping + KV append (one fused kernel), CUDA events",
+                   "kernel": "kv_append_paged_fp8_kernel" if fp8 else "kv_append_paged_kernel"}
 
     # ---- end to end through the public API: pinned host inputs in, output out, every step ----
     host = {k: vals[k].cpu().pin_memory() for k in ("q", "k_new", "v_new")}
@@ -510,7 +615,6 @@ def main():
     # holds one plan, its inputs' upload, the step and its output's download.
     planner = xystep.Planner(wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.block_size, wl.max_blocks, wl.causal,
                              device=dev, num_ctas=pl.num_ctas, kv_fp8=fp8, schedule=args.schedule)
-
     split_planner = (xystep.Fp8SplitPlanner(wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.block_size,
                                             wl.max_blocks, wl.causal, device=dev, num_ctas=pl.num_ctas)
                      if split else None)
@@ -518,7 +622,7 @@ def main():
     def make_batch(stream=None):
         if split:
             return split_planner.plan(meta["cu"], meta["ctx"], meta["free"], stream=stream)
-        return planner.plan(meta["cu"], meta["ctx"], meta["free"], stream=stream)
+        return planner.plan(meta["cu"], meta["ctx"], meta["free"], stream=stream, block_table=shared_bt)
 
     plan_times = []
     out_hosts = [out_host, torch.empty(out.shape, dtype=out.dtype).pin_memory()]
@@ -592,7 +696,7 @@ def main():
     h2d = sum(host[x].numel() * 2 for x in host) + planner_now.last_upload_bytes
     d2h = out_host.numel() * 2
     e2e_s = max_over_ranks(e2e_total / args.steps, world, device=dev)
-    e2e_val = job_throughput(args.config, w, e2e_s, world)
+    e2e_val = job_throughput(config, w, e2e_s, world)
 
     # the task-table build alone (host, into preallocated record arrays), as a step re-plans it
     tt_us = None
@@ -609,50 +713,112 @@ def main():
         tt_us = 1e6 * statistics.median(tt[5:])
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        secs, sw, desc, seqs, seq_secs = oracle_sample(wl, vals, budget_s=12.0, kv=args.kv)
-        cpu = {"value": throughput(args.config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
-               "sample": desc}
+    if rank == 0 and world == 1 and cpu_budget > 0:
+        secs, sw, desc, seqs, seq_secs = oracle_sample(wl, vals, budget_s=cpu_budget, kv=args.kv)
+        cpu = {"value": throughput(config, sw, secs), "unit": unit, "cores": 1, "kind": "oracle",
+               "sample": desc + (" (pages not shared: the oracle reads each sequence's own pages)"
+                                 if shared_bt is not None else "")}
         # the same sample on every host core (one single-threaded process per core)
         sub, secs_all, ncores, desc_all = oracle_sample_cores(wl, vals, seqs, seq_secs, kv=args.kv)
-        cpu["all_cores"] = {"value": throughput(args.config, work(sub, args.kv), secs_all), "unit": unit,
+        cpu["all_cores"] = {"value": throughput(config, work(sub, args.kv), secs_all), "unit": unit,
                             "cores": ncores, "kind": "oracle", "sample": desc_all}
 
-    clocks = clk.summary(w0, w1)
-    if clocks["samples"] == 0:  # the timed region was shorter than one sampling period
-        clocks = clk.summary()
-        clocks["window"] = "whole run (timed region shorter than the 20 ms sampling period)"
+    n_launch_per_step = 1 + sum(1 + (1 if x.merges.shape[0] else 0) for x in parts) + (1 if split and batch.tile
+                                                                                      else 0)
+    res = {
+        "workload": describe(config, args), "value": value, "unit": unit, "ms_per_step": ms_per_step,
+        "steps": args.steps, "warmup": args.warmup,
+        "tokens_per_s": wl.num_tokens * world / (ms_per_step / 1e3),
+        "tflops": w["flops"] / (ms_per_step / 1e3) / 1e12,
+        "l2": (f"L2 flushed before every timed step (a {2 * l2 / 1e6:.0f} MB write outside the step's events): the "
+               f"step touches {touched / 1e6:.0f} MB" if flush else
+               f"no flush: the step touches {touched / 1e6:.0f} MB, far more than the {l2 / 1e6:.0f} MB L2"),
+        "step": "kv_append (slot mapping fused) + paged_attention" + (" + combine" if n_merges else "") +
+                (" (8-bit pages: tile part on bf16 page copies, decode part on codes)" if split else ""),
+        "num_tasks": n_tasks, "num_merges": n_merges, "num_ctas": pl.num_ctas, "schedule": args.schedule,
+        "balance" if args.schedule != 4 else "balance_if_dealt": pl.stats["balance"],
+        "deal_trace": deal_trace,
+        "roofline": roof,
+        "append": append_roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3,
+                "loop": "per step: inputs H2D from pinned memory (upload stream), tables re-planned on the host "
+                        "and uploaded, the step (compute stream), output D2H into pinned memory (download stream); "
+                        "step k+1's inputs go up while step k computes, and the host waits for step k's output "
+                        "after enqueuing step k+1",
+                "plan_us": 1e6 * statistics.median(plan_times[args.warmup:]),
+                "task_table_us": tt_us},
+        "gpu_launches": n_launch_per_step * args.steps,
+        "clocks": clocks,
+    }
+    del vals, batch, out, host, out_hosts, dev_in, planner, split_planner, flush_buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="decode", choices=[c for c in workloads.CONFIGS if c != "tiny"],
+                    help="headline batch")
+    ap.add_argument("--only", action="store_true", help="measure the headline batch alone")
+    ap.add_argument("--impl", default="xy", choices=["xy", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"], help="page format of the KV cache")
+    ap.add_argument("--schedule", type=int, default=None, choices=[0, 1, 2, 3, 4],
+                    help="task-table schedule (default: 4, the dynamic deal)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.default_schedule = 4
+    if args.schedule is None:
+        args.schedule = args.default_schedule
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "xy" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    from paged_kv_varlen_xy_gb300 import build as xybuild
+    xybuild.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    pk = peaks()
+    secondary = {} if args.only else {c: k for c, k in (SECONDARY_FP8 if args.kv == "fp8" else SECONDARY).items()
+                                      if c != args.config}
+    with SmiClocks(dev) as smi:
+        head = measure(args.config, args, dev, pk, world, rank, 0 if args.no_cpu_baseline else 12.0, smi)
+        extra = {key: measure(c, args, dev, pk, world, rank, 0 if args.no_cpu_baseline else 5.0, smi)
+                 for c, key in secondary.items()}
+        run_clocks = smi.summary()
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "e4m3 KV, f16 MMA" if fp8 else "bf16", "data": "synthetic",
-            "config": {"workload": describe(args), "parallelism": f"replicas x{world}",
-                       "l2": (f"inputs (q, new K/V, page pool) {input_bytes / 1e6:.0f} MB, larger than the 129 MB L2; "
-                              "no flush between steps") if input_bytes > 129e6 else
-                             f"inputs {input_bytes / 1e6:.1f} MB fit in the 129 MB L2 (parity-size batch)",
-                       "step": "slot_mapping + kv_append + paged_attention" + (" + combine" if n_merges else "") +
-                               (" (8-bit pages: tile part on bf16 page copies, decode part on codes)" if split else ""),
-                       "tokens_per_s": wl.num_tokens * world / (ms_per_step / 1e3),
-                       "tflops": w["flops"] / (ms_per_step / 1e3) / 1e12,
-                       "num_tasks": n_tasks, "num_merges": n_merges,
-                       "num_ctas": pl.num_ctas, "schedule": args.schedule,
-                       "balance" if args.schedule != 4 else "balance_if_dealt": pl.stats["balance"],
-                       "deal_trace": deal_trace},
-            "roofline": roof,
-            "append": append_roof,
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_s * 1e3,
-                    "loop": "per step: inputs H2D from pinned memory (upload stream), tables re-planned on the host "
-                            "and uploaded, the step (compute stream), output D2H into pinned memory (download stream); "
-                            "step k+1's inputs go up while step k computes, and the host waits for step k's output "
-                            "after enqueuing step k+1",
-                    "plan_us": 1e6 * statistics.median(plan_times[args.warmup:]),
-                    "task_table_us": tt_us},
-            "gpu_launches": n_launch_per_step * args.steps,
-            "clocks": clocks,
+            "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 KV, f16 MMA" if args.kv == "fp8" else "bf16", "data": "synthetic",
+            "config": {"workload": head["workload"], "parallelism": f"replicas x{world}", "l2": head["l2"],
+                       "step": head["step"], "tokens_per_s": head["tokens_per_s"], "tflops": head["tflops"],
+                       "num_tasks": head["num_tasks"], "num_merges": head["num_merges"], "num_ctas": head["num_ctas"],
+                       "schedule": head["schedule"], "deal_trace": head["deal_trace"],
+                       "also_measured": {k: DESC[c] for c, k in secondary.items()}},
+            "roofline": head["roofline"],
+            "append": head["append"],
+            "cpu_baseline": head["cpu_baseline"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "clocks_whole_run": run_clocks,
         }
+        line.update(extra)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

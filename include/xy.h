@@ -151,6 +151,21 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
                        void *stream);
 
 /*
+ * a2 + a3 in one launch (the same two steps as xy_slot_mapping followed by xy_kv_append, fused so
+ * that a step pays one kernel launch for them).  Device call: every new token t finds its slot as
+ * xy_slot_mapping computes it and its K and V rows of every KV head are copied there as
+ * xy_kv_append copies them; the slot is also written to slot_mapping[t] unless slot_mapping is
+ * NULL.  Arguments, layouts, alignment and device error bits as for those two calls (a token
+ * whose slot cannot be formed sets its bit and is skipped).
+ * Errors: XY_ERR_INVALID_ARG, XY_ERR_CUDA.
+ */
+xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
+                             const int32_t *context_lens, const int32_t *block_table, int num_seqs,
+                             int max_blocks, int num_tokens, void *k_pages, void *v_pages, int num_pages,
+                             int num_heads_kv, int block_size, int head_dim, int64_t *slot_mapping,
+                             int32_t *err_word, void *stream);
+
+/*
  * a4 — task table: dynamic decomposer + attention task reorder ([XY] §2.2 components 1 and 2,
  * §4.4 decompose_attention / analyze_load_balance).  Host call, pure.
  * Enumerates, for sequence i -> KV head g -> query tile (q_tile tokens) -> KV chunk (kv_chunk
@@ -367,6 +382,17 @@ xy_status xy_paged_attention_traced(const void *q, const int32_t *cu_seqlens_q,
 xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, const int64_t *slot_mapping, int num_tokens,
                            void *k_pages, void *v_pages, float *k_scales, float *v_scales, int num_pages,
                            int num_heads_kv, int block_size, int head_dim, int32_t *err_word, void *stream);
+
+/* xy_kv_append_paged_fp8: the slot mapping and xy_kv_append_fp8 in one launch, as
+ * xy_kv_append_paged is for bf16 pages: each new token's slot is formed from cu_seqlens_q,
+ * context_lens and block_table (device int32, as for xy_slot_mapping), written to slot_mapping[t]
+ * unless slot_mapping is NULL, and the token's K and V rows are quantized into it.  Every other
+ * argument, limit and error as for xy_kv_append_fp8 and xy_slot_mapping. */
+xy_status xy_kv_append_paged_fp8(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
+                                 const int32_t *context_lens, const int32_t *block_table, int num_seqs,
+                                 int max_blocks, int num_tokens, void *k_pages, void *v_pages, float *k_scales,
+                                 float *v_scales, int num_pages, int num_heads_kv, int block_size, int head_dim,
+                                 int64_t *slot_mapping, int32_t *err_word, void *stream);
 
 /* xy_dequant_pages_fp8: bf16 copies of listed 8-bit pages (a helper of the tensor-core path for
  * prefill and chunk tasks over 8-bit pages, which runs on dequantized copies of the pages those

@@ -24,7 +24,8 @@ C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_n
          "xy_slot_mapping", "xy_kv_append", "xy_build_task_table", "xy_paged_attention",
          "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
          "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8", "xy_paged_attention_dynamic",
-         "xy_paged_attention_traced", "xy_paged_attention_fp8_dynamic")
+         "xy_paged_attention_traced", "xy_paged_attention_fp8_dynamic", "xy_kv_append_paged",
+         "xy_kv_append_paged_fp8")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -90,6 +91,10 @@ def lib():
     L.xy_slot_mapping.restype = I
     L.xy_kv_append.argtypes = [P, P, P, I, P, P, I, I, I, I, P, P]
     L.xy_kv_append.restype = I
+    L.xy_kv_append_paged.argtypes = [P, P, P, P, P, I, I, I, P, P, I, I, I, I, P, P, P]
+    L.xy_kv_append_paged.restype = I
+    L.xy_kv_append_paged_fp8.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, I, I, I, I, P, P, P]
+    L.xy_kv_append_paged_fp8.restype = I
     L.xy_build_task_table.argtypes = [P, P, I, I, I, I, I, I, I, I, I, P, I, P, P, I, P, P, P]
     L.xy_build_task_table.restype = I
     L.xy_paged_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P, P, P]
@@ -302,6 +307,50 @@ def xy_kv_append(k_new, v_new, slot_mapping, k_pages, v_pages, err_word, stream=
                               _dev(slot_mapping, torch.int64, "slot_mapping"), k_new.shape[0],
                               _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P, Hkv, bs, d,
                               _dev(err_word, torch.int32, "err_word"), _stream(stream)), "xy_kv_append")
+
+
+def xy_kv_append_paged(k_new, v_new, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, err_word,
+                       slot_mapping=None, stream=None):
+    """a2 + a3 in one launch (device): each new token's slot from cu_seqlens_q / context_lens /
+    block_table (int32, device), its K/V rows copied there; slot_mapping int64 [T] (optional)
+    receives the slots."""
+    import torch
+    P, Hkv, bs, d = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or tuple(k_new.shape) != tuple(v_new.shape):
+        raise ValueError("K and V shapes differ")
+    T = k_new.shape[0]
+    if k_new.shape[1:] != (Hkv, d) or (slot_mapping is not None and slot_mapping.numel() != T):
+        raise ValueError("k_new must be [T, Hkv, d] and slot_mapping [T]")
+    bf, i32 = torch.bfloat16, torch.int32
+    _check(lib().xy_kv_append_paged(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"),
+                                    _dev(cu_seqlens_q, i32, "cu_seqlens_q"), _dev(context_lens, i32, "context_lens"),
+                                    _dev(block_table, i32, "block_table"), cu_seqlens_q.numel() - 1,
+                                    block_table.shape[1], T, _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"),
+                                    P, Hkv, bs, d,
+                                    _dev(slot_mapping, torch.int64, "slot_mapping") if slot_mapping is not None
+                                    else None, _dev(err_word, i32, "err_word"), _stream(stream)), "xy_kv_append_paged")
+
+
+def xy_kv_append_paged_fp8(k_new, v_new, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_scales,
+                           v_scales, err_word, slot_mapping=None, stream=None):
+    """xy_kv_append_paged for 8-bit pages (the quantizing append of xy_kv_append_fp8)."""
+    import torch
+    P, Hkv, bs, d = k_pages.shape
+    if tuple(v_pages.shape) != tuple(k_pages.shape) or tuple(k_new.shape) != tuple(v_new.shape):
+        raise ValueError("K and V shapes differ")
+    if tuple(k_scales.shape) != (P, Hkv, bs) or tuple(v_scales.shape) != (P, Hkv, bs):
+        raise ValueError("scales must be [P, Hkv, bs]")
+    T = k_new.shape[0]
+    if k_new.shape[1:] != (Hkv, d) or (slot_mapping is not None and slot_mapping.numel() != T):
+        raise ValueError("k_new must be [T, Hkv, d] and slot_mapping [T]")
+    bf, u8, f32, i32 = torch.bfloat16, torch.uint8, torch.float32, torch.int32
+    _check(lib().xy_kv_append_paged_fp8(
+        _dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), _dev(cu_seqlens_q, i32, "cu_seqlens_q"),
+        _dev(context_lens, i32, "context_lens"), _dev(block_table, i32, "block_table"), cu_seqlens_q.numel() - 1,
+        block_table.shape[1], T, _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
+        _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv, bs, d,
+        _dev(slot_mapping, torch.int64, "slot_mapping") if slot_mapping is not None else None,
+        _dev(err_word, i32, "err_word"), _stream(stream)), "xy_kv_append_paged_fp8")
 
 
 def xy_paged_attention(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, scale, causal, tasks, merges,

@@ -46,6 +46,7 @@ __global__ void kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *_
                                  const int64_t *__restrict__ slots, int T, int H, int bs, int vec_per_row,
                                  int64_t pool_slots, uint4 *__restrict__ k_pages, uint4 *__restrict__ v_pages,
                                  int32_t *err) {
+    xy::grid_dep_launch();
     const int64_t total = (int64_t)T * H * vec_per_row;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
          v += (int64_t)gridDim.x * blockDim.x) {
@@ -74,6 +75,7 @@ __global__ void kv_append_pow2_kernel(const uint4 *__restrict__ k_new, const uin
                                       const int64_t *__restrict__ slots, int T, int H, int bs_sh,
                                       int64_t pool_slots, uint4 *__restrict__ k_pages, uint4 *__restrict__ v_pages,
                                       int32_t *err) {
+    xy::grid_dep_launch();
     const int64_t total = ((int64_t)T * H) << VSH;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total;
          v += (int64_t)gridDim.x * blockDim.x) {
@@ -91,6 +93,42 @@ __global__ void kv_append_pow2_kernel(const uint4 *__restrict__ k_new, const uin
         const int64_t dst = ((((page * H + h) << bs_sh) + off) << VSH) + c;
         k_pages[dst] = __ldg(k_new + v);
         v_pages[dst] = __ldg(v_new + v);
+    }
+}
+
+// a2 and a3 in one launch: one CTA per new token (grid-stride), whose first warp finds the
+// token's slot (xy::warp_token_slot) and publishes it in shared memory; then the CTA copies the
+// token's K and V rows of every KV head as 16-byte vectors, consecutive threads on consecutive
+// vectors of the token's contiguous [Hkv, d] block.  slots_out (may be null) receives the slot.
+__global__ void __launch_bounds__(128) kv_append_paged_kernel(
+    const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new, const int32_t *__restrict__ cu,
+    const int32_t *__restrict__ ctx, const int32_t *__restrict__ bt, int S, int MB, int T, int H, int bs, int P,
+    int vec_per_row, int64_t *__restrict__ slots_out, uint4 *__restrict__ k_pages, uint4 *__restrict__ v_pages,
+    int32_t *err) {
+    __shared__ int64_t s_slot;
+    xy::grid_dep_launch();  // the attention kernel after this one may start its prologue
+    const int nvec = H * vec_per_row;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        if (threadIdx.x < 32) {
+            const int64_t slot = xy::warp_token_slot(cu, ctx, bt, S, MB, bs, P, t, threadIdx.x, err);
+            if (threadIdx.x == 0) {
+                s_slot = slot;
+                if (slots_out) slots_out[t] = slot;
+            }
+        }
+        __syncthreads();
+        const int64_t slot = s_slot;
+        __syncthreads();  // s_slot is rewritten for the next token only after every thread read it
+        if (slot < 0) continue;
+        const int64_t page = slot / bs, off = slot - page * bs;
+        const int64_t src0 = (int64_t)t * nvec;
+        for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+            const int h = v / vec_per_row, c = v - h * vec_per_row;
+            const int64_t dst = ((page * H + h) * bs + off) * vec_per_row + c;
+            const uint4 kv = __ldg(k_new + src0 + v), vv = __ldg(v_new + src0 + v);
+            k_pages[dst] = kv;
+            v_pages[dst] = vv;
+        }
     }
 }
 
@@ -163,5 +201,28 @@ extern "C" xy_status xy_kv_append(const void *k_new, const void *v_new, const in
         static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), slot_mapping, num_tokens,
         num_heads_kv, block_size, vec_per_row, (int64_t)num_pages * block_size, static_cast<uint4 *>(k_pages),
         static_cast<uint4 *>(v_pages), err_word);
+    return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
+}
+
+extern "C" xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
+                                        const int32_t *context_lens, const int32_t *block_table, int num_seqs,
+                                        int max_blocks, int num_tokens, void *k_pages, void *v_pages, int num_pages,
+                                        int num_heads_kv, int block_size, int head_dim, int64_t *slot_mapping,
+                                        int32_t *err_word, void *stream) {
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks < 1 || num_pages < 1 || num_heads_kv < 1 || block_size < 1 ||
+        head_dim < 8 || head_dim % 8)
+        return XY_ERR_INVALID_ARG;
+    if (num_tokens == 0) return XY_OK;
+    if (num_seqs < 1 || !cu_seqlens_q || !context_lens || !block_table || !k_new || !v_new || !k_pages || !v_pages)
+        return XY_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pages) || !aligned16(v_pages))
+        return XY_ERR_INVALID_ARG;
+    const int sms = device_sm_count();
+    if (sms <= 0) return XY_ERR_CUDA;
+    const int blocks = num_tokens < sms * 16 ? num_tokens : sms * 16;
+    kv_append_paged_kernel<<<blocks, 128, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new), cu_seqlens_q, context_lens,
+        block_table, num_seqs, max_blocks, num_tokens, num_heads_kv, block_size, num_pages, head_dim / 8,
+        slot_mapping, static_cast<uint4 *>(k_pages), static_cast<uint4 *>(v_pages), err_word);
     return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
 }

@@ -115,9 +115,11 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DY
         if (DYN) dq.init(kMathWarps + C::kProducers);
         *abort_flag = 0;
         xy::fence_mbarrier_init();
-        if (p.trace) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
     }
     __syncthreads();
+    // everything above overlaps the previous kernel (the KV append) under a dependent launch
+    xy::grid_dep_wait();
+    if (p.trace && threadIdx.x == 0) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
 
     if constexpr (C::kSchedWarpUsed) {
         if (warp == C::kSchedWarp) {
@@ -378,8 +380,8 @@ xy_status launch_attention_kernel(const AttnParams &p, const CUtensorMap &km, co
         if (e != cudaSuccess) return xy::cuda_fail(e, "paged_attention_kernel smem attribute");
         configured.mark(dev);
     }
-    paged_attention_kernel<HD, KIND, DYN><<<num_ctas, C::kThreads, C::kSmemBytes, st>>>(km, vm, p);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = xy::launch_dependent(paged_attention_kernel<HD, KIND, DYN>, dim3(num_ctas),
+                                               dim3(C::kThreads), C::kSmemBytes, st, km, vm, p);
     return e == cudaSuccess ? XY_OK : xy::cuda_fail(e, "paged_attention_kernel launch");
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -178,6 +179,66 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ void set_err(int32_t *err_word, int32_t bits) {
     if (err_word) atomicOr(err_word, bits);
+}
+
+// Programmatic dependent launch.  A kernel launched with launch_dependent() may begin while the
+// kernel before it on the stream is still running; grid_dep_wait() then blocks until that kernel
+// has completed and its memory writes are visible (it returns at once when the kernel was not
+// launched that way).  grid_dep_launch() lets such a dependent kernel start before this one ends.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` so that its prologue may overlap the previous kernel on the stream (it must call
+// grid_dep_wait() before it reads anything that kernel writes).
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
+// Physical slot of packed new token t (a2): t belongs to sequence i, the largest i < S with
+// cu[i] <= t, and sits at absolute position p = L_i - q_i + (t - cu[i]); its slot is
+// block_table[i][p / bs] * bs + p % bs.  Executed by one whole warp, which finds i with at most
+// three rounds of 32 parallel loads of cu (S <= 32768) and ballots; every lane returns the slot,
+// or -1 after setting XY_DEV_BAD_TASK (t outside the batch) or XY_DEV_PAGE_OOB (the entry lies
+// outside [0, P)).
+__device__ __forceinline__ int64_t warp_token_slot(const int32_t *__restrict__ cu, const int32_t *__restrict__ ctx,
+                                                   const int32_t *__restrict__ bt, int S, int MB, int bs, int P,
+                                                   int t, int lane, int32_t *err) {
+    int lo = 0, n = S;  // i lies in [lo, lo + n)
+    while (n > 32) {
+        const int step = (n + 31) >> 5;
+        const int idx = lo + lane * step;
+        const unsigned ok = __ballot_sync(0xffffffffu, idx < lo + n && __ldg(cu + idx) <= t);
+        const int k = ok ? 31 - __clz(ok) : 0;
+        lo += k * step;
+        n = min(step, n - k * step);
+    }
+    const unsigned ok = __ballot_sync(0xffffffffu, lane < n && __ldg(cu + lo + lane) <= t);
+    const int i = lo + (ok ? 31 - __clz(ok) : 0);
+    const int c0 = __ldg(cu + i), c1 = __ldg(cu + i + 1);
+    const int64_t p = (int64_t)__ldg(ctx + i) - (c1 - c0) + (t - c0);
+    if (!ok || p < 0 || t >= c1) {
+        if (lane == 0) set_err(err, XY_DEV_BAD_TASK);
+        return -1;
+    }
+    const int64_t lb = p / bs;
+    const int32_t page = lb < MB ? __ldg(bt + (int64_t)i * MB + lb) : -1;
+    if (page < 0 || page >= P) {
+        if (lane == 0) set_err(err, XY_DEV_PAGE_OOB);
+        return -1;
+    }
+    return (int64_t)page * bs + p % bs;
 }
 
 }  // namespace xy

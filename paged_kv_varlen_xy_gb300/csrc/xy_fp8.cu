@@ -24,6 +24,35 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     return r;
 }
 
+// Quantize one bf16 row of D values (src) into E4M3 codes at dst and its scale at *scale; executed
+// by one whole warp, D / 32 consecutive values per lane.
+template <int D>
+__device__ __forceinline__ void quantize_row(const __nv_bfloat16 *__restrict__ src, uint8_t *__restrict__ dst,
+                                             float *__restrict__ scale, int lane) {
+    constexpr int E = D / 32;  // elements per lane
+    float x[E];
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+        const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(src + lane * E + i);
+        x[i] = __low2float(pr);
+        x[i + 1] = __high2float(pr);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    uint16_t code[E / 2];
+#pragma unroll
+    for (int i = 0; i < E; i += 2) code[i / 2] = e4m3x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
+    if (E == 4)
+        *reinterpret_cast<uint32_t *>(dst + lane * E) = (uint32_t)code[0] | ((uint32_t)code[E / 2 - 1] << 16);
+    else
+        *reinterpret_cast<uint16_t *>(dst + lane * E) = code[0];
+    if (lane == 0) *scale = s;
+}
+
 // One warp per (token, KV head) row of K and of V; D = head_dim (64 or 128).
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __nv_bfloat16 *__restrict__ k_new,
@@ -32,7 +61,7 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __nv_bfloat16 
                                                              int64_t pool_slots, uint8_t *__restrict__ k_pages,
                                                              uint8_t *__restrict__ v_pages, float *__restrict__ k_scales,
                                                              float *__restrict__ v_scales, int32_t *err) {
-    constexpr int E = D / 32;  // elements per lane
+    xy::grid_dep_launch();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < 2 * (int64_t)T * H;
@@ -47,31 +76,44 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(const __nv_bfloat16 
             if (lane == 0 && tensor == 0 && h == 0) xy::set_err(err, XY_DEV_SLOT_OOB);
             continue;
         }
-        const __nv_bfloat16 *src = (tensor ? v_new : k_new) + th * D + lane * E;
-        float x[E];
-#pragma unroll
-        for (int i = 0; i < E; i += 2) {
-            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162 *>(src + i);
-            x[i] = __low2float(pr);
-            x[i + 1] = __high2float(pr);
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-        uint16_t code[E / 2];
-#pragma unroll
-        for (int i = 0; i < E; i += 2) code[i / 2] = e4m3x2(__fdiv_rn(x[i], s), __fdiv_rn(x[i + 1], s));
         const int64_t page = slot / bs, off = slot - page * bs;
         const int64_t drow = (page * H + h) * bs + off;
-        uint8_t *dst = (tensor ? v_pages : k_pages) + drow * D + lane * E;
-        if (E == 4)
-            *reinterpret_cast<uint32_t *>(dst) = (uint32_t)code[0] | ((uint32_t)code[E / 2 - 1] << 16);
-        else
-            *reinterpret_cast<uint16_t *>(dst) = code[0];
-        if (lane == 0) (tensor ? v_scales : k_scales)[drow] = s;
+        quantize_row<D>((tensor ? v_new : k_new) + th * D, (tensor ? v_pages : k_pages) + drow * D,
+                        (tensor ? v_scales : k_scales) + drow, lane);
+    }
+}
+
+// The slot mapping and the quantizing append in one launch: one CTA per new token (grid-stride),
+// whose first warp finds the token's slot (xy::warp_token_slot); then its eight warps quantize the
+// token's 2 * H rows (K and V of every KV head).  slots_out (may be null) receives the slot.
+template <int D>
+__global__ void __launch_bounds__(256) kv_append_paged_fp8_kernel(
+    const __nv_bfloat16 *__restrict__ k_new, const __nv_bfloat16 *__restrict__ v_new,
+    const int32_t *__restrict__ cu, const int32_t *__restrict__ ctx, const int32_t *__restrict__ bt, int S, int MB,
+    int T, int H, int bs, int P, int64_t *__restrict__ slots_out, uint8_t *__restrict__ k_pages,
+    uint8_t *__restrict__ v_pages, float *__restrict__ k_scales, float *__restrict__ v_scales, int32_t *err) {
+    __shared__ int64_t s_slot;
+    xy::grid_dep_launch();  // the attention kernel after this one may start its prologue
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        if (warp == 0) {
+            const int64_t slot = xy::warp_token_slot(cu, ctx, bt, S, MB, bs, P, t, lane, err);
+            if (lane == 0) {
+                s_slot = slot;
+                if (slots_out) slots_out[t] = slot;
+            }
+        }
+        __syncthreads();
+        const int64_t slot = s_slot;
+        __syncthreads();  // s_slot is rewritten for the next token only after every thread read it
+        if (slot < 0) continue;
+        const int64_t page = slot / bs, off = slot - page * bs;
+        for (int r = warp; r < 2 * H; r += nwarps) {
+            const int tensor = r / H, h = r - tensor * H;
+            const int64_t drow = (page * H + h) * bs + off;
+            quantize_row<D>((tensor ? v_new : k_new) + ((int64_t)t * H + h) * D,
+                            (tensor ? v_pages : k_pages) + drow * D, (tensor ? v_scales : k_scales) + drow, lane);
+        }
     }
 }
 
@@ -172,5 +214,43 @@ extern "C" xy_status xy_kv_append_fp8(const void *k_new, const void *v_new, cons
             static_cast<const __nv_bfloat16 *>(k_new), static_cast<const __nv_bfloat16 *>(v_new), slot_mapping,
             num_tokens, num_heads_kv, block_size, pool_slots, static_cast<uint8_t *>(k_pages),
             static_cast<uint8_t *>(v_pages), k_scales, v_scales, err_word);
+    return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
+}
+
+extern "C" xy_status xy_kv_append_paged_fp8(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
+                                            const int32_t *context_lens, const int32_t *block_table, int num_seqs,
+                                            int max_blocks, int num_tokens, void *k_pages, void *v_pages,
+                                            float *k_scales, float *v_scales, int num_pages, int num_heads_kv,
+                                            int block_size, int head_dim, int64_t *slot_mapping, int32_t *err_word,
+                                            void *stream) {
+    if (num_tokens < 0 || num_seqs < 0 || max_blocks < 1 || num_pages < 1 || num_heads_kv < 1 || block_size < 16 ||
+        (block_size & (block_size - 1)))
+        return XY_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128) return XY_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return XY_OK;
+    if (num_seqs < 1 || !cu_seqlens_q || !context_lens || !block_table || !k_new || !v_new || !k_pages ||
+        !v_pages || !k_scales || !v_scales || !err_word)
+        return XY_ERR_INVALID_ARG;
+    if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15) return XY_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return XY_ERR_CUDA;
+    const int blocks = num_tokens < sms * 8 ? num_tokens : sms * 8;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto *kn = static_cast<const __nv_bfloat16 *>(k_new);
+    auto *vn = static_cast<const __nv_bfloat16 *>(v_new);
+    auto *kp = static_cast<uint8_t *>(k_pages);
+    auto *vp = static_cast<uint8_t *>(v_pages);
+    if (head_dim == 128)
+        kv_append_paged_fp8_kernel<128><<<blocks, 256, 0, st>>>(kn, vn, cu_seqlens_q, context_lens, block_table,
+                                                                num_seqs, max_blocks, num_tokens, num_heads_kv,
+                                                                block_size, num_pages, slot_mapping, kp, vp, k_scales,
+                                                                v_scales, err_word);
+    else
+        kv_append_paged_fp8_kernel<64><<<blocks, 256, 0, st>>>(kn, vn, cu_seqlens_q, context_lens, block_table,
+                                                               num_seqs, max_blocks, num_tokens, num_heads_kv,
+                                                               block_size, num_pages, slot_mapping, kp, vp, k_scales,
+                                                               v_scales, err_word);
     return cudaGetLastError() == cudaSuccess ? XY_OK : XY_ERR_CUDA;
 }

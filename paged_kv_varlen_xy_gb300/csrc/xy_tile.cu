@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         *dec_go = 0;
         xy::fence_mbarrier_init();
-        if (p.trace) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
     }
     if (warp == kMmaWarp) {
         xy::tmem_alloc(base + kMiscOff, kTmemCols);
@@ -180,6 +179,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     xy::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
+    // everything above overlaps the previous kernel (the KV append) under a dependent launch
+    xy::grid_dep_wait();
+    if (p.trace && threadIdx.x == 0) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
     const int BRt = p.bs < kTileKeys ? p.bs : kTileKeys;  // keys per K/V box
     const int qt_tokens = 128 / p.G;                      // tokens per query tile
 
@@ -898,11 +900,11 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
         }
         configured[dyn].mark(dev);
     }
-    if (dyn)
-        meta_attention_kernel<true><<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
-    else
-        meta_attention_kernel<false><<<num_ctas, kThreads, kSmemBytes, st>>>(km, vm, qm, kmap_d, vmap_d, p);
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e =
+        dyn ? xy::launch_dependent(meta_attention_kernel<true>, dim3(num_ctas), dim3(kThreads), kSmemBytes, st, km, vm,
+                                   qm, kmap_d, vmap_d, p)
+            : xy::launch_dependent(meta_attention_kernel<false>, dim3(num_ctas), dim3(kThreads), kSmemBytes, st, km,
+                                   vm, qm, kmap_d, vmap_d, p);
     return e == cudaSuccess ? XY_OK : cuda_fail(e, "meta_attention_kernel launch");
 }
 

@@ -6,8 +6,9 @@ import torch
 
 from . import (XY_SCHEDULE_DYNAMIC, XY_SCHEDULE_GREEDY, Plan, check_err_word, default_schedule, default_tiles,
                xy_build_block_table, xy_build_step_tables, xy_build_task_table, xy_default_num_ctas,
-               xy_dequant_pages_fp8, xy_kv_append, xy_kv_append_fp8, xy_paged_attention, xy_paged_attention_dynamic,
-               xy_paged_attention_fp8, xy_paged_attention_fp8_dynamic, xy_slot_mapping)
+               xy_dequant_pages_fp8, xy_kv_append_paged, xy_kv_append_paged_fp8, xy_paged_attention,
+               xy_paged_attention_dynamic,
+               xy_paged_attention_fp8, xy_paged_attention_fp8_dynamic)
 
 
 class PagedBatch:
@@ -154,8 +155,10 @@ class Planner:
         first; a caller may do it beforehand to keep the wait out of its own timing)."""
         self._wait_upload()
 
-    def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
-        """Build and upload the metadata of one batch; returns a batch for run() (or run_step)."""
+    def plan(self, cu_seqlens_q, context_lens, free_list, stream=None, block_table=None):
+        """Build and upload the metadata of one batch; returns a batch for run() (or run_step).
+        block_table: a host int32 [S, max_blocks] table from the caller's own page allocator (a
+        prefix cache whose rows share pages, say) that replaces the FIFO table before the upload."""
         self._ensure(1 << 16)
         self._wait_upload()   # the staging buffer is written below
         if self.kv_fp8 and self._q_tile_arg is None:
@@ -169,6 +172,12 @@ class Planner:
                 break
             self._ensure(tbl.bytes)   # too small: grow and build again
         used_bytes = tbl.bytes
+        if block_table is not None:
+            S = len(context_lens)
+            bt = np.ascontiguousarray(block_table, dtype=np.int32)
+            if bt.shape != (S, self.max_blocks):
+                raise ValueError("block_table must be [S, max_blocks] int32")
+            self._host_np[tbl.bt_off:tbl.bt_off + bt.nbytes] = bt.view(np.uint8).ravel()
         stm = torch.cuda.current_stream(self.dev) if stream is None else stream
         self._flip ^= 1
         dbuf = self._dev_bufs[self._flip]
@@ -216,7 +225,6 @@ class Planner:
         st = _stream(stream)
         cu, ctx, bt, err = (ctypes.c_void_p(batch.addr(k)) for k in ("cu", "ctx", "bt", "err"))
         slots = _dev(batch.slots, torch.int64, "slots")
-        _check(L.xy_slot_mapping(cu, ctx, bt, batch.S, batch.MB, T, bs, P, slots, err, st), "xy_slot_mapping")
         tasks, merges = ctypes.c_void_p(batch.addr("tasks")), ctypes.c_void_p(batch.addr("merges"))
         ws = ctypes.c_void_p(self._ws.data_ptr())
         common = (batch.S, T, Hq, Hkv, d, bs, float(scale), int(bool(self.causal)), tasks, batch.num_tasks,
@@ -224,10 +232,10 @@ class Planner:
         bf = torch.bfloat16
         if self.kv_fp8:
             u8, f32 = torch.uint8, torch.float32
-            _check(L.xy_kv_append_fp8(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), slots, T,
-                                      _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
-                                      _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv, bs,
-                                      d, err, st), "xy_kv_append_fp8")
+            _check(L.xy_kv_append_paged_fp8(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), cu, ctx, bt, batch.S,
+                                            batch.MB, T, _dev(k_pages, u8, "k_pages"), _dev(v_pages, u8, "v_pages"),
+                                            _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P, Hkv,
+                                            bs, d, slots, err, st), "xy_kv_append_paged_fp8")
             pools = (_dev(q, bf, "q"), cu, ctx, bt, batch.MB, _dev(k_pages, u8, "k_pages"),
                      _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P)
             if self.dynamic:
@@ -237,9 +245,9 @@ class Planner:
             else:
                 _check(L.xy_paged_attention_fp8(*pools, *common, _dev(out, bf, "out"), st), "xy_paged_attention_fp8")
         else:
-            _check(L.xy_kv_append(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), slots, T,
-                                  _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P, Hkv, bs, d, err, st),
-                   "xy_kv_append")
+            _check(L.xy_kv_append_paged(_dev(k_new, bf, "k_new"), _dev(v_new, bf, "v_new"), cu, ctx, bt, batch.S,
+                                        batch.MB, T, _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P,
+                                        Hkv, bs, d, slots, err, st), "xy_kv_append_paged")
             if self.dynamic:
                 _check(L.xy_paged_attention_dynamic(_dev(q, bf, "q"), cu, ctx, bt, batch.MB,
                                                     _dev(k_pages, bf, "k_pages"), _dev(v_pages, bf, "v_pages"), P,
@@ -256,9 +264,8 @@ def run_step(batch, q, k_new, v_new, k_pages, v_pages, scale, out=None, stream=N
     """a2 slot mapping -> a3 KV append -> a5..a10 attention, all enqueued on `stream`.
     Returns out [T, Hq, d] bf16.  Device-side errors accumulate in batch.err (see check())."""
     out = torch.empty_like(q) if out is None else out
-    P = k_pages.shape[0]
-    xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, batch.block_size, P, batch.slots, batch.err, stream)
-    xy_kv_append(k_new, v_new, batch.slots, k_pages, v_pages, batch.err, stream)
+    xy_kv_append_paged(k_new, v_new, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, batch.err,
+                       slot_mapping=batch.slots, stream=stream)
     pl = batch.plan
     if pl.dynamic:
         xy_paged_attention_dynamic(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, scale, batch.causal,
@@ -273,9 +280,8 @@ def run_step(batch, q, k_new, v_new, k_pages, v_pages, scale, out=None, stream=N
 def run_step_fp8(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, scale, out=None, stream=None):
     """run_step over 8-bit pages (E4M3 codes + per-row fp32 scales); batch built with kv_fp8=True."""
     out = torch.empty_like(q) if out is None else out
-    P = k_pages.shape[0]
-    xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, batch.block_size, P, batch.slots, batch.err, stream)
-    xy_kv_append_fp8(k_new, v_new, batch.slots, k_pages, v_pages, k_scales, v_scales, batch.err, stream)
+    xy_kv_append_paged_fp8(k_new, v_new, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales, v_scales,
+                           batch.err, slot_mapping=batch.slots, stream=stream)
     pl = batch.plan
     if pl.dynamic:
         xy_paged_attention_fp8_dynamic(q, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales,
@@ -518,9 +524,8 @@ def run_step_fp8_split(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_sca
     """One step of an Fp8SplitBatch: slot mapping and the quantizing append for the whole batch,
     then attention_fp8_split."""
     out = torch.empty_like(q) if out is None else out
-    P = k_pages.shape[0]
-    xy_slot_mapping(batch.cu, batch.ctx, batch.block_table, batch.block_size, P, batch.slots, batch.err, stream)
-    xy_kv_append_fp8(k_new, v_new, batch.slots, k_pages, v_pages, k_scales, v_scales, batch.err, stream)
+    xy_kv_append_paged_fp8(k_new, v_new, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales, v_scales,
+                           batch.err, slot_mapping=batch.slots, stream=stream)
     return attention_fp8_split(batch, q, k_pages, v_pages, k_scales, v_scales, scale, out, stream)
 
 

@@ -197,3 +197,75 @@ def test_empty_batch_launches_nothing():
     xy.xy_kv_append(empty, empty, slots, kp, kp, err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_fused_append_equals_slot_mapping_then_append(fp8):
+    # xy_kv_append_paged(_fp8) forms each token's slot in the copy kernel; its slots and pages must
+    # equal those of xy_slot_mapping followed by xy_kv_append(_fp8), and the oracle's, bit for bit
+    import oracle
+    import paged_kv_varlen_xy_gb300 as xy
+    from gpu_cases import bits
+    wl = workloads.custom([5, 1, 300, 1, 40, 7], [5, 33, 900, 4096, 57, 7], 16, 4, 128, 16, seed=91)
+    vals = wl.tensors("cuda")
+    bt_host, _ = xy.xy_build_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
+    cu = torch.from_numpy(wl.cu_seqlens_q).cuda()
+    ctx = torch.from_numpy(wl.context_lens).cuda()
+    bt = torch.from_numpy(bt_host).cuda()
+    T, P = wl.num_tokens, wl.num_pages
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = oracle.step.run_step(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                               bits(vals["q"]), bits(vals["k_new"]), bits(vals["v_new"]), bits(vals["k_pool"]),
+                               bits(vals["v_pool"]), wl.scale, wl.causal, rows=[])
+    results = []
+    for fused in (False, True):
+        slots = torch.full((T,), -7, dtype=torch.int64, device="cuda")
+        if fp8:
+            _, Hkv, bs, d = vals["k_pool"].shape
+            pools = [torch.zeros(P, Hkv, bs, d, dtype=torch.uint8, device="cuda") for _ in range(2)]
+            scl = [torch.zeros(P, Hkv, bs, dtype=torch.float32, device="cuda") for _ in range(2)]
+            if fused:
+                xy.xy_kv_append_paged_fp8(vals["k_new"], vals["v_new"], cu, ctx, bt, pools[0], pools[1], scl[0], scl[1],
+                                          err, slot_mapping=slots)
+            else:
+                xy.xy_slot_mapping(cu, ctx, bt, wl.block_size, P, slots, err)
+                xy.xy_kv_append_fp8(vals["k_new"], vals["v_new"], slots, pools[0], pools[1], scl[0], scl[1], err)
+            pools += scl
+        else:
+            pools = [vals["k_pool"].clone(), vals["v_pool"].clone()]
+            if fused:
+                xy.xy_kv_append_paged(vals["k_new"], vals["v_new"], cu, ctx, bt, pools[0], pools[1], err,
+                                      slot_mapping=slots)
+            else:
+                xy.xy_slot_mapping(cu, ctx, bt, wl.block_size, P, slots, err)
+                xy.xy_kv_append(vals["k_new"], vals["v_new"], slots, pools[0], pools[1], err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        assert np.array_equal(slots.cpu().numpy(), ref["slots"])
+        results.append([x.cpu() for x in pools])
+    for a, b in zip(*results):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    if not fp8:
+        assert np.array_equal(bits(results[1][0]), ref["k_pages"])
+        assert np.array_equal(bits(results[1][1]), ref["v_pages"])
+
+
+def test_fused_append_flags_a_page_outside_the_pool():
+    import paged_kv_varlen_xy_gb300 as xy
+    wl = workloads.custom([3, 1], [40, 20], 4, 2, 64, 16, seed=9)
+    vals = wl.tensors("cuda")
+    bt_host, _ = xy.xy_build_block_table(wl.context_lens, wl.block_size, wl.free_list, wl.max_blocks)
+    bt_host[0, 2] = wl.num_pages + 3     # the page of sequence 0's new tokens lies outside the pool
+    cu, ctx, bt = (torch.from_numpy(a).cuda() for a in (wl.cu_seqlens_q, wl.context_lens, bt_host))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slots = torch.zeros(wl.num_tokens, dtype=torch.int64, device="cuda")
+    before = vals["k_pool"].clone()
+    xy.xy_kv_append_paged(vals["k_new"], vals["v_new"], cu, ctx, bt, vals["k_pool"], vals["v_pool"], err,
+                          slot_mapping=slots)
+    torch.cuda.synchronize()
+    assert int(err.item()) & xy.XY_DEV_PAGE_OOB
+    s = slots.cpu().numpy()
+    assert (s[:3] == -1).all() and s[3] >= 0
+    # only the one token with a valid slot was written
+    changed = (vals["k_pool"] != before).any(dim=-1).any(dim=-1).any(dim=-1).sum().item()
+    assert changed == 1

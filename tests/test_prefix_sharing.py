@@ -122,3 +122,44 @@ def test_gpu_shared_prefix_matches_oracle_and_private_copies(d, G):
         outs[shared] = _bits(out)
     # same lengths, same task table, same page contents: sharing changes nothing
     assert np.array_equal(outs[True], outs[False])
+
+
+@pytest.mark.gpu
+def test_gpu_full_size_prefix_batch_sampled():
+    # the bench's prefix-shared batch (64 x 4096 keys, 3584 on row 0's pages) in its launch
+    # configuration (dynamic deal); the oracle checks every head of eight sampled sequences, each
+    # gathered through the shared block table
+    import workloads
+    from paged_kv_varlen_xy_gb300 import build
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    from gpu_cases import MAX_ABS, MEAN_ABS
+    build.build()
+    wl = workloads.prefix()
+    vals = wl.tensors("cuda")
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, schedule=4)
+    bt = workloads.share_prefix(batch.block_table_host, wl.shared_prefix_tokens, wl.block_size)
+    batch.block_table.copy_(torch.from_numpy(bt))
+    sample = [0, 1, 17, 33, 40, 51, 62, 63]
+    pages = np.unique(np.concatenate([bt[i][bt[i] >= 0] for i in sample]))
+    idx = torch.from_numpy(pages).long().cuda()
+    k_before, v_before = _bits(vals["k_pool"].index_select(0, idx)), _bits(vals["v_pool"].index_select(0, idx))
+    out = xystep.run_step(batch, vals["q"], vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"], wl.scale)
+    torch.cuda.synchronize()
+    assert int(batch.err.item()) == 0
+    lut = {int(p): i for i, p in enumerate(pages)}
+    local = np.array([[lut.get(int(p), -1) if p >= 0 else -1 for p in row] for row in bt], dtype=np.int32)
+    slots = oracle.slot_mapping(wl.cu_seqlens_q, wl.context_lens, bt, wl.block_size)
+    assert np.array_equal(batch.slots.cpu().numpy(), slots)
+    local_slots = np.array([lut[int(s) // wl.block_size] * wl.block_size + int(s) % wl.block_size
+                            if int(s) // wl.block_size in lut else -1 for s in slots], dtype=np.int64)
+    kp, vp = oracle.kv_append(k_before, v_before, _bits(vals["k_new"]), _bits(vals["v_new"]), local_slots)
+    assert np.array_equal(_bits(vals["k_pool"].index_select(0, idx)), kp)
+    assert np.array_equal(_bits(vals["v_pool"].index_select(0, idx)), vp)
+    rows = [(int(wl.cu_seqlens_q[i]), h) for i in sample for h in range(wl.num_heads_q)]
+    ref = oracle.attention_rows(rows, oracle.bf16_bits_to_f64(_bits(vals["q"])), wl.cu_seqlens_q, wl.context_lens,
+                                local, oracle.bf16_bits_to_f64(kp), oracle.bf16_bits_to_f64(vp), wl.scale, True)
+    got = oracle.bf16_bits_to_f64(_bits(out))
+    got = np.stack([got[t, h] for t, h in rows])
+    diff = np.abs(got - ref)
+    assert np.isfinite(got).all() and diff.max() <= MAX_ABS and diff.mean() <= MEAN_ABS, (diff.max(), diff.mean())

@@ -36,6 +36,7 @@ class Workload:
     causal: bool
     seed: int
     free_list: np.ndarray = field(repr=False)   # int32 permutation of range(num_pages)
+    shared_prefix_tokens: int = 0               # > 0: rows share their first pages (share_prefix)
 
     @property
     def num_seqs(self):
@@ -140,6 +141,36 @@ def skew(seed=1005, num_long=4, num_short=252, long_len=131072, short_len=512):
     return _finish("skew", np.ones(num_long + num_short), ctx, 64, 8, 128, 256, True, seed, rng)
 
 
+def verify(seed=1006, num_seqs=64):
+    """64 speculative-verify steps: q U{2..8} draft tokens per sequence over a context U[512, 8192]
+    (including them); Hq=32, Hkv=8, d=128, bs=16 ([ATB] speculative decoding: the target model
+    scores a few draft tokens per sequence in one pass)."""
+    rng = np.random.default_rng(seed)
+    q = rng.integers(2, 8, size=num_seqs, endpoint=True)
+    ctx = rng.integers(512, 8192, size=num_seqs, endpoint=True)
+    return _finish("verify", q, ctx, 32, 8, 128, 16, True, seed, rng)
+
+
+def prefix(seed=1007, num_seqs=64, context=4096, shared=3584):
+    """64 decode sequences of context 4096 whose first 3584 tokens (224 pages of 16) are one shared
+    prompt prefix ([XY] §2.3 technique 2, prefix cache; [ATB] KV cache reuse): every row of the
+    block table points at the same physical pages for it (see share_prefix).  Hq=Hkv=32, d=128."""
+    rng = np.random.default_rng(seed)
+    wl = _finish("prefix", np.ones(num_seqs), np.full(num_seqs, context), 32, 32, 128, 16, True, seed, rng)
+    wl.shared_prefix_tokens = shared
+    return wl
+
+
+def share_prefix(block_table, shared_tokens, block_size):
+    """The block table of a prefix-shared batch: the first shared_tokens / block_size entries of
+    every row replaced by row 0's (the rows' own pages for those positions go unused).  Batch
+    construction only: which physical page each logical page of a sequence is."""
+    n = shared_tokens // block_size
+    bt = np.array(block_table, copy=True)
+    bt[:, :n] = bt[0, :n]
+    return bt
+
+
 def custom(q_lens, context_lens, num_heads_q, num_heads_kv, head_dim, block_size, causal=True,
            seed=7, num_pages=None, name="custom"):
     """Any batch shape (parity tests: ragged tails, several tiles, edge cases)."""
@@ -148,7 +179,8 @@ def custom(q_lens, context_lens, num_heads_q, num_heads_kv, head_dim, block_size
                    causal, seed, rng, num_pages=num_pages)
 
 
-CONFIGS = {"tiny": tiny, "decode": decode, "prefill": prefill, "mixed": mixed, "skew": skew}
+CONFIGS = {"tiny": tiny, "decode": decode, "prefill": prefill, "mixed": mixed, "skew": skew, "verify": verify,
+           "prefix": prefix}
 
 
 def make(name, **kw):
