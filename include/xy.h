@@ -211,6 +211,23 @@ xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t
 #define XY_SCHEDULE_TILE_ROWS 128 /* MMA tile height: the unit of XY_SCHEDULE_MIXED's load */
 #define XY_SCHEDULE_SMALL_ROWS 16 /* tasks of at most this many rows count as small */
 
+/*
+ * The tile policy of the kernels (no counterpart in the pages, whose 16 x 16 tiles are Ascend
+ * sizes): the q_tile and kv_chunk to pass to xy_build_task_table for a batch of this shape.
+ * Host call, pure.  With bf16 pages, head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
+ * 256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise 64/G tokens (at least
+ * 1), the decode path's task height.  Over 8-bit pages (kv_fp8) every task runs on the decode
+ * path: one token per task when pure_decode (one new token per sequence) and G <=
+ * XY_FP8_NARROW_ROWS, else 64/G tokens.  kv_chunk is XY_DEFAULT_KV_CHUNK keys: a multiple of every
+ * page size and of both kernels' KV tiles, long enough that split partials and merges stay few,
+ * short enough that a few long contexts still spread over the SMs.
+ * Errors: XY_ERR_INVALID_ARG (null outputs, Hq not a positive multiple of Hkv).
+ */
+#define XY_DEFAULT_KV_CHUNK 8192
+#define XY_FP8_NARROW_ROWS 16
+xy_status xy_default_tiles(int num_heads_q, int num_heads_kv, int head_dim, int kv_fp8, int pure_decode,
+                           int *q_tile, int *kv_chunk);
+
 xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
                               int num_seqs, int num_heads_q, int num_heads_kv, int head_dim,
                               int causal, int num_ctas, int q_tile, int kv_chunk, int schedule,
@@ -416,7 +433,6 @@ xy_status xy_dequant_pages_fp8(const void *k_codes, const void *v_codes, const f
  * XY_FP8_NARROW_ROWS rows (q_rows = 1), otherwise at most 64 rows (q_tile <= 64 / G).  Tasks
  * outside these limits set XY_DEV_BAD_TASK.
  * Errors: as xy_paged_attention; XY_ERR_UNSUPPORTED for head_dim other than 128 or G > 64. */
-#define XY_FP8_NARROW_ROWS 16
 xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
                                  const int32_t *block_table, int max_blocks, const void *k_pages,
                                  const void *v_pages, const float *k_scales, const float *v_scales,
@@ -451,6 +467,74 @@ xy_status xy_paged_attention_fp8_dynamic(const void *q, const int32_t *cu_seqlen
                                          int num_merges, int num_ctas, void *workspace,
                                          size_t workspace_bytes, int32_t *task_counter, int32_t *err_word,
                                          void *out, void *stream);
+
+/*
+ * One step over 8-bit pages for a batch that mixes one-token (decode) sequences with sequences of
+ * several new tokens (prefill, chunks, verify) -- the pages' unified batch ([XY] §2.2 component
+ * 3: no prefill/decode distinction at the scheduler) with [CANN] §5.2's scale metadata beside the
+ * pages.  The decode sequences run on the 8-bit decode path; the others run on the tcgen05 tile
+ * path over bf16 copies of the pages they read (xy_dequant_pages_fp8), since the tensor cores take
+ * no E4M3 x f16 product.  The two kinds must each form one contiguous range of sequences.
+ *
+ * xy_build_fp8_step_tables: host call, pure.  Splits the batch into its tile range and decode
+ * range, builds the block table (as xy_build_block_table), the list of physical pages the tile
+ * sequences read (in their order; bf16 copy i holds page list[i]), the tile sequences' block
+ * table over those copies (row r: copies 0, 1, ... of tile sequence r, the rest -1), each part's
+ * cu_seqlens_q renumbered from 0, and each part's task and merge tables (XY_SCHEDULE_DYNAMIC, the
+ * xy_default_tiles policy: bf16 tiles for the tile part, 8-bit decode tasks for the other), and
+ * packs them into `staging` at the offsets of *out (multiples of XY_STEP_TABLES_ALIGN) after a
+ * zero error word, cu_seqlens_q, context_lens and the block table, so one host->device copy of
+ * out->bytes bytes carries every table.  *out also gets the parts' sequence and token ranges,
+ * counts and workspace sizes.  staging_bytes < out->bytes: XY_ERR_CAPACITY with *out filled.
+ * Errors: XY_ERR_INVALID_ARG, XY_ERR_CU_SEQLENS, XY_ERR_CONTEXT_LT_QLEN, XY_ERR_OUT_OF_PAGES,
+ *   XY_ERR_CAPACITY (as the builders it composes); XY_ERR_UNSUPPORTED when the kinds interleave,
+ *   head_dim is not 128 or G does not divide 128.
+ */
+typedef struct {
+    size_t err_off, cu_off, ctx_off, bt_off;                                       /* whole batch */
+    size_t tile_cu_off, tile_bt_off, tile_pages_off, tile_tasks_off, tile_merges_off; /* tile part */
+    size_t dec_cu_off, dec_tasks_off, dec_merges_off;                              /* decode part */
+    size_t bytes;                          /* end of the last table */
+    size_t tile_workspace_bytes, dec_workspace_bytes;
+    int tile_seq_begin, tile_seq_end, dec_seq_begin, dec_seq_end;   /* sequence ranges [begin, end) */
+    int tile_tok_begin, tile_tok_end, dec_tok_begin, dec_tok_end;   /* packed token ranges */
+    int tile_num_pages;                    /* pages the tile part copies to bf16 */
+    int tile_num_tasks, tile_num_merges, dec_num_tasks, dec_num_merges;
+    int pages_used;
+} xy_fp8_step_tables;
+
+xy_status xy_build_fp8_step_tables(const int32_t *cu_seqlens_q, const int32_t *context_lens, int num_seqs,
+                                   const int32_t *free_list, int num_free, int block_size, int max_blocks,
+                                   int num_heads_q, int num_heads_kv, int head_dim, int causal, int num_ctas,
+                                   void *staging, size_t staging_bytes, xy_fp8_step_tables *out);
+
+/*
+ * xy_paged_attention_fp8_mixed: the attention of such a step, after the append of the step's new
+ * tokens (xy_kv_append_paged_fp8 over the whole batch).  Device call: the bf16 copies of the tile
+ * part's pages, its tcgen05 attention (dynamic deal) and merges, then the decode part's 8-bit
+ * attention (dynamic deal) and merges, each writing its own rows of out.
+ *   tables: device copy of the first t->bytes bytes of the staging buffer t describes (16-byte
+ *   aligned); t: the host description xy_build_fp8_step_tables filled.
+ *   copy_k, copy_v: device bf16 buffers of copy_pages pages of [Hkv, bs, d] each (caller owned,
+ *   copy_pages >= t->tile_num_pages), scratch of the page copies.
+ *   tile_ws / dec_ws: split-KV workspaces of at least t->tile_workspace_bytes /
+ *   t->dec_workspace_bytes (NULL when 0).  task_counters: device int32[4], 8-byte aligned, zero
+ *   before the first call (the two parts' claim counters, words 0-1 and 2-3, each returned to zero
+ *   by its launch; overlapping calls need different counters).
+ *   q/out [num_tokens, Hq, d], the 8-bit pools and their scales, err_word: as for
+ *   xy_paged_attention_fp8; num_seqs, num_tokens, max_blocks, the head counts, head_dim and
+ *   block_size as passed to the builder.
+ * Errors: XY_ERR_INVALID_ARG (null or misaligned pointers, a description that does not fit the
+ *   sizes), XY_ERR_WORKSPACE (copy or workspace buffers too small), XY_ERR_UNSUPPORTED, XY_ERR_CUDA.
+ */
+xy_status xy_paged_attention_fp8_mixed(const void *q, const void *tables, const xy_fp8_step_tables *t,
+                                       const void *k_pages, const void *v_pages, const float *k_scales,
+                                       const float *v_scales, int num_pages, int num_seqs, int num_tokens,
+                                       int max_blocks, int num_heads_q, int num_heads_kv, int head_dim,
+                                       int block_size, float scale, int causal, int num_ctas, void *copy_k,
+                                       void *copy_v, int copy_pages, void *tile_ws, size_t tile_ws_bytes,
+                                       void *dec_ws, size_t dec_ws_bytes, int32_t *task_counters,
+                                       int32_t *err_word, void *out, void *stream);
 
 /* Self-test of the bounded waits (no counterpart in the pages; not a step of the path).
  * Every mbarrier wait in the attention kernels gives up after a time limit, or when its CTA's

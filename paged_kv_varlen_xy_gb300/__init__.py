@@ -25,7 +25,8 @@ C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_n
          "xy_paged_attention_noalloc", "xy_selftest_bounded_wait", "xy_kv_append_fp8",
          "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8", "xy_paged_attention_dynamic",
          "xy_paged_attention_traced", "xy_paged_attention_fp8_dynamic", "xy_kv_append_paged",
-         "xy_kv_append_paged_fp8")
+         "xy_kv_append_paged_fp8", "xy_default_tiles", "xy_build_fp8_step_tables",
+         "xy_paged_attention_fp8_mixed")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -64,6 +65,17 @@ class StepTables(ctypes.Structure):
                 ("num_merges", ctypes.c_int), ("pages_used", ctypes.c_int), ("stats", TaskStats)]
 
 
+class Fp8StepTables(ctypes.Structure):
+    """xy_fp8_step_tables (include/xy.h): offsets, ranges and counts of a split 8-bit step."""
+    _fields_ = [(n, ctypes.c_size_t) for n in (
+        "err_off", "cu_off", "ctx_off", "bt_off", "tile_cu_off", "tile_bt_off", "tile_pages_off", "tile_tasks_off",
+        "tile_merges_off", "dec_cu_off", "dec_tasks_off", "dec_merges_off", "bytes", "tile_workspace_bytes",
+        "dec_workspace_bytes")] + [(n, ctypes.c_int) for n in (
+        "tile_seq_begin", "tile_seq_end", "dec_seq_begin", "dec_seq_end", "tile_tok_begin", "tile_tok_end",
+        "dec_tok_begin", "dec_tok_end", "tile_num_pages", "tile_num_tasks", "tile_num_merges", "dec_num_tasks",
+        "dec_num_merges", "pages_used")]
+
+
 _lib = None
 
 
@@ -97,6 +109,13 @@ def lib():
     L.xy_kv_append_paged_fp8.restype = I
     L.xy_build_task_table.argtypes = [P, P, I, I, I, I, I, I, I, I, I, P, I, P, P, I, P, P, P]
     L.xy_build_task_table.restype = I
+    L.xy_default_tiles.argtypes = [I, I, I, I, I, P, P]
+    L.xy_default_tiles.restype = I
+    L.xy_build_fp8_step_tables.argtypes = [P, P, I, P, I, I, I, I, I, I, I, I, P, SZ, P]
+    L.xy_build_fp8_step_tables.restype = I
+    L.xy_paged_attention_fp8_mixed.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P, I, P, SZ,
+                                               P, SZ, P, P, P, P]
+    L.xy_paged_attention_fp8_mixed.restype = I
     L.xy_paged_attention.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, P, SZ, P, P, P]
     L.xy_paged_attention.restype = I
     L.xy_paged_attention_noalloc.argtypes = [P, P, P, P, I, P, P, I, I, I, I, I, I, I, F, I, P, I, P, I, I, SZ, P, P,
@@ -536,6 +555,45 @@ def _fp8_args(q, cu_seqlens_q, context_lens, block_table, k_pages, v_pages, k_sc
             _dev(merges, torch.int32, "merges") if nm else None, nm, int(num_ctas), ws_ptr, ws_bytes)
 
 
+def xy_build_fp8_step_tables(cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
+                             head_dim, causal, num_ctas, staging_ptr, staging_bytes):
+    """Tables of a split step over 8-bit pages packed into a host staging buffer (see include/xy.h).
+    Returns (status, Fp8StepTables); status XY_ERR_CAPACITY (-10) means the buffer was too small
+    (tables.bytes says how large it must be); any other error raises XYError."""
+    cu, cu_p = _host_i32(cu_seqlens_q)
+    ctx, ctx_p = _host_i32(context_lens)
+    fl, fl_p = _host_i32(free_list)
+    out = Fp8StepTables()
+    st = lib().xy_build_fp8_step_tables(cu_p, ctx_p, len(ctx), fl_p, len(fl), int(block_size), int(max_blocks),
+                                        int(num_heads_q), int(num_heads_kv), int(head_dim), int(bool(causal)),
+                                        int(num_ctas), ctypes.c_void_p(staging_ptr), int(staging_bytes),
+                                        ctypes.byref(out))
+    if st not in (0, _XY_ERR_CAPACITY):
+        raise XYError(st, "xy_build_fp8_step_tables")
+    return st, out
+
+
+def xy_paged_attention_fp8_mixed(q, tables_dev, t, k_pages, v_pages, k_scales, v_scales, num_seqs, max_blocks, scale,
+                                 causal, num_ctas, copy_k, copy_v, tile_ws, dec_ws, task_counters, err_word, out,
+                                 stream=None):
+    """Attention of a split step over 8-bit pages from the device tables of xy_build_fp8_step_tables
+    (tables_dev: uint8 device tensor holding the staging bytes; t: the Fp8StepTables)."""
+    import torch
+    T, Hq, d = q.shape
+    P, Hkv, bs, _ = k_pages.shape
+    bf, u8, f32 = torch.bfloat16, torch.uint8, torch.float32
+    copy_pages = copy_k.shape[0] if copy_k is not None else 0
+    _check(lib().xy_paged_attention_fp8_mixed(
+        _dev(q, bf, "q"), _dev(tables_dev, u8, "tables"), ctypes.byref(t), _dev(k_pages, u8, "k_pages"),
+        _dev(v_pages, u8, "v_pages"), _dev(k_scales, f32, "k_scales"), _dev(v_scales, f32, "v_scales"), P,
+        int(num_seqs), T, int(max_blocks), Hq, Hkv, d, bs, float(scale), int(bool(causal)), int(num_ctas),
+        _dev(copy_k, bf, "copy_k") if copy_pages else None, _dev(copy_v, bf, "copy_v") if copy_pages else None,
+        copy_pages, _dev(tile_ws, u8, "tile_ws") if tile_ws is not None else None,
+        tile_ws.numel() if tile_ws is not None else 0, _dev(dec_ws, u8, "dec_ws") if dec_ws is not None else None,
+        dec_ws.numel() if dec_ws is not None else 0, _dev(task_counters, torch.int32, "task_counters"),
+        _dev(err_word, torch.int32, "err_word"), _dev(out, bf, "out"), _stream(stream)), "xy_paged_attention_fp8_mixed")
+
+
 def xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, pages, k_out, v_out, err_word, stream=None):
     """bf16 copies of the listed 8-bit pages: k_out/v_out [n, Hkv, bs, d] bf16 <- pages[i] of
     k_pages/v_pages [P, Hkv, bs, d] uint8 with k_scales/v_scales [P, Hkv, bs] fp32; pages int32 [n]."""
@@ -571,20 +629,13 @@ def check_err_word(err_word):
 
 
 def default_tiles(num_heads_q, num_heads_kv, head_dim=128, kv_fp8=False, pure_decode=False):
-    """Tile policy of the kernels.  With head_dim 128 and G = Hq/Hkv dividing 128, a query tile is
-    256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise up to 64 rows
-    (q_tile = 64 // G).  Over 8-bit pages every task runs on the decode path: one token per task in
-    pure decode batches (pure_decode: one new token per sequence) with G <= 16, else up to 64 rows.
-    KV chunks are 8192 keys, a multiple of every
-    page size and of both kernels' KV tiles: long enough that split partials and merges stay few,
-    short enough that a few long contexts still spread over the SMs (measured on the mixed and
-    long-context batches)."""
-    G = num_heads_q // num_heads_kv
-    if kv_fp8:
-        return (1 if pure_decode and G <= XY_FP8_NARROW_ROWS else max(1, 64 // G)), 8192
-    if head_dim == 128 and 128 % G == 0:
-        return 256 // G, 8192
-    return max(1, 64 // G), 8192
+    """(q_tile, kv_chunk): the kernels' tile policy for a batch of this shape (xy_default_tiles:
+    two 128-row tcgen05 tiles per task where the shape allows, else decode-path task heights; over
+    8-bit pages one token per task for pure decode batches; 8192-key KV chunks)."""
+    qt, ch = ctypes.c_int(), ctypes.c_int()
+    _check(lib().xy_default_tiles(int(num_heads_q), int(num_heads_kv), int(head_dim), int(bool(kv_fp8)),
+                                  int(bool(pure_decode)), ctypes.byref(qt), ctypes.byref(ch)), "xy_default_tiles")
+    return qt.value, ch.value
 
 
 class Plan:

@@ -681,3 +681,69 @@ extern "C" xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu
                               tasks, num_tasks, merges, num_merges, num_ctas, scratch, workspace_bytes, err_word,
                               out, stream);
 }
+
+// ---------------------------------------------------------------------------------------------
+// A step over 8-bit pages with decode and multi-token sequences: the tile part on bf16 copies of
+// its pages (tcgen05 tiles), the decode part on the codes, both from the tables of
+// xy_build_fp8_step_tables.
+extern "C" xy_status xy_paged_attention_fp8_mixed(const void *q, const void *tables, const xy_fp8_step_tables *t,
+                                                  const void *k_pages, const void *v_pages, const float *k_scales,
+                                                  const float *v_scales, int num_pages, int num_seqs, int num_tokens,
+                                                  int max_blocks, int num_heads_q, int num_heads_kv, int head_dim,
+                                                  int block_size, float scale, int causal, int num_ctas, void *copy_k,
+                                                  void *copy_v, int copy_pages, void *tile_ws, size_t tile_ws_bytes,
+                                                  void *dec_ws, size_t dec_ws_bytes, int32_t *task_counters,
+                                                  int32_t *err_word, void *out, void *stream) {
+    if (!q || !tables || !t || !out || !task_counters || !aligned16(tables) ||
+        (reinterpret_cast<uintptr_t>(task_counters) & 7) || num_seqs < 0 || num_tokens < 0 || max_blocks < 1 ||
+        num_heads_kv < 1 || num_heads_q < num_heads_kv || num_heads_q % num_heads_kv)
+        return XY_ERR_INVALID_ARG;
+    if (head_dim != 128) return XY_ERR_UNSUPPORTED;
+    // the description must fit this batch
+    if (t->tile_seq_begin < 0 || t->tile_seq_end < t->tile_seq_begin || t->tile_seq_end > num_seqs ||
+        t->dec_seq_begin < 0 || t->dec_seq_end < t->dec_seq_begin || t->dec_seq_end > num_seqs ||
+        t->tile_tok_begin < 0 || t->tile_tok_end < t->tile_tok_begin || t->tile_tok_end > num_tokens ||
+        t->dec_tok_begin < 0 || t->dec_tok_end < t->dec_tok_begin || t->dec_tok_end > num_tokens ||
+        t->tile_num_pages < 0 || t->tile_num_tasks < 0 || t->dec_num_tasks < 0 || t->tile_num_merges < 0 ||
+        t->dec_num_merges < 0)
+        return XY_ERR_INVALID_ARG;
+    const uint8_t *base = static_cast<const uint8_t *>(tables);
+    const size_t row_bytes = (size_t)num_heads_q * head_dim * 2;   // one packed token of q / out
+    const auto *q8 = static_cast<const uint8_t *>(q);
+    auto *o8 = static_cast<uint8_t *>(out);
+    const int32_t *ctx = reinterpret_cast<const int32_t *>(base + t->ctx_off);
+    const int32_t *bt = reinterpret_cast<const int32_t *>(base + t->bt_off);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int nt = t->tile_seq_end - t->tile_seq_begin, nd = t->dec_seq_end - t->dec_seq_begin;
+    if (nt > 0) {
+        if (!copy_k || !copy_v || copy_pages < t->tile_num_pages) return XY_ERR_WORKSPACE;
+        if (t->tile_workspace_bytes > 0 && (!tile_ws || tile_ws_bytes < t->tile_workspace_bytes))
+            return XY_ERR_WORKSPACE;
+        xy_status s = xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, num_pages, num_heads_kv, block_size,
+                                           head_dim, reinterpret_cast<const int32_t *>(base + t->tile_pages_off),
+                                           t->tile_num_pages, copy_k, copy_v, err_word, stream);
+        if (s != XY_OK) return s;
+        s = attention(q8 + (size_t)t->tile_tok_begin * row_bytes, reinterpret_cast<const int32_t *>(base + t->tile_cu_off),
+                      ctx + t->tile_seq_begin, reinterpret_cast<const int32_t *>(base + t->tile_bt_off), max_blocks,
+                      copy_k, copy_v, t->tile_num_pages > 0 ? t->tile_num_pages : 1, nt,
+                      t->tile_tok_end - t->tile_tok_begin, num_heads_q, num_heads_kv, head_dim, block_size, scale,
+                      causal, reinterpret_cast<const xy_task *>(base + t->tile_tasks_off), t->tile_num_tasks,
+                      reinterpret_cast<const xy_merge *>(base + t->tile_merges_off), t->tile_num_merges, num_ctas,
+                      tile_ws, tile_ws_bytes, task_counters, nullptr, err_word,
+                      o8 + (size_t)t->tile_tok_begin * row_bytes, stream);
+        if (s != XY_OK) return s;
+    }
+    if (nd > 0) {
+        if (t->dec_workspace_bytes > 0 && (!dec_ws || dec_ws_bytes < t->dec_workspace_bytes)) return XY_ERR_WORKSPACE;
+        const xy_status s = attention_fp8(
+            q8 + (size_t)t->dec_tok_begin * row_bytes, reinterpret_cast<const int32_t *>(base + t->dec_cu_off),
+            ctx + t->dec_seq_begin, bt + (size_t)t->dec_seq_begin * max_blocks, max_blocks, k_pages, v_pages, k_scales,
+            v_scales, num_pages, nd, t->dec_tok_end - t->dec_tok_begin, num_heads_q, num_heads_kv, head_dim,
+            block_size, scale, causal, reinterpret_cast<const xy_task *>(base + t->dec_tasks_off), t->dec_num_tasks,
+            reinterpret_cast<const xy_merge *>(base + t->dec_merges_off), t->dec_num_merges, num_ctas, dec_ws,
+            dec_ws_bytes, task_counters + 2, err_word, o8 + (size_t)t->dec_tok_begin * row_bytes, stream);
+        if (s != XY_OK) return s;
+    }
+    (void)st;
+    return XY_OK;
+}

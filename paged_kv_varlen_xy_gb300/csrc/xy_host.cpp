@@ -344,6 +344,22 @@ static void task_stats(const std::vector<Rec> &recs, int num_ctas, xy_task_stats
     stats->balance = mx > 0 ? (double)mn / (double)mx : 1.0;
 }
 
+extern "C" xy_status xy_default_tiles(int num_heads_q, int num_heads_kv, int head_dim, int kv_fp8, int pure_decode,
+                                      int *q_tile, int *kv_chunk) {
+    if (!q_tile || !kv_chunk || num_heads_kv < 1 || num_heads_q < num_heads_kv || num_heads_q % num_heads_kv)
+        return XY_ERR_INVALID_ARG;
+    const int G = num_heads_q / num_heads_kv;
+    const int narrow = 64 / G > 1 ? 64 / G : 1;   // rows of a decode-path task: at most 64
+    if (kv_fp8)
+        *q_tile = pure_decode && G <= XY_FP8_NARROW_ROWS ? 1 : narrow;
+    else if (head_dim == 128 && 128 % G == 0)
+        *q_tile = 256 / G;   // two 128-row tcgen05 tiles
+    else
+        *q_tile = narrow;
+    *kv_chunk = XY_DEFAULT_KV_CHUNK;
+    return XY_OK;
+}
+
 extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
                                          int num_seqs, int num_heads_q, int num_heads_kv,
                                          int head_dim, int causal, int num_ctas, int q_tile,
@@ -413,5 +429,135 @@ extern "C" xy_status xy_build_step_tables(const int32_t *cu_seqlens_q, const int
     xy_task *t = reinterpret_cast<xy_task *>(base + out->tasks_off);
     for (size_t k = 0; k < recs.size(); ++k) t[k] = recs[k].t;
     if (!mrg.empty()) std::memcpy(base + out->merges_off, mrg.data(), sizeof(xy_merge) * mrg.size());
+    return XY_OK;
+}
+
+namespace {
+thread_local std::vector<xy_task> g_tile_tasks, g_dec_tasks;
+thread_local std::vector<xy_merge> g_tile_merges, g_dec_merges;
+thread_local std::vector<int32_t> g_cu_part;
+}  // namespace
+
+extern "C" xy_status xy_build_fp8_step_tables(const int32_t *cu_seqlens_q, const int32_t *context_lens,
+                                              int num_seqs, const int32_t *free_list, int num_free, int block_size,
+                                              int max_blocks, int num_heads_q, int num_heads_kv, int head_dim,
+                                              int causal, int num_ctas, void *staging, size_t staging_bytes,
+                                              xy_fp8_step_tables *out) {
+    if (!out || !cu_seqlens_q || (num_seqs > 0 && !context_lens) || (staging_bytes > 0 && !staging) ||
+        max_blocks < 1 || num_seqs < 0 || num_heads_kv < 1 || num_heads_q < num_heads_kv ||
+        num_heads_q % num_heads_kv || num_ctas < 1 || !is_pow2(block_size) || block_size < 16)
+        return XY_ERR_INVALID_ARG;
+    const int G = num_heads_q / num_heads_kv;
+    if (head_dim != 128 || 128 % G) return XY_ERR_UNSUPPORTED;
+    if (cu_seqlens_q[0] != 0) return XY_ERR_CU_SEQLENS;
+    for (int i = 0; i < num_seqs; ++i)
+        if (cu_seqlens_q[i + 1] <= cu_seqlens_q[i]) return XY_ERR_CU_SEQLENS;
+    // the two kinds of sequences must form one contiguous range each
+    int changes = 0;
+    for (int i = 1; i < num_seqs; ++i) {
+        const bool a = cu_seqlens_q[i] - cu_seqlens_q[i - 1] > 1, b = cu_seqlens_q[i + 1] - cu_seqlens_q[i] > 1;
+        changes += a != b;
+    }
+    if (changes > 1) return XY_ERR_UNSUPPORTED;
+    int k = num_seqs;  // first sequence of the second range
+    for (int i = 1; i < num_seqs; ++i)
+        if ((cu_seqlens_q[i] - cu_seqlens_q[i - 1] > 1) != (cu_seqlens_q[i + 1] - cu_seqlens_q[i] > 1)) {
+            k = i;
+            break;
+        }
+    const bool multi_first = num_seqs > 0 && cu_seqlens_q[1] - cu_seqlens_q[0] > 1;
+    int ta = 0, tb = 0, da = 0, db = 0;
+    if (multi_first) {
+        ta = 0, tb = k, da = k, db = num_seqs;
+    } else {
+        da = 0, db = k, ta = k, tb = num_seqs;
+    }
+    std::memset(out, 0, sizeof(*out));
+    out->tile_seq_begin = ta, out->tile_seq_end = tb, out->dec_seq_begin = da, out->dec_seq_end = db;
+    out->tile_tok_begin = cu_seqlens_q[ta], out->tile_tok_end = cu_seqlens_q[tb];
+    out->dec_tok_begin = cu_seqlens_q[da], out->dec_tok_end = cu_seqlens_q[db];
+
+    // the two parts' task tables (dynamic deal), each with its own sequences renumbered from 0
+    g_tile_tasks.clear(), g_dec_tasks.clear(), g_tile_merges.clear(), g_dec_merges.clear();
+    auto part = [&](int a, int b, int kv_fp8, std::vector<xy_task> &tasks, std::vector<xy_merge> &merges,
+                    size_t *ws_bytes) -> xy_status {
+        if (b <= a) return XY_OK;
+        g_cu_part.resize((size_t)(b - a + 1));
+        for (int i = a; i <= b; ++i) g_cu_part[(size_t)(i - a)] = cu_seqlens_q[i] - cu_seqlens_q[a];
+        int q_tile = 0, kv_chunk = 0;
+        xy_status st = xy_default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8, kv_fp8, &q_tile, &kv_chunk);
+        if (st != XY_OK) return st;
+        int64_t ws_rows = 0;
+        st = build_tasks(g_cu_part.data(), context_lens + a, b - a, num_heads_q, num_heads_kv, head_dim, causal,
+                         num_ctas, q_tile, kv_chunk, XY_SCHEDULE_DYNAMIC, &ws_rows);
+        if (st != XY_OK) return st;
+        tasks.resize(g_scratch.recs.size());
+        for (size_t r = 0; r < tasks.size(); ++r) tasks[r] = g_scratch.recs[r].t;
+        merges = g_scratch.mrg;
+        *ws_bytes = (size_t)ws_rows * (size_t)(head_dim + 1) * 4u;
+        return XY_OK;
+    };
+    xy_status st = part(ta, tb, 0, g_tile_tasks, g_tile_merges, &out->tile_workspace_bytes);
+    if (st != XY_OK) return st;
+    st = part(da, db, 1, g_dec_tasks, g_dec_merges, &out->dec_workspace_bytes);
+    if (st != XY_OK) return st;
+    // pages the tile part reads (its sequences' pages in order), copied to bf16 page i
+    int64_t n_pages = 0;
+    for (int i = ta; i < tb; ++i) n_pages += ((int64_t)context_lens[i] + block_size - 1) / block_size;
+    if (n_pages > INT32_MAX) return XY_ERR_UNSUPPORTED;
+    out->tile_num_pages = (int)n_pages;
+    out->tile_num_tasks = (int)g_tile_tasks.size(), out->tile_num_merges = (int)g_tile_merges.size();
+    out->dec_num_tasks = (int)g_dec_tasks.size(), out->dec_num_merges = (int)g_dec_merges.size();
+
+    const size_t A = XY_STEP_TABLES_ALIGN;
+    auto up = [&](size_t x) { return (x + A - 1) / A * A; };
+    const size_t S = (size_t)num_seqs, MB = (size_t)max_blocks;
+    const size_t nt = (size_t)(tb - ta), nd = (size_t)(db - da);
+    out->err_off = 0;
+    out->cu_off = up(4);
+    out->ctx_off = up(out->cu_off + 4 * (S + 1));
+    out->bt_off = up(out->ctx_off + 4 * S);
+    out->tile_cu_off = up(out->bt_off + 4 * S * MB);
+    out->tile_bt_off = up(out->tile_cu_off + 4 * (nt + 1));
+    out->tile_pages_off = up(out->tile_bt_off + 4 * nt * MB);
+    out->tile_tasks_off = up(out->tile_pages_off + 4 * (size_t)n_pages);
+    out->tile_merges_off = up(out->tile_tasks_off + sizeof(xy_task) * g_tile_tasks.size());
+    out->dec_cu_off = up(out->tile_merges_off + sizeof(xy_merge) * g_tile_merges.size());
+    out->dec_tasks_off = up(out->dec_cu_off + 4 * (nd + 1));
+    out->dec_merges_off = up(out->dec_tasks_off + sizeof(xy_task) * g_dec_tasks.size());
+    out->bytes = out->dec_merges_off + sizeof(xy_merge) * g_dec_merges.size();
+    if (out->bytes > staging_bytes) return XY_ERR_CAPACITY;
+
+    uint8_t *base = static_cast<uint8_t *>(staging);
+    int32_t *bt = reinterpret_cast<int32_t *>(base + out->bt_off);
+    st = xy_build_block_table(context_lens, num_seqs, block_size, free_list, num_free, max_blocks, bt,
+                              &out->pages_used);
+    if (st != XY_OK) return st;
+    const int32_t zero = 0;
+    std::memcpy(base + out->err_off, &zero, 4);
+    std::memcpy(base + out->cu_off, cu_seqlens_q, 4 * (S + 1));
+    if (S) std::memcpy(base + out->ctx_off, context_lens, 4 * S);
+    int32_t *cu_t = reinterpret_cast<int32_t *>(base + out->tile_cu_off);
+    int32_t *bt_t = reinterpret_cast<int32_t *>(base + out->tile_bt_off);
+    int32_t *pages = reinterpret_cast<int32_t *>(base + out->tile_pages_off);
+    int32_t next = 0;
+    for (int i = ta; i <= tb && tb > ta; ++i) cu_t[i - ta] = cu_seqlens_q[i] - cu_seqlens_q[ta];
+    for (int i = ta; i < tb; ++i) {
+        const int32_t n = (int32_t)(((int64_t)context_lens[i] + block_size - 1) / block_size);
+        int32_t *row = bt_t + (size_t)(i - ta) * MB;
+        for (int32_t j = 0; j < max_blocks; ++j) row[j] = j < n ? next + j : -1;
+        for (int32_t j = 0; j < n; ++j) pages[next + j] = bt[(size_t)i * MB + j];
+        next += n;
+    }
+    int32_t *cu_d = reinterpret_cast<int32_t *>(base + out->dec_cu_off);
+    for (int i = da; i <= db && db > da; ++i) cu_d[i - da] = cu_seqlens_q[i] - cu_seqlens_q[da];
+    if (!g_tile_tasks.empty())
+        std::memcpy(base + out->tile_tasks_off, g_tile_tasks.data(), sizeof(xy_task) * g_tile_tasks.size());
+    if (!g_tile_merges.empty())
+        std::memcpy(base + out->tile_merges_off, g_tile_merges.data(), sizeof(xy_merge) * g_tile_merges.size());
+    if (!g_dec_tasks.empty())
+        std::memcpy(base + out->dec_tasks_off, g_dec_tasks.data(), sizeof(xy_task) * g_dec_tasks.size());
+    if (!g_dec_merges.empty())
+        std::memcpy(base + out->dec_merges_off, g_dec_merges.data(), sizeof(xy_merge) * g_dec_merges.size());
     return XY_OK;
 }

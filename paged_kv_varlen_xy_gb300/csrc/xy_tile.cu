@@ -704,10 +704,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                             xy::f2_unpack(acc2[1], ls4[2], ls4[3]);
                             l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                         };
+                        // A tile that cuts through some row's visible keys (the causal diagonal, the
+                        // end of the context) runs once per task: its code is kept compact (one 32-key
+                        // chunk per loop step, the mask as the row's count of visible keys in the chunk)
+                        // so that it stays in the instruction cache beside the steady loop.
+                        auto masked_softmax = [&]() {
+                            float mx = -INFINITY;
+#pragma unroll 1
+                            for (int ci = 0; ci < 4; ++ci) {
+                                uint32_t r[32];
+                                xy::tmem_ld32(s_addr + 32 * ci, r);
+                                const int nv = lim - (kt0 + 32 * ci);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, i < nv ? __uint_as_float(r[i]) : -INFINITY);
+                            }
+                            const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
+                            if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
+                                const float alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
+                                m = m_new;
+                                l *= alpha;
+                                if (j > 0) {  // O_X has PV_X(0..j-1); rescale once the last of them is done
+                                    ok = warp_all(xy::mbar_wait(bar(B_OBAR0 + x), (ns - 1) & 1, abort_flag)) && ok;
+                                    xy::tc_fence_after();
+#pragma unroll 1
+                                    for (int h = 0; h < 4; ++h) {
+                                        uint32_t orow[32];
+                                        xy::tmem_ld32(o_addr + h * 32, orow);
+#pragma unroll
+                                        for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+                                        xy::tmem_st32(o_addr + h * 32, orow);
+                                    }
+                                }
+                            }
+                            const float neg_mu = m == -INFINITY ? 0.f : -m;
+                            float ls[2] = {0.f, 0.f};
+#pragma unroll 1
+                            for (int ci = 0; ci < 4; ++ci) {
+                                uint32_t r[32], pk[16];
+                                xy::tmem_ld32(s_addr + 32 * ci, r);
+                                const int nv = lim - (kt0 + 32 * ci);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) {
+                                    const float e0 = fmaf(__uint_as_float(r[2 * i]), p.scale_log2, neg_mu);
+                                    const float e1 = fmaf(__uint_as_float(r[2 * i + 1]), p.scale_log2, neg_mu);
+                                    const float p0 = 2 * i < nv ? ex2(e0) : 0.f, p1 = 2 * i + 1 < nv ? ex2(e1) : 0.f;
+                                    ls[i & 1] += p0 + p1;
+                                    pk[i] = xy::pack_bf16x2(p0, p1);
+                                }
+                                xy::tmem_st16(s_addr + 16 * ci, pk);  // over S columns already read
+                            }
+                            l += ls[0] + ls[1];
+                        };
                         if (full)
                             tile_softmax(std::true_type{});
                         else
-                            tile_softmax(std::false_type{});
+                            masked_softmax();
                     }
                     if (x == 0 && kt0 + kTileKeys > t.kv_end) {
                         // keys at or past kv_end: unused page slots or stale data; their P is 0 and
@@ -745,19 +796,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int w = 0; w < 4; ++w) bad |= vote[x * 4 + w];
             if (rows_on) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                // each thread writes its own row: 32-byte stores (one full sector each) when the
-                // buffers allow, the next 32 O columns loading from TMEM meanwhile
+                // each thread writes its own row, 32 O columns per loop step: 32-byte stores (one full
+                // sector each) when the buffers allow.  The epilogue runs once per task, so its code
+                // is kept compact (one step's code, not four unrolled copies).
                 const bool v8 = ((reinterpret_cast<uintptr_t>(p.out) | reinterpret_cast<uintptr_t>(p.ws_o)) & 31) == 0;
-                auto store_chunk = [&](const uint32_t (&r)[32], int cc) {
-                    if (!valid || bad) return;
-                    if (t.num_splits == 1) {
-                        const int64_t tok = f.seq_start + t.q_start + row / p.G;
-                        const int h = t.kv_head * p.G + row % p.G;
-                        __nv_bfloat16 *dst = p.out + (tok * p.Hq + h) * HD + cc * 32;
+                const bool st_ok = valid && !bad, to_out = t.num_splits == 1;
+                __nv_bfloat16 *dst_o = p.out;
+                float *dst_w = p.ws_o;
+                if (to_out) {
+                    const int64_t tok = f.seq_start + t.q_start + row / p.G;
+                    dst_o += (tok * p.Hq + t.kv_head * p.G + row % p.G) * HD;
+                } else {
+                    dst_w += ((int64_t)t.ws_row + row) * HD;
+                }
+#pragma unroll 1
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t r[32];
+                    xy::tmem_ld32(o_addr + 32 * cc, r);
+                    if (!st_ok) continue;
+                    if (to_out) {
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             w[i] = xy::pack_bf16x2(__uint_as_float(r[2 * i]) * inv, __uint_as_float(r[2 * i + 1]) * inv);
+                        __nv_bfloat16 *dst = dst_o + cc * 32;
                         if (v8) {
                             xy::st_global_v8(dst, reinterpret_cast<const uint32_t(&)[8]>(w[0]));
                             xy::st_global_v8(dst + 16, reinterpret_cast<const uint32_t(&)[8]>(w[8]));
@@ -767,34 +829,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
                         }
                     } else {
-                        float *dst = p.ws_o + ((int64_t)t.ws_row + row) * HD + cc * 32;
-                        uint32_t w[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(r[i]) * inv);
+                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * inv);
+                        float *dst = dst_w + cc * 32;
                         if (v8) {
 #pragma unroll
                             for (int v = 0; v < 4; ++v)
-                                xy::st_global_v8(dst + 8 * v, reinterpret_cast<const uint32_t(&)[8]>(w[8 * v]));
+                                xy::st_global_v8(dst + 8 * v, reinterpret_cast<const uint32_t(&)[8]>(r[8 * v]));
                         } else {
 #pragma unroll
                             for (int v = 0; v < 8; ++v)
-                                reinterpret_cast<uint4 *>(dst)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+                                reinterpret_cast<uint4 *>(dst)[v] = make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
                         }
                     }
-                };
-                uint32_t ra[32], rb[32];
-                xy::tmem_ld32_nowait(o_addr, ra);
-                xy::tmem_wait_ld(ra);
-                xy::tmem_ld32_nowait(o_addr + 32, rb);
-                store_chunk(ra, 0);
-                xy::tmem_wait_ld(rb);
-                xy::tmem_ld32_nowait(o_addr + 64, ra);
-                store_chunk(rb, 1);
-                xy::tmem_wait_ld(ra);
-                xy::tmem_ld32_nowait(o_addr + 96, rb);
-                store_chunk(ra, 2);
-                xy::tmem_wait_ld(rb);
-                store_chunk(rb, 3);
+                }
                 if (valid && !bad && t.num_splits > 1) p.ws_lse[(int64_t)t.ws_row + row] = l > 0.f ? m + __log2f(l) : -INFINITY;
             }
             if (active) {

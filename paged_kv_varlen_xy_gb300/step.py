@@ -4,11 +4,10 @@ KV append and paged attention (device).  Composition of libxy calls only; no ari
 import numpy as np
 import torch
 
-from . import (XY_SCHEDULE_DYNAMIC, XY_SCHEDULE_GREEDY, Plan, check_err_word, default_schedule, default_tiles,
-               xy_build_block_table, xy_build_step_tables, xy_build_task_table, xy_default_num_ctas,
-               xy_dequant_pages_fp8, xy_kv_append_paged, xy_kv_append_paged_fp8, xy_paged_attention,
-               xy_paged_attention_dynamic,
-               xy_paged_attention_fp8, xy_paged_attention_fp8_dynamic)
+from . import (XY_SCHEDULE_DYNAMIC, Plan, check_err_word, default_schedule, default_tiles,
+               xy_build_block_table, xy_build_step_tables, xy_default_num_ctas, xy_kv_append_paged,
+               xy_kv_append_paged_fp8, xy_paged_attention, xy_paged_attention_dynamic, xy_paged_attention_fp8,
+               xy_paged_attention_fp8_dynamic)
 
 
 class PagedBatch:
@@ -297,7 +296,7 @@ def run_step_fp8(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, s
 def split_ranges(q_lens):
     """(multi, single): the sequence ranges [a, b) of sequences with several new tokens and of
     one-token sequences, when each kind is one contiguous range (either may be empty); None when
-    the kinds interleave."""
+    the kinds interleave (the rule xy_build_fp8_step_tables applies)."""
     multi = np.asarray(q_lens) > 1
     S = len(multi)
     changes = int(np.count_nonzero(multi[1:] != multi[:-1])) if S > 1 else 0
@@ -311,80 +310,30 @@ def split_ranges(q_lens):
     return second, first
 
 
-class Fp8SplitBatch:
-    """A batch over 8-bit pages run in two parts: its one-token (decode) sequences on the 8-bit
-    decode path, its sequences with several new tokens (prefill, chunks, verify) on the tcgen05
-    tile path over bf16 copies of the pages those sequences read (xy_dequant_pages_fp8).  The two
-    kinds must form contiguous sequence ranges (see split_ranges); the tile part needs head_dim 128
-    and G dividing 128.  The tile part computes with K and V rounded to bf16 after dequantization."""
-
-    def __init__(self, cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv,
-                 head_dim, causal, device="cuda", num_ctas=None):
-        dev = torch.device(device)
-        cu = np.asarray(cu_seqlens_q, dtype=np.int32)
-        ctx = np.asarray(context_lens, dtype=np.int32)
-        q_lens = cu[1:] - cu[:-1]
-        rng = split_ranges(q_lens)
-        G = num_heads_q // num_heads_kv
-        if rng is None or head_dim != 128 or 128 % G:
-            raise ValueError("batch cannot be split into a decode range and a tile range")
-        (ta, tb), (da, db) = rng
-        self.cu_host, self.ctx_host = cu, ctx
-        self.block_table_host, self.pages_used = xy_build_block_table(ctx, block_size, free_list, max_blocks)
-        self.cu = torch.from_numpy(cu).to(dev)
-        self.ctx = torch.from_numpy(ctx).to(dev)
-        self.block_table = torch.from_numpy(self.block_table_host).to(dev)
-        self.slots = torch.empty(int(cu[-1]), dtype=torch.int64, device=dev)
-        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.block_size, self.causal = block_size, causal
-        self.Hkv, self.d = num_heads_kv, head_dim
-
-        def sub(a, b, fp8):
-            cu_s = (cu[a:b + 1] - cu[a]).astype(np.int32)
-            plan = Plan(cu_s, ctx[a:b], num_heads_q, num_heads_kv, head_dim, causal, device=dev, num_ctas=num_ctas,
-                        kv_fp8=fp8)
-            return dict(seq=(a, b), tok=(int(cu[a]), int(cu[b])), cu=torch.from_numpy(cu_s).to(dev), ctx=self.ctx[a:b],
-                        plan=plan)
-
-        self.decode = sub(da, db, True) if db > da else None
-        self.tile = None
-        if tb > ta:
-            t = sub(ta, tb, False)
-            # pages of the tile sequences, in order, and their block table over the copies
-            n = (ctx[ta:tb].astype(np.int64) + block_size - 1) // block_size
-            pages = np.concatenate([self.block_table_host[i][:k] for i, k in zip(range(ta, tb), n)]).astype(np.int32)
-            bt = -np.ones((tb - ta, max_blocks), dtype=np.int32)
-            base = np.concatenate([[0], np.cumsum(n)[:-1]])
-            for r, (b0, k) in enumerate(zip(base, n)):
-                bt[r, :k] = np.arange(b0, b0 + k, dtype=np.int32)
-            t["pages"] = torch.from_numpy(pages).to(dev)
-            t["bt"] = torch.from_numpy(bt).to(dev)
-            t["k"] = torch.empty(len(pages), num_heads_kv, block_size, head_dim, dtype=torch.bfloat16, device=dev)
-            t["v"] = torch.empty_like(t["k"])
-            self.tile = t
-
-
 class _Part:
-    """The plan of one part of a split batch (the fields the attention calls read from Plan)."""
+    """The plan of one part of a split batch (the fields the bench and tests read from Plan)."""
 
-    def __init__(self, tasks, merges, num_ctas, workspace, schedule, task_counter):
+    def __init__(self, tasks, merges, num_ctas, workspace, task_counter):
         self.tasks, self.merges, self.num_ctas, self.workspace = tasks, merges, num_ctas, workspace
-        self.schedule, self.task_counter = schedule, task_counter
-        self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
+        self.schedule, self.task_counter, self.dynamic = XY_SCHEDULE_DYNAMIC, task_counter, True
+        self.stats = {"balance": None}
+
+
+class _SplitBatch:
+    """A batch of Fp8SplitPlanner.plan(): device views of its tables (cu, ctx, block_table, err,
+    slots) and, per part, its sequence and token ranges and plan (tile / decode, None when empty)."""
 
 
 class Fp8SplitPlanner:
-    """Reusable builder of Fp8SplitBatch-shaped batches for one stream, for a serving loop that
-    re-plans every step over 8-bit pages: the host tables of both parts (block table, the tile
-    part's compact page list and block table over the copies, both task and merge tables, the
-    lengths and a zeroed error word) are packed into one pinned staging buffer and reach the
-    device in one copy; the device buffer, the split-KV workspaces, the slot buffer and the bf16
-    page-copy buffers are kept between steps and grown when a batch needs more.  plan() returns a
-    batch for run_step_fp8_split / attention_fp8_split; its device tables alternate between two
-    buffers as the Planner's do (valid until the plan() after next; plan(stream=s) must be ordered
-    after the kernels of the batch planned two plans earlier)."""
-
-    _ALIGN = 256
+    """Reusable planner of steps over 8-bit pages whose one-token (decode) sequences run on the
+    8-bit decode path and whose multi-token sequences run on the tcgen05 tile path over bf16
+    copies of their pages.  The tables (xy_build_fp8_step_tables: split, block table, page list
+    and compact block table of the tile part, both task and merge tables) are built by libxy into
+    one pinned staging buffer and reach the device in one copy; the device buffers, workspaces,
+    slot buffer, claim counters and page-copy buffers are kept between steps and grown when a batch
+    needs more.  Two device table buffers alternate between plans: a batch's device tables stay
+    valid until the plan() after next (plan(stream=s) must be ordered after the kernels of the
+    batch planned two plans earlier).  This class only marshals arguments."""
 
     def __init__(self, num_heads_q, num_heads_kv, head_dim, block_size, max_blocks, causal, device="cuda",
                  num_ctas=None):
@@ -401,11 +350,12 @@ class Fp8SplitPlanner:
         self._ws = [torch.empty(16, dtype=torch.uint8, device=self.dev) for _ in range(2)]
         self._slots = torch.empty(1, dtype=torch.int64, device=self.dev)
         self._copies = None
-        # the two parts' claim counters (dynamic deal; each launch returns its counter to zero)
-        self._counter = torch.zeros(2, dtype=torch.int32, device=self.dev)
-        self._counter_d = torch.zeros(2, dtype=torch.int32, device=self.dev)
+        # the two parts' claim counters (words 0-1 tile part, 2-3 decode part; each launch returns
+        # its pair to zero)
+        self._counters = torch.zeros(4, dtype=torch.int32, device=self.dev)
         self._copied = torch.cuda.Event() if self.dev.type == "cuda" else None
         self._pending = False
+        self.last_upload_bytes = 0
 
     def _wait_upload(self):
         if self._pending:
@@ -417,52 +367,27 @@ class Fp8SplitPlanner:
         first; a caller may do it beforehand to keep the wait out of its own timing)."""
         self._wait_upload()
 
-    def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
-        cu = np.asarray(cu_seqlens_q, dtype=np.int32)
-        ctx = np.asarray(context_lens, dtype=np.int32)
-        q_lens = cu[1:] - cu[:-1]
-        rng = split_ranges(q_lens)
-        if rng is None:
-            raise ValueError("batch cannot be split into a decode range and a tile range")
-        (ta, tb), (da, db) = rng
-        S, MB, bs = len(ctx), self.MB, self.bs
-        bt, pages_used = xy_build_block_table(ctx, bs, free_list, MB)
-        arrays = {"err": np.zeros(1, np.int32), "cu": cu, "ctx": ctx, "bt": bt}
-        parts = {}
-        if tb > ta:
-            cu_t = (cu[ta:tb + 1] - cu[ta]).astype(np.int32)
-            q_tile, kv_chunk = default_tiles(self.Hq, self.Hkv, self.d)
-            r = xy_build_task_table(cu_t, ctx[ta:tb], self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, q_tile,
-                                    kv_chunk, XY_SCHEDULE_DYNAMIC)
-            n = (ctx[ta:tb].astype(np.int64) + bs - 1) // bs
-            pages = np.concatenate([bt[i][:k] for i, k in zip(range(ta, tb), n)]).astype(np.int32)
-            base = np.concatenate([[0], np.cumsum(n)[:-1]])
-            bt_t = -np.ones((tb - ta, MB), dtype=np.int32)
-            for row, (b0, k) in enumerate(zip(base, n)):
-                bt_t[row, :k] = np.arange(b0, b0 + k, dtype=np.int32)
-            arrays.update(cu_t=cu_t, tasks_t=r["tasks"], merges_t=r["merges"], pages_t=pages, bt_t=bt_t)
-            parts["tile"] = (ta, tb, r)
-        if db > da:
-            cu_d = (cu[da:db + 1] - cu[da]).astype(np.int32)
-            T_d = int(cu[db] - cu[da])
-            q_tile, kv_chunk = default_tiles(self.Hq, self.Hkv, self.d, True, pure_decode=T_d == db - da)
-            r = xy_build_task_table(cu_d, ctx[da:db], self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, q_tile,
-                                    kv_chunk, XY_SCHEDULE_DYNAMIC)
-            arrays.update(cu_d=cu_d, tasks_d=r["tasks"], merges_d=r["merges"])
-            parts["decode"] = (da, db, r)
-        # pack at 256-byte offsets into the pinned staging buffer, one copy to the device
-        off, total = {}, 0
-        for k, a in arrays.items():
-            off[k] = total
-            total += (a.nbytes + self._ALIGN - 1) // self._ALIGN * self._ALIGN
-        self._wait_upload()
-        if self._host is None or self._host.numel() < total:
-            size = max(total, 2 * (self._host.numel() if self._host is not None else 0), 1 << 16)
+    def _ensure(self, nbytes):
+        if self._host is None or self._host.numel() < nbytes:
+            size = max(nbytes, 2 * (self._host.numel() if self._host is not None else 0), 1 << 16)
+            self._wait_upload()
             self._host = torch.empty(size, dtype=torch.uint8).pin_memory()
             self._host_np = self._host.numpy()
             self._dev_bufs = [torch.empty(size, dtype=torch.uint8, device=self.dev) for _ in range(2)]
-        for k, a in arrays.items():
-            self._host_np[off[k]:off[k] + a.nbytes] = a.reshape(-1).view(np.uint8)
+
+    def plan(self, cu_seqlens_q, context_lens, free_list, stream=None):
+        from . import xy_build_fp8_step_tables
+        cu = np.asarray(cu_seqlens_q, dtype=np.int32)
+        ctx = np.asarray(context_lens, dtype=np.int32)
+        self._ensure(1 << 16)
+        self._wait_upload()   # the staging buffer is written below
+        for _ in range(2):
+            st, t = xy_build_fp8_step_tables(cu, ctx, free_list, self.bs, self.MB, self.Hq, self.Hkv, self.d,
+                                             self.causal, self.num_ctas, self._host.data_ptr(), self._host.numel())
+            if st == 0:
+                break
+            self._ensure(t.bytes)   # too small: grow and build again
+        total = t.bytes
         stm = torch.cuda.current_stream(self.dev) if stream is None else stream
         self._flip ^= 1
         dbuf = self._dev_bufs[self._flip]
@@ -472,57 +397,65 @@ class Fp8SplitPlanner:
         self._pending = True
         self.last_upload_bytes = total
 
-        def dv(k, shape):
+        def dv(off, shape):
             n_el = int(np.prod(shape))
-            return dbuf[off[k]:off[k] + 4 * n_el].view(torch.int32).view(*shape)
+            return dbuf[off:off + 4 * n_el].view(torch.int32).view(*shape)
 
+        S, MB, bs = len(ctx), self.MB, self.bs
         b = _SplitBatch()
-        b.cu_host, b.ctx_host, b.block_table_host, b.pages_used = cu, ctx, bt, pages_used
-        b.cu, b.ctx, b.block_table, b.err = dv("cu", (S + 1,)), dv("ctx", (S,)), dv("bt", (S, MB)), dv("err", (1,))
+        b.t, b.tables = t, dbuf
+        b.pages_used = t.pages_used
+        b.cu_host, b.ctx_host = cu, ctx
+        b.cu, b.ctx, b.block_table = dv(t.cu_off, (S + 1,)), dv(t.ctx_off, (S,)), dv(t.bt_off, (S, MB))
+        b.err = dv(t.err_off, (1,))
+        b.block_table_host = self._host_np[t.bt_off:t.bt_off + 4 * S * MB].view(np.int32).reshape(S, MB).copy()
         T = int(cu[-1])
         if self._slots.numel() < T:
             self._slots = torch.empty(max(T, 2 * self._slots.numel()), dtype=torch.int64, device=self.dev)
         b.slots = self._slots[:T]
-        b.block_size, b.causal, b.Hkv, b.d = bs, self.causal, self.Hkv, self.d
-        b.tile = b.decode = None
+        b.block_size, b.causal, b.Hkv, b.d, b.MB, b.num_ctas = bs, self.causal, self.Hkv, self.d, MB, self.num_ctas
+        b.counters = self._counters
 
         def ws(i, nbytes):
-            if self._ws[i].numel() < nbytes:
+            if nbytes and self._ws[i].numel() < nbytes:
                 self._ws[i] = torch.empty(max(nbytes, 2 * self._ws[i].numel()), dtype=torch.uint8, device=self.dev)
-            return self._ws[i]
+            return self._ws[i] if nbytes else None
 
-        if "tile" in parts:
-            a, bnd, r = parts["tile"]
-            n_t, m_t = len(r["tasks"]), len(r["merges"])
-            plan = _Part(dv("tasks_t", (n_t, 8)), dv("merges_t", (m_t, 8)), self.num_ctas,
-                         ws(0, r["workspace_bytes"]), XY_SCHEDULE_DYNAMIC, self._counter)
-            n_pages = len(arrays["pages_t"])
-            need = n_pages * self.Hkv * bs * self.d
-            if self._copies is None or self._copies[0].numel() < need:
-                self._copies = [torch.empty(max(need, 2 * (self._copies[0].numel() if self._copies else 0)),
-                                            dtype=torch.bfloat16, device=self.dev) for _ in range(2)]
-            b.tile = dict(seq=(a, bnd), tok=(int(cu[a]), int(cu[bnd])), cu=dv("cu_t", (bnd - a + 1,)),
-                          ctx=b.ctx[a:bnd], plan=plan, pages=dv("pages_t", (n_pages,)),
-                          bt=dv("bt_t", (bnd - a, MB)),
-                          k=self._copies[0][:need].view(n_pages, self.Hkv, bs, self.d),
-                          v=self._copies[1][:need].view(n_pages, self.Hkv, bs, self.d))
-        if "decode" in parts:
-            a, bnd, r = parts["decode"]
-            n_d, m_d = len(r["tasks"]), len(r["merges"])
-            plan = _Part(dv("tasks_d", (n_d, 8)), dv("merges_d", (m_d, 8)), self.num_ctas,
-                         ws(1, r["workspace_bytes"]), XY_SCHEDULE_DYNAMIC, self._counter_d)
-            b.decode = dict(seq=(a, bnd), tok=(int(cu[a]), int(cu[bnd])), cu=dv("cu_d", (bnd - a + 1,)),
-                            ctx=b.ctx[a:bnd], plan=plan)
+        b.tile_ws, b.dec_ws = ws(0, t.tile_workspace_bytes), ws(1, t.dec_workspace_bytes)
+        need = t.tile_num_pages * self.Hkv * bs * self.d
+        if need and (self._copies is None or self._copies[0].numel() < need):
+            self._copies = [torch.empty(max(need, 2 * (self._copies[0].numel() if self._copies else 0)),
+                                        dtype=torch.bfloat16, device=self.dev) for _ in range(2)]
+        b.copy_k = self._copies[0][:need].view(t.tile_num_pages, self.Hkv, bs, self.d) if need else None
+        b.copy_v = self._copies[1][:need].view(t.tile_num_pages, self.Hkv, bs, self.d) if need else None
+        b.tile = b.decode = None
+        if t.tile_seq_end > t.tile_seq_begin:
+            b.tile = dict(seq=(t.tile_seq_begin, t.tile_seq_end), tok=(t.tile_tok_begin, t.tile_tok_end),
+                          plan=_Part(dv(t.tile_tasks_off, (t.tile_num_tasks, 8)),
+                                     dv(t.tile_merges_off, (t.tile_num_merges, 8)), self.num_ctas, b.tile_ws,
+                                     self._counters[0:2]))
+        if t.dec_seq_end > t.dec_seq_begin:
+            b.decode = dict(seq=(t.dec_seq_begin, t.dec_seq_end), tok=(t.dec_tok_begin, t.dec_tok_end),
+                            plan=_Part(dv(t.dec_tasks_off, (t.dec_num_tasks, 8)),
+                                       dv(t.dec_merges_off, (t.dec_num_merges, 8)), self.num_ctas, b.dec_ws,
+                                       self._counters[2:4]))
         return b
 
 
-class _SplitBatch:
-    """A batch of Fp8SplitPlanner.plan(): the attributes of Fp8SplitBatch."""
+def Fp8SplitBatch(cu_seqlens_q, context_lens, free_list, block_size, max_blocks, num_heads_q, num_heads_kv, head_dim,
+                  causal, device="cuda", num_ctas=None):
+    """One split step's batch over 8-bit pages (a planner used once; see Fp8SplitPlanner).  The tile
+    part computes with K and V rounded to bf16 after dequantization."""
+    pl = Fp8SplitPlanner(num_heads_q, num_heads_kv, head_dim, block_size, max_blocks, causal, device=device,
+                         num_ctas=num_ctas)
+    b = pl.plan(cu_seqlens_q, context_lens, free_list)
+    b._planner = pl   # keeps its buffers alive with the batch
+    return b
 
 
 def run_step_fp8_split(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_scales, scale, out=None, stream=None):
-    """One step of an Fp8SplitBatch: slot mapping and the quantizing append for the whole batch,
-    then attention_fp8_split."""
+    """One step of a split batch: slot mapping and the quantizing append for the whole batch (one
+    launch), then attention_fp8_split."""
     out = torch.empty_like(q) if out is None else out
     xy_kv_append_paged_fp8(k_new, v_new, batch.cu, batch.ctx, batch.block_table, k_pages, v_pages, k_scales, v_scales,
                            batch.err, slot_mapping=batch.slots, stream=stream)
@@ -530,33 +463,12 @@ def run_step_fp8_split(batch, q, k_new, v_new, k_pages, v_pages, k_scales, v_sca
 
 
 def attention_fp8_split(batch, q, k_pages, v_pages, k_scales, v_scales, scale, out, stream=None):
-    """The attention of an Fp8SplitBatch: the tile part (bf16 copies of its pages, tcgen05
-    attention) and the decode part (8-bit decode path), each writing its own rows of out."""
-    t = batch.tile
-    if t is not None:
-        a, b = t["tok"]
-        xy_dequant_pages_fp8(k_pages, v_pages, k_scales, v_scales, t["pages"], t["k"], t["v"], batch.err, stream)
-        pl = t["plan"]
-        if pl.dynamic:
-            xy_paged_attention_dynamic(q[a:b], t["cu"], t["ctx"], t["bt"], t["k"], t["v"], scale, batch.causal,
-                                       pl.tasks, pl.merges, pl.num_ctas, pl.workspace, pl.task_counter, batch.err,
-                                       out[a:b], stream)
-        else:
-            xy_paged_attention(q[a:b], t["cu"], t["ctx"], t["bt"], t["k"], t["v"], scale, batch.causal, pl.tasks,
-                               pl.merges, pl.num_ctas, pl.workspace, batch.err, out[a:b], stream)
-    dd = batch.decode
-    if dd is not None:  # (pages appended above are visible: same stream)
-        a, b = dd["tok"]
-        pl = dd["plan"]
-        sa, sb = dd["seq"]
-        if pl.dynamic:
-            xy_paged_attention_fp8_dynamic(q[a:b], dd["cu"], dd["ctx"], batch.block_table[sa:sb], k_pages, v_pages,
-                                           k_scales, v_scales, scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas,
-                                           pl.workspace, pl.task_counter, batch.err, out[a:b], stream)
-        else:
-            xy_paged_attention_fp8(q[a:b], dd["cu"], dd["ctx"], batch.block_table[sa:sb], k_pages, v_pages,
-                                   k_scales, v_scales, scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas,
-                                   pl.workspace, batch.err, out[a:b], stream)
+    """The attention of a split batch: xy_paged_attention_fp8_mixed (page copies and tcgen05 tiles
+    for the tile part, the 8-bit decode path for the decode part, each writing its rows of out)."""
+    from . import xy_paged_attention_fp8_mixed
+    xy_paged_attention_fp8_mixed(q, batch.tables, batch.t, k_pages, v_pages, k_scales, v_scales, len(batch.ctx_host),
+                                 batch.MB, scale, batch.causal, batch.num_ctas, batch.copy_k, batch.copy_v,
+                                 batch.tile_ws, batch.dec_ws, batch.counters, batch.err, out, stream)
     return out
 
 
