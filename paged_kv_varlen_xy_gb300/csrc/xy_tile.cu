@@ -10,7 +10,7 @@
 // tiles.  One persistent CTA per SM, twelve warps in three warpgroups:
 //   warp 8      producer: TMA loads of the task's query rows (G heads x 128/G tokens per tile,
 //               one 3-D box per 64-column half) and of 128-key K and V tiles gathered page by
-//               page through the block table (2-D boxes, 128-byte swizzle) into a 5-slot ring
+//               page through the block table (2-D boxes, 128-byte swizzle) into a 4-slot ring
 //               (K_j and V_j take separate slots, so K runs ahead of V);
 //   warp 9      MMA issuer (one thread), per K/V tile j:
 //                 PV_A(j-1), S_A(j), PV_B(j-1), S_B(j)
@@ -21,7 +21,8 @@
 //               lane = row), masked row max, exp2, row sum, P back to TMEM.  While one group
 //               works, the tensor core runs the other tile's MMAs.  O_X is rescaled in TMEM only
 //               when a row's running max grows by more than 2^8 (otherwise the stale max is kept,
-//               which is exact because O and the row sum share it).  Epilogue: O / l from TMEM.
+//               which is exact because O and the row sum share it).  Epilogue: O / l from TMEM,
+//               staged in shared memory and written by TMA stores for whole query tiles.
 //               Warps 0..3 are also the math warps of decode-path tasks;
 //   warp 10     second producer of the decode ring; warp 11 claims tasks under the dynamic deal.
 // Registers: the CTA is launched with 168 per thread; the softmax warpgroups raise theirs to 200
@@ -52,7 +53,7 @@ using xy::TaskInfo;
 
 constexpr int HD = 128;
 constexpr int kTileKeys = 128;
-constexpr int kSlots = 5;                       // K/V ring slots (one K or V tile each)
+constexpr int kSlots = 4;                       // K/V ring slots (one K or V tile each)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDecProducerWarp = 10;   // second producer of the decode ring (odd stages)
@@ -88,8 +89,11 @@ using DecRing = xy::dec::Ring<HD, 4, 16>;
 static_assert(XY_TILE_MIN_ROWS <= 16, "decode-path tasks of the unified kernel have at most 16 rows");
 constexpr int kDecStagesOff = 0;
 constexpr int kDecSlotsOff = DecRing::kBytes;
-constexpr int kBarOff = kSlotOff + kSlots * kTileBytes;
-static_assert(kDecSlotsOff + DecRing::kSlotBytes <= kBarOff, "decode path fits in the tile path's bytes");
+// the epilogue's staging of bf16 output rows for the TMA store: one 64-column half of one query
+// tile per softmax group (128 rows x 128 bytes, 128-byte swizzle), outside the decode path's bytes
+constexpr int kStageOff = kSlotOff + kSlots * kTileBytes;
+constexpr int kBarOff = kStageOff + 2 * kHalfBytes;
+static_assert(kDecSlotsOff + DecRing::kSlotBytes <= kStageOff, "decode path fits below the output staging");
 constexpr int kDecBarOff = kBarOff + B_COUNT * 8;    // decode ring full[4], empty[4], task-done[2]
 constexpr int kMiscOff = kDecBarOff + (2 * DecRing::kStages + 2) * 8;  // TMEM base, abort flag, decode go
 constexpr int kVoteOff = kMiscOff + 16;             // one vote per softmax warp, then 2 x 4 decode votes
@@ -114,7 +118,8 @@ __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu
 template <bool DYN>
 __global__ void __launch_bounds__(kThreads, 1)
     meta_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                          const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap_d,
+                          const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                          const __grid_constant__ CUtensorMap kmap_d,
                           const __grid_constant__ CUtensorMap vmap_d, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = xy::smem_u32(smem_raw);
@@ -194,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             xy::prefetch_tensormap(&kmap);
             xy::prefetch_tensormap(&vmap);
             xy::prefetch_tensormap(&qmap);
+            xy::prefetch_tensormap(&omap);
             xy::prefetch_tensormap(&kmap_d);
             xy::prefetch_tensormap(&vmap_d);
         }
@@ -794,7 +800,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             int bad = 0;
 #pragma unroll
             for (int w = 0; w < 4; ++w) bad |= vote[x * 4 + w];
-            if (rows_on) {
+            // A whole query tile (all 128 rows valid) with bf16 output: the group stages its normalized
+            // rows in shared memory (one 64-column half at a time, the TMA's 128-byte swizzle) and one
+            // thread writes each half with a TMA store, which moves whole lines instead of 32-byte
+            // pieces of 128 different rows.  Uniform in the group (it depends on the task and x).
+            const bool tma_out = active && t.num_splits == 1 && R - x * 128 >= 128;
+            if (tma_out) {
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                const bool leader = (warp & 3) == 0 && lane == 0;
+                const uint32_t stage = base + kStageOff + x * kHalfBytes;
+                uint8_t *stage_row = gbase + kStageOff + x * kHalfBytes + trow * 128;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (leader) xy::bulk_wait_read();   // the group's previous store has read the staging
+                    xy::named_bar_sync(1 + x, 128);
+                    uint32_t ra[32], rb[32];
+                    xy::tmem_ld32_nowait(o_addr + hh * 64, ra);
+                    xy::tmem_ld32_nowait(o_addr + hh * 64 + 32, rb);
+                    xy::tmem_wait_ld(ra);
+                    xy::tmem_wait_ld(rb);
+                    if (!bad) {
+                        auto stage_chunks = [&](const uint32_t (&r)[32], int c0) {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {   // 16-byte chunk c0 + c: 8 columns
+                                uint4 v;
+                                v.x = xy::pack_bf16x2(__uint_as_float(r[8 * c]) * inv, __uint_as_float(r[8 * c + 1]) * inv);
+                                v.y = xy::pack_bf16x2(__uint_as_float(r[8 * c + 2]) * inv, __uint_as_float(r[8 * c + 3]) * inv);
+                                v.z = xy::pack_bf16x2(__uint_as_float(r[8 * c + 4]) * inv, __uint_as_float(r[8 * c + 5]) * inv);
+                                v.w = xy::pack_bf16x2(__uint_as_float(r[8 * c + 6]) * inv, __uint_as_float(r[8 * c + 7]) * inv);
+                                *reinterpret_cast<uint4 *>(stage_row + (((c0 + c) ^ (trow & 7)) << 4)) = v;
+                            }
+                        };
+                        stage_chunks(ra, 0);
+                        stage_chunks(rb, 4);
+                    }
+                    xy::fence_async_smem();
+                    xy::named_bar_sync(1 + x, 128);
+                    if (leader && !bad) {
+                        xy::tma_store_3d(&omap, stage, hh * 64, t.kv_head * p.G, f.seq_start + t.q_start + x * qt_tokens);
+                        xy::bulk_commit();
+                    }
+                }
+            } else if (rows_on) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 // each thread writes its own row, 32 O columns per loop step: 32-byte stores (one full
                 // sector each) when the buffers allow.  The epilogue runs once per task, so its code
@@ -863,6 +910,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             *abort_flag = 1;
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
         }
+        // the group's output stores have completed before the CTA leaves
+        if ((warp & 3) == 0 && lane == 0) xy::bulk_wait_all();
     }
 
     xy::tc_fence_before();
@@ -929,6 +978,12 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return XY_ERR_CUDA;
+    // the output in the same layout and boxes, for the epilogue's TMA stores of whole query tiles
+    CUtensorMap om;
+    if (fn(&om, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.out, qdims, qstr, qbox, e3, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return XY_ERR_CUDA;
     static PerDeviceOnce configured[2];  // per instantiation and device
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
@@ -950,9 +1005,9 @@ xy_status launch_meta_attention(const AttnParams &p, const void *k_pages, const 
     }
     const cudaError_t e =
         dyn ? xy::launch_dependent(meta_attention_kernel<true>, dim3(num_ctas), dim3(kThreads), kSmemBytes, st, km, vm,
-                                   qm, kmap_d, vmap_d, p)
+                                   qm, om, kmap_d, vmap_d, p)
             : xy::launch_dependent(meta_attention_kernel<false>, dim3(num_ctas), dim3(kThreads), kSmemBytes, st, km,
-                                   vm, qm, kmap_d, vmap_d, p);
+                                   vm, qm, om, kmap_d, vmap_d, p);
     return e == cudaSuccess ? XY_OK : cuda_fail(e, "meta_attention_kernel launch");
 }
 
