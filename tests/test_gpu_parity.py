@@ -269,3 +269,15 @@ def test_fused_append_flags_a_page_outside_the_pool():
     # only the one token with a valid slot was written
     changed = (vals["k_pool"] != before).any(dim=-1).any(dim=-1).any(dim=-1).sum().item()
     assert changed == 1
+
+
+def test_full_size_verify_sampled():
+    # the bench's speculative-verify batch (64 sequences of 2..8 new tokens over 512..8192 keys) in its
+    # launch configuration: every row of eight sampled sequences
+    wl = workloads.verify()
+    rng = np.random.default_rng(6)
+    seqs = sorted(rng.choice(wl.num_seqs, size=8, replace=False).tolist())
+    cu = wl.cu_seqlens_q
+    rows = [(t, h) for i in seqs for t in range(int(cu[i]), int(cu[i + 1])) for h in range(wl.num_heads_q)]
+    r = run(wl, rows=rows, sample_seqs=seqs, schedule=4)
+    assert_parity(r)
