@@ -85,8 +85,8 @@ enum {
 // The decode path (tasks of at most XY_TILE_MIN_ROWS rows, xy_decode_path.cuh) uses the same
 // bytes: its stage ring from offset 0 and its merge slots after it.  A switch of task kind waits
 // until the other kind's consumers are done with shared memory.
-using DecRing = xy::dec::Ring<HD, 4, 16>;
-static_assert(XY_TILE_MIN_ROWS <= 16, "decode-path tasks of the unified kernel have at most 16 rows");
+using DecRing = xy::dec::Ring<HD, 4, (XY_TILE_MIN_ROWS + 15) / 16 * 16>;
+static_assert(XY_TILE_MIN_ROWS <= DecRing::kMaxRows, "decode-path tasks of the unified kernel fit the ring");
 constexpr int kDecStagesOff = 0;
 constexpr int kDecSlotsOff = DecRing::kBytes;
 // the epilogue's staging of bf16 output rows for the TMA store: one 64-column half of one query
@@ -283,6 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TaskInfo f = tc.cur;
             const xy_task &t = f.t;
             const bool has_b = t.q_rows * p.G > 128;
+            // while the previous task's last S still reads the Q buffer, bring this task's query
+            // rows into L2 (one prefetch per 64-column half of each query tile)
+            if (qk >= 1 && lane < (has_b ? 4 : 2))
+                xy::tma_prefetch_3d(&qmap, (lane & 1) * 64, t.kv_head * p.G, f.seq_start + t.q_start + (lane >> 1) * qt_tokens);
             if (qk >= 1 && !warp_all(xy::mbar_wait(bar(B_QEMPTY), (qk - 1) & 1, abort_flag))) {
                 ok = false;
                 break;
@@ -714,15 +718,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // end of the context) runs once per task: its code is kept compact (one 32-key
                         // chunk per loop step, the mask as the row's count of visible keys in the chunk)
                         // so that it stays in the instruction cache beside the steady loop.
+                        // Each 32-key chunk is classified for the whole warp: no row sees any of its
+                        // keys (no load; P = 0), every row sees all of them (no per-key mask), or the
+                        // chunk holds some row's limit (masked).  On the causal diagonal most chunks
+                        // of a warp's eight tokens are whole or empty.
                         auto masked_softmax = [&]() {
                             float mx = -INFINITY;
 #pragma unroll 1
                             for (int ci = 0; ci < 4; ++ci) {
+                                const int nv = lim - (kt0 + 32 * ci);
+                                if (__all_sync(0xffffffffu, nv <= 0)) continue;
                                 uint32_t r[32];
                                 xy::tmem_ld32(s_addr + 32 * ci, r);
-                                const int nv = lim - (kt0 + 32 * ci);
+                                if (__all_sync(0xffffffffu, nv >= 32)) {
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, i < nv ? __uint_as_float(r[i]) : -INFINITY);
+                                    for (int i = 0; i < 32; i += 2) mx = xy::max3(mx, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                                } else {
+#pragma unroll
+                                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, i < nv ? __uint_as_float(r[i]) : -INFINITY);
+                                }
                             }
                             const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
                             if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
@@ -747,15 +761,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                             for (int ci = 0; ci < 4; ++ci) {
                                 uint32_t r[32], pk[16];
-                                xy::tmem_ld32(s_addr + 32 * ci, r);
                                 const int nv = lim - (kt0 + 32 * ci);
+                                if (__all_sync(0xffffffffu, nv <= 0)) {
 #pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const float e0 = fmaf(__uint_as_float(r[2 * i]), p.scale_log2, neg_mu);
-                                    const float e1 = fmaf(__uint_as_float(r[2 * i + 1]), p.scale_log2, neg_mu);
-                                    const float p0 = 2 * i < nv ? ex2(e0) : 0.f, p1 = 2 * i + 1 < nv ? ex2(e1) : 0.f;
-                                    ls[i & 1] += p0 + p1;
-                                    pk[i] = xy::pack_bf16x2(p0, p1);
+                                    for (int i = 0; i < 16; ++i) pk[i] = 0u;
+                                } else {
+                                    xy::tmem_ld32(s_addr + 32 * ci, r);
+                                    if (__all_sync(0xffffffffu, nv >= 32)) {
+#pragma unroll
+                                        for (int i = 0; i < 16; ++i) {
+                                            const float p0 = ex2(fmaf(__uint_as_float(r[2 * i]), p.scale_log2, neg_mu));
+                                            const float p1 = ex2(fmaf(__uint_as_float(r[2 * i + 1]), p.scale_log2, neg_mu));
+                                            ls[i & 1] += p0 + p1;
+                                            pk[i] = xy::pack_bf16x2(p0, p1);
+                                        }
+                                    } else {
+#pragma unroll
+                                        for (int i = 0; i < 16; ++i) {
+                                            const float e0 = fmaf(__uint_as_float(r[2 * i]), p.scale_log2, neg_mu);
+                                            const float e1 = fmaf(__uint_as_float(r[2 * i + 1]), p.scale_log2, neg_mu);
+                                            const float p0 = 2 * i < nv ? ex2(e0) : 0.f, p1 = 2 * i + 1 < nv ? ex2(e1) : 0.f;
+                                            ls[i & 1] += p0 + p1;
+                                            pk[i] = xy::pack_bf16x2(p0, p1);
+                                        }
+                                    }
                                 }
                                 xy::tmem_st16(s_addr + 16 * ci, pk);  // over S columns already read
                             }
