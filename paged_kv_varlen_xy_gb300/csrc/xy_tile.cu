@@ -424,14 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc.prefetch_next(p);
                 issued = true;
                 for (int j = 0; j <= n && ok; ++j) {
-                    if (j < n) {  // K_j has landed
-                        const int ck = c + 2 * j;
-                        if (!wait(bar(B_FULL0 + ck % kSlots), (ck / kSlots) & 1)) break;
-                    }
                     if (j >= 1) {  // V_{j-1} has landed
                         const int cv = c + 2 * (j - 1) + 1;
                         if (!wait(bar(B_FULL0 + cv % kSlots), (cv / kSlots) & 1)) break;
                     }
+                    // K_j is waited for only before the first S that reads it, so that a K tile
+                    // still in flight does not hold back tile A's PV of the previous tile
+                    bool k_here = j >= n;
                     for (int x = 0; x < nx && ok; ++x) {
                         if (j >= 1) {
                             // P_X(j-1) written (and O_X corrected) by its softmax group; for the
@@ -441,7 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                             xy::tc_fence_after();
                             issue_pv(x, j - 1);
                         }
-                        if (j < n) issue_s(x, j);
+                        if (j < n) {
+                            if (!k_here) {
+                                const int ck = c + 2 * j;
+                                if (!wait(bar(B_FULL0 + ck % kSlots), (ck / kSlots) & 1)) break;
+                                k_here = true;
+                            }
+                            issue_s(x, j);
+                        }
                     }
                     if (!ok) break;
                     if (j >= 1) xy::umma_commit(bar(B_EMPTY0 + (c + 2 * (j - 1) + 1) % kSlots));  // V_{j-1}

@@ -281,3 +281,35 @@ def test_full_size_verify_sampled():
     rows = [(t, h) for i in seqs for t in range(int(cu[i]), int(cu[i + 1])) for h in range(wl.num_heads_q)]
     r = run(wl, rows=rows, sample_seqs=seqs, schedule=4)
     assert_parity(r)
+
+
+@pytest.mark.parametrize("config,launches", [("prefill", 200), ("mixed", 30), ("verify", 100)])
+def test_repeated_launches_bit_identical(config, launches):
+    # Each task's result does not depend on which CTA runs it or on how the warps of a CTA drift
+    # against one another, so back-to-back launches of the bench's batches (dynamic deal) give
+    # bit-identical outputs and raise no device error (a barrier phase overtaken by a fast warp
+    # would show here as a wait that gives up, or as a wrong output).
+    from paged_kv_varlen_xy_gb300 import step as xystep
+    import paged_kv_varlen_xy_gb300 as xy
+
+    wl = workloads.make(config)
+    dev = torch.device("cuda")
+    vals = wl.tensors(dev)
+    batch = xystep.PagedBatch(wl.cu_seqlens_q, wl.context_lens, wl.free_list, wl.block_size, wl.max_blocks,
+                              wl.num_heads_q, wl.num_heads_kv, wl.head_dim, wl.causal, device=dev, schedule=4)
+    first = xystep.run_step(batch, vals["q"], vals["k_new"], vals["v_new"], vals["k_pool"], vals["v_pool"], wl.scale)
+    pl = batch.plan
+    ref = first.view(torch.int16)
+    outs = [torch.empty_like(first) for _ in range(2)]
+    differ = []
+    for i in range(launches):
+        out = outs[i & 1]
+        xy.xy_paged_attention_dynamic(vals["q"], batch.cu, batch.ctx, batch.block_table, vals["k_pool"],
+                                      vals["v_pool"], wl.scale, batch.causal, pl.tasks, pl.merges, pl.num_ctas,
+                                      pl.workspace, pl.task_counter, batch.err, out)
+        if i % 16 == 15 and not torch.equal(out.view(torch.int16), ref):
+            differ.append(i)
+    torch.cuda.synchronize()
+    xystep.check(batch)
+    assert not differ, f"launches {differ} differ from the first"
+    assert torch.equal(outs[(launches - 1) & 1].view(torch.int16), ref)
