@@ -217,7 +217,10 @@ __device__ __forceinline__ void drain(const Smem &sm, int ctr, int pw = 0, int n
 // transpose.  Accumulator tile (cc, e): its row g holds column 32cc + 2g + e and its row g + 8
 // column 32cc + 16 + 2g + e; its columns are the query rows.  Otherwise as consume_task: each math
 // warp takes 32 keys of every stage, and the four merge their (max, sum, O) at the end.
-template <class RG, class F>
+// ONE: the task has a single (token, head) row (G = 1 decode).  Each lane then holds no second
+// real row, and the softmax work of the second accumulator column (masking, maxima, exp2, sums,
+// rescales) is left out; that column's weights are 0, so its accumulators stay 0.
+template <class RG, bool ONE, class F>
 __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
                                  int lane, F first_stage_seen) {
     constexpr int HD = 128;
@@ -232,7 +235,7 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
         return min(lim, t.kv_end);
     };
     const int r0 = 2 * c4, r1 = r0 + 1;  // this lane's query rows (accumulator columns)
-    const int lim0 = row_limit(r0), lim1 = row_limit(r1);
+    const int lim0 = row_limit(r0), lim1 = ONE ? 0 : row_limit(r1);
     int lim_max = max(lim0, lim1);
     lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, 1));
     lim_max = max(lim_max, __shfl_xor_sync(0xffffffffu, lim_max, 2));
@@ -292,24 +295,29 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
                 vmax = fmaxf(vmax, vs[b][h]);
                 const float fk = p.scale_log2 * kx;
                 sc[b][2 * h] = key < lim0 ? sc[b][2 * h] * fk : -INFINITY;
-                sc[b][2 * h + 1] = key < lim1 ? sc[b][2 * h + 1] * fk : -INFINITY;
                 mx0 = fmaxf(mx0, sc[b][2 * h]);
-                mx1 = fmaxf(mx1, sc[b][2 * h + 1]);
+                if constexpr (!ONE) {
+                    sc[b][2 * h + 1] = key < lim1 ? sc[b][2 * h + 1] * fk : -INFINITY;
+                    mx1 = fmaxf(mx1, sc[b][2 * h + 1]);
+                }
             }
         }
         // lazy reference max, as in consume_task; a row's keys lie across the lanes of one column c
         float al0 = 1.f, al1 = 1.f;
-        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || mx1 > m1 + 8.f)) {
+        if (__any_sync(0xffffffffu, mx0 > m0 + 8.f || (!ONE && mx1 > m1 + 8.f))) {
 #pragma unroll
             for (int x = 4; x < 32; x <<= 1) {
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+                if constexpr (!ONE) mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
             }
-            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0, mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+            const float mn0 = mx0 > m0 + 8.f ? mx0 : m0;
             al0 = ex2(m0 - (mn0 == -INFINITY ? 0.f : mn0));
-            al1 = ex2(m1 - (mn1 == -INFINITY ? 0.f : mn1));
             m0 = mn0;
-            m1 = mn1;
+            if constexpr (!ONE) {
+                const float mn1 = mx1 > m1 + 8.f ? mx1 : m1;
+                al1 = ex2(m1 - (mn1 == -INFINITY ? 0.f : mn1));
+                m1 = mn1;
+            }
         }
         const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
         float ps0 = 0.f, ps1 = 0.f;
@@ -318,13 +326,17 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 sc[b][2 * h] = ex2(sc[b][2 * h] - mu0);
-                sc[b][2 * h + 1] = ex2(sc[b][2 * h + 1] - mu1);
                 ps0 += sc[b][2 * h];
-                ps1 += sc[b][2 * h + 1];
+                if constexpr (ONE) {
+                    sc[b][2 * h + 1] = 0.f;
+                } else {
+                    sc[b][2 * h + 1] = ex2(sc[b][2 * h + 1] - mu1);
+                    ps1 += sc[b][2 * h + 1];
+                }
             }
         }
         l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
+        if constexpr (!ONE) l1 = l1 * al1 + ps1;
         bool rescale = al0 != 1.f || al1 != 1.f;
         if (__any_sync(0xffffffffu, vmax > s_max)) {
             // every column c holds the same keys, so the maximum over g is warp-uniform
@@ -332,7 +344,7 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
             for (int x = 4; x < 32; x <<= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, x));
             const float gs = s_max / vmax;
             al0 *= gs;
-            al1 *= gs;
+            if constexpr (!ONE) al1 *= gs;
             s_max = vmax;
             s_inv = 1.f / vmax;
             rescale = true;
@@ -547,10 +559,10 @@ template <int HD, class RG, class F>
 __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem &sm, int &ctr, int &iter, int w,
                              int lane, F first_stage_seen) {
     if constexpr (RG::kFp8) {
-        if constexpr (RG::kOnlyT)
-            return consume_task_f8t<RG>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
-        else if (f.t.q_rows * p.G <= 8)
-            return consume_task_f8t<RG>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
+        if (f.t.q_rows * p.G == 1)
+            return consume_task_f8t<RG, true>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
+        if (RG::kOnlyT || f.t.q_rows * p.G <= 8)
+            return consume_task_f8t<RG, false>(p, f, sm, ctr, iter, w, lane, first_stage_seen);
     }
     const int g4 = lane >> 2, c4 = lane & 3;
     const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;
