@@ -223,10 +223,27 @@ xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t
  * short enough that a few long contexts still spread over the SMs.
  * Errors: XY_ERR_INVALID_ARG (null outputs, Hq not a positive multiple of Hkv).
  */
-#define XY_DEFAULT_KV_CHUNK 8192
+#define XY_DEFAULT_KV_CHUNK 16384
 #define XY_FP8_NARROW_ROWS 16
 xy_status xy_default_tiles(int num_heads_q, int num_heads_kv, int head_dim, int kv_fp8, int pure_decode,
                            int *q_tile, int *kv_chunk);
+
+/*
+ * The KV chunk for one batch (no counterpart in the pages, which do not split a context): among
+ * 8192, 16384, 32768 and 65536 keys, the chunk whose estimated makespan on num_ctas persistent
+ * CTAs is least.  Longer chunks mean fewer tasks, partials and merges; shorter ones let a few long
+ * contexts spread over more SMs.  The estimate counts each (sequence, KV head) pair's L context
+ * keys in ceil(L / chunk) tasks plus a fixed per-task overhead, and takes the larger of a CTA's
+ * average load and the longest-first deal of the full-size chunks; ties go to the longer chunk.
+ * kv_fp8, pure_decode: as for xy_default_tiles (the 8-bit pure-decode kernel with G <= 8 runs two
+ * CTAs per SM slot, so its chunks are sized for twice num_ctas).  Host call, pure.
+ *   context_lens: host int32 [num_seqs] (>= 0).  *kv_chunk receives the chunk (a multiple of
+ *   every page size and of both kernels' KV tiles).
+ * Errors: XY_ERR_INVALID_ARG (null output, negative length, Hq not a positive multiple of Hkv,
+ * num_ctas < 1).
+ */
+xy_status xy_default_kv_chunk(const int32_t *context_lens, int num_seqs, int num_heads_q, int num_heads_kv,
+                              int kv_fp8, int pure_decode, int num_ctas, int *kv_chunk);
 
 xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
                               int num_seqs, int num_heads_q, int num_heads_kv, int head_dim,
@@ -481,7 +498,8 @@ xy_status xy_paged_attention_fp8_dynamic(const void *q, const int32_t *cu_seqlen
  * sequences read (in their order; bf16 copy i holds page list[i]), the tile sequences' block
  * table over those copies (row r: copies 0, 1, ... of tile sequence r, the rest -1), each part's
  * cu_seqlens_q renumbered from 0, and each part's task and merge tables (XY_SCHEDULE_DYNAMIC, the
- * xy_default_tiles policy: bf16 tiles for the tile part, 8-bit decode tasks for the other), and
+ * xy_default_tiles policy: bf16 tiles for the tile part, 8-bit decode tasks for the other, each
+ * part's KV chunk from xy_default_kv_chunk over that part's sequences), and
  * packs them into `staging` at the offsets of *out (multiples of XY_STEP_TABLES_ALIGN) after a
  * zero error word, cu_seqlens_q, context_lens and the block table, so one host->device copy of
  * out->bytes bytes carries every table.  *out also gets the parts' sequence and token ranges,

@@ -26,7 +26,7 @@ C_ABI = ("xy_status_string", "xy_last_error_string", "xy_version", "xy_default_n
          "xy_paged_attention_fp8", "xy_build_step_tables", "xy_dequant_pages_fp8", "xy_paged_attention_dynamic",
          "xy_paged_attention_traced", "xy_paged_attention_fp8_dynamic", "xy_kv_append_paged",
          "xy_kv_append_paged_fp8", "xy_default_tiles", "xy_build_fp8_step_tables",
-         "xy_paged_attention_fp8_mixed")
+         "xy_paged_attention_fp8_mixed", "xy_default_kv_chunk")
 
 # size of the library-owned split-KV scratch used by xy_paged_attention_noalloc
 XY_NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -111,6 +111,8 @@ def lib():
     L.xy_build_task_table.restype = I
     L.xy_default_tiles.argtypes = [I, I, I, I, I, P, P]
     L.xy_default_tiles.restype = I
+    L.xy_default_kv_chunk.argtypes = [P, I, I, I, I, I, I, P]
+    L.xy_default_kv_chunk.restype = I
     L.xy_build_fp8_step_tables.argtypes = [P, P, I, P, I, I, I, I, I, I, I, I, P, SZ, P]
     L.xy_build_fp8_step_tables.restype = I
     L.xy_paged_attention_fp8_mixed.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P, I, P, SZ,
@@ -628,10 +630,21 @@ def check_err_word(err_word):
         raise XYDeviceError(bits)
 
 
+def default_kv_chunk(context_lens, num_heads_q, num_heads_kv, num_ctas, kv_fp8=False, pure_decode=False):
+    """xy_default_kv_chunk: the KV chunk (8192 .. 65536 keys) with the least estimated makespan
+    for this batch's context lengths on num_ctas persistent CTAs."""
+    ctx, pctx = _host_i32(context_lens)
+    ch = ctypes.c_int()
+    _check(lib().xy_default_kv_chunk(pctx, len(ctx), int(num_heads_q), int(num_heads_kv), int(bool(kv_fp8)),
+                                     int(bool(pure_decode)), int(num_ctas), ctypes.byref(ch)), "xy_default_kv_chunk")
+    return ch.value
+
+
 def default_tiles(num_heads_q, num_heads_kv, head_dim=128, kv_fp8=False, pure_decode=False):
     """(q_tile, kv_chunk): the kernels' tile policy for a batch of this shape (xy_default_tiles:
     two 128-row tcgen05 tiles per task where the shape allows, else decode-path task heights; over
-    8-bit pages one token per task for pure decode batches; 8192-key KV chunks)."""
+    8-bit pages one token per task for pure decode batches; 16384-key KV chunks, the shape-only
+    default; default_kv_chunk picks one for a batch's lengths)."""
     qt, ch = ctypes.c_int(), ctypes.c_int()
     _check(lib().xy_default_tiles(int(num_heads_q), int(num_heads_kv), int(head_dim), int(bool(kv_fp8)),
                                   int(bool(pure_decode)), ctypes.byref(qt), ctypes.byref(ch)), "xy_default_tiles")
@@ -650,9 +663,11 @@ class Plan:
         cu = np.asarray(cu_seqlens_q)
         schedule = default_schedule(kv_fp8) if schedule is None else schedule
         self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
-        dq, dk = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8,
-                               pure_decode=len(cu) > 1 and int(cu[-1]) == len(cu) - 1)
-        self.q_tile, self.kv_chunk = q_tile or dq, kv_chunk or dk
+        pure = len(cu) > 1 and int(cu[-1]) == len(cu) - 1
+        dq, _ = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8, pure_decode=pure)
+        self.q_tile = q_tile or dq
+        self.kv_chunk = kv_chunk or default_kv_chunk(context_lens, num_heads_q, num_heads_kv, self.num_ctas, kv_fp8,
+                                                     pure)
         self.schedule = schedule
         # the dynamic deal's claim counter (every launch returns it to zero)
         self.task_counter = torch.zeros(2, dtype=torch.int32, device=dev) if self.dynamic else None

@@ -5,6 +5,7 @@
 // cann-recipes-infer Paged KV Cache / Packed Sequence notes (dpshk.com/news/5336026) §2.2, §3.2.
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -360,6 +361,48 @@ extern "C" xy_status xy_default_tiles(int num_heads_q, int num_heads_kv, int hea
     return XY_OK;
 }
 
+// Batch-aware KV chunk: among 8192, 16384, 32768 and 65536 keys, the chunk whose estimated
+// makespan is least.  Each (sequence, KV head) pair streams its L context keys in ceil(L / c)
+// tasks; a task costs its keys plus a fixed overhead (task set-up, the cross-warp merge, a split
+// partial), and the estimate is the larger of the average load of a CTA and what the full-size
+// chunks alone need when dealt longest first (ceil(full / CTAs) of them on the busiest CTA).  Ties
+// go to the longer chunk (fewer partials to merge).  The 8-bit pure-decode kernel with G <= 8 runs
+// two CTAs per SM slot (xy_paged_attention_fp8_dynamic), so its chunks are sized for twice the CTAs.
+extern "C" xy_status xy_default_kv_chunk(const int32_t *context_lens, int num_seqs, int num_heads_q,
+                                         int num_heads_kv, int kv_fp8, int pure_decode, int num_ctas,
+                                         int *kv_chunk) {
+    if (!kv_chunk || num_seqs < 0 || (num_seqs > 0 && !context_lens) || num_heads_kv < 1 ||
+        num_heads_q < num_heads_kv || num_heads_q % num_heads_kv || num_ctas < 1)
+        return XY_ERR_INVALID_ARG;
+    const int G = num_heads_q / num_heads_kv;
+    const double ctas = (double)num_ctas * (kv_fp8 && pure_decode && G <= 8 ? 2 : 1);
+    constexpr double kTaskOverheadKeys = 512.0;
+    int best = XY_DEFAULT_KV_CHUNK;
+    double best_t = -1.0;
+    for (int c = 8192; c <= 65536; c *= 2) {
+        double keys = 0.0, tasks = 0.0, full = 0.0;
+        int longest = 0;
+        for (int i = 0; i < num_seqs; ++i) {
+            const int L = context_lens[i];
+            if (L < 0) return XY_ERR_INVALID_ARG;
+            keys += L;
+            tasks += (L + c - 1) / c;
+            full += L / c;
+            longest = L > longest ? L : longest;
+        }
+        keys *= num_heads_kv, tasks *= num_heads_kv, full *= num_heads_kv;
+        const double avg = (keys + kTaskOverheadKeys * tasks) / ctas;
+        const double rounds = std::ceil(full / ctas) * ((double)c + kTaskOverheadKeys);
+        const double t = std::max(std::max(avg, rounds), (double)std::min(c, longest) + kTaskOverheadKeys);
+        if (best_t < 0.0 || t <= best_t) {
+            best_t = t;
+            best = c;
+        }
+    }
+    *kv_chunk = best;
+    return XY_OK;
+}
+
 extern "C" xy_status xy_build_task_table(const int32_t *cu_seqlens_q, const int32_t *context_lens,
                                          int num_seqs, int num_heads_q, int num_heads_kv,
                                          int head_dim, int causal, int num_ctas, int q_tile,
@@ -486,6 +529,9 @@ extern "C" xy_status xy_build_fp8_step_tables(const int32_t *cu_seqlens_q, const
         for (int i = a; i <= b; ++i) g_cu_part[(size_t)(i - a)] = cu_seqlens_q[i] - cu_seqlens_q[a];
         int q_tile = 0, kv_chunk = 0;
         xy_status st = xy_default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8, kv_fp8, &q_tile, &kv_chunk);
+        if (st != XY_OK) return st;
+        st = xy_default_kv_chunk(context_lens + a, b - a, num_heads_q, num_heads_kv, kv_fp8, kv_fp8, num_ctas,
+                                 &kv_chunk);
         if (st != XY_OK) return st;
         int64_t ws_rows = 0;
         st = build_tasks(g_cu_part.data(), context_lens + a, b - a, num_heads_q, num_heads_kv, head_dim, causal,

@@ -4,7 +4,7 @@ KV append and paged attention (device).  Composition of libxy calls only; no ari
 import numpy as np
 import torch
 
-from . import (XY_SCHEDULE_DYNAMIC, Plan, check_err_word, default_schedule, default_tiles,
+from . import (XY_SCHEDULE_DYNAMIC, Plan, check_err_word, default_kv_chunk, default_schedule, default_tiles,
                xy_build_block_table, xy_build_step_tables, xy_default_num_ctas, xy_kv_append_paged,
                xy_kv_append_paged_fp8, xy_paged_attention, xy_paged_attention_dynamic, xy_paged_attention_fp8,
                xy_paged_attention_fp8_dynamic)
@@ -116,6 +116,8 @@ class Planner:
         schedule = default_schedule(kv_fp8) if schedule is None else schedule
         self.dynamic = schedule == XY_SCHEDULE_DYNAMIC
         tiles = default_tiles(num_heads_q, num_heads_kv, head_dim, kv_fp8)
+        # the KV chunk per batch (default_kv_chunk of its lengths) unless one is given
+        self._kv_chunk_arg = kv_chunk
         self.kv_chunk = kv_chunk or tiles[1]
         self.q_tile, self.schedule = q_tile or tiles[0], schedule
         # the dynamic deal's claim counter (every launch returns it to zero)
@@ -160,9 +162,12 @@ class Planner:
         prefix cache whose rows share pages, say) that replaces the FIFO table before the upload."""
         self._ensure(1 << 16)
         self._wait_upload()   # the staging buffer is written below
+        T = int(cu_seqlens_q[-1])
+        pure = T == len(context_lens)
         if self.kv_fp8 and self._q_tile_arg is None:
-            T = int(cu_seqlens_q[-1])
-            self.q_tile = default_tiles(self.Hq, self.Hkv, self.d, True, pure_decode=T == len(context_lens))[0]
+            self.q_tile = default_tiles(self.Hq, self.Hkv, self.d, True, pure_decode=pure)[0]
+        if self._kv_chunk_arg is None:
+            self.kv_chunk = default_kv_chunk(context_lens, self.Hq, self.Hkv, self.num_ctas, self.kv_fp8, pure)
         for _ in range(2):
             st, tbl = xy_build_step_tables(cu_seqlens_q, context_lens, free_list, self.block_size, self.max_blocks,
                                            self.Hq, self.Hkv, self.d, self.causal, self.num_ctas, self.q_tile,

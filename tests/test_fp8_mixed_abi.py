@@ -72,7 +72,8 @@ def test_builder_tables_compose_the_host_calls(xy, q_lens, ctx):
         a, b = idx[0], idx[-1] + 1
         sub_cu = (cu[a:b + 1] - cu[a]).astype(np.int32)
         assert np.array_equal(_i32(staging, off_cu, b - a + 1), sub_cu)
-        qt, ch = xy.default_tiles(8, 2, 128, kv_fp8=fp8, pure_decode=fp8)
+        qt, _ = xy.default_tiles(8, 2, 128, kv_fp8=fp8, pure_decode=fp8)
+        ch = xy.default_kv_chunk(L[a:b], 8, 2, 37, kv_fp8=fp8, pure_decode=fp8)
         r = xy.xy_build_task_table(sub_cu, L[a:b], 8, 2, 128, True, 37, qt, ch, xy.XY_SCHEDULE_DYNAMIC)
         assert np.array_equal(_i32(staging, off_t, 8 * nt).reshape(nt, 8), r["tasks"])
         assert np.array_equal(_i32(staging, off_m, 8 * nm).reshape(nm, 8), r["merges"])

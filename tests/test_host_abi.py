@@ -187,3 +187,26 @@ def test_step_tables_pack_both_builders_outputs():
     assert np.array_equal(i32(tbl.merges_off, 8 * tbl.num_merges).reshape(-1, 8), ref["merges"])
     assert tbl.workspace_bytes == ref["workspace_bytes"] and tbl.stats.balance == ref["stats"]["balance"]
     assert tbl.bytes == tbl.merges_off + 32 * tbl.num_merges
+
+
+def test_default_kv_chunk_policy(xy):
+    # the chunk with the least estimated makespan: four contexts of 128K keys beside many short
+    # ones split into 32768-key tasks on 152 CTAs, 16384 on the 8-bit pure-decode kernel's twice as
+    # many CTAs; a single 1M-key context into 8192-key tasks (256 longer tasks would leave a second
+    # round on some CTAs); contexts that no candidate splits take the longest chunk
+    skew = workloads.make("skew")
+    assert xy.default_kv_chunk(skew.context_lens, 64, 8, 152) == 32768
+    assert xy.default_kv_chunk(skew.context_lens, 64, 8, 152, kv_fp8=True, pure_decode=True) == 16384
+    assert xy.default_kv_chunk([1 << 20], 8, 8, 152) == 8192
+    assert xy.default_kv_chunk([100, 4096, 8000], 32, 8, 152) == 65536
+    assert xy.default_kv_chunk([], 32, 8, 152) == 65536
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        ctx = rng.integers(0, 300000, size=int(rng.integers(1, 40)))
+        c = xy.default_kv_chunk(ctx, 8, 8, int(rng.integers(1, 300)), kv_fp8=bool(rng.integers(2)))
+        assert c in (8192, 16384, 32768, 65536) and c % 256 == 0
+    for bad in (dict(context_lens=[-1]), dict(num_ctas=0), dict(num_heads_q=6, num_heads_kv=4)):
+        args = dict(context_lens=[10], num_heads_q=8, num_heads_kv=8, num_ctas=152)
+        args.update(bad)
+        with pytest.raises(xy.XYError):
+            xy.default_kv_chunk(**args)
