@@ -84,6 +84,7 @@ struct Cfg {
 template <int HD, int KIND, bool DYN>
 __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DYN>::kMinBlocks)
     paged_attention_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                           const __grid_constant__ CUtensorMap ksmap, const __grid_constant__ CUtensorMap vsmap,
                            const AttnParams p) {
     using C = Cfg<HD, KIND, DYN>;
     using RG = typename C::RG;
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DY
             const int first_win = DYN ? tc.win : pref_win;
             pref_valid = false;
             ok = xy::dec::produce_task<HD, RG>(
-                p, f, &kmap, &vmap, sm, ctr, lane, first_win, have_first,
+                p, f, &kmap, &vmap, &ksmap, &vsmap, sm, ctr, lane, first_win, have_first,
                 [&]() {
                     // the next record has arrived by now: prefetch its numbers and first window
                     tc.prefetch_next(p);
@@ -365,11 +366,27 @@ bool make_pool_map_u8(CUtensorMap *map, const void *pool, int64_t rows, int box_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over an 8-bit pool's scale array viewed as [pages * Hkv rows, bs floats]: a box is one
+// (page, head) row of bs scales, one row high, for TMA gathers of four pages' rows at a time.
+bool make_scale_map(CUtensorMap *map, const float *scales, int64_t rows, int block_size) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const int box = block_size < 256 ? block_size : 256;   // (a box dimension is at most 256)
+    cuuint64_t dims[2] = {(cuuint64_t)block_size, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)block_size * 4u};
+    cuuint32_t bx[2] = {(cuuint32_t)box, 1u};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(scales), dims, strides, bx, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ksm / vsm: the 8-bit pages' scale maps (any valid map for bf16 pages, which do not read them)
 template <int HD, int KIND, bool DYN>
-xy_status launch_attention_kernel(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
-                                  cudaStream_t st) {
+xy_status launch_attention_kernel(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm,
+                                  const CUtensorMap &ksm, const CUtensorMap &vsm, int num_ctas, cudaStream_t st) {
     using C = Cfg<HD, KIND, DYN>;
     static xy::PerDeviceOnce configured;  // the attribute is per device
     int dev = 0;
@@ -381,16 +398,16 @@ xy_status launch_attention_kernel(const AttnParams &p, const CUtensorMap &km, co
         configured.mark(dev);
     }
     const cudaError_t e = xy::launch_dependent(paged_attention_kernel<HD, KIND, DYN>, dim3(num_ctas),
-                                               dim3(C::kThreads), C::kSmemBytes, st, km, vm, p);
+                                               dim3(C::kThreads), C::kSmemBytes, st, km, vm, ksm, vsm, p);
     return e == cudaSuccess ? XY_OK : xy::cuda_fail(e, "paged_attention_kernel launch");
 }
 
 template <int HD, int KIND>
-xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, int num_ctas,
-                 const xy_merge *merges, int num_merges, cudaStream_t st) {
+xy_status launch(const AttnParams &p, const CUtensorMap &km, const CUtensorMap &vm, const CUtensorMap &ksm,
+                 const CUtensorMap &vsm, int num_ctas, const xy_merge *merges, int num_merges, cudaStream_t st) {
     if (p.num_tasks > 0) {
-        const xy_status ks = p.dyn ? launch_attention_kernel<HD, KIND, true>(p, km, vm, num_ctas, st)
-                                   : launch_attention_kernel<HD, KIND, false>(p, km, vm, num_ctas, st);
+        const xy_status ks = p.dyn ? launch_attention_kernel<HD, KIND, true>(p, km, vm, ksm, vsm, num_ctas, st)
+                                   : launch_attention_kernel<HD, KIND, false>(p, km, vm, ksm, vsm, num_ctas, st);
         if (ks != XY_OK) return ks;
     }
     if (num_merges > 0) {
@@ -510,8 +527,8 @@ xy_status attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *c
         }
         p.num_tasks = 0;  // ... so only the split-KV merge remains
     }
-    return head_dim == 128 ? launch<128, kBf16>(p, km, vm, num_ctas, merges, num_merges, st)
-                           : launch<64, kBf16>(p, km, vm, num_ctas, merges, num_merges, st);
+    return head_dim == 128 ? launch<128, kBf16>(p, km, vm, km, vm, num_ctas, merges, num_merges, st)
+                           : launch<64, kBf16>(p, km, vm, km, vm, num_ctas, merges, num_merges, st);
 }
 
 }  // namespace
@@ -559,13 +576,18 @@ xy_status attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_
     CUtensorMap km, vm;
     if (!make_pool_map_u8(&km, k_pages, rows, box_rows) || !make_pool_map_u8(&vm, v_pages, rows, box_rows))
         return XY_ERR_CUDA;
+    CUtensorMap ksm, vsm;
+    if (!make_scale_map(&ksm, k_scales, (int64_t)num_pages * num_heads_kv, block_size) ||
+        !make_scale_map(&vsm, v_scales, (int64_t)num_pages * num_heads_kv, block_size))
+        return XY_ERR_CUDA;
     // every task runs on the decode path (f16 MMAs on converted codes)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool narrow = num_tokens == num_seqs && p.G <= XY_FP8_NARROW_ROWS;
     // pure decode with G <= 8 under the dynamic deal: two half-size CTAs per SM slot
-    if (narrow && p.G <= 8 && p.dyn) return launch<128, kFp8Tiny>(p, km, vm, 2 * num_ctas, merges, num_merges, st);
-    return narrow ? launch<128, kFp8Narrow>(p, km, vm, num_ctas, merges, num_merges, st)
-                  : launch<128, kFp8Wide>(p, km, vm, num_ctas, merges, num_merges, st);
+    if (narrow && p.G <= 8 && p.dyn)
+        return launch<128, kFp8Tiny>(p, km, vm, ksm, vsm, 2 * num_ctas, merges, num_merges, st);
+    return narrow ? launch<128, kFp8Narrow>(p, km, vm, ksm, vsm, num_ctas, merges, num_merges, st)
+                  : launch<128, kFp8Wide>(p, km, vm, ksm, vsm, num_ctas, merges, num_merges, st);
 }
 }  // namespace
 

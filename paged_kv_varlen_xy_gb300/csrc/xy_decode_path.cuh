@@ -122,10 +122,13 @@ __device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) 
 // `pg_first` is the task's first block-table window if it was prefetched (else -1 with
 // have_first false).  `first_stage_done()` runs once, right after this warp's first stage of the
 // task is issued (the caller prefetches the next task there).  Returns false if a wait gave up.
+// 8-bit pages: ksmap / vsmap view the K and V scale arrays as [pages * Hkv rows, bs floats] with a
+// one-row box; with pages of at most 32 tokens a stage's scales come four pages per copy (TMA
+// gather4) instead of one bulk copy per page and tensor (null for bf16 pages).
 template <int HD, class RG, class F>
 __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUtensorMap *kmap, const CUtensorMap *vmap,
-                             const Smem &sm, int &ctr, int lane, int pg_first, bool have_first, F first_stage_done,
-                             int pw = 0, int npw = 1) {
+                             const CUtensorMap *ksmap, const CUtensorMap *vsmap, const Smem &sm, int &ctr, int lane,
+                             int pg_first, bool have_first, F first_stage_done, int pw = 0, int npw = 1) {
     const xy_task &t = f.t;
     const int bs_sh = 31 - __clz(p.bs);                   // page size is a power of two
     const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;  // keys per TMA box
@@ -151,7 +154,11 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
             pg_nxt = load_window(p, t.seq, win0 + 32, lane);
         }
         // one box per (page, tensor), both column halves; 8-bit pages add each box's K and V scales
-        const int n_copies = nbox * (RG::kFp8 ? 4 : 2);
+        // (one bulk copy per page and tensor, or for pages of at most 32 tokens one gather of four
+        // pages' scale rows per tensor)
+        const bool gather = RG::kFp8 && BR <= 32;
+        const int ngather = (nbox + 3) >> 2;
+        const int n_copies = nbox * (RG::kFp8 && !gather ? 4 : 2);
         const int b = lane % nbox;
         int my_pg = __shfl_sync(0xffffffffu, pg_win, ((kv0 + (b << br_sh)) >> bs_sh) - win0);
         if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
@@ -163,7 +170,8 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
         const uint32_t q_bytes = q_here ? (uint32_t)t.q_rows * row_bytes : 0u;
         const uint32_t stage = sm.stages + s * RG::kStageBytes;
         const uint32_t kv_bytes =
-            RG::kFp8 ? (uint32_t)(nbox * BR * (2 * 128 + 2 * 4)) : (uint32_t)(n_copies * RG::kHalves * BR * 128);
+            RG::kFp8 ? (uint32_t)(nbox * BR * 2 * 128 + (gather ? ngather * 4 : nbox) * BR * 2 * 4)
+                     : (uint32_t)(n_copies * RG::kHalves * BR * 128);
         if (lane == 0) mbar_arrive_expect_tx(sm.full_bar + 8 * s, kv_bytes + q_bytes);
         __syncwarp();
         if (lane < n_copies) {
@@ -182,6 +190,22 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
             } else {
                 const uint32_t dst = stage + tensor * RG::kTensorBytes + b * RG::kHalves * BR * 128;
                 tma_load_3d(dst, tensor ? vmap : kmap, 0, y, 0, sm.full_bar + 8 * s);
+            }
+        }
+        if constexpr (RG::kFp8) {
+            if (gather) {
+                // scale rows (page * Hkv + head) of boxes 4g .. 4g + 3; a group past the stage's last
+                // page repeats that page's row (the extra rows land in unused scale slots of the stage)
+                const int srow = my_pg * p.Hkv + t.kv_head;   // box `lane % nbox`'s row
+                for (int g = 0; g < ngather; ++g) {
+                    int r[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) r[i] = __shfl_sync(0xffffffffu, srow, min(4 * g + i, nbox - 1));
+                    if (lane < 2) {
+                        const uint32_t dst = stage + RG::kScaleOff + lane * RG::kKeys * 4 + g * 4 * BR * 4;
+                        tma_gather4(dst, lane ? vsmap : ksmap, 0, r[0], r[1], r[2], r[3], sm.full_bar + 8 * s);
+                    }
+                }
             }
         }
         if (q_here) {

@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool have_first = DYN || pref_valid;
                 const int first_win = DYN ? tc.win : pref_win;
                 pref_valid = false;
-                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, dsm, dctr, lane, first_win, have_first,
+                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, nullptr, nullptr, dsm, dctr, lane, first_win, have_first,
                                                         [&]() {
                                                             tc.prefetch_next(p);
                                                             if (tc.have_next) {
@@ -518,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int first_win = DYN ? tc.win : pref_win;
             pref_valid = false;
             ok = xy::dec::produce_task<HD, DecRing>(
-                p, f, &kmap_d, &vmap_d, dsm, dctr, lane, first_win, have_first,
+                p, f, &kmap_d, &vmap_d, nullptr, nullptr, dsm, dctr, lane, first_win, have_first,
                 [&]() {
                     tc.prefetch_next(p);
                     if (tc.have_next) {

@@ -313,3 +313,42 @@ def test_repeated_launches_bit_identical(config, launches):
     xystep.check(batch)
     assert not differ, f"launches {differ} differ from the first"
     assert torch.equal(outs[(launches - 1) & 1].view(torch.int16), ref)
+
+
+@pytest.mark.parametrize("G,kv_chunk", [(4, None), (4, 256), (8, 384), (2, None)])
+def test_single_query_tile_tasks_every_row(G, kv_chunk):
+    # tile tasks of at most 128 rows (one query tile, group B idle) over two or more K/V tiles:
+    # whole 128-row tiles (the TMA store epilogue), partial ones, odd and even tile counts, ragged
+    # ends, split partials
+    rng = np.random.default_rng(90 + G)
+    qt = 128 // G
+    q = [qt, qt - 3, 5, qt, 9, qt // 2, qt]
+    ctx = [qi + int(rng.integers(130, 1500)) for qi in q]
+    ctx[0] = q[0] + 256   # an even number of 128-key tiles from the start
+    ctx[3] = q[3] + 383
+    wl = workloads.custom(q, ctx, 2 * G, 2, 128, 16, True, seed=70 + G, name="paired")
+    assert_parity(run(wl, q_tile=qt, kv_chunk=kv_chunk, schedule=4))
+    assert_parity(run(wl, q_tile=qt, kv_chunk=kv_chunk, schedule=3))
+
+
+def test_single_query_tile_tasks_sharp_score_growth_and_nan_pool():
+    # the lazy rescale of one-tile tasks whose row maxima jump between K/V tiles; stale NaN rows
+    # past kv_end never reach the outputs
+    G = 4
+    q = [32, 20, 32]
+    ctx = [32 + 700, 20 + 300, 32 + 1000]
+    wl = workloads.custom(q, ctx, 8, 2, 128, 16, True, seed=81, name="paired_sharp")
+
+    def grow(vals):
+        # pages scaled by powers of two in random page order, as in the sharp-growth test above
+        g = torch.Generator().manual_seed(6)
+        f = torch.tensor([1.0, 4.0, 16.0, 64.0])[torch.randint(0, 4, (vals["k_pool"].shape[0],), generator=g)]
+        vals["k_pool"].mul_(f.to(vals["k_pool"].device, torch.bfloat16).view(-1, 1, 1, 1))
+        vals["k_new"].mul_(64.0)
+
+    assert_parity(run(wl, q_tile=32, schedule=4, transform=grow))
+    # the whole pool starts as NaN and every context token is appended (q = L), so only slots past
+    # each context end stay NaN; 32-token query tiles past the first 96 tokens span two or more
+    # K/V tiles
+    wl = workloads.custom([300, 200, 150], [300, 200, 150], 8, 2, 128, 16, True, seed=82, name="paired_nan")
+    assert_parity(run(wl, q_tile=32, schedule=4, pool_fill=float("nan")), check_pages=False)
