@@ -218,9 +218,10 @@ xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t
  * 256/G tokens (two 128-row tcgen05 tiles sharing each K/V tile); otherwise 64/G tokens (at least
  * 1), the decode path's task height.  Over 8-bit pages (kv_fp8) every task runs on the decode
  * path: one token per task when pure_decode (one new token per sequence) and G <=
- * XY_FP8_NARROW_ROWS, else 64/G tokens.  kv_chunk is XY_DEFAULT_KV_CHUNK keys: a multiple of every
- * page size and of both kernels' KV tiles, long enough that split partials and merges stay few,
- * short enough that a few long contexts still spread over the SMs.
+ * XY_FP8_NARROW_ROWS, else 64/G tokens.  kv_chunk is XY_DEFAULT_KV_CHUNK keys, the shape-only
+ * default: a multiple of every page size and of both kernels' KV tiles, long enough that split
+ * partials and merges stay few, short enough that a few long contexts still spread over the SMs;
+ * xy_default_kv_chunk picks one for a batch's context lengths.
  * Errors: XY_ERR_INVALID_ARG (null outputs, Hq not a positive multiple of Hkv).
  */
 #define XY_DEFAULT_KV_CHUNK 16384
