@@ -446,8 +446,11 @@ def measure(config, args, dev, pk, world, rank, cpu_budget, smi):
     if fp8:
         # the 8-bit pool: every bf16 pool row appended (quantized) once, before any timing
         Pp, Hkv, bs, d = vals["k_pool"].shape
+        # K and V codes in one allocation, V after K: the attention brings a page's K and V codes
+        # with one copy (separate allocations work too, with a copy per page and pool)
+        codes = torch.empty(2, Pp, Hkv, bs, d, dtype=torch.uint8, device=dev)
+        vals["k_codes"], vals["v_codes"] = codes[0], codes[1]
         for name in ("k", "v"):
-            vals[name + "_codes"] = torch.empty(Pp, Hkv, bs, d, dtype=torch.uint8, device=dev)
             vals[name + "_scales"] = torch.empty(Pp, Hkv, bs, dtype=torch.float32, device=dev)
         rows = {n: vals[n + "_pool"].permute(0, 2, 1, 3).reshape(Pp * bs, Hkv, d).contiguous() for n in ("k", "v")}
         xy.xy_kv_append_fp8(rows["k"], rows["v"], torch.arange(Pp * bs, dtype=torch.int64, device=dev),

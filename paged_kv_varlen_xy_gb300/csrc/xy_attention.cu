@@ -366,6 +366,21 @@ bool make_pool_map_u8(CUtensorMap *map, const void *pool, int64_t rows, int box_
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over K and V 8-bit pools in one allocation, the V pool kv_gap bytes after the K pool:
+// (128 bytes, rows, K|V); a box (128, box_rows, 2) lands as [K rows][V rows], each [box_rows][128 B]
+// with the 128-byte swizzle.
+bool make_pool_map_u8_kv(CUtensorMap *map, const void *k_pool, int64_t rows, int box_rows, uint64_t kv_gap) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128u, (cuuint64_t)rows, 2u};
+    cuuint64_t strides[2] = {128u, (cuuint64_t)kv_gap};
+    cuuint32_t box[3] = {128u, (cuuint32_t)box_rows, 2u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(k_pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D map over an 8-bit pool's scale array viewed as [pages * Hkv rows, bs floats]: a box is one
 // (page, head) row of bs scales, one row high, for TMA gathers of four pages' rows at a time.
 bool make_scale_map(CUtensorMap *map, const float *scales, int64_t rows, int block_size) {
@@ -468,6 +483,7 @@ xy_status make_params(const void *q, const int32_t *cu_seqlens_q, const int32_t 
     p.vsc = nullptr;
     p.dyn = nullptr;
     p.trace = nullptr;
+    p.kv3d = 0;
     p.MB = max_blocks;
     p.P = num_pages;
     p.S = num_seqs;
@@ -574,8 +590,18 @@ xy_status attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_
     static_assert(Cfg<128, kFp8Wide>::RG::kKeys == Cfg<128, kFp8Narrow>::RG::kKeys, "one box height");
     const int box_rows = block_size < keys ? block_size : keys;
     CUtensorMap km, vm;
-    if (!make_pool_map_u8(&km, k_pages, rows, box_rows) || !make_pool_map_u8(&vm, v_pages, rows, box_rows))
+    // V codes at a fixed distance after the K codes in one allocation (16-byte multiple, past the K
+    // pool): one 3-D map over both, whose box brings a page's K and V codes in one copy
+    const uintptr_t kva = reinterpret_cast<uintptr_t>(k_pages), vva = reinterpret_cast<uintptr_t>(v_pages);
+    const uint64_t kv_gap = vva > kva ? (uint64_t)(vva - kva) : 0;
+    const bool kv3d = kv_gap >= (uint64_t)rows * 128u && kv_gap % 16 == 0 && kv_gap < (1ull << 40);
+    if (kv3d) {
+        if (!make_pool_map_u8_kv(&km, k_pages, rows, box_rows, kv_gap)) return XY_ERR_CUDA;
+        vm = km;
+        p.kv3d = 1;
+    } else if (!make_pool_map_u8(&km, k_pages, rows, box_rows) || !make_pool_map_u8(&vm, v_pages, rows, box_rows)) {
         return XY_ERR_CUDA;
+    }
     CUtensorMap ksm, vsm;
     if (!make_scale_map(&ksm, k_scales, (int64_t)num_pages * num_heads_kv, block_size) ||
         !make_scale_map(&vsm, v_scales, (int64_t)num_pages * num_heads_kv, block_size))

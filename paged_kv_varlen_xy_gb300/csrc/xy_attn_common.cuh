@@ -28,6 +28,7 @@ struct AttnParams {
     unsigned long long *trace;  // per-CTA record {start ns, end ns, tasks run, rows x keys} (null: off)
     int64_t ws_rows;
     int MB, P, S, T, Hq, Hkv, G, bs, causal, num_tasks;
+    int kv3d;          // 8-bit pages: K and V codes in one allocation, one 3-D map (kmap) fetches both
     float scale_log2;
 };
 

@@ -80,10 +80,14 @@ struct RingF8 {
     static_assert(KEYS % (32 * kMathWarps) == 0, "32 keys per math warp and step");
 };
 
-// Byte offset of 16-byte chunk `chunk` of key `key` in an 8-bit stage tensor: boxes of BR keys
-// are contiguous [BR][128 B] (so key k's row starts at k * 128) with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t swz8(int key, int chunk) {
-    return (uint32_t)(key * 128 + ((chunk ^ (key & 7)) << 4));
+// Byte offset, from the stage start, of 16-byte chunk `chunk` of key `key`'s K (kv = 0) or V
+// (kv = 1) codes in an 8-bit stage.  The stage holds its keys in boxes of BR = 2^br_sh keys (one
+// per page, or per 128 keys of a longer page), each box as [K rows][V rows] of [BR][128 B] with the
+// 128-byte swizzle: so one copy can bring a page's K and V codes when the two pools share one
+// allocation (a 3-D tensor map), and two copies land in the same places when they do not.
+__device__ __forceinline__ uint32_t swz8kv(int kv, int key, int chunk, int br_sh) {
+    return (uint32_t)(((((key >> br_sh) << 1) | kv) << (br_sh + 7)) + ((key & ((1 << br_sh) - 1)) << 7) +
+                      ((chunk ^ (key & 7)) << 4));
 }
 
 // Shared-memory handles of the decode path, set up by the hosting kernel.
@@ -158,7 +162,9 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
         // pages' scale rows per tensor)
         const bool gather = RG::kFp8 && BR <= 32;
         const int ngather = (nbox + 3) >> 2;
-        const int n_copies = nbox * (RG::kFp8 && !gather ? 4 : 2);
+        // 8-bit pools in one allocation (p.kv3d): one 3-D box brings a page's K and V codes
+        const int n_code = RG::kFp8 && p.kv3d ? nbox : 2 * nbox;
+        const int n_copies = RG::kFp8 ? n_code + (gather ? 0 : 2 * nbox) : 2 * nbox;
         const int b = lane % nbox;
         int my_pg = __shfl_sync(0xffffffffu, pg_win, ((kv0 + (b << br_sh)) >> bs_sh) - win0);
         if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
@@ -179,13 +185,21 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
             const int key = kv0 + (b << br_sh);
             const int y = ((my_pg * p.Hkv + t.kv_head) << bs_sh) + (key & (p.bs - 1));
             if constexpr (RG::kFp8) {
-                if (tensor < 2) {
-                    tma_load_2d(stage + tensor * RG::kTensorBytes + b * BR * 128, tensor ? vmap : kmap, 0, y,
-                                sm.full_bar + 8 * s);
+                // lane groups of nbox: the codes (one 3-D box per page, or a K box and a V box),
+                // then the scales (K, V) when they are not gathered; box b's codes land as
+                // [K rows][V rows] (swz8kv)
+                const int code_groups = p.kv3d ? 1 : 2;
+                if (tensor < code_groups) {
+                    if (p.kv3d)
+                        tma_load_3d(stage + (b << (br_sh + 8)), kmap, 0, y, 0, sm.full_bar + 8 * s);
+                    else
+                        tma_load_2d(stage + (((b << 1) | tensor) << (br_sh + 7)), tensor ? vmap : kmap, 0, y,
+                                    sm.full_bar + 8 * s);
                 } else {
-                    const float *src = (tensor == 2 ? p.ksc : p.vsc) + y;  // the box's BR scales
-                    bulk_load(stage + RG::kScaleOff + (tensor - 2) * RG::kKeys * 4 + b * BR * 4, src,
-                              (uint32_t)BR * 4, sm.full_bar + 8 * s);
+                    const int st = tensor - code_groups;                    // 0: K scales, 1: V scales
+                    const float *src = (st ? p.vsc : p.ksc) + y;           // the box's BR scales
+                    bulk_load(stage + RG::kScaleOff + st * RG::kKeys * 4 + b * BR * 4, src, (uint32_t)BR * 4,
+                              sm.full_bar + 8 * s);
                 }
             } else {
                 const uint32_t dst = stage + tensor * RG::kTensorBytes + b * RG::kHalves * BR * 128;
@@ -250,6 +264,7 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
     constexpr int HD = 128;
     static_assert(RG::kKeys == 32 * kMathWarps, "32 keys per math warp and stage");
     const int g4 = lane >> 2, c4 = lane & 3;
+    const int br_sh = 31 - __clz(p.bs < RG::kKeys ? p.bs : RG::kKeys);   // keys per stage box
     const xy_task t = f.t;
     const int R = t.q_rows * p.G;  // at most 8
     const int qn = f.qn, L = f.L;
@@ -290,7 +305,7 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
                 // its key, i.e. the A fragment (rows = keys) of one k-step in Q's k-order
                 const int krow = kr + 16 * b + ((mi & 1) << 3) + (lane & 7);
                 uint32_t r[4], lo[4], hi[4];
-                ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+                ldsm_x4(kst + swz8kv(0, krow, 2 * cc + (mi >> 1), br_sh), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(r[i], lo[i], hi[i]);
                 const uint32_t a0[4] = {lo[0], lo[1], hi[0], hi[1]};
@@ -409,7 +424,7 @@ __device__ bool consume_task_f8t(const AttnParams &p, const TaskInfo &f, const S
 #pragma unroll
             for (int cc = 0; cc < HD / 32; ++cc) {
                 uint32_t r[4], ev[4], od[4];
-                ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+                ldsm_x4_t(kst + swz8kv(1, vrow, 2 * cc + (mi >> 1), br_sh), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     // bytes (k0 c0, k0 c1, k1 c0, k1 c1) regrouped as (k0 c0, k1 c0, k0 c1, k1 c1)
@@ -643,7 +658,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
             for (int b = 0; b < 2; ++b) {
                 const int krow = kr + 16 * b + ((mi & 1) << 3) + (lane & 7);
                 uint32_t r[4];
-                ldsm_x4(kst + swz8(krow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+                ldsm_x4(kst + swz8kv(0, krow, 2 * cc + (mi >> 1), br_sh), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     uint32_t b0, b1;
@@ -759,7 +774,7 @@ __device__ bool consume_task(const AttnParams &p, const TaskInfo &f, const Smem 
 #pragma unroll
             for (int cc = 0; cc < HD / 32; ++cc) {
                 uint32_t r[4];
-                ldsm_x4_t(vst + swz8(vrow, 2 * cc + (mi >> 1)), r[0], r[1], r[2], r[3]);
+                ldsm_x4_t(kst + swz8kv(1, vrow, 2 * cc + (mi >> 1), br_sh), r[0], r[1], r[2], r[3]);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     // bytes (k0 c0, k0 c1, k1 c0, k1 c1) regrouped as (k0 c0, k1 c0, k0 c1, k1 c1)

@@ -51,9 +51,12 @@ def test_append_fp8_bit_exact(d):
 GREEDY, DYN = 3, 4
 
 
-def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False, schedule=None, num_ctas=None):
+def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False, schedule=None, num_ctas=None, layout="separate"):
     """One step over 8-bit pages on the GPU and in the oracle, on workload wl's bf16 values
-    (optionally with each pool / new row multiplied by a power of two from row_scale)."""
+    (optionally with each pool / new row multiplied by a power of two from row_scale).
+    layout: the code pools as two allocations ("separate"), as one allocation with V after K
+    ("one": the attention fetches a page's K and V codes with one 3-D copy), or as one allocation
+    with V before K ("v_first": two copies per page)."""
     import paged_kv_varlen_xy_gb300 as xy
     from paged_kv_varlen_xy_gb300 import build
     from paged_kv_varlen_xy_gb300 import step as xystep
@@ -68,7 +71,11 @@ def _run_fp8(wl, kv_chunk=None, row_scale=None, split=False, schedule=None, num_
             vals[name] = (vals[name].float() * f).to(torch.bfloat16)
     P, Hkv, bs, d = vals["k_pool"].shape
     err = torch.zeros(1, dtype=torch.int32, device=dev)
-    codes = {n: torch.zeros(P, Hkv, bs, d, dtype=torch.uint8, device=dev) for n in ("k", "v")}
+    if layout == "separate":
+        codes = {n: torch.zeros(P, Hkv, bs, d, dtype=torch.uint8, device=dev) for n in ("k", "v")}
+    else:
+        both = torch.zeros(2, P, Hkv, bs, d, dtype=torch.uint8, device=dev)
+        codes = {"k": both[0], "v": both[1]} if layout == "one" else {"k": both[1], "v": both[0]}
     scl = {n: torch.zeros(P, Hkv, bs, dtype=torch.float32, device=dev) for n in ("k", "v")}
     slots_all = torch.arange(P * bs, dtype=torch.int64, device=dev)
     krows = vals["k_pool"].permute(0, 2, 1, 3).reshape(P * bs, Hkv, d).contiguous().to(dev)
@@ -290,3 +297,21 @@ def test_fp8_split_tile_and_decode_parts(q_lens, ctx):
     wl = workloads.custom(q_lens, ctx, 16, 4, 128, 16, True, seed=71)
     r = _run_fp8(wl, split=True)
     _assert_fp8_parity(r)
+
+
+@pytest.mark.parametrize("layout", ["one", "v_first"])
+@pytest.mark.parametrize("config", ["decode16", "decode256", "verify"])
+def test_code_pools_in_one_allocation(layout, config):
+    # K and V code pools in one allocation: V after K (one 3-D copy per page brings both) or V
+    # before K (a copy per page and pool), over 16- and 256-token pages, one-token and multi-token
+    # sequences (the tiny two-CTA kernel and the wide decode path)
+    rng = np.random.default_rng(11)
+    if config == "verify":
+        q = rng.integers(2, 9, size=12)
+        wl = workloads.custom(q, q + rng.integers(100, 3000, size=12), 16, 4, 128, 16, True, seed=12, name="v1")
+    else:
+        bs = 16 if config == "decode16" else 256
+        wl = workloads.custom(np.ones(20, dtype=np.int64), rng.integers(50, 3000, size=20), 16, 4, 128, bs, True,
+                              seed=13, name="d1")
+    _assert_fp8_parity(_run_fp8(wl, layout=layout, schedule=4))
+    _assert_fp8_parity(_run_fp8(wl, layout=layout, kv_chunk=256, schedule=3))
