@@ -449,7 +449,11 @@ xy_status xy_dequant_pages_fp8(const void *k_codes, const void *v_codes, const f
  * (exact for bf16 values of magnitude 2^-14 .. 65504).  Every task runs on the decode path: in a
  * pure decode batch (num_tokens == num_seqs) with G <= XY_FP8_NARROW_ROWS a task has at most
  * XY_FP8_NARROW_ROWS rows (q_rows = 1), otherwise at most 64 rows (q_tile <= 64 / G).  Tasks
- * outside these limits set XY_DEV_BAD_TASK.
+ * outside these limits set XY_DEV_BAD_TASK.  Layout hint (results are the same either way): when
+ * v_pages lies after the whole K pool in the same address space (for example both pools as halves
+ * of one allocation, V second) at a distance that is a multiple of 16 bytes, one copy brings a
+ * page's K and V codes, which helps small pages (16-token pages: 12 instead of 20 copies per
+ * 128-key stage); otherwise each page takes a copy per pool.
  * Errors: as xy_paged_attention; XY_ERR_UNSUPPORTED for head_dim other than 128 or G > 64. */
 xy_status xy_paged_attention_fp8(const void *q, const int32_t *cu_seqlens_q, const int32_t *context_lens,
                                  const int32_t *block_table, int max_blocks, const void *k_pages,
