@@ -638,20 +638,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         m4[i & 3] = fmaxf(m4[i & 3], kt0 + c0 + i < lim ? __uint_as_float(r[i]) : -INFINITY);
                                 }
                             };
-                            xy::tmem_ld32_nowait(s_addr, ca);
-                            xy::tmem_wait_ld(ca);
-                            xy::tmem_ld32_nowait(s_addr + 32, cb);
-                            max_chunk(ca, 0);
-                            xy::tmem_wait_ld(cb);
-                            xy::tmem_ld32_nowait(s_addr + 64, ca);
-                            max_chunk(cb, 32);
-                            xy::tmem_wait_ld(ca);
-                            xy::tmem_ld32_nowait(s_addr + 96, cb);
-                            max_chunk(ca, 64);
-                            xy::tmem_wait_ld(cb);
-                            xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
-                            max_chunk(cb, 96);
-                            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                            float mx;
+                            if constexpr (kFull) {
+                                // every key is visible: the TMEM load itself returns each chunk's
+                                // maximum (tcgen05.ld.red), two chunks in flight per round trip
+                                float mxa, mxb;
+                                xy::tmem_ld32_max_nowait(s_addr, ca, mxa);
+                                xy::tmem_ld32_max_nowait(s_addr + 32, cb, mxb);
+                                xy::tmem_wait_ld_max(ca, mxa);
+                                xy::tmem_wait_ld_max(cb, mxb);
+                                const float mx01 = fmaxf(mxa, mxb);
+                                xy::tmem_ld32_max_nowait(s_addr + 64, ca, mxa);
+                                xy::tmem_ld32_max_nowait(s_addr + 96, cb, mxb);
+                                xy::tmem_wait_ld_max(ca, mxa);
+                                xy::tmem_wait_ld_max(cb, mxb);
+                                mx = fmaxf(mx01, fmaxf(mxa, mxb));
+                                xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
+                            } else {
+                                xy::tmem_ld32_nowait(s_addr, ca);
+                                xy::tmem_wait_ld(ca);
+                                xy::tmem_ld32_nowait(s_addr + 32, cb);
+                                max_chunk(ca, 0);
+                                xy::tmem_wait_ld(cb);
+                                xy::tmem_ld32_nowait(s_addr + 64, ca);
+                                max_chunk(cb, 32);
+                                xy::tmem_wait_ld(ca);
+                                xy::tmem_ld32_nowait(s_addr + 96, cb);
+                                max_chunk(ca, 64);
+                                xy::tmem_wait_ld(cb);
+                                xy::tmem_ld32_nowait(s_addr, ca);  // pass 2's first chunk
+                                max_chunk(cb, 96);
+                                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                            }
                             const float m_new = fmaxf(m, mx * p.scale_log2);  // the scale is positive
                             const bool rescale = __any_sync(0xffffffffu, m_new > m + kRescaleThreshold);
                             xy::tmem_wait_ld(ca);
