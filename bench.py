@@ -54,8 +54,11 @@ DESC = {
     "prefix": "prefix-shared decode: 64 seqs x L=4096, first 3584 tokens on shared pages, Hq=Hkv=32, d 128, bs 16",
 }
 # measured in the default run beside the headline batch, under these keys of the JSON line
-SECONDARY = {"prefill": "prefill", "mixed": "mixed", "skew": "skew", "verify": "verify", "prefix": "prefix_shared"}
-SECONDARY_FP8 = {"prefill": "prefill", "mixed": "mixed", "skew": "skew"}
+# batches measured beside the headline one: JSON key -> (batch, page format); the default (bf16)
+# line also carries the decode batch over 8-bit pages
+SECONDARY = {"prefill": ("prefill", "bf16"), "mixed": ("mixed", "bf16"), "skew": ("skew", "bf16"),
+             "verify": ("verify", "bf16"), "prefix_shared": ("prefix", "bf16"), "decode_fp8": ("decode", "fp8")}
+SECONDARY_FP8 = {"prefill": ("prefill", "fp8"), "mixed": ("mixed", "fp8"), "skew": ("skew", "fp8")}
 
 
 def peaks():
@@ -796,12 +799,14 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     pk = peaks()
-    secondary = {} if args.only else {c: k for c, k in (SECONDARY_FP8 if args.kv == "fp8" else SECONDARY).items()
-                                      if c != args.config}
+    secondary = {} if args.only else {k: (c, kv) for k, (c, kv) in
+                                      (SECONDARY_FP8 if args.kv == "fp8" else SECONDARY).items()
+                                      if (c, kv) != (args.config, args.kv)}
     with SmiClocks(dev) as smi:
         head = measure(args.config, args, dev, pk, world, rank, 0 if args.no_cpu_baseline else 12.0, smi)
-        extra = {key: measure(c, args, dev, pk, world, rank, 0 if args.no_cpu_baseline else 5.0, smi)
-                 for c, key in secondary.items()}
+        extra = {key: measure(c, argparse.Namespace(**{**vars(args), "kv": kv}), dev, pk, world, rank,
+                              0 if args.no_cpu_baseline else 5.0, smi)
+                 for key, (c, kv) in secondary.items()}
         run_clocks = smi.summary()
     if rank == 0:
         line = {
@@ -812,7 +817,8 @@ def main():
                        "step": head["step"], "tokens_per_s": head["tokens_per_s"], "tflops": head["tflops"],
                        "num_tasks": head["num_tasks"], "num_merges": head["num_merges"], "num_ctas": head["num_ctas"],
                        "schedule": head["schedule"], "deal_trace": head["deal_trace"],
-                       "also_measured": {k: DESC[c] for c, k in secondary.items()}},
+                       "also_measured": {k: describe(c, argparse.Namespace(**{**vars(args), "kv": kv}))
+                                         for k, (c, kv) in secondary.items()}},
             "roofline": head["roofline"],
             "append": head["append"],
             "cpu_baseline": head["cpu_baseline"],
