@@ -70,7 +70,10 @@ __device__ __forceinline__ int load_window(const AttnParams &p, int seq, int b0,
 // e % kQueueSlots; every other warp of the CTA reads every entry, in order.  Per slot: full completes when the entry is
 // published, empty when all readers have read it, taken when the lead reader (the warp that
 // issues the task's first copies) has read it.  Entry e + 1 is claimed once entry e is taken, so a
-// CTA holds at most one claimed task beyond the one it is starting.
+// CTA holds at most one claimed task beyond the one it is starting.  A lead reader may instead
+// defer `taken` until the task it is issuing is nearly done (TaskCursor::defer_taken): the next
+// task is then chosen close to the time the CTA needs it, which keeps the deal longest-first
+// when a CTA runs only a few tasks.
 constexpr int kQueueSlots = 8;
 constexpr int kQueueEnd = -2;  // sequence id of the entry that ends the table
 
@@ -167,6 +170,8 @@ struct TaskCursor {
     int read = 0;
     int win = -1;  // this lane's page of the entry's first block-table window (whole-warp readers)
     bool single = false, lead = false, failed = false;
+    bool defer_taken = false;  // lead reader: `taken` waits for release_claim() (or the next read)
+    int pend = -1;             // slot whose `taken` arrival is deferred
     volatile int *votes = nullptr;  // [2][vote_n]: a group of warps that agree on every read
     int vote_bar = 0, vote_n = 0, vote_i = 0;
 
@@ -184,7 +189,15 @@ struct TaskCursor {
         vote_n = n;
         vote_i = i;
     }
+    // A deferring lead reader lets the scheduler claim the next task.  Idempotent per entry.
+    __device__ void release_claim() {
+        if (pend >= 0) {
+            if (single || (threadIdx.x & 31) == 0) mbar_arrive(dq->taken + 8 * pend);
+            pend = -1;
+        }
+    }
     __device__ void read_entry() {
+        release_claim();  // an entry is always taken before the next one is read
         const int s = read % kQueueSlots;
         bool ok = mbar_wait(dq->full + 8 * s, (read / kQueueSlots) & 1, dq->abort);
         if (!single) ok = __all_sync(0xffffffffu, ok);
@@ -197,8 +210,9 @@ struct TaskCursor {
             }
             if (single || (threadIdx.x & 31) == 0) {
                 mbar_arrive(dq->empty + 8 * s);
-                if (lead) mbar_arrive(dq->taken + 8 * s);
+                if (lead && !defer_taken) mbar_arrive(dq->taken + 8 * s);
             }
+            if (lead && defer_taken) pend = s;
             r = cur.t.seq == kQueueEnd ? 0 : 1;
         }
         ++read;

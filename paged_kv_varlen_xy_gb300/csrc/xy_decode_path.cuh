@@ -125,14 +125,20 @@ __device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) 
 // each producer waits only on its own slots' empty barriers).  `ctr` counts all of the stages.
 // `pg_first` is the task's first block-table window if it was prefetched (else -1 with
 // have_first false).  `first_stage_done()` runs once, right after this warp's first stage of the
-// task is issued (the caller prefetches the next task there).  Returns false if a wait gave up.
+// task is issued (the caller prefetches the next task there), and `stage_done(keys_left)` after
+// each of this warp's stages with the task's keys beyond that stage.  Returns false if a wait
+// gave up.
 // 8-bit pages: ksmap / vsmap view the K and V scale arrays as [pages * Hkv rows, bs floats] with a
 // one-row box; with pages of at most 32 tokens a stage's scales come four pages per copy (TMA
 // gather4) instead of one bulk copy per page and tensor (null for bf16 pages).
-template <int HD, class RG, class F>
+struct NoStageHook {
+    __device__ void operator()(int) const {}
+};
+template <int HD, class RG, class F, class H = NoStageHook>
 __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUtensorMap *kmap, const CUtensorMap *vmap,
                              const CUtensorMap *ksmap, const CUtensorMap *vsmap, const Smem &sm, int &ctr, int lane,
-                             int pg_first, bool have_first, F first_stage_done, int pw = 0, int npw = 1) {
+                             int pg_first, bool have_first, F first_stage_done, int pw = 0, int npw = 1,
+                             H stage_done = H()) {
     const xy_task &t = f.t;
     const int bs_sh = 31 - __clz(p.bs);                   // page size is a power of two
     const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;  // keys per TMA box
@@ -234,6 +240,7 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
             first_mine = false;
             first_stage_done();
         }
+        stage_done(t.kv_end - (kv0 + nkeys));
         __syncwarp();
     }
     return true;

@@ -53,6 +53,7 @@ using xy::TaskInfo;
 
 constexpr int HD = 128;
 constexpr int kTileKeys = 128;
+constexpr int kClaimAheadKeys = 512;            // dynamic deal: see the producer's claim release
 constexpr int kSlots = 4;                       // K/V ring slots (one K or V tile each)
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -216,6 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long n_run = 0, work = 0;  // trace: tasks issued and their rows x keys
         TaskCursor tc;
         tc.attach(q, false, true);  // the lead reader: its reads pace the claims
+        // the next task is claimed once the current one has at most kClaimAheadKeys keys left to
+        // issue: early enough for the claim's global reads to land before the ring drains
+        tc.defer_taken = true;
         tc.begin(p);
         while (tc.have && ok) {
             tc.load_next_record(p);
@@ -275,7 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                     pref_win = xy::load_window(p, tn.seq, tn.kv_start / p.bs, lane);
                                                             }
                                                         },
-                                                        0, 2);
+                                                        0, 2, [&](int keys_left) {
+                                                            if (keys_left <= kClaimAheadKeys) tc.release_claim();
+                                                        });
                 ++nd;
                 tc.advance(p);
                 continue;
@@ -340,6 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 }
+                if (t.kv_end - (kv0 + nkeys) <= kClaimAheadKeys) tc.release_claim();
                 if (first) {
                     first = false;
                     tc.prefetch_next(p);
@@ -352,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc.advance(p);
         }
+        tc.release_claim();  // (a loop left early may still hold one)
         if (!ok || tc.failed) {
             if (lane == 0) xy::set_err(p.err, XY_DEV_TIMEOUT);
             *abort_flag = 1;
