@@ -236,8 +236,9 @@ xy_status xy_default_tiles(int num_heads_q, int num_heads_kv, int head_dim, int 
  * contexts spread over more SMs.  The estimate counts each (sequence, KV head) pair's L context
  * keys in ceil(L / chunk) tasks plus a fixed per-task overhead, and takes the larger of a CTA's
  * average load and the longest-first deal of the full-size chunks; ties go to the longer chunk.
- * kv_fp8, pure_decode: as for xy_default_tiles (the 8-bit pure-decode kernel with G <= 8 runs two
- * CTAs per SM slot, so its chunks are sized for twice num_ctas).  Host call, pure.
+ * kv_fp8, pure_decode: as for xy_default_tiles (under the dynamic deal pure decode batches run
+ * two CTAs per SM slot -- 8-bit pages with G <= 8, bf16 pages with G <= 16 -- so their chunks are
+ * sized for twice num_ctas).  Host call, pure.
  *   context_lens: host int32 [num_seqs] (>= 0).  *kv_chunk receives the chunk (a multiple of
  *   every page size and of both kernels' KV tiles).
  * Errors: XY_ERR_INVALID_ARG (null output, negative length, Hq not a positive multiple of Hkv,
@@ -350,10 +351,16 @@ xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
  * The kernels xy_paged_attention launches for the batch (the unified tcgen05 kernel, or the
  * decode-path kernel for pure decode batches and shapes the tile kernel does not take) run every
  * task, but instead of walking a fixed share of the table, each persistent CTA claims the next
- * unclaimed task with an atomic add on task_counter[0]: a scheduler warp claims task k + 1 when
- * the CTA starts task k.  CTAs thus take tasks in table order (largest first for XY_SCHEDULE_DYNAMIC
- * tables), and a CTA that drew short tasks takes more of them.  A task's result does not depend
- * on which CTA runs it: outputs are bit-identical to xy_paged_attention's on the same tasks.
+ * unclaimed task with an atomic add on task_counter[0].  In the unified kernel a scheduler warp
+ * claims the CTA's next task once the current one has at most 512 keys left to issue; in the
+ * decode-path kernel when the CTA starts its current task.  CTAs thus take tasks in table order
+ * (largest first for XY_SCHEDULE_DYNAMIC tables), and a CTA that drew short tasks takes more of
+ * them.  A pure decode batch (num_tokens == num_seqs, G <= 16) runs as 2 * num_ctas half-size
+ * decode-path CTAs (two per SM: two stages and two producer warps each, the first of which
+ * claims the tasks), since the dynamic deal does not depend on the grid size; such a batch's
+ * tables have tasks of at most 16 rows (q_rows = 1), and a hand-made table with taller tasks sets
+ * XY_DEV_BAD_TASK and leaves their rows unwritten.  A task's result does not depend on which CTA
+ * runs it: outputs are bit-identical to xy_paged_attention's on the same tasks.
  *   task_counter: device int32[2], 8-byte aligned, owned by the caller, zero before the first
  *   call (e.g. zeroed at allocation).  Word 0 counts claims, word 1 the CTAs done claiming; the
  *   last CTA to finish claiming returns both to zero, so every launch leaves the counter ready for
@@ -384,7 +391,8 @@ xy_status xy_paged_attention_dynamic(const void *q, const int32_t *cu_seqlens_q,
  * that ratio.
  *   task_counter: NULL runs what xy_paged_attention runs (the static deal: CTA c takes positions
  *   c, c + num_ctas, ... of the table, on the unified tcgen05 kernel or the decode-path kernel);
- *   a counter runs what xy_paged_attention_dynamic runs (the dynamic deal).
+ *   a counter runs what xy_paged_attention_dynamic runs (the dynamic deal), except that a pure
+ *   decode batch keeps one decode-path CTA per SM slot (one trace record each).
  *   cta_trace: device uint64 [num_ctas][4], 8-byte aligned: {start ns, end ns, tasks run, sum of
  *   q_rows * G * (kv_end - kv_start) over them}; times from the GPU's global timer (ns), start
  *   when the CTA begins, end when its last task is stored.  A CTA whose waits gave up

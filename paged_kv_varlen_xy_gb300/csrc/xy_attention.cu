@@ -51,7 +51,7 @@ using xy::dec::kMathWarps;
 // prefill or chunk task shares each K/V stage among 64 rows).  8-bit stages hold 128 keys (about
 // the bytes of a 64-key bf16 stage); with 16-token pages that is 32 copies per stage (codes and
 // scales of 8 pages), so four producer warps, one per ring slot, keep the ring ahead.
-enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2, kFp8Tiny = 3 };
+enum Kind { kBf16 = 0, kFp8Narrow = 1, kFp8Wide = 2, kFp8Tiny = 3, kBf16Tiny = 4 };
 
 template <int HD, int KIND, bool DYN = false>
 struct Cfg {
@@ -59,10 +59,12 @@ struct Cfg {
         KIND == kFp8Tiny, xy::dec::RingF8<2, 16, 128, true>,
         typename std::conditional<KIND == kFp8Narrow, xy::dec::RingF8<4, 16>,
         typename std::conditional<KIND == kFp8Wide, xy::dec::RingF8<4, 16 * kMathWarps>,
-                                  xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type>::type;
-    static constexpr int kProducers = KIND == kBf16 || KIND == kFp8Tiny ? 2 : 4;
-    // kFp8Tiny: half-size CTAs (two stages, two producers, transposed products only), two per SM
-    static constexpr int kMinBlocks = KIND == kFp8Tiny ? 2 : 1;
+        typename std::conditional<KIND == kBf16Tiny, xy::dec::Ring<HD, 2, 16>,
+                                  xy::dec::Ring<HD, HD == 128 ? 4 : 6, 16 * kMathWarps>>::type>::type>::type>::type;
+    static constexpr int kProducers = KIND == kFp8Narrow || KIND == kFp8Wide ? 4 : 2;
+    // kFp8Tiny, kBf16Tiny: half-size CTAs (two stages, two producers, tasks of at most 16 rows;
+    // over 8-bit pages the transposed products only), two per SM
+    static constexpr int kMinBlocks = KIND == kFp8Tiny || KIND == kBf16Tiny ? 2 : 1;
     static_assert(RG::kStages >= kProducers, "every producer owns a ring slot");
     // math warps, producer warps, then (dynamic deal over bf16 pages) the scheduler warp.  Over
     // 8-bit pages a ninth warp would put three warps on one SM sub-partition and cap the registers
@@ -543,6 +545,11 @@ xy_status attention(const void *q, const int32_t *cu_seqlens_q, const int32_t *c
         }
         p.num_tasks = 0;  // ... so only the split-KV merge remains
     }
+    // pure decode under the dynamic deal: two half-size CTAs per SM slot (a traced launch keeps
+    // one CTA per slot, one trace record each)
+    if (pure_decode && p.dyn && !p.trace)
+        return head_dim == 128 ? launch<128, kBf16Tiny>(p, km, vm, km, vm, 2 * num_ctas, merges, num_merges, st)
+                               : launch<64, kBf16Tiny>(p, km, vm, km, vm, 2 * num_ctas, merges, num_merges, st);
     return head_dim == 128 ? launch<128, kBf16>(p, km, vm, km, vm, num_ctas, merges, num_merges, st)
                            : launch<64, kBf16>(p, km, vm, km, vm, num_ctas, merges, num_merges, st);
 }

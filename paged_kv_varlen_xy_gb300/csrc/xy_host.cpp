@@ -375,7 +375,9 @@ extern "C" xy_status xy_default_kv_chunk(const int32_t *context_lens, int num_se
         num_heads_q < num_heads_kv || num_heads_q % num_heads_kv || num_ctas < 1)
         return XY_ERR_INVALID_ARG;
     const int G = num_heads_q / num_heads_kv;
-    const double ctas = (double)num_ctas * (kv_fp8 && pure_decode && G <= 8 ? 2 : 1);
+    // pure decode batches under the dynamic deal run two half-size CTAs per SM slot (8-bit pages:
+    // G <= 8; bf16 pages: every pure decode batch, G <= 16)
+    const double ctas = (double)num_ctas * (pure_decode && G <= (kv_fp8 ? 8 : 16) ? 2 : 1);
     constexpr double kTaskOverheadKeys = 512.0;
     int best = XY_DEFAULT_KV_CHUNK;
     double best_t = -1.0;

@@ -191,12 +191,15 @@ def test_step_tables_pack_both_builders_outputs():
 
 def test_default_kv_chunk_policy(xy):
     # the chunk with the least estimated makespan: four contexts of 128K keys beside many short
-    # ones split into 32768-key tasks on 152 CTAs, 16384 on the 8-bit pure-decode kernel's twice as
-    # many CTAs; a single 1M-key context into 8192-key tasks (256 longer tasks would leave a second
+    # ones split into 32768-key tasks on 152 CTAs, 16384 on the pure-decode kernels' twice as many
+    # CTAs; a single 1M-key context into 8192-key tasks (256 longer tasks would leave a second
     # round on some CTAs); contexts that no candidate splits take the longest chunk
     skew = workloads.make("skew")
     assert xy.default_kv_chunk(skew.context_lens, 64, 8, 152) == 32768
     assert xy.default_kv_chunk(skew.context_lens, 64, 8, 152, kv_fp8=True, pure_decode=True) == 16384
+    assert xy.default_kv_chunk(skew.context_lens, 64, 8, 152, pure_decode=True) == 16384
+    # G = 32 pure decode over 8-bit pages keeps one CTA per SM slot
+    assert xy.default_kv_chunk(skew.context_lens, 256, 8, 152, kv_fp8=True, pure_decode=True) == 32768
     assert xy.default_kv_chunk([1 << 20], 8, 8, 152) == 8192
     assert xy.default_kv_chunk([100, 4096, 8000], 32, 8, 152) == 65536
     assert xy.default_kv_chunk([], 32, 8, 152) == 65536
