@@ -568,6 +568,10 @@ def measure(config, args, dev, pk, world, rank, cpu_budget, smi):
         torch.cuda.synchronize()
         xystep.check(batch)
         deal_trace = xy.trace_summary(trace.cpu().numpy())
+        if wl.num_tokens == wl.num_seqs and wl.group <= 16 and pl.dynamic:
+            # the timed launches of a pure decode batch run two half-size CTAs per SM slot; a
+            # traced launch keeps one CTA (one record) per slot
+            deal_trace["kernel"] = "one decode-path CTA per SM slot (the timed launches run two)"
 
     value = job_throughput(config, w, ms_per_step / 1e3, world)
     unit, bound = unit_of(config)
