@@ -363,7 +363,11 @@ def attention_kernel(wl, kv="bf16", schedule=3):
     128, G divides 128 and the batch is not pure decode (one token per sequence, G <= 16);
     otherwise, and always over 8-bit pages, the decode-path kernel."""
     if schedule == 4:
-        return attention_kernel(wl, kv) + " (dynamic deal)"
+        name = attention_kernel(wl, kv)
+        G = wl.num_heads_q // wl.num_heads_kv
+        if name == "paged_attention_kernel" and wl.num_tokens == wl.num_seqs and G <= (8 if kv == "fp8" else 16):
+            name += ", two CTAs per SM"   # pure decode under the dynamic deal: half-size CTAs
+        return name + " (dynamic deal)"
     if kv == "fp8":
         return "paged_attention_kernel"
     G = wl.num_heads_q // wl.num_heads_kv
