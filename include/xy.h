@@ -156,7 +156,9 @@ xy_status xy_kv_append(const void *k_new, const void *v_new, const int64_t *slot
  * xy_slot_mapping computes it and its K and V rows of every KV head are copied there as
  * xy_kv_append copies them; the slot is also written to slot_mapping[t] unless slot_mapping is
  * NULL.  Arguments, layouts, alignment and device error bits as for those two calls (a token
- * whose slot cannot be formed sets its bit and is skipped).
+ * whose slot cannot be formed sets its bit and is skipped).  The kernel lets the next kernel on
+ * the stream start at once (a programmatic dependent launch): the paged attention calls use this
+ * to stream the keys older than the step's new tokens while the append still runs.
  * Errors: XY_ERR_INVALID_ARG, XY_ERR_CUDA.
  */
 xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t *cu_seqlens_q,
@@ -295,6 +297,12 @@ xy_status xy_build_step_tables(const int32_t *cu_seqlens_q, const int32_t *conte
  *   the same batch and the same num_ctas.
  *   workspace: device, >= the workspace_bytes the builder returned (may be NULL when 0).
  *   err_word: device int32 (see XY_DEV_*).
+ * Launch: a programmatic dependent launch, so the kernel may start while the kernel ahead of it
+ * on the stream still runs if that kernel allows it (this library's KV append kernels do).  It
+ * then copies the K/V rows of each task's new tokens (keys >= context_len - q_len) only after
+ * that kernel has finished; everything else it reads -- q, the tables, the older K/V rows -- it
+ * may read before.  A caller's own kernel ahead of this call that lets dependents start early
+ * must therefore have written those inputs before it does so.
  * Supported: head_dim 64 or 128; block_size a power of two in [16, 256]; kv_chunk (of
  * xy_build_task_table) a multiple of 128 keys.  Rows per task (q_rows * G, G = Hq/Hkv): up to 256
  * when head_dim is 128 and G divides 128 (tasks with more than 16 rows then run on tcgen05 tensor

@@ -120,8 +120,10 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DY
         xy::fence_mbarrier_init();
     }
     __syncthreads();
-    // everything above overlaps the previous kernel (the KV append) under a dependent launch
-    xy::grid_dep_wait();
+    // Under a dependent launch this kernel may run while the kernel ahead of it on the stream (the
+    // step's KV append) still writes the new tokens' K/V rows: only the producer warps wait for it,
+    // each before its first copy of such rows (xy::dec::produce_task); everything else read here
+    // is not written by the append.
     if (p.trace && threadIdx.x == 0) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
 
     if constexpr (C::kSchedWarpUsed) {
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DY
             xy::prefetch_tensormap(&vmap);
         }
         int ctr = 0, pref_win = -1;
-        bool ok = true, pref_valid = false;
+        bool ok = true, pref_valid = false, dep_ready = false;
         // inline claims (8-bit pages): producer warp 0 claims task k + 1 once it has issued its
         // first stage of task k (so the claim overlaps the copies), or as it leaves task k
         const bool claims = C::kInlineClaims && pw == 0;
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(Cfg<HD, KIND, DYN>::kThreads, Cfg<HD, KIND, DY
             const int first_win = DYN ? tc.win : pref_win;
             pref_valid = false;
             ok = xy::dec::produce_task<HD, RG>(
-                p, f, &kmap, &vmap, &ksmap, &vsmap, sm, ctr, lane, first_win, have_first,
+                p, f, &kmap, &vmap, &ksmap, &vsmap, sm, ctr, lane, first_win, have_first, dep_ready,
                 [&]() {
                     // the next record has arrived by now: prefetch its numbers and first window
                     tc.prefetch_next(p);

@@ -128,6 +128,11 @@ __device__ __forceinline__ bool task_ok(const TaskInfo &f, const AttnParams &p) 
 // task is issued (the caller prefetches the next task there), and `stage_done(keys_left)` after
 // each of this warp's stages with the task's keys beyond that stage.  Returns false if a wait
 // gave up.
+// `dep_ready`: whether this warp has waited for the kernel ahead on the stream (the step's KV
+// append, whose dependent launch lets this kernel start while it runs).  The warp waits before its
+// first stage that holds one of a task's new tokens (keys >= L - qn, the rows the append writes);
+// stages of older keys -- and the query rows, tables and block-table windows, which the append
+// does not write -- go out before it.
 // 8-bit pages: ksmap / vsmap view the K and V scale arrays as [pages * Hkv rows, bs floats] with a
 // one-row box; with pages of at most 32 tokens a stage's scales come four pages per copy (TMA
 // gather4) instead of one bulk copy per page and tensor (null for bf16 pages).
@@ -137,8 +142,8 @@ struct NoStageHook {
 template <int HD, class RG, class F, class H = NoStageHook>
 __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUtensorMap *kmap, const CUtensorMap *vmap,
                              const CUtensorMap *ksmap, const CUtensorMap *vsmap, const Smem &sm, int &ctr, int lane,
-                             int pg_first, bool have_first, F first_stage_done, int pw = 0, int npw = 1,
-                             H stage_done = H()) {
+                             int pg_first, bool have_first, bool &dep_ready, F first_stage_done, int pw = 0,
+                             int npw = 1, H stage_done = H()) {
     const xy_task &t = f.t;
     const int bs_sh = 31 - __clz(p.bs);                   // page size is a power of two
     const int BR = p.bs < RG::kKeys ? p.bs : RG::kKeys;  // keys per TMA box
@@ -176,6 +181,10 @@ __device__ bool produce_task(const AttnParams &p, const TaskInfo &f, const CUten
         if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
             set_err(p.err, XY_DEV_PAGE_OOB);
             my_pg = 0;
+        }
+        if (!dep_ready && kv0 + nkeys > f.L - f.qn) {
+            grid_dep_wait();
+            dep_ready = true;
         }
         // the task's first stage also carries its query rows
         const bool q_here = kv0 == t.kv_start;

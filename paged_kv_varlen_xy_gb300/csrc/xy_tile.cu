@@ -185,8 +185,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     xy::tc_fence_after();
     const uint32_t tbase = *tmem_slot;
-    // everything above overlaps the previous kernel (the KV append) under a dependent launch
-    xy::grid_dep_wait();
+    // Under a dependent launch this kernel may run while the kernel ahead of it on the stream (the
+    // step's KV append) still writes the new tokens' K/V rows: only the producer warps wait for it,
+    // each before its first copy of such rows; everything else read here is not written by the
+    // append.
     if (p.trace && threadIdx.x == 0) p.trace[4 * blockIdx.x] = xy::global_timer_ns();
     const int BRt = p.bs < kTileKeys ? p.bs : kTileKeys;  // keys per K/V box
     const int qt_tokens = 128 / p.G;                      // tokens per query tile
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c = 0, qk = 0;          // tile path: ring slot uses, tasks
         int dctr = 0, nd = 0;       // decode path: stages issued, tasks
         int last_kind = 0;          // 1 tile, 2 decode
-        bool ok = true;
+        bool ok = true, dep_ready = false;  // dep_ready: waited for the kernel ahead (the KV append)
         int pref_win = -1;
         bool pref_valid = false;
         unsigned long long n_run = 0, work = 0;  // trace: tasks issued and their rows x keys
@@ -269,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool have_first = DYN || pref_valid;
                 const int first_win = DYN ? tc.win : pref_win;
                 pref_valid = false;
-                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, nullptr, nullptr, dsm, dctr, lane, first_win, have_first,
+                ok = xy::dec::produce_task<HD, DecRing>(p, f, &kmap_d, &vmap_d, nullptr, nullptr, dsm, dctr, lane, first_win, have_first, dep_ready,
                                                         [&]() {
                                                             tc.prefetch_next(p);
                                                             if (tc.have_next) {
@@ -324,6 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b = lane % nbox;
                 int my_pg = __shfl_sync(0xffffffffu, pg_win, (kv0 + b * BRt) / p.bs - win0);
                 const int n_copies = nbox * 2;  // (page box) x (2 halves), per tensor
+                if (!dep_ready && kv0 + nkeys > f.L - f.qn) {  // the tile holds new tokens' rows
+                    xy::grid_dep_wait();
+                    dep_ready = true;
+                }
                 if (lane < n_copies && (my_pg < 0 || my_pg >= p.P)) {
                     xy::set_err(p.err, XY_DEV_PAGE_OOB);
                     my_pg = 0;
@@ -483,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp about as long as the math warps need to consume one; with the producer warp on the
         // even stages and this warp on the odd ones the ring stays ahead of the math.
         int dctr = 0, nd = 0, pref_win = -1;
-        bool ok = true, pref_valid = false, after_tile = false;
+        bool ok = true, pref_valid = false, after_tile = false, dep_ready = false;
         TaskCursor tc;
         tc.attach(q, false, false);
         tc.begin(p);
@@ -526,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int first_win = DYN ? tc.win : pref_win;
             pref_valid = false;
             ok = xy::dec::produce_task<HD, DecRing>(
-                p, f, &kmap_d, &vmap_d, nullptr, nullptr, dsm, dctr, lane, first_win, have_first,
+                p, f, &kmap_d, &vmap_d, nullptr, nullptr, dsm, dctr, lane, first_win, have_first, dep_ready,
                 [&]() {
                     tc.prefetch_next(p);
                     if (tc.have_next) {
