@@ -63,7 +63,8 @@ extern "C" xy_status xy_build_block_table(const int32_t *context_lens, int num_s
         if (n > max_blocks) return XY_ERR_CAPACITY;
         if (pos + n > num_free) return XY_ERR_OUT_OF_PAGES;
         int32_t *row = block_table + (int64_t)i * max_blocks;
-        for (int64_t j = 0; j < max_blocks; ++j) row[j] = j < n ? free_list[pos + j] : -1;
+        std::memcpy(row, free_list + pos, sizeof(int32_t) * (size_t)n);
+        std::fill(row + n, row + max_blocks, -1);
         pos += n;
     }
     if (pages_used) *pages_used = (int)pos;
@@ -81,43 +82,82 @@ struct BuildScratch {
     std::vector<Rec> recs, sorted;
     std::vector<xy_merge> mrg;
     std::vector<uint32_t> order, order2;
+    std::vector<uint64_t> keys, keys2;
     std::vector<uint32_t> hist;
     std::vector<int64_t> tload;
     std::vector<int> tree, cta_of, pos_of, count;
 };
 thread_local BuildScratch g_scratch;
 
-// order = 0 .. n-1 sorted stably by recs[i].load, largest first: LSD radix sort of the
-// complemented loads (loads are below 2^55), 11-bit digits, digits that are equal for every
-// key skipped.
-void sort_by_load_desc(const std::vector<Rec> &recs, BuildScratch &sc) {
+// recs sorted stably by load, largest first: a counting sort of the complemented loads (loads are
+// below 2^55) when they span few distinct steps, else an LSD radix sort with 11-bit digits,
+// digits that are equal for every key skipped.  Each pass moves
+// (key, index) pairs, so it reads them in order; the records move once, at the end.
+void sort_by_load_desc(std::vector<Rec> &recs, BuildScratch &sc) {
     const size_t n = recs.size();
     std::vector<uint32_t> &a = sc.order, &b = sc.order2;
+    std::vector<uint64_t> &ka = sc.keys, &kb = sc.keys2;
     a.resize(n);
     b.resize(n);
-    for (size_t i = 0; i < n; ++i) a[i] = (uint32_t)i;
+    ka.resize(n);
+    kb.resize(n);
     const uint64_t kMask = (uint64_t(1) << 55) - 1;
-    auto key = [&](uint32_t i) { return kMask - (uint64_t)recs[i].load; };
     uint64_t all_or = 0, all_and = ~uint64_t(0);
     for (size_t i = 0; i < n; ++i) {
-        all_or |= key((uint32_t)i);
-        all_and &= key((uint32_t)i);
+        a[i] = (uint32_t)i;
+        ka[i] = kMask - (uint64_t)recs[i].load;
+        all_or |= ka[i];
+        all_and &= ka[i];
     }
     const uint64_t varies = all_or ^ all_and;
-    sc.hist.resize(2048);
-    for (int shift = 0; shift < 55; shift += 11) {
-        if (((varies >> shift) & 2047u) == 0) continue;
-        std::fill(sc.hist.begin(), sc.hist.end(), 0u);
-        for (size_t i = 0; i < n; ++i) ++sc.hist[(key(a[i]) >> shift) & 2047u];
+    if (varies == 0) return;  // every load equal: the order stays
+    // Loads are multiples of a power of two (the charged rows) and usually span a narrow range:
+    // then one counting pass over (key - min) >> tz, at most 2^16 buckets, sorts them.
+    const int tz = __builtin_ctzll(varies);
+    uint64_t kmin = ~uint64_t(0), kmax = 0;
+    for (size_t i = 0; i < n; ++i) {
+        kmin = std::min(kmin, ka[i]);
+        kmax = std::max(kmax, ka[i]);
+    }
+    const uint64_t span = (kmax - kmin) >> tz;
+    if (span < (uint64_t(1) << 16)) {
+        sc.hist.assign((size_t)span + 1, 0u);
+        for (size_t i = 0; i < n; ++i) ++sc.hist[(ka[i] - kmin) >> tz];
         uint32_t sum = 0;
         for (uint32_t &h : sc.hist) {
             const uint32_t c = h;
             h = sum;
             sum += c;
         }
-        for (size_t i = 0; i < n; ++i) b[sc.hist[(key(a[i]) >> shift) & 2047u]++] = a[i];
-        a.swap(b);
+        std::vector<Rec> &sorted = sc.sorted;
+        sorted.resize(n);
+        for (size_t i = 0; i < n; ++i) sorted[sc.hist[(ka[i] - kmin) >> tz]++] = recs[i];
+        recs.swap(sorted);
+        return;
     }
+    sc.hist.resize(2048);
+    for (int shift = 0; shift < 55; shift += 11) {
+        if (((varies >> shift) & 2047u) == 0) continue;
+        std::fill(sc.hist.begin(), sc.hist.end(), 0u);
+        for (size_t i = 0; i < n; ++i) ++sc.hist[(ka[i] >> shift) & 2047u];
+        uint32_t sum = 0;
+        for (uint32_t &h : sc.hist) {
+            const uint32_t c = h;
+            h = sum;
+            sum += c;
+        }
+        for (size_t i = 0; i < n; ++i) {
+            const uint32_t d = sc.hist[(ka[i] >> shift) & 2047u]++;
+            b[d] = a[i];
+            kb[d] = ka[i];
+        }
+        a.swap(b);
+        ka.swap(kb);
+    }
+    std::vector<Rec> &sorted = sc.sorted;
+    sorted.resize(n);
+    for (size_t k = 0; k < n; ++k) sorted[k] = recs[a[k]];
+    recs.swap(sorted);
 }
 }  // namespace
 
@@ -262,10 +302,6 @@ static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context
     {
         // stable sort by load, largest first
         sort_by_load_desc(recs, sc);
-        std::vector<Rec> &sorted = sc.sorted;
-        sorted.resize(recs.size());
-        for (size_t k = 0; k < recs.size(); ++k) sorted[k] = recs[sc.order[k]];
-        recs.swap(sorted);
     }
     if (schedule == XY_SCHEDULE_SERPENTINE || schedule == XY_SCHEDULE_MIXED) {
         // serpentine deal: every complete odd round of num_ctas positions is reversed
@@ -331,11 +367,13 @@ static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context
 }
 
 static void task_stats(const std::vector<Rec> &recs, int num_ctas, xy_task_stats *stats) {
-    std::vector<int64_t> cta(num_ctas, 0);
+    std::vector<int64_t> &cta = g_scratch.tload;   // (free once the builder has returned)
+    cta.assign(num_ctas, 0);
     int64_t total = 0;
-    for (size_t k = 0; k < recs.size(); ++k) {
-        cta[k % num_ctas] += recs[k].load;
+    for (size_t k = 0, c = 0; k < recs.size(); ++k) {   // position k belongs to CTA k mod num_ctas
+        cta[c] += recs[k].load;
         total += recs[k].load;
+        if (++c == (size_t)num_ctas) c = 0;
     }
     const int64_t mx = *std::max_element(cta.begin(), cta.end());
     const int64_t mn = *std::min_element(cta.begin(), cta.end());
