@@ -122,6 +122,22 @@ def test_task_table_fuzz(xy):
         assert mine["workspace_bytes"] == ref["workspace_bytes"]
 
 
+@pytest.mark.parametrize("schedule", [0, 1, 2, 3, 4])
+def test_task_table_sort_regimes(xy, schedule):
+    # the builder sorts loads with one counting pass when they span fewer than 2^16 steps of their
+    # common power of two, else with an LSD radix sort: both give the oracle's stable order,
+    # equal loads (ties) included
+    narrow = ([1] * 40 + [3, 3], [700, 700, 650] + [512] * 37 + [40, 41], 4096)
+    wide = ([1, 5, 300, 2, 77, 1], [1, 2000, 300, 70000, 900, 65536], 4096)
+    unsplit = ([1, 2, 1, 1, 40], [1, 100000, 70000, 2, 99999], 131072)   # > 2^16 steps at every schedule
+    for q, ctx, chunk in (narrow, wide, unsplit):
+        args = (oracle.pack_cu_seqlens(q), np.array(ctx), 8, 2, 128, True, 7, 16, chunk, schedule)
+        mine = xy.xy_build_task_table(*args)
+        ref = oracle.build_task_table(*args)
+        assert np.array_equal(mine["tasks"], ref["tasks"])
+        assert np.array_equal(mine["merges"], ref["merges"])
+
+
 def test_task_table_errors(xy):
     with pytest.raises(xy.XYError) as e:
         xy.xy_build_task_table([1, 3], [5], 4, 2, 64, True, 8, 8, 64)
