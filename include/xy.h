@@ -194,9 +194,12 @@ xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t
  * CTAs then hold different numbers of tasks: the table keeps the layout above and the positions
  * a CTA does not use hold hole records {-1, 0, 0, 0, 0, 0, 0, -1}, which the kernels skip, so
  * *num_tasks counts the holes too (num_ctas times the longest list).  XY_SCHEDULE_DYNAMIC charges
- * tasks as XY_SCHEDULE_GREEDY does and only sorts them: the table is meant for
- * xy_paged_attention_dynamic, whose CTAs claim tasks in table order at run time (stats are the
- * sums of positions modulo num_ctas).
+ * tasks as XY_SCHEDULE_GREEDY does and only orders them: sorted the same way, then the tasks of a
+ * (sequence, KV head) whose sequence is a chunk over a long prior context (q_len > 1 and
+ * context_len - q_len >= q_len) moved up behind the first (largest) of them, keeping their order,
+ * so that a chunk's query tiles run together and share its prior context in L2.  The table is
+ * meant for xy_paged_attention_dynamic, whose CTAs claim tasks in table order at run time (stats
+ * are the sums of positions modulo num_ctas).
  *   cu_seqlens_q [num_seqs+1], context_lens [num_seqs]: host int32.
  *   tasks [max_tasks], merges [max_merges]: host outputs; pass NULL (with max 0) to query counts.
  *   *num_tasks, *num_merges: counts; *workspace_bytes = rows * (head_dim + 1) * 4 (fp32 partial
@@ -208,7 +211,7 @@ xy_status xy_kv_append_paged(const void *k_new, const void *v_new, const int32_t
 #define XY_SCHEDULE_SERPENTINE 1  /* the same sort, serpentine ("symmetric round-robin") deal */
 #define XY_SCHEDULE_MIXED 2       /* padded-tile load, sort, serpentine deal, per-CTA interleave */
 #define XY_SCHEDULE_GREEDY 3      /* padded-tile load + per-task cost, greedy deal, hole records */
-#define XY_SCHEDULE_DYNAMIC 4     /* the same loads, sorted; claimed by CTAs at run time */
+#define XY_SCHEDULE_DYNAMIC 4     /* the same loads, sorted (a chunk's tasks together); claimed at run time */
 #define XY_SCHEDULE_TASK_KEYS 512 /* per-task cost of XY_SCHEDULE_GREEDY, in keys */
 #define XY_SCHEDULE_TILE_ROWS 128 /* MMA tile height: the unit of XY_SCHEDULE_MIXED's load */
 #define XY_SCHEDULE_SMALL_ROWS 16 /* tasks of at most this many rows count as small */
@@ -362,8 +365,8 @@ xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
  * unclaimed task with an atomic add on task_counter[0].  In the unified kernel a scheduler warp
  * claims the CTA's next task once the current one has at most 512 keys left to issue; in the
  * decode-path kernel when the CTA starts its current task.  CTAs thus take tasks in table order
- * (largest first for XY_SCHEDULE_DYNAMIC tables), and a CTA that drew short tasks takes more of
- * them.  A pure decode batch (num_tokens == num_seqs, G <= 16) runs as 2 * num_ctas half-size
+ * (largest first for XY_SCHEDULE_DYNAMIC tables, a chunk's tasks together), and a CTA that drew
+ * short tasks takes more of them.  A pure decode batch (num_tokens == num_seqs, G <= 16) runs as 2 * num_ctas half-size
  * decode-path CTAs (two per SM: two stages and two producer warps each, the first of which
  * claims the tasks), since the dynamic deal does not depend on the grid size; such a batch's
  * tables have tasks of at most 16 rows (q_rows = 1), and a hand-made table with taller tasks sets
@@ -374,8 +377,8 @@ xy_status xy_paged_attention_noalloc(const void *q, const int32_t *cu_seqlens_q,
  *   last CTA to finish claiming returns both to zero, so every launch leaves the counter ready for
  *   the next one, with no reset on the host or the stream.  Calls that overlap on the GPU need
  *   different counters.
- *   tasks: any table of xy_build_task_table for this batch (XY_SCHEDULE_DYNAMIC: sorted, no
- *   holes; hole records of other schedules are skipped).
+ *   tasks: any table of xy_build_task_table for this batch (XY_SCHEDULE_DYNAMIC: ordered as
+ *   described there, no holes; hole records of other schedules are skipped).
  *   All other arguments, layouts, limits and errors are those of xy_paged_attention;
  *   XY_ERR_INVALID_ARG also for a null or misaligned task_counter.  A launch whose waits gave up
  *   (XY_DEV_TIMEOUT) still returns the counter to zero.

@@ -87,6 +87,25 @@ def _interleave(big, small, c, num_ctas):
     return [t for _, _, t in keyed]
 
 
+def _group_chunk_tasks(order, records, cu, context_lens):
+    """Schedule 4's order after the sort: the tasks of one (sequence, KV head) whose sequence is a
+    chunk over a long prior context (more than one new token, prior context L - q >= q) follow the
+    first of them in the sorted order, keeping their own order; every other task keeps its place.
+    Written as its definition: a stable sort by (position of the group's first task, position)."""
+    first = {}
+    keyed = []
+    for pos, k in enumerate(order):
+        i, g = records[k][0], records[k][1]
+        qn = cu[i + 1] - cu[i]
+        if qn > 1 and int(context_lens[i]) - qn >= qn:
+            first.setdefault((i, g), pos)
+            keyed.append((first[(i, g)], pos, k))
+        else:
+            keyed.append((pos, pos, k))
+    keyed.sort(key=lambda x: (x[0], x[1]))
+    return [k for _, _, k in keyed]
+
+
 def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head_dim, causal,
                      num_ctas, q_tile, kv_chunk, schedule=0):
     """Return dict(tasks=int32 [n, 8] in dealt order, merges=int32 [m, 8], loads=int64 [n],
@@ -97,7 +116,8 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
     schedule 1: the same sort, serpentine deal.  schedule 2: charged load, serpentine deal and
     per-CTA proportional interleave.  schedule 3: greedy deal with HOLE records (see above).
     schedule 4: schedule 3's loads, sorted, not dealt: the CTAs claim tasks in this order at run
-    time (the cta_loads reported are those of positions mod num_ctas).
+    time (the cta_loads reported are those of positions mod num_ctas); the tasks of a chunk over a
+    long prior context are then brought together (_group_chunk_tasks).
     """
     if schedule not in SCHEDULES:
         raise ValueError("schedule must be 0, 1, 2, 3 or 4")
@@ -140,6 +160,8 @@ def build_task_table(cu_seqlens_q, context_lens, num_heads_q, num_heads_kv, head
                         loads.append(r * (k1 - k0))
 
     order = sorted(range(len(records)), key=lambda k: loads[k], reverse=True)
+    if schedule == 4:
+        order = _group_chunk_tasks(order, records, cu, context_lens)
     if schedule in (1, 2):
         order = _serpentine(order, num_ctas)
     if schedule == 2:

@@ -86,6 +86,8 @@ struct BuildScratch {
     std::vector<uint32_t> hist;
     std::vector<int64_t> tload;
     std::vector<int> tree, cta_of, pos_of, count;
+    std::vector<int64_t> gstart;       // dynamic deal: per (sequence, KV head) group
+    std::vector<uint32_t> glist;
 };
 thread_local BuildScratch g_scratch;
 
@@ -160,6 +162,58 @@ void sort_by_load_desc(std::vector<Rec> &recs, BuildScratch &sc) {
     recs.swap(sorted);
 }
 }  // namespace
+
+// XY_SCHEDULE_DYNAMIC's order after the sort: the tasks of a (sequence, KV head) whose sequence is
+// a chunk over a long prior context (more than one new token, prior context at least as long as
+// the chunk) follow the first (largest) of them, in their sorted order; every other task keeps its
+// place relative to the rest.  That is, a stable sort by (position of the task's group leader,
+// position).  The chunk's query-tile tasks then run at about the same time and read the shared
+// prior context while it is in L2 instead of fetching it again from DRAM.
+static void group_chunk_tasks(std::vector<Rec> &recs, const int32_t *cu, const int32_t *ctx, int num_seqs,
+                              int num_heads_kv, BuildScratch &sc) {
+    auto grouped = [&](int i) {
+        const int64_t qn = (int64_t)cu[i + 1] - cu[i], L = ctx[i];
+        return qn > 1 && L - qn >= qn;
+    };
+    bool any = false;
+    for (int i = 0; i < num_seqs && !any; ++i) any = grouped(i);
+    if (!any) return;
+    const size_t n = recs.size();
+    const size_t ng = (size_t)num_seqs * (size_t)num_heads_kv;
+    auto gid = [&](const Rec &r) -> int64_t {
+        return grouped(r.t.seq) ? (int64_t)r.t.seq * num_heads_kv + r.t.kv_head : -1;
+    };
+    // each group's tasks in sorted order: counting sort of the positions by group
+    std::vector<int64_t> &start = sc.gstart;
+    start.assign(ng + 1, 0);
+    for (size_t p = 0; p < n; ++p) {
+        const int64_t g = gid(recs[p]);
+        if (g >= 0) ++start[g + 1];
+    }
+    for (size_t g = 0; g < ng; ++g) start[g + 1] += start[g];
+    std::vector<uint32_t> &list = sc.glist;
+    list.resize((size_t)start[ng]);
+    {
+        std::vector<int> &fill = sc.count;
+        fill.assign(ng, 0);
+        for (size_t p = 0; p < n; ++p) {
+            const int64_t g = gid(recs[p]);
+            if (g >= 0) list[(size_t)(start[g] + fill[g]++)] = (uint32_t)p;
+        }
+    }
+    std::vector<Rec> &out = sc.sorted;
+    out.clear();
+    out.reserve(n);
+    for (size_t p = 0; p < n; ++p) {
+        const int64_t g = gid(recs[p]);
+        if (g < 0) {
+            out.push_back(recs[p]);
+        } else if (list[(size_t)start[g]] == (uint32_t)p) {  // the group's leader: the whole group
+            for (int64_t q = start[g]; q < start[g + 1]; ++q) out.push_back(recs[list[(size_t)q]]);
+        }
+    }
+    recs.swap(out);
+}
 
 // XY_SCHEDULE_MIXED, per CTA: the tasks at positions c, c + num_ctas, ... split into large
 // (rows > XY_SCHEDULE_SMALL_ROWS) and small ones, each list in dealt order.  A task's key is
@@ -303,6 +357,7 @@ static xy_status build_tasks(const int32_t *cu_seqlens_q, const int32_t *context
         // stable sort by load, largest first
         sort_by_load_desc(recs, sc);
     }
+    if (schedule == XY_SCHEDULE_DYNAMIC) group_chunk_tasks(recs, cu_seqlens_q, context_lens, num_seqs, num_heads_kv, sc);
     if (schedule == XY_SCHEDULE_SERPENTINE || schedule == XY_SCHEDULE_MIXED) {
         // serpentine deal: every complete odd round of num_ctas positions is reversed
         const size_t n = (size_t)num_ctas;

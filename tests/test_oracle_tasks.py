@@ -263,11 +263,15 @@ def test_unknown_schedule_rejected():
 
 
 def test_dynamic_schedule_is_the_greedy_loads_sorted_and_undealt():
-    # schedule 4 holds exactly the greedy schedule's tasks (no holes), in stable descending order
-    # of the same loads: the order in which CTAs claim them at run time
+    # schedule 4 holds exactly the greedy schedule's tasks (no holes) in descending order of the
+    # same loads, except that the tasks of a chunk over a long prior context (q > 1 new tokens,
+    # L - q >= q) follow the largest task of their (sequence, KV head): the group leaders and the
+    # other tasks form a descending list, each group is contiguous and descending, and ties keep
+    # the enumeration order (sequence, kv head, query tile, chunk) -- which fixes the order
     rng = np.random.default_rng(8)
     q = rng.integers(1, 40, size=9)
     L = q + rng.integers(0, 900, size=9)
+    q[0], L[1] = 1, q[1]   # a decode row and a prompt without prior context beside the chunks
     cu = np.concatenate([[0], np.cumsum(q)])
     dyn = build_task_table(cu, L, 8, 2, 128, True, 5, 16, 256, schedule=4)
     gre = build_task_table(cu, L, 8, 2, 128, True, 5, 16, 256, schedule=3)
@@ -275,12 +279,30 @@ def test_dynamic_schedule_is_the_greedy_loads_sorted_and_undealt():
     assert len(dyn["tasks"]) == len(real) and not np.any(dyn["tasks"][:, 0] < 0)
     key = lambda t: tuple(t)
     assert sorted(map(key, dyn["tasks"])) == sorted(map(key, real))
-    assert np.all(np.diff(dyn["loads"]) <= 0)
-    # ties keep enumeration order (sequence, kv head, query tile, chunk)
-    for a in range(len(dyn["tasks"]) - 1):
-        if dyn["loads"][a] == dyn["loads"][a + 1]:
-            ta, tb = dyn["tasks"][a], dyn["tasks"][a + 1]
-            assert (ta[0], ta[1], ta[2], ta[4]) < (tb[0], tb[1], tb[2], tb[4])
+    tasks, loads = dyn["tasks"], dyn["loads"]
+    chunk = {i for i in range(len(q)) if q[i] > 1 and L[i] - q[i] >= q[i]}
+    assert 0 < len(chunk) < len(q)
+    group = [(int(t[0]), int(t[1])) if int(t[0]) in chunk else None for t in tasks]
+    assert any(sum(1 for x in group if x == g) > 1 for g in set(group) if g is not None)
+
+    def enum_order(a, b):
+        ta, tb = tasks[a], tasks[b]
+        return (ta[0], ta[1], ta[2], ta[4]) < (tb[0], tb[1], tb[2], tb[4])
+
+    heads, seen, pos = [], set(), 0
+    while pos < len(tasks):
+        heads.append(pos)
+        g, end = group[pos], pos
+        if g is not None:
+            assert g not in seen   # a group is contiguous
+            seen.add(g)
+            while end + 1 < len(tasks) and group[end + 1] == g:
+                end += 1
+            for a in range(pos, end):
+                assert loads[a] > loads[a + 1] or (loads[a] == loads[a + 1] and enum_order(a, a + 1))
+        pos = end + 1
+    for a, b in zip(heads, heads[1:]):
+        assert loads[a] > loads[b] or (loads[a] == loads[b] and enum_order(a, b))
 
 
 def test_greedy_schedule_is_longest_processing_time_first():
